@@ -1,0 +1,90 @@
+/* colimoe_oracle.h — CPU oracle for the quantized MoE feed-forward block.
+ *
+ * TEST INFRASTRUCTURE ONLY. This is the plain, slow, obviously-correct statement of what the
+ * block computes, used to check the CUDA library. Only the test suite, the smoke check and the
+ * benchmark's CPU-baseline leg may load it; the product path (libcolimoe) never links or calls
+ * it, and the two share no code, headers or tables.
+ *
+ * Source of the definitions (cited per function in colimoe_oracle.c):
+ *   [glm.c]   colibri-strix, c/glm.c @98759bf — QT tensor formats, matmul/matmul_q/matmul_i4/
+ *             matmul_i2, sigmoidf/siluf, moe() phases A–E.
+ *   [glm.c']  colibri-strix, c/glm.c @97c756a — same file, later revision (matmul_i4_pair).
+ *   [metal]   colibri, c/backend_metal.mm @93cde63 — shaders mm_gemv, moe_gemv, moe_silu,
+ *             r_router, r_top8, r_top8_par; host moe_submit/moe_finish.
+ *
+ * Precision: dot products accumulate in double and are rounded once to float, then multiplied
+ * by the float row scale (the pages apply the scale after the sum). Every elementwise step
+ * (sigmoid, bias add, renormalisation, SiLU·mul, weighted combine) runs in float, in the order
+ * the pages give, because the pages hold those values in float and the router's comparisons
+ * decide integers (the selected expert ids) in that precision.
+ *
+ * Parity status: every function here is pinned by tests against hand-worked examples, closed
+ * forms, brute force or invariants (see tests/test_oracle_pins.py). No function is unpinned.
+ */
+#ifndef COLIMOE_ORACLE_H
+#define COLIMOE_ORACLE_H
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* weight formats of the QT tensor ([glm.c] QT struct): 0 f32, 1 int8, 2 int4, 3 int2 */
+#define ORACLE_FMT_F32  0
+#define ORACLE_FMT_INT8 1
+#define ORACLE_FMT_INT4 2
+#define ORACLE_FMT_INT2 3
+
+/* bytes of one packed row of In elements */
+int64_t oracle_row_bytes(int fmt, int64_t In);
+
+/* dequantised value of element i of one packed row (no scale) */
+float oracle_deq(int fmt, const uint8_t *row, int64_t i);
+
+/* y[o] = (float)(sum_i deq(W[o,i]) * v[i]) * s[o]   for o in [0,O); W is [O][row_bytes(In)]
+ * (f32 weights: s may be NULL, meaning scale 1). */
+void oracle_qgemv(int fmt, const void *W, const float *s, const float *v, int O, int In, float *y);
+
+/* Router scores for T tokens: sig[t,e] = sigmoid(x_t . Wr_e), choice[t,e] = sig + bias[e].
+ * Returns 0, or -1 if any score or choice is not finite. */
+int oracle_router(const float *x, int T, int H, const float *Wr, const float *bias, int E,
+                  float *sig, float *choice);
+
+/* Top-K selection with optional TOPK override (ksel, 0 = K) and adaptive top-p (top_p in (0,1),
+ * 0 = off), then optional renormalisation and routed scaling.  idx/w are [T,K]; entries beyond
+ * keff[t] are set to -1 / 0.  keff may be NULL.  Returns 0 or -1 on bad arguments. */
+int oracle_select(const float *sig, const float *choice, int T, int E, int K, int ksel,
+                  float top_p, int norm_topk, float routed_scale,
+                  int32_t *idx, float *w, int32_t *keff);
+
+/* Token->expert buckets.  counts[E]; offsets[E+1] (exclusive prefix sum); perm[N] lists the
+ * assignment ids a = t*K + k (k < keff[t]) grouped by expert, ascending a within a group;
+ * N = sum keff.  keff may be NULL (all K).  Returns N, or -1 on an out-of-range index. */
+int oracle_buckets(const int32_t *idx, const int32_t *keff, int T, int K, int E,
+                   int32_t *counts, int32_t *offsets, int32_t *perm);
+
+/* One SwiGLU expert on one vector: g = gate.x, u = up.x, h = silu(g)*u, y = down.h.
+ * gate/up are [Iin][row_bytes(H)], down is [H][row_bytes(Iin)]. */
+void oracle_expert(int fmt, const void *gate_w, const float *gate_s, const void *up_w,
+                   const float *up_s, const void *down_w, const float *down_s,
+                   int H, int Iin, const float *x, float *y);
+
+/* The whole block for T tokens.  Experts are given as host pointer tables of length E.
+ * shared_* may be NULL when I_shared == 0.  idx_out/w_out/keff_out optional ([T,K], [T]).
+ * Returns 0, or -1 on bad arguments or non-finite router scores. */
+int oracle_moe_forward(int T, int H, int I, int E, int K, int ksel, float top_p,
+                       int norm_topk, float routed_scale, int routed_fmt,
+                       const float *x, const float *Wr, const float *bias,
+                       const void *const *gate_w, const float *const *gate_s,
+                       const void *const *up_w, const float *const *up_s,
+                       const void *const *down_w, const float *const *down_s,
+                       int I_shared, int shared_fmt,
+                       const void *sh_gate_w, const float *sh_gate_s,
+                       const void *sh_up_w, const float *sh_up_s,
+                       const void *sh_down_w, const float *sh_down_s,
+                       float *out, int32_t *idx_out, float *w_out, int32_t *keff_out);
+
+#ifdef __cplusplus
+}
+#endif
+#endif

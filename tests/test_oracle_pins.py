@@ -1,0 +1,447 @@
+"""Pins of the CPU oracle against facts fixed by the pages and by mathematics.
+
+Each test checks the oracle against something other than itself: hand-worked examples from the
+pages' definitions (tests/golden/), closed forms, brute force on tiny inputs, textbook special
+cases computed by a library routine, and invariants. A plausible slip in the oracle — nibble
+order, the -8 offset, scale before/after the sum, gate/up swapped, SiLU on the wrong operand,
+tie-break direction, weights taken from the biased choice, renorm epsilon, combine weights,
+shared-expert weight, bucket stability — fails at least one of them.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from conftest import golden_lines, gap_filter
+
+F8, F4, F2, F32 = oracle.FMT_INT8, oracle.FMT_INT4, oracle.FMT_INT2, oracle.FMT_F32
+
+
+# ---------------------------------------------------------------- independent decoder (numpy)
+def np_deq(fmt, W, n):
+    """Dequantise a packed [O, row_bytes] matrix to float64 [O, n] with numpy bit operations —
+    written separately from the oracle's per-element decoder."""
+    W = np.asarray(W, dtype=np.uint8)
+    if fmt == F8:
+        return W[:, :n].view(np.int8).astype(np.float64)
+    if fmt == F4:
+        lo = (W & 0x0F).astype(np.int64) - 8
+        hi = (W >> 4).astype(np.int64) - 8
+        return np.stack([lo, hi], axis=2).reshape(W.shape[0], -1)[:, :n].astype(np.float64)
+    if fmt == F2:
+        f = [((W >> (2 * j)) & 3).astype(np.int64) - 2 for j in range(4)]
+        return np.stack(f, axis=2).reshape(W.shape[0], -1)[:, :n].astype(np.float64)
+    raise ValueError(fmt)
+
+
+def rand_packed(rng, fmt, O, n):
+    rb = oracle.row_bytes(fmt, n)
+    if fmt == F8:
+        return rng.integers(-128, 128, size=(O, rb), dtype=np.int8).view(np.uint8)
+    return rng.integers(0, 256, size=(O, rb), dtype=np.uint8)
+
+
+def ulp_close(a, b, ulps=1):
+    a = np.asarray(a, np.float32)
+    b = np.asarray(b, np.float32)
+    sp = np.spacing(np.maximum(np.abs(a), np.abs(b)).astype(np.float32))
+    return np.all(np.abs(a.astype(np.float64) - b.astype(np.float64)) <= ulps * sp)
+
+
+# ---------------------------------------------------------------- unpack
+def test_unpack_golden():
+    n_cases = 0
+    for line in golden_lines("unpack.txt"):
+        lhs, rhs = line.split(":")
+        fmt, n, hx = lhs.split()
+        fmt, n = int(fmt), int(n)
+        row = np.frombuffer(bytes.fromhex(hx), dtype=np.uint8)
+        expect = np.array([float(v) for v in rhs.split()], np.float32)
+        got = oracle.deq_row(fmt, row, n)
+        assert np.array_equal(got, expect), (line, got)
+        assert np.array_equal(np_deq(fmt, row[None, :], n)[0], expect), line
+        n_cases += 1
+    assert n_cases >= 10
+
+
+def test_row_bytes():
+    # QT row strides: In, ceil(In/2), ceil(In/4) bytes, 4*In for f32
+    assert [oracle.row_bytes(F8, n) for n in (1, 7, 8)] == [1, 7, 8]
+    assert [oracle.row_bytes(F4, n) for n in (1, 2, 3, 6144)] == [1, 1, 2, 3072]
+    assert [oracle.row_bytes(F2, n) for n in (1, 4, 5, 2048)] == [1, 1, 2, 512]
+    assert oracle.row_bytes(F32, 5) == 20
+
+
+# ---------------------------------------------------------------- quantised GEMV
+@pytest.mark.parametrize("fmt", [F8, F4, F2])
+@pytest.mark.parametrize("O,n", [(5, 13), (3, 16), (7, 1)])
+def test_qgemv_unit_vectors_give_scaled_columns(fmt, O, n):
+    rng = np.random.default_rng(100 + fmt * 10 + n)
+    W = rand_packed(rng, fmt, O, n)
+    s = rng.uniform(0.5, 2.0, O).astype(np.float32)
+    D = np_deq(fmt, W, n)
+    for i in range(n):
+        e = np.zeros(n, np.float32)
+        e[i] = 1.0
+        y = oracle.qgemv(fmt, W, s, e, O, n)
+        assert np.array_equal(y, (D[:, i].astype(np.float32) * s)), i
+
+
+@pytest.mark.parametrize("fmt", [F8, F4, F2])
+def test_qgemv_scale_multiplies_rounded_sum(fmt):
+    rng = np.random.default_rng(7 + fmt)
+    O, n = 9, 301
+    W = rand_packed(rng, fmt, O, n)
+    s = rng.uniform(1e-3, 1e-2, O).astype(np.float32)
+    v = rng.standard_normal(n).astype(np.float32)
+    y = oracle.qgemv(fmt, W, s, v, O, n)
+    exact = np.array([math.fsum(np_deq(fmt, W, n)[o] * v.astype(np.float64)) for o in range(O)])
+    expect = exact.astype(np.float32) * s  # round the sum to float once, then scale
+    assert ulp_close(y, expect, 1)
+
+
+@pytest.mark.parametrize("fmt", [F8, F4, F2])
+def test_scale_one_int_path_equals_float_path(fmt):
+    # With all scales 1 the quantised path equals the f32 path on the dequantised weights.
+    rng = np.random.default_rng(11 + fmt)
+    O, n = 17, 257
+    W = rand_packed(rng, fmt, O, n)
+    Wf = np_deq(fmt, W, n).astype(np.float32)
+    v = rng.standard_normal(n).astype(np.float32)
+    y_int = oracle.qgemv(fmt, W, np.ones(O, np.float32), v, O, n)
+    y_f32 = oracle.qgemv(F32, Wf.view(np.uint8), None, v, O, n)
+    assert np.array_equal(y_int, y_f32)
+
+
+@pytest.mark.parametrize("fmt,bits", [(F8, 8), (F4, 4), (F2, 2)])
+def test_pages_quantizer_roundtrip(fmt, bits):
+    """Quantise float rows the way the pages' quantize_rows / pack_int4 / pack_int2 do
+    (symmetric per row, s = amax/qmax, v = round-half-even(w/s) clamped, stored as v+8 in a
+    nibble (low nibble first) or v+2 in a 2-bit field), then dequantise with the oracle:
+    |deq*s - w| <= s/2 wherever w/s was in range."""
+    rng = np.random.default_rng(5 + bits)
+    O, n = 6, 37
+    w = rng.standard_normal((O, n)).astype(np.float32)
+    qmax = (1 << (bits - 1)) - 1
+    rb = oracle.row_bytes(fmt, n)
+    packed = np.zeros((O, rb), np.uint8)
+    scales = np.zeros(O, np.float32)
+    for o in range(O):
+        s = max(np.float32(np.abs(w[o]).max()) / np.float32(qmax), np.float32(1e-8))
+        scales[o] = s
+        v = np.clip(np.rint(w[o] / s), -qmax - 1, qmax).astype(np.int64)
+        if fmt == F8:
+            packed[o, :n] = v.astype(np.int8).view(np.uint8)
+        elif fmt == F4:
+            for i in range(n):
+                packed[o, i // 2] |= np.uint8((v[i] + 8) << (4 * (i % 2)))
+        else:
+            for i in range(n):
+                packed[o, i // 4] |= np.uint8((v[i] + 2) << (2 * (i % 4)))
+    for o in range(O):
+        d = oracle.deq_row(fmt, packed[o], n) * scales[o]
+        assert np.all(np.abs(d - w[o]) <= scales[o] * 0.5 * (1 + 1e-6) + 1e-12), o
+
+
+# ---------------------------------------------------------------- router
+def test_router_closed_form():
+    rng = np.random.default_rng(3)
+    T, H, E = 3, 8, 5
+    x = rng.standard_normal((T, H)).astype(np.float32)
+    Wr = np.zeros((E, H), np.float32)
+    cols = [4, 0, 7, 2, 2]
+    for e, c in enumerate(cols):
+        Wr[e, c] = 2.0 ** -e  # logit = x[c] * 2^-e exactly
+    bias = rng.uniform(-0.1, 0.1, E).astype(np.float32)
+    sig, ch = oracle.router(x, Wr, bias)
+    for t in range(T):
+        for e, c in enumerate(cols):
+            lg = float(x[t, c]) * 2.0 ** -e
+            s = 1.0 / (1.0 + math.exp(-lg))
+            assert ulp_close(sig[t, e], np.float32(s), 2)
+            assert ch[t, e] == np.float32(sig[t, e] + bias[e])
+    sig0, _ = oracle.router(np.zeros((1, H), np.float32), Wr, bias)
+    assert np.all(sig0 == 0.5)
+
+
+def test_router_rejects_non_finite():
+    x = np.zeros((1, 4), np.float32)
+    x[0, 1] = np.nan
+    with pytest.raises(ValueError):
+        oracle.router(x, np.ones((3, 4), np.float32), np.zeros(3, np.float32))
+
+
+def _parse_route(line):
+    parts = [p.split() for p in line.split("|")]
+    K, ksel, top_p, norm, rs = parts[0]
+    return (int(K), int(ksel), float(top_p), int(norm), float(rs),
+            np.array(parts[1], np.float32), np.array(parts[2], np.float32),
+            np.array(parts[3], np.int32), np.array(parts[4], np.float32), int(parts[5][0]))
+
+
+def test_select_golden():
+    n_cases = 0
+    for line in golden_lines("route.txt"):
+        K, ksel, top_p, norm, rs, sig, bias, eidx, ew, ekeff = _parse_route(line)
+        ch = (sig + bias).astype(np.float32)
+        idx, w, keff = oracle.select(sig[None], ch[None], K, norm, rs, ksel, top_p)
+        assert np.array_equal(idx[0], eidx), line
+        assert ulp_close(w[0], ew, 1), (line, w)
+        assert keff[0] == ekeff
+        n_cases += 1
+    assert n_cases == 4
+
+
+def _brute_topk(ch, K):
+    order = sorted(range(len(ch)), key=lambda e: (-float(ch[e]), e))
+    return order[:K]
+
+
+@pytest.mark.parametrize("E", [1, 2, 3, 5, 8, 12, 33, 64, 256])
+def test_select_matches_brute_force_sort(E):
+    rng = np.random.default_rng(E)
+    for trial in range(60):
+        K = int(rng.integers(1, min(E, 9) + 1))
+        T = 4
+        if trial % 2:
+            # few distinct values: many exact ties
+            ch = rng.choice(np.array([0.1, 0.25, 0.5, 0.75], np.float32), size=(T, E))
+            sig = ch.copy()
+        else:
+            sig = rng.uniform(0, 1, (T, E)).astype(np.float32)
+            ch = (sig + rng.uniform(-0.1, 0.1, (T, E)).astype(np.float32)).astype(np.float32)
+        idx, w, keff = oracle.select(sig, ch, K, 0, 1.0)
+        for t in range(T):
+            assert list(idx[t]) == _brute_topk(ch[t], K)
+            assert np.array_equal(w[t], sig[t, idx[t]])  # weights are scores, not choices
+        assert np.all(keff == K)
+
+
+def test_select_exhaustive_small():
+    vals = np.array([0.25, 0.5, 0.75], np.float32)
+    E = 5
+    import itertools
+    for pattern in itertools.product(range(3), repeat=E):
+        ch = vals[list(pattern)][None, :]
+        for K in range(1, E + 1):
+            idx, _, _ = oracle.select(ch, ch, K, 0, 1.0)
+            assert list(idx[0]) == _brute_topk(ch[0], K)
+
+
+@pytest.mark.parametrize("rs", [1.0, 2.5])
+def test_renorm_sums_to_routed_scale(rs):
+    rng = np.random.default_rng(9)
+    T, E, K = 50, 64, 8
+    sig = rng.uniform(0.01, 1, (T, E)).astype(np.float32)
+    idx, w, _ = oracle.select(sig, sig, K, 1, rs)
+    tot = w.astype(np.float64).sum(axis=1)
+    assert np.all(np.abs(tot - rs) <= 4 * K * np.spacing(np.float32(rs)))
+    _, w0, _ = oracle.select(sig, sig, K, 0, rs)
+    assert np.array_equal(w0, (np.take_along_axis(sig, idx, 1) * np.float32(rs)).astype(np.float32))
+
+
+def test_top_p_prefix_rule_brute_force():
+    rng = np.random.default_rng(21)
+    T, E, K = 200, 32, 8
+    sig = rng.uniform(0, 1, (T, E)).astype(np.float32)
+    ch = (sig + rng.uniform(-0.3, 0.3, (T, E))).astype(np.float32)
+    p = 0.6
+    idx, w, keff = oracle.select(sig, ch, K, 0, 1.0, 0, p)
+    for t in range(T):
+        sel = _brute_topk(ch[t], K)
+        ws = sorted([float(sig[t, e]) for e in sel], reverse=True)
+        tot = sum(ws)
+        cum = np.cumsum(ws)
+        if np.min(np.abs(cum - p * tot)) < 1e-5:
+            continue  # too close to the threshold to decide in double
+        ke = int(np.argmax(cum >= p * tot)) + 1
+        assert keff[t] == ke
+        assert np.allclose(w[t, :ke], ws[:ke], rtol=0, atol=0)
+        assert np.all(idx[t, ke:] == -1)
+
+
+# ---------------------------------------------------------------- buckets
+def test_buckets_golden():
+    for line in golden_lines("buckets.txt"):
+        parts = [p.split() for p in line.split("|")]
+        T, K, E = map(int, parts[0])
+        idx = np.array(parts[1], np.int32).reshape(T, K)
+        counts, offsets, perm = oracle.buckets(idx, E)
+        assert list(counts) == list(map(int, parts[2]))
+        assert list(offsets) == list(map(int, parts[3]))
+        assert list(perm) == list(map(int, parts[4]))
+
+
+@pytest.mark.parametrize("T,K,E", [(1, 8, 64), (32, 8, 256), (100, 3, 7), (2048, 8, 256)])
+def test_buckets_invariants(T, K, E):
+    rng = np.random.default_rng(T + K + E)
+    idx = np.stack([rng.choice(E, K, replace=False) for _ in range(T)]).astype(np.int32)
+    counts, offsets, perm = oracle.buckets(idx, E)
+    assert counts.sum() == T * K
+    assert np.array_equal(np.sort(perm), np.arange(T * K))
+    assert np.array_equal(offsets, np.concatenate([[0], np.cumsum(counts)]))
+    for e in range(E):
+        seg = perm[offsets[e]:offsets[e + 1]]
+        assert np.all(idx.reshape(-1)[seg] == e)  # perm reproduces idx
+        assert np.all(np.diff(seg // K) > 0)  # strictly increasing tokens within a bucket
+    # with keff: only the first keff[t] of each row are bucketed
+    keff = rng.integers(1, K + 1, T).astype(np.int32)
+    c2, o2, p2 = oracle.buckets(idx, E, keff)
+    assert c2.sum() == keff.sum() and len(p2) == keff.sum()
+    assert np.all(p2 % K < keff[p2 // K])
+
+
+# ---------------------------------------------------------------- the block
+def _silu(z):
+    return z / (1.0 + math.exp(-z))
+
+
+def _tiny_block(routed, shared, Wr, bias, x, E, K, H, I, Is, fmt, norm=1, rs=1.0):
+    def slabify(mats):
+        return {k: np.ascontiguousarray(v) for k, v in mats.items()}
+    cfg = dict(T=x.shape[0], H=H, I=I, E=E, K=K, I_shared=Is, norm_topk=norm, routed_scale=rs,
+               routed_fmt=fmt, shared_fmt=fmt)
+    return dict(cfg=cfg, x=x, Wr=Wr, bias=bias, routed=[slabify(r) for r in routed],
+                shared=None if shared is None else slabify(shared))
+
+
+def _i8(rows):
+    return np.array(rows, np.int8).view(np.uint8)
+
+
+def test_block_hand_worked():
+    """H=2, I=1, E=2, K=1, shared I_s=1, int8 weights.  Router logits are 0 for both experts,
+    so sig = 0.5 each; bias (0, 0.25) selects expert 1; renorm gives w = 1, routed_scale 2
+    gives w = 2.  Expert 1: g = 1, u = 2, h = 2*silu(1), y = (h, -h/2).  Shared: g = 3, u = 1,
+    h = silu(3), y = (h, 2h).  out = 2*y1 + y_sh."""
+    H, I, Is = 2, 1, 1
+    one = lambda n: np.ones(n, np.float32)
+    dummy = dict(gate_w=_i8([[0, 0]]), gate_s=one(1), up_w=_i8([[0, 0]]), up_s=one(1),
+                 down_w=_i8([[0], [0]]), down_s=one(2))
+    e1 = dict(gate_w=_i8([[1, 0]]), gate_s=one(1), up_w=_i8([[0, 1]]), up_s=one(1),
+              down_w=_i8([[1], [-1]]), down_s=np.array([1.0, 0.5], np.float32))
+    sh = dict(gate_w=_i8([[1, 1]]), gate_s=one(1), up_w=_i8([[1, 0]]), up_s=one(1),
+              down_w=_i8([[1], [2]]), down_s=one(2))
+    blk = _tiny_block([dummy, e1], sh, np.zeros((2, H), np.float32),
+                      np.array([0.0, 0.25], np.float32), np.array([[1.0, 2.0]], np.float32),
+                      2, 1, H, I, Is, F8, norm=1, rs=2.0)
+    out, idx, w, keff = oracle.moe_forward(blk)
+    assert idx[0, 0] == 1 and w[0, 0] == 2.0 and keff[0] == 1
+    h1 = _silu(1.0) * 2.0
+    hs = _silu(3.0)
+    expect = np.array([2 * h1 + hs, 2 * (-0.5 * h1) + 2 * hs])
+    assert np.allclose(out[0], expect, rtol=1e-6, atol=0)
+
+
+def _torch_ffn(fmt, ex, x, H, Iin):
+    """Dense SwiGLU on the dequantised weights, in float64 with torch: down(silu(gate x)*(up x))."""
+    Wg = torch.tensor(np_deq(fmt, ex["gate_w"], H) * ex["gate_s"][:, None].astype(np.float64))
+    Wu = torch.tensor(np_deq(fmt, ex["up_w"], H) * ex["up_s"][:, None].astype(np.float64))
+    Wd = torch.tensor(np_deq(fmt, ex["down_w"], Iin) * ex["down_s"][:, None].astype(np.float64))
+    xt = torch.tensor(x.astype(np.float64))
+    return (Wd @ (torch.nn.functional.silu(Wg @ xt) * (Wu @ xt))).numpy()
+
+
+@pytest.mark.parametrize("fmt", [F8, F4, F2])
+def test_block_single_expert_is_dense_swiglu(fmt):
+    """E=1, K=1, renormalised: the routed weight is s/(s+1e-20) = 1 exactly, so the block is two
+    dense SwiGLU FFNs (routed + shared) — a textbook layer, computed here with torch in float64."""
+    cfg = dict(T=3, H=96, I=64, E=1, K=1, I_shared=32, norm_topk=1, routed_scale=1.0,
+               routed_fmt=fmt, shared_fmt=fmt, zipf=False)
+    blk = synth.make_block(cfg, seed=31 + fmt)
+    out, idx, w, _ = oracle.moe_forward(blk)
+    assert np.all(idx == 0) and np.all(w == 1.0)
+    for t in range(cfg["T"]):
+        ref = (_torch_ffn(fmt, blk["routed"][0], blk["x"][t], 96, 64) +
+               _torch_ffn(fmt, blk["shared"], blk["x"][t], 96, 32))
+        assert np.allclose(out[t], ref, rtol=0, atol=2e-5 * np.sqrt(np.mean(ref ** 2)))
+
+
+def test_block_combine_weights_and_shared_weight_one():
+    cfg = dict(T=4, H=64, I=32, E=6, K=3, I_shared=16, norm_topk=1, routed_scale=2.5,
+               routed_fmt=F4, shared_fmt=F8, zipf=False)
+    blk = synth.make_block(cfg, seed=77, row_filter=gap_filter(3))
+    out, idx, w, _ = oracle.moe_forward(blk)
+    for t in range(cfg["T"]):
+        ref = _torch_ffn(F8, blk["shared"], blk["x"][t], 64, 16)
+        for k in range(3):
+            ref = ref + float(w[t, k]) * _torch_ffn(F4, blk["routed"][idx[t, k]], blk["x"][t], 64, 32)
+        assert np.allclose(out[t], ref, rtol=0, atol=2e-5 * np.sqrt(np.mean(ref ** 2)))
+    # and the weights are the renormalised, scaled sigmoid scores of the selected experts
+    sig, _ = oracle.router(blk["x"], blk["Wr"], blk["bias"])
+    s = np.take_along_axis(sig, idx, 1).astype(np.float64)
+    assert np.allclose(w, 2.5 * s / s.sum(1, keepdims=True), rtol=1e-6)
+
+
+def test_block_rows_are_independent():
+    cfg = dict(T=5, H=64, I=32, E=8, K=2, I_shared=32, norm_topk=1, routed_scale=2.5,
+               routed_fmt=F4, shared_fmt=F4, zipf=False)
+    blk = synth.make_block(cfg, seed=5)
+    out, idx, w, _ = oracle.moe_forward(blk)
+    for t in range(5):
+        o1, i1, w1, _ = oracle.moe_forward(blk, x=blk["x"][t:t + 1])
+        assert np.array_equal(o1[0], out[t]) and np.array_equal(i1[0], idx[t])
+
+
+def test_block_linear_in_down_scales():
+    cfg = dict(T=3, H=64, I=32, E=8, K=2, I_shared=32, norm_topk=1, routed_scale=2.5,
+               routed_fmt=F8, shared_fmt=F8, zipf=False)
+    blk = synth.make_block(cfg, seed=6)
+    out, _, _, _ = oracle.moe_forward(blk)
+    for ex in blk["routed"] + [blk["shared"]]:
+        ex["down_s"][:] *= np.float32(2.0)
+    out2, _, _, _ = oracle.moe_forward(blk)
+    assert np.array_equal(out2, 2 * out)
+    # zero the shared expert: only the routed sum remains
+    blk["shared"]["down_s"][:] = 0
+    out3, _, _, _ = oracle.moe_forward(blk)
+    assert not np.array_equal(out3, out2)
+
+
+def test_block_expert_relabelling():
+    cfg = dict(T=4, H=64, I=32, E=8, K=3, I_shared=0, norm_topk=1, routed_scale=1.0,
+               routed_fmt=F4, shared_fmt=F4, zipf=False)
+    blk = synth.make_block(cfg, seed=8)
+    out, idx, w, _ = oracle.moe_forward(blk)
+    pi = np.random.default_rng(1).permutation(8)  # new id of old expert e is pi[e]
+    blk2 = dict(blk)
+    inv = np.argsort(pi)
+    blk2["Wr"] = blk["Wr"][inv]
+    blk2["bias"] = blk["bias"][inv]
+    blk2["routed"] = [blk["routed"][inv[j]] for j in range(8)]
+    out2, idx2, w2, _ = oracle.moe_forward(blk2)
+    assert np.array_equal(out2, out)
+    assert np.array_equal(idx2, pi[idx])
+    assert np.array_equal(w2, w)
+
+
+# ---------------------------------------------------------------- the input generator
+def test_generator_is_deterministic():
+    a = synth.make_block(0)
+    b = synth.make_block(0)
+    assert np.array_equal(a["routed_slabs"], b["routed_slabs"])
+    assert np.array_equal(a["x"], b["x"]) and np.array_equal(a["Wr"], b["Wr"])
+
+
+def test_gap_filter_enforces_margin():
+    blk = synth.make_block(1, row_filter=gap_filter(8))
+    _, ch = oracle.router(blk["x"], blk["Wr"], blk["bias"])
+    top = -np.sort(-ch[0])[:9].astype(np.float64)
+    assert np.all(-np.diff(top) > 1e-5)
+
+
+def test_skewed_bias_concentrates_assignments():
+    """The skewed continuous-batch workload: the 20% most-used experts take about half of the
+    assignments (measured over many token draws with the same router)."""
+    cfg = synth.config(3)
+    rng = np.random.Generator(np.random.PCG64(synth.seed_for(3)))
+    Wr, bias = synth.make_router(rng, cfg)
+    x = np.random.default_rng(0).standard_normal((512, cfg["H"])).astype(np.float32)
+    sig, ch = oracle.router(x, Wr, bias)
+    idx, _, _ = oracle.select(sig, ch, cfg["K"], 1, 2.5)
+    counts = np.bincount(idx.reshape(-1), minlength=cfg["E"])
+    top = np.sort(counts)[::-1][: cfg["E"] // 5].sum() / counts.sum()
+    assert 0.45 <= top <= 0.55, top

@@ -1,0 +1,385 @@
+#!/usr/bin/env python
+"""Benchmark of the quantized MoE feed-forward block on GB300.
+
+A step is one whole block (router, selection, buckets, gate/up + SiLU*mul, down, combine) over
+one batch of synthetic tokens, through the C ABI. Default workload: small decode (T=1, H=2048,
+I=1024, 64 int4 experts top-8, no shared expert). Inputs are resident in HBM; activations
+rotate through 16 pre-drawn batches and a 512 MiB buffer is written between timed steps so that
+no step finds its expert weights in the 129 MB L2.
+
+Prints one JSON line (rank 0). `--impl reference` times the CPU oracle instead, on the host
+cores, on the same workload.
+
+Under torchrun (N > 1) every rank runs an independent replica on its own GPU (the block has no
+cross-GPU exchange on this path): value = tokens of all ranks / max time over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import synth  # noqa: E402
+
+METRIC = "MoE-block tokens/s"
+UNIT = "tokens/s"
+ROTATE = 16
+FLUSH_BYTES = 512 << 20
+
+# DRAM bytes (read + write) per launch of the gate/up kernel measured by ncu
+# (dram__bytes_read.sum + dram__bytes_write.sum), keyed by workload, with the hash of the kernel
+# sources they were taken on; a changed kernel reports null until it is measured again.
+NCU_TRAFFIC = {}
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for name in ("expert.cu", "qdot.cuh", "common.cuh"):
+        with open(os.path.join(ROOT, "quantized_expert_decode_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="colimoe", choices=["colimoe", "reference"])
+    ap.add_argument("--workload", type=int, default=1, choices=sorted(synth.CONFIGS))
+    ap.add_argument("--cpu-seconds", type=float, default=10.0,
+                    help="CPU work budget of the oracle baseline sample")
+    return ap.parse_args()
+
+
+# ------------------------------------------------------------------ algorithmic bytes
+def expert_bytes(fmt, H, I):
+    """(gate+up bytes, down bytes) of one expert: packed weights + fp32 row scales."""
+    gu = 2 * (I * synth.row_bytes(fmt, H) + 4 * I)
+    dn = H * synth.row_bytes(fmt, I) + 4 * H
+    return gu, dn
+
+
+def step_bytes(cfg, n_active):
+    """Algorithmic bytes one block call must read: each distinct selected expert once, the
+    shared expert, the router weights and bias (activations excluded)."""
+    gu, dn = expert_bytes(cfg["routed_fmt"], cfg["H"], cfg["I"])
+    b = n_active * (gu + dn)
+    gu_s = dn_s = 0
+    if cfg["I_shared"] > 0:
+        gu_s, dn_s = expert_bytes(cfg["shared_fmt"], cfg["H"], cfg["I_shared"])
+    router = cfg["E"] * cfg["H"] * 4 + cfg["E"] * 4
+    return dict(total=b + gu_s + dn_s + router, experts=b + gu_s + dn_s,
+                gateup=n_active * gu + gu_s, down=n_active * dn + dn_s)
+
+
+def load_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-i", str(self.gpu), "-lms", "200"], stdout=open(self.path, "w"),
+                stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(rows)}
+
+
+# ------------------------------------------------------------------ distributed plumbing
+def dist_init(n_gpus):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        import torch
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    return rank, world, local
+
+
+def dist_barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def dist_max(v, world, device="cpu"):
+    if world == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(v)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def dist_sum(v, world, device="cpu"):
+    if world == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(v)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------ CPU oracle (baseline)
+def oracle_sample(cfg, blk, xs, budget_s):
+    """Time the CPU oracle, as it stands, on whole tokens of the workload until `budget_s`
+    seconds of work are done (at least one token). Returns (tokens/s, tokens, seconds)."""
+    import oracle
+    oracle.build()
+    flat = xs.reshape(-1, cfg["H"])
+    n, t0 = 0, time.perf_counter()
+    while True:
+        oracle.moe_forward(blk, x=flat[n % len(flat)][None, :])
+        n += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s:
+            return n / el, n, el
+
+
+def cpu_cores_used():
+    return 1  # the oracle is single-threaded C
+
+
+# ------------------------------------------------------------------ the GPU arm
+def run_colimoe(args, rank, world, local):
+    import torch
+    import quantized_expert_decode_gb300 as q
+    from quantized_expert_decode_gb300.device import DeviceBlock
+
+    dev_name = f"cuda:{local}"
+    torch.cuda.set_device(local)
+    cid = args.workload
+    cfg = synth.config(cid)
+    blk = synth.make_block(cid)
+    dev = DeviceBlock(blk, device=dev_name)
+    T, H, K = cfg["T"], cfg["H"], cfg["K"]
+    xs_np = synth.make_x_batches(cfg, synth.seed_for(cid) + 97 * rank, ROTATE)
+    xs = torch.from_numpy(xs_np).to(dev_name)
+    out = torch.empty((T, H), dtype=torch.float32, device=dev_name)
+    flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev_name)
+    stream = torch.cuda.current_stream()
+
+    def events():
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
+        for e in evs:
+            e.record(stream)  # creates the underlying cudaEvent_t
+        return evs
+
+    step_ev = [events() for _ in range(args.steps)]
+    warm_ev = events()
+    torch.cuda.synchronize()
+
+    for i in range(args.warmup):
+        flush.fill_(float(i))
+        q.coli_moe_forward_profiled(dev.desc, xs[i % ROTATE], dev.Wr, dev.bias, dev.table,
+                                    dev.shared, out, warm_ev, dev.ws, dev.ws_bytes, stream)
+    q.coli_moe_check(dev.ws, stream)
+    torch.cuda.synchronize()
+    dist_barrier(world)
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    for i in range(args.steps):
+        flush.fill_(float(i))
+        q.coli_moe_forward_profiled(dev.desc, xs[i % ROTATE], dev.Wr, dev.bias, dev.table,
+                                    dev.shared, out, step_ev[i], dev.ws, dev.ws_bytes, stream)
+    torch.cuda.synchronize()
+    dist_barrier(world)
+    time.sleep(0.2)
+    clk = clocks.stop()
+    q.coli_moe_check(dev.ws, stream)
+
+    stage = np.array([[step_ev[i][j].elapsed_time(step_ev[i][j + 1]) for j in range(4)]
+                      for i in range(args.steps)])  # ms
+    step_ms = stage.sum(axis=1)
+    total_s = float(step_ms.sum()) / 1e3
+    # distinct routed experts each rotated batch reads (from the library's own routing)
+    idx = torch.empty((T, K), dtype=torch.int32, device=dev_name)
+    wts = torch.empty((T, K), dtype=torch.float32, device=dev_name)
+    uniq = []
+    for b in range(ROTATE):
+        q.coli_moe_route(dev.desc, xs[b], dev.Wr, dev.bias, idx, wts, None, None, None, None,
+                         dev.ws, dev.ws_bytes, stream)
+        ids = idx.cpu().numpy()
+        uniq.append(len(np.unique(ids[ids >= 0])))
+    n_active = np.array([uniq[i % ROTATE] for i in range(args.steps)])
+    max_s = dist_max(total_s, world, dev_name if world > 1 else "cpu")
+    tokens = dist_sum(T * args.steps, world, dev_name if world > 1 else "cpu")
+    value = tokens / max_s
+
+    bytes_per = [step_bytes(cfg, int(u)) for u in n_active]
+    hbm_peak, peak_kind = load_peaks()
+    gu_ms = stage[:, 1]
+    gu_bytes = np.array([b["gateup"] for b in bytes_per], np.float64)
+    achieved = float(gu_bytes.sum() / (gu_ms.sum() / 1e3) / 1e9)
+    block_gbs = float(sum(b["total"] for b in bytes_per) / total_s / 1e9)
+    expert_gbs = float(sum(b["experts"] for b in bytes_per) / total_s / 1e9)
+    src = kernel_source_hash()
+    tr = NCU_TRAFFIC.get(cid)
+    traffic = tr["bytes"] if tr and tr["src"] == src else None
+
+    # end to end through the host-buffer entry point: H2D of x and D2H of out inside each step
+    x_host = torch.from_numpy(xs_np).pin_memory()
+    out_host = torch.empty((T, H), dtype=torch.float32).pin_memory()
+    for i in range(args.warmup):
+        q.coli_moe_forward_host(dev.desc, x_host[i % ROTATE], dev.Wr, dev.bias, dev.table,
+                                dev.shared, out_host, dev.ws, dev.ws_bytes, stream)
+    e2e_s = 0.0
+    for i in range(args.steps):
+        flush.fill_(float(i))
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        q.coli_moe_forward_host(dev.desc, x_host[i % ROTATE], dev.Wr, dev.bias, dev.table,
+                                dev.shared, out_host, dev.ws, dev.ws_bytes, stream)
+        e2e_s += time.perf_counter() - t0
+    e2e_max = dist_max(e2e_s, world, dev_name if world > 1 else "cpu")
+
+    cpu = None
+    if rank == 0:
+        v, n, el = oracle_sample(cfg, blk, xs_np, args.cpu_seconds)
+        cpu = {"value": v, "unit": UNIT, "cores": cpu_cores_used(), "kind": "oracle",
+               "sample": f"{n} tokens of the workload's rotating batches, single-threaded C "
+                         f"oracle, {el:.1f} s"}
+
+    if rank != 0:
+        return None
+    gu_launch_ms = float(gu_ms.mean())
+    return {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": float(step_ms.mean()), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32 (int4/int8 weights dequantised exactly)",
+        "data": "synthetic (seeded; random-init int weights with the workload's shapes)",
+        "config": {"workload": f"{cfg['name']} (T={T}, H={H}, I={cfg['I']}, E={cfg['E']}, K={K}, "
+                               f"I_shared={cfg['I_shared']})",
+                   "tokens_per_step": T, "l2": "512 MiB buffer written between timed steps; "
+                                              "activations rotate over 16 batches",
+                   "parallelism": f"replicas x{world}"},
+        "weight_stream_gbs": expert_gbs, "block_bytes_gbs": block_gbs,
+        "frac_of_8tbs": expert_gbs / 8000.0,
+        "active_experts_mean": float(np.mean(n_active)),
+        "stages_ms": {"route": float(stage[:, 0].mean()), "gateup": gu_launch_ms,
+                      "down": float(stage[:, 2].mean()), "combine": float(stage[:, 3].mean())},
+        "roofline": {"kernel": "gateup_kernel", "bound": "hbm", "achieved": achieved,
+                     "peak": hbm_peak, "peak_kind": peak_kind, "unit": "GB/s",
+                     "frac": achieved / hbm_peak, "traffic": traffic,
+                     "algorithmic_bytes_per_launch": float(gu_bytes.mean()),
+                     "avg_launch_ms": gu_launch_ms, "kernel_src": src},
+        "cpu_baseline": cpu,
+        "e2e": {"value": tokens / e2e_max, "unit": UNIT, "h2d_bytes_per_step": T * H * 4,
+                "d2h_bytes_per_step": T * H * 4},
+        "gpu_launches": 6 * args.steps,
+        "clocks": clk,
+    }
+
+
+# ------------------------------------------------------------------ the reference arm
+def run_reference(args, rank, world):
+    if rank != 0:
+        return None
+    cid = args.workload
+    cfg = synth.config(cid)
+    blk = synth.make_block(cid)
+    xs = synth.make_x_batches(cfg, synth.seed_for(cid), ROTATE)
+    import oracle
+    oracle.build()
+    flat = xs.reshape(-1, cfg["H"])
+    # each step: one token of the workload (the oracle's per-token loop), bounded so that
+    # warmup + steps finish in minutes
+    for i in range(args.warmup):
+        oracle.moe_forward(blk, x=flat[i % len(flat)][None, :])
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        oracle.moe_forward(blk, x=flat[i % len(flat)][None, :])
+    el = time.perf_counter() - t0
+    v = args.steps / el
+    return {
+        "impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * el / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64 accumulate",
+        "data": "synthetic (seeded)",
+        "config": {"workload": f"{cfg['name']} (T={cfg['T']}, H={cfg['H']}, I={cfg['I']}, "
+                               f"E={cfg['E']}, K={cfg['K']}, I_shared={cfg['I_shared']})",
+                   "tokens_per_step": 1, "parallelism": "host cores"},
+        "cpu_baseline": {"kind": "oracle", "cores": cpu_cores_used(), "value": v, "unit": UNIT,
+                         "sample": f"{args.steps} single tokens of the workload"},
+        "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    args = parse()
+    rank, world, local = dist_init(args.gpus)
+    if args.impl == "reference":
+        res = run_reference(args, rank, world)
+    else:
+        res = run_colimoe(args, rank, world, local)
+    if rank == 0 and res is not None:
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

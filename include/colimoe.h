@@ -1,0 +1,164 @@
+/* colimoe.h — C ABI of libcolimoe: one MoE feed-forward block on quantized expert weights,
+ * computed by hand-written CUDA kernels for GB300 (sm_103a).
+ *
+ * What the block computes (colibri-strix c/glm.c @98759bf, function moe(); colibri
+ * c/backend_metal.mm @93cde63, shaders r_router / r_top8 / moe_gemv / moe_silu):
+ *   for every token t (a row of x[T,H]):
+ *     logit[e]  = x_t . W_r[e]                       (fp32 router, moe() phase A)
+ *     sig[e]    = 1 / (1 + exp(-logit[e]))          (sigmoidf)
+ *     choice[e] = sig[e] + bias[e]                  (noaux_tc selection bias, n_group = 1)
+ *     idx[0..K) = greedy top-K of choice, ties to the lower expert index (r_top8 / r_top8_par)
+ *     w[k]      = sig[idx[k]]; optional adaptive top-p truncation (TOPP) and TOPK override;
+ *                 if norm_topk: w /= (sum w + 1e-20); then w *= routed_scale
+ *     for each kept k, expert e = idx[k] (moe() phases C/D):
+ *       g = G_e x_t, u = U_e x_t, h = silu(g) * u, y = D_e h
+ *       out_t += w[k] * y                            (in selection order)
+ *     out_t += shared expert SwiGLU(x_t)             (weight 1, moe() phase E)
+ *   A quantized matrix W[O][In] with per-row scale s[O] is used as
+ *     (W v)[o] = (sum_i deq(W[o,i]) * v[i]) * s[o]     (matmul_q / matmul_i4 / matmul_i2)
+ *   deq: COLI_FMT_INT8 — signed byte; COLI_FMT_INT4 — element i in byte i/2, low nibble for
+ *   even i, value = nibble - 8; COLI_FMT_INT2 — element i in byte i/4 at bit 2*(i%4),
+ *   value = field - 2 (the QT tensor formats of glm.c).
+ *
+ * Conventions for every entry point:
+ *  - All tensors are row-major and live in DEVICE memory unless the argument says HOST.
+ *    The caller owns every buffer, including the workspace; the library never allocates,
+ *    frees or synchronises inside coli_moe_route / coli_moe_forward / coli_moe_qgemv: work is
+ *    enqueued on `stream` (a cudaStream_t; NULL = the legacy default stream) on the current
+ *    device, and the call returns when it is enqueued.
+ *  - Return value: COLI_MOE_OK (0) or a negative COLI_MOE_E* code. Arguments are validated
+ *    on the host before anything is launched; on an error nothing is enqueued.
+ *    Faults that happen while the kernels run surface at the caller's next synchronisation;
+ *    kernel-detected conditions (no selectable expert, a misaligned routed-expert pointer,
+ *    an expired bounded wait) set an error word in the workspace that coli_moe_check reads.
+ *    route / forward calls clear that word when they start, so it reports the latest call.
+ *  - There is no CPU fallback: every step runs in this library's kernels.
+ *  - Packed weight rows must start on 16-byte boundaries: H and I must be multiples of 16
+ *    (int8), 32 (int4) or 64 (int2), and every weight and scale pointer 16-byte aligned;
+ *    x and out must be 16-byte aligned. Violations return COLI_MOE_EALIGN / COLI_MOE_ENOTSUP.
+ *  - Limits: 1 <= K <= min(E, 32), E <= 1024, T <= 65536, H, I <= 65536.
+ */
+#ifndef COLIMOE_H
+#define COLIMOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *coli_stream_t; /* the same type as cudaStream_t */
+
+/* weight formats (glm.c QT struct; 0 = f32 is not an expert format here) */
+#define COLI_FMT_INT8 1
+#define COLI_FMT_INT4 2
+#define COLI_FMT_INT2 3
+
+/* return codes */
+#define COLI_MOE_OK 0
+#define COLI_MOE_EINVAL (-1)     /* a null required pointer or an out-of-range size/option */
+#define COLI_MOE_ENOTSUP (-2)    /* a valid request this build does not implement (format, dims) */
+#define COLI_MOE_EALIGN (-3)     /* a pointer or row stride is not 16-byte aligned */
+#define COLI_MOE_EWORKSPACE (-4) /* ws is NULL, misaligned (256 B) or smaller than required */
+#define COLI_MOE_ECUDA (-5)      /* a CUDA runtime call failed; see coli_moe_last_cuda_error */
+#define COLI_MOE_EDEVICE (-6)    /* the current device is not compute capability 10.3 */
+#define COLI_MOE_EKERNEL (-7)    /* a kernel flagged an error in the workspace (coli_moe_check) */
+
+/* Block description (the config.json fields moe() reads: hidden_size, moe_intermediate_size,
+ * n_routed_experts, num_experts_per_tok, n_shared_experts * moe_intermediate_size,
+ * norm_topk_prob, routed_scaling_factor; plus glm.c's TOPK and TOPP switches). */
+typedef struct {
+    int32_t T;            /* tokens (rows of x and out), >= 1 */
+    int32_t H;            /* hidden size */
+    int32_t I;            /* routed expert intermediate size */
+    int32_t E;            /* routed experts */
+    int32_t K;            /* experts per token */
+    int32_t I_shared;     /* shared expert intermediate size; 0 = no shared expert */
+    int32_t norm_topk;    /* 1: renormalise the kept weights to sum 1 before scaling */
+    float routed_scale;   /* routed_scaling_factor, multiplies the kept weights */
+    int32_t routed_fmt;   /* COLI_FMT_* of every routed expert */
+    int32_t shared_fmt;   /* COLI_FMT_* of the shared expert (may differ from routed_fmt) */
+    int32_t ksel;         /* TOPK override: keep min(ksel, K) experts; 0 = K */
+    float top_p;          /* adaptive top-p in (0,1); 0 = off */
+} coli_moe_desc;
+
+/* One expert's six device pointers: gate/up are [I][row_bytes(H)] with fp32 scales [I];
+ * down is [H][row_bytes(I)] with fp32 scales [H] (I = I_shared for the shared expert). */
+typedef struct {
+    const void *gate_w;
+    const void *up_w;
+    const void *down_w;
+    const float *gate_s;
+    const float *up_s;
+    const float *down_s;
+} coli_moe_expert;
+
+/* Bytes of device workspace coli_moe_route / coli_moe_forward / coli_moe_forward_host need
+ * for this description (256-byte aligned base required). Returns 0 if desc is invalid. */
+size_t coli_moe_workspace_bytes(const coli_moe_desc *desc);
+
+/* Router + selection + buckets (moe() phases A and B; r_router + r_top8_par).
+ *   x [T,H] fp32, W_r [E,H] fp32, bias [E] fp32                           (inputs)
+ *   idx [T,K] int32, w [T,K] fp32: the kept experts in selection order and their weights;
+ *     slots beyond keff[t] hold -1 / 0                                       (outputs)
+ *   keff [T] int32: experts kept per token (K unless ksel/top_p cut it)    (output, may be NULL)
+ *   counts [E], offsets [E+1], perm [T*K] int32: token->expert buckets — perm lists the
+ *     assignment ids a = t*K + k grouped by expert, ascending a within each expert,
+ *     offsets is the exclusive prefix sum of counts                         (outputs, may be NULL)
+ *   ws / ws_bytes: workspace of at least coli_moe_workspace_bytes(desc) bytes. */
+int coli_moe_route(const coli_moe_desc *desc, const float *x, const float *W_r,
+                   const float *bias, int32_t *idx, float *w, int32_t *keff, int32_t *counts,
+                   int32_t *offsets, int32_t *perm, void *ws, size_t ws_bytes,
+                   coli_stream_t stream);
+
+/* The whole block: out[T,H] (fp32, overwritten) = routed experts combined in selection order
+ * with their weights, plus the shared expert.
+ *   experts: DEVICE array [E] of coli_moe_expert (device pointers inside).
+ *   shared:  HOST pointer to one coli_moe_expert holding device pointers; NULL iff
+ *            desc->I_shared == 0.
+ *   idx_out / w_out: optional DEVICE [T,K] copies of the routing (may be NULL).
+ * Every step runs in fp32 on the CUDA cores (exact dequantisation, fp32 accumulation). */
+int coli_moe_forward(const coli_moe_desc *desc, const float *x, const float *W_r,
+                     const float *bias, const coli_moe_expert *experts,
+                     const coli_moe_expert *shared, float *out, int32_t *idx_out,
+                     float *w_out, void *ws, size_t ws_bytes, coli_stream_t stream);
+
+/* Same work as coli_moe_forward, and it records caller-created CUDA events (cudaEvent_t,
+ * passed as void*) on `stream` at the stage boundaries: events[0] before the router,
+ * events[1] after routing and bucketing, events[2] after the gate/up (+SiLU*mul) kernel,
+ * events[3] after the down kernel, events[4] after the combine. n_events must be 5.
+ * Meant for live per-stage timing; the events are only recorded, never synchronised. */
+int coli_moe_forward_profiled(const coli_moe_desc *desc, const float *x, const float *W_r,
+                              const float *bias, const coli_moe_expert *experts,
+                              const coli_moe_expert *shared, float *out, void *const *events,
+                              int n_events, void *ws, size_t ws_bytes, coli_stream_t stream);
+
+/* Same as coli_moe_forward, but x_host and out_host are HOST buffers (page-locked memory
+ * gives asynchronous copies). The copies go through the workspace; the call synchronises
+ * `stream` before it returns, so out_host is ready on return. */
+int coli_moe_forward_host(const coli_moe_desc *desc, const float *x_host, const float *W_r,
+                          const float *bias, const coli_moe_expert *experts,
+                          const coli_moe_expert *shared, float *out_host, void *ws,
+                          size_t ws_bytes, coli_stream_t stream);
+
+/* Quantized GEMV/GEMM building block: y[t][o] = (sum_i deq(W[o,i]) * x[t][i]) * s[o] for
+ * t < T, o < O (matmul_q / matmul_i4 / matmul_i2; mm_gemv). W is [O][row_bytes(In)], s [O],
+ * x [T][In] fp32, y [T][O] fp32. Uses no workspace. */
+int coli_moe_qgemv(int32_t fmt, const void *W, const float *s, const float *x, float *y,
+                   int32_t O, int32_t In, int32_t T, coli_stream_t stream);
+
+/* Synchronises `stream`, reads and clears the workspace error word. Returns COLI_MOE_OK,
+ * COLI_MOE_EKERNEL if a kernel flagged an error since the last check, or COLI_MOE_ECUDA. */
+int coli_moe_check(void *ws, coli_stream_t stream);
+
+/* Static description of a return code. */
+const char *coli_moe_strerror(int code);
+
+/* The cudaError_t of the last COLI_MOE_ECUDA returned on this thread (0 if none). */
+int coli_moe_last_cuda_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* COLIMOE_H */

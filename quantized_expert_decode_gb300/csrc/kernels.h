@@ -1,0 +1,46 @@
+// kernels.h — host-side launchers of libcolimoe's kernels (internal, not part of the ABI).
+#pragma once
+
+#include "common.cuh"
+
+namespace colimoe {
+
+// Everything the expert kernels need to find their work; device pointers into the workspace.
+struct ExpertWork {
+    const coli_moe_expert *experts;  // device [E]
+    coli_moe_expert shared;          // by value; unused when I_shared == 0
+    const float *x;                  // [T][H]
+    const int32_t *counts;           // [E]
+    const int32_t *offsets;          // [E+1]
+    const int32_t *perm;             // [T*K]
+    const int32_t *act;              // [E]
+    const int32_t *meta;             // [0] = U
+    float *h;                        // [(T*K + T)][ldh]
+    float *y;                        // [(T*K + T)][H]
+    int32_t *err;
+    int T, H, I, E, K, I_shared, routed_fmt, shared_fmt;
+    int ldh;                         // row stride of h in floats (max(I, I_shared))
+    int slots;                       // grid.y: max active routed experts + (shared ? 1 : 0)
+};
+
+// router.cu
+cudaError_t launch_router_partial(const float *x, const float *W_r, float *part, int T, int H,
+                                  int E, int splits, cudaStream_t s);
+cudaError_t launch_select(const float *part, int splits, const float *bias, int T, int E, int K,
+                          int ksel, float top_p, int norm_topk, float routed_scale, float *sig,
+                          float *choice, int32_t *idx, float *w, int32_t *keff, int32_t *err,
+                          cudaStream_t s);
+cudaError_t launch_bucket(const int32_t *idx, const int32_t *keff, int T, int K, int E,
+                          int32_t *counts, int32_t *offsets, int32_t *perm, int32_t *pos,
+                          int32_t *act, int32_t *meta, int32_t *err, cudaStream_t s);
+
+// expert.cu
+cudaError_t launch_gateup(const ExpertWork &w, cudaStream_t s);
+cudaError_t launch_down(const ExpertWork &w, cudaStream_t s);
+cudaError_t launch_combine(const float *y, const float *wts, const int32_t *keff,
+                           const int32_t *pos, int T, int H, int K, int has_shared, float *out,
+                           cudaStream_t s);
+cudaError_t launch_qgemv(int fmt, const void *W, const float *sc, const float *x, float *y, int O,
+                         int In, int T, cudaStream_t s);
+
+}  // namespace colimoe

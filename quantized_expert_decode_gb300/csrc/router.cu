@@ -1,0 +1,366 @@
+// router.cu — router logits, top-K selection and token->expert bucketing.
+//
+// Phase A of moe() in colibri-strix c/glm.c @98759bf (and the r_router / r_top8 / r_top8_par
+// shaders of colibri c/backend_metal.mm @93cde63): logit = x . W_r[e] in fp32,
+// sig = 1/(1+exp(-logit)), choice = sig + bias[e], greedy top-K over choice with ties to the
+// lower expert index, w = sig of the chosen experts, optional TOPK / TOPP, renormalisation
+// and routed_scale. Phase B (batch union) becomes a stable counting sort of the assignment
+// ids a = t*K + k by expert.
+#include <cfloat>
+#include <climits>
+
+#include "kernels.h"
+
+namespace colimoe {
+
+// ---------------------------------------------------------------- router partial logits
+// part[s][t][e] = sum over the s-th slice of H of x[t][h] * W_r[e][h]. A 32-token x 64-expert
+// output tile per CTA, k staged through shared memory 32 at a time; the k range is split
+// into `splits` slices so that small T still fills the GPU. Partials are summed in a fixed
+// order by the selection kernel (no atomics: the logits are reproducible run to run).
+__global__ void __launch_bounds__(256)
+router_partial_kernel(const float *__restrict__ x, const float *__restrict__ Wr,
+                      float *__restrict__ part, int T, int H, int E, int kslice) {
+    constexpr int TM = kRouterTM, TE = kRouterTE, TK = kRouterTK;
+    __shared__ float xs[TK][TM + 4];
+    __shared__ __align__(16) float wsm[TK][TE + 4];
+    const int tid = threadIdx.x;
+    const int t0 = blockIdx.x * TM, e0 = blockIdx.y * TE, s = blockIdx.z;
+    const int kb = s * kslice;
+    const int ke = min(H, kb + kslice);
+    const int tx = tid % 16, ty = tid / 16;  // experts tx*4..+3, tokens ty*2..+1
+    float acc[2][4] = {};
+    for (int k0 = kb; k0 < ke; k0 += TK) {
+        {   // x tile: 32 tokens x 32 k, one float4 per thread, stored k-major
+            const int r = tid / 8, kc = (tid % 8) * 4;
+            float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (t0 + r < T && k0 + kc < ke)
+                v = *reinterpret_cast<const float4 *>(x + (size_t)(t0 + r) * H + k0 + kc);
+            xs[kc + 0][r] = v.x;
+            xs[kc + 1][r] = v.y;
+            xs[kc + 2][r] = v.z;
+            xs[kc + 3][r] = v.w;
+        }
+#pragma unroll
+        for (int half = 0; half < 2; half++) {  // W_r tile: 64 experts x 32 k
+            const int r = half * 32 + tid / 8, kc = (tid % 8) * 4;
+            float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (e0 + r < E && k0 + kc < ke)
+                v = *reinterpret_cast<const float4 *>(Wr + (size_t)(e0 + r) * H + k0 + kc);
+            wsm[kc + 0][r] = v.x;
+            wsm[kc + 1][r] = v.y;
+            wsm[kc + 2][r] = v.z;
+            wsm[kc + 3][r] = v.w;
+        }
+        __syncthreads();
+#pragma unroll 8
+        for (int k = 0; k < TK; k++) {
+            const float a0 = xs[k][ty * 2], a1 = xs[k][ty * 2 + 1];
+            const float4 b = *reinterpret_cast<const float4 *>(&wsm[k][tx * 4]);
+            acc[0][0] = fmaf(a0, b.x, acc[0][0]);
+            acc[0][1] = fmaf(a0, b.y, acc[0][1]);
+            acc[0][2] = fmaf(a0, b.z, acc[0][2]);
+            acc[0][3] = fmaf(a0, b.w, acc[0][3]);
+            acc[1][0] = fmaf(a1, b.x, acc[1][0]);
+            acc[1][1] = fmaf(a1, b.y, acc[1][1]);
+            acc[1][2] = fmaf(a1, b.z, acc[1][2]);
+            acc[1][3] = fmaf(a1, b.w, acc[1][3]);
+        }
+        __syncthreads();
+    }
+#pragma unroll
+    for (int i = 0; i < 2; i++) {
+        const int t = t0 + ty * 2 + i;
+        if (t >= T) continue;
+#pragma unroll
+        for (int j = 0; j < 4; j++) {
+            const int e = e0 + tx * 4 + j;
+            if (e < E) part[((size_t)s * T + t) * E + e] = acc[i][j];
+        }
+    }
+}
+
+cudaError_t launch_router_partial(const float *x, const float *W_r, float *part, int T, int H,
+                                  int E, int splits, cudaStream_t st) {
+    int kslice = (H + splits - 1) / splits;
+    kslice = (kslice + kRouterTK - 1) / kRouterTK * kRouterTK;
+    dim3 grid((T + kRouterTM - 1) / kRouterTM, (E + kRouterTE - 1) / kRouterTE, splits);
+    router_partial_kernel<<<grid, 256, 0, st>>>(x, W_r, part, T, H, E, kslice);
+    return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------- top-K selection
+// One warp per token. Lane l owns experts [l*PER, l*PER + PER) (a contiguous block, as in
+// r_top8_par), so a lane-local ascending scan with strict '>' keeps the lowest index among
+// equal choices, and the cross-lane argmax breaks ties toward the lower index: together the
+// serial first-max-wins order of moe()'s greedy loop. The TOPP / renorm / scale tail runs on
+// lane 0 with the same float operations in the same order as the serial code.
+template <int PER>
+__global__ void __launch_bounds__(256)
+select_kernel(const float *__restrict__ part, int S, const float *__restrict__ bias, int T, int E,
+              int K, int Ksel, float top_p, int norm_topk, float routed_scale,
+              float *__restrict__ sig_out, float *__restrict__ ch_out, int32_t *__restrict__ idx,
+              float *__restrict__ w, int32_t *__restrict__ keff, int32_t *__restrict__ err) {
+    __shared__ float s_w[8][kMaxK];
+    __shared__ int s_i[8][kMaxK];
+    const int warp = threadIdx.x / kWarp, lane = threadIdx.x % kWarp;
+    const int t = blockIdx.x * 8 + warp;
+    if (t >= T) return;
+    const int base = lane * PER;
+    float ch[PER], sg[PER];
+#pragma unroll
+    for (int j = 0; j < PER; j++) {
+        const int e = base + j;
+        if (e < E) {
+            float lg = 0.f;
+            for (int s = 0; s < S; s++) lg += part[((size_t)s * T + t) * E + e];
+            const float sv = 1.f / (1.f + expf(-lg));
+            const float cv = sv + bias[e];
+            sig_out[(size_t)t * E + e] = sv;
+            ch_out[(size_t)t * E + e] = cv;
+            sg[j] = sv;
+            ch[j] = cv;
+        } else {
+            sg[j] = 0.f;
+            ch[j] = -INFINITY;
+        }
+    }
+    uint32_t taken = 0;
+    int nsel = 0;
+    for (int k = 0; k < Ksel; k++) {
+        float bv = -1e30f, bs = 0.f;
+        int bi = INT_MAX;
+#pragma unroll
+        for (int j = 0; j < PER; j++) {
+            if (!((taken >> j) & 1u) && ch[j] > bv) {
+                bv = ch[j];
+                bi = base + j;
+                bs = sg[j];
+            }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const float ov = __shfl_down_sync(kFull, bv, o);
+            const int oi = __shfl_down_sync(kFull, bi, o);
+            const float os = __shfl_down_sync(kFull, bs, o);
+            if (ov > bv || (ov == bv && oi < bi)) {
+                bv = ov;
+                bi = oi;
+                bs = os;
+            }
+        }
+        bi = __shfl_sync(kFull, bi, 0);
+        bs = __shfl_sync(kFull, bs, 0);
+        if (bi == INT_MAX) {
+            if (lane == 0) atomicCAS(err, 0, (int)kErrNoCandidate);
+            break;
+        }
+        if (bi >= base && bi < base + PER) taken |= 1u << (bi - base);
+        if (lane == 0) {
+            s_i[warp][k] = bi;
+            s_w[warp][k] = bs;
+        }
+        nsel = k + 1;
+    }
+    __syncwarp();
+    if (lane != 0) return;
+    float *ww = s_w[warp];
+    int *id = s_i[warp];
+    int Ke = nsel;
+    if (top_p > 0.f && top_p < 1.f) {
+        for (int a = 1; a < nsel; a++) {
+            const int ia = id[a];
+            const float wa = ww[a];
+            int b = a - 1;
+            while (b >= 0 && ww[b] < wa) {
+                ww[b + 1] = ww[b];
+                id[b + 1] = id[b];
+                b--;
+            }
+            ww[b + 1] = wa;
+            id[b + 1] = ia;
+        }
+        float tot = 1e-20f;
+        for (int k = 0; k < nsel; k++) tot = __fadd_rn(tot, ww[k]);
+        float cum = 0.f;
+        for (int k = 0; k < nsel; k++) {
+            cum = __fadd_rn(cum, ww[k]);
+            if (cum >= __fmul_rn(top_p, tot)) {
+                Ke = k + 1;
+                break;
+            }
+        }
+    }
+    if (norm_topk) {
+        float sm = 0.f;
+        for (int k = 0; k < Ke; k++) sm = __fadd_rn(sm, ww[k]);
+        sm = __fadd_rn(sm, 1e-20f);
+        for (int k = 0; k < Ke; k++) ww[k] = __fdiv_rn(ww[k], sm);
+    }
+    for (int k = 0; k < K; k++) {
+        const bool kept = k < Ke;
+        idx[(size_t)t * K + k] = kept ? id[k] : -1;
+        w[(size_t)t * K + k] = kept ? __fmul_rn(ww[k], routed_scale) : 0.f;
+    }
+    if (keff) keff[t] = Ke;
+}
+
+cudaError_t launch_select(const float *part, int splits, const float *bias, int T, int E, int K,
+                          int ksel, float top_p, int norm_topk, float routed_scale, float *sig,
+                          float *choice, int32_t *idx, float *w, int32_t *keff, int32_t *err,
+                          cudaStream_t st) {
+    const int Ksel = (ksel > 0 && ksel < K) ? ksel : K;
+    const int per = (E + kWarp - 1) / kWarp;
+    dim3 grid((T + 7) / 8);
+#define COLI_SELECT(P)                                                                            \
+    select_kernel<P><<<grid, 256, 0, st>>>(part, splits, bias, T, E, K, Ksel, top_p, norm_topk,   \
+                                           routed_scale, sig, choice, idx, w, keff, err)
+    if (per <= 1) COLI_SELECT(1);
+    else if (per <= 2) COLI_SELECT(2);
+    else if (per <= 4) COLI_SELECT(4);
+    else if (per <= 8) COLI_SELECT(8);
+    else if (per <= 16) COLI_SELECT(16);
+    else COLI_SELECT(32);
+#undef COLI_SELECT
+    return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------- buckets
+// Exclusive scan over the 1024 threads of the block; returns this thread's prefix and the
+// block total in *total.
+__device__ int block_excl_scan_1024(int v, int *scratch /* >= 33 ints */, int *total) {
+    const int lane = threadIdx.x % kWarp, warp = threadIdx.x / kWarp;
+    int inc = v;
+#pragma unroll
+    for (int o = 1; o < kWarp; o <<= 1) {
+        const int n = __shfl_up_sync(kFull, inc, o);
+        if (lane >= o) inc += n;
+    }
+    if (lane == kWarp - 1) scratch[warp] = inc;
+    __syncthreads();
+    if (warp == 0) {
+        int ws = scratch[lane];
+        int wi = ws;
+#pragma unroll
+        for (int o = 1; o < kWarp; o <<= 1) {
+            const int n = __shfl_up_sync(kFull, wi, o);
+            if (lane >= o) wi += n;
+        }
+        scratch[lane] = wi - ws;  // exclusive prefix of warp totals
+        if (lane == kWarp - 1) scratch[32] = wi;
+    }
+    __syncthreads();
+    const int r = scratch[warp] + inc - v;
+    *total = scratch[32];
+    __syncthreads();
+    return r;
+}
+
+// Single CTA of 1024 threads. counts[e] = assignments of expert e; offsets = exclusive scan;
+// perm lists the kept assignments a (k < keff[t]) grouped by expert, ascending a within an
+// expert (each 1024-assignment chunk is placed in order: rank inside the warp from a
+// match-any mask, then the warps' per-expert counts are scanned); pos[a] is a's slot in
+// perm (-1 when not kept); act lists the experts with a non-empty bucket, ascending;
+// meta = {U, N}.
+__global__ void __launch_bounds__(1024)
+bucket_kernel(const int32_t *__restrict__ idx, const int32_t *__restrict__ keff, int T, int K,
+              int E, int32_t *__restrict__ counts, int32_t *__restrict__ offsets,
+              int32_t *__restrict__ perm, int32_t *__restrict__ pos, int32_t *__restrict__ act,
+              int32_t *__restrict__ meta, int32_t *__restrict__ err) {
+    extern __shared__ int sm[];
+    int *cnt = sm;                 // [E]
+    int *off = cnt + E;            // [E]
+    int *fill = off + E;           // [E]
+    int *chunk = fill + E;         // [E]
+    int *wc = chunk + E;           // [32][E]
+    int *scratch = wc + 32 * E;    // [33]
+    const int tid = threadIdx.x, lane = tid % kWarp, warp = tid / kWarp;
+    const int N = T * K;
+    auto expert_of = [&](int a) -> int {
+        if (a >= N) return -1;
+        const int t = a / K, k = a % K;
+        if (keff && k >= keff[t]) return -1;
+        const int e = idx[a];
+        if (e < 0 || e >= E) {
+            atomicCAS(err, 0, (int)kErrBadExpert);
+            return -1;
+        }
+        return e;
+    };
+    for (int e = tid; e < E; e += blockDim.x) {
+        cnt[e] = 0;
+        fill[e] = 0;
+    }
+    __syncthreads();
+    for (int a = tid; a < N; a += blockDim.x) {
+        const int e = expert_of(a);
+        if (e >= 0) atomicAdd(&cnt[e], 1);
+    }
+    __syncthreads();
+    // offsets and the active list (E <= 1024: one expert per thread)
+    {
+        const int c = tid < E ? cnt[tid] : 0;
+        int tot;
+        const int ex = block_excl_scan_1024(c, scratch, &tot);
+        if (tid < E) {
+            off[tid] = ex;
+            counts[tid] = c;
+            offsets[tid] = ex;
+        }
+        if (tid == 0) offsets[E] = tot;
+        int nact;
+        const int ax = block_excl_scan_1024(c > 0 ? 1 : 0, scratch, &nact);
+        if (tid < E && c > 0) act[ax] = tid;
+        if (tid == 0) {
+            meta[0] = nact;
+            meta[1] = tot;
+        }
+    }
+    __syncthreads();
+    for (int a0 = 0; a0 < N; a0 += blockDim.x) {
+        for (int i = tid; i < 32 * E; i += blockDim.x) wc[i] = 0;
+        __syncthreads();
+        const int a = a0 + tid;
+        const int e = expert_of(a);
+        const unsigned peers = __match_any_sync(kFull, e);
+        const int rank = __popc(peers & ((1u << lane) - 1u));
+        if (e >= 0 && rank == 0) wc[warp * E + e] = __popc(peers);
+        __syncthreads();
+        for (int x = tid; x < E; x += blockDim.x) {
+            int run = 0;
+            for (int w = 0; w < 32; w++) {
+                const int v = wc[w * E + x];
+                wc[w * E + x] = run;
+                run += v;
+            }
+            chunk[x] = run;
+        }
+        __syncthreads();
+        if (a < N) {
+            if (e >= 0) {
+                const int p = off[e] + fill[e] + wc[warp * E + e] + rank;
+                perm[p] = a;
+                pos[a] = p;
+            } else {
+                pos[a] = -1;
+            }
+        }
+        __syncthreads();
+        for (int x = tid; x < E; x += blockDim.x) fill[x] += chunk[x];
+        __syncthreads();
+    }
+}
+
+cudaError_t launch_bucket(const int32_t *idx, const int32_t *keff, int T, int K, int E,
+                          int32_t *counts, int32_t *offsets, int32_t *perm, int32_t *pos,
+                          int32_t *act, int32_t *meta, int32_t *err, cudaStream_t st) {
+    const size_t smem = (size_t)(4 * E + 32 * E + 33) * sizeof(int);
+    cudaError_t e = cudaFuncSetAttribute(bucket_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)smem);
+    if (e != cudaSuccess) return e;
+    bucket_kernel<<<1, 1024, smem, st>>>(idx, keff, T, K, E, counts, offsets, perm, pos, act, meta,
+                                         err);
+    return cudaGetLastError();
+}
+
+}  // namespace colimoe

@@ -40,3 +40,27 @@ def gap_filter(K, gap=GAP):
         return (np.diff(-top, axis=1) > gap).all(axis=1)
 
     return ok
+
+
+def top_p_filter(K, ksel, top_p, gap=GAP):
+    """Row filter for top-p cases: besides the choice margin, the selected experts' sigmoid
+    scores must be pairwise separated, and no running sum of the sorted scores may sit within
+    `gap` of top_p * total — so fp32 summation order cannot change the kept prefix."""
+    import oracle
+    choice_ok = gap_filter(K, gap)
+
+    def ok(x, Wr, bias):
+        good = choice_ok(x, Wr, bias)
+        sig, ch = oracle.router(x, Wr, bias)
+        idx, _, _ = oracle.select(sig, ch, K, 0, 1.0, ksel, 0.0)
+        for t in range(x.shape[0]):
+            sel = idx[t][idx[t] >= 0]
+            s = np.sort(sig[t, sel].astype(np.float64))[::-1]
+            if len(s) > 1 and np.min(-np.diff(s)) <= gap:
+                good[t] = False
+            cum = np.cumsum(s)
+            if np.min(np.abs(cum - top_p * cum[-1])) <= gap:
+                good[t] = False
+        return good
+
+    return ok

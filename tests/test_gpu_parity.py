@@ -1,0 +1,231 @@
+"""Parity of the CUDA library with the CPU oracle, through the C ABI.
+
+Bars (from the block's definition and fp32 arithmetic): selected expert ids, keff and the
+token->expert buckets bit-exact; routing weights within 1e-5 relative (fp32 logit sums in a
+different order, then sigmoid / renorm); block outputs max|err| <= 1e-4 * rms(oracle) on the
+fp32 CUDA-core path. Inputs are drawn so that the K+1 best router choices of every token are
+separated by more than 1e-5 (tests/conftest.py gap_filter), so the selection is decided the
+same way on both sides.
+"""
+import zlib
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from conftest import gap_filter, top_p_filter
+
+pytestmark = pytest.mark.gpu
+
+OUT_TOL = 1e-4
+W_RTOL = 1e-5
+
+
+@pytest.fixture(scope="module")
+def qed():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    import quantized_expert_decode_gb300 as q
+    return q
+
+
+def rms(a):
+    return float(np.sqrt(np.mean(np.asarray(a, np.float64) ** 2)))
+
+
+def assert_out_close(got, ref, tol=OUT_TOL, what=""):
+    got = np.asarray(got, np.float64)
+    ref = np.asarray(ref, np.float64)
+    err = np.max(np.abs(got - ref))
+    assert np.all(np.isfinite(got)), what
+    assert err <= tol * rms(ref), f"{what}: max|err| {err:.3e} > {tol} * rms {rms(ref):.3e}"
+
+
+def run_forward(q, dev, x_np, check=True):
+    T, H = x_np.shape
+    K = dev.cfg["K"]
+    dev.set_tokens(T)
+    x = torch.from_numpy(x_np).to(dev.device)
+    out = torch.empty((T, H), dtype=torch.float32, device=dev.device)
+    idx = torch.empty((T, K), dtype=torch.int32, device=dev.device)
+    w = torch.empty((T, K), dtype=torch.float32, device=dev.device)
+    q.coli_moe_forward(dev.desc, x, dev.Wr, dev.bias, dev.table, dev.shared, out, idx, w,
+                       dev.ws, dev.ws_bytes)
+    if check:
+        q.coli_moe_check(dev.ws)
+    torch.cuda.synchronize()
+    return out.cpu().numpy(), idx.cpu().numpy(), w.cpu().numpy()
+
+
+def run_route(q, dev, x_np):
+    T, H = x_np.shape
+    K, E = dev.cfg["K"], dev.cfg["E"]
+    dev.set_tokens(T)
+    d = dev.device
+    x = torch.from_numpy(x_np).to(d)
+    idx = torch.empty((T, K), dtype=torch.int32, device=d)
+    w = torch.empty((T, K), dtype=torch.float32, device=d)
+    keff = torch.empty(T, dtype=torch.int32, device=d)
+    counts = torch.empty(E, dtype=torch.int32, device=d)
+    offsets = torch.empty(E + 1, dtype=torch.int32, device=d)
+    perm = torch.full((T * K,), -7, dtype=torch.int32, device=d)
+    q.coli_moe_route(dev.desc, x, dev.Wr, dev.bias, idx, w, keff, counts, offsets, perm, dev.ws,
+                     dev.ws_bytes)
+    q.coli_moe_check(dev.ws)
+    torch.cuda.synchronize()
+    return [t.cpu().numpy() for t in (idx, w, keff, counts, offsets, perm)]
+
+
+def check_route(q, blk, dev, ksel=0, top_p=0.0):
+    idx, w, keff, counts, offsets, perm = run_route(q, dev, blk["x"])
+    sig, ch = oracle.router(blk["x"], blk["Wr"], blk["bias"])
+    cfg = blk["cfg"]
+    oi, ow, ok = oracle.select(sig, ch, cfg["K"], cfg["norm_topk"], cfg["routed_scale"], ksel, top_p)
+    assert np.array_equal(idx, oi)
+    assert np.array_equal(keff, ok)
+    assert np.allclose(w, ow, rtol=W_RTOL, atol=0)
+    oc, oo, op = oracle.buckets(oi, cfg["E"], ok)
+    assert np.array_equal(counts, oc) and np.array_equal(offsets, oo)
+    assert np.array_equal(perm[: len(op)], op)
+
+
+def check_forward(q, blk, dev, tokens=None, ksel=0, top_p=0.0, tol=OUT_TOL):
+    out, idx, w = run_forward(q, dev, blk["x"])
+    rows = range(blk["x"].shape[0]) if tokens is None else tokens
+    for t in rows:
+        ro, ri, rw, rk = oracle.moe_forward(blk, x=blk["x"][t:t + 1], ksel=ksel, top_p=top_p)
+        assert np.array_equal(idx[t], ri[0]), t
+        assert np.allclose(w[t], rw[0], rtol=W_RTOL, atol=0), t
+        assert_out_close(out[t], ro[0], tol, what=f"token {t}")
+    return out
+
+
+def make(cfg, seed, K=None):
+    K = cfg["K"] if K is None else K
+    return synth.make_block(cfg, seed=seed, row_filter=gap_filter(K))
+
+
+# ------------------------------------------------------------------ building block: qgemv
+@pytest.mark.parametrize("fmt", [1, 2, 3])
+def test_qgemv_unit_vectors_exact(qed, fmt):
+    rng = np.random.default_rng(fmt)
+    O, In = 37, 2 * {1: 16, 2: 32, 3: 64}[fmt]
+    rb = synth.row_bytes(fmt, In)
+    W = rng.integers(0, 256, size=(O, rb), dtype=np.uint8)
+    s = rng.uniform(0.5, 2, O).astype(np.float32)
+    x = np.eye(In, dtype=np.float32)  # T = In unit vectors
+    d = torch.device("cuda")
+    y = torch.empty((In, O), dtype=torch.float32, device=d)
+    q = qed
+    q.coli_moe_qgemv(fmt, torch.from_numpy(W).to(d), torch.from_numpy(s).to(d),
+                     torch.from_numpy(x).to(d), y, O, In, In)
+    got = y.cpu().numpy()
+    for i in range(In):
+        e = np.zeros(In, np.float32)
+        e[i] = 1
+        assert np.array_equal(got[i], oracle.qgemv(fmt, W, s, e, O, In)), i
+
+
+@pytest.mark.parametrize("fmt", [1, 2, 3])
+@pytest.mark.parametrize("T", [1, 3, 4, 9])
+def test_qgemv_random(qed, fmt, T):
+    rng = np.random.default_rng(10 * fmt + T)
+    O, In = 70, 6 * {1: 16, 2: 32, 3: 64}[fmt]
+    rb = synth.row_bytes(fmt, In)
+    W = rng.integers(0, 256, size=(O, rb), dtype=np.uint8)
+    s = rng.uniform(0.5, 2, O).astype(np.float32)
+    x = rng.standard_normal((T, In)).astype(np.float32)
+    d = torch.device("cuda")
+    y = torch.empty((T, O), dtype=torch.float32, device=d)
+    qed.coli_moe_qgemv(fmt, torch.from_numpy(W).to(d), torch.from_numpy(s).to(d),
+                       torch.from_numpy(x).to(d), y, O, In, T)
+    got = y.cpu().numpy()
+    for t in range(T):
+        assert_out_close(got[t], oracle.qgemv(fmt, W, s, x[t], O, In), what=f"t={t}")
+
+
+# ------------------------------------------------------------------ the five workloads
+@pytest.fixture(scope="module")
+def blocks(qed):
+    cache = {}
+
+    def get(cid):
+        if cid not in cache:
+            cfg = synth.config(cid)
+            blk = make(cfg, synth.seed_for(cid))
+            from quantized_expert_decode_gb300.device import DeviceBlock
+            cache.clear()  # keep one large block resident at a time
+            torch.cuda.empty_cache()
+            cache[cid] = (blk, DeviceBlock(blk))
+        return cache[cid]
+    return get
+
+
+@pytest.mark.parametrize("cid", [0, 1, 2, 3, 4])
+def test_route_workload(qed, blocks, cid):
+    blk, dev = blocks(cid)
+    check_route(qed, blk, dev)
+
+
+@pytest.mark.parametrize("cid,tokens", [(0, None), (1, None), (2, None), (3, [0, 7, 19, 31]),
+                                        (4, [0, 1, 777, 2047])])
+def test_forward_workload(qed, blocks, cid, tokens):
+    blk, dev = blocks(cid)
+    check_forward(qed, blk, dev, tokens)
+
+
+def test_forward_is_deterministic(qed, blocks):
+    blk, dev = blocks(3)
+    a, _, _ = run_forward(qed, dev, blk["x"])
+    b, _, _ = run_forward(qed, dev, blk["x"])
+    assert np.array_equal(a, b)
+
+
+def test_forward_host_matches_device(qed, blocks):
+    blk, dev = blocks(3)
+    out_d, _, _ = run_forward(qed, dev, blk["x"])
+    x_h = torch.from_numpy(blk["x"]).pin_memory()
+    out_h = torch.empty(blk["x"].shape, dtype=torch.float32).pin_memory()
+    qed.coli_moe_forward_host(dev.desc, x_h, dev.Wr, dev.bias, dev.table, dev.shared, out_h,
+                              dev.ws, dev.ws_bytes)
+    assert np.array_equal(out_h.numpy(), out_d)
+
+
+# ------------------------------------------------------------------ ragged and degenerate shapes
+EDGE = [
+    # name, cfg overrides
+    ("ragged-int4", dict(T=7, H=352, I=160, E=40, K=3, I_shared=96, routed_fmt=2, shared_fmt=2)),
+    ("mixed-fmt", dict(T=5, H=256, I=128, E=24, K=4, I_shared=64, routed_fmt=2, shared_fmt=1)),
+    ("int2", dict(T=6, H=384, I=192, E=16, K=2, I_shared=128, routed_fmt=3, shared_fmt=3)),
+    ("k1-no-shared", dict(T=3, H=128, I=64, E=5, K=1, I_shared=0, routed_fmt=1, shared_fmt=1)),
+    ("k-equals-e", dict(T=4, H=128, I=64, E=6, K=6, I_shared=32, routed_fmt=2, shared_fmt=1)),
+    ("one-expert", dict(T=9, H=64, I=32, E=1, K=1, I_shared=0, routed_fmt=2, shared_fmt=2)),
+    ("no-renorm", dict(T=3, H=128, I=64, E=12, K=3, I_shared=32, norm_topk=0, routed_scale=1.5)),
+    ("hot-bucket", dict(T=23, H=128, I=64, E=3, K=2, I_shared=64)),
+    ("max-e-k", dict(T=2, H=64, I=32, E=1024, K=32, I_shared=0)),
+]
+
+
+@pytest.mark.parametrize("name,over", EDGE, ids=[e[0] for e in EDGE])
+def test_edge_shapes(qed, name, over):
+    from quantized_expert_decode_gb300.device import DeviceBlock
+    cfg = dict(T=4, H=128, I=64, E=8, K=2, I_shared=64, norm_topk=1, routed_scale=2.5,
+               routed_fmt=2, shared_fmt=2, zipf=False)
+    cfg.update(over)
+    blk = make(cfg, seed=zlib.crc32(name.encode()) % 1000)
+    dev = DeviceBlock(blk)
+    check_route(qed, blk, dev)
+    check_forward(qed, blk, dev)
+
+
+@pytest.mark.parametrize("ksel,top_p", [(3, 0.0), (0, 0.5), (5, 0.8)])
+def test_topk_override_and_top_p(qed, ksel, top_p):
+    from quantized_expert_decode_gb300.device import DeviceBlock
+    cfg = dict(T=16, H=256, I=128, E=32, K=8, I_shared=64, norm_topk=1, routed_scale=2.5,
+               routed_fmt=2, shared_fmt=2, zipf=False)
+    blk = synth.make_block(cfg, seed=ksel * 10 + int(top_p * 10),
+                           row_filter=top_p_filter(8, ksel, top_p))
+    dev = DeviceBlock(blk, ksel=ksel, top_p=top_p)
+    check_route(qed, blk, dev, ksel=ksel, top_p=top_p)
+    check_forward(qed, blk, dev, ksel=ksel, top_p=top_p)

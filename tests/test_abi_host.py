@@ -11,8 +11,8 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 @pytest.fixture(scope="module")
 def q():
-    from quantized_expert_decode_gb300 import build
-    build.build()
+    import __graft_entry__
+    __graft_entry__._builder().build()
     import quantized_expert_decode_gb300 as q
     return q
 

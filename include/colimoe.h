@@ -158,6 +158,34 @@ const char *coli_moe_strerror(int code);
 /* The cudaError_t of the last COLI_MOE_ECUDA returned on this thread (0 if none). */
 int coli_moe_last_cuda_error(void);
 
+/* ---- Forward without any caller-provided or allocated scratch ----
+ * The pages have no counterpart of this entry point; it exists for callers that cannot call
+ * cudaMalloc: code running where device allocation is forbidden or unavailable (a host
+ * application whose memory pool owns all device memory, a plugin or sandbox that may only
+ * launch work, a latency-critical loop that must never enter the allocator), and that
+ * therefore cannot provide the workspace coli_moe_forward asks for.
+ *
+ * It computes exactly what coli_moe_forward computes, with the same arguments minus the
+ * workspace and the optional routing outputs. Its scratch is one fixed array of
+ * COLI_MOE_NOALLOC_SCRATCH_BYTES inside the library's device image: every GPU on which the
+ * library is loaded holds that much memory until the process exits. The caller still owns
+ * and passes x, the weights and out.
+ *   - Sizes: a description whose coli_moe_workspace_bytes() exceeds
+ *     COLI_MOE_NOALLOC_SCRATCH_BYTES is rejected with COLI_MOE_EWORKSPACE before anything is
+ *     launched (at H = 6144, I = I_shared = 2048, E = 256, K = 8 this admits T <= 64).
+ *   - Set-up: the first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress, with that device current) and keeps it; make that first call
+ *     before any stream capture.
+ *   - Sharing: all calls, on every stream and thread, use the same array, which keeps the last
+ *     call's contents (each call clears what must start at zero). Calls whose work overlaps on
+ *     the GPU — on different streams, or from different threads without ordering — race on
+ *     it and give wrong results; order them on one stream.
+ *   - It calls no cudaMalloc, cudaFree or other allocating routine. */
+#define COLI_MOE_NOALLOC_SCRATCH_BYTES ((size_t)32 << 20)
+int coli_moe_forward_noalloc(const coli_moe_desc *desc, const float *x, const float *W_r,
+                             const float *bias, const coli_moe_expert *experts,
+                             const coli_moe_expert *shared, float *out, coli_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

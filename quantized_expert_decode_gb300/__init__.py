@@ -26,7 +26,9 @@ COLI_MOE_EKERNEL = -7
 # every symbol include/colimoe.h declares
 EXPORTS = ("coli_moe_workspace_bytes", "coli_moe_route", "coli_moe_forward", "coli_moe_forward_profiled",
            "coli_moe_forward_host", "coli_moe_qgemv", "coli_moe_check", "coli_moe_strerror",
-           "coli_moe_last_cuda_error")
+           "coli_moe_last_cuda_error", "coli_moe_forward_noalloc")
+
+COLI_MOE_NOALLOC_SCRATCH_BYTES = 32 << 20
 
 
 class coli_moe_desc(ctypes.Structure):
@@ -74,6 +76,8 @@ def _load():
     lib.coli_moe_check.restype = ctypes.c_int
     lib.coli_moe_strerror.argtypes = [ctypes.c_int]
     lib.coli_moe_strerror.restype = ctypes.c_char_p
+    lib.coli_moe_forward_noalloc.argtypes = [D, P, P, P, P, X, P, P]
+    lib.coli_moe_forward_noalloc.restype = ctypes.c_int
     lib.coli_moe_last_cuda_error.argtypes = []
     lib.coli_moe_last_cuda_error.restype = ctypes.c_int
     return lib
@@ -174,3 +178,15 @@ def coli_moe_check(ws, stream=None, raise_on_error=True):
 
 def coli_moe_strerror(code) -> str:
     return _lib.coli_moe_strerror(code).decode()
+
+
+def coli_moe_forward_noalloc(desc, x, W_r, bias, experts, shared, out, stream=None,
+                             raise_on_error=True):
+    """The block without a workspace, for callers that cannot allocate device memory: the
+    library's fixed COLI_MOE_NOALLOC_SCRATCH_BYTES device array serves as scratch. Calls share
+    that array, so calls that overlap on the GPU race; the first call on a device should come
+    before any stream capture."""
+    sh = ctypes.byref(shared) if shared is not None else None
+    rc = _lib.coli_moe_forward_noalloc(ctypes.byref(desc), _ptr(x), _ptr(W_r), _ptr(bias),
+                                       _ptr(experts), sh, _ptr(out), _stream(stream))
+    return _check(rc, "coli_moe_forward_noalloc", raise_on_error)

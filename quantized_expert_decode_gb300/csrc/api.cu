@@ -3,6 +3,7 @@
 // header says so (coli_moe_forward_host, coli_moe_check).
 #include <cmath>
 #include <cstring>
+#include <mutex>
 
 #include "kernels.h"
 
@@ -289,3 +290,48 @@ const char *coli_moe_strerror(int code) {
 int coli_moe_last_cuda_error(void) { return g_last_cuda; }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------- no-allocation forward
+// Scratch of coli_moe_forward_noalloc: a fixed array in this module's device image, so a
+// caller that cannot allocate device memory can still run the block. Host code never uses the
+// name as an address (on the host it is only a stand-in for the symbol); the device address
+// is looked up once per device with cudaGetSymbolAddress while that device is current.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[COLI_MOE_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+constexpr int kNoallocDevices = 64;
+std::mutex g_noalloc_mu;
+void *g_noalloc_ptr[kNoallocDevices];
+
+int noalloc_scratch(void **out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (dev < 0 || dev >= kNoallocDevices) return COLI_MOE_ENOTSUP;
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    if (!g_noalloc_ptr[dev]) {
+        void *p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (e != cudaSuccess) return cuda_fail(e);
+        if (!p) return COLI_MOE_EWORKSPACE;
+        g_noalloc_ptr[dev] = p;
+    }
+    *out = g_noalloc_ptr[dev];
+    return COLI_MOE_OK;
+}
+}  // namespace
+
+extern "C" int coli_moe_forward_noalloc(const coli_moe_desc *desc, const float *x,
+                                        const float *W_r, const float *bias,
+                                        const coli_moe_expert *experts,
+                                        const coli_moe_expert *shared, float *out,
+                                        coli_stream_t stream) {
+    int rc = validate_desc(desc);
+    if (rc) return rc;
+    if (ws_layout(*desc).total > COLI_MOE_NOALLOC_SCRATCH_BYTES) return COLI_MOE_EWORKSPACE;
+    if ((rc = check_device())) return rc;
+    void *ws = nullptr;
+    if ((rc = noalloc_scratch(&ws))) return rc;
+    return coli_moe_forward(desc, x, W_r, bias, experts, shared, out, nullptr, nullptr, ws,
+                            COLI_MOE_NOALLOC_SCRATCH_BYTES, stream);
+}

@@ -1,0 +1,65 @@
+"""coli_moe_forward_noalloc — the forward for callers that cannot allocate device memory.
+
+Such callers (a host whose memory pool owns the whole device, a plugin that may only launch
+work, a loop that must never enter the allocator) cannot hand the library a workspace. This
+entry point runs the same block on a fixed scratch array inside the library's device image.
+The test compares it with coli_moe_forward on the same inputs, two calls in a row (the second
+on fresh activations, so stale scratch from the first call would show), and checks that a
+description needing more than the fixed scratch is refused. It builds its own inputs, so it
+passes alone in a fresh process as well as after the rest of the suite; the file name keeps
+it last in collection order.
+"""
+import numpy as np
+import pytest
+import torch
+
+import synth
+
+pytestmark = pytest.mark.gpu
+
+TOL = 1e-4  # max|err| <= TOL * rms(reference), as in the parity tests
+
+
+def _rms(a):
+    return float(np.sqrt(np.mean(np.asarray(a, np.float64) ** 2)))
+
+
+@pytest.mark.parametrize("cfg", [
+    dict(T=6, H=512, I=256, E=16, K=3, I_shared=128, norm_topk=1, routed_scale=2.5,
+         routed_fmt=2, shared_fmt=1, zipf=False),
+    synth.config(1),
+])
+def test_noalloc_matches_forward_twice(cfg):
+    assert torch.cuda.is_available(), "needs a CUDA device"
+    import quantized_expert_decode_gb300 as q
+    from quantized_expert_decode_gb300.device import DeviceBlock
+
+    blk = synth.make_block(cfg, seed=4242)
+    dev = DeviceBlock(blk)
+    assert q.coli_moe_workspace_bytes(dev.desc) <= q.COLI_MOE_NOALLOC_SCRATCH_BYTES
+    T, H = cfg["T"], cfg["H"]
+    xs = synth.make_x_batches(cfg, 4242, 2)
+    for call in range(2):  # two calls in a row share the fixed scratch
+        x = torch.from_numpy(xs[call]).cuda()
+        ref = torch.empty((T, H), dtype=torch.float32, device="cuda")
+        got = torch.full((T, H), float("nan"), dtype=torch.float32, device="cuda")
+        q.coli_moe_forward(dev.desc, x, dev.Wr, dev.bias, dev.table, dev.shared, ref,
+                           ws=dev.ws, ws_bytes=dev.ws_bytes)
+        q.coli_moe_forward_noalloc(dev.desc, x, dev.Wr, dev.bias, dev.table, dev.shared, got)
+        torch.cuda.synchronize()
+        r = ref.cpu().numpy()
+        g = got.cpu().numpy()
+        assert np.all(np.isfinite(g)), call
+        err = float(np.max(np.abs(g.astype(np.float64) - r)))
+        assert err <= TOL * _rms(r), (call, err)
+
+
+def test_noalloc_refuses_oversize_description():
+    import quantized_expert_decode_gb300 as q
+    big = q.make_desc(T=2048, H=6144, I=2048, E=256, K=8, I_shared=2048, routed_scale=2.5)
+    assert q.coli_moe_workspace_bytes(big) > q.COLI_MOE_NOALLOC_SCRATCH_BYTES
+    dummy = torch.empty(16, dtype=torch.float32, device="cuda")
+    ex = q.coli_moe_expert(*[dummy.data_ptr()] * 6)
+    rc = q.coli_moe_forward_noalloc(big, dummy, dummy, dummy, dummy, ex, dummy,
+                                    raise_on_error=False)
+    assert rc == q.COLI_MOE_EWORKSPACE

@@ -1,7 +1,9 @@
 // api.cu — the C ABI of libcolimoe (include/colimoe.h): argument validation, workspace layout
 // and the launch sequence of the block. No allocation, no synchronisation except where the
 // header says so (coli_moe_forward_host, coli_moe_check).
+#include <algorithm>
 #include <cmath>
+#include <cstddef>
 #include <cstring>
 #include <mutex>
 
@@ -111,10 +113,85 @@ int record(void *const *events, int i, cudaStream_t st) {
     return e == cudaSuccess ? COLI_MOE_OK : cuda_fail(e);
 }
 
+int num_sms() {
+    static int cache[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 152;
+    if (dev >= 0 && dev < 64 && cache[dev]) return cache[dev];
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1) n = 152;
+    if (dev >= 0 && dev < 64) cache[dev] = n;
+    return n;
+}
+
+// T <= 64: router, selection, buckets, experts and combine in one persistent launch
+// (decode.cu); T > 8 computes the router logits in a preceding launch.
+int run_forward_decode(const coli_moe_desc *d, const float *x, const float *W_r, const float *bias,
+                       const coli_moe_expert *experts, const coli_moe_expert *shared, float *out,
+                       int32_t *idx_out, float *w_out, void *ws, cudaStream_t st,
+                       void *const *events) {
+    const WsLayout L = ws_layout(*d);
+    DecParams P{};
+    decode_plan(*d, P);
+    P.x = x;
+    P.Wr = W_r;
+    P.bias = bias;
+    P.experts = experts;
+    if (shared) P.shared = *shared;
+    P.out = out;
+    P.part = ws_ptr<float>(ws, L.part);
+    P.sig = ws_ptr<float>(ws, L.sig);
+    P.choice = ws_ptr<float>(ws, L.choice);
+    P.w = w_out ? w_out : ws_ptr<float>(ws, L.w);
+    P.idx = idx_out ? idx_out : ws_ptr<int32_t>(ws, L.idx);
+    P.keff = ws_ptr<int32_t>(ws, L.keff);
+    P.counts = ws_ptr<int32_t>(ws, L.counts);
+    P.offsets = ws_ptr<int32_t>(ws, L.offsets);
+    P.perm = ws_ptr<int32_t>(ws, L.perm);
+    P.pos = ws_ptr<int32_t>(ws, L.pos);
+    P.act = ws_ptr<int32_t>(ws, L.act);
+    P.h = ws_ptr<float>(ws, L.h);
+    P.y = ws_ptr<float>(ws, L.y);
+    P.ctrl = ws_ptr<DecCtrl>(ws, L.err);
+    P.tab = ws_ptr<DecTable>(ws, L.tab);
+    P.T = d->T;
+    P.H = d->H;
+    P.I = d->I;
+    P.E = d->E;
+    P.K = d->K;
+    P.Is = d->I_shared;
+    P.rfmt = d->routed_fmt;
+    P.sfmt = d->shared_fmt;
+    P.Ksel = ksel_of(d);
+    P.norm_topk = d->norm_topk;
+    P.top_p = d->top_p;
+    P.rscale = d->routed_scale;
+    P.ldh = d->I > d->I_shared ? d->I : d->I_shared;
+    const int splits = std::min(L.router_splits, 16);
+    if (P.route_only) P.nks = splits;
+    if ((size_t)P.nks * d->T * d->E * sizeof(float) > L.sig - L.part) return COLI_MOE_ENOTSUP;
+    const size_t ctrl_bytes = offsetof(DecCtrl, dn_cnt) + (size_t)P.dn_rb * sizeof(int);
+    int rc;
+    if ((rc = record(events, 0, st))) return rc;
+    cudaError_t e = cudaMemsetAsync(P.ctrl, 0, ctrl_bytes, st);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (P.route_only &&
+        (e = launch_router_partial(x, W_r, P.part, d->T, d->H, d->E, splits, st)) != cudaSuccess)
+        return cuda_fail(e);
+    if ((rc = record(events, 1, st))) return rc;
+    const int grid = decode_ctas_per_sm(P) * num_sms();
+    if ((e = launch_decode(P, grid, st)) != cudaSuccess) return cuda_fail(e);
+    if ((rc = record(events, 2, st))) return rc;
+    if ((rc = record(events, 3, st))) return rc;
+    return record(events, 4, st);
+}
+
 int run_forward(const coli_moe_desc *d, const float *x, const float *W_r, const float *bias,
                 const coli_moe_expert *experts, const coli_moe_expert *shared, float *out,
                 int32_t *idx_out, float *w_out, void *ws, cudaStream_t st,
                 void *const *events = nullptr) {
+    if (decode_supported(*d))
+        return run_forward_decode(d, x, W_r, bias, experts, shared, out, idx_out, w_out, ws, st, events);
     const WsLayout L = ws_layout(*d);
     if (int rc0 = record(events, 0, st)) return rc0;
     int32_t *idx = idx_out ? idx_out : ws_ptr<int32_t>(ws, L.idx);

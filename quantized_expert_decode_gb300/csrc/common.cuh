@@ -38,7 +38,8 @@ __host__ __device__ inline int elems_per_chunk(int fmt) {
 
 // Device workspace layout. Every region starts on a 256-byte boundary.
 struct WsLayout {
-    size_t err;       // int32[16]: [0] error word
+    size_t err;       // control block of the call; its first int32 is the error word
+    size_t tab;       // decode item table
     size_t part;      // f32 [S][T][E] router partial logits
     size_t sig;       // f32 [T][E]
     size_t choice;    // f32 [T][E]
@@ -76,6 +77,9 @@ inline int router_splits(const coli_moe_desc &d) {
     return (int)want;
 }
 
+size_t decode_ctrl_bytes();
+size_t decode_table_bytes();
+
 inline WsLayout ws_layout(const coli_moe_desc &d) {
     WsLayout L{};
     size_t p = 0;
@@ -88,7 +92,8 @@ inline WsLayout ws_layout(const coli_moe_desc &d) {
     const size_t rows = T * K + (d.I_shared > 0 ? T : 0);
     const size_t imax = (size_t)(d.I > d.I_shared ? d.I : d.I_shared);
     L.router_splits = router_splits(d);
-    L.err = take(64);
+    L.err = take(decode_ctrl_bytes());
+    L.tab = take(decode_table_bytes());
     L.part = take((size_t)L.router_splits * T * E * 4);
     L.sig = take(T * E * 4);
     L.choice = take(T * E * 4);

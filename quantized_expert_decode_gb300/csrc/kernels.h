@@ -23,6 +23,57 @@ struct ExpertWork {
     int slots;                       // grid.y: max active routed experts + (shared ? 1 : 0)
 };
 
+// ---------------------------------------------------------------- decode.cu
+constexpr int kDecMaxT = 64;              // the persistent decode kernel serves T <= 64
+constexpr int kDecMaxRowBlocks = 1024;    // H / 64 row blocks of the down projection
+
+// Counters of one decode call (zeroed before each launch; err stays the first word, which is
+// also the workspace error word read by coli_moe_check).
+struct DecCtrl {
+    int err, queue, router_done, routing_ready;
+    int pad[12];
+    int gu_done[kMaxE + 1];            // finished gate/up items per slot (shared: index kMaxE)
+    int dn_cnt[kDecMaxRowBlocks];      // finished down items per 64-row block
+};
+
+// Item table published by the routing CTA.
+struct DecTable {
+    int U, n_total, gu_base, dn_base, dn_expected, pad[3];
+    int slot_e[kMaxE + 1];
+    int slot_n[kMaxE + 1];
+    int slot_pbase[kMaxE + 1];
+    int slot_groups[kMaxE + 1];
+    int gu_off[kMaxE + 2];
+    int dn_off[kMaxE + 2];
+};
+
+struct DecParams {
+    const float *x, *Wr, *bias;
+    const coli_moe_expert *experts;
+    coli_moe_expert shared;
+    float *out;
+    float *part;               // router partial logits [nks][T][E]
+    float *sig, *choice, *w;
+    int32_t *idx, *keff, *counts, *offsets, *perm, *pos, *act;
+    float *h, *y;
+    DecCtrl *ctrl;
+    DecTable *tab;
+    int T, H, I, E, K, Is, rfmt, sfmt, Ksel, norm_topk;
+    float top_p, rscale;
+    int ldh;
+    int NV, nst, xs_stride, xs_bytes;
+    int R, route_only;         // router items; route_only: one item that only selects
+    int neb, nks, rks_floats;  // router expert blocks, k-slices, floats per k-slice
+    int G_sh_rb, groups_sh, G_sh;
+    int gu_rb, dn_rb;
+};
+
+void decode_plan(const coli_moe_desc &d, DecParams &P);
+bool decode_supported(const coli_moe_desc &d);
+size_t decode_smem_bytes(const DecParams &P);
+int decode_ctas_per_sm(const DecParams &P);
+cudaError_t launch_decode(const DecParams &P, int grid, cudaStream_t s);
+
 // router.cu
 cudaError_t launch_router_partial(const float *x, const float *W_r, float *part, int T, int H,
                                   int E, int splits, cudaStream_t s);

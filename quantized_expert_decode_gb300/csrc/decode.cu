@@ -1,6 +1,6 @@
 // decode.cu — the whole MoE block for decode-sized batches (T <= 64) in ONE persistent launch.
 //
-// Work is a list of items claimed in order from a global queue:
+// Work is a list of items, each CTA taking a static share (see Producer::run):
 //   router items       logits of 32 experts over one slice of H, for T <= 8 tokens
 //                      (colibri-strix c/glm.c @98759bf moe() phase A; r_router shader)
 //   shared gate/up     8 rows of the shared expert's gate and up (phase E)
@@ -19,10 +19,11 @@
 // (cp.async.bulk, completion counted on an mbarrier per stage); consumers dequantise from
 // shared memory (qdot.cuh) against activations staged, pre-scaled and permuted, in shared
 // memory. Dependencies between items (routing -> routed items, an expert's gate/up -> its
-// down, all experts' down of a row block -> the combine) are counters in the workspace. A
-// CTA only ever waits for items claimed before its own, which are held by running CTAs, so
-// progress is guaranteed; every wait is still bounded (2 s of %globaltimer), after which the
-// kernel records kErrWaitExpired and goes on without blocking the GPU.
+// down, all experts' down of a row block -> the combine) are counters in the workspace. Every
+// CTA finishes all of its earlier-phase items before it waits on a later phase, and the launch
+// is cooperative (all CTAs resident), so progress is guaranteed; every wait is still bounded
+// (2 s of %globaltimer), after which the kernel records kErrWaitExpired and goes on without
+// blocking the GPU.
 #include <algorithm>
 
 #include "kernels.h"
@@ -48,14 +49,26 @@ constexpr int kSharedSlotKey = kMaxE;           // gu_done index of the shared e
 
 enum Kind : int { kEnd = 0, kRouter = 1, kGateUp = 2, kDown = 3, kRouteOnly = 4 };
 
+// What the consumers need about the expert of an item (filled in by the producer, so that
+// consumers make no global lookups per item).
+struct ItemSlot {
+    const float *s0, *s1;  // gate/up: gate and up row scales; down: down row scales
+    int fmt, inter;        // weight format, intermediate size of this expert
+    int n, pbase;          // tokens using it, first bucket position (routed)
+    int key;               // gu_done index: routed slot, or kSharedSlotKey
+    int need;              // gate/up items of this expert that its down items wait for
+    int shared;
+};
+
 struct StageDesc {
-    int kind, item;
-    int slot;        // routed slot (0..U-1), U = shared; router: expert block
+    int kind;
+    int sidx, nst;   // stage index in the item, stages in the item
+    int slot;        // routed slot (0..U-1) or U = shared; router: expert block
     int rb;          // row block (gate/up: 8 pairs, down: 64 rows); router: k-slice
     int tg;          // token group
-    int sidx, nst;   // stage index in the item, stages in the item
     int row0, nrows; // rows carried by this stage (gate/up: pairs; down: rows; router: experts)
     int k0, kbytes;  // byte range of each row carried (gate/up, router); down: whole rows
+    ItemSlot it;
 };
 
 __device__ __forceinline__ void flag_error(DecCtrl *c, int code) { atomicCAS(&c->err, 0, code); }
@@ -146,6 +159,8 @@ __device__ SlotInfo slot_info(const DecParams &P, int slot, int U) {
 __device__ __forceinline__ bool bad_ptr16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) != 0; }
 
 // ------------------------------------------------------------------ producer
+__device__ __forceinline__ int range_lo(int n, int c, int G) { return (int)((long long)n * c / G); }
+
 struct Producer {
     const DecParams &P;
     uint8_t *ring;
@@ -188,11 +203,27 @@ struct Producer {
         __syncwarp();
     }
 
+    __device__ ItemSlot item_slot(const SlotInfo &si, bool down) const {
+        ItemSlot it;
+        it.s0 = down ? si.ds : si.gs;
+        it.s1 = si.us;
+        it.fmt = si.fmt;
+        it.inter = si.inter;
+        it.n = si.n;
+        it.pbase = si.pbase;
+        it.key = si.key;
+        it.need = si.shared ? P.G_sh : P.gu_rb * si.groups;
+        it.shared = si.shared ? 1 : 0;
+        return it;
+    }
+
     // T > 8: the logits come from an earlier launch; one item only runs the selection
-    __device__ void route_only_item(int item) {
+    __device__ void route_only_item() {
         const int s = acquire();
         if (lane == 0) {
-            desc[s] = StageDesc{kRouteOnly, item, 0, 0, 0, 0, 1, 0, 0, 0, 0};
+            desc[s].kind = kRouteOnly;
+            desc[s].sidx = 0;
+            desc[s].nst = 1;
             mbar_arrive(&full[s]);
         }
         __syncwarp();
@@ -205,13 +236,23 @@ struct Producer {
         const int kbeg = ks * P.rks_floats;
         const int kend = min(P.H, kbeg + P.rks_floats);
         const int nst = (kend - kbeg + kRtKc / 4 - 1) / (kRtKc / 4);
+        const int ne = min(kRtE, P.E - e0);
         for (int st = 0; st < nst; st++) {
             const int s = acquire();
             const int kf = kbeg + st * (kRtKc / 4);
             const int nf = min(kRtKc / 4, kend - kf);
-            const int ne = min(kRtE, P.E - e0);
             if (lane == 0) {
-                desc[s] = StageDesc{kRouter, item, eb, ks, 0, st, nst, e0, ne, kf * 4, nf * 4};
+                StageDesc &d = desc[s];
+                d.kind = kRouter;
+                d.sidx = st;
+                d.nst = nst;
+                d.slot = eb;
+                d.rb = ks;
+                d.tg = 0;
+                d.row0 = e0;
+                d.nrows = ne;
+                d.k0 = kf * 4;
+                d.kbytes = nf * 4;
                 mbar_arrive_expect_tx(&full[s], (uint32_t)(ne * nf * 4));
             }
             __syncwarp();
@@ -221,17 +262,29 @@ struct Producer {
         }
     }
 
-    __device__ void gateup_item(int item, int slot, int rb, int tg, const SlotInfo &si) {
+    __device__ void gateup_item(int slot, int rb, int tg, const SlotInfo &si) {
         const int64_t rbytes = row_bytes(si.fmt, P.H);
         const int j0 = rb * kGuPairs;
         const int np = min(kGuPairs, si.inter - j0);
         const int nst = (int)((rbytes + kGuKc - 1) / kGuKc);
+        const ItemSlot it = item_slot(si, false);
         for (int st = 0; st < nst; st++) {
             const int s = acquire();
             const int k0 = st * kGuKc;
             const int kb = (int)((rbytes - k0) < kGuKc ? (rbytes - k0) : kGuKc);
             if (lane == 0) {
-                desc[s] = StageDesc{kGateUp, item, slot, rb, tg, st, nst, j0, np, k0, kb};
+                StageDesc &d = desc[s];
+                d.kind = kGateUp;
+                d.sidx = st;
+                d.nst = nst;
+                d.slot = slot;
+                d.rb = rb;
+                d.tg = tg;
+                d.row0 = j0;
+                d.nrows = np;
+                d.k0 = k0;
+                d.kbytes = kb;
+                d.it = it;
                 mbar_arrive_expect_tx(&full[s], (uint32_t)(2 * np * kb));
             }
             __syncwarp();
@@ -246,19 +299,31 @@ struct Producer {
         }
     }
 
-    __device__ void down_item(int item, int slot, int rb, int tg, const SlotInfo &si) {
+    __device__ void down_item(int slot, int rb, int tg, const SlotInfo &si) {
         const int64_t rbytes = row_bytes(si.fmt, si.inter);
         const int64_t rfit = kSB / rbytes;
         const int rps = rfit < 1 ? 1 : (rfit > 16 ? 16 : (int)rfit);
         const int d0 = rb * kDnRows;
         const int nrows = min(kDnRows, P.H - d0);
         const int nst = (nrows + rps - 1) / rps;
+        const ItemSlot it = item_slot(si, true);
         for (int st = 0; st < nst; st++) {
             const int s = acquire();
             const int r0 = d0 + st * rps;
             const int nr = min(rps, d0 + nrows - r0);
             if (lane == 0) {
-                desc[s] = StageDesc{kDown, item, slot, rb, tg, st, nst, r0, nr, 0, (int)rbytes};
+                StageDesc &d = desc[s];
+                d.kind = kDown;
+                d.sidx = st;
+                d.nst = nst;
+                d.slot = slot;
+                d.rb = rb;
+                d.tg = tg;
+                d.row0 = r0;
+                d.nrows = nr;
+                d.k0 = 0;
+                d.kbytes = (int)rbytes;
+                d.it = it;
                 mbar_arrive_expect_tx(&full[s], (uint32_t)(nr * rbytes));
                 bulk_g2s(stage_buf(s), si.dw + (size_t)r0 * rbytes, (uint32_t)(nr * rbytes), &full[s]);
             }
@@ -267,61 +332,83 @@ struct Producer {
         }
     }
 
+    __device__ bool slot_ok(const SlotInfo &si) {
+        if (bad_ptr16(si.gw) || bad_ptr16(si.uw) || bad_ptr16(si.dw)) {
+            if (lane == 0) flag_error(P.ctrl, kErrBadExpert);
+            return false;
+        }
+        return true;
+    }
+
+    // Static schedule: CTA c takes router items c, c+G, ...; then its contiguous share of the
+    // shared expert's gate/up items; after routing, its contiguous share of the routed gate/up
+    // items and then of all down items. Inside each share the items run in increasing order, so
+    // every wait is on work that some co-resident CTA reaches first (cooperative launch).
     __device__ void run() {
-        const int gu_base = P.R + P.G_sh;
-        for (;;) {
-            int item = 0;
-            if (lane == 0) item = atomicAdd(&P.ctrl->queue, 1);
-            item = __shfl_sync(kFull, item, 0);
-            if (item < P.R) {
-                if (P.route_only) route_only_item(item);
-                else router_item(item);
-                continue;
-            }
-            if (item < gu_base) {
-                const int l = item - P.R;
-                const int U0 = 0;  // shared slot info does not depend on routing
-                SlotInfo si = slot_info(P, 0, U0);
-                gateup_item(item, -1, l % P.G_sh_rb, l / P.G_sh_rb, si);
-                continue;
-            }
-            // routed work: the item table is published by the routing CTA
-            int ready = 1;
-            if (lane == 0) ready = wait_at_least(&P.ctrl->routing_ready, 1, P.ctrl) ? 1 : 0;
-            ready = __shfl_sync(kFull, ready, 0);
-            __threadfence();
+        const int G = gridDim.x, c = blockIdx.x;
+        for (int r = c; r < P.R; r += G) {
+            if (P.route_only) route_only_item();
+            else router_item(r);
+        }
+        if (P.G_sh > 0) {
+            const int b = range_lo(P.G_sh, c, G), e = range_lo(P.G_sh, c + 1, G);
+            const SlotInfo si = slot_info(P, 0, 0);
+            for (int l = b; l < e; l++) gateup_item(-1, l % P.G_sh_rb, l / P.G_sh_rb, si);
+        }
+        int ready = 1;
+        if (lane == 0) ready = wait_at_least(&P.ctrl->routing_ready, 1, P.ctrl) ? 1 : 0;
+        ready = __shfl_sync(kFull, ready, 0);
+        __threadfence();
+        if (ready) {
             const DecTable *tb = P.tab;
-            const int n_total = __ldcg(&tb->n_total);
-            if (!ready || item >= n_total) {
-                publish_end();
-                drain();
-                return;
-            }
             const int U = __ldcg(&tb->U);
-            const int dn_base = __ldcg(&tb->dn_base);
-            if (item < dn_base) {
-                const int l = item - gu_base;
-                const int slot = upper_slot(tb->gu_off, U, l);
-                const int ll = l - __ldcg(&tb->gu_off[slot]);
+            // routed gate/up share
+            const int gu_tot = __ldcg(&tb->gu_off[U]);
+            int b = range_lo(gu_tot, c, G), e = range_lo(gu_tot, c + 1, G);
+            if (b < e) {
+                int slot = upper_slot(tb->gu_off, U, b);
+                int lo = __ldcg(&tb->gu_off[slot]), hi = __ldcg(&tb->gu_off[slot + 1]);
                 SlotInfo si = slot_info(P, slot, U);
-                if (bad_ptr16(si.gw) || bad_ptr16(si.uw)) {
-                    if (lane == 0) flag_error(P.ctrl, kErrBadExpert);
-                    continue;
+                bool ok = slot_ok(si);
+                for (int l = b; l < e; l++) {
+                    while (l >= hi) {
+                        slot++;
+                        lo = hi;
+                        hi = __ldcg(&tb->gu_off[slot + 1]);
+                        si = slot_info(P, slot, U);
+                        ok = slot_ok(si);
+                    }
+                    if (!ok) continue;
+                    const int ll = l - lo;
+                    gateup_item(slot, ll % P.gu_rb, ll / P.gu_rb, si);
                 }
-                gateup_item(item, slot, ll % P.gu_rb, ll / P.gu_rb, si);
-            } else {
-                const int l = item - dn_base;
-                const int nslots = U + (P.Is > 0 ? 1 : 0);
-                const int slot = upper_slot(tb->dn_off, nslots, l);
-                const int ll = l - __ldcg(&tb->dn_off[slot]);
+            }
+            // down share (routed slots, then the shared expert as slot U)
+            const int nslots = U + (P.Is > 0 ? 1 : 0);
+            const int dn_tot = __ldcg(&tb->dn_off[nslots]);
+            b = range_lo(dn_tot, c, G);
+            e = range_lo(dn_tot, c + 1, G);
+            if (b < e) {
+                int slot = upper_slot(tb->dn_off, nslots, b);
+                int lo = __ldcg(&tb->dn_off[slot]), hi = __ldcg(&tb->dn_off[slot + 1]);
                 SlotInfo si = slot_info(P, slot, U);
-                if (bad_ptr16(si.dw)) {
-                    if (lane == 0) flag_error(P.ctrl, kErrBadExpert);
-                    continue;
+                bool ok = slot_ok(si);
+                for (int l = b; l < e; l++) {
+                    while (l >= hi) {
+                        slot++;
+                        lo = hi;
+                        hi = __ldcg(&tb->dn_off[slot + 1]);
+                        si = slot_info(P, slot, U);
+                        ok = slot_ok(si);
+                    }
+                    if (!ok) continue;
+                    const int ll = l - lo;
+                    down_item(slot, ll % P.dn_rb, ll / P.dn_rb, si);
                 }
-                down_item(item, slot, ll % P.dn_rb, ll / P.dn_rb, si);
             }
         }
+        publish_end();
+        drain();
     }
 };
 
@@ -604,53 +691,50 @@ struct Consumer {
     int *sflag;    // shared flag word
     int tid, lane, warp;
     int seq = 0;
-    int xs_key = -1;  // T == 1: format of the x currently staged (-1: none)
+    int key0 = -1, key1 = -1, key2 = -1;  // what XS currently holds (kind, slot/bucket, group)
+    int dn_expected = -1;
     float2 acc[2][4];
     float racc[4][8];
 
-    __device__ void stage_tokens_x(const SlotInfo &si, int tg) {
-        const int nv = min(P.NV, si.n - tg * P.NV);
-        if (P.T == 1 && xs_key == si.fmt) return;
+    // activations of token group tg of the item's expert, staged pre-scaled and permuted for
+    // its format (x for gate/up, h for down); skipped when XS already holds them
+    __device__ void stage_acts(const ItemSlot &it, int tg, bool down) {
+        const int k0 = down ? 2 : 1;
+        const int k1 = down ? it.key : (P.T == 1 ? 0 : (it.shared ? -1 : it.pbase));
+        const int k2 = (P.T == 1 && !down) ? it.fmt : tg * 8 + it.fmt;
+        if (key0 == k0 && key1 == k1 && key2 == k2) return;
+        const int nv = min(P.NV, it.n - tg * P.NV);
+        const int len = down ? it.inter : P.H;
+        const int gran = it.fmt == COLI_FMT_INT4 ? 32 : it.fmt == COLI_FMT_INT8 ? 16 : 64;
+        const int CPR = len / gran;
         consumer_bar();
         for (int v = 0; v < P.NV; v++) {
             float *dst = xs + (size_t)v * P.xs_stride;
             if (v < nv) {
                 const int pv = tg * P.NV + v;
-                const int t = si.shared ? pv : __ldcg(P.perm + si.pbase + pv) / P.K;
-                const float *src = P.x + (size_t)t * P.H;
-                if (si.fmt == COLI_FMT_INT4) stage_vec<COLI_FMT_INT4>(src, dst, P.H, P.H / 32, tid, kCT);
-                else if (si.fmt == COLI_FMT_INT8) stage_vec<COLI_FMT_INT8>(src, dst, P.H, P.H / 16, tid, kCT);
-                else stage_vec<COLI_FMT_INT2>(src, dst, P.H, P.H / 64, tid, kCT);
-            } else {
-                for (int i = tid; i < P.H; i += kCT) dst[i] = 0.f;
-            }
-        }
-        xs_key = P.T == 1 ? si.fmt : -1;
-        consumer_bar();
-    }
-
-    __device__ void stage_tokens_h(const SlotInfo &si, int tg) {
-        const int nv = min(P.NV, si.n - tg * P.NV);
-        consumer_bar();
-        for (int v = 0; v < P.NV; v++) {
-            float *dst = xs + (size_t)v * P.xs_stride;
-            if (v < nv) {
-                const int pv = tg * P.NV + v;
-                const int row = si.shared ? P.T * P.K + pv : si.pbase + pv;
-                const float *src = P.h + (size_t)row * P.ldh;
-                for (int i = tid; i < si.inter; i += kCT) {
+                const float *src;
+                if (down) {
+                    const int row = it.shared ? P.T * P.K + pv : it.pbase + pv;
+                    src = P.h + (size_t)row * P.ldh;
+                } else {
+                    const int t = it.shared ? pv : __ldcg(P.perm + it.pbase + pv) / P.K;
+                    src = P.x + (size_t)t * P.H;
+                }
+                for (int i = tid; i < len; i += kCT) {
                     float sc;
                     int at;
-                    if (si.fmt == COLI_FMT_INT4) at = staged_index<COLI_FMT_INT4>(i, si.inter / 32, sc);
-                    else if (si.fmt == COLI_FMT_INT8) at = staged_index<COLI_FMT_INT8>(i, si.inter / 16, sc);
-                    else at = staged_index<COLI_FMT_INT2>(i, si.inter / 64, sc);
-                    dst[at] = __ldcg(src + i) * sc;
+                    if (it.fmt == COLI_FMT_INT4) at = staged_index<COLI_FMT_INT4>(i, CPR, sc);
+                    else if (it.fmt == COLI_FMT_INT8) at = staged_index<COLI_FMT_INT8>(i, CPR, sc);
+                    else at = staged_index<COLI_FMT_INT2>(i, CPR, sc);
+                    dst[at] = (down ? __ldcg(src + i) : __ldg(src + i)) * sc;
                 }
             } else {
-                for (int i = tid; i < si.inter; i += kCT) dst[i] = 0.f;
+                for (int i = tid; i < len; i += kCT) dst[i] = 0.f;
             }
         }
-        xs_key = -1;
+        key0 = k0;
+        key1 = k1;
+        key2 = k2;
         consumer_bar();
     }
 
@@ -711,7 +795,7 @@ struct Consumer {
         if (last) {
             __threadfence();
             route_final(P, reinterpret_cast<int *>(xs));
-            xs_key = -1;
+            key0 = -1;
         }
     }
 
@@ -734,7 +818,7 @@ struct Consumer {
     }
 
     template <int NV>
-    __device__ void gateup_finish_t(const StageDesc &d, const SlotInfo &si) {
+    __device__ void gateup_finish_t(const StageDesc &d) {
         float2 a[2][NV];
 #pragma unroll
         for (int r = 0; r < 2; r++)
@@ -742,16 +826,17 @@ struct Consumer {
             for (int v = 0; v < NV; v++) a[r][v] = acc[r][v];
         float sum[2][NV];
         warp_reduce_acc<2, NV>(a, sum);
+        const ItemSlot &it = d.it;
         const int j = d.row0 + warp;
-        const int nv = min(P.NV, si.n - d.tg * P.NV);
+        const int nv = min(P.NV, it.n - d.tg * P.NV);
         if (warp < d.nrows) {
 #pragma unroll
             for (int v = 0; v < NV; v++) {
                 if (lane == v && v < nv) {
-                    const float g = sum[0][v] * si.gs[j];
-                    const float u = sum[1][v] * si.us[j];
+                    const float g = sum[0][v] * it.s0[j];
+                    const float u = sum[1][v] * it.s1[j];
                     const int pv = d.tg * P.NV + v;
-                    const int row = si.shared ? P.T * P.K + pv : si.pbase + pv;
+                    const int row = it.shared ? P.T * P.K + pv : it.pbase + pv;
                     P.h[(size_t)row * P.ldh + j] = g / (1.f + expf(-g)) * u;
                 }
             }
@@ -760,10 +845,11 @@ struct Consumer {
 
     // ---------------- down stages: each warp owns whole rows of the stage
     template <int FMT, int NV>
-    __device__ void down_stage_t(const StageDesc &d, const uint8_t *buf, const SlotInfo &si) {
-        const int64_t rbytes = d.kbytes;
-        const int CPR = si.inter / QGeom<FMT>::EPC;
-        const int nv = min(P.NV, si.n - d.tg * P.NV);
+    __device__ void down_stage_t(const StageDesc &d, const uint8_t *buf) {
+        const ItemSlot &it = d.it;
+        const int rbytes = d.kbytes;
+        const int CPR = it.inter / QGeom<FMT>::EPC;
+        const int nv = min(P.NV, it.n - d.tg * P.NV);
         for (int r = warp; r < d.nrows; r += kCW) {
             const uint8_t *rows[1] = {buf + r * rbytes};
             float2 a[1][NV];
@@ -777,8 +863,8 @@ struct Consumer {
             for (int v = 0; v < NV; v++) {
                 if (lane == v && v < nv) {
                     const int pv = d.tg * P.NV + v;
-                    const int row = si.shared ? P.T * P.K + pv : si.pbase + pv;
-                    P.y[(size_t)row * P.H + dd] = sum[0][v] * si.ds[dd];
+                    const int row = it.shared ? P.T * P.K + pv : it.pbase + pv;
+                    P.y[(size_t)row * P.H + dd] = sum[0][v] * it.s0[dd];
                 }
             }
         }
@@ -802,7 +888,8 @@ struct Consumer {
     }
 
     template <int NV>
-    __device__ void process_nv(const StageDesc &d, const uint8_t *buf, SlotInfo &si) {
+    __device__ void process_nv(const StageDesc &d, const uint8_t *buf) {
+        const int fmt = d.it.fmt;
         if (d.kind == kGateUp) {
             if (d.sidx == 0) {
 #pragma unroll
@@ -810,19 +897,17 @@ struct Consumer {
 #pragma unroll
                     for (int v = 0; v < 4; v++) acc[r][v] = make_float2(0.f, 0.f);
             }
-            if (si.fmt == COLI_FMT_INT4) gateup_stage_t<COLI_FMT_INT4, NV>(d, buf);
-            else if (si.fmt == COLI_FMT_INT8) gateup_stage_t<COLI_FMT_INT8, NV>(d, buf);
+            if (fmt == COLI_FMT_INT4) gateup_stage_t<COLI_FMT_INT4, NV>(d, buf);
+            else if (fmt == COLI_FMT_INT8) gateup_stage_t<COLI_FMT_INT8, NV>(d, buf);
             else gateup_stage_t<COLI_FMT_INT2, NV>(d, buf);
         } else {
-            if (si.fmt == COLI_FMT_INT4) down_stage_t<COLI_FMT_INT4, NV>(d, buf, si);
-            else if (si.fmt == COLI_FMT_INT8) down_stage_t<COLI_FMT_INT8, NV>(d, buf, si);
-            else down_stage_t<COLI_FMT_INT2, NV>(d, buf, si);
+            if (fmt == COLI_FMT_INT4) down_stage_t<COLI_FMT_INT4, NV>(d, buf);
+            else if (fmt == COLI_FMT_INT8) down_stage_t<COLI_FMT_INT8, NV>(d, buf);
+            else down_stage_t<COLI_FMT_INT2, NV>(d, buf);
         }
     }
 
     __device__ void run() {
-        SlotInfo si{};
-        int U = 0;
         for (;;) {
             const int s = seq % P.nst, use = seq / P.nst;
             if (!mbar_wait(&full[s], use & 1, P.ctrl)) break;  // flagged; the producer drains
@@ -834,7 +919,7 @@ struct Consumer {
                 if (lane == 0) mbar_arrive(&empty[s]);
                 seq++;
                 route_final(P, reinterpret_cast<int *>(xs));
-                xs_key = -1;
+                key0 = -1;
                 continue;
             }
             if (d.kind == kRouter) {
@@ -846,42 +931,37 @@ struct Consumer {
                 continue;
             }
             if (d.sidx == 0) {
-                // a new gate/up or down item: resolve its expert and stage its activations
-                if (d.slot >= 0) U = __ldcg(&P.tab->U);
-                si = d.slot < 0 ? slot_info(P, 0, 0) : slot_info(P, d.slot, U);
                 if (d.kind == kGateUp) {
-                    stage_tokens_x(si, d.tg);
+                    stage_acts(d.it, d.tg, false);
                 } else {
-                    if (tid == 0) {
-                        const int need = si.shared ? P.G_sh : P.gu_rb * si.groups;
-                        wait_at_least(&P.ctrl->gu_done[si.key], need, P.ctrl);
-                    }
+                    // this expert's h rows must be complete before they are staged
+                    if (tid == 0) wait_at_least(&P.ctrl->gu_done[d.it.key], d.it.need, P.ctrl);
                     consumer_bar();
                     __threadfence();
-                    stage_tokens_h(si, d.tg);
+                    stage_acts(d.it, d.tg, true);
                 }
             }
-            if (P.NV == 1) process_nv<1>(d, buf, si);
-            else if (P.NV == 2) process_nv<2>(d, buf, si);
-            else process_nv<4>(d, buf, si);
+            if (P.NV == 1) process_nv<1>(d, buf);
+            else if (P.NV == 2) process_nv<2>(d, buf);
+            else process_nv<4>(d, buf);
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[s]);
             seq++;
             if (d.sidx != d.nst - 1) continue;
             // item complete
             if (d.kind == kGateUp) {
-                if (P.NV == 1) gateup_finish_t<1>(d, si);
-                else if (P.NV == 2) gateup_finish_t<2>(d, si);
-                else gateup_finish_t<4>(d, si);
+                if (P.NV == 1) gateup_finish_t<1>(d);
+                else if (P.NV == 2) gateup_finish_t<2>(d);
+                else gateup_finish_t<4>(d);
                 __threadfence();
                 consumer_bar();
-                if (tid == 0) atomicAdd(&P.ctrl->gu_done[si.key], 1);
+                if (tid == 0) atomicAdd(&P.ctrl->gu_done[d.it.key], 1);
             } else {
                 __threadfence();
                 consumer_bar();
                 if (tid == 0) {
-                    const int expected = __ldcg(&P.tab->dn_expected);
-                    *sflag = atomicAdd(&P.ctrl->dn_cnt[d.rb], 1) == expected - 1;
+                    if (dn_expected < 0) dn_expected = __ldcg(&P.tab->dn_expected);
+                    *sflag = atomicAdd(&P.ctrl->dn_cnt[d.rb], 1) == dn_expected - 1;
                 }
                 consumer_bar();
                 const bool last = *sflag;
@@ -972,8 +1052,10 @@ cudaError_t launch_decode(const DecParams &P, int grid, cudaStream_t st) {
     const size_t smem = decode_smem_bytes(P);
     cudaError_t e = cudaFuncSetAttribute(moe_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    moe_decode_kernel<<<grid, kDecThreads, smem, st>>>(P);
-    return cudaGetLastError();
+    // cooperative: every CTA of the static schedule is resident at once
+    void *args[] = {const_cast<DecParams *>(&P)};
+    return cudaLaunchCooperativeKernel((const void *)moe_decode_kernel, dim3(grid), dim3(kDecThreads), args,
+                                       smem, st);
 }
 
 int decode_ctas_per_sm(const DecParams &P) {

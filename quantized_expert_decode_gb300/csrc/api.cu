@@ -170,7 +170,9 @@ int run_forward_decode(const coli_moe_desc *d, const float *x, const float *W_r,
     const int splits = std::min(L.router_splits, 16);
     if (P.route_only) P.nks = splits;
     if ((size_t)P.nks * d->T * d->E * sizeof(float) > L.sig - L.part) return COLI_MOE_ENOTSUP;
-    const size_t ctrl_bytes = offsetof(DecCtrl, dn_cnt) + (size_t)P.dn_rb * sizeof(int);
+    const size_t ctrl_bytes = sizeof(DecCtrl);
+    const int grid = num_sms();
+    if (!decode_plan_grid(*d, P, grid) || decode_ctas_per_sm(P) < 1) return COLI_MOE_ENOTSUP;
     int rc;
     if ((rc = record(events, 0, st))) return rc;
     cudaError_t e = cudaMemsetAsync(P.ctrl, 0, ctrl_bytes, st);
@@ -179,7 +181,6 @@ int run_forward_decode(const coli_moe_desc *d, const float *x, const float *W_r,
         (e = launch_router_partial(x, W_r, P.part, d->T, d->H, d->E, splits, st)) != cudaSuccess)
         return cuda_fail(e);
     if ((rc = record(events, 1, st))) return rc;
-    const int grid = decode_ctas_per_sm(P) * num_sms();
     if ((e = launch_decode(P, grid, st)) != cudaSuccess) return cuda_fail(e);
     if ((rc = record(events, 2, st))) return rc;
     if ((rc = record(events, 3, st))) return rc;
@@ -190,8 +191,12 @@ int run_forward(const coli_moe_desc *d, const float *x, const float *W_r, const 
                 const coli_moe_expert *experts, const coli_moe_expert *shared, float *out,
                 int32_t *idx_out, float *w_out, void *ws, cudaStream_t st,
                 void *const *events = nullptr) {
-    if (decode_supported(*d))
-        return run_forward_decode(d, x, W_r, bias, experts, shared, out, idx_out, w_out, ws, st, events);
+    if (decode_supported(*d)) {
+        DecParams probe{};
+        decode_plan(*d, probe);
+        if (decode_plan_grid(*d, probe, num_sms()))
+            return run_forward_decode(d, x, W_r, bias, experts, shared, out, idx_out, w_out, ws, st, events);
+    }
     const WsLayout L = ws_layout(*d);
     if (int rc0 = record(events, 0, st)) return rc0;
     int32_t *idx = idx_out ? idx_out : ws_ptr<int32_t>(ws, L.idx);

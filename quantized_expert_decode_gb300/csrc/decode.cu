@@ -6,9 +6,10 @@
 //   shared gate/up     8 rows of the shared expert's gate and up (phase E)
 //   routed gate/up     8 rows of one selected expert's gate and up, for up to NV tokens
 //                      (phases C/D: g = gate.x, u = up.x, h = silu(g)*u; moe_gemv + moe_silu)
-//   down               64 rows of one expert's down projection, then, by the item that
-//                      completes a 64-row block across all experts, the weighted combine of
-//                      that block in selection order plus the shared expert (phases C/D/E)
+//   down               each CTA owns a slice of the H output rows: for every selected expert
+//                      and the shared one it computes its rows of y = down.h into shared
+//                      memory, then combines them in selection order plus the shared expert
+//                      and writes out (phases C/D/E) — no atomics, no global y
 // The item ids of routed work are only known after routing: the CTA that finishes the last
 // router item (an atomic ticket) runs the top-K selection (r_top8_par's lane-blocked warp
 // argmax, ties to the lower index, TOPK/TOPP, renorm, routed scale), the token->expert
@@ -18,8 +19,8 @@
 // their weights into a ring of 16 KB shared-memory stages with bulk asynchronous copies
 // (cp.async.bulk, completion counted on an mbarrier per stage); consumers dequantise from
 // shared memory (qdot.cuh) against activations staged, pre-scaled and permuted, in shared
-// memory. Dependencies between items (routing -> routed items, an expert's gate/up -> its
-// down, all experts' down of a row block -> the combine) are counters in the workspace. Every
+// memory. Dependencies (routing -> routed work, an expert's gate/up -> its down) are counters
+// in the workspace, raised once per CTA per expert. Every
 // CTA finishes all of its earlier-phase items before it waits on a later phase, and the launch
 // is cooperative (all CTAs resident), so progress is guaranteed; every wait is still bounded
 // (2 s of %globaltimer), after which the kernel records kErrWaitExpired and goes on without
@@ -43,7 +44,6 @@ constexpr int kGuKc = kSB / (2 * kGuPairs);     // 1024 bytes of each row per st
 constexpr int kRtE = 32;                        // experts per router item (4 per consumer warp)
 constexpr int kRtKc = kSB / kRtE;               // 512 bytes (128 floats) of each W_r row per stage
 constexpr int kRtStages = 4;                    // stages per router item
-constexpr int kDnRows = 64;                     // down rows per item
 constexpr unsigned long long kWaitNs = 2000000000ull;
 constexpr int kSharedSlotKey = kMaxE;           // gu_done index of the shared expert
 
@@ -56,7 +56,7 @@ struct ItemSlot {
     int fmt, inter;        // weight format, intermediate size of this expert
     int n, pbase;          // tokens using it, first bucket position (routed)
     int key;               // gu_done index: routed slot, or kSharedSlotKey
-    int need;              // gate/up items of this expert that its down items wait for
+    int need;              // gate/up items of this expert that its down work waits for
     int shared;
 };
 
@@ -68,6 +68,8 @@ struct StageDesc {
     int tg;          // token group
     int row0, nrows; // rows carried by this stage (gate/up: pairs; down: rows; router: experts)
     int k0, kbytes;  // byte range of each row carried (gate/up, router); down: whole rows
+    int sig;         // gate/up: >0 on the last stage of this CTA's run of items of one expert
+                     // (the number of items in the run, added to that expert's counter)
     ItemSlot it;
 };
 
@@ -169,10 +171,10 @@ struct Producer {
     int lane;
     int seq = 0;
 
-    __device__ uint8_t *stage_buf(int s) { return ring + (size_t)s * kSB; }
+    __device__ __forceinline__ uint8_t *stage_buf(int s) { return ring + (size_t)s * kSB; }
 
     // wait for ring stage `seq` to be free, return its index
-    __device__ int acquire() {
+    __device__ __forceinline__ int acquire() {
         const int s = seq % P.nst, use = seq / P.nst;
         if (use > 0) {
             if (lane == 0) mbar_wait(&empty[s], (use - 1) & 1, P.ctrl);
@@ -181,7 +183,7 @@ struct Producer {
         return s;
     }
 
-    __device__ void publish_end() {
+    __device__ __forceinline__ void publish_end() {
         const int s = acquire();
         if (lane == 0) {
             desc[s].kind = kEnd;
@@ -193,7 +195,7 @@ struct Producer {
 
     // before the producer leaves, every copy it issued has landed (each stage's last use has
     // completed its phase), so no bulk copy is in flight when the CTA exits
-    __device__ void drain() {
+    __device__ __forceinline__ void drain() {
         if (lane == 0) {
             for (int s = 0; s < P.nst && s < seq; s++) {
                 const int last = s + ((seq - 1 - s) / P.nst) * P.nst;
@@ -203,7 +205,7 @@ struct Producer {
         __syncwarp();
     }
 
-    __device__ ItemSlot item_slot(const SlotInfo &si, bool down) const {
+    __device__ __forceinline__ ItemSlot item_slot(const SlotInfo &si, bool down) const {
         ItemSlot it;
         it.s0 = down ? si.ds : si.gs;
         it.s1 = si.us;
@@ -218,7 +220,7 @@ struct Producer {
     }
 
     // T > 8: the logits come from an earlier launch; one item only runs the selection
-    __device__ void route_only_item() {
+    __device__ __forceinline__ void route_only_item() {
         const int s = acquire();
         if (lane == 0) {
             desc[s].kind = kRouteOnly;
@@ -230,7 +232,7 @@ struct Producer {
         seq++;
     }
 
-    __device__ void router_item(int item) {
+    __device__ __forceinline__ void router_item(int item) {
         const int eb = item % P.neb, ks = item / P.neb;
         const int e0 = eb * kRtE;
         const int kbeg = ks * P.rks_floats;
@@ -253,6 +255,7 @@ struct Producer {
                 d.nrows = ne;
                 d.k0 = kf * 4;
                 d.kbytes = nf * 4;
+                d.sig = 0;
                 mbar_arrive_expect_tx(&full[s], (uint32_t)(ne * nf * 4));
             }
             __syncwarp();
@@ -262,7 +265,9 @@ struct Producer {
         }
     }
 
-    __device__ void gateup_item(int slot, int rb, int tg, const SlotInfo &si) {
+    // 8 row pairs (gate row j, up row j) of one expert for token group tg; `sig` is set on the
+    // item's last stage when it closes this CTA's run of items of that expert
+    __device__ __forceinline__ void gateup_item(int slot, int rb, int tg, const SlotInfo &si, int sig) {
         const int64_t rbytes = row_bytes(si.fmt, P.H);
         const int j0 = rb * kGuPairs;
         const int np = min(kGuPairs, si.inter - j0);
@@ -284,6 +289,7 @@ struct Producer {
                 d.nrows = np;
                 d.k0 = k0;
                 d.kbytes = kb;
+                d.sig = st == nst - 1 ? sig : 0;
                 d.it = it;
                 mbar_arrive_expect_tx(&full[s], (uint32_t)(2 * np * kb));
             }
@@ -299,30 +305,30 @@ struct Producer {
         }
     }
 
-    __device__ void down_item(int slot, int rb, int tg, const SlotInfo &si) {
+    // rows [r_lo, r_hi) of one expert's down projection for token group tg, whole rows per stage
+    __device__ __forceinline__ void down_rows(int slot, int tg, int r_lo, int r_hi, const SlotInfo &si) {
         const int64_t rbytes = row_bytes(si.fmt, si.inter);
         const int64_t rfit = kSB / rbytes;
         const int rps = rfit < 1 ? 1 : (rfit > 16 ? 16 : (int)rfit);
-        const int d0 = rb * kDnRows;
-        const int nrows = min(kDnRows, P.H - d0);
-        const int nst = (nrows + rps - 1) / rps;
+        const int nst = (r_hi - r_lo + rps - 1) / rps;
         const ItemSlot it = item_slot(si, true);
         for (int st = 0; st < nst; st++) {
             const int s = acquire();
-            const int r0 = d0 + st * rps;
-            const int nr = min(rps, d0 + nrows - r0);
+            const int r0 = r_lo + st * rps;
+            const int nr = min(rps, r_hi - r0);
             if (lane == 0) {
                 StageDesc &d = desc[s];
                 d.kind = kDown;
                 d.sidx = st;
                 d.nst = nst;
                 d.slot = slot;
-                d.rb = rb;
+                d.rb = 0;
                 d.tg = tg;
                 d.row0 = r0;
                 d.nrows = nr;
-                d.k0 = 0;
+                d.k0 = r_lo;
                 d.kbytes = (int)rbytes;
+                d.sig = 0;
                 d.it = it;
                 mbar_arrive_expect_tx(&full[s], (uint32_t)(nr * rbytes));
                 bulk_g2s(stage_buf(s), si.dw + (size_t)r0 * rbytes, (uint32_t)(nr * rbytes), &full[s]);
@@ -332,7 +338,7 @@ struct Producer {
         }
     }
 
-    __device__ bool slot_ok(const SlotInfo &si) {
+    __device__ __forceinline__ bool slot_ok(const SlotInfo &si) {
         if (bad_ptr16(si.gw) || bad_ptr16(si.uw) || bad_ptr16(si.dw)) {
             if (lane == 0) flag_error(P.ctrl, kErrBadExpert);
             return false;
@@ -340,11 +346,12 @@ struct Producer {
         return true;
     }
 
-    // Static schedule: CTA c takes router items c, c+G, ...; then its contiguous share of the
-    // shared expert's gate/up items; after routing, its contiguous share of the routed gate/up
-    // items and then of all down items. Inside each share the items run in increasing order, so
-    // every wait is on work that some co-resident CTA reaches first (cooperative launch).
-    __device__ void run() {
+    // Static schedule. CTA c takes router items c, c+G, ...; its contiguous share of the shared
+    // expert's gate/up items; after routing, its contiguous share of the routed gate/up items;
+    // then its slice of the H down-projection rows for every expert. Each phase finishes in a CTA
+    // before it waits on the next, and all CTAs are resident (cooperative launch), so every wait
+    // is on work some running CTA reaches first.
+    __device__ __forceinline__ void run() {
         const int G = gridDim.x, c = blockIdx.x;
         for (int r = c; r < P.R; r += G) {
             if (P.route_only) route_only_item();
@@ -353,7 +360,8 @@ struct Producer {
         if (P.G_sh > 0) {
             const int b = range_lo(P.G_sh, c, G), e = range_lo(P.G_sh, c + 1, G);
             const SlotInfo si = slot_info(P, 0, 0);
-            for (int l = b; l < e; l++) gateup_item(-1, l % P.G_sh_rb, l / P.G_sh_rb, si);
+            for (int l = b; l < e; l++)
+                gateup_item(-1, l % P.G_sh_rb, l / P.G_sh_rb, si, l == e - 1 ? e - b : 0);
         }
         int ready = 1;
         if (lane == 0) ready = wait_at_least(&P.ctrl->routing_ready, 1, P.ctrl) ? 1 : 0;
@@ -362,14 +370,14 @@ struct Producer {
         if (ready) {
             const DecTable *tb = P.tab;
             const int U = __ldcg(&tb->U);
-            // routed gate/up share
             const int gu_tot = __ldcg(&tb->gu_off[U]);
-            int b = range_lo(gu_tot, c, G), e = range_lo(gu_tot, c + 1, G);
+            const int b = range_lo(gu_tot, c, G), e = range_lo(gu_tot, c + 1, G);
             if (b < e) {
                 int slot = upper_slot(tb->gu_off, U, b);
                 int lo = __ldcg(&tb->gu_off[slot]), hi = __ldcg(&tb->gu_off[slot + 1]);
                 SlotInfo si = slot_info(P, slot, U);
                 bool ok = slot_ok(si);
+                int run_start = b;
                 for (int l = b; l < e; l++) {
                     while (l >= hi) {
                         slot++;
@@ -377,33 +385,22 @@ struct Producer {
                         hi = __ldcg(&tb->gu_off[slot + 1]);
                         si = slot_info(P, slot, U);
                         ok = slot_ok(si);
+                        run_start = l;
                     }
                     if (!ok) continue;
                     const int ll = l - lo;
-                    gateup_item(slot, ll % P.gu_rb, ll / P.gu_rb, si);
+                    const bool run_end = (l == e - 1) || (l + 1 >= hi);
+                    gateup_item(slot, ll % P.gu_rb, ll / P.gu_rb, si, run_end ? l + 1 - run_start : 0);
                 }
             }
-            // down share (routed slots, then the shared expert as slot U)
+            // this CTA's rows of every expert's down projection (routed slots, then shared)
+            const int r_lo = range_lo(P.H, c, G), r_hi = range_lo(P.H, c + 1, G);
             const int nslots = U + (P.Is > 0 ? 1 : 0);
-            const int dn_tot = __ldcg(&tb->dn_off[nslots]);
-            b = range_lo(dn_tot, c, G);
-            e = range_lo(dn_tot, c + 1, G);
-            if (b < e) {
-                int slot = upper_slot(tb->dn_off, nslots, b);
-                int lo = __ldcg(&tb->dn_off[slot]), hi = __ldcg(&tb->dn_off[slot + 1]);
-                SlotInfo si = slot_info(P, slot, U);
-                bool ok = slot_ok(si);
-                for (int l = b; l < e; l++) {
-                    while (l >= hi) {
-                        slot++;
-                        lo = hi;
-                        hi = __ldcg(&tb->dn_off[slot + 1]);
-                        si = slot_info(P, slot, U);
-                        ok = slot_ok(si);
-                    }
-                    if (!ok) continue;
-                    const int ll = l - lo;
-                    down_item(slot, ll % P.dn_rb, ll / P.dn_rb, si);
+            if (r_lo < r_hi) {
+                for (int slot = 0; slot < nslots; slot++) {
+                    const SlotInfo si = slot_info(P, slot, U);
+                    if (!slot_ok(si)) continue;
+                    for (int tg = 0; tg < si.groups; tg++) down_rows(slot, tg, r_lo, r_hi, si);
                 }
             }
         }
@@ -570,7 +567,8 @@ __device__ void route_final(const DecParams &P, int *scr) {
         else if (per <= 16) select_token<16>(P, t, lane, P.nks);
         else select_token<32>(P, t, lane, P.nks);
     }
-    __threadfence();
+    consumer_bar();  // the buckets below read idx/keff through L2 (ld.cg) in the same CTA
+    if (tid == 0) __threadfence();
     consumer_bar();
     // buckets: counts, offsets, active list, stable perm / pos
     const int E = P.E, N = P.T * P.K;
@@ -641,9 +639,9 @@ __device__ void route_final(const DecParams &P, int *scr) {
     // item table: slots 0..U-1 routed (ascending expert id), slot U shared
     DecTable *tb = P.tab;
     const bool sh = P.Is > 0;
-    int *gu = wc, *dn = wc + (E + 2);  // reuse: per-slot item counts, scanned
+    int *gu = wc;  // reuse: per-slot gate/up item counts, scanned
     for (int u = tid; u < U + 1; u += kCT) {
-        int g = 0, d = 0;
+        int g = 0;
         if (u < U) {
             const int e = __ldcg(P.act + u);
             const int n = cnt[e];
@@ -652,33 +650,21 @@ __device__ void route_final(const DecParams &P, int *scr) {
             tb->slot_n[u] = n;
             tb->slot_pbase[u] = off[e];
             tb->slot_groups[u] = g;
-            gu[u] = P.gu_rb * g;
-            d = P.dn_rb * g;
-        } else {
-            gu[u] = 0;
-            d = sh ? P.dn_rb * P.groups_sh : 0;
         }
-        dn[u] = d;
+        gu[u] = u < U ? P.gu_rb * g : 0;
     }
     consumer_bar();
     const int gu_tot = scan_smem(gu, U + 1, tmp);
-    const int dn_tot = scan_smem(dn, U + 1, tmp);
-    for (int u = tid; u < U + 1; u += kCT) {
-        tb->gu_off[u] = gu[u];
-        tb->dn_off[u] = dn[u];
-    }
+    for (int u = tid; u < U + 1; u += kCT) tb->gu_off[u] = gu[u];
     if (tid == 0) {
         tb->gu_off[U + 1] = gu_tot;
-        tb->dn_off[U + 1] = dn_tot;
         tb->U = U;
-        tb->gu_base = P.R + P.G_sh;
-        tb->dn_base = P.R + P.G_sh + gu_tot;
-        tb->n_total = P.R + P.G_sh + gu_tot + dn_tot;
-        tb->dn_expected = dn_tot / P.dn_rb;  // every slot's token groups, shared included
     }
-    __threadfence();
     consumer_bar();
-    if (tid == 0) atomicExch(&P.ctrl->routing_ready, 1);
+    if (tid == 0) {
+        __threadfence();
+        atomicExch(&P.ctrl->routing_ready, 1);
+    }
 }
 
 // ------------------------------------------------------------------ consumers
@@ -688,17 +674,17 @@ struct Consumer {
     uint64_t *full, *empty;
     StageDesc *desc;
     float *xs;     // activation staging / routing scratch
+    float *ybuf;   // this CTA's rows of y: [T*K + T][rows_cta]
     int *sflag;    // shared flag word
     int tid, lane, warp;
     int seq = 0;
     int key0 = -1, key1 = -1, key2 = -1;  // what XS currently holds (kind, slot/bucket, group)
-    int dn_expected = -1;
     float2 acc[2][4];
     float racc[4][8];
 
     // activations of token group tg of the item's expert, staged pre-scaled and permuted for
     // its format (x for gate/up, h for down); skipped when XS already holds them
-    __device__ void stage_acts(const ItemSlot &it, int tg, bool down) {
+    __device__ __forceinline__ void stage_acts(const ItemSlot &it, int tg, bool down) {
         const int k0 = down ? 2 : 1;
         const int k1 = down ? it.key : (P.T == 1 ? 0 : (it.shared ? -1 : it.pbase));
         const int k2 = (P.T == 1 && !down) ? it.fmt : tg * 8 + it.fmt;
@@ -739,7 +725,7 @@ struct Consumer {
     }
 
     // ---------------- router stage: 4 experts per warp, up to 8 tokens, one float4 per lane
-    __device__ void router_stage(const StageDesc &d, const uint8_t *buf) {
+    __device__ __forceinline__ void router_stage(const StageDesc &d, const uint8_t *buf) {
         if (d.sidx == 0) {
 #pragma unroll
             for (int r = 0; r < 4; r++)
@@ -773,7 +759,7 @@ struct Consumer {
         }
     }
 
-    __device__ void router_finish(const StageDesc &d) {
+    __device__ __forceinline__ void router_finish(const StageDesc &d) {
         // d.slot = expert block, d.rb = k-slice
 #pragma unroll
         for (int r = 0; r < 4; r++)
@@ -786,14 +772,17 @@ struct Consumer {
                 const int e = d.row0 + warp * 4 + r;
                 if (lane == 0 && warp * 4 + r < d.nrows) P.part[((size_t)d.rb * P.T + t) * P.E + e] = s;
             }
-        __threadfence();
         consumer_bar();
-        if (tid == 0) *sflag = atomicAdd(&P.ctrl->router_done, 1) == P.R - 1;
+        if (tid == 0) {
+            __threadfence();
+            const bool lastone = atomicAdd(&P.ctrl->router_done, 1) == P.R - 1;
+            if (lastone) __threadfence();
+            *sflag = lastone;
+        }
         consumer_bar();
         const bool last = *sflag;
         consumer_bar();
         if (last) {
-            __threadfence();
             route_final(P, reinterpret_cast<int *>(xs));
             key0 = -1;
         }
@@ -801,7 +790,7 @@ struct Consumer {
 
     // ---------------- gate/up stages: warp w owns row pair w (gate row, up row)
     template <int FMT, int NV>
-    __device__ void gateup_stage_t(const StageDesc &d, const uint8_t *buf) {
+    __device__ __forceinline__ void gateup_stage_t(const StageDesc &d, const uint8_t *buf) {
         if (warp >= d.nrows) return;
         const uint8_t *rows[2] = {buf + warp * kGuKc, buf + (kGuPairs + warp) * kGuKc};
         float2 a[2][NV];
@@ -818,7 +807,7 @@ struct Consumer {
     }
 
     template <int NV>
-    __device__ void gateup_finish_t(const StageDesc &d) {
+    __device__ __forceinline__ void gateup_finish_t(const StageDesc &d) {
         float2 a[2][NV];
 #pragma unroll
         for (int r = 0; r < 2; r++)
@@ -843,9 +832,9 @@ struct Consumer {
         }
     }
 
-    // ---------------- down stages: each warp owns whole rows of the stage
+    // ---------------- down stages: each warp owns whole rows of the stage; y goes to ybuf
     template <int FMT, int NV>
-    __device__ void down_stage_t(const StageDesc &d, const uint8_t *buf) {
+    __device__ __forceinline__ void down_stage_t(const StageDesc &d, const uint8_t *buf) {
         const ItemSlot &it = d.it;
         const int rbytes = d.kbytes;
         const int CPR = it.inter / QGeom<FMT>::EPC;
@@ -864,31 +853,34 @@ struct Consumer {
                 if (lane == v && v < nv) {
                     const int pv = d.tg * P.NV + v;
                     const int row = it.shared ? P.T * P.K + pv : it.pbase + pv;
-                    P.y[(size_t)row * P.H + dd] = sum[0][v] * it.s0[dd];
+                    ybuf[(size_t)row * P.rows_cta + (dd - d.k0)] = sum[0][v] * it.s0[dd];
                 }
             }
         }
     }
 
-    __device__ void combine_block(int rb) {
-        const int d0 = rb * kDnRows, d1 = min(P.H, d0 + kDnRows);
-        const int nd = d1 - d0;
+    // out rows of this CTA's slice: selection order, then the shared expert
+    __device__ __forceinline__ void combine_rows() {
+        const int G = gridDim.x, c = blockIdx.x;
+        const int r_lo = range_lo(P.H, c, G), r_hi = range_lo(P.H, c + 1, G);
+        const int nd = r_hi - r_lo;
+        consumer_bar();
         for (int i = tid; i < P.T * nd; i += kCT) {
-            const int t = i / nd, dd = d0 + i % nd;
+            const int t = i / nd, rr = i % nd;
             const int ke = __ldcg(P.keff + t);
             float a = 0.f;
             for (int k = 0; k < ke; k++) {
                 const float wk = __ldcg(P.w + (size_t)t * P.K + k);
                 const int p = __ldcg(P.pos + (size_t)t * P.K + k);
-                a = __fadd_rn(a, __fmul_rn(wk, __ldcg(P.y + (size_t)p * P.H + dd)));
+                a = __fadd_rn(a, __fmul_rn(wk, ybuf[(size_t)p * P.rows_cta + rr]));
             }
-            if (P.Is > 0) a = __fadd_rn(a, __ldcg(P.y + ((size_t)P.T * P.K + t) * P.H + dd));
-            P.out[(size_t)t * P.H + dd] = a;
+            if (P.Is > 0) a = __fadd_rn(a, ybuf[((size_t)P.T * P.K + t) * P.rows_cta + rr]);
+            P.out[(size_t)t * P.H + r_lo + rr] = a;
         }
     }
 
     template <int NV>
-    __device__ void process_nv(const StageDesc &d, const uint8_t *buf) {
+    __device__ __forceinline__ void process_nv(const StageDesc &d, const uint8_t *buf) {
         const int fmt = d.it.fmt;
         if (d.kind == kGateUp) {
             if (d.sidx == 0) {
@@ -907,7 +899,8 @@ struct Consumer {
         }
     }
 
-    __device__ void run() {
+    __device__ __forceinline__ void run() {
+        bool did_down = false;
         for (;;) {
             const int s = seq % P.nst, use = seq / P.nst;
             if (!mbar_wait(&full[s], use & 1, P.ctrl)) break;  // flagged; the producer drains
@@ -934,10 +927,15 @@ struct Consumer {
                 if (d.kind == kGateUp) {
                     stage_acts(d.it, d.tg, false);
                 } else {
+                    did_down = true;
                     // this expert's h rows must be complete before they are staged
-                    if (tid == 0) wait_at_least(&P.ctrl->gu_done[d.it.key], d.it.need, P.ctrl);
-                    consumer_bar();
-                    __threadfence();
+                    if (key0 != 2 || key1 != d.it.key || key2 != d.tg * 8 + d.it.fmt) {
+                        if (tid == 0) {
+                            wait_at_least(&P.ctrl->gu_done[d.it.key], d.it.need, P.ctrl);
+                            __threadfence();
+                        }
+                        consumer_bar();
+                    }
                     stage_acts(d.it, d.tg, true);
                 }
             }
@@ -947,31 +945,20 @@ struct Consumer {
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[s]);
             seq++;
-            if (d.sidx != d.nst - 1) continue;
-            // item complete
-            if (d.kind == kGateUp) {
+            if (d.kind == kGateUp && d.sidx == d.nst - 1) {
                 if (P.NV == 1) gateup_finish_t<1>(d);
                 else if (P.NV == 2) gateup_finish_t<2>(d);
                 else gateup_finish_t<4>(d);
-                __threadfence();
-                consumer_bar();
-                if (tid == 0) atomicAdd(&P.ctrl->gu_done[d.it.key], 1);
-            } else {
-                __threadfence();
-                consumer_bar();
-                if (tid == 0) {
-                    if (dn_expected < 0) dn_expected = __ldcg(&P.tab->dn_expected);
-                    *sflag = atomicAdd(&P.ctrl->dn_cnt[d.rb], 1) == dn_expected - 1;
-                }
-                consumer_bar();
-                const bool last = *sflag;
-                consumer_bar();
-                if (last) {
-                    __threadfence();
-                    combine_block(d.rb);
+                if (d.sig > 0) {  // this CTA's run of items of the expert is done: publish it
+                    consumer_bar();
+                    if (tid == 0) {
+                        __threadfence();
+                        atomicAdd(&P.ctrl->gu_done[d.it.key], d.sig);
+                    }
                 }
             }
         }
+        if (did_down) combine_rows();
     }
 };
 
@@ -979,7 +966,8 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(const DecPar
     extern __shared__ __align__(128) uint8_t smem[];
     uint8_t *ring = smem;
     float *xs = reinterpret_cast<float *>(smem + (size_t)P.nst * kSB);
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem + (size_t)P.nst * kSB + P.xs_bytes);
+    float *ybuf = reinterpret_cast<float *>(smem + (size_t)P.nst * kSB + P.xs_bytes);
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + (size_t)P.nst * kSB + P.xs_bytes + P.ybuf_bytes);
     uint64_t *empty = full + P.nst;
     StageDesc *desc = reinterpret_cast<StageDesc *>(empty + P.nst);
     int *sflag = reinterpret_cast<int *>(desc + P.nst);
@@ -996,7 +984,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(const DecPar
         Producer pr{P, ring, full, empty, desc, lane};
         pr.run();
     } else {
-        Consumer co{P, ring, full, empty, desc, xs, sflag, tid, lane, warp};
+        Consumer co{P, ring, full, empty, desc, xs, ybuf, sflag, tid, lane, warp};
         co.run();
     }
 }
@@ -1007,14 +995,15 @@ size_t decode_ctrl_bytes() { return sizeof(DecCtrl); }
 size_t decode_table_bytes() { return sizeof(DecTable); }
 
 size_t decode_smem_bytes(const DecParams &P) {
-    return (size_t)P.nst * kSB + P.xs_bytes + 2 * P.nst * sizeof(uint64_t) + P.nst * sizeof(StageDesc) + 16;
+    return (size_t)P.nst * kSB + P.xs_bytes + P.ybuf_bytes + 2 * P.nst * sizeof(uint64_t) +
+           P.nst * sizeof(StageDesc) + 16;
 }
 
 // Host-side geometry of the decode launch (static item counts, staging sizes).
 void decode_plan(const coli_moe_desc &d, DecParams &P) {
     const int T = d.T;
-    P.NV = T == 1 ? 1 : (T <= 2 ? 2 : 4);
-    P.nst = T == 1 ? 5 : 6;
+    P.NV = T == 1 ? 1 : (T <= 2 || T > 32 ? 2 : 4);
+    P.nst = 2;  // set by decode_plan_grid
     const int maxdim = std::max(d.H, std::max(d.I, d.I_shared));
     P.xs_stride = maxdim;
     const size_t xs_vec = (size_t)P.NV * maxdim * sizeof(float);
@@ -1035,7 +1024,19 @@ void decode_plan(const coli_moe_desc &d, DecParams &P) {
     P.G_sh_rb = d.I_shared > 0 ? (d.I_shared + kGuPairs - 1) / kGuPairs : 0;
     P.G_sh = P.G_sh_rb * P.groups_sh;
     P.gu_rb = (d.I + kGuPairs - 1) / kGuPairs;
-    P.dn_rb = (d.H + kDnRows - 1) / kDnRows;
+}
+
+// the grid is one CTA per SM; each owns ceil(H / grid) rows of the down projection
+// and as many 16 KB ring stages (2..6) as fit beside the staging and y buffers
+bool decode_plan_grid(const coli_moe_desc &d, DecParams &P, int grid) {
+    P.rows_cta = (d.H + grid - 1) / grid;
+    const size_t rows = (size_t)d.T * d.K + (d.I_shared > 0 ? d.T : 0);
+    P.ybuf_bytes = (int)align_up(rows * P.rows_cta * sizeof(float), 128);
+    const long budget = 227L * 1024 - P.xs_bytes - P.ybuf_bytes - 1024;
+    const long nst = std::min(6L, budget / kSB);
+    if (nst < 2) return false;
+    P.nst = (int)nst;
+    return decode_smem_bytes(P) <= 227u * 1024;
 }
 
 bool decode_supported(const coli_moe_desc &d) {
@@ -1044,7 +1045,6 @@ bool decode_supported(const coli_moe_desc &d) {
     const int64_t dn_r = row_bytes(d.routed_fmt, d.I);
     const int64_t dn_s = d.I_shared > 0 ? row_bytes(d.shared_fmt, d.I_shared) : 0;
     if (dn_r > kSB || dn_s > kSB) return false;
-    if (d.H / kDnRows + 1 > kDecMaxRowBlocks) return false;
     return true;
 }
 

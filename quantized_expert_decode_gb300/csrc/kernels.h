@@ -25,7 +25,6 @@ struct ExpertWork {
 
 // ---------------------------------------------------------------- decode.cu
 constexpr int kDecMaxT = 64;              // the persistent decode kernel serves T <= 64
-constexpr int kDecMaxRowBlocks = 1024;    // H / 64 row blocks of the down projection
 
 // Counters of one decode call (zeroed before each launch; err stays the first word, which is
 // also the workspace error word read by coli_moe_check).
@@ -33,18 +32,16 @@ struct DecCtrl {
     int err, queue, router_done, routing_ready;
     int pad[12];
     int gu_done[kMaxE + 1];            // finished gate/up items per slot (shared: index kMaxE)
-    int dn_cnt[kDecMaxRowBlocks];      // finished down items per 64-row block
 };
 
 // Item table published by the routing CTA.
 struct DecTable {
-    int U, n_total, gu_base, dn_base, dn_expected, pad[3];
+    int U, pad[7];
     int slot_e[kMaxE + 1];
     int slot_n[kMaxE + 1];
     int slot_pbase[kMaxE + 1];
     int slot_groups[kMaxE + 1];
     int gu_off[kMaxE + 2];
-    int dn_off[kMaxE + 2];
 };
 
 struct DecParams {
@@ -65,10 +62,12 @@ struct DecParams {
     int R, route_only;         // router items; route_only: one item that only selects
     int neb, nks, rks_floats;  // router expert blocks, k-slices, floats per k-slice
     int G_sh_rb, groups_sh, G_sh;
-    int gu_rb, dn_rb;
+    int gu_rb;
+    int rows_cta, ybuf_bytes;  // down rows per CTA, bytes of the CTA's y buffer
 };
 
 void decode_plan(const coli_moe_desc &d, DecParams &P);
+bool decode_plan_grid(const coli_moe_desc &d, DecParams &P, int grid);
 bool decode_supported(const coli_moe_desc &d);
 size_t decode_smem_bytes(const DecParams &P);
 int decode_ctas_per_sm(const DecParams &P);

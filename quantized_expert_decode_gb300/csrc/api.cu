@@ -129,10 +129,9 @@ int num_sms() {
 int run_forward_decode(const coli_moe_desc *d, const float *x, const float *W_r, const float *bias,
                        const coli_moe_expert *experts, const coli_moe_expert *shared, float *out,
                        int32_t *idx_out, float *w_out, void *ws, cudaStream_t st,
-                       void *const *events) {
+                       void *const *events, const DecParams &plan, int grid) {
     const WsLayout L = ws_layout(*d);
-    DecParams P{};
-    decode_plan(*d, P);
+    DecParams P = plan;
     P.x = x;
     P.Wr = W_r;
     P.bias = bias;
@@ -170,12 +169,9 @@ int run_forward_decode(const coli_moe_desc *d, const float *x, const float *W_r,
     const int splits = std::min(L.router_splits, 16);
     if (P.route_only) P.nks = splits;
     if ((size_t)P.nks * d->T * d->E * sizeof(float) > L.sig - L.part) return COLI_MOE_ENOTSUP;
-    const size_t ctrl_bytes = sizeof(DecCtrl);
-    const int grid = num_sms();
-    if (!decode_plan_grid(*d, P, grid) || decode_ctas_per_sm(P) < 1) return COLI_MOE_ENOTSUP;
     int rc;
     if ((rc = record(events, 0, st))) return rc;
-    cudaError_t e = cudaMemsetAsync(P.ctrl, 0, ctrl_bytes, st);
+    cudaError_t e = cudaMemsetAsync(P.ctrl, 0, sizeof(DecCtrl), st);
     if (e != cudaSuccess) return cuda_fail(e);
     if (P.route_only &&
         (e = launch_router_partial(x, W_r, P.part, d->T, d->H, d->E, splits, st)) != cudaSuccess)
@@ -187,15 +183,31 @@ int run_forward_decode(const coli_moe_desc *d, const float *x, const float *W_r,
     return record(events, 4, st);
 }
 
+// the persistent decode kernel's plan and grid for this description (false: not applicable)
+bool decode_plan_for(const coli_moe_desc &d, DecParams &P, int &grid) {
+    if (!decode_supported(d)) return false;
+    const int sms = num_sms();
+    grid = 2 * sms;
+    if (!decode_plan(d, P, grid)) return false;
+    const int occ = decode_ctas_per_sm(P);
+    if (occ < 1) return false;
+    if (occ < 2) {
+        grid = sms;
+        if (!decode_plan(d, P, grid)) return false;
+    }
+    return true;
+}
+
 int run_forward(const coli_moe_desc *d, const float *x, const float *W_r, const float *bias,
                 const coli_moe_expert *experts, const coli_moe_expert *shared, float *out,
                 int32_t *idx_out, float *w_out, void *ws, cudaStream_t st,
                 void *const *events = nullptr) {
-    if (decode_supported(*d)) {
-        DecParams probe{};
-        decode_plan(*d, probe);
-        if (decode_plan_grid(*d, probe, num_sms()))
-            return run_forward_decode(d, x, W_r, bias, experts, shared, out, idx_out, w_out, ws, st, events);
+    {
+        DecParams plan{};
+        int grid = 0;
+        if (decode_plan_for(*d, plan, grid))
+            return run_forward_decode(d, x, W_r, bias, experts, shared, out, idx_out, w_out, ws, st, events,
+                                      plan, grid);
     }
     const WsLayout L = ws_layout(*d);
     if (int rc0 = record(events, 0, st)) return rc0;

@@ -1,30 +1,27 @@
 // decode.cu — the whole MoE block for decode-sized batches (T <= 64) in ONE persistent launch.
 //
-// Work is a list of items, each CTA taking a static share (see Producer::run):
-//   router items       logits of 32 experts over one slice of H, for T <= 8 tokens
-//                      (colibri-strix c/glm.c @98759bf moe() phase A; r_router shader)
-//   shared gate/up     8 rows of the shared expert's gate and up (phase E)
-//   routed gate/up     8 rows of one selected expert's gate and up, for up to NV tokens
-//                      (phases C/D: g = gate.x, u = up.x, h = silu(g)*u; moe_gemv + moe_silu)
-//   down               each CTA owns a slice of the H output rows: for every selected expert
-//                      and the shared one it computes its rows of y = down.h into shared
-//                      memory, then combines them in selection order plus the shared expert
-//                      and writes out (phases C/D/E) — no atomics, no global y
-// The item ids of routed work are only known after routing: the CTA that finishes the last
-// router item (an atomic ticket) runs the top-K selection (r_top8_par's lane-blocked warp
-// argmax, ties to the lower index, TOPK/TOPP, renorm, routed scale), the token->expert
-// buckets and the item table, then publishes a flag.
-//
-// Each CTA has 8 consumer warps and 1 producer warp. The producer claims items and streams
-// their weights into a ring of 16 KB shared-memory stages with bulk asynchronous copies
-// (cp.async.bulk, completion counted on an mbarrier per stage); consumers dequantise from
-// shared memory (qdot.cuh) against activations staged, pre-scaled and permuted, in shared
-// memory. Dependencies (routing -> routed work, an expert's gate/up -> its down) are counters
-// in the workspace, raised once per CTA per expert. Every
-// CTA finishes all of its earlier-phase items before it waits on a later phase, and the launch
-// is cooperative (all CTAs resident), so progress is guaranteed; every wait is still bounded
-// (2 s of %globaltimer), after which the kernel records kErrWaitExpired and goes on without
-// blocking the GPU.
+// Phases, each split statically and contiguously over the CTAs (two per SM, cooperative
+// launch, so every CTA is resident and a wait is only ever on an earlier phase):
+//   A  routing (colibri-strix c/glm.c @98759bf moe() phase A; r_router / r_top8_par shaders):
+//      T <= 8: router items — logits of 32 experts over one slice of H — write partial logits;
+//      the last item of each 32-expert block (atomic ticket) sums that block's partials in a
+//      fixed order; the last block runs the selection. T > 8: the partial logits come from a
+//      router launch before this kernel; every CTA sums a share, the last one selects.
+//      Selection (one CTA, everything in shared memory): sigmoid, bias, greedy top-K with ties
+//      to the lower index, TOPK/TOPP, renorm, routed scale, token->expert buckets (stable) and
+//      the unit table of the expert phases; then a flag is published.
+//   B  shared expert gate/up rows (known before routing: overlaps phase A)
+//   C  routed gate/up rows: h = silu(gate.x * s_g) * (up.x * s_u)   (moe() phases C/D)
+//   D  down rows: y = (down.h) * s_d, for every selected expert and the shared one
+//   E  combine: out = sum_k w_k y_k in selection order + y_shared   (moe() phases C/D/E)
+// Units of B/C are one row pair (gate row j, up row j) of one expert for one group of up to
+// NV tokens; units of D are one down row. A CTA walks its share in segments that have the same
+// expert and tokens: the segment's activations are staged once in shared memory (pre-scaled and
+// permuted, see qdot.cuh), then each warp streams its units' rows with 16-byte loads kept
+// several chunks ahead in registers, across unit boundaries.
+// Dependencies are counters in the workspace, raised once per CTA per expert (gate/up -> down)
+// or per CTA (down -> combine). Every wait is bounded (2 s of %globaltimer); on expiry the kernel
+// records kErrWaitExpired and carries on, so a fault in the schedule can not hang the GPU.
 #include <algorithm>
 
 #include "kernels.h"
@@ -35,52 +32,21 @@ namespace colimoe {
 
 namespace {
 
-constexpr int kCW = 8;                          // consumer warps
-constexpr int kCT = kCW * kWarp;                // consumer threads
-constexpr int kDecThreads = kCT + kWarp;        // + one producer warp
-constexpr int kSB = 16384;                      // bytes per ring stage
-constexpr int kGuPairs = 8;                     // gate/up row pairs per item (one per consumer warp)
-constexpr int kGuKc = kSB / (2 * kGuPairs);     // 1024 bytes of each row per stage
-constexpr int kRtE = 32;                        // experts per router item (4 per consumer warp)
-constexpr int kRtKc = kSB / kRtE;               // 512 bytes (128 floats) of each W_r row per stage
-constexpr int kRtStages = 4;                    // stages per router item
+constexpr int kNT = 256;                 // threads per CTA
+constexpr int kNW = kNT / kWarp;         // warps per CTA
+constexpr int kRtE = 32;                 // experts per router item (4 per warp)
+constexpr int kDepth = 4;                // 16-byte chunks kept in flight per lane and row
 constexpr unsigned long long kWaitNs = 2000000000ull;
-constexpr int kSharedSlotKey = kMaxE;           // gu_done index of the shared expert
-
-enum Kind : int { kEnd = 0, kRouter = 1, kGateUp = 2, kDown = 3, kRouteOnly = 4 };
-
-// What the consumers need about the expert of an item (filled in by the producer, so that
-// consumers make no global lookups per item).
-struct ItemSlot {
-    const float *s0, *s1;  // gate/up: gate and up row scales; down: down row scales
-    int fmt, inter;        // weight format, intermediate size of this expert
-    int n, pbase;          // tokens using it, first bucket position (routed)
-    int key;               // gu_done index: routed slot, or kSharedSlotKey
-    int need;              // gate/up items of this expert that its down work waits for
-    int shared;
-};
-
-struct StageDesc {
-    int kind;
-    int sidx, nst;   // stage index in the item, stages in the item
-    int slot;        // routed slot (0..U-1) or U = shared; router: expert block
-    int rb;          // row block (gate/up: 8 pairs, down: 64 rows); router: k-slice
-    int tg;          // token group
-    int row0, nrows; // rows carried by this stage (gate/up: pairs; down: rows; router: experts)
-    int k0, kbytes;  // byte range of each row carried (gate/up, router); down: whole rows
-    int sig;         // gate/up: >0 on the last stage of this CTA's run of items of one expert
-                     // (the number of items in the run, added to that expert's counter)
-    ItemSlot it;
-};
+constexpr int kSharedKey = kMaxE;        // gu_done index of the shared expert
 
 __device__ __forceinline__ void flag_error(DecCtrl *c, int code) { atomicCAS(&c->err, 0, code); }
 
-// bounded wait until *p >= target; returns false (and flags) on timeout
+// bounded wait until *p >= target; false (and flagged) on timeout
 __device__ bool wait_at_least(const int *p, int target, DecCtrl *c) {
     if (ld_volatile(p) >= target) return true;
     const uint64_t t0 = globaltimer_ns();
     while (ld_volatile(p) < target) {
-        __nanosleep(128);
+        __nanosleep(64);
         if (globaltimer_ns() - t0 > kWaitNs) {
             flag_error(c, kErrWaitExpired);
             return false;
@@ -89,21 +55,9 @@ __device__ bool wait_at_least(const int *p, int target, DecCtrl *c) {
     return true;
 }
 
-__device__ bool mbar_wait(uint64_t *bar, uint32_t parity, DecCtrl *c) {
-    if (mbar_try_wait(bar, parity)) return true;
-    const uint64_t t0 = globaltimer_ns();
-    while (!mbar_try_wait(bar, parity)) {
-        if (globaltimer_ns() - t0 > kWaitNs) {
-            flag_error(c, kErrWaitExpired);
-            return false;
-        }
-    }
-    return true;
-}
+__device__ __forceinline__ int range_lo(int n, int c, int G) { return (int)((long long)n * c / G); }
 
-__device__ __forceinline__ void consumer_bar() { named_bar(1, kCT); }
-
-// first index i in [0, n) with off[i+1] > x (off is a prefix array of length n+1)
+// first index i in [0, n) with off[i+1] > x (off: nondecreasing prefix array, off[0] = 0)
 __device__ int upper_slot(const int *off, int n, int x) {
     int lo = 0, hi = n - 1;
     while (lo < hi) {
@@ -114,313 +68,177 @@ __device__ int upper_slot(const int *off, int n, int x) {
     return lo;
 }
 
-struct SlotInfo {
-    const uint8_t *gw, *uw, *dw;
-    const float *gs, *us, *ds;
-    int fmt, inter, n, pbase, groups, key;
-    bool shared;
+__device__ __forceinline__ bool bad16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) != 0; }
+
+// ------------------------------------------------------------------ the streaming core
+// One warp streams `nunits` units of NR packed rows each (CPR 16-byte chunks per row), lane l
+// taking chunks l, l+32, ... of every row, with kDepth chunk-steps of loads in flight across unit
+// boundaries. rows_of(i, rows) gives unit i's row pointers; epi(i, sums) gets the finished
+// warp-reduced dot products with the NV staged vectors.
+template <int FMT, int NR, int NV, class RowsOf, class Epi>
+__device__ __forceinline__ void warp_stream(int nunits, int CPR, const float *xs, int xstride, int lane,
+                                            RowsOf rows_of, Epi epi) {
+    using G = QGeom<FMT>;
+    if (nunits <= 0) return;
+    const int S = (CPR + kWarp - 1) / kWarp;  // steps per unit
+    const int total = nunits * S;
+    uint4 buf[kDepth][NR];
+    int iu = 0, ik = 0;  // issue cursor: unit, step within unit
+    auto issue = [&](uint4 (&b)[NR]) {
+        if (iu < nunits) {
+            const int c = lane + kWarp * ik;
+            const uint8_t *rr[NR];
+            rows_of(iu, rr);
+#pragma unroll
+            for (int r = 0; r < NR; r++) b[r] = c < CPR ? ld_stream_16(rr[r] + 16 * c) : make_uint4(0, 0, 0, 0);
+            if (++ik == S) {
+                ik = 0;
+                iu++;
+            }
+        }
+    };
+#pragma unroll
+    for (int j = 0; j < kDepth; j++) issue(buf[j]);
+    float2 acc[NR][NV];
+#pragma unroll
+    for (int r = 0; r < NR; r++)
+#pragma unroll
+        for (int v = 0; v < NV; v++) acc[r][v] = make_float2(0.f, 0.f);
+    const float4 *xs4 = reinterpret_cast<const float4 *>(xs);
+    const int xstride4 = xstride / 4;
+    int cu = 0, ck = 0;  // compute cursor
+    for (int s0 = 0; s0 < total; s0 += kDepth) {
+#pragma unroll
+        for (int j = 0; j < kDepth; j++) {
+            if (s0 + j < total) {
+                const int c = lane + kWarp * ck;
+                if (c < CPR) {
+#pragma unroll
+                    for (int wi = 0; wi < 4; wi++) {
+                        float4 xv[NV][G::F4W];
+#pragma unroll
+                        for (int v = 0; v < NV; v++)
+#pragma unroll
+                            for (int q = 0; q < G::F4W; q++)
+                                xv[v][q] = xs4[v * xstride4 + (wi * G::F4W + q) * CPR + c];
+#pragma unroll
+                        for (int r = 0; r < NR; r++) {
+                            const uint32_t w = word_of(buf[j][r], wi);
+                            const uint32_t wh = w >> 16;
+#pragma unroll
+                            for (int m = 0; m < G::HALF; m++) {
+                                const uint32_t lo = lop3_and_xor(w, G::mask(m), G::xorv(m));
+                                const uint32_t hi = lop3_and_xor(wh, G::mask(m), G::xorv(m));
+                                const float2 d = __fadd2_rn(make_float2(__uint_as_float(lo), __uint_as_float(hi)),
+                                                            make_float2(-G::magic(m), -G::magic(m)));
+#pragma unroll
+                                for (int v = 0; v < NV; v++) {
+                                    const float4 &x4 = xv[v][m >> 1];
+                                    const float2 x2 = (m & 1) ? make_float2(x4.z, x4.w) : make_float2(x4.x, x4.y);
+                                    acc[r][v] = __ffma2_rn(d, x2, acc[r][v]);
+                                }
+                            }
+                        }
+                    }
+                }
+                issue(buf[j]);
+                if (++ck == S) {
+                    float sums[NR][NV];
+                    warp_reduce_acc<NR, NV>(acc, sums);
+                    epi(cu, sums);
+#pragma unroll
+                    for (int r = 0; r < NR; r++)
+#pragma unroll
+                        for (int v = 0; v < NV; v++) acc[r][v] = make_float2(0.f, 0.f);
+                    ck = 0;
+                    cu++;
+                }
+            }
+        }
+    }
+}
+
+// ------------------------------------------------------------------ routing
+struct Scratch {  // shared-memory layout of the selection step (inside the staging buffer)
+    int *cnt, *off, *fill, *chk, *actv, *wc, *tmp, *idx, *keff, *gu, *dn;
+    float *w;
 };
 
-__device__ SlotInfo slot_info(const DecParams &P, int slot, int U) {
-    SlotInfo s;
-    if (P.Is > 0 && slot == U) {
-        s.gw = static_cast<const uint8_t *>(P.shared.gate_w);
-        s.uw = static_cast<const uint8_t *>(P.shared.up_w);
-        s.dw = static_cast<const uint8_t *>(P.shared.down_w);
-        s.gs = P.shared.gate_s;
-        s.us = P.shared.up_s;
-        s.ds = P.shared.down_s;
-        s.fmt = P.sfmt;
-        s.inter = P.Is;
-        s.n = P.T;
-        s.pbase = 0;
-        s.groups = P.groups_sh;
-        s.key = kSharedSlotKey;
-        s.shared = true;
-        return s;
-    }
-    const DecTable *tb = P.tab;
-    const int e = __ldcg(&tb->slot_e[slot]);
-    const coli_moe_expert ex = P.experts[e];
-    s.gw = static_cast<const uint8_t *>(ex.gate_w);
-    s.uw = static_cast<const uint8_t *>(ex.up_w);
-    s.dw = static_cast<const uint8_t *>(ex.down_w);
-    s.gs = ex.gate_s;
-    s.us = ex.up_s;
-    s.ds = ex.down_s;
-    s.fmt = P.rfmt;
-    s.inter = P.I;
-    s.n = __ldcg(&tb->slot_n[slot]);
-    s.pbase = __ldcg(&tb->slot_pbase[slot]);
-    s.groups = __ldcg(&tb->slot_groups[slot]);
-    s.key = slot;
-    s.shared = false;
+__device__ __forceinline__ Scratch scratch_of(void *base, int E, int T, int K) {
+    Scratch s;
+    int *p = static_cast<int *>(base);
+    s.cnt = p;
+    s.off = s.cnt + E;
+    s.fill = s.off + E;
+    s.chk = s.fill + E;
+    s.actv = s.chk + E;
+    s.wc = s.actv + E;
+    s.tmp = s.wc + kNW * E;
+    s.idx = s.tmp + 16;
+    s.keff = s.idx + T * K;
+    s.gu = s.keff + T;
+    s.dn = s.gu + (E + 2);
+    s.w = reinterpret_cast<float *>(s.dn + (E + 2));
     return s;
 }
 
-__device__ __forceinline__ bool bad_ptr16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) != 0; }
-
-// ------------------------------------------------------------------ producer
-__device__ __forceinline__ int range_lo(int n, int c, int G) { return (int)((long long)n * c / G); }
-
-struct Producer {
-    const DecParams &P;
-    uint8_t *ring;
-    uint64_t *full, *empty;
-    StageDesc *desc;
-    int lane;
-    int seq = 0;
-
-    __device__ __forceinline__ uint8_t *stage_buf(int s) { return ring + (size_t)s * kSB; }
-
-    // wait for ring stage `seq` to be free, return its index
-    __device__ __forceinline__ int acquire() {
-        const int s = seq % P.nst, use = seq / P.nst;
-        if (use > 0) {
-            if (lane == 0) mbar_wait(&empty[s], (use - 1) & 1, P.ctrl);
-            __syncwarp();
-        }
-        return s;
+// exclusive scan in place of n <= 2048 ints in shared memory by the CTA; returns the total
+__device__ int scan_smem(int *a, int n, int *tmp) {
+    const int tid = threadIdx.x, lane = tid % kWarp, warp = tid / kWarp;
+    int loc[8], sum = 0;
+#pragma unroll
+    for (int i = 0; i < 8; i++) {
+        const int j = tid * 8 + i;
+        loc[i] = j < n ? a[j] : 0;
+        sum += loc[i];
     }
-
-    __device__ __forceinline__ void publish_end() {
-        const int s = acquire();
-        if (lane == 0) {
-            desc[s].kind = kEnd;
-            mbar_arrive(&full[s]);
-        }
-        __syncwarp();
-        seq++;
+    int inc = sum;
+#pragma unroll
+    for (int o = 1; o < kWarp; o <<= 1) {
+        const int v = __shfl_up_sync(kFull, inc, o);
+        if (lane >= o) inc += v;
     }
-
-    // before the producer leaves, every copy it issued has landed (each stage's last use has
-    // completed its phase), so no bulk copy is in flight when the CTA exits
-    __device__ __forceinline__ void drain() {
-        if (lane == 0) {
-            for (int s = 0; s < P.nst && s < seq; s++) {
-                const int last = s + ((seq - 1 - s) / P.nst) * P.nst;
-                mbar_wait(&full[s], (last / P.nst) & 1, P.ctrl);
-            }
+    if (lane == kWarp - 1) tmp[warp] = inc;
+    __syncthreads();
+    if (tid == 0) {
+        int run = 0;
+        for (int w = 0; w < kNW; w++) {
+            const int v = tmp[w];
+            tmp[w] = run;
+            run += v;
         }
-        __syncwarp();
+        tmp[kNW] = run;
     }
-
-    __device__ __forceinline__ ItemSlot item_slot(const SlotInfo &si, bool down) const {
-        ItemSlot it;
-        it.s0 = down ? si.ds : si.gs;
-        it.s1 = si.us;
-        it.fmt = si.fmt;
-        it.inter = si.inter;
-        it.n = si.n;
-        it.pbase = si.pbase;
-        it.key = si.key;
-        it.need = si.shared ? P.G_sh : P.gu_rb * si.groups;
-        it.shared = si.shared ? 1 : 0;
-        return it;
+    __syncthreads();
+    int run = tmp[warp] + inc - sum;
+#pragma unroll
+    for (int i = 0; i < 8; i++) {
+        const int j = tid * 8 + i;
+        if (j < n) a[j] = run;
+        run += loc[i];
     }
+    const int total = tmp[kNW];
+    __syncthreads();
+    return total;
+}
 
-    // T > 8: the logits come from an earlier launch; one item only runs the selection
-    __device__ __forceinline__ void route_only_item() {
-        const int s = acquire();
-        if (lane == 0) {
-            desc[s].kind = kRouteOnly;
-            desc[s].sidx = 0;
-            desc[s].nst = 1;
-            mbar_arrive(&full[s]);
-        }
-        __syncwarp();
-        seq++;
-    }
-
-    __device__ __forceinline__ void router_item(int item) {
-        const int eb = item % P.neb, ks = item / P.neb;
-        const int e0 = eb * kRtE;
-        const int kbeg = ks * P.rks_floats;
-        const int kend = min(P.H, kbeg + P.rks_floats);
-        const int nst = (kend - kbeg + kRtKc / 4 - 1) / (kRtKc / 4);
-        const int ne = min(kRtE, P.E - e0);
-        for (int st = 0; st < nst; st++) {
-            const int s = acquire();
-            const int kf = kbeg + st * (kRtKc / 4);
-            const int nf = min(kRtKc / 4, kend - kf);
-            if (lane == 0) {
-                StageDesc &d = desc[s];
-                d.kind = kRouter;
-                d.sidx = st;
-                d.nst = nst;
-                d.slot = eb;
-                d.rb = ks;
-                d.tg = 0;
-                d.row0 = e0;
-                d.nrows = ne;
-                d.k0 = kf * 4;
-                d.kbytes = nf * 4;
-                d.sig = 0;
-                mbar_arrive_expect_tx(&full[s], (uint32_t)(ne * nf * 4));
-            }
-            __syncwarp();
-            if (lane < ne)
-                bulk_g2s(stage_buf(s) + lane * kRtKc, P.Wr + (size_t)(e0 + lane) * P.H + kf, nf * 4, &full[s]);
-            seq++;
-        }
-    }
-
-    // 8 row pairs (gate row j, up row j) of one expert for token group tg; `sig` is set on the
-    // item's last stage when it closes this CTA's run of items of that expert
-    __device__ __forceinline__ void gateup_item(int slot, int rb, int tg, const SlotInfo &si, int sig) {
-        const int64_t rbytes = row_bytes(si.fmt, P.H);
-        const int j0 = rb * kGuPairs;
-        const int np = min(kGuPairs, si.inter - j0);
-        const int nst = (int)((rbytes + kGuKc - 1) / kGuKc);
-        const ItemSlot it = item_slot(si, false);
-        for (int st = 0; st < nst; st++) {
-            const int s = acquire();
-            const int k0 = st * kGuKc;
-            const int kb = (int)((rbytes - k0) < kGuKc ? (rbytes - k0) : kGuKc);
-            if (lane == 0) {
-                StageDesc &d = desc[s];
-                d.kind = kGateUp;
-                d.sidx = st;
-                d.nst = nst;
-                d.slot = slot;
-                d.rb = rb;
-                d.tg = tg;
-                d.row0 = j0;
-                d.nrows = np;
-                d.k0 = k0;
-                d.kbytes = kb;
-                d.sig = st == nst - 1 ? sig : 0;
-                d.it = it;
-                mbar_arrive_expect_tx(&full[s], (uint32_t)(2 * np * kb));
-            }
-            __syncwarp();
-            if (lane < 2 * kGuPairs) {
-                const int p = lane % kGuPairs, m = lane / kGuPairs;
-                if (p < np) {
-                    const uint8_t *src = (m ? si.uw : si.gw) + (size_t)(j0 + p) * rbytes + k0;
-                    bulk_g2s(stage_buf(s) + (m * kGuPairs + p) * kGuKc, src, kb, &full[s]);
-                }
-            }
-            seq++;
-        }
-    }
-
-    // rows [r_lo, r_hi) of one expert's down projection for token group tg, whole rows per stage
-    __device__ __forceinline__ void down_rows(int slot, int tg, int r_lo, int r_hi, const SlotInfo &si) {
-        const int64_t rbytes = row_bytes(si.fmt, si.inter);
-        const int64_t rfit = kSB / rbytes;
-        const int rps = rfit < 1 ? 1 : (rfit > 16 ? 16 : (int)rfit);
-        const int nst = (r_hi - r_lo + rps - 1) / rps;
-        const ItemSlot it = item_slot(si, true);
-        for (int st = 0; st < nst; st++) {
-            const int s = acquire();
-            const int r0 = r_lo + st * rps;
-            const int nr = min(rps, r_hi - r0);
-            if (lane == 0) {
-                StageDesc &d = desc[s];
-                d.kind = kDown;
-                d.sidx = st;
-                d.nst = nst;
-                d.slot = slot;
-                d.rb = 0;
-                d.tg = tg;
-                d.row0 = r0;
-                d.nrows = nr;
-                d.k0 = r_lo;
-                d.kbytes = (int)rbytes;
-                d.sig = 0;
-                d.it = it;
-                mbar_arrive_expect_tx(&full[s], (uint32_t)(nr * rbytes));
-                bulk_g2s(stage_buf(s), si.dw + (size_t)r0 * rbytes, (uint32_t)(nr * rbytes), &full[s]);
-            }
-            __syncwarp();
-            seq++;
-        }
-    }
-
-    __device__ __forceinline__ bool slot_ok(const SlotInfo &si) {
-        if (bad_ptr16(si.gw) || bad_ptr16(si.uw) || bad_ptr16(si.dw)) {
-            if (lane == 0) flag_error(P.ctrl, kErrBadExpert);
-            return false;
-        }
-        return true;
-    }
-
-    // Static schedule. CTA c takes router items c, c+G, ...; its contiguous share of the shared
-    // expert's gate/up items; after routing, its contiguous share of the routed gate/up items;
-    // then its slice of the H down-projection rows for every expert. Each phase finishes in a CTA
-    // before it waits on the next, and all CTAs are resident (cooperative launch), so every wait
-    // is on work some running CTA reaches first.
-    __device__ __forceinline__ void run() {
-        const int G = gridDim.x, c = blockIdx.x;
-        for (int r = c; r < P.R; r += G) {
-            if (P.route_only) route_only_item();
-            else router_item(r);
-        }
-        if (P.G_sh > 0) {
-            const int b = range_lo(P.G_sh, c, G), e = range_lo(P.G_sh, c + 1, G);
-            const SlotInfo si = slot_info(P, 0, 0);
-            for (int l = b; l < e; l++)
-                gateup_item(-1, l % P.G_sh_rb, l / P.G_sh_rb, si, l == e - 1 ? e - b : 0);
-        }
-        int ready = 1;
-        if (lane == 0) ready = wait_at_least(&P.ctrl->routing_ready, 1, P.ctrl) ? 1 : 0;
-        ready = __shfl_sync(kFull, ready, 0);
-        __threadfence();
-        if (ready) {
-            const DecTable *tb = P.tab;
-            const int U = __ldcg(&tb->U);
-            const int gu_tot = __ldcg(&tb->gu_off[U]);
-            const int b = range_lo(gu_tot, c, G), e = range_lo(gu_tot, c + 1, G);
-            if (b < e) {
-                int slot = upper_slot(tb->gu_off, U, b);
-                int lo = __ldcg(&tb->gu_off[slot]), hi = __ldcg(&tb->gu_off[slot + 1]);
-                SlotInfo si = slot_info(P, slot, U);
-                bool ok = slot_ok(si);
-                int run_start = b;
-                for (int l = b; l < e; l++) {
-                    while (l >= hi) {
-                        slot++;
-                        lo = hi;
-                        hi = __ldcg(&tb->gu_off[slot + 1]);
-                        si = slot_info(P, slot, U);
-                        ok = slot_ok(si);
-                        run_start = l;
-                    }
-                    if (!ok) continue;
-                    const int ll = l - lo;
-                    const bool run_end = (l == e - 1) || (l + 1 >= hi);
-                    gateup_item(slot, ll % P.gu_rb, ll / P.gu_rb, si, run_end ? l + 1 - run_start : 0);
-                }
-            }
-            // this CTA's rows of every expert's down projection (routed slots, then shared)
-            const int r_lo = range_lo(P.H, c, G), r_hi = range_lo(P.H, c + 1, G);
-            const int nslots = U + (P.Is > 0 ? 1 : 0);
-            if (r_lo < r_hi) {
-                for (int slot = 0; slot < nslots; slot++) {
-                    const SlotInfo si = slot_info(P, slot, U);
-                    if (!slot_ok(si)) continue;
-                    for (int tg = 0; tg < si.groups; tg++) down_rows(slot, tg, r_lo, r_hi, si);
-                }
-            }
-        }
-        publish_end();
-        drain();
-    }
-};
-
-// ------------------------------------------------------------------ routing (one CTA)
+// one warp: selection of token t from its logits (sigmoid, bias, greedy top-K, TOPP, renorm,
+// scale). Lane l owns experts [l*PER, l*PER + PER), so the lane-local strict '>' ascending scan
+// plus a cross-lane argmax preferring the lower index reproduce the serial first-max-wins order.
 template <int PER>
-__device__ void select_token(const DecParams &P, int t, int lane, int nks) {
+__device__ void select_token(const DecParams &P, int t, int lane, const Scratch &sc) {
     const int base = lane * PER;
     float ch[PER], sg[PER];
 #pragma unroll
     for (int j = 0; j < PER; j++) {
         const int e = base + j;
+        ch[j] = e < P.E ? __ldcg(P.sig + (size_t)t * P.E + e) : 0.f;  // logits, all loads in flight
+    }
+#pragma unroll
+    for (int j = 0; j < PER; j++) {
+        const int e = base + j;
         if (e < P.E) {
-            float lg = 0.f;
-            for (int s = 0; s < nks; s++) lg += __ldcg(P.part + ((size_t)s * P.T + t) * P.E + e);
-            const float sv = 1.f / (1.f + expf(-lg));
+            const float sv = 1.f / (1.f + expf(-ch[j]));
             const float cv = sv + P.bias[e];
             P.sig[(size_t)t * P.E + e] = sv;
             P.choice[(size_t)t * P.E + e] = cv;
@@ -462,13 +280,12 @@ __device__ void select_token(const DecParams &P, int t, int lane, int nks) {
             break;
         }
         if (bi >= base && bi < base + PER) taken |= 1u << (bi - base);
-        if (lane == k) {  // lane k keeps selection k
+        if (lane == k) {
             my_i = bi;
             my_w = bs;
         }
         nsel = k + 1;
     }
-    // tail on lane 0 with the pages' float operations and order (TOPP, renorm, scale)
     float ww[kMaxK];
     int id[kMaxK];
     for (int k = 0; k < nsel; k++) {
@@ -509,483 +326,508 @@ __device__ void select_token(const DecParams &P, int t, int lane, int nks) {
     }
     for (int k = 0; k < P.K; k++) {
         const bool kept = k < Ke;
-        P.idx[(size_t)t * P.K + k] = kept ? id[k] : -1;
-        P.w[(size_t)t * P.K + k] = kept ? __fmul_rn(ww[k], P.rscale) : 0.f;
+        const int vi = kept ? id[k] : -1;
+        const float vw = kept ? __fmul_rn(ww[k], P.rscale) : 0.f;
+        P.idx[(size_t)t * P.K + k] = vi;
+        P.w[(size_t)t * P.K + k] = vw;
+        sc.idx[t * P.K + k] = vi;
+        sc.w[t * P.K + k] = vw;
     }
     P.keff[t] = Ke;
+    sc.keff[t] = Ke;
 }
 
-// exclusive scan of n <= 1024 ints held in shared memory, in place, by the 256 consumer threads;
-// returns the total
-__device__ int scan_smem(int *a, int n, int *tmp /* >= 9 ints */) {
+// selection, buckets and the unit table, by one CTA, from the logits in P.sig
+__device__ void route_final(const DecParams &P, void *scratch) {
     const int tid = threadIdx.x, lane = tid % kWarp, warp = tid / kWarp;
-    int loc[8], sum = 0;  // n <= 2048
-#pragma unroll
-    for (int i = 0; i < 8; i++) {
-        const int j = tid * 8 + i;
-        loc[i] = j < n ? a[j] : 0;
-        sum += loc[i];
-    }
-    int inc = sum;
-#pragma unroll
-    for (int o = 1; o < kWarp; o <<= 1) {
-        const int v = __shfl_up_sync(kFull, inc, o);
-        if (lane >= o) inc += v;
-    }
-    if (lane == kWarp - 1) tmp[warp] = inc;
-    consumer_bar();
-    if (tid == 0) {
-        int run = 0;
-        for (int w = 0; w < kCW; w++) {
-            const int v = tmp[w];
-            tmp[w] = run;
-            run += v;
-        }
-        tmp[kCW] = run;
-    }
-    consumer_bar();
-    int run = tmp[warp] + inc - sum;
-#pragma unroll
-    for (int i = 0; i < 8; i++) {
-        const int j = tid * 8 + i;
-        if (j < n) a[j] = run;
-        run += loc[i];
-    }
-    const int total = tmp[kCW];
-    consumer_bar();
-    return total;
-}
-
-__device__ void route_final(const DecParams &P, int *scr) {
-    const int tid = threadIdx.x, lane = tid % kWarp, warp = tid / kWarp;
+    const Scratch sc = scratch_of(scratch, P.E, P.T, P.K);
     const int per = (P.E + kWarp - 1) / kWarp;
-    for (int t = warp; t < P.T; t += kCW) {
-        if (per <= 1) select_token<1>(P, t, lane, P.nks);
-        else if (per <= 2) select_token<2>(P, t, lane, P.nks);
-        else if (per <= 4) select_token<4>(P, t, lane, P.nks);
-        else if (per <= 8) select_token<8>(P, t, lane, P.nks);
-        else if (per <= 16) select_token<16>(P, t, lane, P.nks);
-        else select_token<32>(P, t, lane, P.nks);
+    for (int t = warp; t < P.T; t += kNW) {
+        if (per <= 1) select_token<1>(P, t, lane, sc);
+        else if (per <= 2) select_token<2>(P, t, lane, sc);
+        else if (per <= 4) select_token<4>(P, t, lane, sc);
+        else if (per <= 8) select_token<8>(P, t, lane, sc);
+        else if (per <= 16) select_token<16>(P, t, lane, sc);
+        else select_token<32>(P, t, lane, sc);
     }
-    consumer_bar();  // the buckets below read idx/keff through L2 (ld.cg) in the same CTA
-    if (tid == 0) __threadfence();
-    consumer_bar();
-    // buckets: counts, offsets, active list, stable perm / pos
     const int E = P.E, N = P.T * P.K;
-    int *cnt = scr, *off = cnt + E, *fill = off + E, *chk = fill + E, *actv = chk + E;
-    int *wc = actv + E, *tmp = wc + kCW * E;
-    for (int e = tid; e < E; e += kCT) {
-        cnt[e] = 0;
-        fill[e] = 0;
+    for (int e = tid; e < E; e += kNT) {
+        sc.cnt[e] = 0;
+        sc.fill[e] = 0;
     }
-    consumer_bar();
+    __syncthreads();
     auto expert_of = [&](int a) -> int {
         if (a >= N) return -1;
-        const int t = a / P.K, k = a % P.K;
-        if (k >= __ldcg(P.keff + t)) return -1;
-        return __ldcg(P.idx + a);
+        return (a % P.K) < sc.keff[a / P.K] ? sc.idx[a] : -1;
     };
-    for (int a = tid; a < N; a += kCT) {
+    for (int a = tid; a < N; a += kNT) {
         const int e = expert_of(a);
-        if (e >= 0) atomicAdd(&cnt[e], 1);
+        if (e >= 0) atomicAdd(&sc.cnt[e], 1);
     }
-    consumer_bar();
-    for (int e = tid; e < E; e += kCT) {
-        off[e] = cnt[e];
-        actv[e] = cnt[e] > 0 ? 1 : 0;
-        P.counts[e] = cnt[e];
+    __syncthreads();
+    for (int e = tid; e < E; e += kNT) {
+        sc.off[e] = sc.cnt[e];
+        sc.actv[e] = sc.cnt[e] > 0 ? 1 : 0;
+        P.counts[e] = sc.cnt[e];
     }
-    consumer_bar();
-    const int total = scan_smem(off, E, tmp);
-    const int U = scan_smem(actv, E, tmp);
-    for (int e = tid; e < E; e += kCT) {
-        P.offsets[e] = off[e];
-        if (cnt[e] > 0) P.act[actv[e]] = e;
+    __syncthreads();
+    const int total = scan_smem(sc.off, E, sc.tmp);
+    const int U = scan_smem(sc.actv, E, sc.tmp);
+    for (int e = tid; e < E; e += kNT) {
+        P.offsets[e] = sc.off[e];
+        if (sc.cnt[e] > 0) {
+            P.act[sc.actv[e]] = e;
+            sc.chk[sc.actv[e]] = e;  // active experts, ascending (chk is free until the chunk loop)
+        }
     }
     if (tid == 0) P.offsets[E] = total;
-    consumer_bar();
-    for (int a0 = 0; a0 < N; a0 += kCT) {
-        for (int i = tid; i < kCW * E; i += kCT) wc[i] = 0;
-        consumer_bar();
+    __syncthreads();
+    // unit table: slot u < U is the u-th active expert; slot U the shared expert
+    for (int u = tid; u < U + 1; u += kNT) {
+        int g = 0;
+        if (u < U) {
+            const int e = sc.chk[u];
+            g = (sc.cnt[e] + P.NV - 1) / P.NV;
+            P.tab->slot_e[u] = e;
+            P.tab->slot_n[u] = sc.cnt[e];
+            P.tab->slot_pbase[u] = sc.off[e];
+            P.tab->slot_groups[u] = g;
+            sc.gu[u] = g * P.I;
+            sc.dn[u] = g * P.H;
+        } else {
+            sc.gu[u] = 0;
+            sc.dn[u] = P.Is > 0 ? P.groups_sh * P.H : 0;
+        }
+    }
+    __syncthreads();
+    const int gu_tot = scan_smem(sc.gu, U + 1, sc.tmp);
+    const int dn_tot = scan_smem(sc.dn, U + 1, sc.tmp);
+    for (int u = tid; u < U + 1; u += kNT) {
+        P.tab->gu_off[u] = sc.gu[u];
+        P.tab->dn_off[u] = sc.dn[u];
+    }
+    if (tid == 0) {
+        P.tab->gu_off[U + 1] = gu_tot;
+        P.tab->dn_off[U + 1] = dn_tot;
+        P.tab->U = U;
+        P.tab->gu_tot = gu_tot;
+        P.tab->dn_tot = dn_tot;
+    }
+    // stable perm / pos: 256-assignment chunks in order; inside a chunk, rank within the warp
+    // from a match-any mask, then the warps' per-expert counts are scanned
+    for (int a0 = 0; a0 < N; a0 += kNT) {
+        for (int i = tid; i < kNW * E; i += kNT) sc.wc[i] = 0;
+        __syncthreads();
         const int a = a0 + tid;
         const int e = expert_of(a);
         const unsigned peers = __match_any_sync(kFull, e);
         const int rank = __popc(peers & ((1u << lane) - 1u));
-        if (e >= 0 && rank == 0) wc[warp * E + e] = __popc(peers);
-        consumer_bar();
-        for (int x = tid; x < E; x += kCT) {
+        if (e >= 0 && rank == 0) sc.wc[warp * E + e] = __popc(peers);
+        __syncthreads();
+        for (int x = tid; x < E; x += kNT) {
             int run = 0;
-            for (int w = 0; w < kCW; w++) {
-                const int v = wc[w * E + x];
-                wc[w * E + x] = run;
+            for (int w = 0; w < kNW; w++) {
+                const int v = sc.wc[w * E + x];
+                sc.wc[w * E + x] = run;
                 run += v;
             }
-            chk[x] = run;
+            sc.chk[x] = run;
         }
-        consumer_bar();
+        __syncthreads();
         if (a < N) {
             if (e >= 0) {
-                const int p = off[e] + fill[e] + wc[warp * E + e] + rank;
+                const int p = sc.off[e] + sc.fill[e] + sc.wc[warp * E + e] + rank;
                 P.perm[p] = a;
                 P.pos[a] = p;
             } else {
                 P.pos[a] = -1;
             }
         }
-        consumer_bar();
-        for (int x = tid; x < E; x += kCT) fill[x] += chk[x];
-        consumer_bar();
+        __syncthreads();
+        for (int x = tid; x < E; x += kNT) sc.fill[x] += sc.chk[x];
+        __syncthreads();
     }
-    // item table: slots 0..U-1 routed (ascending expert id), slot U shared
-    DecTable *tb = P.tab;
-    const bool sh = P.Is > 0;
-    int *gu = wc;  // reuse: per-slot gate/up item counts, scanned
-    for (int u = tid; u < U + 1; u += kCT) {
-        int g = 0;
-        if (u < U) {
-            const int e = __ldcg(P.act + u);
-            const int n = cnt[e];
-            g = (n + P.NV - 1) / P.NV;
-            tb->slot_e[u] = e;
-            tb->slot_n[u] = n;
-            tb->slot_pbase[u] = off[e];
-            tb->slot_groups[u] = g;
-        }
-        gu[u] = u < U ? P.gu_rb * g : 0;
-    }
-    consumer_bar();
-    const int gu_tot = scan_smem(gu, U + 1, tmp);
-    for (int u = tid; u < U + 1; u += kCT) tb->gu_off[u] = gu[u];
-    if (tid == 0) {
-        tb->gu_off[U + 1] = gu_tot;
-        tb->U = U;
-    }
-    consumer_bar();
     if (tid == 0) {
         __threadfence();
         atomicExch(&P.ctrl->routing_ready, 1);
     }
 }
 
-// ------------------------------------------------------------------ consumers
-struct Consumer {
-    const DecParams &P;
-    uint8_t *ring;
-    uint64_t *full, *empty;
-    StageDesc *desc;
-    float *xs;     // activation staging / routing scratch
-    float *ybuf;   // this CTA's rows of y: [T*K + T][rows_cta]
-    int *sflag;    // shared flag word
-    int tid, lane, warp;
-    int seq = 0;
-    int key0 = -1, key1 = -1, key2 = -1;  // what XS currently holds (kind, slot/bucket, group)
-    float2 acc[2][4];
-    float racc[4][8];
-
-    // activations of token group tg of the item's expert, staged pre-scaled and permuted for
-    // its format (x for gate/up, h for down); skipped when XS already holds them
-    __device__ __forceinline__ void stage_acts(const ItemSlot &it, int tg, bool down) {
-        const int k0 = down ? 2 : 1;
-        const int k1 = down ? it.key : (P.T == 1 ? 0 : (it.shared ? -1 : it.pbase));
-        const int k2 = (P.T == 1 && !down) ? it.fmt : tg * 8 + it.fmt;
-        if (key0 == k0 && key1 == k1 && key2 == k2) return;
-        const int nv = min(P.NV, it.n - tg * P.NV);
-        const int len = down ? it.inter : P.H;
-        const int gran = it.fmt == COLI_FMT_INT4 ? 32 : it.fmt == COLI_FMT_INT8 ? 16 : 64;
-        const int CPR = len / gran;
-        consumer_bar();
-        for (int v = 0; v < P.NV; v++) {
-            float *dst = xs + (size_t)v * P.xs_stride;
-            if (v < nv) {
-                const int pv = tg * P.NV + v;
-                const float *src;
-                if (down) {
-                    const int row = it.shared ? P.T * P.K + pv : it.pbase + pv;
-                    src = P.h + (size_t)row * P.ldh;
-                } else {
-                    const int t = it.shared ? pv : __ldcg(P.perm + it.pbase + pv) / P.K;
-                    src = P.x + (size_t)t * P.H;
-                }
-                for (int i = tid; i < len; i += kCT) {
-                    float sc;
-                    int at;
-                    if (it.fmt == COLI_FMT_INT4) at = staged_index<COLI_FMT_INT4>(i, CPR, sc);
-                    else if (it.fmt == COLI_FMT_INT8) at = staged_index<COLI_FMT_INT8>(i, CPR, sc);
-                    else at = staged_index<COLI_FMT_INT2>(i, CPR, sc);
-                    dst[at] = (down ? __ldcg(src + i) : __ldg(src + i)) * sc;
-                }
-            } else {
-                for (int i = tid; i < len; i += kCT) dst[i] = 0.f;
-            }
-        }
-        key0 = k0;
-        key1 = k1;
-        key2 = k2;
-        consumer_bar();
-    }
-
-    // ---------------- router stage: 4 experts per warp, up to 8 tokens, one float4 per lane
-    __device__ __forceinline__ void router_stage(const StageDesc &d, const uint8_t *buf) {
-        if (d.sidx == 0) {
+// T <= 8: partial logits of 32 experts (4 per warp) over one slice of H
+__device__ void router_item(const DecParams &P, int item) {
+    const int warp = threadIdx.x / kWarp, lane = threadIdx.x % kWarp;
+    const int eb = item % P.neb, ks = item / P.neb;
+    const int kb = ks * P.rks_floats, ke = min(P.H, kb + P.rks_floats);
+    float acc[4][8];
 #pragma unroll
-            for (int r = 0; r < 4; r++)
+    for (int r = 0; r < 4; r++)
 #pragma unroll
-                for (int t = 0; t < 8; t++) racc[r][t] = 0.f;
+        for (int t = 0; t < 8; t++) acc[r][t] = 0.f;
+    int e[4];
+#pragma unroll
+    for (int r = 0; r < 4; r++) e[r] = min(eb * kRtE + warp * 4 + r, P.E - 1);
+    for (int k = kb + 4 * lane; k < ke; k += 4 * kWarp) {
+        float4 wv[4];
+#pragma unroll
+        for (int r = 0; r < 4; r++) {
+            const uint4 u = ld_stream_16(P.Wr + (size_t)e[r] * P.H + k);
+            wv[r] = make_float4(__uint_as_float(u.x), __uint_as_float(u.y), __uint_as_float(u.z), __uint_as_float(u.w));
         }
-        const int nf4 = d.kbytes / 16;
-        const int kf = d.k0 / 4 + lane * 4;
-        if (lane < nf4) {
-            float4 wv[4];
+#pragma unroll
+        for (int t = 0; t < 8; t++) {
+            if (t >= P.T) break;
+            const float4 xv = __ldg(reinterpret_cast<const float4 *>(P.x + (size_t)t * P.H + k));
 #pragma unroll
             for (int r = 0; r < 4; r++) {
-                const int er = warp * 4 + r;
-                wv[r] = er < d.nrows ? *reinterpret_cast<const float4 *>(buf + er * kRtKc + lane * 16)
-                                     : make_float4(0.f, 0.f, 0.f, 0.f);
-            }
-#pragma unroll
-            for (int t = 0; t < 8; t++) {
-                if (t >= P.T) break;
-                const float4 xv = __ldg(reinterpret_cast<const float4 *>(P.x + (size_t)t * P.H + kf));
-#pragma unroll
-                for (int r = 0; r < 4; r++) {
-                    float a = racc[r][t];
-                    a = fmaf(wv[r].x, xv.x, a);
-                    a = fmaf(wv[r].y, xv.y, a);
-                    a = fmaf(wv[r].z, xv.z, a);
-                    a = fmaf(wv[r].w, xv.w, a);
-                    racc[r][t] = a;
-                }
+                float a = acc[r][t];
+                a = fmaf(wv[r].x, xv.x, a);
+                a = fmaf(wv[r].y, xv.y, a);
+                a = fmaf(wv[r].z, xv.z, a);
+                a = fmaf(wv[r].w, xv.w, a);
+                acc[r][t] = a;
             }
         }
     }
+#pragma unroll
+    for (int r = 0; r < 4; r++)
+#pragma unroll
+        for (int t = 0; t < 8; t++) {
+            if (t >= P.T) break;
+            float s = acc[r][t];
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(kFull, s, o);
+            const int er = eb * kRtE + warp * 4 + r;
+            if (lane == 0 && er < P.E) P.part[((size_t)ks * P.T + t) * P.E + er] = s;
+        }
+}
 
-    __device__ __forceinline__ void router_finish(const StageDesc &d) {
-        // d.slot = expert block, d.rb = k-slice
-#pragma unroll
-        for (int r = 0; r < 4; r++)
-#pragma unroll
-            for (int t = 0; t < 8; t++) {
-                if (t >= P.T) break;
-                float s = racc[r][t];
-#pragma unroll
-                for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(kFull, s, o);
-                const int e = d.row0 + warp * 4 + r;
-                if (lane == 0 && warp * 4 + r < d.nrows) P.part[((size_t)d.rb * P.T + t) * P.E + e] = s;
-            }
-        consumer_bar();
-        if (tid == 0) {
-            __threadfence();
-            const bool lastone = atomicAdd(&P.ctrl->router_done, 1) == P.R - 1;
-            if (lastone) __threadfence();
-            *sflag = lastone;
+// logits = fixed-order sums of the partials, for flat logit indices [lo, hi) (t-major)
+__device__ void reduce_logits(const DecParams &P, int lo, int hi) {
+    for (int i = lo + (int)threadIdx.x; i < hi; i += kNT) {
+        float s = 0.f;
+        int k = 0;
+        for (; k + 4 <= P.nks; k += 4) {
+            const float a0 = __ldcg(P.part + (size_t)(k + 0) * P.T * P.E + i);
+            const float a1 = __ldcg(P.part + (size_t)(k + 1) * P.T * P.E + i);
+            const float a2 = __ldcg(P.part + (size_t)(k + 2) * P.T * P.E + i);
+            const float a3 = __ldcg(P.part + (size_t)(k + 3) * P.T * P.E + i);
+            s += a0;
+            s += a1;
+            s += a2;
+            s += a3;
         }
-        consumer_bar();
-        const bool last = *sflag;
-        consumer_bar();
-        if (last) {
-            route_final(P, reinterpret_cast<int *>(xs));
-            key0 = -1;
-        }
+        for (; k < P.nks; k++) s += __ldcg(P.part + (size_t)k * P.T * P.E + i);
+        P.sig[i] = s;
     }
+}
 
-    // ---------------- gate/up stages: warp w owns row pair w (gate row, up row)
-    template <int FMT, int NV>
-    __device__ __forceinline__ void gateup_stage_t(const StageDesc &d, const uint8_t *buf) {
-        if (warp >= d.nrows) return;
-        const uint8_t *rows[2] = {buf + warp * kGuKc, buf + (kGuPairs + warp) * kGuKc};
-        float2 a[2][NV];
-#pragma unroll
-        for (int r = 0; r < 2; r++)
-#pragma unroll
-            for (int v = 0; v < NV; v++) a[r][v] = acc[r][v];
-        qdot_smem_acc<FMT, 2, NV>(rows, d.k0 / 16, d.kbytes / 16, xs, P.xs_stride, P.H / QGeom<FMT>::EPC,
-                                  lane, a);
-#pragma unroll
-        for (int r = 0; r < 2; r++)
-#pragma unroll
-            for (int v = 0; v < NV; v++) acc[r][v] = a[r][v];
-    }
-
-    template <int NV>
-    __device__ __forceinline__ void gateup_finish_t(const StageDesc &d) {
-        float2 a[2][NV];
-#pragma unroll
-        for (int r = 0; r < 2; r++)
-#pragma unroll
-            for (int v = 0; v < NV; v++) a[r][v] = acc[r][v];
-        float sum[2][NV];
-        warp_reduce_acc<2, NV>(a, sum);
-        const ItemSlot &it = d.it;
-        const int j = d.row0 + warp;
-        const int nv = min(P.NV, it.n - d.tg * P.NV);
-        if (warp < d.nrows) {
-#pragma unroll
-            for (int v = 0; v < NV; v++) {
-                if (lane == v && v < nv) {
-                    const float g = sum[0][v] * it.s0[j];
-                    const float u = sum[1][v] * it.s1[j];
-                    const int pv = d.tg * P.NV + v;
-                    const int row = it.shared ? P.T * P.K + pv : it.pbase + pv;
-                    P.h[(size_t)row * P.ldh + j] = g / (1.f + expf(-g)) * u;
-                }
-            }
-        }
-    }
-
-    // ---------------- down stages: each warp owns whole rows of the stage; y goes to ybuf
-    template <int FMT, int NV>
-    __device__ __forceinline__ void down_stage_t(const StageDesc &d, const uint8_t *buf) {
-        const ItemSlot &it = d.it;
-        const int rbytes = d.kbytes;
-        const int CPR = it.inter / QGeom<FMT>::EPC;
-        const int nv = min(P.NV, it.n - d.tg * P.NV);
-        for (int r = warp; r < d.nrows; r += kCW) {
-            const uint8_t *rows[1] = {buf + r * rbytes};
-            float2 a[1][NV];
-#pragma unroll
-            for (int v = 0; v < NV; v++) a[0][v] = make_float2(0.f, 0.f);
-            qdot_smem_acc<FMT, 1, NV>(rows, 0, CPR, xs, P.xs_stride, CPR, lane, a);
-            float sum[1][NV];
-            warp_reduce_acc<1, NV>(a, sum);
-            const int dd = d.row0 + r;
-#pragma unroll
-            for (int v = 0; v < NV; v++) {
-                if (lane == v && v < nv) {
-                    const int pv = d.tg * P.NV + v;
-                    const int row = it.shared ? P.T * P.K + pv : it.pbase + pv;
-                    ybuf[(size_t)row * P.rows_cta + (dd - d.k0)] = sum[0][v] * it.s0[dd];
-                }
-            }
-        }
-    }
-
-    // out rows of this CTA's slice: selection order, then the shared expert
-    __device__ __forceinline__ void combine_rows() {
-        const int G = gridDim.x, c = blockIdx.x;
-        const int r_lo = range_lo(P.H, c, G), r_hi = range_lo(P.H, c + 1, G);
-        const int nd = r_hi - r_lo;
-        consumer_bar();
-        for (int i = tid; i < P.T * nd; i += kCT) {
-            const int t = i / nd, rr = i % nd;
-            const int ke = __ldcg(P.keff + t);
-            float a = 0.f;
-            for (int k = 0; k < ke; k++) {
-                const float wk = __ldcg(P.w + (size_t)t * P.K + k);
-                const int p = __ldcg(P.pos + (size_t)t * P.K + k);
-                a = __fadd_rn(a, __fmul_rn(wk, ybuf[(size_t)p * P.rows_cta + rr]));
-            }
-            if (P.Is > 0) a = __fadd_rn(a, ybuf[((size_t)P.T * P.K + t) * P.rows_cta + rr]);
-            P.out[(size_t)t * P.H + r_lo + rr] = a;
-        }
-    }
-
-    template <int NV>
-    __device__ __forceinline__ void process_nv(const StageDesc &d, const uint8_t *buf) {
-        const int fmt = d.it.fmt;
-        if (d.kind == kGateUp) {
-            if (d.sidx == 0) {
-#pragma unroll
-                for (int r = 0; r < 2; r++)
-#pragma unroll
-                    for (int v = 0; v < 4; v++) acc[r][v] = make_float2(0.f, 0.f);
-            }
-            if (fmt == COLI_FMT_INT4) gateup_stage_t<COLI_FMT_INT4, NV>(d, buf);
-            else if (fmt == COLI_FMT_INT8) gateup_stage_t<COLI_FMT_INT8, NV>(d, buf);
-            else gateup_stage_t<COLI_FMT_INT2, NV>(d, buf);
-        } else {
-            if (fmt == COLI_FMT_INT4) down_stage_t<COLI_FMT_INT4, NV>(d, buf);
-            else if (fmt == COLI_FMT_INT8) down_stage_t<COLI_FMT_INT8, NV>(d, buf);
-            else down_stage_t<COLI_FMT_INT2, NV>(d, buf);
-        }
-    }
-
-    __device__ __forceinline__ void run() {
-        bool did_down = false;
-        for (;;) {
-            const int s = seq % P.nst, use = seq / P.nst;
-            if (!mbar_wait(&full[s], use & 1, P.ctrl)) break;  // flagged; the producer drains
-            const StageDesc d = desc[s];
-            if (d.kind == kEnd) break;
-            const uint8_t *buf = ring + (size_t)s * kSB;
-            if (d.kind == kRouteOnly) {
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&empty[s]);
-                seq++;
-                route_final(P, reinterpret_cast<int *>(xs));
-                key0 = -1;
-                continue;
-            }
-            if (d.kind == kRouter) {
-                router_stage(d, buf);
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&empty[s]);
-                seq++;
-                if (d.sidx == d.nst - 1) router_finish(d);
-                continue;
-            }
-            if (d.sidx == 0) {
-                if (d.kind == kGateUp) {
-                    stage_acts(d.it, d.tg, false);
-                } else {
-                    did_down = true;
-                    // this expert's h rows must be complete before they are staged
-                    if (key0 != 2 || key1 != d.it.key || key2 != d.tg * 8 + d.it.fmt) {
-                        if (tid == 0) {
-                            wait_at_least(&P.ctrl->gu_done[d.it.key], d.it.need, P.ctrl);
-                            __threadfence();
-                        }
-                        consumer_bar();
-                    }
-                    stage_acts(d.it, d.tg, true);
-                }
-            }
-            if (P.NV == 1) process_nv<1>(d, buf);
-            else if (P.NV == 2) process_nv<2>(d, buf);
-            else process_nv<4>(d, buf);
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&empty[s]);
-            seq++;
-            if (d.kind == kGateUp && d.sidx == d.nst - 1) {
-                if (P.NV == 1) gateup_finish_t<1>(d);
-                else if (P.NV == 2) gateup_finish_t<2>(d);
-                else gateup_finish_t<4>(d);
-                if (d.sig > 0) {  // this CTA's run of items of the expert is done: publish it
-                    consumer_bar();
-                    if (tid == 0) {
-                        __threadfence();
-                        atomicAdd(&P.ctrl->gu_done[d.it.key], d.sig);
-                    }
-                }
-            }
-        }
-        if (did_down) combine_rows();
-    }
+// ------------------------------------------------------------------ expert phases
+struct Seg {  // one segment of units with the same expert and tokens (broadcast in smem)
+    const uint8_t *w0, *w1;  // gate/up rows, or down rows in w0
+    const float *s0, *s1;    // their row scales
+    int fmt, inter, n, pbase, shared, tg, key, need;
+    int ulo, uhi;            // units [ulo, uhi) of this CTA in the segment
+    int ubase;               // unit index of the segment's first unit (row 0)
 };
 
-__global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(const DecParams P) {
-    extern __shared__ __align__(128) uint8_t smem[];
-    uint8_t *ring = smem;
-    float *xs = reinterpret_cast<float *>(smem + (size_t)P.nst * kSB);
-    float *ybuf = reinterpret_cast<float *>(smem + (size_t)P.nst * kSB + P.xs_bytes);
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem + (size_t)P.nst * kSB + P.xs_bytes + P.ybuf_bytes);
-    uint64_t *empty = full + P.nst;
-    StageDesc *desc = reinterpret_cast<StageDesc *>(empty + P.nst);
-    int *sflag = reinterpret_cast<int *>(desc + P.nst);
-    const int tid = threadIdx.x, warp = tid / kWarp, lane = tid % kWarp;
-    if (tid == 0) {
-        for (int s = 0; s < P.nst; s++) {
-            mbar_init(&full[s], 1);
-            mbar_init(&empty[s], kCW);
+// stage the activations of token group tg (x rows for gate/up, h rows for down) into xs
+__device__ void stage_acts(const DecParams &P, const Seg &g, bool down, float *xs) {
+    const int nv = min(P.NV, g.n - g.tg * P.NV);
+    const int len = down ? g.inter : P.H;
+    const int gran = g.fmt == COLI_FMT_INT4 ? 32 : g.fmt == COLI_FMT_INT8 ? 16 : 64;
+    const int CPR = len / gran;
+    for (int v = 0; v < P.NV; v++) {
+        float *dst = xs + (size_t)v * P.xs_stride;
+        if (v < nv) {
+            const int pv = g.tg * P.NV + v;
+            const float *src;
+            if (down) {
+                const int row = g.shared ? P.T * P.K + pv : g.pbase + pv;
+                src = P.h + (size_t)row * P.ldh;
+            } else {
+                const int t = g.shared ? pv : __ldcg(P.perm + g.pbase + pv) / P.K;
+                src = P.x + (size_t)t * P.H;
+            }
+            for (int i = threadIdx.x; i < len; i += kNT) {
+                float sc;
+                int at;
+                if (g.fmt == COLI_FMT_INT4) at = staged_index<COLI_FMT_INT4>(i, CPR, sc);
+                else if (g.fmt == COLI_FMT_INT8) at = staged_index<COLI_FMT_INT8>(i, CPR, sc);
+                else at = staged_index<COLI_FMT_INT2>(i, CPR, sc);
+                dst[at] = (down ? __ldcg(src + i) : __ldg(src + i)) * sc;
+            }
+        } else {
+            for (int i = threadIdx.x; i < len; i += kNT) dst[i] = 0.f;
         }
-        fence_mbar_init();
+    }
+}
+
+template <int FMT, int NV>
+__device__ void gateup_units(const DecParams &P, const Seg &g, const float *xs) {
+    const int warp = threadIdx.x / kWarp, lane = threadIdx.x % kWarp;
+    const int nu = g.uhi - g.ulo;
+    const int mine = nu > warp ? (nu - warp + kNW - 1) / kNW : 0;
+    const int64_t rb = row_bytes(FMT, P.H);
+    const int nv = min(P.NV, g.n - g.tg * P.NV);
+    const int jbase = g.ulo - g.ubase;  // row of the segment's first unit of this CTA
+    warp_stream<FMT, 2, NV>(
+        mine, (int)(rb / 16), xs, P.xs_stride, lane,
+        [&](int i, const uint8_t *(&rr)[2]) {
+            const int j = jbase + warp + kNW * i;
+            rr[0] = g.w0 + (size_t)j * rb;
+            rr[1] = g.w1 + (size_t)j * rb;
+        },
+        [&](int i, const float (&s)[2][NV]) {
+            const int j = jbase + warp + kNW * i;
+#pragma unroll
+            for (int v = 0; v < NV; v++) {
+                if (lane == v && v < nv) {
+                    const float gv = s[0][v] * g.s0[j];
+                    const float uv = s[1][v] * g.s1[j];
+                    const int pv = g.tg * P.NV + v;
+                    const int row = g.shared ? P.T * P.K + pv : g.pbase + pv;
+                    P.h[(size_t)row * P.ldh + j] = gv / (1.f + expf(-gv)) * uv;
+                }
+            }
+        });
+}
+
+template <int FMT, int NV>
+__device__ void down_units(const DecParams &P, const Seg &g, const float *xs) {
+    const int warp = threadIdx.x / kWarp, lane = threadIdx.x % kWarp;
+    const int nu = g.uhi - g.ulo;
+    const int mine = nu > warp ? (nu - warp + kNW - 1) / kNW : 0;
+    const int64_t rb = row_bytes(FMT, g.inter);
+    const int nv = min(P.NV, g.n - g.tg * P.NV);
+    const int dbase = g.ulo - g.ubase;
+    warp_stream<FMT, 1, NV>(
+        mine, (int)(rb / 16), xs, P.xs_stride, lane,
+        [&](int i, const uint8_t *(&rr)[1]) { rr[0] = g.w0 + (size_t)(dbase + warp + kNW * i) * rb; },
+        [&](int i, const float (&s)[1][NV]) {
+            const int d = dbase + warp + kNW * i;
+#pragma unroll
+            for (int v = 0; v < NV; v++) {
+                if (lane == v && v < nv) {
+                    const int pv = g.tg * P.NV + v;
+                    const int row = g.shared ? P.T * P.K + pv : g.pbase + pv;
+                    P.y[(size_t)row * P.H + d] = s[0][v] * g.s0[d];
+                }
+            }
+        });
+}
+
+template <int NV>
+__device__ void run_units(const DecParams &P, const Seg &g, bool down, const float *xs) {
+    if (down) {
+        if (g.fmt == COLI_FMT_INT4) down_units<COLI_FMT_INT4, NV>(P, g, xs);
+        else if (g.fmt == COLI_FMT_INT8) down_units<COLI_FMT_INT8, NV>(P, g, xs);
+        else down_units<COLI_FMT_INT2, NV>(P, g, xs);
+    } else {
+        if (g.fmt == COLI_FMT_INT4) gateup_units<COLI_FMT_INT4, NV>(P, g, xs);
+        else if (g.fmt == COLI_FMT_INT8) gateup_units<COLI_FMT_INT8, NV>(P, g, xs);
+        else gateup_units<COLI_FMT_INT2, NV>(P, g, xs);
+    }
+}
+
+// fill the segment of unit l (thread 0 only): unit spaces are slot-major, then token group,
+// then row; routed slots come from the table, the shared expert is slot U (or the static
+// shared phase when U < 0)
+__device__ void make_seg(const DecParams &P, int slot, int U, int slot_base, int l, int e_share, bool down, Seg &g) {
+    const bool shared = U < 0 || slot == U;
+    const int rows_per_group = down ? P.H : (shared ? P.Is : P.I);
+    if (shared) {
+        g.w0 = static_cast<const uint8_t *>(down ? P.shared.down_w : P.shared.gate_w);
+        g.w1 = static_cast<const uint8_t *>(P.shared.up_w);
+        g.s0 = down ? P.shared.down_s : P.shared.gate_s;
+        g.s1 = P.shared.up_s;
+        g.fmt = P.sfmt;
+        g.inter = P.Is;
+        g.n = P.T;
+        g.pbase = 0;
+        g.key = kSharedKey;
+        g.need = P.G_sh;
+    } else {
+        const int e = __ldcg(&P.tab->slot_e[slot]);
+        const coli_moe_expert ex = P.experts[e];
+        g.w0 = static_cast<const uint8_t *>(down ? ex.down_w : ex.gate_w);
+        g.w1 = static_cast<const uint8_t *>(ex.up_w);
+        g.s0 = down ? ex.down_s : ex.gate_s;
+        g.s1 = ex.up_s;
+        g.fmt = P.rfmt;
+        g.inter = P.I;
+        g.n = __ldcg(&P.tab->slot_n[slot]);
+        g.pbase = __ldcg(&P.tab->slot_pbase[slot]);
+        g.key = slot;
+        g.need = __ldcg(&P.tab->slot_groups[slot]) * P.I;
+        if (bad16(ex.gate_w) || bad16(ex.up_w) || bad16(ex.down_w)) flag_error(P.ctrl, kErrBadExpert);
+    }
+    g.shared = shared ? 1 : 0;
+    const int local = l - slot_base;
+    g.tg = local / rows_per_group;
+    g.ubase = slot_base + g.tg * rows_per_group;
+    g.ulo = l;
+    g.uhi = min(e_share, g.ubase + rows_per_group);
+}
+
+// walk this CTA's share [b, e) of a unit space (gate/up or down) segment by segment
+template <int NV>
+__device__ void run_share(const DecParams &P, int b, int e, bool down, bool shared_phase, float *xs, Seg *sg,
+                          int *skey) {
+    const int tid = threadIdx.x;
+    if (b >= e) return;
+    int U = -1, slot = 0, slot_base = 0, slot_end = 0, done_in_slot = 0;
+    const int *off = down ? P.tab->dn_off : P.tab->gu_off;
+    if (!shared_phase) U = __ldcg(&P.tab->U);
+    const int nslots = shared_phase ? 1 : (down ? U + (P.Is > 0 ? 1 : 0) : U);
+    if (tid == 0) {
+        if (shared_phase) {
+            slot_base = 0;
+            slot_end = P.G_sh;
+        } else {
+            slot = upper_slot(off, nslots, b);
+            slot_base = __ldcg(off + slot);
+            slot_end = __ldcg(off + slot + 1);
+        }
+    }
+    int l = b;
+    while (l < e) {
+        __syncthreads();  // the previous segment's units are done with xs and sg
+        if (tid == 0) {
+            while (l >= slot_end) {  // next slot (thread 0's cursor)
+                slot++;
+                slot_base = slot_end;
+                slot_end = __ldcg(off + slot + 1);
+            }
+            make_seg(P, slot, shared_phase ? -1 : U, slot_base, l, min(e, slot_end), down, *sg);
+            if (down) {  // this expert's h rows must all be written
+                wait_at_least(&P.ctrl->gu_done[sg->key], sg->need, P.ctrl);
+                __threadfence();
+            }
+        }
+        __syncthreads();
+        const Seg g = *sg;
+        // activations: skip restaging when xs already holds them (same kind, tokens and format)
+        const int k0 = down ? 2 : 1;
+        const int k1 = down ? g.key : (P.T == 1 ? 0 : (g.shared ? -1 : g.pbase));
+        const int k2 = (P.T == 1 && !down) ? g.fmt : g.tg * 8 + g.fmt;
+        if (!(skey[0] == k0 && skey[1] == k1 && skey[2] == k2)) {
+            stage_acts(P, g, down, xs);
+            __syncthreads();
+            if (tid == 0) {
+                skey[0] = k0;
+                skey[1] = k1;
+                skey[2] = k2;
+            }
+        }
+        run_units<NV>(P, g, down, xs);
+        l = g.uhi;
+        if (!down) {  // publish this CTA's gate/up units of the expert when its run ends
+            __syncthreads();  // every warp's h stores precede thread 0's release
+            if (tid == 0) {
+                done_in_slot += g.uhi - g.ulo;
+                if (l >= e || l >= slot_end) {
+                    __threadfence();
+                    atomicAdd(&P.ctrl->gu_done[g.key], done_in_slot);
+                    done_in_slot = 0;
+                }
+            }
+        }
     }
     __syncthreads();
-    if (warp == kCW) {
-        Producer pr{P, ring, full, empty, desc, lane};
-        pr.run();
+}
+
+template <int NV>
+__global__ void __launch_bounds__(kNT, 2) moe_decode_kernel(const DecParams P) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    float *xs = reinterpret_cast<float *>(smem);
+    Seg *sg = reinterpret_cast<Seg *>(smem + P.xs_bytes);
+    int *skey = reinterpret_cast<int *>(sg + 1);
+    int *sflag = skey + 3;
+    const int tid = threadIdx.x, G = gridDim.x, c = blockIdx.x;
+    if (tid == 0) skey[0] = skey[1] = skey[2] = -1;
+
+    // ---------------- A: routing
+    if (!P.route_only) {
+        if (c < P.R) {
+            router_item(P, c);
+            __syncthreads();
+            const int eb = c % P.neb;
+            if (tid == 0) {
+                __threadfence();
+                const bool last = atomicAdd(&P.ctrl->eb_done[eb], 1) == P.nks - 1;
+                if (last) __threadfence();
+                *sflag = last;
+            }
+            __syncthreads();
+            if (*sflag) {  // last k-slice of this expert block: its logits
+                const int e0 = eb * kRtE, e1 = min(P.E, e0 + kRtE);
+                for (int t = 0; t < P.T; t++) reduce_logits(P, t * P.E + e0, t * P.E + e1);
+                __syncthreads();
+                if (tid == 0) {
+                    __threadfence();
+                    const bool last = atomicAdd(&P.ctrl->router_done, 1) == P.neb - 1;
+                    if (last) __threadfence();
+                    *sflag = last;
+                }
+                __syncthreads();
+                if (*sflag) route_final(P, xs);
+            }
+            __syncthreads();
+        }
     } else {
-        Consumer co{P, ring, full, empty, desc, xs, ybuf, sflag, tid, lane, warp};
-        co.run();
+        reduce_logits(P, range_lo(P.T * P.E, c, G), range_lo(P.T * P.E, c + 1, G));
+        __syncthreads();
+        if (tid == 0) {
+            __threadfence();
+            const bool last = atomicAdd(&P.ctrl->router_done, 1) == G - 1;
+            if (last) __threadfence();
+            *sflag = last;
+        }
+        __syncthreads();
+        if (*sflag) route_final(P, xs);
+        __syncthreads();
+    }
+    if (tid == 0) skey[0] = -1;  // xs may have served as routing scratch
+
+    // ---------------- B: the shared expert's gate/up (independent of routing)
+    if (P.Is > 0) run_share<NV>(P, range_lo(P.G_sh, c, G), range_lo(P.G_sh, c + 1, G), false, true, xs, sg, skey);
+
+    // ---------------- C: routed gate/up
+    if (tid == 0) {
+        wait_at_least(&P.ctrl->routing_ready, 1, P.ctrl);
+        __threadfence();
+    }
+    __syncthreads();
+    const int gu_tot = __ldcg(&P.tab->gu_tot);
+    run_share<NV>(P, range_lo(gu_tot, c, G), range_lo(gu_tot, c + 1, G), false, false, xs, sg, skey);
+
+    // ---------------- D: down rows of every expert
+    const int dn_tot = __ldcg(&P.tab->dn_tot);
+    const int db = range_lo(dn_tot, c, G), de = range_lo(dn_tot, c + 1, G);
+    run_share<NV>(P, db, de, true, false, xs, sg, skey);
+    if (tid == 0) {
+        __threadfence();
+        atomicAdd(&P.ctrl->dn_done, de - db);
+    }
+
+    // ---------------- E: combine this CTA's rows of out
+    if (tid == 0) {
+        wait_at_least(&P.ctrl->dn_done, dn_tot, P.ctrl);
+        __threadfence();
+    }
+    __syncthreads();
+    const int r_lo = range_lo(P.H, c, G), r_hi = range_lo(P.H, c + 1, G), nd = r_hi - r_lo;
+    for (int i = tid; i < P.T * nd; i += kNT) {
+        const int t = i / nd, d = r_lo + i % nd;
+        const int ke = __ldcg(P.keff + t);
+        float a = 0.f;
+        for (int k = 0; k < ke; k++) {
+            const float wk = __ldcg(P.w + (size_t)t * P.K + k);
+            const int p = __ldcg(P.pos + (size_t)t * P.K + k);
+            a = __fadd_rn(a, __fmul_rn(wk, __ldcg(P.y + (size_t)p * P.H + d)));
+        }
+        if (P.Is > 0) a = __fadd_rn(a, __ldcg(P.y + ((size_t)P.T * P.K + t) * P.H + d));
+        P.out[(size_t)t * P.H + d] = a;
     }
 }
 
@@ -994,76 +836,57 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(const DecPar
 size_t decode_ctrl_bytes() { return sizeof(DecCtrl); }
 size_t decode_table_bytes() { return sizeof(DecTable); }
 
-size_t decode_smem_bytes(const DecParams &P) {
-    return (size_t)P.nst * kSB + P.xs_bytes + P.ybuf_bytes + 2 * P.nst * sizeof(uint64_t) +
-           P.nst * sizeof(StageDesc) + 16;
-}
+size_t decode_smem_bytes(const DecParams &P) { return (size_t)P.xs_bytes + sizeof(Seg) + 64; }
 
-// Host-side geometry of the decode launch (static item counts, staging sizes).
-void decode_plan(const coli_moe_desc &d, DecParams &P) {
+// Host-side geometry of the decode launch for a grid of `grid` CTAs.
+bool decode_plan(const coli_moe_desc &d, DecParams &P, int grid) {
     const int T = d.T;
-    P.NV = T == 1 ? 1 : (T <= 2 || T > 32 ? 2 : 4);
-    P.nst = 2;  // set by decode_plan_grid
+    P.NV = T == 1 ? 1 : (T <= 2 ? 2 : 4);
     const int maxdim = std::max(d.H, std::max(d.I, d.I_shared));
     P.xs_stride = maxdim;
     const size_t xs_vec = (size_t)P.NV * maxdim * sizeof(float);
-    const size_t xs_route = (size_t)(5 * d.E + kCW * d.E + 2 * (d.E + 2) + 16) * sizeof(int);
-    P.xs_bytes = (int)align_up(std::max(xs_vec, xs_route), 128);
-    const bool in_kernel_router = T <= 8;
+    const size_t scratch = (size_t)(5 * d.E + kNW * d.E + 16 + 2 * T * d.K + T + 2 * (d.E + 2) + 16) * sizeof(int);
+    P.xs_bytes = (int)align_up(std::max(xs_vec, scratch), 128);
+    P.route_only = T <= 8 ? 0 : 1;
     P.neb = (d.E + kRtE - 1) / kRtE;
-    // about 64 router items: split H into k-slices of whole 128-float stages
-    const int max_slices = (d.H + kRtKc / 4 - 1) / (kRtKc / 4);
-    int nks = std::min(max_slices, std::max(1, (64 + P.neb - 1) / P.neb));
-    const int stages = (max_slices + nks - 1) / nks;
-    P.rks_floats = stages * (kRtKc / 4);
-    nks = (d.H + P.rks_floats - 1) / P.rks_floats;
-    P.route_only = in_kernel_router ? 0 : 1;
-    P.nks = in_kernel_router ? nks : 0;  // T > 8: set by the caller to the router launch's splits
-    P.R = in_kernel_router ? P.neb * nks : 1;
+    if (!P.route_only) {
+        // router items: expert blocks x k-slices of whole float4 groups, at most one per CTA
+        const int max_slices = std::max(1, d.H / 128);
+        int nks = std::max(1, std::min({grid / P.neb, max_slices, 16}));
+        P.rks_floats = (d.H / nks + 3) / 4 * 4;
+        nks = (d.H + P.rks_floats - 1) / P.rks_floats;
+        P.nks = nks;
+        P.R = P.neb * nks;
+        if (P.R > grid) return false;
+    } else {
+        P.R = 0;  // P.nks is the separate router launch's split count
+    }
     P.groups_sh = d.I_shared > 0 ? (T + P.NV - 1) / P.NV : 0;
-    P.G_sh_rb = d.I_shared > 0 ? (d.I_shared + kGuPairs - 1) / kGuPairs : 0;
-    P.G_sh = P.G_sh_rb * P.groups_sh;
-    P.gu_rb = (d.I + kGuPairs - 1) / kGuPairs;
-}
-
-// the grid is one CTA per SM; each owns ceil(H / grid) rows of the down projection
-// and as many 16 KB ring stages (2..6) as fit beside the staging and y buffers
-bool decode_plan_grid(const coli_moe_desc &d, DecParams &P, int grid) {
-    P.rows_cta = (d.H + grid - 1) / grid;
-    const size_t rows = (size_t)d.T * d.K + (d.I_shared > 0 ? d.T : 0);
-    P.ybuf_bytes = (int)align_up(rows * P.rows_cta * sizeof(float), 128);
-    const long budget = 227L * 1024 - P.xs_bytes - P.ybuf_bytes - 1024;
-    const long nst = std::min(6L, budget / kSB);
-    if (nst < 2) return false;
-    P.nst = (int)nst;
-    return decode_smem_bytes(P) <= 227u * 1024;
+    P.G_sh = d.I_shared > 0 ? P.groups_sh * d.I_shared : 0;
+    return decode_smem_bytes(P) <= 113u * 1024;
 }
 
 bool decode_supported(const coli_moe_desc &d) {
-    if (d.T > kDecMaxT || d.T < 1) return false;
-    // every gate/up row k-chunk and every down row must fit a 16 KB ring stage
-    const int64_t dn_r = row_bytes(d.routed_fmt, d.I);
-    const int64_t dn_s = d.I_shared > 0 ? row_bytes(d.shared_fmt, d.I_shared) : 0;
-    if (dn_r > kSB || dn_s > kSB) return false;
-    return true;
+    return d.T >= 1 && d.T <= kDecMaxT && (d.E + kRtE - 1) / kRtE <= 32;
 }
 
 cudaError_t launch_decode(const DecParams &P, int grid, cudaStream_t st) {
     const size_t smem = decode_smem_bytes(P);
-    cudaError_t e = cudaFuncSetAttribute(moe_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    const void *fn = P.NV == 1 ? (const void *)moe_decode_kernel<1>
+                   : P.NV == 2 ? (const void *)moe_decode_kernel<2> : (const void *)moe_decode_kernel<4>;
+    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     // cooperative: every CTA of the static schedule is resident at once
     void *args[] = {const_cast<DecParams *>(&P)};
-    return cudaLaunchCooperativeKernel((const void *)moe_decode_kernel, dim3(grid), dim3(kDecThreads), args,
-                                       smem, st);
+    return cudaLaunchCooperativeKernel(fn, dim3(grid), dim3(kNT), args, smem, st);
 }
 
 int decode_ctas_per_sm(const DecParams &P) {
     int n = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, moe_decode_kernel, kDecThreads, decode_smem_bytes(P)) !=
-        cudaSuccess)
-        return 1;
-    return n < 1 ? 1 : n;
+    const void *fn = P.NV == 1 ? (const void *)moe_decode_kernel<1>
+                   : P.NV == 2 ? (const void *)moe_decode_kernel<2> : (const void *)moe_decode_kernel<4>;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, kNT, decode_smem_bytes(P)) != cudaSuccess) return 0;
+    return n;
 }
 
 }  // namespace colimoe

@@ -29,19 +29,22 @@ constexpr int kDecMaxT = 64;              // the persistent decode kernel serves
 // Counters of one decode call (zeroed before each launch; err stays the first word, which is
 // also the workspace error word read by coli_moe_check).
 struct DecCtrl {
-    int err, queue, router_done, routing_ready;
+    int err, router_done, routing_ready, dn_done;
     int pad[12];
-    int gu_done[kMaxE + 1];            // finished gate/up items per slot (shared: index kMaxE)
+    int eb_done[32];                   // finished router k-slices per 32-expert block
+    int gu_done[kMaxE + 1];            // finished gate/up units per slot (shared: index kMaxE)
 };
 
-// Item table published by the routing CTA.
+// Unit table published by the routing CTA: slot u < U is the u-th active expert (ascending
+// id), slot U the shared expert.
 struct DecTable {
-    int U, pad[7];
+    int U, gu_tot, dn_tot, pad[5];
     int slot_e[kMaxE + 1];
     int slot_n[kMaxE + 1];
     int slot_pbase[kMaxE + 1];
     int slot_groups[kMaxE + 1];
-    int gu_off[kMaxE + 2];
+    int gu_off[kMaxE + 2];             // gate/up units before slot u (routed slots)
+    int dn_off[kMaxE + 2];             // down units before slot u (routed slots, then shared)
 };
 
 struct DecParams {
@@ -50,7 +53,7 @@ struct DecParams {
     coli_moe_expert shared;
     float *out;
     float *part;               // router partial logits [nks][T][E]
-    float *sig, *choice, *w;
+    float *sig, *choice, *w;   // sig holds the logits until the selection turns them into scores
     int32_t *idx, *keff, *counts, *offsets, *perm, *pos, *act;
     float *h, *y;
     DecCtrl *ctrl;
@@ -58,16 +61,13 @@ struct DecParams {
     int T, H, I, E, K, Is, rfmt, sfmt, Ksel, norm_topk;
     float top_p, rscale;
     int ldh;
-    int NV, nst, xs_stride, xs_bytes;
-    int R, route_only;         // router items; route_only: one item that only selects
+    int NV, xs_stride, xs_bytes;
+    int R, route_only;         // router items; route_only: logits come from a separate launch
     int neb, nks, rks_floats;  // router expert blocks, k-slices, floats per k-slice
-    int G_sh_rb, groups_sh, G_sh;
-    int gu_rb;
-    int rows_cta, ybuf_bytes;  // down rows per CTA, bytes of the CTA's y buffer
+    int groups_sh, G_sh;       // shared expert token groups and gate/up units
 };
 
-void decode_plan(const coli_moe_desc &d, DecParams &P);
-bool decode_plan_grid(const coli_moe_desc &d, DecParams &P, int grid);
+bool decode_plan(const coli_moe_desc &d, DecParams &P, int grid);
 bool decode_supported(const coli_moe_desc &d);
 size_t decode_smem_bytes(const DecParams &P);
 int decode_ctas_per_sm(const DecParams &P);

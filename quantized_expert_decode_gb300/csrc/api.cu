@@ -152,7 +152,6 @@ int run_forward_decode(const coli_moe_desc *d, const float *x, const float *W_r,
     P.h = ws_ptr<float>(ws, L.h);
     P.y = ws_ptr<float>(ws, L.y);
     P.ctrl = ws_ptr<DecCtrl>(ws, L.err);
-    P.tab = ws_ptr<DecTable>(ws, L.tab);
     P.T = d->T;
     P.H = d->H;
     P.I = d->I;

@@ -39,7 +39,6 @@ __host__ __device__ inline int elems_per_chunk(int fmt) {
 // Device workspace layout. Every region starts on a 256-byte boundary.
 struct WsLayout {
     size_t err;       // control block of the call; its first int32 is the error word
-    size_t tab;       // decode item table
     size_t part;      // f32 [S][T][E] router partial logits
     size_t sig;       // f32 [T][E]
     size_t choice;    // f32 [T][E]
@@ -78,7 +77,6 @@ inline int router_splits(const coli_moe_desc &d) {
 }
 
 size_t decode_ctrl_bytes();
-size_t decode_table_bytes();
 
 inline WsLayout ws_layout(const coli_moe_desc &d) {
     WsLayout L{};
@@ -93,7 +91,6 @@ inline WsLayout ws_layout(const coli_moe_desc &d) {
     const size_t imax = (size_t)(d.I > d.I_shared ? d.I : d.I_shared);
     L.router_splits = router_splits(d);
     L.err = take(decode_ctrl_bytes());
-    L.tab = take(decode_table_bytes());
     L.part = take((size_t)L.router_splits * T * E * 4);
     L.sig = take(T * E * 4);
     L.choice = take(T * E * 4);

@@ -2,15 +2,15 @@
 //
 // Phases, each split statically and contiguously over the CTAs (two per SM, cooperative
 // launch, so every CTA is resident and a wait is only ever on an earlier phase):
-//   A  routing (colibri-strix c/glm.c @98759bf moe() phase A; r_router / r_top8_par shaders):
-//      T <= 8: router items — logits of 32 experts over one slice of H — write partial logits;
-//      the last item of each 32-expert block (atomic ticket) sums that block's partials in a
-//      fixed order; the last block runs the selection. T > 8: the partial logits come from a
-//      router launch before this kernel; every CTA sums a share, the last one selects.
-//      Selection (one CTA, everything in shared memory): sigmoid, bias, greedy top-K with ties
-//      to the lower index, TOPK/TOPP, renorm, routed scale, token->expert buckets (stable) and
-//      the unit table of the expert phases; then a flag is published.
-//   B  shared expert gate/up rows (known before routing: overlaps phase A)
+//   A  router logits (colibri-strix c/glm.c @98759bf moe() phase A; r_router shader):
+//      T <= 8: router items — partial logits of 32 experts over one slice of H; T > 8: the
+//      partials come from a router launch before this kernel and every CTA sums a share.
+//   B  shared expert gate/up rows (independent of routing: runs while A completes)
+//   R  routing, by EVERY CTA for itself once all partials are in (one counter wait): logits
+//      summed in a fixed order, sigmoid, bias, greedy top-K with ties to the lower index
+//      (r_top8 / r_top8_par), TOPK/TOPP, renorm, routed scale, stable token->expert buckets and
+//      the unit tables — all in shared memory; CTA 0 also writes the routing outputs. Running
+//      it everywhere keeps a cold, single-CTA step off the critical path.
 //   C  routed gate/up rows: h = silu(gate.x * s_g) * (up.x * s_u)   (moe() phases C/D)
 //   D  down rows: y = (down.h) * s_d, for every selected expert and the shared one
 //   E  combine: out = sum_k w_k y_k in selection order + y_shared   (moe() phases C/D/E)
@@ -19,8 +19,8 @@
 // expert and tokens: the segment's activations are staged once in shared memory (pre-scaled and
 // permuted, see qdot.cuh), then each warp streams its units' rows with 16-byte loads kept
 // several chunks ahead in registers, across unit boundaries.
-// Dependencies are counters in the workspace, raised once per CTA per expert (gate/up -> down)
-// or per CTA (down -> combine). Every wait is bounded (2 s of %globaltimer); on expiry the kernel
+// Dependencies are counters in the workspace: router items -> routing, gate/up -> down (raised
+// once per CTA per expert), down -> combine (once per CTA). Every wait is bounded (2 s of %globaltimer); on expiry the kernel
 // records kErrWaitExpired and carries on, so a fault in the schedule can not hang the GPU.
 #include <algorithm>
 
@@ -35,7 +35,7 @@ namespace {
 constexpr int kNT = 256;                 // threads per CTA
 constexpr int kNW = kNT / kWarp;         // warps per CTA
 constexpr int kRtE = 32;                 // experts per router item (4 per warp)
-constexpr int kDepth = 4;                // 16-byte chunks kept in flight per lane and row
+constexpr int kInflight = 8;             // 16-byte loads in flight per lane (rows x depth)
 constexpr unsigned long long kWaitNs = 2000000000ull;
 constexpr int kSharedKey = kMaxE;        // gu_done index of the shared expert
 
@@ -73,12 +73,13 @@ __device__ __forceinline__ bool bad16(const void *p) { return (reinterpret_cast<
 // ------------------------------------------------------------------ the streaming core
 // One warp streams `nunits` units of NR packed rows each (CPR 16-byte chunks per row), lane l
 // taking chunks l, l+32, ... of every row, with kDepth chunk-steps of loads in flight across unit
-// boundaries. rows_of(i, rows) gives unit i's row pointers; epi(i, sums) gets the finished
+// boundaries (kInflight / NR steps). rows_of(i, rows) gives unit i's row pointers; epi(i, sums) gets the finished
 // warp-reduced dot products with the NV staged vectors.
 template <int FMT, int NR, int NV, class RowsOf, class Epi>
 __device__ __forceinline__ void warp_stream(int nunits, int CPR, const float *xs, int xstride, int lane,
                                             RowsOf rows_of, Epi epi) {
     using G = QGeom<FMT>;
+    constexpr int kDepth = kInflight / NR;  // chunk-steps in flight
     if (nunits <= 0) return;
     const int S = (CPR + kWarp - 1) / kWarp;  // steps per unit
     const int total = nunits * S;
@@ -159,27 +160,66 @@ __device__ __forceinline__ void warp_stream(int nunits, int CPR, const float *xs
 }
 
 // ------------------------------------------------------------------ routing
-struct Scratch {  // shared-memory layout of the selection step (inside the staging buffer)
-    int *cnt, *off, *fill, *chk, *actv, *wc, *tmp, *idx, *keff, *gu, *dn;
-    float *w;
+// This CTA's copy of the routing result (shared memory, alive until the kernel ends).
+struct RTab {
+    int *slot_e, *slot_n, *slot_pbase, *slot_groups;  // [E+1]: slot u < U routed, U shared
+    int *gu_off, *dn_off;                             // [E+2]: units before slot u
+    int *perm, *pos;                                  // [T*K]
+    float *w;                                         // [T*K] kept weights (0 beyond keff)
+    int *keff;                                        // [T]
+    int *U;
 };
 
-__device__ __forceinline__ Scratch scratch_of(void *base, int E, int T, int K) {
-    Scratch s;
+size_t rtab_bytes(int T, int E, int K) {
+    return (size_t)(4 * (E + 1) + 2 * (E + 2) + 3 * T * K + T + 16) * 4;
+}
+
+__device__ __forceinline__ RTab rtab_of(void *base, int T, int E, int K) {
+    RTab r;
     int *p = static_cast<int *>(base);
-    s.cnt = p;
+    r.slot_e = p;
+    r.slot_n = r.slot_e + (E + 1);
+    r.slot_pbase = r.slot_n + (E + 1);
+    r.slot_groups = r.slot_pbase + (E + 1);
+    r.gu_off = r.slot_groups + (E + 1);
+    r.dn_off = r.gu_off + (E + 2);
+    r.perm = r.dn_off + (E + 2);
+    r.pos = r.perm + T * K;
+    r.w = reinterpret_cast<float *>(r.pos + T * K);
+    r.keff = reinterpret_cast<int *>(r.w + T * K);
+    r.U = r.keff + T;
+    return r;
+}
+
+// Scratch of the routing step (inside the activation staging buffer).
+struct RScratch {
+    float *sg, *ch;          // [T][E] sigmoid scores, choices
+    int *sel_i;              // [T][K] selected expert ids in selection order
+    float *sel_w;            // [T][K] their scores
+    int *nvalid;             // [T]
+    int *cnt, *off, *fill, *chk, *actv, *wc, *tmp;
+};
+
+__device__ __forceinline__ RScratch rscratch_of(void *base, const DecParams &P) {
+    RScratch s;
+    const int TE = P.T * P.E, TK = P.T * P.K, E = P.E;
+    s.sg = static_cast<float *>(base);
+    s.ch = s.sg + TE;
+    s.sel_w = s.ch + TE;
+    s.sel_i = reinterpret_cast<int *>(s.sel_w + TK);
+    s.nvalid = s.sel_i + TK;
+    s.cnt = s.nvalid + P.T;
     s.off = s.cnt + E;
     s.fill = s.off + E;
     s.chk = s.fill + E;
     s.actv = s.chk + E;
     s.wc = s.actv + E;
     s.tmp = s.wc + kNW * E;
-    s.idx = s.tmp + 16;
-    s.keff = s.idx + T * K;
-    s.gu = s.keff + T;
-    s.dn = s.gu + (E + 2);
-    s.w = reinterpret_cast<float *>(s.dn + (E + 2));
     return s;
+}
+
+size_t rscratch_bytes(int T, int E, int K) {
+    return (size_t)(2 * T * E + 2 * T * K + T + 5 * E + kNW * E + 16 + 16) * 4;
 }
 
 // exclusive scan in place of n <= 2048 ints in shared memory by the CTA; returns the total
@@ -222,36 +262,21 @@ __device__ int scan_smem(int *a, int n, int *tmp) {
     return total;
 }
 
-// one warp: selection of token t from its logits (sigmoid, bias, greedy top-K, TOPP, renorm,
-// scale). Lane l owns experts [l*PER, l*PER + PER), so the lane-local strict '>' ascending scan
-// plus a cross-lane argmax preferring the lower index reproduce the serial first-max-wins order.
+// one warp: greedy top-Ksel of token t over the choices in shared memory. Lane l owns experts
+// [l*PER, l*PER + PER), so a lane-local strict '>' ascending scan plus a cross-lane argmax
+// preferring the lower index reproduce the serial first-max-wins order.
 template <int PER>
-__device__ void select_token(const DecParams &P, int t, int lane, const Scratch &sc) {
+__device__ void argmax_rounds(const DecParams &P, const RScratch &s, int t, int lane) {
     const int base = lane * PER;
     float ch[PER], sg[PER];
 #pragma unroll
     for (int j = 0; j < PER; j++) {
         const int e = base + j;
-        ch[j] = e < P.E ? __ldcg(P.sig + (size_t)t * P.E + e) : 0.f;  // logits, all loads in flight
-    }
-#pragma unroll
-    for (int j = 0; j < PER; j++) {
-        const int e = base + j;
-        if (e < P.E) {
-            const float sv = 1.f / (1.f + expf(-ch[j]));
-            const float cv = sv + P.bias[e];
-            P.sig[(size_t)t * P.E + e] = sv;
-            P.choice[(size_t)t * P.E + e] = cv;
-            sg[j] = sv;
-            ch[j] = cv;
-        } else {
-            sg[j] = 0.f;
-            ch[j] = -INFINITY;
-        }
+        ch[j] = e < P.E ? s.ch[t * P.E + e] : -INFINITY;
+        sg[j] = e < P.E ? s.sg[t * P.E + e] : 0.f;
     }
     uint32_t taken = 0;
-    int nsel = 0, my_i = -1;
-    float my_w = 0.f;
+    int nsel = 0;
     for (int k = 0; k < P.Ksel; k++) {
         float bv = -1e30f, bs = 0.f;
         int bi = 0x7fffffff;
@@ -275,223 +300,329 @@ __device__ void select_token(const DecParams &P, int t, int lane, const Scratch 
         }
         bi = __shfl_sync(kFull, bi, 0);
         bs = __shfl_sync(kFull, bs, 0);
-        if (bi == 0x7fffffff) {
-            if (lane == 0) flag_error(P.ctrl, kErrNoCandidate);
-            break;
-        }
+        if (bi == 0x7fffffff) break;
         if (bi >= base && bi < base + PER) taken |= 1u << (bi - base);
-        if (lane == k) {
-            my_i = bi;
-            my_w = bs;
+        if (lane == 0) {
+            s.sel_i[t * P.K + k] = bi;
+            s.sel_w[t * P.K + k] = bs;
         }
         nsel = k + 1;
     }
-    float ww[kMaxK];
-    int id[kMaxK];
-    for (int k = 0; k < nsel; k++) {
-        ww[k] = __shfl_sync(kFull, my_w, k);
-        id[k] = __shfl_sync(kFull, my_i, k);
-    }
-    if (lane != 0) return;
-    int Ke = nsel;
-    if (P.top_p > 0.f && P.top_p < 1.f) {
-        for (int a = 1; a < nsel; a++) {
-            const int ia = id[a];
-            const float wa = ww[a];
-            int b = a - 1;
-            while (b >= 0 && ww[b] < wa) {
-                ww[b + 1] = ww[b];
-                id[b + 1] = id[b];
-                b--;
-            }
-            ww[b + 1] = wa;
-            id[b + 1] = ia;
-        }
-        float tot = 1e-20f;
-        for (int k = 0; k < nsel; k++) tot = __fadd_rn(tot, ww[k]);
-        float cum = 0.f;
-        for (int k = 0; k < nsel; k++) {
-            cum = __fadd_rn(cum, ww[k]);
-            if (cum >= __fmul_rn(P.top_p, tot)) {
-                Ke = k + 1;
-                break;
-            }
-        }
-    }
-    if (P.norm_topk) {
-        float sm = 0.f;
-        for (int k = 0; k < Ke; k++) sm = __fadd_rn(sm, ww[k]);
-        sm = __fadd_rn(sm, 1e-20f);
-        for (int k = 0; k < Ke; k++) ww[k] = __fdiv_rn(ww[k], sm);
-    }
-    for (int k = 0; k < P.K; k++) {
-        const bool kept = k < Ke;
-        const int vi = kept ? id[k] : -1;
-        const float vw = kept ? __fmul_rn(ww[k], P.rscale) : 0.f;
-        P.idx[(size_t)t * P.K + k] = vi;
-        P.w[(size_t)t * P.K + k] = vw;
-        sc.idx[t * P.K + k] = vi;
-        sc.w[t * P.K + k] = vw;
-    }
-    P.keff[t] = Ke;
-    sc.keff[t] = Ke;
+    if (lane == 0) s.nvalid[t] = nsel;
 }
 
-// selection, buckets and the unit table, by one CTA, from the logits in P.sig
-__device__ void route_final(const DecParams &P, void *scratch) {
+// The routing of all T tokens by this CTA, from the logits (the fixed-order sum of the nks
+// partial slices when from_partials, else slice 0 already holds them). Results go to rt; CTA 0
+// also writes the routing outputs of the workspace / caller.
+__device__ __noinline__ void route_local(const DecParams &P, float *scratch, const RTab &rt, bool from_partials) {
     const int tid = threadIdx.x, lane = tid % kWarp, warp = tid / kWarp;
-    const Scratch sc = scratch_of(scratch, P.E, P.T, P.K);
-    const int per = (P.E + kWarp - 1) / kWarp;
-    for (int t = warp; t < P.T; t += kNW) {
-        if (per <= 1) select_token<1>(P, t, lane, sc);
-        else if (per <= 2) select_token<2>(P, t, lane, sc);
-        else if (per <= 4) select_token<4>(P, t, lane, sc);
-        else if (per <= 8) select_token<8>(P, t, lane, sc);
-        else if (per <= 16) select_token<16>(P, t, lane, sc);
-        else select_token<32>(P, t, lane, sc);
-    }
-    const int E = P.E, N = P.T * P.K;
-    for (int e = tid; e < E; e += kNT) {
-        sc.cnt[e] = 0;
-        sc.fill[e] = 0;
-    }
-    __syncthreads();
-    auto expert_of = [&](int a) -> int {
-        if (a >= N) return -1;
-        return (a % P.K) < sc.keff[a / P.K] ? sc.idx[a] : -1;
-    };
-    for (int a = tid; a < N; a += kNT) {
-        const int e = expert_of(a);
-        if (e >= 0) atomicAdd(&sc.cnt[e], 1);
-    }
-    __syncthreads();
-    for (int e = tid; e < E; e += kNT) {
-        sc.off[e] = sc.cnt[e];
-        sc.actv[e] = sc.cnt[e] > 0 ? 1 : 0;
-        P.counts[e] = sc.cnt[e];
-    }
-    __syncthreads();
-    const int total = scan_smem(sc.off, E, sc.tmp);
-    const int U = scan_smem(sc.actv, E, sc.tmp);
-    for (int e = tid; e < E; e += kNT) {
-        P.offsets[e] = sc.off[e];
-        if (sc.cnt[e] > 0) {
-            P.act[sc.actv[e]] = e;
-            sc.chk[sc.actv[e]] = e;  // active experts, ascending (chk is free until the chunk loop)
-        }
-    }
-    if (tid == 0) P.offsets[E] = total;
-    __syncthreads();
-    // unit table: slot u < U is the u-th active expert; slot U the shared expert
-    for (int u = tid; u < U + 1; u += kNT) {
-        int g = 0;
-        if (u < U) {
-            const int e = sc.chk[u];
-            g = (sc.cnt[e] + P.NV - 1) / P.NV;
-            P.tab->slot_e[u] = e;
-            P.tab->slot_n[u] = sc.cnt[e];
-            P.tab->slot_pbase[u] = sc.off[e];
-            P.tab->slot_groups[u] = g;
-            sc.gu[u] = g * P.I;
-            sc.dn[u] = g * P.H;
+    const bool out = blockIdx.x == 0;
+    const RScratch s = rscratch_of(scratch, P);
+    const int T = P.T, E = P.E, K = P.K, TE = T * E;
+    // 1. logits -> sigmoid scores and choices (all loads of a thread issued together)
+    for (int i = tid; i < TE; i += kNT) {
+        float lg = 0.f;
+        if (from_partials) {
+            float a[16];
+#pragma unroll
+            for (int k = 0; k < 16; k++)
+                if (k < P.nks) a[k] = __ldcg(P.part + (size_t)k * TE + i);
+#pragma unroll
+            for (int k = 0; k < 16; k++)
+                if (k < P.nks) lg += a[k];
         } else {
-            sc.gu[u] = 0;
-            sc.dn[u] = P.Is > 0 ? P.groups_sh * P.H : 0;
+            lg = __ldcg(P.part + i);
+        }
+        const float sv = 1.f / (1.f + expf(-lg));
+        const float cv = sv + P.bias[i % E];
+        s.sg[i] = sv;
+        s.ch[i] = cv;
+        if (out) {
+            P.sig[i] = sv;
+            P.choice[i] = cv;
+        }
+    }
+    if (tid < T) s.nvalid[tid] = 0;
+    __syncthreads();
+    // 2. greedy top-Ksel. T <= 8: by rank — every (token, expert) counts the experts that beat
+    //    it (a higher choice, or an equal choice and a lower index); that count is its position
+    //    in the serial greedy order. Larger T: warp rounds of lane-blocked argmax.
+    if (T <= 8) {
+        for (int i = tid; i < TE; i += kNT) {
+            const int t = i / E, e = i % E;
+            const float c = s.ch[i];
+            if (!(c > -1e30f)) continue;  // never selectable: the serial scan starts at -1e30
+            const float *row = s.ch + t * E;
+            int r = 0;
+            for (int e2 = 0; e2 < E; e2++) {
+                const float c2 = row[e2];
+                r += (c2 > c) || (c2 == c && e2 < e);
+            }
+            atomicAdd(&s.nvalid[t], 1);
+            if (r < P.Ksel) {
+                s.sel_i[t * K + r] = e;
+                s.sel_w[t * K + r] = s.sg[i];
+            }
+        }
+        __syncthreads();
+        if (tid < T) s.nvalid[tid] = min(s.nvalid[tid], P.Ksel);
+    } else {
+        const int per = (E + kWarp - 1) / kWarp;
+        for (int t = warp; t < T; t += kNW) {
+            if (per <= 1) argmax_rounds<1>(P, s, t, lane);
+            else if (per <= 2) argmax_rounds<2>(P, s, t, lane);
+            else if (per <= 4) argmax_rounds<4>(P, s, t, lane);
+            else if (per <= 8) argmax_rounds<8>(P, s, t, lane);
+            else if (per <= 16) argmax_rounds<16>(P, s, t, lane);
+            else argmax_rounds<32>(P, s, t, lane);
         }
     }
     __syncthreads();
-    const int gu_tot = scan_smem(sc.gu, U + 1, sc.tmp);
-    const int dn_tot = scan_smem(sc.dn, U + 1, sc.tmp);
-    for (int u = tid; u < U + 1; u += kNT) {
-        P.tab->gu_off[u] = sc.gu[u];
-        P.tab->dn_off[u] = sc.dn[u];
-    }
-    if (tid == 0) {
-        P.tab->gu_off[U + 1] = gu_tot;
-        P.tab->dn_off[U + 1] = dn_tot;
-        P.tab->U = U;
-        P.tab->gu_tot = gu_tot;
-        P.tab->dn_tot = dn_tot;
-    }
-    // stable perm / pos: 256-assignment chunks in order; inside a chunk, rank within the warp
-    // from a match-any mask, then the warps' per-expert counts are scanned
-    for (int a0 = 0; a0 < N; a0 += kNT) {
-        for (int i = tid; i < kNW * E; i += kNT) sc.wc[i] = 0;
-        __syncthreads();
-        const int a = a0 + tid;
-        const int e = expert_of(a);
-        const unsigned peers = __match_any_sync(kFull, e);
-        const int rank = __popc(peers & ((1u << lane) - 1u));
-        if (e >= 0 && rank == 0) sc.wc[warp * E + e] = __popc(peers);
-        __syncthreads();
-        for (int x = tid; x < E; x += kNT) {
-            int run = 0;
-            for (int w = 0; w < kNW; w++) {
-                const int v = sc.wc[w * E + x];
-                sc.wc[w * E + x] = run;
-                run += v;
+    // 3. per token: TOPP truncation, renormalisation, routed scale (the pages' float order)
+    for (int t = tid; t < T; t += kNT) {
+        const int nsel = s.nvalid[t];
+        int *id = s.sel_i + t * K;
+        float *ww = s.sel_w + t * K;
+        if (nsel < P.Ksel && out) flag_error(P.ctrl, kErrNoCandidate);
+        int Ke = nsel;
+        if (P.top_p > 0.f && P.top_p < 1.f) {
+            for (int a = 1; a < nsel; a++) {
+                const int ia = id[a];
+                const float wa = ww[a];
+                int b = a - 1;
+                while (b >= 0 && ww[b] < wa) {
+                    ww[b + 1] = ww[b];
+                    id[b + 1] = id[b];
+                    b--;
+                }
+                ww[b + 1] = wa;
+                id[b + 1] = ia;
             }
-            sc.chk[x] = run;
+            float tot = 1e-20f;
+            for (int k = 0; k < nsel; k++) tot = __fadd_rn(tot, ww[k]);
+            float cum = 0.f;
+            for (int k = 0; k < nsel; k++) {
+                cum = __fadd_rn(cum, ww[k]);
+                if (cum >= __fmul_rn(P.top_p, tot)) {
+                    Ke = k + 1;
+                    break;
+                }
+            }
         }
-        __syncthreads();
-        if (a < N) {
-            if (e >= 0) {
-                const int p = sc.off[e] + sc.fill[e] + sc.wc[warp * E + e] + rank;
-                P.perm[p] = a;
-                P.pos[a] = p;
+        float sm = 1.f;
+        if (P.norm_topk) {
+            sm = 0.f;
+            for (int k = 0; k < Ke; k++) sm = __fadd_rn(sm, ww[k]);
+            sm = __fadd_rn(sm, 1e-20f);
+        }
+        for (int k = 0; k < K; k++) {
+            const bool kept = k < Ke;
+            const float wn = kept ? (P.norm_topk ? __fdiv_rn(ww[k], sm) : ww[k]) : 0.f;
+            const float wk = kept ? __fmul_rn(wn, P.rscale) : 0.f;
+            const int ik = kept ? id[k] : -1;
+            id[k] = ik;
+            rt.w[t * K + k] = wk;
+            if (out) {
+                P.idx[(size_t)t * K + k] = ik;
+                P.w[(size_t)t * K + k] = wk;
+            }
+        }
+        rt.keff[t] = Ke;
+        if (out) P.keff[t] = Ke;
+    }
+    __syncthreads();
+    // 4. buckets and the unit tables (slot u < U: u-th active expert, ascending id; U: shared)
+    const int GUPER = (P.I + 1) / 2, DNPER = (P.H + 1) / 2;
+    int U;
+    if (T == 1) {  // one token: its kept experts are distinct
+        const int Ke = rt.keff[0];
+        if (out) {
+            for (int e = tid; e < E; e += kNT) {
+                int c = 0, o = 0;
+                for (int k = 0; k < Ke; k++) {
+                    const int ek = s.sel_i[k];
+                    c += ek == e;
+                    o += ek < e;
+                }
+                P.counts[e] = c;
+                P.offsets[e] = o;
+            }
+            if (tid == 0) P.offsets[E] = Ke;
+        }
+        if (tid < K) {
+            if (tid < Ke) {
+                const int e = s.sel_i[tid];
+                int slot = 0;
+                for (int k = 0; k < Ke; k++) slot += s.sel_i[k] < e;
+                rt.slot_e[slot] = e;
+                rt.slot_n[slot] = 1;
+                rt.slot_pbase[slot] = slot;
+                rt.slot_groups[slot] = 1;
+                rt.perm[slot] = tid;
+                rt.pos[tid] = slot;
+                if (out) {
+                    P.act[slot] = e;
+                    P.perm[slot] = tid;
+                    P.pos[tid] = slot;
+                }
             } else {
-                P.pos[a] = -1;
+                rt.pos[tid] = -1;
+                if (out) P.pos[tid] = -1;
             }
         }
+        U = Ke;
+        for (int u = tid; u <= U + 1; u += kNT) {
+            rt.gu_off[u] = min(u, U) * GUPER;
+            rt.dn_off[u] = min(u, U) * DNPER + (u > U && P.Is > 0 ? P.groups_sh * DNPER : 0);
+        }
+    } else {
+        const int N = T * K;
+        for (int e = tid; e < E; e += kNT) {
+            s.cnt[e] = 0;
+            s.fill[e] = 0;
+        }
         __syncthreads();
-        for (int x = tid; x < E; x += kNT) sc.fill[x] += sc.chk[x];
+        auto expert_of = [&](int a) -> int { return a < N ? s.sel_i[a] : -1; };  // -1 when not kept
+        for (int a = tid; a < N; a += kNT) {
+            const int e = expert_of(a);
+            if (e >= 0) atomicAdd(&s.cnt[e], 1);
+        }
         __syncthreads();
+        for (int e = tid; e < E; e += kNT) {
+            s.off[e] = s.cnt[e];
+            s.actv[e] = s.cnt[e] > 0 ? 1 : 0;
+            if (out) P.counts[e] = s.cnt[e];
+        }
+        __syncthreads();
+        const int total = scan_smem(s.off, E, s.tmp);
+        U = scan_smem(s.actv, E, s.tmp);
+        for (int e = tid; e < E; e += kNT) {
+            if (out) P.offsets[e] = s.off[e];
+            if (s.cnt[e] > 0) {
+                const int u = s.actv[e];
+                const int g = (s.cnt[e] + P.NV - 1) / P.NV;
+                rt.slot_e[u] = e;
+                rt.slot_n[u] = s.cnt[e];
+                rt.slot_pbase[u] = s.off[e];
+                rt.slot_groups[u] = g;
+                rt.gu_off[u] = g * GUPER;
+                rt.dn_off[u] = g * DNPER;
+                if (out) P.act[u] = e;
+            }
+        }
+        if (tid == 0) {
+            if (out) P.offsets[E] = total;
+            rt.gu_off[U] = 0;
+            rt.dn_off[U] = P.Is > 0 ? P.groups_sh * DNPER : 0;
+        }
+        __syncthreads();
+        const int gu_tot = scan_smem(rt.gu_off, U + 1, s.tmp);
+        const int dn_tot = scan_smem(rt.dn_off, U + 1, s.tmp);
+        if (tid == 0) {
+            rt.gu_off[U + 1] = gu_tot;
+            rt.dn_off[U + 1] = dn_tot;
+        }
+        // stable perm / pos: 256-assignment chunks in order; inside a chunk, rank within the
+        // warp from a match-any mask, then the warps' per-expert counts are scanned
+        for (int a0 = 0; a0 < N; a0 += kNT) {
+            for (int i = tid; i < kNW * E; i += kNT) s.wc[i] = 0;
+            __syncthreads();
+            const int a = a0 + tid;
+            const int e = expert_of(a);
+            const unsigned peers = __match_any_sync(kFull, e);
+            const int rank = __popc(peers & ((1u << lane) - 1u));
+            if (e >= 0 && rank == 0) s.wc[warp * E + e] = __popc(peers);
+            __syncthreads();
+            for (int x = tid; x < E; x += kNT) {
+                int run = 0;
+                for (int w = 0; w < kNW; w++) {
+                    const int v = s.wc[w * E + x];
+                    s.wc[w * E + x] = run;
+                    run += v;
+                }
+                s.chk[x] = run;
+            }
+            __syncthreads();
+            if (a < N) {
+                const int p = e >= 0 ? s.off[e] + s.fill[e] + s.wc[warp * E + e] + rank : -1;
+                if (e >= 0) rt.perm[p] = a;
+                rt.pos[a] = p;
+                if (out) {
+                    if (e >= 0) P.perm[p] = a;
+                    P.pos[a] = p;
+                }
+            }
+            __syncthreads();
+            for (int x = tid; x < E; x += kNT) s.fill[x] += s.chk[x];
+            __syncthreads();
+        }
     }
     if (tid == 0) {
-        __threadfence();
-        atomicExch(&P.ctrl->routing_ready, 1);
+        *rt.U = U;
+        rt.slot_e[U] = -1;  // the shared expert
+        rt.slot_n[U] = T;
+        rt.slot_pbase[U] = 0;
+        rt.slot_groups[U] = P.groups_sh;
     }
+    __syncthreads();
 }
 
-// T <= 8: partial logits of 32 experts (4 per warp) over one slice of H
-__device__ void router_item(const DecParams &P, int item) {
+// T <= 8: partial logits of 32 experts (4 per warp) over one slice of H; each lane keeps two
+// float4 steps of W_r and x loads in flight
+template <int TM>  // tokens handled: P.T <= TM
+__device__ __noinline__ void router_item(const DecParams &P, int item) {
     const int warp = threadIdx.x / kWarp, lane = threadIdx.x % kWarp;
     const int eb = item % P.neb, ks = item / P.neb;
     const int kb = ks * P.rks_floats, ke = min(P.H, kb + P.rks_floats);
-    float acc[4][8];
+    float acc[4][TM];
 #pragma unroll
     for (int r = 0; r < 4; r++)
 #pragma unroll
-        for (int t = 0; t < 8; t++) acc[r][t] = 0.f;
+        for (int t = 0; t < TM; t++) acc[r][t] = 0.f;
     int e[4];
 #pragma unroll
     for (int r = 0; r < 4; r++) e[r] = min(eb * kRtE + warp * 4 + r, P.E - 1);
-    for (int k = kb + 4 * lane; k < ke; k += 4 * kWarp) {
-        float4 wv[4];
+    constexpr int B = 2;
+    for (int k0 = kb + 4 * lane; k0 < ke; k0 += 4 * kWarp * B) {
+        float4 wv[B][4];
 #pragma unroll
-        for (int r = 0; r < 4; r++) {
-            const uint4 u = ld_stream_16(P.Wr + (size_t)e[r] * P.H + k);
-            wv[r] = make_float4(__uint_as_float(u.x), __uint_as_float(u.y), __uint_as_float(u.z), __uint_as_float(u.w));
-        }
-#pragma unroll
-        for (int t = 0; t < 8; t++) {
-            if (t >= P.T) break;
-            const float4 xv = __ldg(reinterpret_cast<const float4 *>(P.x + (size_t)t * P.H + k));
+        for (int b = 0; b < B; b++) {
+            const int k = k0 + b * 4 * kWarp;
 #pragma unroll
             for (int r = 0; r < 4; r++) {
-                float a = acc[r][t];
-                a = fmaf(wv[r].x, xv.x, a);
-                a = fmaf(wv[r].y, xv.y, a);
-                a = fmaf(wv[r].z, xv.z, a);
-                a = fmaf(wv[r].w, xv.w, a);
-                acc[r][t] = a;
+                uint4 u = make_uint4(0, 0, 0, 0);
+                if (k < ke) u = ld_stream_16(P.Wr + (size_t)e[r] * P.H + k);
+                wv[b][r] = make_float4(__uint_as_float(u.x), __uint_as_float(u.y), __uint_as_float(u.z),
+                                       __uint_as_float(u.w));
             }
+        }
+#pragma unroll
+        for (int t = 0; t < TM; t++) {
+            if (t >= P.T) break;
+            float4 xv[B];
+#pragma unroll
+            for (int b = 0; b < B; b++) {
+                const int k = k0 + b * 4 * kWarp;
+                xv[b] = k < ke ? __ldg(reinterpret_cast<const float4 *>(P.x + (size_t)t * P.H + k))
+                               : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+#pragma unroll
+            for (int b = 0; b < B; b++)
+#pragma unroll
+                for (int r = 0; r < 4; r++) {
+                    float a = acc[r][t];
+                    a = fmaf(wv[b][r].x, xv[b].x, a);
+                    a = fmaf(wv[b][r].y, xv[b].y, a);
+                    a = fmaf(wv[b][r].z, xv[b].z, a);
+                    a = fmaf(wv[b][r].w, xv[b].w, a);
+                    acc[r][t] = a;
+                }
         }
     }
 #pragma unroll
     for (int r = 0; r < 4; r++)
 #pragma unroll
-        for (int t = 0; t < 8; t++) {
+        for (int t = 0; t < TM; t++) {
             if (t >= P.T) break;
             float s = acc[r][t];
 #pragma unroll
@@ -501,41 +632,65 @@ __device__ void router_item(const DecParams &P, int item) {
         }
 }
 
-// logits = fixed-order sums of the partials, for flat logit indices [lo, hi) (t-major)
-__device__ void reduce_logits(const DecParams &P, int lo, int hi) {
+// T > 8: logits = fixed-order sums of the partials for flat indices [lo, hi), into slice 0
+__device__ __noinline__ void reduce_logits(const DecParams &P, int lo, int hi) {
     for (int i = lo + (int)threadIdx.x; i < hi; i += kNT) {
+        float a[16];
+#pragma unroll
+        for (int k = 0; k < 16; k++)
+            if (k < P.nks) a[k] = __ldcg(P.part + (size_t)k * P.T * P.E + i);
         float s = 0.f;
-        int k = 0;
-        for (; k + 4 <= P.nks; k += 4) {
-            const float a0 = __ldcg(P.part + (size_t)(k + 0) * P.T * P.E + i);
-            const float a1 = __ldcg(P.part + (size_t)(k + 1) * P.T * P.E + i);
-            const float a2 = __ldcg(P.part + (size_t)(k + 2) * P.T * P.E + i);
-            const float a3 = __ldcg(P.part + (size_t)(k + 3) * P.T * P.E + i);
-            s += a0;
-            s += a1;
-            s += a2;
-            s += a3;
-        }
-        for (; k < P.nks; k++) s += __ldcg(P.part + (size_t)k * P.T * P.E + i);
-        P.sig[i] = s;
+#pragma unroll
+        for (int k = 0; k < 16; k++)
+            if (k < P.nks) s += a[k];
+        P.part[i] = s;  // slice 0, index i: only this thread reads or writes it here
     }
 }
 
 // ------------------------------------------------------------------ expert phases
 struct Seg {  // one segment of units with the same expert and tokens (broadcast in smem)
-    const uint8_t *w0, *w1;  // gate/up rows, or down rows in w0
+    const uint8_t *w0, *w1;  // gate and up rows, or down rows in w0
     const float *s0, *s1;    // their row scales
     int fmt, inter, n, pbase, shared, tg, key, need;
     int ulo, uhi;            // units [ulo, uhi) of this CTA in the segment
-    int ubase;               // unit index of the segment's first unit (row 0)
+    int ubase;               // unit index of the segment's first unit
 };
 
-// stage the activations of token group tg (x rows for gate/up, h rows for down) into xs
-__device__ void stage_acts(const DecParams &P, const Seg &g, bool down, float *xs) {
+// stage the activations of token group tg (x rows for gate/up, h rows for down) into xs. Each
+// thread issues all its float4 loads of a row before it stores any.
+template <int FMT>
+__device__ __forceinline__ void stage_row(const float *__restrict__ src, float *dst, int len, bool coherent) {
+    const int CPR = len / QGeom<FMT>::EPC;
+    const int n4 = len / 4;
+    constexpr int B = 4;
+    for (int q0 = threadIdx.x; q0 < n4; q0 += kNT * B) {
+        float4 v[B];
+#pragma unroll
+        for (int j = 0; j < B; j++) {
+            const int q = q0 + j * kNT;
+            if (q < n4)
+                v[j] = coherent ? __ldcg(reinterpret_cast<const float4 *>(src) + q)
+                                : __ldg(reinterpret_cast<const float4 *>(src) + q);
+        }
+#pragma unroll
+        for (int j = 0; j < B; j++) {
+            const int q = q0 + j * kNT;
+            if (q < n4) {
+                const float e4[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+#pragma unroll
+                for (int u = 0; u < 4; u++) {
+                    float sc;
+                    const int at = staged_index<FMT>(4 * q + u, CPR, sc);
+                    dst[at] = e4[u] * sc;
+                }
+            }
+        }
+    }
+}
+
+__device__ __noinline__ void stage_acts(const DecParams &P, const RTab &rt, const Seg &g, bool down, float *xs) {
     const int nv = min(P.NV, g.n - g.tg * P.NV);
     const int len = down ? g.inter : P.H;
-    const int gran = g.fmt == COLI_FMT_INT4 ? 32 : g.fmt == COLI_FMT_INT8 ? 16 : 64;
-    const int CPR = len / gran;
     for (int v = 0; v < P.NV; v++) {
         float *dst = xs + (size_t)v * P.xs_stride;
         if (v < nv) {
@@ -545,23 +700,19 @@ __device__ void stage_acts(const DecParams &P, const Seg &g, bool down, float *x
                 const int row = g.shared ? P.T * P.K + pv : g.pbase + pv;
                 src = P.h + (size_t)row * P.ldh;
             } else {
-                const int t = g.shared ? pv : __ldcg(P.perm + g.pbase + pv) / P.K;
+                const int t = g.shared ? pv : rt.perm[g.pbase + pv] / P.K;
                 src = P.x + (size_t)t * P.H;
             }
-            for (int i = threadIdx.x; i < len; i += kNT) {
-                float sc;
-                int at;
-                if (g.fmt == COLI_FMT_INT4) at = staged_index<COLI_FMT_INT4>(i, CPR, sc);
-                else if (g.fmt == COLI_FMT_INT8) at = staged_index<COLI_FMT_INT8>(i, CPR, sc);
-                else at = staged_index<COLI_FMT_INT2>(i, CPR, sc);
-                dst[at] = (down ? __ldcg(src + i) : __ldg(src + i)) * sc;
-            }
+            if (g.fmt == COLI_FMT_INT4) stage_row<COLI_FMT_INT4>(src, dst, len, down);
+            else if (g.fmt == COLI_FMT_INT8) stage_row<COLI_FMT_INT8>(src, dst, len, down);
+            else stage_row<COLI_FMT_INT2>(src, dst, len, down);
         } else {
             for (int i = threadIdx.x; i < len; i += kNT) dst[i] = 0.f;
         }
     }
 }
 
+// gate/up: a unit is two row pairs (rows j and j+1 of gate and of up)
 template <int FMT, int NV>
 __device__ void gateup_units(const DecParams &P, const Seg &g, const float *xs) {
     const int warp = threadIdx.x / kWarp, lane = threadIdx.x % kWarp;
@@ -569,29 +720,39 @@ __device__ void gateup_units(const DecParams &P, const Seg &g, const float *xs) 
     const int mine = nu > warp ? (nu - warp + kNW - 1) / kNW : 0;
     const int64_t rb = row_bytes(FMT, P.H);
     const int nv = min(P.NV, g.n - g.tg * P.NV);
-    const int jbase = g.ulo - g.ubase;  // row of the segment's first unit of this CTA
-    warp_stream<FMT, 2, NV>(
+    const int ubase = g.ulo - g.ubase;  // unit of the segment's first unit of this CTA
+    warp_stream<FMT, 4, NV>(
         mine, (int)(rb / 16), xs, P.xs_stride, lane,
-        [&](int i, const uint8_t *(&rr)[2]) {
-            const int j = jbase + warp + kNW * i;
+        [&](int i, const uint8_t *(&rr)[4]) {
+            const int j = 2 * (ubase + warp + kNW * i);
+            const int j1 = min(j + 1, g.inter - 1);
             rr[0] = g.w0 + (size_t)j * rb;
             rr[1] = g.w1 + (size_t)j * rb;
+            rr[2] = g.w0 + (size_t)j1 * rb;
+            rr[3] = g.w1 + (size_t)j1 * rb;
         },
-        [&](int i, const float (&s)[2][NV]) {
-            const int j = jbase + warp + kNW * i;
+        [&](int i, const float (&s)[4][NV]) {
+            const int j = 2 * (ubase + warp + kNW * i);
 #pragma unroll
             for (int v = 0; v < NV; v++) {
                 if (lane == v && v < nv) {
-                    const float gv = s[0][v] * g.s0[j];
-                    const float uv = s[1][v] * g.s1[j];
                     const int pv = g.tg * P.NV + v;
                     const int row = g.shared ? P.T * P.K + pv : g.pbase + pv;
-                    P.h[(size_t)row * P.ldh + j] = gv / (1.f + expf(-gv)) * uv;
+#pragma unroll
+                    for (int q = 0; q < 2; q++) {
+                        const int jq = j + q;
+                        if (jq < g.inter) {
+                            const float gv = s[2 * q][v] * g.s0[jq];
+                            const float uv = s[2 * q + 1][v] * g.s1[jq];
+                            P.h[(size_t)row * P.ldh + jq] = gv / (1.f + expf(-gv)) * uv;
+                        }
+                    }
                 }
             }
         });
 }
 
+// down: a unit is two consecutive rows
 template <int FMT, int NV>
 __device__ void down_units(const DecParams &P, const Seg &g, const float *xs) {
     const int warp = threadIdx.x / kWarp, lane = threadIdx.x % kWarp;
@@ -599,18 +760,24 @@ __device__ void down_units(const DecParams &P, const Seg &g, const float *xs) {
     const int mine = nu > warp ? (nu - warp + kNW - 1) / kNW : 0;
     const int64_t rb = row_bytes(FMT, g.inter);
     const int nv = min(P.NV, g.n - g.tg * P.NV);
-    const int dbase = g.ulo - g.ubase;
-    warp_stream<FMT, 1, NV>(
+    const int ubase = g.ulo - g.ubase;
+    warp_stream<FMT, 2, NV>(
         mine, (int)(rb / 16), xs, P.xs_stride, lane,
-        [&](int i, const uint8_t *(&rr)[1]) { rr[0] = g.w0 + (size_t)(dbase + warp + kNW * i) * rb; },
-        [&](int i, const float (&s)[1][NV]) {
-            const int d = dbase + warp + kNW * i;
+        [&](int i, const uint8_t *(&rr)[2]) {
+            const int d = 2 * (ubase + warp + kNW * i);
+            rr[0] = g.w0 + (size_t)d * rb;
+            rr[1] = g.w0 + (size_t)min(d + 1, P.H - 1) * rb;
+        },
+        [&](int i, const float (&s)[2][NV]) {
+            const int d = 2 * (ubase + warp + kNW * i);
 #pragma unroll
             for (int v = 0; v < NV; v++) {
                 if (lane == v && v < nv) {
                     const int pv = g.tg * P.NV + v;
                     const int row = g.shared ? P.T * P.K + pv : g.pbase + pv;
-                    P.y[(size_t)row * P.H + d] = s[0][v] * g.s0[d];
+#pragma unroll
+                    for (int q = 0; q < 2; q++)
+                        if (d + q < P.H) P.y[(size_t)row * P.H + d + q] = s[q][v] * g.s0[d + q];
                 }
             }
         });
@@ -629,76 +796,83 @@ __device__ void run_units(const DecParams &P, const Seg &g, bool down, const flo
     }
 }
 
-// fill the segment of unit l (thread 0 only): unit spaces are slot-major, then token group,
-// then row; routed slots come from the table, the shared expert is slot U (or the static
-// shared phase when U < 0)
-__device__ void make_seg(const DecParams &P, int slot, int U, int slot_base, int l, int e_share, bool down, Seg &g) {
-    const bool shared = U < 0 || slot == U;
-    const int rows_per_group = down ? P.H : (shared ? P.Is : P.I);
-    if (shared) {
-        g.w0 = static_cast<const uint8_t *>(down ? P.shared.down_w : P.shared.gate_w);
-        g.w1 = static_cast<const uint8_t *>(P.shared.up_w);
-        g.s0 = down ? P.shared.down_s : P.shared.gate_s;
-        g.s1 = P.shared.up_s;
-        g.fmt = P.sfmt;
-        g.inter = P.Is;
-        g.n = P.T;
-        g.pbase = 0;
-        g.key = kSharedKey;
-        g.need = P.G_sh;
-    } else {
-        const int e = __ldcg(&P.tab->slot_e[slot]);
-        const coli_moe_expert ex = P.experts[e];
-        g.w0 = static_cast<const uint8_t *>(down ? ex.down_w : ex.gate_w);
-        g.w1 = static_cast<const uint8_t *>(ex.up_w);
-        g.s0 = down ? ex.down_s : ex.gate_s;
-        g.s1 = ex.up_s;
-        g.fmt = P.rfmt;
-        g.inter = P.I;
-        g.n = __ldcg(&P.tab->slot_n[slot]);
-        g.pbase = __ldcg(&P.tab->slot_pbase[slot]);
-        g.key = slot;
-        g.need = __ldcg(&P.tab->slot_groups[slot]) * P.I;
-        if (bad16(ex.gate_w) || bad16(ex.up_w) || bad16(ex.down_w)) flag_error(P.ctrl, kErrBadExpert);
+// first index i in [0, n) with off[i+1] > x, off in shared memory
+__device__ __forceinline__ int upper_slot_smem(const int *off, int n, int x) {
+    int lo = 0, hi = n - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        if (off[mid + 1] > x) hi = mid;
+        else lo = mid + 1;
     }
-    g.shared = shared ? 1 : 0;
-    const int local = l - slot_base;
-    g.tg = local / rows_per_group;
-    g.ubase = slot_base + g.tg * rows_per_group;
-    g.ulo = l;
-    g.uhi = min(e_share, g.ubase + rows_per_group);
+    return lo;
 }
 
-// walk this CTA's share [b, e) of a unit space (gate/up or down) segment by segment
+// fill the segment of unit l (thread 0 only). Unit spaces run slot by slot, then token group,
+// then unit; shared_phase: the shared expert's gate/up before routing.
+__device__ __noinline__ void make_seg(const DecParams &P, const RTab &rt, int slot, int U, int slot_base, int l,
+                                      int e_share, bool down, bool shared_phase, Seg &g) {
+    const int GUPER = (P.I + 1) / 2, GUPER_SH = (P.Is + 1) / 2, DNPER = (P.H + 1) / 2;
+    const bool shared = shared_phase || slot == U;
+    coli_moe_expert ex;
+    int n, pbase, groups;
+    if (shared) {
+        ex = P.shared;
+        n = P.T;
+        pbase = 0;
+        groups = P.groups_sh;
+    } else {
+        ex = P.experts[rt.slot_e[slot]];
+        n = rt.slot_n[slot];
+        pbase = rt.slot_pbase[slot];
+        groups = rt.slot_groups[slot];
+        if (bad16(ex.gate_w) || bad16(ex.up_w) || bad16(ex.down_w)) flag_error(P.ctrl, kErrBadExpert);
+    }
+    g.w0 = static_cast<const uint8_t *>(down ? ex.down_w : ex.gate_w);
+    g.w1 = static_cast<const uint8_t *>(ex.up_w);
+    g.s0 = down ? ex.down_s : ex.gate_s;
+    g.s1 = ex.up_s;
+    g.fmt = shared ? P.sfmt : P.rfmt;
+    g.inter = shared ? P.Is : P.I;
+    g.n = n;
+    g.pbase = pbase;
+    g.shared = shared ? 1 : 0;
+    g.key = shared ? kSharedKey : slot;
+    g.need = shared ? P.G_sh : groups * GUPER;
+    const int per = down ? DNPER : (shared ? GUPER_SH : GUPER);
+    const int local = l - slot_base;
+    g.tg = local / per;
+    g.ubase = slot_base + g.tg * per;
+    g.ulo = l;
+    g.uhi = min(e_share, g.ubase + per);
+}
+
+// walk this CTA's share [b, e) of a unit space segment by segment; off/nslots: the unit prefix
+// over the slots (shared memory), unused in the shared phase
 template <int NV>
-__device__ void run_share(const DecParams &P, int b, int e, bool down, bool shared_phase, float *xs, Seg *sg,
-                          int *skey) {
+__device__ void run_share(const DecParams &P, const RTab &rt, int b, int e, bool down, bool shared_phase,
+                          const int *off, int nslots, int U, float *xs, Seg *sg, int *skey) {
     const int tid = threadIdx.x;
     if (b >= e) return;
-    int U = -1, slot = 0, slot_base = 0, slot_end = 0, done_in_slot = 0;
-    const int *off = down ? P.tab->dn_off : P.tab->gu_off;
-    if (!shared_phase) U = __ldcg(&P.tab->U);
-    const int nslots = shared_phase ? 1 : (down ? U + (P.Is > 0 ? 1 : 0) : U);
+    int slot = 0, slot_base = 0, slot_end = 0, done_in_slot = 0;
     if (tid == 0) {
         if (shared_phase) {
-            slot_base = 0;
             slot_end = P.G_sh;
         } else {
-            slot = upper_slot(off, nslots, b);
-            slot_base = __ldcg(off + slot);
-            slot_end = __ldcg(off + slot + 1);
+            slot = upper_slot_smem(off, nslots, b);
+            slot_base = off[slot];
+            slot_end = off[slot + 1];
         }
     }
     int l = b;
     while (l < e) {
         __syncthreads();  // the previous segment's units are done with xs and sg
         if (tid == 0) {
-            while (l >= slot_end) {  // next slot (thread 0's cursor)
+            while (l >= slot_end) {
                 slot++;
                 slot_base = slot_end;
-                slot_end = __ldcg(off + slot + 1);
+                slot_end = off[slot + 1];
             }
-            make_seg(P, slot, shared_phase ? -1 : U, slot_base, l, min(e, slot_end), down, *sg);
+            make_seg(P, rt, slot, U, slot_base, l, min(e, slot_end), down, shared_phase, *sg);
             if (down) {  // this expert's h rows must all be written
                 wait_at_least(&P.ctrl->gu_done[sg->key], sg->need, P.ctrl);
                 __threadfence();
@@ -711,7 +885,7 @@ __device__ void run_share(const DecParams &P, int b, int e, bool down, bool shar
         const int k1 = down ? g.key : (P.T == 1 ? 0 : (g.shared ? -1 : g.pbase));
         const int k2 = (P.T == 1 && !down) ? g.fmt : g.tg * 8 + g.fmt;
         if (!(skey[0] == k0 && skey[1] == k1 && skey[2] == k2)) {
-            stage_acts(P, g, down, xs);
+            stage_acts(P, rt, g, down, xs);
             __syncthreads();
             if (tid == 0) {
                 skey[0] = k0;
@@ -740,71 +914,56 @@ template <int NV>
 __global__ void __launch_bounds__(kNT, 2) moe_decode_kernel(const DecParams P) {
     extern __shared__ __align__(128) uint8_t smem[];
     float *xs = reinterpret_cast<float *>(smem);
-    Seg *sg = reinterpret_cast<Seg *>(smem + P.xs_bytes);
+    const RTab rt = rtab_of(smem + P.xs_bytes, P.T, P.E, P.K);
+    Seg *sg = reinterpret_cast<Seg *>(smem + P.xs_bytes + P.rt_bytes);
     int *skey = reinterpret_cast<int *>(sg + 1);
-    int *sflag = skey + 3;
     const int tid = threadIdx.x, G = gridDim.x, c = blockIdx.x;
     if (tid == 0) skey[0] = skey[1] = skey[2] = -1;
 
-    // ---------------- A: routing
+    // ---------------- A: router partial logits
     if (!P.route_only) {
         if (c < P.R) {
-            router_item(P, c);
+            router_item<NV == 1 ? 1 : (NV == 2 ? 2 : 8)>(P, c);
             __syncthreads();
-            const int eb = c % P.neb;
             if (tid == 0) {
                 __threadfence();
-                const bool last = atomicAdd(&P.ctrl->eb_done[eb], 1) == P.nks - 1;
-                if (last) __threadfence();
-                *sflag = last;
+                atomicAdd(&P.ctrl->router_done, 1);
             }
-            __syncthreads();
-            if (*sflag) {  // last k-slice of this expert block: its logits
-                const int e0 = eb * kRtE, e1 = min(P.E, e0 + kRtE);
-                for (int t = 0; t < P.T; t++) reduce_logits(P, t * P.E + e0, t * P.E + e1);
-                __syncthreads();
-                if (tid == 0) {
-                    __threadfence();
-                    const bool last = atomicAdd(&P.ctrl->router_done, 1) == P.neb - 1;
-                    if (last) __threadfence();
-                    *sflag = last;
-                }
-                __syncthreads();
-                if (*sflag) route_final(P, xs);
-            }
-            __syncthreads();
         }
     } else {
         reduce_logits(P, range_lo(P.T * P.E, c, G), range_lo(P.T * P.E, c + 1, G));
         __syncthreads();
         if (tid == 0) {
             __threadfence();
-            const bool last = atomicAdd(&P.ctrl->router_done, 1) == G - 1;
-            if (last) __threadfence();
-            *sflag = last;
+            atomicAdd(&P.ctrl->router_done, 1);
         }
-        __syncthreads();
-        if (*sflag) route_final(P, xs);
-        __syncthreads();
     }
-    if (tid == 0) skey[0] = -1;  // xs may have served as routing scratch
 
     // ---------------- B: the shared expert's gate/up (independent of routing)
-    if (P.Is > 0) run_share<NV>(P, range_lo(P.G_sh, c, G), range_lo(P.G_sh, c + 1, G), false, true, xs, sg, skey);
+    if (P.Is > 0)
+        run_share<NV>(P, rt, range_lo(P.G_sh, c, G), range_lo(P.G_sh, c + 1, G), false, true, nullptr, 0, -1, xs,
+                      sg, skey);
 
-    // ---------------- C: routed gate/up
+    // ---------------- R: routing, by this CTA for itself
     if (tid == 0) {
-        wait_at_least(&P.ctrl->routing_ready, 1, P.ctrl);
+        wait_at_least(&P.ctrl->router_done, P.route_only ? G : P.R, P.ctrl);
         __threadfence();
+        skey[0] = -1;  // xs becomes routing scratch
     }
     __syncthreads();
-    const int gu_tot = __ldcg(&P.tab->gu_tot);
-    run_share<NV>(P, range_lo(gu_tot, c, G), range_lo(gu_tot, c + 1, G), false, false, xs, sg, skey);
+    route_local(P, xs, rt, !P.route_only);
+    const int U = *rt.U;
+
+    // ---------------- C: routed gate/up
+    const int gu_tot = rt.gu_off[U];
+    run_share<NV>(P, rt, range_lo(gu_tot, c, G), range_lo(gu_tot, c + 1, G), false, false, rt.gu_off, U, U, xs, sg,
+                  skey);
 
     // ---------------- D: down rows of every expert
-    const int dn_tot = __ldcg(&P.tab->dn_tot);
+    const int nslots = U + (P.Is > 0 ? 1 : 0);
+    const int dn_tot = rt.dn_off[nslots];
     const int db = range_lo(dn_tot, c, G), de = range_lo(dn_tot, c + 1, G);
-    run_share<NV>(P, db, de, true, false, xs, sg, skey);
+    run_share<NV>(P, rt, db, de, true, false, rt.dn_off, nslots, U, xs, sg, skey);
     if (tid == 0) {
         __threadfence();
         atomicAdd(&P.ctrl->dn_done, de - db);
@@ -819,13 +978,10 @@ __global__ void __launch_bounds__(kNT, 2) moe_decode_kernel(const DecParams P) {
     const int r_lo = range_lo(P.H, c, G), r_hi = range_lo(P.H, c + 1, G), nd = r_hi - r_lo;
     for (int i = tid; i < P.T * nd; i += kNT) {
         const int t = i / nd, d = r_lo + i % nd;
-        const int ke = __ldcg(P.keff + t);
+        const int ke = rt.keff[t];
         float a = 0.f;
-        for (int k = 0; k < ke; k++) {
-            const float wk = __ldcg(P.w + (size_t)t * P.K + k);
-            const int p = __ldcg(P.pos + (size_t)t * P.K + k);
-            a = __fadd_rn(a, __fmul_rn(wk, __ldcg(P.y + (size_t)p * P.H + d)));
-        }
+        for (int k = 0; k < ke; k++)
+            a = __fadd_rn(a, __fmul_rn(rt.w[t * P.K + k], __ldcg(P.y + (size_t)rt.pos[t * P.K + k] * P.H + d)));
         if (P.Is > 0) a = __fadd_rn(a, __ldcg(P.y + ((size_t)P.T * P.K + t) * P.H + d));
         P.out[(size_t)t * P.H + d] = a;
     }
@@ -834,9 +990,8 @@ __global__ void __launch_bounds__(kNT, 2) moe_decode_kernel(const DecParams P) {
 }  // namespace
 
 size_t decode_ctrl_bytes() { return sizeof(DecCtrl); }
-size_t decode_table_bytes() { return sizeof(DecTable); }
 
-size_t decode_smem_bytes(const DecParams &P) { return (size_t)P.xs_bytes + sizeof(Seg) + 64; }
+size_t decode_smem_bytes(const DecParams &P) { return (size_t)P.xs_bytes + P.rt_bytes + sizeof(Seg) + 64; }
 
 // Host-side geometry of the decode launch for a grid of `grid` CTAs.
 bool decode_plan(const coli_moe_desc &d, DecParams &P, int grid) {
@@ -845,8 +1000,9 @@ bool decode_plan(const coli_moe_desc &d, DecParams &P, int grid) {
     const int maxdim = std::max(d.H, std::max(d.I, d.I_shared));
     P.xs_stride = maxdim;
     const size_t xs_vec = (size_t)P.NV * maxdim * sizeof(float);
-    const size_t scratch = (size_t)(5 * d.E + kNW * d.E + 16 + 2 * T * d.K + T + 2 * (d.E + 2) + 16) * sizeof(int);
+    const size_t scratch = rscratch_bytes(T, d.E, d.K);
     P.xs_bytes = (int)align_up(std::max(xs_vec, scratch), 128);
+    P.rt_bytes = (int)align_up(rtab_bytes(T, d.E, d.K), 128);
     P.route_only = T <= 8 ? 0 : 1;
     P.neb = (d.E + kRtE - 1) / kRtE;
     if (!P.route_only) {
@@ -862,7 +1018,7 @@ bool decode_plan(const coli_moe_desc &d, DecParams &P, int grid) {
         P.R = 0;  // P.nks is the separate router launch's split count
     }
     P.groups_sh = d.I_shared > 0 ? (T + P.NV - 1) / P.NV : 0;
-    P.G_sh = d.I_shared > 0 ? P.groups_sh * d.I_shared : 0;
+    P.G_sh = d.I_shared > 0 ? P.groups_sh * ((d.I_shared + 1) / 2) : 0;
     return decode_smem_bytes(P) <= 113u * 1024;
 }
 

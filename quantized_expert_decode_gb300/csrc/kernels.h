@@ -29,22 +29,9 @@ constexpr int kDecMaxT = 64;              // the persistent decode kernel serves
 // Counters of one decode call (zeroed before each launch; err stays the first word, which is
 // also the workspace error word read by coli_moe_check).
 struct DecCtrl {
-    int err, router_done, routing_ready, dn_done;
-    int pad[12];
-    int eb_done[32];                   // finished router k-slices per 32-expert block
+    int err, router_done, dn_done;
+    int pad[13];
     int gu_done[kMaxE + 1];            // finished gate/up units per slot (shared: index kMaxE)
-};
-
-// Unit table published by the routing CTA: slot u < U is the u-th active expert (ascending
-// id), slot U the shared expert.
-struct DecTable {
-    int U, gu_tot, dn_tot, pad[5];
-    int slot_e[kMaxE + 1];
-    int slot_n[kMaxE + 1];
-    int slot_pbase[kMaxE + 1];
-    int slot_groups[kMaxE + 1];
-    int gu_off[kMaxE + 2];             // gate/up units before slot u (routed slots)
-    int dn_off[kMaxE + 2];             // down units before slot u (routed slots, then shared)
 };
 
 struct DecParams {
@@ -52,16 +39,15 @@ struct DecParams {
     const coli_moe_expert *experts;
     coli_moe_expert shared;
     float *out;
-    float *part;               // router partial logits [nks][T][E]
-    float *sig, *choice, *w;   // sig holds the logits until the selection turns them into scores
+    float *part;               // router partial logits [nks][T][E] (T > 8: slice 0 = logits)
+    float *sig, *choice, *w;
     int32_t *idx, *keff, *counts, *offsets, *perm, *pos, *act;
     float *h, *y;
     DecCtrl *ctrl;
-    DecTable *tab;
     int T, H, I, E, K, Is, rfmt, sfmt, Ksel, norm_topk;
     float top_p, rscale;
     int ldh;
-    int NV, xs_stride, xs_bytes;
+    int NV, xs_stride, xs_bytes, rt_bytes;
     int R, route_only;         // router items; route_only: logits come from a separate launch
     int neb, nks, rks_floats;  // router expert blocks, k-slices, floats per k-slice
     int groups_sh, G_sh;       // shared expert token groups and gate/up units

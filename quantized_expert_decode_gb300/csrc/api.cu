@@ -176,14 +176,24 @@ int run_forward_decode(const coli_moe_desc *d, const float *x, const float *W_r,
         (e = launch_router_partial(x, W_r, P.part, d->T, d->H, d->E, splits, st)) != cudaSuccess)
         return cuda_fail(e);
     if ((rc = record(events, 1, st))) return rc;
-    if ((e = launch_decode(P, grid, st)) != cudaSuccess) return cuda_fail(e);
+    if ((e = P.single ? launch_decode1(P, grid, st) : launch_decode(P, grid, st)) != cudaSuccess) return cuda_fail(e);
     if ((rc = record(events, 2, st))) return rc;
     if ((rc = record(events, 3, st))) return rc;
     return record(events, 4, st);
 }
 
-// the persistent decode kernel's plan and grid for this description (false: not applicable)
+// the persistent decode kernel's plan and grid for this description (false: not applicable):
+// the single-token kernel for T = 1 when its shared memory fits, else the token-group kernel
 bool decode_plan_for(const coli_moe_desc &d, DecParams &P, int &grid) {
+    const int sms0 = num_sms();
+    for (int per_sm = 2; per_sm >= 1 && d.T == 1; per_sm--) {
+        DecParams Q{};
+        grid = per_sm * sms0;
+        if (decode1_plan(d, Q, grid) && decode1_ctas_per_sm(Q) >= per_sm) {
+            P = Q;
+            return true;
+        }
+    }
     if (!decode_supported(d)) return false;
     const int sms = num_sms();
     grid = 2 * sms;

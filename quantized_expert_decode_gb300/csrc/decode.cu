@@ -24,140 +24,11 @@
 // records kErrWaitExpired and carries on, so a fault in the schedule can not hang the GPU.
 #include <algorithm>
 
-#include "kernels.h"
-#include "ptx.cuh"
-#include "qdot.cuh"
+#include "decode_parts.cuh"
 
 namespace colimoe {
 
 namespace {
-
-constexpr int kNT = 256;                 // threads per CTA
-constexpr int kNW = kNT / kWarp;         // warps per CTA
-constexpr int kRtE = 32;                 // experts per router item (4 per warp)
-constexpr int kInflight = 8;             // 16-byte loads in flight per lane (rows x depth)
-constexpr unsigned long long kWaitNs = 2000000000ull;
-constexpr int kSharedKey = kMaxE;        // gu_done index of the shared expert
-
-__device__ __forceinline__ void flag_error(DecCtrl *c, int code) { atomicCAS(&c->err, 0, code); }
-
-// bounded wait until *p >= target; false (and flagged) on timeout
-__device__ bool wait_at_least(const int *p, int target, DecCtrl *c) {
-    if (ld_volatile(p) >= target) return true;
-    const uint64_t t0 = globaltimer_ns();
-    while (ld_volatile(p) < target) {
-        __nanosleep(64);
-        if (globaltimer_ns() - t0 > kWaitNs) {
-            flag_error(c, kErrWaitExpired);
-            return false;
-        }
-    }
-    return true;
-}
-
-__device__ __forceinline__ int range_lo(int n, int c, int G) { return (int)((long long)n * c / G); }
-
-// first index i in [0, n) with off[i+1] > x (off: nondecreasing prefix array, off[0] = 0)
-__device__ int upper_slot(const int *off, int n, int x) {
-    int lo = 0, hi = n - 1;
-    while (lo < hi) {
-        const int mid = (lo + hi) >> 1;
-        if (__ldcg(off + mid + 1) > x) hi = mid;
-        else lo = mid + 1;
-    }
-    return lo;
-}
-
-__device__ __forceinline__ bool bad16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) != 0; }
-
-// ------------------------------------------------------------------ the streaming core
-// One warp streams `nunits` units of NR packed rows each (CPR 16-byte chunks per row), lane l
-// taking chunks l, l+32, ... of every row, with kDepth chunk-steps of loads in flight across unit
-// boundaries (kInflight / NR steps). rows_of(i, rows) gives unit i's row pointers; epi(i, sums) gets the finished
-// warp-reduced dot products with the NV staged vectors.
-template <int FMT, int NR, int NV, class RowsOf, class Epi>
-__device__ __forceinline__ void warp_stream(int nunits, int CPR, const float *xs, int xstride, int lane,
-                                            RowsOf rows_of, Epi epi) {
-    using G = QGeom<FMT>;
-    constexpr int kDepth = kInflight / NR;  // chunk-steps in flight
-    if (nunits <= 0) return;
-    const int S = (CPR + kWarp - 1) / kWarp;  // steps per unit
-    const int total = nunits * S;
-    uint4 buf[kDepth][NR];
-    int iu = 0, ik = 0;  // issue cursor: unit, step within unit
-    auto issue = [&](uint4 (&b)[NR]) {
-        if (iu < nunits) {
-            const int c = lane + kWarp * ik;
-            const uint8_t *rr[NR];
-            rows_of(iu, rr);
-#pragma unroll
-            for (int r = 0; r < NR; r++) b[r] = c < CPR ? ld_stream_16(rr[r] + 16 * c) : make_uint4(0, 0, 0, 0);
-            if (++ik == S) {
-                ik = 0;
-                iu++;
-            }
-        }
-    };
-#pragma unroll
-    for (int j = 0; j < kDepth; j++) issue(buf[j]);
-    float2 acc[NR][NV];
-#pragma unroll
-    for (int r = 0; r < NR; r++)
-#pragma unroll
-        for (int v = 0; v < NV; v++) acc[r][v] = make_float2(0.f, 0.f);
-    const float4 *xs4 = reinterpret_cast<const float4 *>(xs);
-    const int xstride4 = xstride / 4;
-    int cu = 0, ck = 0;  // compute cursor
-    for (int s0 = 0; s0 < total; s0 += kDepth) {
-#pragma unroll
-        for (int j = 0; j < kDepth; j++) {
-            if (s0 + j < total) {
-                const int c = lane + kWarp * ck;
-                if (c < CPR) {
-#pragma unroll
-                    for (int wi = 0; wi < 4; wi++) {
-                        float4 xv[NV][G::F4W];
-#pragma unroll
-                        for (int v = 0; v < NV; v++)
-#pragma unroll
-                            for (int q = 0; q < G::F4W; q++)
-                                xv[v][q] = xs4[v * xstride4 + (wi * G::F4W + q) * CPR + c];
-#pragma unroll
-                        for (int r = 0; r < NR; r++) {
-                            const uint32_t w = word_of(buf[j][r], wi);
-                            const uint32_t wh = w >> 16;
-#pragma unroll
-                            for (int m = 0; m < G::HALF; m++) {
-                                const uint32_t lo = lop3_and_xor(w, G::mask(m), G::xorv(m));
-                                const uint32_t hi = lop3_and_xor(wh, G::mask(m), G::xorv(m));
-                                const float2 d = __fadd2_rn(make_float2(__uint_as_float(lo), __uint_as_float(hi)),
-                                                            make_float2(-G::magic(m), -G::magic(m)));
-#pragma unroll
-                                for (int v = 0; v < NV; v++) {
-                                    const float4 &x4 = xv[v][m >> 1];
-                                    const float2 x2 = (m & 1) ? make_float2(x4.z, x4.w) : make_float2(x4.x, x4.y);
-                                    acc[r][v] = __ffma2_rn(d, x2, acc[r][v]);
-                                }
-                            }
-                        }
-                    }
-                }
-                issue(buf[j]);
-                if (++ck == S) {
-                    float sums[NR][NV];
-                    warp_reduce_acc<NR, NV>(acc, sums);
-                    epi(cu, sums);
-#pragma unroll
-                    for (int r = 0; r < NR; r++)
-#pragma unroll
-                        for (int v = 0; v < NV; v++) acc[r][v] = make_float2(0.f, 0.f);
-                    ck = 0;
-                    cu++;
-                }
-            }
-        }
-    }
-}
 
 // ------------------------------------------------------------------ routing
 // This CTA's copy of the routing result (shared memory, alive until the kernel ends).
@@ -432,7 +303,7 @@ __device__ __noinline__ void route_local(const DecParams &P, float *scratch, con
     }
     __syncthreads();
     // 4. buckets and the unit tables (slot u < U: u-th active expert, ascending id; U: shared)
-    const int GUPER = (P.I + 1) / 2, DNPER = (P.H + 1) / 2;
+    const int GUPER = (P.I + 1) / 2, DNPER = (P.H + 3) / 4;
     int U;
     if (T == 1) {  // one token: its kept experts are distinct
         const int Ke = rt.keff[0];
@@ -567,160 +438,140 @@ __device__ __noinline__ void route_local(const DecParams &P, float *scratch, con
     __syncthreads();
 }
 
-// T <= 8: partial logits of 32 experts (4 per warp) over one slice of H; each lane keeps two
-// float4 steps of W_r and x loads in flight
-template <int TM>  // tokens handled: P.T <= TM
-__device__ __noinline__ void router_item(const DecParams &P, int item) {
-    const int warp = threadIdx.x / kWarp, lane = threadIdx.x % kWarp;
-    const int eb = item % P.neb, ks = item / P.neb;
-    const int kb = ks * P.rks_floats, ke = min(P.H, kb + P.rks_floats);
-    float acc[4][TM];
-#pragma unroll
-    for (int r = 0; r < 4; r++)
-#pragma unroll
-        for (int t = 0; t < TM; t++) acc[r][t] = 0.f;
-    int e[4];
-#pragma unroll
-    for (int r = 0; r < 4; r++) e[r] = min(eb * kRtE + warp * 4 + r, P.E - 1);
-    constexpr int B = 2;
-    for (int k0 = kb + 4 * lane; k0 < ke; k0 += 4 * kWarp * B) {
-        float4 wv[B][4];
-#pragma unroll
-        for (int b = 0; b < B; b++) {
-            const int k = k0 + b * 4 * kWarp;
-#pragma unroll
-            for (int r = 0; r < 4; r++) {
-                uint4 u = make_uint4(0, 0, 0, 0);
-                if (k < ke) u = ld_stream_16(P.Wr + (size_t)e[r] * P.H + k);
-                wv[b][r] = make_float4(__uint_as_float(u.x), __uint_as_float(u.y), __uint_as_float(u.z),
-                                       __uint_as_float(u.w));
-            }
-        }
-#pragma unroll
-        for (int t = 0; t < TM; t++) {
-            if (t >= P.T) break;
-            float4 xv[B];
-#pragma unroll
-            for (int b = 0; b < B; b++) {
-                const int k = k0 + b * 4 * kWarp;
-                xv[b] = k < ke ? __ldg(reinterpret_cast<const float4 *>(P.x + (size_t)t * P.H + k))
-                               : make_float4(0.f, 0.f, 0.f, 0.f);
-            }
-#pragma unroll
-            for (int b = 0; b < B; b++)
-#pragma unroll
-                for (int r = 0; r < 4; r++) {
-                    float a = acc[r][t];
-                    a = fmaf(wv[b][r].x, xv[b].x, a);
-                    a = fmaf(wv[b][r].y, xv[b].y, a);
-                    a = fmaf(wv[b][r].z, xv[b].z, a);
-                    a = fmaf(wv[b][r].w, xv[b].w, a);
-                    acc[r][t] = a;
-                }
-        }
-    }
-#pragma unroll
-    for (int r = 0; r < 4; r++)
-#pragma unroll
-        for (int t = 0; t < TM; t++) {
-            if (t >= P.T) break;
-            float s = acc[r][t];
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(kFull, s, o);
-            const int er = eb * kRtE + warp * 4 + r;
-            if (lane == 0 && er < P.E) P.part[((size_t)ks * P.T + t) * P.E + er] = s;
-        }
-}
-
-// T > 8: logits = fixed-order sums of the partials for flat indices [lo, hi), into slice 0
-__device__ __noinline__ void reduce_logits(const DecParams &P, int lo, int hi) {
-    for (int i = lo + (int)threadIdx.x; i < hi; i += kNT) {
-        float a[16];
-#pragma unroll
-        for (int k = 0; k < 16; k++)
-            if (k < P.nks) a[k] = __ldcg(P.part + (size_t)k * P.T * P.E + i);
-        float s = 0.f;
-#pragma unroll
-        for (int k = 0; k < 16; k++)
-            if (k < P.nks) s += a[k];
-        P.part[i] = s;  // slice 0, index i: only this thread reads or writes it here
-    }
-}
-
 // ------------------------------------------------------------------ expert phases
-struct Seg {  // one segment of units with the same expert and tokens (broadcast in smem)
+constexpr int kScCap = 64;  // units per segment piece: their row scales are staged in smem
+
+struct Seg {  // one segment piece: units of one expert and token group (broadcast in smem)
     const uint8_t *w0, *w1;  // gate and up rows, or down rows in w0
     const float *s0, *s1;    // their row scales
-    int fmt, inter, n, pbase, shared, tg, key, need;
-    int ulo, uhi;            // units [ulo, uhi) of this CTA in the segment
-    int ubase;               // unit index of the segment's first unit
+    int fmt, inter, n, pbase, shared, tg, key, need, nv;
+    int ulo, uhi;            // units [ulo, uhi) of this CTA in the piece
+    int ubase;               // unit index of the token group's first unit
 };
 
-// stage the activations of token group tg (x rows for gate/up, h rows for down) into xs. Each
-// thread issues all its float4 loads of a row before it stores any.
+// per-CTA scratch next to the staged activations and the routing tables
+struct Misc {
+    Seg sg;
+    int skey[4];
+    int xshift;               // integer core: X = round(x * 2^xshift)
+    float xinv;               // 2^-xshift
+    float redf[kNW];
+    float sc[2][4 * kScCap];  // row scales of the piece's units (gate/up: gate, up; down: [0])
+};
+
+// One vector in 24-bit block fixed point for the integer core (idot.cuh); leaves s and 2^-s in
+// m (published by the caller's next barrier).
 template <int FMT>
-__device__ __forceinline__ void stage_row(const float *__restrict__ src, float *dst, int len, bool coherent) {
-    const int CPR = len / QGeom<FMT>::EPC;
-    const int n4 = len / 4;
+__device__ void stage_limbs(const float *__restrict__ src, int len, bool coherent, uint8_t *xq, Misc &m) {
+    const int tid = threadIdx.x, lane = tid % kWarp, warp = tid / kWarp;
+    const int CPR = len / QGeom<FMT>::EPC, n4 = len / 4;
     constexpr int B = 4;
-    for (int q0 = threadIdx.x; q0 < n4; q0 += kNT * B) {
+    float mx = 0.f;
+    for (int q0 = tid; q0 < n4; q0 += kNT * B) {
         float4 v[B];
 #pragma unroll
         for (int j = 0; j < B; j++) {
             const int q = q0 + j * kNT;
-            if (q < n4)
-                v[j] = coherent ? __ldcg(reinterpret_cast<const float4 *>(src) + q)
-                                : __ldg(reinterpret_cast<const float4 *>(src) + q);
+            if (q < n4) v[j] = ld_act4(src, q, coherent);
         }
 #pragma unroll
-        for (int j = 0; j < B; j++) {
-            const int q = q0 + j * kNT;
-            if (q < n4) {
-                const float e4[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+        for (int j = 0; j < B; j++)
+            if (q0 + j * kNT < n4)
+                mx = fmaxf(mx, fmaxf(fmaxf(fabsf(v[j].x), fabsf(v[j].y)), fmaxf(fabsf(v[j].z), fabsf(v[j].w))));
+    }
 #pragma unroll
-                for (int u = 0; u < 4; u++) {
-                    float sc;
-                    const int at = staged_index<FMT>(4 * q + u, CPR, sc);
-                    dst[at] = e4[u] * sc;
-                }
-            }
-        }
+    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, o));
+    if (lane == 0) m.redf[warp] = mx;
+    __syncthreads();
+    mx = m.redf[0];
+#pragma unroll
+    for (int w = 1; w < kNW; w++) mx = fmaxf(mx, m.redf[w]);
+    const int s = fixed_shift(mx);
+    stage_limbs_vec<FMT>(src, len, coherent, xq, FixedScale(s), tid, kNT);
+    if (tid == 0) {
+        m.xshift = s;
+        m.xinv = ldexpf(1.f, -s);
     }
 }
 
-__device__ __noinline__ void stage_acts(const DecParams &P, const RTab &rt, const Seg &g, bool down, float *xs) {
-    const int nv = min(P.NV, g.n - g.tg * P.NV);
+__device__ __noinline__ void stage_acts(const DecParams &P, const RTab &rt, const Seg &g, bool down, void *xs,
+                                        Misc &m) {
     const int len = down ? g.inter : P.H;
+    auto src_of = [&](int v) -> const float * {
+        const int pv = g.tg * P.NV + v;
+        if (down) {
+            const int row = g.shared ? P.T * P.K + pv : g.pbase + pv;
+            return P.h + (size_t)row * P.ldh;
+        }
+        const int t = g.shared ? pv : rt.perm[g.pbase + pv] / P.K;
+        return P.x + (size_t)t * P.H;
+    };
+    if (g.nv == 1) {
+        uint8_t *xq = static_cast<uint8_t *>(xs);
+        if (g.fmt == COLI_FMT_INT4) stage_limbs<COLI_FMT_INT4>(src_of(0), len, down, xq, m);
+        else if (g.fmt == COLI_FMT_INT8) stage_limbs<COLI_FMT_INT8>(src_of(0), len, down, xq, m);
+        else stage_limbs<COLI_FMT_INT2>(src_of(0), len, down, xq, m);
+        return;
+    }
+    float *xf = static_cast<float *>(xs);
     for (int v = 0; v < P.NV; v++) {
-        float *dst = xs + (size_t)v * P.xs_stride;
-        if (v < nv) {
-            const int pv = g.tg * P.NV + v;
-            const float *src;
-            if (down) {
-                const int row = g.shared ? P.T * P.K + pv : g.pbase + pv;
-                src = P.h + (size_t)row * P.ldh;
-            } else {
-                const int t = g.shared ? pv : rt.perm[g.pbase + pv] / P.K;
-                src = P.x + (size_t)t * P.H;
-            }
-            if (g.fmt == COLI_FMT_INT4) stage_row<COLI_FMT_INT4>(src, dst, len, down);
-            else if (g.fmt == COLI_FMT_INT8) stage_row<COLI_FMT_INT8>(src, dst, len, down);
-            else stage_row<COLI_FMT_INT2>(src, dst, len, down);
+        float *dst = xf + (size_t)v * P.xs_stride;
+        if (v < g.nv) {
+            if (g.fmt == COLI_FMT_INT4) stage_row<COLI_FMT_INT4>(src_of(v), dst, len, down);
+            else if (g.fmt == COLI_FMT_INT8) stage_row<COLI_FMT_INT8>(src_of(v), dst, len, down);
+            else stage_row<COLI_FMT_INT2>(src_of(v), dst, len, down);
         } else {
             for (int i = threadIdx.x; i < len; i += kNT) dst[i] = 0.f;
         }
     }
 }
 
+// h or y row of token v of the piece's group
+__device__ __forceinline__ int act_row(const DecParams &P, const Seg &g, int v) {
+    const int pv = g.tg * P.NV + v;
+    return g.shared ? P.T * P.K + pv : g.pbase + pv;
+}
+
 // gate/up: a unit is two row pairs (rows j and j+1 of gate and of up)
-template <int FMT, int NV>
-__device__ void gateup_units(const DecParams &P, const Seg &g, const float *xs) {
+template <int FMT>
+__device__ void gateup_units_int(const DecParams &P, const Seg &g, const void *xs, const Misc &m) {
     const int warp = threadIdx.x / kWarp, lane = threadIdx.x % kWarp;
     const int nu = g.uhi - g.ulo;
     const int mine = nu > warp ? (nu - warp + kNW - 1) / kNW : 0;
     const int64_t rb = row_bytes(FMT, P.H);
-    const int nv = min(P.NV, g.n - g.tg * P.NV);
-    const int ubase = g.ulo - g.ubase;  // unit of the segment's first unit of this CTA
+    const int ubase = g.ulo - g.ubase;
+    const float xinv = m.xinv;
+    float *hrow = P.h + (size_t)act_row(P, g, 0) * P.ldh;
+    warp_stream_int<FMT, 4>(
+        mine, (int)(rb / 16), lane,
+        [&](int i, const uint8_t *(&rr)[4]) {
+            const int j = 2 * (ubase + warp + kNW * i);
+            const int j1 = min(j + 1, g.inter - 1);
+            rr[0] = g.w0 + (size_t)j * rb;
+            rr[1] = g.w1 + (size_t)j * rb;
+            rr[2] = g.w0 + (size_t)j1 * rb;
+            rr[3] = g.w1 + (size_t)j1 * rb;
+        },
+        [&](int) { return static_cast<const uint4 *>(xs); }, [](int) { return 0; },
+        [&](int i, const long long (&s)[4], int) {
+            const int lj = 2 * (warp + kNW * i) + lane;  // row within the piece's scales
+            const int jq = 2 * ubase + lj;
+            if (lane < 2 && jq < g.inter) {
+                const long long sg = lane ? s[2] : s[0], su = lane ? s[3] : s[1];
+                const float gv = (__ll2float_rn(sg) * xinv) * m.sc[0][lj];
+                const float uv = (__ll2float_rn(su) * xinv) * m.sc[1][lj];
+                hrow[jq] = gv / (1.f + expf(-gv)) * uv;
+            }
+        });
+}
+
+template <int FMT, int NV>
+__device__ void gateup_units_flt(const DecParams &P, const Seg &g, const float *xs, const Misc &m) {
+    const int warp = threadIdx.x / kWarp, lane = threadIdx.x % kWarp;
+    const int nu = g.uhi - g.ulo;
+    const int mine = nu > warp ? (nu - warp + kNW - 1) / kNW : 0;
+    const int64_t rb = row_bytes(FMT, P.H);
+    const int ubase = g.ulo - g.ubase;
     warp_stream<FMT, 4, NV>(
         mine, (int)(rb / 16), xs, P.xs_stride, lane,
         [&](int i, const uint8_t *(&rr)[4]) {
@@ -732,19 +583,18 @@ __device__ void gateup_units(const DecParams &P, const Seg &g, const float *xs) 
             rr[3] = g.w1 + (size_t)j1 * rb;
         },
         [&](int i, const float (&s)[4][NV]) {
-            const int j = 2 * (ubase + warp + kNW * i);
+            const int lj = 2 * (warp + kNW * i);
+            const int j = 2 * ubase + lj;
 #pragma unroll
             for (int v = 0; v < NV; v++) {
-                if (lane == v && v < nv) {
-                    const int pv = g.tg * P.NV + v;
-                    const int row = g.shared ? P.T * P.K + pv : g.pbase + pv;
+                if (lane == v && v < g.nv) {
+                    float *hrow = P.h + (size_t)act_row(P, g, v) * P.ldh;
 #pragma unroll
                     for (int q = 0; q < 2; q++) {
-                        const int jq = j + q;
-                        if (jq < g.inter) {
-                            const float gv = s[2 * q][v] * g.s0[jq];
-                            const float uv = s[2 * q + 1][v] * g.s1[jq];
-                            P.h[(size_t)row * P.ldh + jq] = gv / (1.f + expf(-gv)) * uv;
+                        if (j + q < g.inter) {
+                            const float gv = s[2 * q][v] * m.sc[0][lj + q];
+                            const float uv = s[2 * q + 1][v] * m.sc[1][lj + q];
+                            hrow[j + q] = gv / (1.f + expf(-gv)) * uv;
                         }
                     }
                 }
@@ -752,47 +602,88 @@ __device__ void gateup_units(const DecParams &P, const Seg &g, const float *xs) 
         });
 }
 
-// down: a unit is two consecutive rows
-template <int FMT, int NV>
-__device__ void down_units(const DecParams &P, const Seg &g, const float *xs) {
+// down: a unit is four consecutive rows
+template <int FMT>
+__device__ void down_units_int(const DecParams &P, const Seg &g, const void *xs, const Misc &m) {
     const int warp = threadIdx.x / kWarp, lane = threadIdx.x % kWarp;
     const int nu = g.uhi - g.ulo;
     const int mine = nu > warp ? (nu - warp + kNW - 1) / kNW : 0;
     const int64_t rb = row_bytes(FMT, g.inter);
-    const int nv = min(P.NV, g.n - g.tg * P.NV);
     const int ubase = g.ulo - g.ubase;
-    warp_stream<FMT, 2, NV>(
-        mine, (int)(rb / 16), xs, P.xs_stride, lane,
-        [&](int i, const uint8_t *(&rr)[2]) {
-            const int d = 2 * (ubase + warp + kNW * i);
-            rr[0] = g.w0 + (size_t)d * rb;
-            rr[1] = g.w0 + (size_t)min(d + 1, P.H - 1) * rb;
+    const float xinv = m.xinv;
+    float *yrow = P.y + (size_t)act_row(P, g, 0) * P.H;
+    warp_stream_int<FMT, 4>(
+        mine, (int)(rb / 16), lane,
+        [&](int i, const uint8_t *(&rr)[4]) {
+            const int d = 4 * (ubase + warp + kNW * i);
+#pragma unroll
+            for (int q = 0; q < 4; q++) rr[q] = g.w0 + (size_t)min(d + q, P.H - 1) * rb;
         },
-        [&](int i, const float (&s)[2][NV]) {
-            const int d = 2 * (ubase + warp + kNW * i);
+        [&](int) { return static_cast<const uint4 *>(xs); }, [](int) { return 0; },
+        [&](int i, const long long (&s)[4], int) {
+            const int ld = 4 * (warp + kNW * i) + lane;
+            const int d = 4 * ubase + ld;
+            if (lane < 4 && d < P.H) {
+                const long long sv = lane == 0 ? s[0] : lane == 1 ? s[1] : lane == 2 ? s[2] : s[3];
+                yrow[d] = (__ll2float_rn(sv) * xinv) * m.sc[0][ld];
+            }
+        });
+}
+
+template <int FMT, int NV>
+__device__ void down_units_flt(const DecParams &P, const Seg &g, const float *xs, const Misc &m) {
+    const int warp = threadIdx.x / kWarp, lane = threadIdx.x % kWarp;
+    const int nu = g.uhi - g.ulo;
+    const int mine = nu > warp ? (nu - warp + kNW - 1) / kNW : 0;
+    const int64_t rb = row_bytes(FMT, g.inter);
+    const int ubase = g.ulo - g.ubase;
+    warp_stream<FMT, 4, NV>(
+        mine, (int)(rb / 16), xs, P.xs_stride, lane,
+        [&](int i, const uint8_t *(&rr)[4]) {
+            const int d = 4 * (ubase + warp + kNW * i);
+#pragma unroll
+            for (int q = 0; q < 4; q++) rr[q] = g.w0 + (size_t)min(d + q, P.H - 1) * rb;
+        },
+        [&](int i, const float (&s)[4][NV]) {
+            const int ld = 4 * (warp + kNW * i);
+            const int d = 4 * ubase + ld;
 #pragma unroll
             for (int v = 0; v < NV; v++) {
-                if (lane == v && v < nv) {
-                    const int pv = g.tg * P.NV + v;
-                    const int row = g.shared ? P.T * P.K + pv : g.pbase + pv;
+                if (lane == v && v < g.nv) {
+                    float *yrow = P.y + (size_t)act_row(P, g, v) * P.H;
 #pragma unroll
-                    for (int q = 0; q < 2; q++)
-                        if (d + q < P.H) P.y[(size_t)row * P.H + d + q] = s[q][v] * g.s0[d + q];
+                    for (int q = 0; q < 4; q++)
+                        if (d + q < P.H) yrow[d + q] = s[q][v] * m.sc[0][ld + q];
                 }
             }
         });
 }
 
 template <int NV>
-__device__ void run_units(const DecParams &P, const Seg &g, bool down, const float *xs) {
-    if (down) {
-        if (g.fmt == COLI_FMT_INT4) down_units<COLI_FMT_INT4, NV>(P, g, xs);
-        else if (g.fmt == COLI_FMT_INT8) down_units<COLI_FMT_INT8, NV>(P, g, xs);
-        else down_units<COLI_FMT_INT2, NV>(P, g, xs);
-    } else {
-        if (g.fmt == COLI_FMT_INT4) gateup_units<COLI_FMT_INT4, NV>(P, g, xs);
-        else if (g.fmt == COLI_FMT_INT8) gateup_units<COLI_FMT_INT8, NV>(P, g, xs);
-        else gateup_units<COLI_FMT_INT2, NV>(P, g, xs);
+__device__ void run_units(const DecParams &P, const Seg &g, bool down, const void *xs, const Misc &m) {
+    if (g.nv == 1) {
+        if (down) {
+            if (g.fmt == COLI_FMT_INT4) down_units_int<COLI_FMT_INT4>(P, g, xs, m);
+            else if (g.fmt == COLI_FMT_INT8) down_units_int<COLI_FMT_INT8>(P, g, xs, m);
+            else down_units_int<COLI_FMT_INT2>(P, g, xs, m);
+        } else {
+            if (g.fmt == COLI_FMT_INT4) gateup_units_int<COLI_FMT_INT4>(P, g, xs, m);
+            else if (g.fmt == COLI_FMT_INT8) gateup_units_int<COLI_FMT_INT8>(P, g, xs, m);
+            else gateup_units_int<COLI_FMT_INT2>(P, g, xs, m);
+        }
+        return;
+    }
+    if constexpr (NV > 1) {
+        const float *xf = static_cast<const float *>(xs);
+        if (down) {
+            if (g.fmt == COLI_FMT_INT4) down_units_flt<COLI_FMT_INT4, NV>(P, g, xf, m);
+            else if (g.fmt == COLI_FMT_INT8) down_units_flt<COLI_FMT_INT8, NV>(P, g, xf, m);
+            else down_units_flt<COLI_FMT_INT2, NV>(P, g, xf, m);
+        } else {
+            if (g.fmt == COLI_FMT_INT4) gateup_units_flt<COLI_FMT_INT4, NV>(P, g, xf, m);
+            else if (g.fmt == COLI_FMT_INT8) gateup_units_flt<COLI_FMT_INT8, NV>(P, g, xf, m);
+            else gateup_units_flt<COLI_FMT_INT2, NV>(P, g, xf, m);
+        }
     }
 }
 
@@ -807,11 +698,11 @@ __device__ __forceinline__ int upper_slot_smem(const int *off, int n, int x) {
     return lo;
 }
 
-// fill the segment of unit l (thread 0 only). Unit spaces run slot by slot, then token group,
-// then unit; shared_phase: the shared expert's gate/up before routing.
+// fill the piece of unit l (thread 0 only) and ask L2 for its rows. Unit spaces run slot by
+// slot, then token group, then unit; shared_phase: the shared expert's gate/up before routing.
 __device__ __noinline__ void make_seg(const DecParams &P, const RTab &rt, int slot, int U, int slot_base, int l,
                                       int e_share, bool down, bool shared_phase, Seg &g) {
-    const int GUPER = (P.I + 1) / 2, GUPER_SH = (P.Is + 1) / 2, DNPER = (P.H + 1) / 2;
+    const int GUPER = (P.I + 1) / 2, GUPER_SH = (P.Is + 1) / 2, DNPER = (P.H + 3) / 4;
     const bool shared = shared_phase || slot == U;
     coli_moe_expert ex;
     int n, pbase, groups;
@@ -841,16 +732,26 @@ __device__ __noinline__ void make_seg(const DecParams &P, const RTab &rt, int sl
     const int per = down ? DNPER : (shared ? GUPER_SH : GUPER);
     const int local = l - slot_base;
     g.tg = local / per;
+    g.nv = min(P.NV, n - g.tg * P.NV);
     g.ubase = slot_base + g.tg * per;
     g.ulo = l;
-    g.uhi = min(e_share, g.ubase + per);
+    g.uhi = min(min(e_share, g.ubase + per), l + kScCap);
+    if (down) {
+        const int64_t rb = row_bytes(g.fmt, g.inter);
+        prefetch_rows(g.w0, 4 * (g.ulo - g.ubase), min(4 * (g.uhi - g.ubase), P.H), rb);
+    } else {
+        const int64_t rb = row_bytes(g.fmt, P.H);
+        const int j0 = 2 * (g.ulo - g.ubase), j1 = min(2 * (g.uhi - g.ubase), g.inter);
+        prefetch_rows(g.w0, j0, j1, rb);
+        prefetch_rows(g.w1, j0, j1, rb);
+    }
 }
 
-// walk this CTA's share [b, e) of a unit space segment by segment; off/nslots: the unit prefix
+// walk this CTA's share [b, e) of a unit space piece by piece; off/nslots: the unit prefix
 // over the slots (shared memory), unused in the shared phase
 template <int NV>
 __device__ void run_share(const DecParams &P, const RTab &rt, int b, int e, bool down, bool shared_phase,
-                          const int *off, int nslots, int U, float *xs, Seg *sg, int *skey) {
+                          const int *off, int nslots, int U, void *xs, Misc &m) {
     const int tid = threadIdx.x;
     if (b >= e) return;
     int slot = 0, slot_base = 0, slot_end = 0, done_in_slot = 0;
@@ -865,35 +766,51 @@ __device__ void run_share(const DecParams &P, const RTab &rt, int b, int e, bool
     }
     int l = b;
     while (l < e) {
-        __syncthreads();  // the previous segment's units are done with xs and sg
+        __syncthreads();  // the previous piece's units are done with xs, sg and sc
         if (tid == 0) {
             while (l >= slot_end) {
                 slot++;
                 slot_base = slot_end;
                 slot_end = off[slot + 1];
             }
-            make_seg(P, rt, slot, U, slot_base, l, min(e, slot_end), down, shared_phase, *sg);
-            if (down) {  // this expert's h rows must all be written
-                wait_at_least(&P.ctrl->gu_done[sg->key], sg->need, P.ctrl);
-                __threadfence();
-            }
+            make_seg(P, rt, slot, U, slot_base, l, min(e, slot_end), down, shared_phase, m.sg);
         }
         __syncthreads();
-        const Seg g = *sg;
+        const Seg g = m.sg;
+        // row scales of the piece (loads issued before any wait or staging)
+        const int nrow = down ? 4 * (g.uhi - g.ulo) : 2 * (g.uhi - g.ulo);
+        const int r0 = (down ? 4 : 2) * (g.ulo - g.ubase);
+        const int rlim = down ? P.H : g.inter;
+        float sv0 = 0.f, sv1 = 0.f;
+        if (tid < nrow && r0 + tid < rlim) {
+            sv0 = __ldg(g.s0 + r0 + tid);
+            if (!down) sv1 = __ldg(g.s1 + r0 + tid);
+        }
+        if (down) {  // this expert's h rows must all be written
+            if (tid == 0) {
+                wait_at_least(&P.ctrl->gu_done[g.key], g.need, P.ctrl);
+                __threadfence();
+            }
+            __syncthreads();
+        }
         // activations: skip restaging when xs already holds them (same kind, tokens and format)
-        const int k0 = down ? 2 : 1;
+        const int k0 = (down ? 2 : 1) + (g.nv == 1 ? 4 : 0);
         const int k1 = down ? g.key : (P.T == 1 ? 0 : (g.shared ? -1 : g.pbase));
         const int k2 = (P.T == 1 && !down) ? g.fmt : g.tg * 8 + g.fmt;
-        if (!(skey[0] == k0 && skey[1] == k1 && skey[2] == k2)) {
-            stage_acts(P, rt, g, down, xs);
-            __syncthreads();
+        if (!(m.skey[0] == k0 && m.skey[1] == k1 && m.skey[2] == k2)) {
+            stage_acts(P, rt, g, down, xs, m);
             if (tid == 0) {
-                skey[0] = k0;
-                skey[1] = k1;
-                skey[2] = k2;
+                m.skey[0] = k0;
+                m.skey[1] = k1;
+                m.skey[2] = k2;
             }
         }
-        run_units<NV>(P, g, down, xs);
+        if (tid < nrow) {
+            m.sc[0][tid] = sv0;
+            m.sc[1][tid] = sv1;
+        }
+        __syncthreads();
+        run_units<NV>(P, g, down, xs, m);
         l = g.uhi;
         if (!down) {  // publish this CTA's gate/up units of the expert when its run ends
             __syncthreads();  // every warp's h stores precede thread 0's release
@@ -913,12 +830,11 @@ __device__ void run_share(const DecParams &P, const RTab &rt, int b, int e, bool
 template <int NV>
 __global__ void __launch_bounds__(kNT, 2) moe_decode_kernel(const DecParams P) {
     extern __shared__ __align__(128) uint8_t smem[];
-    float *xs = reinterpret_cast<float *>(smem);
+    void *xs = smem;
     const RTab rt = rtab_of(smem + P.xs_bytes, P.T, P.E, P.K);
-    Seg *sg = reinterpret_cast<Seg *>(smem + P.xs_bytes + P.rt_bytes);
-    int *skey = reinterpret_cast<int *>(sg + 1);
+    Misc &m = *reinterpret_cast<Misc *>(smem + P.xs_bytes + P.rt_bytes);
     const int tid = threadIdx.x, G = gridDim.x, c = blockIdx.x;
-    if (tid == 0) skey[0] = skey[1] = skey[2] = -1;
+    if (tid == 0) m.skey[0] = m.skey[1] = m.skey[2] = -1;
 
     // ---------------- A: router partial logits
     if (!P.route_only) {
@@ -941,29 +857,27 @@ __global__ void __launch_bounds__(kNT, 2) moe_decode_kernel(const DecParams P) {
 
     // ---------------- B: the shared expert's gate/up (independent of routing)
     if (P.Is > 0)
-        run_share<NV>(P, rt, range_lo(P.G_sh, c, G), range_lo(P.G_sh, c + 1, G), false, true, nullptr, 0, -1, xs,
-                      sg, skey);
+        run_share<NV>(P, rt, range_lo(P.G_sh, c, G), range_lo(P.G_sh, c + 1, G), false, true, nullptr, 0, -1, xs, m);
 
     // ---------------- R: routing, by this CTA for itself
     if (tid == 0) {
         wait_at_least(&P.ctrl->router_done, P.route_only ? G : P.R, P.ctrl);
         __threadfence();
-        skey[0] = -1;  // xs becomes routing scratch
+        m.skey[0] = -1;  // xs becomes routing scratch
     }
     __syncthreads();
-    route_local(P, xs, rt, !P.route_only);
+    route_local(P, static_cast<float *>(xs), rt, !P.route_only);
     const int U = *rt.U;
 
     // ---------------- C: routed gate/up
     const int gu_tot = rt.gu_off[U];
-    run_share<NV>(P, rt, range_lo(gu_tot, c, G), range_lo(gu_tot, c + 1, G), false, false, rt.gu_off, U, U, xs, sg,
-                  skey);
+    run_share<NV>(P, rt, range_lo(gu_tot, c, G), range_lo(gu_tot, c + 1, G), false, false, rt.gu_off, U, U, xs, m);
 
     // ---------------- D: down rows of every expert
     const int nslots = U + (P.Is > 0 ? 1 : 0);
     const int dn_tot = rt.dn_off[nslots];
     const int db = range_lo(dn_tot, c, G), de = range_lo(dn_tot, c + 1, G);
-    run_share<NV>(P, rt, db, de, true, false, rt.dn_off, nslots, U, xs, sg, skey);
+    run_share<NV>(P, rt, db, de, true, false, rt.dn_off, nslots, U, xs, m);
     if (tid == 0) {
         __threadfence();
         atomicAdd(&P.ctrl->dn_done, de - db);
@@ -991,7 +905,7 @@ __global__ void __launch_bounds__(kNT, 2) moe_decode_kernel(const DecParams P) {
 
 size_t decode_ctrl_bytes() { return sizeof(DecCtrl); }
 
-size_t decode_smem_bytes(const DecParams &P) { return (size_t)P.xs_bytes + P.rt_bytes + sizeof(Seg) + 64; }
+size_t decode_smem_bytes(const DecParams &P) { return (size_t)P.xs_bytes + P.rt_bytes + sizeof(Misc) + 64; }
 
 // Host-side geometry of the decode launch for a grid of `grid` CTAs.
 bool decode_plan(const coli_moe_desc &d, DecParams &P, int grid) {
@@ -1041,7 +955,10 @@ int decode_ctas_per_sm(const DecParams &P) {
     int n = 0;
     const void *fn = P.NV == 1 ? (const void *)moe_decode_kernel<1>
                    : P.NV == 2 ? (const void *)moe_decode_kernel<2> : (const void *)moe_decode_kernel<4>;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, kNT, decode_smem_bytes(P)) != cudaSuccess) return 0;
+    const size_t smem = decode_smem_bytes(P);
+    // the query counts against the kernel's dynamic shared-memory limit: raise it first
+    if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) return 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, kNT, smem) != cudaSuccess) return 0;
     return n;
 }
 

@@ -1,0 +1,338 @@
+// decode_parts.cuh — device pieces shared by the persistent decode kernels (decode.cu for
+// token groups, decode1.cu for one token): bounded waits, the router item, the float and
+// integer streaming cores, activation staging and L2 prefetch. Internal to libcolimoe; every
+// translation unit gets its own copy (anonymous namespace).
+#pragma once
+
+#include "idot.cuh"
+#include "kernels.h"
+#include "ptx.cuh"
+#include "qdot.cuh"
+
+namespace colimoe {
+namespace {
+
+constexpr int kNT = 256;                 // threads per CTA
+constexpr int kNW = kNT / kWarp;         // warps per CTA
+constexpr int kRtE = 32;                 // experts per router item (4 per warp)
+constexpr int kInflight = 8;             // 16-byte loads in flight per lane (rows x depth)
+constexpr unsigned long long kWaitNs = 2000000000ull;
+constexpr int kSharedKey = kMaxE;        // gu_done index of the shared expert
+
+__device__ __forceinline__ void flag_error(DecCtrl *c, int code) { atomicCAS(&c->err, 0, code); }
+
+// bounded wait until *p >= target; false (and flagged) on timeout
+__device__ bool wait_at_least(const int *p, int target, DecCtrl *c) {
+    if (ld_volatile(p) >= target) return true;
+    const uint64_t t0 = globaltimer_ns();
+    while (ld_volatile(p) < target) {
+        __nanosleep(64);
+        if (globaltimer_ns() - t0 > kWaitNs) {
+            flag_error(c, kErrWaitExpired);
+            return false;
+        }
+    }
+    return true;
+}
+
+__device__ __forceinline__ int range_lo(int n, int c, int G) { return (int)((long long)n * c / G); }
+
+// first index i in [0, n) with off[i+1] > x (off: nondecreasing prefix array, off[0] = 0)
+__device__ int upper_slot(const int *off, int n, int x) {
+    int lo = 0, hi = n - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        if (__ldcg(off + mid + 1) > x) hi = mid;
+        else lo = mid + 1;
+    }
+    return lo;
+}
+
+__device__ __forceinline__ bool bad16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) != 0; }
+
+// ------------------------------------------------------------------ the streaming core
+// One warp streams `nunits` units of NR packed rows each (CPR 16-byte chunks per row), lane l
+// taking chunks l, l+32, ... of every row, with kDepth chunk-steps of loads in flight across unit
+// boundaries (kInflight / NR steps). rows_of(i, rows) gives unit i's row pointers; epi(i, sums) gets the finished
+// warp-reduced dot products with the NV staged vectors.
+template <int FMT, int NR, int NV, class RowsOf, class Epi>
+__device__ __forceinline__ void warp_stream(int nunits, int CPR, const float *xs, int xstride, int lane,
+                                            RowsOf rows_of, Epi epi) {
+    using G = QGeom<FMT>;
+    constexpr int kDepth = kInflight / NR;  // chunk-steps in flight
+    if (nunits <= 0) return;
+    const int S = (CPR + kWarp - 1) / kWarp;  // steps per unit
+    const int total = nunits * S;
+    uint4 buf[kDepth][NR];
+    int iu = 0, ik = 0;  // issue cursor: unit, step within unit
+    auto issue = [&](uint4 (&b)[NR]) {
+        if (iu < nunits) {
+            const int c = lane + kWarp * ik;
+            const uint8_t *rr[NR];
+            rows_of(iu, rr);
+#pragma unroll
+            for (int r = 0; r < NR; r++) b[r] = c < CPR ? ld_stream_16(rr[r] + 16 * c) : make_uint4(0, 0, 0, 0);
+            if (++ik == S) {
+                ik = 0;
+                iu++;
+            }
+        }
+    };
+#pragma unroll
+    for (int j = 0; j < kDepth; j++) issue(buf[j]);
+    float2 acc[NR][NV];
+#pragma unroll
+    for (int r = 0; r < NR; r++)
+#pragma unroll
+        for (int v = 0; v < NV; v++) acc[r][v] = make_float2(0.f, 0.f);
+    const float4 *xs4 = reinterpret_cast<const float4 *>(xs);
+    const int xstride4 = xstride / 4;
+    int cu = 0, ck = 0;  // compute cursor
+    for (int s0 = 0; s0 < total; s0 += kDepth) {
+#pragma unroll
+        for (int j = 0; j < kDepth; j++) {
+            if (s0 + j < total) {
+                const int c = lane + kWarp * ck;
+                if (c < CPR) {
+#pragma unroll
+                    for (int wi = 0; wi < 4; wi++) {
+                        float4 xv[NV][G::F4W];
+#pragma unroll
+                        for (int v = 0; v < NV; v++)
+#pragma unroll
+                            for (int q = 0; q < G::F4W; q++)
+                                xv[v][q] = xs4[v * xstride4 + (wi * G::F4W + q) * CPR + c];
+#pragma unroll
+                        for (int r = 0; r < NR; r++) {
+                            const uint32_t w = word_of(buf[j][r], wi);
+                            const uint32_t wh = w >> 16;
+#pragma unroll
+                            for (int m = 0; m < G::HALF; m++) {
+                                const uint32_t lo = lop3_and_xor(w, G::mask(m), G::xorv(m));
+                                const uint32_t hi = lop3_and_xor(wh, G::mask(m), G::xorv(m));
+                                const float2 d = __fadd2_rn(make_float2(__uint_as_float(lo), __uint_as_float(hi)),
+                                                            make_float2(-G::magic(m), -G::magic(m)));
+#pragma unroll
+                                for (int v = 0; v < NV; v++) {
+                                    const float4 &x4 = xv[v][m >> 1];
+                                    const float2 x2 = (m & 1) ? make_float2(x4.z, x4.w) : make_float2(x4.x, x4.y);
+                                    acc[r][v] = __ffma2_rn(d, x2, acc[r][v]);
+                                }
+                            }
+                        }
+                    }
+                }
+                issue(buf[j]);
+                if (++ck == S) {
+                    float sums[NR][NV];
+                    warp_reduce_acc<NR, NV>(acc, sums);
+                    epi(cu, sums);
+#pragma unroll
+                    for (int r = 0; r < NR; r++)
+#pragma unroll
+                        for (int v = 0; v < NV; v++) acc[r][v] = make_float2(0.f, 0.f);
+                    ck = 0;
+                    cu++;
+                }
+            }
+        }
+    }
+}
+
+// The same walk for single-token groups on the integer core (idot.cuh): xq_of(i) gives the
+// staged activation limbs unit i is dotted with; epi(i, sums, d) gets the exact warp totals S_r
+// of unit i's NR rows and d = pre(i), the unit's epilogue operands (row scales), which are
+// loaded two units ahead.
+template <int FMT, int NR, int INFL = kInflight, class RowsOf, class XqOf, class Pre, class Epi>
+__device__ __forceinline__ void warp_stream_int(int nunits, int CPR, int lane, RowsOf rows_of, XqOf xq_of, Pre pre,
+                                                Epi epi) {
+    constexpr int kDepth = INFL / NR;
+    if (nunits <= 0) return;
+    const int S = (CPR + kWarp - 1) / kWarp;
+    const int total = nunits * S;
+    uint4 buf[kDepth][NR];
+    int iu = 0, ik = 0;
+    const uint8_t *rr[NR];  // row pointers of the unit being issued (looked up once per unit)
+    rows_of(0, rr);
+    auto issue = [&](uint4 (&b)[NR]) {
+        if (iu < nunits) {
+            const int c = lane + kWarp * ik;
+#pragma unroll
+            for (int r = 0; r < NR; r++) b[r] = c < CPR ? ld_stream_16(rr[r] + 16 * c) : make_uint4(0, 0, 0, 0);
+            if (++ik == S) {
+                ik = 0;
+                if (++iu < nunits) rows_of(iu, rr);
+            }
+        }
+    };
+#pragma unroll
+    for (int j = 0; j < kDepth; j++) issue(buf[j]);
+    auto d0 = pre(0);
+    decltype(d0) d1 = d0;
+    if (nunits > 1) d1 = pre(1);
+    int acc[NR][3];
+#pragma unroll
+    for (int r = 0; r < NR; r++) acc[r][0] = acc[r][1] = acc[r][2] = 0;
+    int cu = 0, ck = 0;
+    const uint4 *xq4 = xq_of(0);
+    for (int s0 = 0; s0 < total; s0 += kDepth) {
+#pragma unroll
+        for (int j = 0; j < kDepth; j++) {
+            if (s0 + j < total) {
+                const int c = lane + kWarp * ck;
+                if (c < CPR) idot_chunk<FMT, NR>(buf[j], xq4, CPR, c, acc);
+                issue(buf[j]);
+                if (++ck == S) {
+                    long long sums[NR];
+                    idot_reduce<FMT, NR>(acc, sums);
+                    epi(cu, sums, d0);
+                    d0 = d1;
+                    if (cu + 2 < nunits) d1 = pre(cu + 2);
+#pragma unroll
+                    for (int r = 0; r < NR; r++) acc[r][0] = acc[r][1] = acc[r][2] = 0;
+                    ck = 0;
+                    cu++;
+                    if (cu < nunits) xq4 = xq_of(cu);
+                }
+            }
+        }
+    }
+}
+
+// ------------------------------------------------------------------ router items
+// T <= 8: partial logits of 32 experts (4 per warp) over one slice of H; each lane keeps two
+// float4 steps of W_r and x loads in flight
+template <int TM>  // tokens handled: P.T <= TM
+__device__ __noinline__ void router_item(const DecParams &P, int item) {
+    const int warp = threadIdx.x / kWarp, lane = threadIdx.x % kWarp;
+    const int eb = item % P.neb, ks = item / P.neb;
+    const int kb = ks * P.rks_floats, ke = min(P.H, kb + P.rks_floats);
+    float acc[4][TM];
+#pragma unroll
+    for (int r = 0; r < 4; r++)
+#pragma unroll
+        for (int t = 0; t < TM; t++) acc[r][t] = 0.f;
+    int e[4];
+#pragma unroll
+    for (int r = 0; r < 4; r++) e[r] = min(eb * kRtE + warp * 4 + r, P.E - 1);
+    constexpr int B = 2;
+    for (int k0 = kb + 4 * lane; k0 < ke; k0 += 4 * kWarp * B) {
+        float4 wv[B][4];
+#pragma unroll
+        for (int b = 0; b < B; b++) {
+            const int k = k0 + b * 4 * kWarp;
+#pragma unroll
+            for (int r = 0; r < 4; r++) {
+                uint4 u = make_uint4(0, 0, 0, 0);
+                if (k < ke) u = ld_stream_16(P.Wr + (size_t)e[r] * P.H + k);
+                wv[b][r] = make_float4(__uint_as_float(u.x), __uint_as_float(u.y), __uint_as_float(u.z),
+                                       __uint_as_float(u.w));
+            }
+        }
+#pragma unroll
+        for (int t = 0; t < TM; t++) {
+            if (t >= P.T) break;
+            float4 xv[B];
+#pragma unroll
+            for (int b = 0; b < B; b++) {
+                const int k = k0 + b * 4 * kWarp;
+                xv[b] = k < ke ? __ldg(reinterpret_cast<const float4 *>(P.x + (size_t)t * P.H + k))
+                               : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+#pragma unroll
+            for (int b = 0; b < B; b++)
+#pragma unroll
+                for (int r = 0; r < 4; r++) {
+                    float a = acc[r][t];
+                    a = fmaf(wv[b][r].x, xv[b].x, a);
+                    a = fmaf(wv[b][r].y, xv[b].y, a);
+                    a = fmaf(wv[b][r].z, xv[b].z, a);
+                    a = fmaf(wv[b][r].w, xv[b].w, a);
+                    acc[r][t] = a;
+                }
+        }
+    }
+#pragma unroll
+    for (int r = 0; r < 4; r++)
+#pragma unroll
+        for (int t = 0; t < TM; t++) {
+            if (t >= P.T) break;
+            float s = acc[r][t];
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(kFull, s, o);
+            const int er = eb * kRtE + warp * 4 + r;
+            if (lane == 0 && er < P.E) P.part[((size_t)ks * P.T + t) * P.E + er] = s;
+        }
+}
+
+// T > 8: logits = fixed-order sums of the partials for flat indices [lo, hi), into slice 0
+__device__ __noinline__ void reduce_logits(const DecParams &P, int lo, int hi) {
+    for (int i = lo + (int)threadIdx.x; i < hi; i += kNT) {
+        float a[16];
+#pragma unroll
+        for (int k = 0; k < 16; k++)
+            if (k < P.nks) a[k] = __ldcg(P.part + (size_t)k * P.T * P.E + i);
+        float s = 0.f;
+#pragma unroll
+        for (int k = 0; k < 16; k++)
+            if (k < P.nks) s += a[k];
+        P.part[i] = s;  // slice 0, index i: only this thread reads or writes it here
+    }
+}
+
+// ------------------------------------------------------------------ staging and prefetch
+__device__ __forceinline__ float4 ld_act4(const float *src, int q, bool coherent) {
+    return coherent ? __ldcg(reinterpret_cast<const float4 *>(src) + q)
+                    : __ldg(reinterpret_cast<const float4 *>(src) + q);
+}
+
+// stage the activations of token group tg (x rows for gate/up, h rows for down) into xs. Each
+// thread issues all its float4 loads of a row before it stores any.
+template <int FMT>
+__device__ __forceinline__ void stage_row(const float *__restrict__ src, float *dst, int len, bool coherent) {
+    const int CPR = len / QGeom<FMT>::EPC;
+    const int n4 = len / 4;
+    constexpr int B = 4;
+    for (int q0 = threadIdx.x; q0 < n4; q0 += kNT * B) {
+        float4 v[B];
+#pragma unroll
+        for (int j = 0; j < B; j++) {
+            const int q = q0 + j * kNT;
+            if (q < n4) v[j] = ld_act4(src, q, coherent);
+        }
+#pragma unroll
+        for (int j = 0; j < B; j++) {
+            const int q = q0 + j * kNT;
+            if (q < n4) {
+                const float e4[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+#pragma unroll
+                for (int u = 0; u < 4; u++) {
+                    float sc;
+                    const int at = staged_index<FMT>(4 * q + u, CPR, sc);
+                    dst[at] = e4[u] * sc;
+                }
+            }
+        }
+    }
+}
+
+// one 128-byte line to L2 (no alignment rule beyond the natural one)
+__device__ __forceinline__ void prefetch_line_l2(const void *p) {
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
+__device__ __forceinline__ void prefetch_l2(const void *p, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
+// ask L2 for rows [r0, r1) of a matrix with rb bytes per row (16-byte multiples), 32 KB a piece
+__device__ void prefetch_rows(const uint8_t *base, int r0, int r1, int64_t rb) {
+    if (r1 <= r0) return;
+    const uint8_t *p = base + (size_t)r0 * rb;
+    const int64_t n = (int64_t)(r1 - r0) * rb;
+    constexpr int64_t kPiece = 32768;
+    for (int64_t o = 0; o < n; o += kPiece) prefetch_l2(p + o, (uint32_t)(n - o < kPiece ? n - o : kPiece));
+}
+
+}  // namespace
+}  // namespace colimoe

@@ -1,0 +1,192 @@
+// idot.cuh — the integer dot-product core for single-token groups.
+//
+// Computes, for NR packed weight rows and ONE activation vector x, the exact integer sums
+//   S_r = sum_i v[r, i] * X[i]
+// where v is the dequantised integer of the glm.c QT format (int8: the signed byte; int4:
+// nibble - 8; int2: field - 2) and X is x in 24-bit block fixed point:
+//   X[i] = round(x[i] * 2^s),  s chosen per vector so that max|x| * 2^s < 2^22.
+// The dot product is then S_r * 2^-s, formed exactly in int64 before its one conversion to
+// float; the caller applies the row scale, as matmul_q / matmul_i4 / matmul_i2 do.
+//
+// Why integers: the float route spends one LOP3 per weight plus an f32x2 subtract and FMA per
+// two, and LOP3 issues at half rate, so on GB300 it cannot unpack int4 as fast as HBM delivers
+// it. DP4A multiplies four signed weight bytes by four activation bytes and accumulates into an
+// int32 in one (half-rate) instruction: with X split into three byte limbs
+//   X = X2 * 2^16 + X1 * 2^8 + X0   (X0, X1 unsigned, X2 signed)
+// a 32-bit word of int4 costs one shift, two LOP3 and six DP4A.
+//
+// Signed fields in place: a field f of b bits moved to the top of its byte and XOR-ed with
+// 0x80 reads, as a signed byte, 2^(8-b) * (f - 2^(b-1)) — the dequantised value times a power of
+// two. For int4, (w & 0xF0F0F0F0) ^ 0x80808080 gives the odd nibbles as 16 * (f - 8) and the
+// same after w << 4 gives the even ones; int2 shifts each of its four fields to the top; int8
+// bytes are used as they are. Every product carries the same factor SC (16, 64 or 1), which
+// the final sum drops with an exact arithmetic shift.
+//
+// Staged activation layout (per vector, bytes): for the 16-byte weight chunk c of a row (EPC
+// elements), the activation limbs are grouped by the word of the chunk they meet; NSS sub-steps
+// of WPSS words each use three uint4 of limbs, stored at uint4 index (ss*3 + j)*CPR + c so
+// that the 32 lanes of a warp, which take consecutive chunks, read consecutive uint4s. Inside
+// a sub-step, u32 number u = (wl*NGW + g)*3 + l holds limb l of the four elements of field
+// group g of word wl (byte b of the u32 = the element in byte b of the weight word).
+#pragma once
+
+#include "qdot.cuh"
+
+namespace colimoe {
+
+template <int FMT>
+struct IQ;
+template <>
+struct IQ<COLI_FMT_INT8> {
+    static constexpr int NSS = 1, WPSS = 4, NGW = 1, LOG_SC = 0;
+};
+template <>
+struct IQ<COLI_FMT_INT4> {
+    static constexpr int NSS = 2, WPSS = 2, NGW = 2, LOG_SC = 4;
+};
+template <>
+struct IQ<COLI_FMT_INT2> {
+    static constexpr int NSS = 4, WPSS = 1, NGW = 4, LOG_SC = 6;
+};
+
+// d = c + dot(signed bytes of a, bytes of b); SB: the bytes of b are signed
+template <bool SB>
+__device__ __forceinline__ int dp4a_s(uint32_t a, uint32_t b, int c) {
+    int d;
+    if (SB) asm("dp4a.s32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    else asm("dp4a.s32.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+
+// field group g of weight word w as signed bytes SC * value
+template <int FMT>
+__device__ __forceinline__ uint32_t signed_fields(uint32_t w, int g) {
+    if (FMT == COLI_FMT_INT4) return lop3_and_xor(g == 0 ? (w << 4) : w, 0xF0F0F0F0u, 0x80808080u);
+    if (FMT == COLI_FMT_INT2) return lop3_and_xor(w << (6 - 2 * g), 0xC0C0C0C0u, 0x80808080u);
+    return w;
+}
+
+// accumulate one 16-byte chunk of NR rows (w[r]) against the staged limbs: acc[r][limb]
+template <int FMT, int NR>
+__device__ __forceinline__ void idot_chunk(const uint4 (&w)[NR], const uint4 *xq4, int CPR, int c,
+                                           int (&acc)[NR][3]) {
+    using I = IQ<FMT>;
+#pragma unroll
+    for (int ss = 0; ss < I::NSS; ss++) {
+        const uint4 xa = xq4[(ss * 3 + 0) * CPR + c];
+        const uint4 xb = xq4[(ss * 3 + 1) * CPR + c];
+        const uint4 xc = xq4[(ss * 3 + 2) * CPR + c];
+        const uint32_t xv[12] = {xa.x, xa.y, xa.z, xa.w, xb.x, xb.y, xb.z, xb.w, xc.x, xc.y, xc.z, xc.w};
+#pragma unroll
+        for (int r = 0; r < NR; r++) {
+#pragma unroll
+            for (int wl = 0; wl < I::WPSS; wl++) {
+                const uint32_t wd = word_of(w[r], ss * I::WPSS + wl);
+#pragma unroll
+                for (int g = 0; g < I::NGW; g++) {
+                    const uint32_t a = signed_fields<FMT>(wd, g);
+                    const int u = (wl * I::NGW + g) * 3;
+                    acc[r][0] = dp4a_s<false>(a, xv[u + 0], acc[r][0]);
+                    acc[r][1] = dp4a_s<false>(a, xv[u + 1], acc[r][1]);
+                    acc[r][2] = dp4a_s<true>(a, xv[u + 2], acc[r][2]);
+                }
+            }
+        }
+    }
+}
+
+// lane partials -> exact warp totals S_r (every lane gets them)
+template <int FMT, int NR>
+__device__ __forceinline__ void idot_reduce(const int (&acc)[NR][3], long long (&out)[NR]) {
+    constexpr int LS = IQ<FMT>::LOG_SC;
+#pragma unroll
+    for (int r = 0; r < NR; r++) {
+        long long p = ((long long)(acc[r][2] >> LS) << 16) + ((long long)(acc[r][1] >> LS) << 8) +
+                      (long long)(acc[r][0] >> LS);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) p += __shfl_xor_sync(kFull, p, o);
+        out[r] = p;
+    }
+}
+
+// the shift s of a vector whose largest magnitude is mx (0 for an all-zero vector)
+__device__ __forceinline__ int fixed_shift(float mx) {
+    if (!(mx > 0.f)) return 0;
+    const int ex = (int)((__float_as_uint(mx) >> 23) & 255u);
+    return 21 - (ex == 0 ? -126 : ex - 127);
+}
+
+// X = round(x * 2^s), with 2^s applied as two exact factors (s reaches 147 for subnormal input)
+struct FixedScale {
+    float f1, f2;
+    __device__ __forceinline__ explicit FixedScale(int s) {
+        const int s1 = max(-126, min(126, s)), s2 = s - s1;
+        f1 = __int_as_float((s1 + 127) << 23);
+        f2 = __int_as_float((s2 + 127) << 23);
+    }
+    __device__ __forceinline__ int operator()(float x) const { return __float2int_rn((x * f1) * f2); }
+};
+
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+    uint32_t d;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+    return d;
+}
+
+// limbs of four values: w0 = their bytes 0, w1 = bytes 1, w2 = bytes 2 (X2 for |X| < 2^22)
+__device__ __forceinline__ void pack_limbs(int a, int b, int c, int d, uint32_t &w0, uint32_t &w1, uint32_t &w2) {
+    const uint32_t ab = prmt(a, b, 0x5140u), cd = prmt(c, d, 0x5140u);  // a0 b0 a1 b1 / c0 d0 c1 d1
+    w0 = prmt(ab, cd, 0x5410u);
+    w1 = prmt(ab, cd, 0x7632u);
+    w2 = prmt(prmt(a, b, 0x0062u), prmt(c, d, 0x0062u), 0x5410u);
+}
+
+// Stage item p of a vector (n a multiple of EPC, CPR = n / EPC): p = ss * CPR + c takes the 16
+// elements of sub-step ss of chunk c, packs their limbs and writes the three uint4 of the
+// layout, so consecutive items write consecutive uint4s.
+template <int FMT>
+__device__ __forceinline__ void stage_limb_item(const float *__restrict__ src, int CPR, bool coherent, uint4 *xq4,
+                                                const FixedScale &fx, int p) {
+    using G = QGeom<FMT>;
+    using I = IQ<FMT>;
+    const int c = p % CPR, ss = p / CPR;
+    const float4 *s4 = reinterpret_cast<const float4 *>(src + c * G::EPC + ss * 16);
+    float4 v[4];
+#pragma unroll
+    for (int k = 0; k < 4; k++) v[k] = coherent ? __ldcg(s4 + k) : __ldg(s4 + k);
+    int X[16];
+#pragma unroll
+    for (int k = 0; k < 4; k++) {
+        X[4 * k + 0] = fx(v[k].x);
+        X[4 * k + 1] = fx(v[k].y);
+        X[4 * k + 2] = fx(v[k].z);
+        X[4 * k + 3] = fx(v[k].w);
+    }
+    uint32_t o[12];
+#pragma unroll
+    for (int wl = 0; wl < I::WPSS; wl++)
+#pragma unroll
+        for (int g = 0; g < I::NGW; g++) {
+            const int e0 = wl * G::EPW + g, u = (wl * I::NGW + g) * 3;
+            pack_limbs(X[e0], X[e0 + I::NGW], X[e0 + 2 * I::NGW], X[e0 + 3 * I::NGW], o[u], o[u + 1], o[u + 2]);
+        }
+#pragma unroll
+    for (int j = 0; j < 3; j++)
+        xq4[(ss * 3 + j) * CPR + c] = make_uint4(o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
+}
+
+// items per vector of n elements
+template <int FMT>
+__host__ __device__ __forceinline__ int limb_items(int n) {
+    return n / QGeom<FMT>::EPC * IQ<FMT>::NSS;
+}
+
+// the whole vector, items p0, p0 + dp, ...
+template <int FMT>
+__device__ __forceinline__ void stage_limbs_vec(const float *__restrict__ src, int n, bool coherent, uint8_t *xq,
+                                                const FixedScale &fx, int p0, int dp) {
+    const int CPR = n / QGeom<FMT>::EPC, items = limb_items<FMT>(n);
+    for (int p = p0; p < items; p += dp) stage_limb_item<FMT>(src, CPR, coherent, reinterpret_cast<uint4 *>(xq), fx, p);
+}
+
+}  // namespace colimoe

@@ -30,7 +30,9 @@ constexpr int kDecMaxT = 64;              // the persistent decode kernel serves
 // also the workspace error word read by coli_moe_check).
 struct DecCtrl {
     int err, router_done, dn_done;
-    int pad[13];
+    int gu_all;                        // single-token kernel: finished gate/up units, all slots
+    int pad[12];
+    int hmax[kMaxK + 1];               // single-token kernel: max |h| per slot (float bits)
     int gu_done[kMaxE + 1];            // finished gate/up units per slot (shared: index kMaxE)
 };
 
@@ -51,6 +53,8 @@ struct DecParams {
     int R, route_only;         // router items; route_only: logits come from a separate launch
     int neb, nks, rks_floats;  // router expert blocks, k-slices, floats per k-slice
     int groups_sh, G_sh;       // shared expert token groups and gate/up units
+    // single-token kernel (decode1.cu): shared-memory offsets and output rows per CTA
+    int single, d1_act_off, d1_rsc_off, d1_y_off, d1_rows;
 };
 
 bool decode_plan(const coli_moe_desc &d, DecParams &P, int grid);
@@ -58,6 +62,11 @@ bool decode_supported(const coli_moe_desc &d);
 size_t decode_smem_bytes(const DecParams &P);
 int decode_ctas_per_sm(const DecParams &P);
 cudaError_t launch_decode(const DecParams &P, int grid, cudaStream_t s);
+
+// decode1.cu: the single-token kernel
+bool decode1_plan(const coli_moe_desc &d, DecParams &P, int grid);
+int decode1_ctas_per_sm(const DecParams &P);
+cudaError_t launch_decode1(const DecParams &P, int grid, cudaStream_t s);
 
 // router.cu
 cudaError_t launch_router_partial(const float *x, const float *W_r, float *part, int T, int H,

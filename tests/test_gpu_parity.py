@@ -229,3 +229,56 @@ def test_topk_override_and_top_p(qed, ksel, top_p):
     dev = DeviceBlock(blk, ksel=ksel, top_p=top_p)
     check_route(qed, blk, dev, ksel=ksel, top_p=top_p)
     check_forward(qed, blk, dev, ksel=ksel, top_p=top_p)
+
+
+# ------------------------------------------------------------------ one token (the single-token kernel)
+# T = 1 runs its own kernel: every routed/shared format pair, ragged sizes, fewer output-row
+# blocks than CTAs, E not a multiple of 4, K at its maximum, no shared expert, no renorm.
+EDGE1 = [
+    ("i8-i8", dict(H=512, I=256, E=16, K=4, I_shared=128, routed_fmt=1, shared_fmt=1)),
+    ("i4-i8", dict(H=768, I=384, E=40, K=6, I_shared=256, routed_fmt=2, shared_fmt=1)),
+    ("i2-i4", dict(H=384, I=192, E=16, K=2, I_shared=128, routed_fmt=3, shared_fmt=2)),
+    ("i8-i2", dict(H=320, I=128, E=9, K=3, I_shared=192, routed_fmt=1, shared_fmt=3)),
+    ("ragged-e37", dict(H=352, I=160, E=37, K=5, I_shared=96, routed_fmt=2, shared_fmt=2)),
+    ("few-rows", dict(H=64, I=64, E=6, K=2, I_shared=64, routed_fmt=2, shared_fmt=2)),
+    ("k32", dict(H=256, I=128, E=64, K=32, I_shared=0, routed_fmt=2, shared_fmt=2)),
+    ("k1-no-shared", dict(H=128, I=64, E=5, K=1, I_shared=0, routed_fmt=2, shared_fmt=2)),
+    ("no-renorm", dict(H=256, I=128, E=12, K=3, I_shared=64, norm_topk=0, routed_scale=1.5)),
+    ("e1024", dict(H=128, I=64, E=1024, K=8, I_shared=64, routed_fmt=2, shared_fmt=2)),
+]
+
+
+@pytest.mark.parametrize("name,over", EDGE1, ids=[e[0] for e in EDGE1])
+def test_one_token_shapes(qed, name, over):
+    from quantized_expert_decode_gb300.device import DeviceBlock
+    cfg = dict(T=1, H=128, I=64, E=8, K=2, I_shared=64, norm_topk=1, routed_scale=2.5,
+               routed_fmt=2, shared_fmt=2, zipf=False)
+    cfg.update(over)
+    blk = make(cfg, seed=zlib.crc32(("one-" + name).encode()) % 1000)
+    dev = DeviceBlock(blk)
+    check_route(qed, blk, dev)
+    check_forward(qed, blk, dev)
+
+
+@pytest.mark.parametrize("ksel,top_p", [(3, 0.0), (0, 0.5), (5, 0.8)])
+def test_one_token_topk_and_top_p(qed, ksel, top_p):
+    from quantized_expert_decode_gb300.device import DeviceBlock
+    cfg = dict(T=1, H=256, I=128, E=32, K=8, I_shared=64, norm_topk=1, routed_scale=2.5,
+               routed_fmt=2, shared_fmt=2, zipf=False)
+    blk = synth.make_block(cfg, seed=100 + ksel * 10 + int(top_p * 10),
+                           row_filter=top_p_filter(8, ksel, top_p))
+    dev = DeviceBlock(blk, ksel=ksel, top_p=top_p)
+    check_route(qed, blk, dev, ksel=ksel, top_p=top_p)
+    check_forward(qed, blk, dev, ksel=ksel, top_p=top_p)
+
+
+def test_one_token_many_calls(qed, blocks):
+    """Fresh tokens through the same block, back to back: counters and scratch start clean."""
+    blk, dev = blocks(1)
+    cfg = blk["cfg"]
+    xs = synth.make_x_batches(cfg, 515, 6)
+    for i in range(6):
+        out, idx, w = run_forward(qed, dev, xs[i])
+        ro, ri, rw, rk = oracle.moe_forward(blk, x=xs[i])
+        assert np.array_equal(idx[0], ri[0]), i
+        assert_out_close(out[0], ro[0], what=f"call {i}")

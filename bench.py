@@ -38,7 +38,7 @@ ROTATE = 16
 FLUSH_BYTES = 512 << 20
 DECODE_MAX_T = 64  # the library runs T <= 64 as one persistent decode kernel
 
-# DRAM bytes (read + write) per launch of the gate/up kernel measured by ncu
+# DRAM bytes (read + write) per launch of the roofline kernel measured by ncu
 # (dram__bytes_read.sum + dram__bytes_write.sum), keyed by workload, with the hash of the kernel
 # sources they were taken on; a changed kernel reports null until it is measured again.
 NCU_TRAFFIC = {}
@@ -46,7 +46,8 @@ NCU_TRAFFIC = {}
 
 def kernel_source_hash() -> str:
     h = hashlib.sha256()
-    for name in ("decode.cu", "expert.cu", "qdot.cuh", "common.cuh", "ptx.cuh"):
+    for name in ("decode.cu", "decode1.cu", "decode_parts.cuh", "idot.cuh", "expert.cu", "qdot.cuh",
+                 "common.cuh", "ptx.cuh"):
         with open(os.path.join(ROOT, "quantized_expert_decode_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -273,9 +274,9 @@ def run_colimoe(args, rank, world, local):
     hbm_peak, peak_kind = load_peaks()
     fused = T <= DECODE_MAX_T
     if fused:
-        # one persistent kernel does the whole block; for T > 8 the router logits come from
-        # a separate launch before it (timed in the route stage)
-        kname = "moe_decode_kernel"
+        # one persistent kernel does the whole block (T = 1: the single-token kernel); for
+        # T > 8 the router logits come from a separate launch before it
+        kname = "moe_decode1_kernel" if T == 1 else "moe_decode_kernel"
         k_ms = stage[:, 1]
         k_bytes = np.array([b["experts"] + (b["total"] - b["experts"] if T <= 8 else 0)
                             for b in bytes_per], np.float64)
@@ -331,7 +332,7 @@ def run_colimoe(args, rank, world, local):
         "weight_stream_gbs": expert_gbs, "block_bytes_gbs": block_gbs,
         "frac_of_8tbs": expert_gbs / 8000.0,
         "active_experts_mean": float(np.mean(n_active)),
-        "stages_ms": ({"prologue": float(stage[:, 0].mean()), "moe_decode_kernel": k_launch_ms}
+        "stages_ms": ({"prologue": float(stage[:, 0].mean()), kname: k_launch_ms}
                       if fused else
                       {"route": float(stage[:, 0].mean()), "gateup": k_launch_ms,
                        "down": float(stage[:, 2].mean()), "combine": float(stage[:, 3].mean())}),

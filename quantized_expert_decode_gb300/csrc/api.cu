@@ -226,6 +226,38 @@ int run_forward(const coli_moe_desc *d, const float *x, const float *W_r, const 
     int rc = run_route(d, x, W_r, bias, idx, w, keff, nullptr, nullptr, nullptr, true, ws, st);
     if (rc) return rc;
     if ((rc = record(events, 1, st))) return rc;
+    if (d->T > kDecMaxT && prefill_supported(*d)) {
+        PrefillWork pw{};
+        pw.experts = experts;
+        if (shared) pw.shared = *shared;
+        pw.x = x;
+        pw.counts = ws_ptr<int32_t>(ws, L.counts);
+        pw.offsets = ws_ptr<int32_t>(ws, L.offsets);
+        pw.perm = ws_ptr<int32_t>(ws, L.perm);
+        pw.xb = ws_ptr<uint16_t>(ws, L.y);  // read by the gate/up GEMM only, before y is written
+        pw.hb = ws_ptr<uint16_t>(ws, L.h);
+        pw.y = ws_ptr<float>(ws, L.y);
+        pw.err = ws_ptr<int32_t>(ws, L.err);
+        pw.T = d->T;
+        pw.H = d->H;
+        pw.I = d->I;
+        pw.E = d->E;
+        pw.K = d->K;
+        pw.I_shared = d->I_shared;
+        pw.routed_fmt = d->routed_fmt;
+        pw.shared_fmt = d->shared_fmt;
+        pw.ldh = d->I > d->I_shared ? d->I : d->I_shared;
+        pw.grid = num_sms();
+        cudaError_t e;
+        if ((e = launch_prefill(pw, 0, st)) != cudaSuccess) return cuda_fail(e);
+        if ((rc = record(events, 2, st))) return rc;
+        if ((e = launch_prefill(pw, 1, st)) != cudaSuccess) return cuda_fail(e);
+        if ((rc = record(events, 3, st))) return rc;
+        if ((e = launch_combine(pw.y, w, keff, ws_ptr<int32_t>(ws, L.pos), d->T, d->H, d->K,
+                                d->I_shared > 0, out, st)) != cudaSuccess)
+            return cuda_fail(e);
+        return record(events, 4, st);
+    }
     ExpertWork W{};
     W.experts = experts;
     if (shared) W.shared = *shared;

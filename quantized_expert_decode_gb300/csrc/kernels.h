@@ -68,6 +68,21 @@ bool decode1_plan(const coli_moe_desc &d, DecParams &P, int grid);
 int decode1_ctas_per_sm(const DecParams &P);
 cudaError_t launch_decode1(const DecParams &P, int grid, cudaStream_t s);
 
+// prefill.cu: the tensor-core expert GEMMs for T > 64
+struct PrefillWork {
+    const coli_moe_expert *experts;  // device [E]
+    coli_moe_expert shared;
+    const float *x;
+    const int32_t *counts, *offsets, *perm;
+    uint16_t *xb, *hb;               // bf16 activations / h (block-permuted K order)
+    float *y;
+    int32_t *err;
+    int T, H, I, E, K, I_shared, routed_fmt, shared_fmt, ldh, grid;
+};
+bool prefill_supported(const coli_moe_desc &d);
+// part 0: activation pre-pass + gate/up GEMM; part 1: down GEMM
+cudaError_t launch_prefill(const PrefillWork &w, int part, cudaStream_t s);
+
 // router.cu
 cudaError_t launch_router_partial(const float *x, const float *W_r, float *part, int T, int H,
                                   int E, int splits, cudaStream_t s);

@@ -1,0 +1,495 @@
+// prefill.cu — the expert GEMMs of large batches (T > 64) on the 5th-generation tensor cores.
+//
+// With tens of tokens per expert the gate/up and down products are real dense contractions
+// (colibri-strix c/glm.c @98759bf moe() phases C/D, batched over the tokens of one expert), so
+// they run as grouped bf16 GEMMs with fp32 accumulation in tensor memory:
+//   gate/up: for each expert slot, A = its gate and up rows (dequantised to bf16 on the fly,
+//            interleaved so that row 2r is gate row j0+r and row 2r+1 is up row j0+r),
+//            B = the slot's tokens' activations in bf16; epilogue h = silu(g*s_g) * (u*s_u)
+//   down:    A = the slot's down rows, B = its h rows in bf16; epilogue y = acc * s_d
+// Swap-AB: weight rows are the MMA's M = 128 (the long dimension), tokens its N (16..128).
+//
+// One persistent CTA per SM walks the tiles (slot, token block, row block) of a launch:
+//   warps 0-3  producers: each K-block of 64, thread r dequantises row r of A straight into the
+//              128-byte-swizzled K-major layout tcgen05 reads, and threads n < N copy token row
+//              n of B; then they arrive on the stage's `full` mbarrier
+//   warp 4     one thread issues four tcgen05.mma (K = 16 each) per stage and commits the
+//              stage's `empty` mbarrier to their completion; after the last K-block it commits
+//              `accf`
+//   warps 0-3  epilogue: tcgen05.ld of the 128 x N accumulator tile, then the fused epilogue
+// K order: the dot product does not depend on the order of K, so within each block of 8 (int4)
+// or 16 (int2) elements K is permuted the same way in A and B — the order in which the
+// magic-number unpack produces bf16 pairs — and no byte shuffles are needed. The activations
+// (x, and h written by the gate/up epilogue) are stored in that order.
+// Every mbarrier wait is bounded; on expiry the CTA flags the error, drains the MMAs it issued,
+// frees its tensor memory and returns.
+#include <algorithm>
+
+#include "common.cuh"
+#include "kernels.h"
+#include "ptx.cuh"
+#include "tc.cuh"
+
+namespace colimoe {
+
+namespace {
+
+constexpr int kTcM = 128;       // MMA M: weight rows per tile
+constexpr int kTcN = 128;       // max tokens per tile (MMA N, multiple of 16)
+constexpr int kTcKB = 64;       // K per stage (one 128-byte swizzle row of bf16)
+constexpr int kTcStages = 4;
+constexpr int kTcThreads = 160;  // 4 producer/epilogue warps + 1 MMA warp
+constexpr int kTcProd = 128;
+constexpr unsigned long long kTcWaitNs = 2000000000ull;
+
+struct PfParams {
+    const coli_moe_expert *experts;  // device [E]
+    coli_moe_expert shared;
+    const int32_t *counts, *offsets; // routed buckets
+    const uint16_t *xb;              // bf16 activations [T*K + T][H] (block-permuted per format)
+    uint16_t *hb;                    // bf16 h [T*K + T][ldh] (block-permuted per format)
+    float *y;                        // [T*K + T][H]
+    int32_t *err;
+    int T, H, I, E, K, Is, rfmt, sfmt, ldh;
+    int down;                        // 0: gate/up GEMM, 1: down GEMM
+};
+
+struct TcSmem {  // after the 1024-aligned stage buffers
+    uint64_t full[kTcStages], empty[kTcStages], accf, drain;
+    uint32_t tmem_base;
+    int abort;
+    int pref[kMaxE + 2];  // tiles before slot g (slots 0..E-1 routed, E shared)
+};
+
+constexpr size_t kStageA = (size_t)kTcM * 128, kStageB = (size_t)kTcN * 128;
+constexpr size_t kTcSmemBytes = 1024 + kTcStages * (kStageA + kStageB) + sizeof(TcSmem);
+
+// position of element j of a K block in the permuted order of format fmt
+__host__ __device__ __forceinline__ int kperm(int fmt, int j) {
+    if (fmt == COLI_FMT_INT4) return (j & ~7) | ((j & 3) << 1) | ((j >> 2) & 1);
+    if (fmt == COLI_FMT_INT2) return (j & ~15) | ((j & 7) << 1) | ((j >> 3) & 1);
+    return j;
+}
+
+__device__ __forceinline__ uint32_t bf16x2_fma(uint32_t a, uint32_t b, uint32_t c) {
+    uint32_t d;
+    asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+__device__ __forceinline__ uint32_t lop3_and_or(uint32_t a, uint32_t b, uint32_t c) {
+    uint32_t d;
+    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(a), "r"(b), "r"(c));  // (a & b) | c
+    return d;
+}
+
+// bf16 pair (lo, hi) of two floats, round to nearest even
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+    uint32_t d;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+    return d;
+}
+
+// Dequantise one 16-byte chunk of packed weights to bf16 in the permuted K order: int4 gives
+// 32 values (4 chunks of 16 B), int2 64 (8 chunks), int8 16 (2 chunks). The bf16 magic: a field
+// f in bits 0..3 (resp. 0..1) of a halfword OR-ed with 0x4300 is the bf16 128 + f, exactly;
+// subtracting 128 + 8 (resp. 128 + 2) leaves f - 8 (resp. f - 2) exactly.
+template <int FMT>
+__device__ __forceinline__ void deq_chunk_bf16(const uint4 &q, uint32_t *out) {
+    const uint32_t wds[4] = {q.x, q.y, q.z, q.w};
+    if (FMT == COLI_FMT_INT4) {
+        const uint32_t one = 0x3F803F80u, off = 0xC308C308u;  // 1.0, -136.0
+#pragma unroll
+        for (int i = 0; i < 4; i++)
+#pragma unroll
+            for (int m = 0; m < 4; m++)
+                out[4 * i + m] = bf16x2_fma(lop3_and_or(wds[i] >> (4 * m), 0x000F000Fu, 0x43004300u), one, off);
+    } else if (FMT == COLI_FMT_INT2) {
+        const uint32_t one = 0x3F803F80u, off = 0xC302C302u;  // 1.0, -130.0
+#pragma unroll
+        for (int i = 0; i < 4; i++)
+#pragma unroll
+            for (int m = 0; m < 8; m++)
+                out[8 * i + m] = bf16x2_fma(lop3_and_or(wds[i] >> (2 * m), 0x00030003u, 0x43004300u), one, off);
+    } else {
+#pragma unroll
+        for (int i = 0; i < 4; i++) {
+            const int w = (int)wds[i];
+            out[2 * i] = pack_bf16((float)((w << 24) >> 24), (float)((w << 16) >> 24));
+            out[2 * i + 1] = pack_bf16((float)((w << 8) >> 24), (float)(w >> 24));
+        }
+    }
+}
+
+// store 16-byte chunk c (0..7) of row r of a K-major 128-byte-swizzled tile
+__device__ __forceinline__ void st_sw128(uint8_t *tile, int r, int c, uint4 v) {
+    *reinterpret_cast<uint4 *>(tile + (r >> 3) * 1024 + (r & 7) * 128 + ((c ^ (r & 7)) << 4)) = v;
+}
+
+__device__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity, TcSmem &ts, int32_t *err) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    while (!mbar_try_wait(bar, parity)) {
+        if (*reinterpret_cast<volatile int *>(&ts.abort)) return false;
+        if (globaltimer_ns() - t0 > kTcWaitNs) {
+            *reinterpret_cast<volatile int *>(&ts.abort) = 1;
+            atomicCAS(err, 0, (int)kErrWaitExpired);
+            return false;
+        }
+    }
+    return true;
+}
+
+struct Tile {
+    const uint8_t *w0, *w1;  // gate/up rows (or down rows in w0)
+    const float *s0, *s1;
+    int fmt, inter, n0, ncur, N, pbase, row0;  // row0: first j (gate/up) or d (down)
+};
+
+__device__ int slot_rows(const PfParams &P, int g) { return g < P.E ? P.counts[g] : P.T; }
+
+__device__ Tile make_tile(const PfParams &P, const TcSmem &ts, int t) {
+    // slot of tile t: last g with pref[g] <= t
+    int lo = 0, hi = P.E + (P.Is > 0 ? 1 : 0) - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (ts.pref[mid] <= t) lo = mid;
+        else hi = mid - 1;
+    }
+    const int g = lo;
+    const bool sh = g == P.E;
+    const coli_moe_expert ex = sh ? P.shared : P.experts[g];
+    Tile T;
+    T.fmt = sh ? P.sfmt : P.rfmt;
+    T.inter = sh ? P.Is : P.I;
+    const int mt = P.down ? (P.H + kTcM - 1) / kTcM : (T.inter + 63) / 64;
+    const int local = t - ts.pref[g];
+    const int nb = local / mt, mb = local % mt;
+    const int n = slot_rows(P, g);
+    T.n0 = nb * kTcN;
+    T.ncur = min(kTcN, n - T.n0);
+    T.N = (T.ncur + 15) & ~15;
+    T.pbase = sh ? P.T * P.K : P.offsets[g];
+    T.row0 = P.down ? mb * kTcM : mb * 64;
+    T.w0 = static_cast<const uint8_t *>(P.down ? ex.down_w : ex.gate_w);
+    T.w1 = static_cast<const uint8_t *>(ex.up_w);
+    T.s0 = P.down ? ex.down_s : ex.gate_s;
+    T.s1 = ex.up_s;
+    return T;
+}
+
+template <int FMT>
+__device__ __forceinline__ void produce_a(const PfParams &P, const Tile &T, int kb, uint8_t *sa, int r) {
+    // A row r: gate/up interleaved (even: gate j0 + r/2, odd: up), or down row d0 + r
+    const uint8_t *base;
+    int64_t rb;
+    if (P.down) {
+        rb = row_bytes(FMT, T.inter);
+        base = T.w0 + (size_t)min(T.row0 + r, P.H - 1) * rb;
+    } else {
+        rb = row_bytes(FMT, P.H);
+        const int j = min(T.row0 + (r >> 1), T.inter - 1);
+        base = ((r & 1) ? T.w1 : T.w0) + (size_t)j * rb;
+    }
+    constexpr int QB = FMT == COLI_FMT_INT4 ? 32 : FMT == COLI_FMT_INT2 ? 16 : 64;  // bytes per K-block
+    constexpr int NQ = QB / 16;
+    const uint8_t *src = base + (size_t)kb * QB;
+    uint4 q[NQ];
+#pragma unroll
+    for (int i = 0; i < NQ; i++) q[i] = __ldg(reinterpret_cast<const uint4 *>(src) + i);
+    uint32_t o[32];
+#pragma unroll
+    for (int i = 0; i < NQ; i++) deq_chunk_bf16<FMT>(q[i], o + i * (32 / NQ));
+#pragma unroll
+    for (int c = 0; c < 8; c++) st_sw128(sa, r, c, make_uint4(o[4 * c], o[4 * c + 1], o[4 * c + 2], o[4 * c + 3]));
+}
+
+__device__ __forceinline__ void produce_b(const PfParams &P, const Tile &T, int kb, uint8_t *sb, int n) {
+    const int rows_total = P.T * P.K + P.T;
+    const int row = min(T.pbase + T.n0 + n, rows_total - 1);
+    const uint16_t *src = P.down ? P.hb + (size_t)row * P.ldh : P.xb + (size_t)row * P.H;
+    const uint4 *s4 = reinterpret_cast<const uint4 *>(src + (size_t)kb * kTcKB);
+    uint4 v[8];
+#pragma unroll
+    for (int c = 0; c < 8; c++) v[c] = __ldcg(s4 + c);
+#pragma unroll
+    for (int c = 0; c < 8; c++) st_sw128(sb, n, c, v[c]);
+}
+
+__device__ __forceinline__ uint16_t bf16_bits(float f) {
+    return (uint16_t)(pack_bf16(f, 0.f) & 0xFFFFu);
+}
+
+__global__ void __launch_bounds__(kTcThreads, 1) moe_prefill_tc_kernel(const PfParams P) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t *smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+    uint8_t *sA = smem, *sB = smem + kTcStages * kStageA;
+    TcSmem &ts = *reinterpret_cast<TcSmem *>(smem + kTcStages * (kStageA + kStageB));
+    const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
+    const int nslots = P.E + (P.Is > 0 ? 1 : 0);
+
+    // tile prefix over the slots: per-thread chunk sums, a warp scan of the chunk sums, then
+    // every thread writes its chunk's prefix entries
+    {
+        constexpr int kChunks = kTcThreads;
+        const int per = (nslots + kChunks - 1) / kChunks;
+        auto tiles_of = [&](int g) {
+            const int inter = g == P.E ? P.Is : P.I;
+            const int mt = P.down ? (P.H + kTcM - 1) / kTcM : (inter + 63) / 64;
+            return mt * ((slot_rows(P, g) + kTcN - 1) / kTcN);
+        };
+        int loc[8], sum = 0;  // per <= 8: nslots <= kMaxE + 1 = 1025 <= 8 * 160
+#pragma unroll
+        for (int i = 0; i < 8; i++) {
+            const int g = tid * per + i;
+            loc[i] = (i < per && g < nslots) ? tiles_of(g) : 0;
+            sum += loc[i];
+        }
+        ts.pref[tid] = sum;  // scratch: chunk sums (pref is rewritten below)
+        __syncthreads();
+        if (warp == 0) {
+            int v[5], s5 = 0;
+#pragma unroll
+            for (int i = 0; i < 5; i++) {
+                v[i] = ts.pref[5 * lane + i];
+                s5 += v[i];
+            }
+            int inc = s5;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int u = __shfl_up_sync(0xffffffffu, inc, o);
+                if (lane >= o) inc += u;
+            }
+            int run = inc - s5;
+#pragma unroll
+            for (int i = 0; i < 5; i++) {
+                const int vi = v[i];
+                ts.pref[5 * lane + i] = run;
+                run += vi;
+            }
+            if (lane == 31) ts.pref[kMaxE + 1] = inc;  // total
+        }
+        __syncthreads();
+        int run = ts.pref[tid];
+        const int total_tiles = ts.pref[kMaxE + 1];
+        __syncthreads();
+#pragma unroll
+        for (int i = 0; i < 8; i++) {
+            const int g = tid * per + i;
+            if (i < per && g < nslots) ts.pref[g] = run;
+            run += loc[i];
+        }
+        if (tid == 0) ts.pref[nslots] = total_tiles;
+    }
+    if (tid == 0) {
+        ts.abort = 0;
+        for (int s = 0; s < kTcStages; s++) {
+            mbar_init(&ts.full[s], kTcProd);
+            mbar_init(&ts.empty[s], 1);
+        }
+        mbar_init(&ts.accf, 1);
+        mbar_init(&ts.drain, 1);
+        fence_mbar_init();
+    }
+    if (warp == 4) {
+        tmem_alloc(&ts.tmem_base, kTcN);
+        tmem_relinquish();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tbase = ts.tmem_base;
+    const int total = ts.pref[nslots];
+
+    uint32_t gk = 0;  // K-blocks handled by this CTA so far (stage ring position)
+    int it = 0;       // tiles handled so far
+    for (int t = blockIdx.x; t < total; t += gridDim.x, it++) {
+        const Tile T = make_tile(P, ts, t);
+        const int nkb = (P.down ? T.inter : P.H) / kTcKB;
+        if (warp < 4) {
+            // scales of this thread's epilogue row, loaded ahead of the K loop
+            float sc0 = 0.f, sc1 = 0.f;
+            if (P.down) {
+                sc0 = __ldg(T.s0 + min(T.row0 + tid, P.H - 1));
+            } else if ((tid & 1) == 0) {
+                const int j = min(T.row0 + (tid >> 1), T.inter - 1);
+                sc0 = __ldg(T.s0 + j);
+                sc1 = __ldg(T.s1 + j);
+            }
+            for (int kb = 0; kb < nkb; kb++, gk++) {
+                const int s = gk % kTcStages;
+                const uint32_t use = gk / kTcStages;
+                if (use > 0 && !mbar_wait_bounded(&ts.empty[s], (use - 1) & 1, ts, P.err)) break;
+                uint8_t *sa = sA + s * kStageA, *sb = sB + s * kStageB;
+                if (T.fmt == COLI_FMT_INT4) produce_a<COLI_FMT_INT4>(P, T, kb, sa, tid);
+                else if (T.fmt == COLI_FMT_INT8) produce_a<COLI_FMT_INT8>(P, T, kb, sa, tid);
+                else produce_a<COLI_FMT_INT2>(P, T, kb, sa, tid);
+                if (tid < T.N) produce_b(P, T, kb, sb, tid);
+                fence_async_smem();
+                mbar_arrive(&ts.full[s]);
+            }
+            // epilogue
+            if (ts.abort == 0 && mbar_wait_bounded(&ts.accf, it & 1, ts, P.err)) {
+                tc_fence_after_sync();
+                const uint32_t trow = tbase + ((uint32_t)(warp * 32) << 16);
+                const int R = tid;  // accumulator row (TMEM lane)
+                for (int c0 = 0; c0 < T.N; c0 += 16) {
+                    uint32_t r[16];
+                    tmem_ld_x16(trow + c0, r);
+                    tmem_ld_wait();
+                    if (P.down) {
+                        const int d = T.row0 + R;
+                        if (d < P.H) {
+#pragma unroll
+                            for (int i = 0; i < 16; i++) {
+                                const int n = c0 + i;
+                                if (n < T.ncur)
+                                    P.y[(size_t)(T.pbase + T.n0 + n) * P.H + d] = __uint_as_float(r[i]) * sc0;
+                            }
+                        }
+                    } else {
+                        uint32_t pr[16];
+#pragma unroll
+                        for (int i = 0; i < 16; i++) pr[i] = __shfl_xor_sync(0xffffffffu, r[i], 1);
+                        const int j = T.row0 + (R >> 1);
+                        if ((R & 1) == 0 && j < T.inter) {
+                            const int col = kperm(T.fmt, j);
+#pragma unroll
+                            for (int i = 0; i < 16; i++) {
+                                const int n = c0 + i;
+                                if (n < T.ncur) {
+                                    const float gv = __uint_as_float(r[i]) * sc0;
+                                    const float uv = __uint_as_float(pr[i]) * sc1;
+                                    const float hv = gv / (1.f + expf(-gv)) * uv;
+                                    P.hb[(size_t)(T.pbase + T.n0 + n) * P.ldh + col] = bf16_bits(hv);
+                                }
+                            }
+                        }
+                    }
+                }
+            }
+            tc_fence_before_sync();
+            named_bar(1, kTcThreads);  // the accumulator may be overwritten
+        } else {
+            if (lane == 0) {
+                const uint32_t idesc = idesc_bf16_f32(kTcM, T.N);
+                for (int kb = 0; kb < nkb; kb++, gk++) {
+                    const int s = gk % kTcStages;
+                    if (!mbar_wait_bounded(&ts.full[s], (gk / kTcStages) & 1, ts, P.err)) break;
+                    tc_fence_after_sync();
+                    const uint32_t a0 = smem_u32(sA + s * kStageA), b0 = smem_u32(sB + s * kStageB);
+#pragma unroll
+                    for (int k = 0; k < kTcKB / 16; k++)
+                        tc_mma_bf16(tbase, sdesc_k_sw128(a0 + 32 * k), sdesc_k_sw128(b0 + 32 * k), idesc,
+                                    (kb | k) != 0);
+                    tc_commit(&ts.empty[s]);
+                }
+                tc_commit(&ts.accf);
+            } else {
+                gk += nkb;
+            }
+            __syncwarp();
+            named_bar(1, kTcThreads);
+            tc_fence_after_sync();
+        }
+        if (*reinterpret_cast<volatile int *>(&ts.abort)) break;
+    }
+    // every MMA this CTA issued has completed before the tensor memory is freed
+    if (warp == 4 && lane == 0) {
+        tc_commit(&ts.drain);
+        mbar_wait_bounded(&ts.drain, 0, ts, P.err);
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    if (warp == 4) {
+        tc_fence_after_sync();
+        tmem_dealloc(tbase, kTcN);
+    }
+}
+
+// x (fp32) -> bf16 rows in bucket order (rows p < T*K: token perm[p] / K, up to offsets[E]) and
+// plain order for the shared expert (rows T*K + t), K-permuted per the rows' weight format.
+__global__ void prefill_prepass_kernel(const float *__restrict__ x, const int32_t *__restrict__ perm,
+                                       const int32_t *__restrict__ offsets, uint16_t *xb, int T, int H, int K, int E,
+                                       int rfmt, int sfmt, int has_shared) {
+    const int nblk = H / 16;
+    const long long total = (long long)(T * K + (has_shared ? T : 0)) * nblk;
+    const int kept = offsets[E];
+    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
+         i += (long long)gridDim.x * blockDim.x) {
+        const int p = (int)(i / nblk), b = (int)(i % nblk);
+        int t, fmt;
+        if (p < T * K) {
+            if (p >= kept) continue;
+            t = perm[p] / K;
+            fmt = rfmt;
+        } else {
+            t = p - T * K;
+            fmt = sfmt;
+        }
+        const float4 *src = reinterpret_cast<const float4 *>(x + (size_t)t * H + b * 16);
+        float v[16];
+#pragma unroll
+        for (int q = 0; q < 4; q++) {
+            const float4 f = __ldg(src + q);
+            v[4 * q] = f.x;
+            v[4 * q + 1] = f.y;
+            v[4 * q + 2] = f.z;
+            v[4 * q + 3] = f.w;
+        }
+        float o[16];
+#pragma unroll
+        for (int j = 0; j < 16; j++) o[kperm(fmt, j)] = v[j];
+        uint32_t w[8];
+#pragma unroll
+        for (int j = 0; j < 8; j++) w[j] = pack_bf16(o[2 * j], o[2 * j + 1]);
+        uint4 *dst = reinterpret_cast<uint4 *>(xb + (size_t)p * H + b * 16);
+        dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+        dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+    }
+}
+
+}  // namespace
+
+bool prefill_supported(const coli_moe_desc &d) {
+    return d.H % 64 == 0 && d.I % 64 == 0 && d.I_shared % 64 == 0 && d.E <= kMaxE;
+}
+
+size_t prefill_smem_bytes() { return kTcSmemBytes; }
+
+cudaError_t launch_prefill(const PrefillWork &w, int part, cudaStream_t st) {
+    cudaError_t e;
+    if (part == 0) {
+        const long long total = (long long)(w.T * w.K + (w.I_shared > 0 ? w.T : 0)) * (w.H / 16);
+        const int threads = 256;
+        const int blocks = (int)std::min<long long>((total + threads - 1) / threads, 152LL * 16);
+        prefill_prepass_kernel<<<blocks, threads, 0, st>>>(w.x, w.perm, w.offsets, w.xb, w.T, w.H, w.K, w.E,
+                                                           w.routed_fmt, w.shared_fmt, w.I_shared > 0);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
+    if ((e = cudaFuncSetAttribute(moe_prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  (int)kTcSmemBytes)) != cudaSuccess)
+        return e;
+    PfParams P{};
+    P.experts = w.experts;
+    P.shared = w.shared;
+    P.counts = w.counts;
+    P.offsets = w.offsets;
+    P.xb = w.xb;
+    P.hb = w.hb;
+    P.y = w.y;
+    P.err = w.err;
+    P.T = w.T;
+    P.H = w.H;
+    P.I = w.I;
+    P.E = w.E;
+    P.K = w.K;
+    P.Is = w.I_shared;
+    P.rfmt = w.routed_fmt;
+    P.sfmt = w.shared_fmt;
+    P.ldh = w.ldh;
+    P.down = part;
+    moe_prefill_tc_kernel<<<w.grid, kTcThreads, kTcSmemBytes, st>>>(P);
+    return cudaGetLastError();
+}
+
+}  // namespace colimoe

@@ -21,6 +21,9 @@ pytestmark = pytest.mark.gpu
 
 OUT_TOL = 1e-4
 W_RTOL = 1e-5
+# T > 64 runs the expert GEMMs on the tensor cores with bf16 activations and fp32 accumulation
+PREFILL_TOL = 2e-2
+PREFILL_MIN_T = 65
 
 
 @pytest.fixture(scope="module")
@@ -172,7 +175,8 @@ def test_route_workload(qed, blocks, cid):
                                         (4, [0, 1, 777, 2047])])
 def test_forward_workload(qed, blocks, cid, tokens):
     blk, dev = blocks(cid)
-    check_forward(qed, blk, dev, tokens)
+    tol = PREFILL_TOL if blk["cfg"]["T"] >= PREFILL_MIN_T else OUT_TOL
+    check_forward(qed, blk, dev, tokens, tol=tol)
 
 
 def test_forward_is_deterministic(qed, blocks):
@@ -282,3 +286,39 @@ def test_one_token_many_calls(qed, blocks):
         ro, ri, rw, rk = oracle.moe_forward(blk, x=xs[i])
         assert np.array_equal(idx[0], ri[0]), i
         assert_out_close(out[0], ro[0], what=f"call {i}")
+
+
+# ------------------------------------------------------------------ prefill (tensor-core GEMMs)
+# T > 64: every format pair, token counts that leave ragged N tiles, more tokens per expert than
+# one N tile holds, no shared expert, and a 16-bit-unfriendly activation scale.
+PREFILL = [
+    ("i4-i4", dict(T=96, H=256, I=128, E=8, K=2, I_shared=128)),
+    ("i8-i8", dict(T=80, H=192, I=128, E=6, K=2, I_shared=64, routed_fmt=1, shared_fmt=1)),
+    ("i2-i4", dict(T=70, H=128, I=192, E=5, K=2, I_shared=128, routed_fmt=3, shared_fmt=2)),
+    ("i4-i8", dict(T=130, H=320, I=64, E=4, K=3, I_shared=192, routed_fmt=2, shared_fmt=1)),
+    ("hot-expert", dict(T=300, H=128, I=128, E=3, K=1, I_shared=0)),
+    ("no-shared", dict(T=100, H=256, I=256, E=16, K=4, I_shared=0)),
+]
+
+
+@pytest.mark.parametrize("name,over", PREFILL, ids=[e[0] for e in PREFILL])
+def test_prefill_shapes(qed, name, over):
+    from quantized_expert_decode_gb300.device import DeviceBlock
+    cfg = dict(H=128, I=64, E=8, K=2, I_shared=64, norm_topk=1, routed_scale=2.5,
+               routed_fmt=2, shared_fmt=2, zipf=False)
+    cfg.update(over)
+    blk = make(cfg, seed=zlib.crc32(("pf-" + name).encode()) % 1000)
+    dev = DeviceBlock(blk)
+    check_route(qed, blk, dev)
+    check_forward(qed, blk, dev, tol=PREFILL_TOL)
+
+
+def test_prefill_is_deterministic(qed):
+    from quantized_expert_decode_gb300.device import DeviceBlock
+    cfg = dict(T=96, H=256, I=128, E=8, K=2, I_shared=128, norm_topk=1, routed_scale=2.5,
+               routed_fmt=2, shared_fmt=2, zipf=False)
+    blk = make(cfg, seed=5)
+    dev = DeviceBlock(blk)
+    a, _, _ = run_forward(qed, dev, blk["x"])
+    b, _, _ = run_forward(qed, dev, blk["x"])
+    assert np.array_equal(a, b)

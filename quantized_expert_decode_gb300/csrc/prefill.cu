@@ -9,14 +9,20 @@
 //   down:    A = the slot's down rows, B = its h rows in bf16; epilogue y = acc * s_d
 // Swap-AB: weight rows are the MMA's M = 128 (the long dimension), tokens its N (16..128).
 //
-// One persistent CTA per SM walks the tiles (slot, token block, row block) of a launch:
-//   warps 0-3  producers: each K-block of 64, thread r dequantises row r of A straight into the
-//              128-byte-swizzled K-major layout tcgen05 reads, and threads n < N copy token row
-//              n of B; then they arrive on the stage's `full` mbarrier
-//   warp 4     one thread issues four tcgen05.mma (K = 16 each) per stage and commits the
-//              stage's `empty` mbarrier to their completion; after the last K-block it commits
-//              `accf`
-//   warps 0-3  epilogue: tcgen05.ld of the 128 x N accumulator tile, then the fused epilogue
+// One persistent CTA per SM walks the tiles (slot, token block, row block) of a launch, its
+// warps specialised:
+//   warps 0-7  producers, over the CTA's K-steps (64 wide) of all its tiles in order, thread
+//              (r, half) owning half a row: three steps ahead, cp.async copies that half of A
+//              row r's packed weight bytes into a raw buffer and of token row r < N of B (bf16)
+//              straight into its 128-byte-swizzled K-major slots; then, for the current step,
+//              it dequantises its raw half row into the swizzled bf16 A tile and the stage's
+//              `full` mbarrier collects the 256 arrivals (two producer warps per SMSP)
+//   warp 8     one thread issues four tcgen05.mma (K = 16 each) per stage into one of two TMEM
+//              accumulators and commits the stage's `empty` mbarrier to their completion; after
+//              a tile's last step it commits that accumulator's `accf`
+//   warps 9-12 epilogue: tcgen05.ld of the 128 x N tile (warp w reads TMEM lanes 32 (w % 4)..),
+//              the fused epilogue, then `tfree` hands the accumulator back to the MMA warp, so
+//              the next tile's MMAs run while the epilogue reads this one
 // K order: the dot product does not depend on the order of K, so within each block of 8 (int4)
 // or 16 (int2) elements K is permuted the same way in A and B — the order in which the
 // magic-number unpack produces bf16 pairs — and no byte shuffles are needed. The activations
@@ -34,12 +40,15 @@ namespace colimoe {
 
 namespace {
 
-constexpr int kTcM = 128;       // MMA M: weight rows per tile
-constexpr int kTcN = 128;       // max tokens per tile (MMA N, multiple of 16)
-constexpr int kTcKB = 64;       // K per stage (one 128-byte swizzle row of bf16)
-constexpr int kTcStages = 4;
-constexpr int kTcThreads = 160;  // 4 producer/epilogue warps + 1 MMA warp
-constexpr int kTcProd = 128;
+constexpr int kTcM = 128;        // MMA M: weight rows per tile
+constexpr int kTcN = 128;        // max tokens per tile (MMA N, multiple of 16)
+constexpr int kTcKB = 64;        // K per stage (one 128-byte swizzle row of bf16)
+constexpr int kTcStages = 5;
+constexpr int kTcAhead = 3;      // K-steps the producers' copies run ahead
+constexpr int kTcThreads = 416;  // producers 0-7, MMA warp 8, epilogue 9-12
+constexpr int kTcProd = 256, kTcEpi = 128;
+constexpr int kTcMmaWarp = 8;
+constexpr int kTcRawStride = 80; // bytes per raw weight row in a stage (>= 64, bank-spread)
 constexpr unsigned long long kTcWaitNs = 2000000000ull;
 
 struct PfParams {
@@ -55,14 +64,14 @@ struct PfParams {
 };
 
 struct TcSmem {  // after the 1024-aligned stage buffers
-    uint64_t full[kTcStages], empty[kTcStages], accf, drain;
+    uint64_t full[kTcStages], empty[kTcStages], accf[2], tfree[2], drain;
     uint32_t tmem_base;
     int abort;
     int pref[kMaxE + 2];  // tiles before slot g (slots 0..E-1 routed, E shared)
 };
 
-constexpr size_t kStageA = (size_t)kTcM * 128, kStageB = (size_t)kTcN * 128;
-constexpr size_t kTcSmemBytes = 1024 + kTcStages * (kStageA + kStageB) + sizeof(TcSmem);
+constexpr size_t kStageA = (size_t)kTcM * 128, kStageB = (size_t)kTcN * 128, kStageRaw = (size_t)kTcM * kTcRawStride;
+constexpr size_t kTcSmemBytes = 1024 + kTcStages * (kStageA + kStageB + kStageRaw) + sizeof(TcSmem);
 
 // position of element j of a K block in the permuted order of format fmt
 __host__ __device__ __forceinline__ int kperm(int fmt, int j) {
@@ -89,33 +98,32 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     return d;
 }
 
-// Dequantise one 16-byte chunk of packed weights to bf16 in the permuted K order: int4 gives
-// 32 values (4 chunks of 16 B), int2 64 (8 chunks), int8 16 (2 chunks). The bf16 magic: a field
-// f in bits 0..3 (resp. 0..1) of a halfword OR-ed with 0x4300 is the bf16 128 + f, exactly;
-// subtracting 128 + 8 (resp. 128 + 2) leaves f - 8 (resp. f - 2) exactly.
+// Dequantise 32 consecutive weights (int4: 4 words, int2: 2, int8: 8) to 16 bf16 pairs in the
+// permuted K order. The bf16 magic: a field f in bits 0..3 (resp. 0..1) of a halfword OR-ed
+// with 0x4300 is the bf16 128 + f, exactly; adding -(128 + 8) (resp. -(128 + 2)) leaves f - 8
+// (resp. f - 2) exactly. int8 bytes go through float (every int8 value is exact in bf16).
 template <int FMT>
-__device__ __forceinline__ void deq_chunk_bf16(const uint4 &q, uint32_t *out) {
-    const uint32_t wds[4] = {q.x, q.y, q.z, q.w};
+__device__ __forceinline__ void deq32_bf16(const uint32_t *w, uint32_t (&out)[16]) {
     if (FMT == COLI_FMT_INT4) {
         const uint32_t one = 0x3F803F80u, off = 0xC308C308u;  // 1.0, -136.0
 #pragma unroll
         for (int i = 0; i < 4; i++)
 #pragma unroll
             for (int m = 0; m < 4; m++)
-                out[4 * i + m] = bf16x2_fma(lop3_and_or(wds[i] >> (4 * m), 0x000F000Fu, 0x43004300u), one, off);
+                out[4 * i + m] = bf16x2_fma(lop3_and_or(w[i] >> (4 * m), 0x000F000Fu, 0x43004300u), one, off);
     } else if (FMT == COLI_FMT_INT2) {
         const uint32_t one = 0x3F803F80u, off = 0xC302C302u;  // 1.0, -130.0
 #pragma unroll
-        for (int i = 0; i < 4; i++)
+        for (int i = 0; i < 2; i++)
 #pragma unroll
             for (int m = 0; m < 8; m++)
-                out[8 * i + m] = bf16x2_fma(lop3_and_or(wds[i] >> (2 * m), 0x00030003u, 0x43004300u), one, off);
+                out[8 * i + m] = bf16x2_fma(lop3_and_or(w[i] >> (2 * m), 0x00030003u, 0x43004300u), one, off);
     } else {
 #pragma unroll
-        for (int i = 0; i < 4; i++) {
-            const int w = (int)wds[i];
-            out[2 * i] = pack_bf16((float)((w << 24) >> 24), (float)((w << 16) >> 24));
-            out[2 * i + 1] = pack_bf16((float)((w << 8) >> 24), (float)(w >> 24));
+        for (int i = 0; i < 8; i++) {
+            const int v = (int)w[i];
+            out[2 * i] = pack_bf16((float)((v << 24) >> 24), (float)((v << 16) >> 24));
+            out[2 * i + 1] = pack_bf16((float)((v << 8) >> 24), (float)(v >> 24));
         }
     }
 }
@@ -177,42 +185,111 @@ __device__ Tile make_tile(const PfParams &P, const TcSmem &ts, int t) {
     return T;
 }
 
-template <int FMT>
-__device__ __forceinline__ void produce_a(const PfParams &P, const Tile &T, int kb, uint8_t *sa, int r) {
-    // A row r: gate/up interleaved (even: gate j0 + r/2, odd: up), or down row d0 + r
-    const uint8_t *base;
-    int64_t rb;
-    if (P.down) {
-        rb = row_bytes(FMT, T.inter);
-        base = T.w0 + (size_t)min(T.row0 + r, P.H - 1) * rb;
-    } else {
-        rb = row_bytes(FMT, P.H);
-        const int j = min(T.row0 + (r >> 1), T.inter - 1);
-        base = ((r & 1) ? T.w1 : T.w0) + (size_t)j * rb;
-    }
-    constexpr int QB = FMT == COLI_FMT_INT4 ? 32 : FMT == COLI_FMT_INT2 ? 16 : 64;  // bytes per K-block
-    constexpr int NQ = QB / 16;
-    const uint8_t *src = base + (size_t)kb * QB;
-    uint4 q[NQ];
-#pragma unroll
-    for (int i = 0; i < NQ; i++) q[i] = __ldg(reinterpret_cast<const uint4 *>(src) + i);
-    uint32_t o[32];
-#pragma unroll
-    for (int i = 0; i < NQ; i++) deq_chunk_bf16<FMT>(q[i], o + i * (32 / NQ));
-#pragma unroll
-    for (int c = 0; c < 8; c++) st_sw128(sa, r, c, make_uint4(o[4 * c], o[4 * c + 1], o[4 * c + 2], o[4 * c + 3]));
+__device__ __forceinline__ void cp_async16(void *dst_smem, const void *src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst_smem)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
+// ask L2 for rows [r0, r1) of a matrix with rb bytes per row (16-byte multiples), 32 KB a piece
+__device__ void prefetch_rows_l2(const uint8_t *base, int r0, int r1, int64_t rb) {
+    if (r1 <= r0) return;
+    const uint8_t *p = base + (size_t)r0 * rb;
+    const int64_t n = (int64_t)(r1 - r0) * rb;
+    for (int64_t o = 0; o < n; o += 32768)
+        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p + o), "r"((uint32_t)(n - o < 32768 ? n - o : 32768))
+                     : "memory");
 }
 
-__device__ __forceinline__ void produce_b(const PfParams &P, const Tile &T, int kb, uint8_t *sb, int n) {
+// the weight rows of tile T
+__device__ void prefetch_tile_a(const PfParams &P, const Tile &T) {
+    if (P.down) {
+        prefetch_rows_l2(T.w0, T.row0, min(T.row0 + kTcM, P.H), row_bytes(T.fmt, T.inter));
+    } else {
+        const int j1 = min(T.row0 + kTcM / 2, T.inter);
+        prefetch_rows_l2(T.w0, T.row0, j1, row_bytes(T.fmt, P.H));
+        prefetch_rows_l2(T.w1, T.row0, j1, row_bytes(T.fmt, P.H));
+    }
+}
+
+__device__ __forceinline__ int qbytes(int fmt) { return fmt == COLI_FMT_INT4 ? 32 : fmt == COLI_FMT_INT2 ? 16 : 64; }
+
+__device__ __forceinline__ void cp_async8(void *dst_smem, const void *src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(smem_u32(dst_smem)), "l"(src) : "memory");
+}
+
+// The producer thread (r, h) of a tile: its half h of A row r (gate/up interleaved — even rows
+// gate j0 + r/2, odd rows up — or down row d0 + r) and of B row r (token n0 + r, clamped to the
+// buffer; rows >= N are not copied).
+struct ProdRow {
+    const uint8_t *a;   // packed weights of A row r at K-step 0, half h
+    const uint16_t *b;  // bf16 activations of B row r at K-step 0, half h
+    int qh;             // packed bytes per half K-step
+    bool has_b;
+};
+
+__device__ __forceinline__ ProdRow prod_row(const PfParams &P, const Tile &T, int r, int h) {
+    ProdRow pr;
+    const int qb = qbytes(T.fmt);
+    const uint8_t *base;
+    if (P.down) {
+        base = T.w0 + (size_t)min(T.row0 + r, P.H - 1) * row_bytes(T.fmt, T.inter);
+    } else {
+        const int j = min(T.row0 + (r >> 1), T.inter - 1);
+        base = ((r & 1) ? T.w1 : T.w0) + (size_t)j * row_bytes(T.fmt, P.H);
+    }
+    pr.qh = qb / 2;
+    pr.a = base + h * pr.qh;
     const int rows_total = P.T * P.K + P.T;
-    const int row = min(T.pbase + T.n0 + n, rows_total - 1);
-    const uint16_t *src = P.down ? P.hb + (size_t)row * P.ldh : P.xb + (size_t)row * P.H;
-    const uint4 *s4 = reinterpret_cast<const uint4 *>(src + (size_t)kb * kTcKB);
-    uint4 v[8];
+    const int row = min(T.pbase + T.n0 + r, rows_total - 1);
+    pr.b = (P.down ? P.hb + (size_t)row * P.ldh : P.xb + (size_t)row * P.H) + 32 * h;
+    pr.has_b = r < T.N;
+    return pr;
+}
+
+// K-step kb: cp.async of the half rows into the stage's raw buffer and B tile
+__device__ __forceinline__ void issue_step(const ProdRow &pr, int kb, uint8_t *raw, uint8_t *sb, int r, int h) {
+    const uint8_t *src = pr.a + (size_t)kb * 2 * pr.qh;
+    uint8_t *dst = raw + r * kTcRawStride + h * pr.qh;
+    if (pr.qh == 8) cp_async8(dst, src);
+    else
+        for (int i = 0; i < pr.qh / 16; i++) cp_async16(dst + 16 * i, src + 16 * i);
+    if (pr.has_b) {
+        const uint16_t *bs = pr.b + (size_t)kb * kTcKB;
 #pragma unroll
-    for (int c = 0; c < 8; c++) v[c] = __ldcg(s4 + c);
+        for (int c = 0; c < 4; c++) {
+            const int cc = 4 * h + c;
+            cp_async16(sb + (r >> 3) * 1024 + (r & 7) * 128 + ((cc ^ (r & 7)) << 4), bs + 8 * c);
+        }
+    }
+}
+
+// dequantise the thread's raw half row into chunks 4h..4h+3 of row r of the swizzled bf16 A tile
+template <int FMT>
+__device__ __forceinline__ void dequant_half(const uint8_t *raw, uint8_t *sa, int r, int h) {
+    constexpr int QH = (FMT == COLI_FMT_INT4 ? 32 : FMT == COLI_FMT_INT2 ? 16 : 64) / 2;
+    constexpr int NW = QH / 4;
+    uint32_t w[NW];
+    const uint8_t *src = raw + r * kTcRawStride + h * QH;
+    if (QH == 8) {
+        const uint2 v = *reinterpret_cast<const uint2 *>(src);
+        w[0] = v.x;
+        w[1] = v.y;
+    } else {
 #pragma unroll
-    for (int c = 0; c < 8; c++) st_sw128(sb, n, c, v[c]);
+        for (int i = 0; i < QH / 16; i++) {
+            const uint4 v = *reinterpret_cast<const uint4 *>(src + 16 * i);
+            w[4 * i] = v.x;
+            w[4 * i + 1] = v.y;
+            w[4 * i + 2] = v.z;
+            w[4 * i + 3] = v.w;
+        }
+    }
+    uint32_t o[16];
+    deq32_bf16<FMT>(w, o);
+#pragma unroll
+    for (int c = 0; c < 4; c++) st_sw128(sa, r, 4 * h + c, make_uint4(o[4 * c], o[4 * c + 1], o[4 * c + 2], o[4 * c + 3]));
 }
 
 __device__ __forceinline__ uint16_t bf16_bits(float f) {
@@ -222,15 +299,15 @@ __device__ __forceinline__ uint16_t bf16_bits(float f) {
 __global__ void __launch_bounds__(kTcThreads, 1) moe_prefill_tc_kernel(const PfParams P) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
-    uint8_t *sA = smem, *sB = smem + kTcStages * kStageA;
-    TcSmem &ts = *reinterpret_cast<TcSmem *>(smem + kTcStages * (kStageA + kStageB));
+    uint8_t *sA = smem, *sB = smem + kTcStages * kStageA, *sR = sB + kTcStages * kStageB;
+    TcSmem &ts = *reinterpret_cast<TcSmem *>(sR + kTcStages * kStageRaw);
     const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
     const int nslots = P.E + (P.Is > 0 ? 1 : 0);
 
     // tile prefix over the slots: per-thread chunk sums, a warp scan of the chunk sums, then
     // every thread writes its chunk's prefix entries
     {
-        constexpr int kChunks = kTcThreads;
+        constexpr int kChunks = 160;
         const int per = (nslots + kChunks - 1) / kChunks;
         auto tiles_of = [&](int g) {
             const int inter = g == P.E ? P.Is : P.I;
@@ -241,10 +318,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) moe_prefill_tc_kernel(const PfP
 #pragma unroll
         for (int i = 0; i < 8; i++) {
             const int g = tid * per + i;
-            loc[i] = (i < per && g < nslots) ? tiles_of(g) : 0;
+            loc[i] = (tid < kChunks && i < per && g < nslots) ? tiles_of(g) : 0;
             sum += loc[i];
         }
-        ts.pref[tid] = sum;  // scratch: chunk sums (pref is rewritten below)
+        if (tid < kChunks) ts.pref[tid] = sum;  // scratch: chunk sums (pref is rewritten below)
         __syncthreads();
         if (warp == 0) {
             int v[5], s5 = 0;
@@ -269,14 +346,16 @@ __global__ void __launch_bounds__(kTcThreads, 1) moe_prefill_tc_kernel(const PfP
             if (lane == 31) ts.pref[kMaxE + 1] = inc;  // total
         }
         __syncthreads();
-        int run = ts.pref[tid];
+        int run = tid < kChunks ? ts.pref[tid] : 0;
         const int total_tiles = ts.pref[kMaxE + 1];
         __syncthreads();
+        if (tid < kChunks) {
 #pragma unroll
-        for (int i = 0; i < 8; i++) {
-            const int g = tid * per + i;
-            if (i < per && g < nslots) ts.pref[g] = run;
-            run += loc[i];
+            for (int i = 0; i < 8; i++) {
+                const int g = tid * per + i;
+                if (i < per && g < nslots) ts.pref[g] = run;
+                run += loc[i];
+            }
         }
         if (tid == 0) ts.pref[nslots] = total_tiles;
     }
@@ -286,12 +365,15 @@ __global__ void __launch_bounds__(kTcThreads, 1) moe_prefill_tc_kernel(const PfP
             mbar_init(&ts.full[s], kTcProd);
             mbar_init(&ts.empty[s], 1);
         }
-        mbar_init(&ts.accf, 1);
+        for (int b = 0; b < 2; b++) {
+            mbar_init(&ts.accf[b], 1);
+            mbar_init(&ts.tfree[b], kTcEpi);
+        }
         mbar_init(&ts.drain, 1);
         fence_mbar_init();
     }
-    if (warp == 4) {
-        tmem_alloc(&ts.tmem_base, kTcN);
+    if (warp == kTcMmaWarp) {
+        tmem_alloc(&ts.tmem_base, 2 * kTcN);
         tmem_relinquish();
     }
     tc_fence_before_sync();
@@ -299,79 +381,69 @@ __global__ void __launch_bounds__(kTcThreads, 1) moe_prefill_tc_kernel(const PfP
     tc_fence_after_sync();
     const uint32_t tbase = ts.tmem_base;
     const int total = ts.pref[nslots];
+    const int G = gridDim.x;
+    auto nkb_of = [&](const Tile &T) { return (P.down ? T.inter : P.H) / kTcKB; };
 
-    uint32_t gk = 0;  // K-blocks handled by this CTA so far (stage ring position)
-    int it = 0;       // tiles handled so far
-    for (int t = blockIdx.x; t < total; t += gridDim.x, it++) {
-        const Tile T = make_tile(P, ts, t);
-        const int nkb = (P.down ? T.inter : P.H) / kTcKB;
-        if (warp < 4) {
-            // scales of this thread's epilogue row, loaded ahead of the K loop
-            float sc0 = 0.f, sc1 = 0.f;
-            if (P.down) {
-                sc0 = __ldg(T.s0 + min(T.row0 + tid, P.H - 1));
-            } else if ((tid & 1) == 0) {
-                const int j = min(T.row0 + (tid >> 1), T.inter - 1);
-                sc0 = __ldg(T.s0 + j);
-                sc1 = __ldg(T.s1 + j);
-            }
-            for (int kb = 0; kb < nkb; kb++, gk++) {
-                const int s = gk % kTcStages;
-                const uint32_t use = gk / kTcStages;
-                if (use > 0 && !mbar_wait_bounded(&ts.empty[s], (use - 1) & 1, ts, P.err)) break;
-                uint8_t *sa = sA + s * kStageA, *sb = sB + s * kStageB;
-                if (T.fmt == COLI_FMT_INT4) produce_a<COLI_FMT_INT4>(P, T, kb, sa, tid);
-                else if (T.fmt == COLI_FMT_INT8) produce_a<COLI_FMT_INT8>(P, T, kb, sa, tid);
-                else produce_a<COLI_FMT_INT2>(P, T, kb, sa, tid);
-                if (tid < T.N) produce_b(P, T, kb, sb, tid);
-                fence_async_smem();
-                mbar_arrive(&ts.full[s]);
-            }
-            // epilogue
-            if (ts.abort == 0 && mbar_wait_bounded(&ts.accf, it & 1, ts, P.err)) {
-                tc_fence_after_sync();
-                const uint32_t trow = tbase + ((uint32_t)(warp * 32) << 16);
-                const int R = tid;  // accumulator row (TMEM lane)
-                for (int c0 = 0; c0 < T.N; c0 += 16) {
-                    uint32_t r[16];
-                    tmem_ld_x16(trow + c0, r);
-                    tmem_ld_wait();
-                    if (P.down) {
-                        const int d = T.row0 + R;
-                        if (d < P.H) {
-#pragma unroll
-                            for (int i = 0; i < 16; i++) {
-                                const int n = c0 + i;
-                                if (n < T.ncur)
-                                    P.y[(size_t)(T.pbase + T.n0 + n) * P.H + d] = __uint_as_float(r[i]) * sc0;
-                            }
-                        }
-                    } else {
-                        uint32_t pr[16];
-#pragma unroll
-                        for (int i = 0; i < 16; i++) pr[i] = __shfl_xor_sync(0xffffffffu, r[i], 1);
-                        const int j = T.row0 + (R >> 1);
-                        if ((R & 1) == 0 && j < T.inter) {
-                            const int col = kperm(T.fmt, j);
-#pragma unroll
-                            for (int i = 0; i < 16; i++) {
-                                const int n = c0 + i;
-                                if (n < T.ncur) {
-                                    const float gv = __uint_as_float(r[i]) * sc0;
-                                    const float uv = __uint_as_float(pr[i]) * sc1;
-                                    const float hv = gv / (1.f + expf(-gv)) * uv;
-                                    P.hb[(size_t)(T.pbase + T.n0 + n) * P.ldh + col] = bf16_bits(hv);
-                                }
-                            }
-                        }
+    if (warp < 8) {
+        // ---------------- producers
+        const int r = tid & 127, h = tid >> 7;
+        int ti = blockIdx.x, ki = 0;  // issue cursor: tile, K-step
+        Tile Ti = ti < total ? make_tile(P, ts, ti) : Tile{};
+        ProdRow pi = prod_row(P, Ti, r, h);
+        int nki = ti < total ? nkb_of(Ti) : 0;
+        // weight rows go to L2 one tile ahead of the copies that read them
+        if (tid == 0 && ti < total) prefetch_tile_a(P, Ti);
+        if (tid == 0 && ti + G < total) prefetch_tile_a(P, make_tile(P, ts, ti + G));
+        uint32_t gi = 0;              // steps issued
+        auto issue_next = [&]() {
+            if (ti < total) {
+                const int s = gi % kTcStages;
+                const uint32_t use = gi / kTcStages;
+                if (use > 0 && !mbar_wait_bounded(&ts.empty[s], (use - 1) & 1, ts, P.err)) return;
+                issue_step(pi, ki, sR + s * kStageRaw, sB + s * kStageB, r, h);
+                gi++;
+                if (++ki == nki) {
+                    ki = 0;
+                    ti += G;
+                    if (ti < total) {
+                        Ti = make_tile(P, ts, ti);
+                        pi = prod_row(P, Ti, r, h);
+                        nki = nkb_of(Ti);
+                        if (tid == 0 && ti + G < total) prefetch_tile_a(P, make_tile(P, ts, ti + G));
                     }
                 }
             }
-            tc_fence_before_sync();
-            named_bar(1, kTcThreads);  // the accumulator may be overwritten
-        } else {
-            if (lane == 0) {
-                const uint32_t idesc = idesc_bf16_f32(kTcM, T.N);
+            cp_async_commit();
+        };
+        for (int d = 0; d < kTcAhead; d++) issue_next();
+        uint32_t gp = 0;  // steps processed
+        for (int t = blockIdx.x; t < total && !ts.abort; t += G) {
+            const Tile T = make_tile(P, ts, t);
+            const int fmt = T.fmt, nkb = nkb_of(T);
+            for (int kb = 0; kb < nkb; kb++, gp++) {
+                issue_next();
+                cp_async_wait<kTcAhead>();  // this step's copies have landed
+                const int s = gp % kTcStages;
+                if (fmt == COLI_FMT_INT4) dequant_half<COLI_FMT_INT4>(sR + s * kStageRaw, sA + s * kStageA, r, h);
+                else if (fmt == COLI_FMT_INT8) dequant_half<COLI_FMT_INT8>(sR + s * kStageRaw, sA + s * kStageA, r, h);
+                else dequant_half<COLI_FMT_INT2>(sR + s * kStageRaw, sA + s * kStageA, r, h);
+                fence_async_smem();
+                mbar_arrive(&ts.full[s]);
+                if (ts.abort) break;
+            }
+        }
+        cp_async_wait<0>();
+    } else if (warp == kTcMmaWarp) {
+        // ---------------- MMA issuer
+        if (lane == 0) {
+            uint32_t gk = 0;
+            int it = 0;
+            for (int t = blockIdx.x; t < total && !ts.abort; t += G, it++) {
+                const Tile T = make_tile(P, ts, t);
+                const int nkb = nkb_of(T), b = it & 1;
+                if (it >= 2 && !mbar_wait_bounded(&ts.tfree[b], ((it >> 1) - 1) & 1, ts, P.err)) break;
+                tc_fence_after_sync();
+                const uint32_t idesc = idesc_bf16_f32(kTcM, T.N), dcol = tbase + b * kTcN;
                 for (int kb = 0; kb < nkb; kb++, gk++) {
                     const int s = gk % kTcStages;
                     if (!mbar_wait_bounded(&ts.full[s], (gk / kTcStages) & 1, ts, P.err)) break;
@@ -379,30 +451,76 @@ __global__ void __launch_bounds__(kTcThreads, 1) moe_prefill_tc_kernel(const PfP
                     const uint32_t a0 = smem_u32(sA + s * kStageA), b0 = smem_u32(sB + s * kStageB);
 #pragma unroll
                     for (int k = 0; k < kTcKB / 16; k++)
-                        tc_mma_bf16(tbase, sdesc_k_sw128(a0 + 32 * k), sdesc_k_sw128(b0 + 32 * k), idesc,
-                                    (kb | k) != 0);
+                        tc_mma_bf16(dcol, sdesc_k_sw128(a0 + 32 * k), sdesc_k_sw128(b0 + 32 * k), idesc, (kb | k) != 0);
                     tc_commit(&ts.empty[s]);
                 }
-                tc_commit(&ts.accf);
-            } else {
-                gk += nkb;
+                tc_commit(&ts.accf[b]);
             }
-            __syncwarp();
-            named_bar(1, kTcThreads);
-            tc_fence_after_sync();
+            // every MMA issued has completed before the tensor memory is freed
+            tc_commit(&ts.drain);
+            mbar_wait_bounded(&ts.drain, 0, ts, P.err);
         }
-        if (*reinterpret_cast<volatile int *>(&ts.abort)) break;
-    }
-    // every MMA this CTA issued has completed before the tensor memory is freed
-    if (warp == 4 && lane == 0) {
-        tc_commit(&ts.drain);
-        mbar_wait_bounded(&ts.drain, 0, ts, P.err);
+        __syncwarp();
+    } else {
+        // ---------------- epilogue
+        const int R = 32 * (warp % 4) + lane;  // accumulator row = TMEM lane of this thread
+        int it = 0;
+        for (int t = blockIdx.x; t < total && !ts.abort; t += G, it++) {
+            const Tile T = make_tile(P, ts, t);
+            const int b = it & 1;
+            float sc0 = 0.f, sc1 = 0.f;
+            if (P.down) {
+                sc0 = __ldg(T.s0 + min(T.row0 + R, P.H - 1));
+            } else if ((R & 1) == 0) {
+                const int j = min(T.row0 + (R >> 1), T.inter - 1);
+                sc0 = __ldg(T.s0 + j);
+                sc1 = __ldg(T.s1 + j);
+            }
+            if (!mbar_wait_bounded(&ts.accf[b], (it >> 1) & 1, ts, P.err)) break;
+            tc_fence_after_sync();
+            const uint32_t trow = tbase + b * kTcN + ((uint32_t)(32 * (warp % 4)) << 16);
+            for (int c0 = 0; c0 < T.N; c0 += 16) {
+                uint32_t v[16];
+                tmem_ld_x16(trow + c0, v);
+                tmem_ld_wait();
+                if (P.down) {
+                    const int d = T.row0 + R;
+                    if (d < P.H) {
+#pragma unroll
+                        for (int i = 0; i < 16; i++) {
+                            const int n = c0 + i;
+                            if (n < T.ncur) P.y[(size_t)(T.pbase + T.n0 + n) * P.H + d] = __uint_as_float(v[i]) * sc0;
+                        }
+                    }
+                } else {
+                    uint32_t pv[16];
+#pragma unroll
+                    for (int i = 0; i < 16; i++) pv[i] = __shfl_xor_sync(0xffffffffu, v[i], 1);
+                    const int j = T.row0 + (R >> 1);
+                    if ((R & 1) == 0 && j < T.inter) {
+                        const int col = kperm(T.fmt, j);
+#pragma unroll
+                        for (int i = 0; i < 16; i++) {
+                            const int n = c0 + i;
+                            if (n < T.ncur) {
+                                const float gv = __uint_as_float(v[i]) * sc0;
+                                const float uv = __uint_as_float(pv[i]) * sc1;
+                                const float hv = gv / (1.f + expf(-gv)) * uv;
+                                P.hb[(size_t)(T.pbase + T.n0 + n) * P.ldh + col] = bf16_bits(hv);
+                            }
+                        }
+                    }
+                }
+            }
+            tc_fence_before_sync();
+            mbar_arrive(&ts.tfree[b]);
+        }
     }
     tc_fence_before_sync();
     __syncthreads();
-    if (warp == 4) {
+    if (warp == kTcMmaWarp) {
         tc_fence_after_sync();
-        tmem_dealloc(tbase, kTcN);
+        tmem_dealloc(tbase, 2 * kTcN);
     }
 }
 

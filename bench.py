@@ -41,7 +41,9 @@ DECODE_MAX_T = 64  # the library runs T <= 64 as one persistent decode kernel
 # DRAM bytes (read + write) per launch of the roofline kernel measured by ncu
 # (dram__bytes_read.sum + dram__bytes_write.sum), keyed by workload, with the hash of the kernel
 # sources they were taken on; a changed kernel reports null until it is measured again.
-NCU_TRAFFIC = {}
+NCU_TRAFFIC = {
+    1: {"bytes": 25946368, "src": "43303e63175ee2b3"},  # moe_decode1_kernel, small decode
+}
 
 
 def kernel_source_hash() -> str:
@@ -62,7 +64,40 @@ def parse():
     ap.add_argument("--workload", type=int, default=1, choices=sorted(synth.CONFIGS))
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="CPU work budget of the oracle baseline sample")
+    ap.add_argument("--calls", type=int, default=0,
+                    help="profiling mode: only run this many forward calls (L2 flushed between "
+                         "them) and exit; for ncu captures")
+    ap.add_argument("--experts", type=int, default=0, help="profiling mode: override E")
+    ap.add_argument("--tokens", type=int, default=0, help="profiling mode: override T")
     return ap.parse_args()
+
+
+def run_calls(args):
+    """Profiling mode: N plain forward calls of the workload (optionally with fewer experts or
+    tokens, to keep an ncu capture small), a 64 MiB buffer written between them."""
+    import torch
+    import quantized_expert_decode_gb300 as q
+    from quantized_expert_decode_gb300.device import DeviceBlock
+    over = {}
+    if args.experts:
+        over["E"] = args.experts
+    if args.tokens:
+        over["T"] = args.tokens
+    cfg = synth.config(args.workload, **over)
+    blk = synth.make_block(cfg, seed=synth.seed_for(args.workload))
+    dev = DeviceBlock(blk)
+    T, H = cfg["T"], cfg["H"]
+    xs = torch.from_numpy(synth.make_x_batches(cfg, 7, 4)).cuda()
+    out = torch.empty((T, H), dtype=torch.float32, device="cuda")
+    flush = torch.empty(16 << 20, dtype=torch.float32, device="cuda")
+    for i in range(args.calls):
+        flush.fill_(float(i))
+        q.coli_moe_forward(dev.desc, xs[i % 4], dev.Wr, dev.bias, dev.table, dev.shared, out,
+                           ws=dev.ws, ws_bytes=dev.ws_bytes)
+    q.coli_moe_check(dev.ws)
+    torch.cuda.synchronize()
+    print(json.dumps({"calls": args.calls, "workload": cfg["name"], "T": T, "E": cfg["E"],
+                      "out_abs_sum": float(out.abs().sum())}))
 
 
 # ------------------------------------------------------------------ algorithmic bytes
@@ -86,13 +121,19 @@ def step_bytes(cfg, n_active):
                 gateup=n_active * gu + gu_s, down=n_active * dn + dn_s)
 
 
-def load_peaks():
+def load_peaks(kind="hbm"):
+    """(peak, 'measured'|'fallback'): HBM copy GB/s, or dense bf16 TFLOP/s (burst)."""
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
             p = json.load(f)
-        return float(p["hbm_gbs"]), "measured"
+        return (float(p["hbm_gbs"]) if kind == "hbm" else float(p["bf16_tflops"])), "measured"
     except Exception:
-        return 6800.0, "fallback"
+        return (6800.0 if kind == "hbm" else 1900.0), "fallback"
+
+
+def gateup_flops(cfg, assignments):
+    """FLOPs of the gate and up products of one block call (2 per multiply-add)."""
+    return 2 * cfg["H"] * 2 * (assignments * cfg["I"] + cfg["T"] * cfg["I_shared"])
 
 
 # ------------------------------------------------------------------ clocks
@@ -282,11 +323,17 @@ def run_colimoe(args, rank, world, local):
                             for b in bytes_per], np.float64)
         launches = 1 if T <= 8 else 2
     else:
-        kname = "gateup_kernel"
+        # T > 64: the expert products run as tcgen05 GEMMs; the gate/up launch (with its bf16
+        # activation pre-pass) is the dominant kernel and its bound is the tensor pipe
+        kname = "moe_prefill_tc_kernel"
         k_ms = stage[:, 1]
         k_bytes = np.array([b["gateup"] for b in bytes_per], np.float64)
-        launches = 6
+        launches = 7  # router partial, select, bucket, pre-pass, two GEMMs, combine
     achieved = float(k_bytes.sum() / (k_ms.sum() / 1e3) / 1e9)
+    if not fused:
+        flops = gateup_flops(cfg, T * K)
+        tc_peak, tc_kind = load_peaks("tensor")
+        tc_achieved = flops / (float(k_ms.mean()) / 1e3) / 1e12
     block_gbs = float(sum(b["total"] for b in bytes_per) / total_s / 1e9)
     expert_gbs = float(sum(b["experts"] for b in bytes_per) / total_s / 1e9)
     src = kernel_source_hash()
@@ -334,13 +381,20 @@ def run_colimoe(args, rank, world, local):
         "active_experts_mean": float(np.mean(n_active)),
         "stages_ms": ({"prologue": float(stage[:, 0].mean()), kname: k_launch_ms}
                       if fused else
-                      {"route": float(stage[:, 0].mean()), "gateup": k_launch_ms,
-                       "down": float(stage[:, 2].mean()), "combine": float(stage[:, 3].mean())}),
-        "roofline": {"kernel": kname, "bound": "hbm", "achieved": achieved,
-                     "peak": hbm_peak, "peak_kind": peak_kind, "unit": "GB/s",
-                     "frac": achieved / hbm_peak, "traffic": traffic,
-                     "algorithmic_bytes_per_launch": float(k_bytes.mean()),
-                     "avg_launch_ms": k_launch_ms, "kernel_src": src},
+                      {"route": float(stage[:, 0].mean()), "prepass_gateup_gemm": k_launch_ms,
+                       "down_gemm": float(stage[:, 2].mean()), "combine": float(stage[:, 3].mean())}),
+        "roofline": ({"kernel": kname, "bound": "hbm", "achieved": achieved,
+                      "peak": hbm_peak, "peak_kind": peak_kind, "unit": "GB/s",
+                      "frac": achieved / hbm_peak, "traffic": traffic,
+                      "algorithmic_bytes_per_launch": float(k_bytes.mean()),
+                      "avg_launch_ms": k_launch_ms, "kernel_src": src}
+                     if fused else
+                     {"kernel": kname, "bound": "tensor", "achieved": tc_achieved,
+                      "peak": tc_peak, "peak_kind": tc_kind + " bf16 burst", "unit": "TFLOP/s",
+                      "frac": tc_achieved / tc_peak, "traffic": traffic,
+                      "algorithmic_flops_per_launch": float(gateup_flops(cfg, T * K)),
+                      "weight_bytes_per_launch": float(k_bytes.mean()),
+                      "avg_launch_ms": k_launch_ms, "kernel_src": src}),
         "cpu_baseline": cpu,
         "e2e": {"value": tokens / e2e_max, "unit": UNIT, "h2d_bytes_per_step": T * H * 4,
                 "d2h_bytes_per_step": T * H * 4},
@@ -385,6 +439,9 @@ def run_reference(args, rank, world):
 
 def main():
     args = parse()
+    if args.calls:
+        run_calls(args)
+        return
     rank, world, local = dist_init(args.gpus)
     if args.impl == "reference":
         res = run_reference(args, rank, world)

@@ -14,8 +14,9 @@
 //   C  routed gate/up rows: h = silu(gate.x * s_g) * (up.x * s_u)   (moe() phases C/D)
 //   D  down rows: y = (down.h) * s_d, for every selected expert and the shared one
 //   E  combine: out = sum_k w_k y_k in selection order + y_shared   (moe() phases C/D/E)
-// Units of B/C are one row pair (gate row j, up row j) of one expert for one group of up to
-// NV tokens; units of D are one down row. A CTA walks its share in segments that have the same
+// Units of B/C are two row pairs (gate and up rows j, j+1) of one expert for one group of up to
+// NV tokens; units of D are four down rows. Each phase's units are handed out in chunks by an
+// atomic counter (CTAs whose units are cheaper take more). A CTA walks its share in segments that have the same
 // expert and tokens: the segment's activations are staged once in shared memory (pre-scaled and
 // permuted, see qdot.cuh), then each warp streams its units' rows with 16-byte loads kept
 // several chunks ahead in registers, across unit boundaries.
@@ -191,7 +192,35 @@ __device__ __noinline__ void route_local(const DecParams &P, float *scratch, con
     const RScratch s = rscratch_of(scratch, P);
     const int T = P.T, E = P.E, K = P.K, TE = T * E;
     // 1. logits -> sigmoid scores and choices (all loads of a thread issued together)
-    for (int i = tid; i < TE; i += kNT) {
+    if (!from_partials) {  // slice 0 holds the summed logits: batch a thread's loads
+        constexpr int B = 8;
+        for (int i0 = tid; i0 < TE; i0 += kNT * B) {
+            float lg[B], bs[B];
+#pragma unroll
+            for (int j = 0; j < B; j++) {
+                const int i = i0 + j * kNT;
+                if (i < TE) {
+                    lg[j] = __ldcg(P.part + i);
+                    bs[j] = __ldg(P.bias + i % E);
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < B; j++) {
+                const int i = i0 + j * kNT;
+                if (i < TE) {
+                    const float sv = 1.f / (1.f + expf(-lg[j]));
+                    const float cv = sv + bs[j];
+                    s.sg[i] = sv;
+                    s.ch[i] = cv;
+                    if (out) {
+                        P.sig[i] = sv;
+                        P.choice[i] = cv;
+                    }
+                }
+            }
+        }
+    }
+    for (int i = tid; i < TE && from_partials; i += kNT) {
         float lg = 0.f;
         if (from_partials) {
             float a[16];
@@ -453,6 +482,7 @@ struct Seg {  // one segment piece: units of one expert and token group (broadca
 struct Misc {
     Seg sg;
     int skey[4];
+    int chunk;                // the chunk this CTA took from a phase queue
     int xshift;               // integer core: X = round(x * 2^xshift)
     float xinv;               // 2^-xshift
     float redf[kNW];
@@ -659,6 +689,20 @@ __device__ void down_units_flt(const DecParams &P, const Seg &g, const float *xs
         });
 }
 
+template <int NVF>
+__device__ void run_units_flt(const DecParams &P, const Seg &g, bool down, const void *xs, const Misc &m) {
+    const float *xf = static_cast<const float *>(xs);
+    if (down) {
+        if (g.fmt == COLI_FMT_INT4) down_units_flt<COLI_FMT_INT4, NVF>(P, g, xf, m);
+        else if (g.fmt == COLI_FMT_INT8) down_units_flt<COLI_FMT_INT8, NVF>(P, g, xf, m);
+        else down_units_flt<COLI_FMT_INT2, NVF>(P, g, xf, m);
+    } else {
+        if (g.fmt == COLI_FMT_INT4) gateup_units_flt<COLI_FMT_INT4, NVF>(P, g, xf, m);
+        else if (g.fmt == COLI_FMT_INT8) gateup_units_flt<COLI_FMT_INT8, NVF>(P, g, xf, m);
+        else gateup_units_flt<COLI_FMT_INT2, NVF>(P, g, xf, m);
+    }
+}
+
 template <int NV>
 __device__ void run_units(const DecParams &P, const Seg &g, bool down, const void *xs, const Misc &m) {
     if (g.nv == 1) {
@@ -674,16 +718,19 @@ __device__ void run_units(const DecParams &P, const Seg &g, bool down, const voi
         return;
     }
     if constexpr (NV > 1) {
-        const float *xf = static_cast<const float *>(xs);
-        if (down) {
-            if (g.fmt == COLI_FMT_INT4) down_units_flt<COLI_FMT_INT4, NV>(P, g, xf, m);
-            else if (g.fmt == COLI_FMT_INT8) down_units_flt<COLI_FMT_INT8, NV>(P, g, xf, m);
-            else down_units_flt<COLI_FMT_INT2, NV>(P, g, xf, m);
-        } else {
-            if (g.fmt == COLI_FMT_INT4) gateup_units_flt<COLI_FMT_INT4, NV>(P, g, xf, m);
-            else if (g.fmt == COLI_FMT_INT8) gateup_units_flt<COLI_FMT_INT8, NV>(P, g, xf, m);
-            else gateup_units_flt<COLI_FMT_INT2, NV>(P, g, xf, m);
+        // the float core sized to the group's own token count (a partial last group of an
+        // expert computes no lanes for tokens it does not have)
+        if constexpr (NV > 2) {
+            if (g.nv == 2) {
+                run_units_flt<2>(P, g, down, xs, m);
+                return;
+            }
+            if (g.nv == 3) {
+                run_units_flt<3>(P, g, down, xs, m);
+                return;
+            }
         }
+        run_units_flt<NV>(P, g, down, xs, m);
     }
 }
 
@@ -827,6 +874,28 @@ __device__ void run_share(const DecParams &P, const RTab &rt, int b, int e, bool
     __syncthreads();
 }
 
+constexpr int kChunk = 64;  // units per chunk of a phase queue
+
+// Dynamic shares: chunks of kChunk units, handed out in order by the phase's counter, so that a
+// CTA whose units are cheaper (single-token groups on the integer core) takes more of them.
+// A chunk is taken only when the CTA is about to work on it. Returns the units this CTA did.
+template <int NV>
+__device__ int run_queue(const DecParams &P, const RTab &rt, int tot, int *q, bool down, bool shared_phase,
+                         const int *off, int nslots, int U, void *xs, Misc &m) {
+    int done = 0;
+    for (;;) {
+        if (threadIdx.x == 0) m.chunk = atomicAdd(q, 1);
+        __syncthreads();
+        const int b = m.chunk * kChunk;
+        __syncthreads();  // every thread has read the chunk before thread 0 takes the next
+        if (b >= tot) break;
+        const int e = min(tot, b + kChunk);
+        run_share<NV>(P, rt, b, e, down, shared_phase, off, nslots, U, xs, m);
+        done += e - b;
+    }
+    return done;
+}
+
 template <int NV>
 __global__ void __launch_bounds__(kNT, 2) moe_decode_kernel(const DecParams P) {
     extern __shared__ __align__(128) uint8_t smem[];
@@ -857,7 +926,7 @@ __global__ void __launch_bounds__(kNT, 2) moe_decode_kernel(const DecParams P) {
 
     // ---------------- B: the shared expert's gate/up (independent of routing)
     if (P.Is > 0)
-        run_share<NV>(P, rt, range_lo(P.G_sh, c, G), range_lo(P.G_sh, c + 1, G), false, true, nullptr, 0, -1, xs, m);
+        run_queue<NV>(P, rt, P.G_sh, &P.ctrl->q_b, false, true, nullptr, 0, -1, xs, m);
 
     // ---------------- R: routing, by this CTA for itself
     if (tid == 0) {
@@ -871,16 +940,15 @@ __global__ void __launch_bounds__(kNT, 2) moe_decode_kernel(const DecParams P) {
 
     // ---------------- C: routed gate/up
     const int gu_tot = rt.gu_off[U];
-    run_share<NV>(P, rt, range_lo(gu_tot, c, G), range_lo(gu_tot, c + 1, G), false, false, rt.gu_off, U, U, xs, m);
+    run_queue<NV>(P, rt, gu_tot, &P.ctrl->q_c, false, false, rt.gu_off, U, U, xs, m);
 
     // ---------------- D: down rows of every expert
     const int nslots = U + (P.Is > 0 ? 1 : 0);
     const int dn_tot = rt.dn_off[nslots];
-    const int db = range_lo(dn_tot, c, G), de = range_lo(dn_tot, c + 1, G);
-    run_share<NV>(P, rt, db, de, true, false, rt.dn_off, nslots, U, xs, m);
+    const int dn_mine = run_queue<NV>(P, rt, dn_tot, &P.ctrl->q_d, true, false, rt.dn_off, nslots, U, xs, m);
     if (tid == 0) {
         __threadfence();
-        atomicAdd(&P.ctrl->dn_done, de - db);
+        atomicAdd(&P.ctrl->dn_done, dn_mine);
     }
 
     // ---------------- E: combine this CTA's rows of out

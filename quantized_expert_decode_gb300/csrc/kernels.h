@@ -31,7 +31,8 @@ constexpr int kDecMaxT = 64;              // the persistent decode kernel serves
 struct DecCtrl {
     int err, router_done, dn_done;
     int gu_all;                        // single-token kernel: finished gate/up units, all slots
-    int pad[12];
+    int q_b, q_c, q_d;                 // token-group kernel: next chunk of phases B, C, D
+    int pad[9];
     int hmax[kMaxK + 1];               // single-token kernel: max |h| per slot (float bits)
     int gu_done[kMaxE + 1];            // finished gate/up units per slot (shared: index kMaxE)
 };

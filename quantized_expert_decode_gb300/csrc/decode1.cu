@@ -19,8 +19,9 @@
 //      for its own block of output rows d, y[slot][d] for every slot, then
 //      out[d] = sum_k w_k y[pos_k][d] in selection order, + y[U][d]  (moe() phases C/D/E)
 //      — the combine needs no y round trip through memory and no final wait.
-// Warps walk their gate/up and down units without CTA barriers; each CTA asks L2 for the rows
-// of its next phase as soon as it knows them (cp.async.bulk.prefetch). Every wait is bounded.
+// Warps walk their gate/up and down units without CTA barriers. (Asking L2 for each phase's
+// rows ahead with cp.async.bulk.prefetch was measured: it slowed large decode by 11 %, so the
+// loads go straight to HBM.) Every wait is bounded.
 #include <algorithm>
 
 #include "decode_parts.cuh"
@@ -354,22 +355,6 @@ __device__ __noinline__ void down_run(const DecParams &P, D1S &m, const uint8_t 
         });
 }
 
-// the CTA's gate/up rows of units [b, e) go to L2 ahead of their loads
-__device__ void prefetch_gateup(const DecParams &P, const D1S &m, int b, int e, bool shared, int fmt) {
-    const int inter = shared ? P.Is : P.I, per = (inter + 1) / 2;
-    const int64_t rb = row_bytes(fmt, P.H);
-    for (int l = b; l < e;) {
-        const int slot = shared ? kShSlot : l / per;
-        const int base = shared ? 0 : slot * per;
-        const int hi = min(e, base + per);
-        const Rec &r = m.rec[slot];
-        const int j0 = 2 * (l - base), j1 = min(2 * (hi - base), inter);
-        prefetch_rows(r.gw, j0, j1, rb);
-        prefetch_rows(r.uw, j0, j1, rb);
-        l = hi;
-    }
-}
-
 template <int RF, int SF>
 __global__ void __launch_bounds__(kNT, 2) moe_decode1_kernel(const DecParams P) {
     extern __shared__ __align__(128) uint8_t smem[];
@@ -387,7 +372,6 @@ __global__ void __launch_bounds__(kNT, 2) moe_decode1_kernel(const DecParams P) 
     if (tid == 0 && P.Is > 0) m.rec[kShSlot] = rec_of(P.shared);
     __syncthreads();
     const int bb = range_lo(P.G_sh, c, G), be = range_lo(P.G_sh, c + 1, G);
-    if (tid == 0 && be > bb) prefetch_gateup(P, m, bb, be, true, SF);
     // routing reads the bias and the expert table right after its wait: warm them in L2
     {
         const int lb = (P.E * 4 + 127) / 128, lt = (P.E * (int)sizeof(coli_moe_expert) + 127) / 128;
@@ -423,7 +407,6 @@ __global__ void __launch_bounds__(kNT, 2) moe_decode1_kernel(const DecParams P) 
     // ---------------- C: routed gate/up
     const int gu_tot = U * GUPER;
     const int cb = range_lo(gu_tot, c, G), ce = range_lo(gu_tot, c + 1, G);
-    if (tid == 0) prefetch_gateup(P, m, cb, ce, false, RF);
     gateup_run<RF>(P, m, xq_r, cb, ce, false);
     __syncthreads();
     if (tid < U || (tid == kShSlot && P.Is > 0))
@@ -434,9 +417,6 @@ __global__ void __launch_bounds__(kNT, 2) moe_decode1_kernel(const DecParams P) 
     if (tid == 0) {
         __threadfence();
         atomicAdd(&P.ctrl->gu_all, (be - bb) + (ce - cb));
-        // this CTA's down rows, every slot, to L2 while the others finish gate/up
-        for (int u = 0; u < U; u++) prefetch_rows(m.rec[u].dw, 4 * gb, min(4 * ge, P.H), row_bytes(RF, P.I));
-        if (P.Is > 0) prefetch_rows(m.rec[kShSlot].dw, 4 * gb, min(4 * ge, P.H), row_bytes(SF, P.Is));
     }
 
     // ---------------- D: all h staged, this CTA's output rows for every slot, combine

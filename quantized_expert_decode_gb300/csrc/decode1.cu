@@ -15,10 +15,12 @@
 //      is slot U. Their weight pointers go to shared memory in one round trip.
 //   C  routed gate/up rows: h = silu(gate.x * s_g) * (up.x * s_u); every CTA also records the
 //      largest |h| of each slot it wrote, the block fixed-point exponent of the down step
-//   D  once every gate/up row is in (one counter), each CTA stages ALL h vectors and computes,
-//      for its own block of output rows d, y[slot][d] for every slot, then
+//   D  once every gate/up row is in (one counter): (slot, 4-row group) units split slot-major
+//      over the CTAs, so each stages only the one or two h vectors its units read; y rows
+//      go to the workspace
+//   E  once every down row is in (one counter): each CTA's rows of
 //      out[d] = sum_k w_k y[pos_k][d] in selection order, + y[U][d]  (moe() phases C/D/E)
-//      — the combine needs no y round trip through memory and no final wait.
+//      (staging every h vector in every CTA to combine without y was measured slower)
 // Warps walk their gate/up and down units without CTA barriers. (Asking L2 for each phase's
 // rows ahead with cp.async.bulk.prefetch was measured: it slowed large decode by 11 %, so the
 // loads go straight to HBM.) Every wait is bounded.
@@ -65,23 +67,60 @@ __device__ __forceinline__ Rec rec_of(const coli_moe_expert &e) {
     return r;
 }
 
-// X: x -> limbs in the routed layout (and the shared one when it differs)
+// X: x -> limbs in the routed layout (and the shared one when it differs). A thread's items
+// (16 elements each) are loaded once and kept in registers across the max reduction when it
+// has at most two of them (H <= 8192); larger H reloads them for the conversion.
+template <int FMT>
+__device__ __forceinline__ void limbs_from_regs(const float4 (&v)[4], uint8_t *xq, int CPR, int p,
+                                                const FixedScale &fx) {
+    using G = QGeom<FMT>;
+    using I = IQ<FMT>;
+    const int c = p % CPR, ss = p / CPR;
+    int X[16];
+#pragma unroll
+    for (int k = 0; k < 4; k++) {
+        X[4 * k + 0] = fx(v[k].x);
+        X[4 * k + 1] = fx(v[k].y);
+        X[4 * k + 2] = fx(v[k].z);
+        X[4 * k + 3] = fx(v[k].w);
+    }
+    uint32_t o[12];
+#pragma unroll
+    for (int wl = 0; wl < I::WPSS; wl++)
+#pragma unroll
+        for (int g = 0; g < I::NGW; g++) {
+            const int e0 = wl * G::EPW + g, u = (wl * I::NGW + g) * 3;
+            pack_limbs(X[e0], X[e0 + I::NGW], X[e0 + 2 * I::NGW], X[e0 + 3 * I::NGW], o[u], o[u + 1], o[u + 2]);
+        }
+    uint4 *xq4 = reinterpret_cast<uint4 *>(xq);
+#pragma unroll
+    for (int j = 0; j < 3; j++)
+        xq4[(ss * 3 + j) * CPR + c] = make_uint4(o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
+}
+
 template <int RF, int SF>
 __device__ void stage_x(const DecParams &P, uint8_t *xq_r, uint8_t *xq_s, bool two, D1S &m) {
     const int tid = threadIdx.x, lane = tid % kWarp, warp = tid / kWarp;
-    const int n4 = P.H / 4;
+    const int n16 = P.H / 16;  // 16-element groups; group q is item q of every layout ordering
     const float4 *x4 = reinterpret_cast<const float4 *>(P.x);
-    constexpr int B = 4;
+    const bool in_regs = n16 <= 2 * kNT;
+    float4 v[2][4];
     float mx = 0.f;
-    for (int q0 = tid; q0 < n4; q0 += kNT * B) {
-        float4 v[B];
+    for (int q0 = tid; q0 < n16; q0 += 2 * kNT) {
 #pragma unroll
-        for (int j = 0; j < B; j++)
-            if (q0 + j * kNT < n4) v[j] = __ldg(x4 + q0 + j * kNT);
+        for (int j = 0; j < 2; j++) {
+            const int q = q0 + j * kNT;
+            if (q < n16)
 #pragma unroll
-        for (int j = 0; j < B; j++)
-            if (q0 + j * kNT < n4)
-                mx = fmaxf(mx, fmaxf(fmaxf(fabsf(v[j].x), fabsf(v[j].y)), fmaxf(fabsf(v[j].z), fabsf(v[j].w))));
+                for (int k = 0; k < 4; k++) v[j][k] = __ldg(x4 + 4 * q + k);
+        }
+#pragma unroll
+        for (int j = 0; j < 2; j++)
+            if (q0 + j * kNT < n16)
+#pragma unroll
+                for (int k = 0; k < 4; k++)
+                    mx = fmaxf(mx, fmaxf(fmaxf(fabsf(v[j][k].x), fabsf(v[j][k].y)),
+                                         fmaxf(fabsf(v[j][k].z), fabsf(v[j][k].w))));
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, o));
@@ -92,8 +131,33 @@ __device__ void stage_x(const DecParams &P, uint8_t *xq_r, uint8_t *xq_s, bool t
     for (int w = 1; w < kNW; w++) mx = fmaxf(mx, m.redf[w]);
     const int s = fixed_shift(mx);
     const FixedScale fx(s);
-    stage_limbs_vec<RF>(P.x, P.H, false, xq_r, fx, tid, kNT);
-    if (two) stage_limbs_vec<SF>(P.x, P.H, false, xq_s, fx, tid, kNT);
+    // the 16 elements of group q are item q of a layout whose items are (ss, c) with
+    // p = ss * CPR + c covering elements c * EPC + ss * 16: map q to that p
+    auto item_of = [&](int fmt_epc, int fmt_nss, int q) {
+        const int cpr = P.H / fmt_epc;
+        const int c = q / fmt_nss, ss = q % fmt_nss;
+        return ss * cpr + c;
+    };
+    for (int q0 = tid; q0 < n16; q0 += 2 * kNT) {
+        if (!in_regs) {
+#pragma unroll
+            for (int j = 0; j < 2; j++) {
+                const int q = q0 + j * kNT;
+                if (q < n16)
+#pragma unroll
+                    for (int k = 0; k < 4; k++) v[j][k] = __ldg(x4 + 4 * q + k);
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < 2; j++) {
+            const int q = q0 + j * kNT;
+            if (q < n16) {
+                limbs_from_regs<RF>(v[j], xq_r, P.H / QGeom<RF>::EPC, item_of(QGeom<RF>::EPC, IQ<RF>::NSS, q), fx);
+                if (two)
+                    limbs_from_regs<SF>(v[j], xq_s, P.H / QGeom<SF>::EPC, item_of(QGeom<SF>::EPC, IQ<SF>::NSS, q), fx);
+            }
+        }
+    }
     if (tid == 0) {
         m.xshift = s;
         m.xinv = ldexpf(1.f, -s);
@@ -306,23 +370,23 @@ __device__ __noinline__ void gateup_run(const DecParams &P, D1S &m, const uint8_
         });
 }
 
-// D: down units of `nsl` slots starting at slot0 over this CTA's row groups [gb, gb + ng);
-// unit i -> slot slot0 + i / ng, rows 4*(gb + i % ng) .. +3; y goes to ybuf[slot][row - 4*gb].
+// D: down units [lo, hi) of the slot-major space (unit l: slot l / ngr, rows 4 (l % ngr) .. +3);
+// slot u's staged h sits at hq + (u - s0) * hs. y goes to the workspace row of the slot.
 // rot rotates the warp order so that two calls share the warps evenly.
 template <int FMT>
-__device__ __noinline__ void down_run(const DecParams &P, D1S &m, const uint8_t *hq, int hq_stride, int slot0, int nsl,
-                         int gb, int ng, int rot, float *ybuf) {
+__device__ __noinline__ void down_run(const DecParams &P, D1S &m, const uint8_t *hq, int hs, int s0, int lo, int hi,
+                                      int ngr, int rot) {
     const int lane = threadIdx.x % kWarp;
     const int warp = (threadIdx.x / kWarp + kNW - rot) % kNW;
-    const int nu = nsl * ng;
+    const int nu = hi - lo;
     const int mine = nu > warp ? (nu - warp + kNW - 1) / kNW : 0;
-    const bool sh = P.Is > 0 && slot0 == m.U;
+    const bool sh = P.Is > 0 && lo / ngr == m.U;
     const int inter = sh ? P.Is : P.I;
     const int64_t rb = row_bytes(FMT, inter);
     auto unit = [&](int i, int &slot, int &grp) {
-        const int l = warp + kNW * i;
-        slot = slot0 + l / ng;
-        grp = gb + l % ng;
+        const int l = lo + warp + kNW * i;
+        slot = l / ngr;
+        grp = l - slot * ngr;
     };
     warp_stream_int<FMT, 4, kInfl1>(
         mine, (int)(rb / 16), lane,
@@ -336,7 +400,7 @@ __device__ __noinline__ void down_run(const DecParams &P, D1S &m, const uint8_t 
         [&](int i) {
             int slot, grp;
             unit(i, slot, grp);
-            return reinterpret_cast<const uint4 *>(hq + (size_t)(slot - slot0) * hq_stride);
+            return reinterpret_cast<const uint4 *>(hq + (size_t)(slot - s0) * hs);
         },
         [&](int i) {
             int slot, grp;
@@ -350,7 +414,7 @@ __device__ __noinline__ void down_run(const DecParams &P, D1S &m, const uint8_t 
             const int d = 4 * grp + lane;
             if (lane < 4 && d < P.H) {
                 const long long sv = lane == 0 ? s[0] : lane == 1 ? s[1] : lane == 2 ? s[2] : s[3];
-                ybuf[slot * P.d1_rows + d - 4 * gb] = (__ll2float_rn(sv) * m.hinv[slot]) * sc;
+                P.y[(size_t)(sh ? P.K : slot) * P.H + d] = (__ll2float_rn(sv) * m.hinv[slot - s0]) * sc;
             }
         });
 }
@@ -362,7 +426,6 @@ __global__ void __launch_bounds__(kNT, 2) moe_decode1_kernel(const DecParams P) 
     uint8_t *act = smem + P.d1_act_off;
     float *rsg = reinterpret_cast<float *>(smem + P.d1_rsc_off);
     float *rch = rsg + ((P.E + 3) & ~3);
-    float *ybuf = reinterpret_cast<float *>(smem + P.d1_y_off);
     const int tid = threadIdx.x, G = gridDim.x, c = blockIdx.x;
     const bool two = P.Is > 0 && SF != RF;
     uint8_t *xq_r = act, *xq_s = two ? act + 3 * P.H : act;
@@ -371,7 +434,10 @@ __global__ void __launch_bounds__(kNT, 2) moe_decode1_kernel(const DecParams P) 
     if (tid <= kMaxK) m.hmax[tid] = 0;
     if (tid == 0 && P.Is > 0) m.rec[kShSlot] = rec_of(P.shared);
     __syncthreads();
-    const int bb = range_lo(P.G_sh, c, G), be = range_lo(P.G_sh, c + 1, G);
+    // the shared expert's gate/up goes to the CTAs without a router item, so that every CTA
+    // reaches the routing wait at about the same time
+    const int nb = G - P.R > 0 ? G - P.R : G, cb0 = G - P.R > 0 ? c - P.R : c;
+    const int bb = cb0 < 0 ? 0 : range_lo(P.G_sh, cb0, nb), be = cb0 < 0 ? 0 : range_lo(P.G_sh, cb0 + 1, nb);
     // routing reads the bias and the expert table right after its wait: warm them in L2
     {
         const int lb = (P.E * 4 + 127) / 128, lt = (P.E * (int)sizeof(coli_moe_expert) + 127) / 128;
@@ -412,54 +478,71 @@ __global__ void __launch_bounds__(kNT, 2) moe_decode1_kernel(const DecParams P) 
     if (tid < U || (tid == kShSlot && P.Is > 0))
         if (m.hmax[tid] != 0) atomicMax(&P.ctrl->hmax[tid], m.hmax[tid]);
     __syncthreads();
-    const int ngr = P.H / 4;
-    const int gb = range_lo(ngr, c, G), ge = range_lo(ngr, c + 1, G), ng = ge - gb;
     if (tid == 0) {
         __threadfence();
         atomicAdd(&P.ctrl->gu_all, (be - bb) + (ce - cb));
     }
 
-    // ---------------- D: all h staged, this CTA's output rows for every slot, combine
+    // ---------------- D: down rows, (slot, 4-row group) units split slot-major over the CTAs, so
+    // a CTA stages only the one or two h vectors its units read
     if (tid == 0) {
         wait_at_least(&P.ctrl->gu_all, P.G_sh + gu_tot, P.ctrl);
         __threadfence();
     }
     __syncthreads();
     const int nsl = U + (P.Is > 0 ? 1 : 0);
-    if (tid < nsl) {
-        const int hi = tid < U ? tid : kShSlot;
-        const int s = fixed_shift(__int_as_float(__ldcg(&P.ctrl->hmax[hi])));
+    const int ngr = P.H / 4, ND = nsl * ngr;
+    const int db = range_lo(ND, c, G), de = range_lo(ND, c + 1, G);
+    const int s0 = db / ngr, ns = de > db ? (de - 1) / ngr - s0 + 1 : 0;
+    const int hs = 3 * (P.I > P.Is ? P.I : P.Is);  // staged bytes per h vector
+    if (tid < ns) {
+        const int u = s0 + tid;
+        const int s = fixed_shift(__int_as_float(__ldcg(&P.ctrl->hmax[u < U ? u : kShSlot])));
         m.hshift[tid] = s;
         m.hinv[tid] = ldexpf(1.f, -s);
     }
     __syncthreads();
-    const int hs_r = 3 * P.I;  // staged bytes per routed h vector
-    uint8_t *hq_s = act + (size_t)U * hs_r;
+    for (int j = 0; j < ns; j++) {
+        const int u = s0 + j;
+        const FixedScale fx(m.hshift[j]);
+        if (u < U) stage_limbs_vec<RF>(P.h + (size_t)u * P.ldh, P.I, true, act + (size_t)j * hs, fx, tid, kNT);
+        else stage_limbs_vec<SF>(P.h + (size_t)P.K * P.ldh, P.Is, true, act + (size_t)j * hs, fx, tid, kNT);
+    }
+    __syncthreads();
     {
-        const int ir = limb_items<RF>(P.I), is = P.Is > 0 ? limb_items<SF>(P.Is) : 0;
-        const int cpr_r = P.I / QGeom<RF>::EPC, cpr_s = P.Is / QGeom<SF>::EPC;
-        for (int p = tid; p < U * ir + is; p += kNT) {
-            if (p < U * ir) {
-                const int u = p / ir;
-                stage_limb_item<RF>(P.h + (size_t)u * P.ldh, cpr_r, true,
-                                    reinterpret_cast<uint4 *>(act + (size_t)u * hs_r), FixedScale(m.hshift[u]), p - u * ir);
-            } else {
-                stage_limb_item<SF>(P.h + (size_t)P.K * P.ldh, cpr_s, true, reinterpret_cast<uint4 *>(hq_s),
-                                    FixedScale(m.hshift[U]), p - U * ir);
-            }
-        }
+        const int split = U * ngr;  // routed units below, shared units from here
+        const int rlo = db, rhi = min(de, split), slo = max(db, split), shi = de;
+        if (rhi > rlo) down_run<RF>(P, m, act, hs, s0, rlo, rhi, ngr, 0);
+        if (shi > slo) down_run<SF>(P, m, act, hs, s0, slo, shi, ngr, rhi > rlo ? (rhi - rlo) % kNW : 0);
     }
     __syncthreads();
-    if (ng > 0) {
-        down_run<RF>(P, m, act, hs_r, 0, U, gb, ng, 0, ybuf);
-        if (P.Is > 0) down_run<SF>(P, m, hq_s, 0, U, 1, gb, ng, (U * ng) % kNW, ybuf);
+    if (tid == 0) {
+        __threadfence();
+        atomicAdd(&P.ctrl->dn_done, de - db);
+    }
+
+    // ---------------- E: this CTA's rows of out, selection order then the shared expert
+    if (tid == 0) {
+        wait_at_least(&P.ctrl->dn_done, ND, P.ctrl);
+        __threadfence();
     }
     __syncthreads();
-    for (int r = tid; r < 4 * ng; r += kNT) {
-        const int d = 4 * gb + r;
+    const int r_lo = range_lo(P.H, c, G), r_hi = range_lo(P.H, c + 1, G);
+    for (int d = r_lo + tid; d < r_hi; d += kNT) {
+        float yv[kMaxK + 1];
+#pragma unroll
+        for (int k = 0; k <= kMaxK; k++)
+            if (k < U) yv[k] = __ldcg(P.y + (size_t)m.pos[k] * P.H + d);
+            else if (k == U && P.Is > 0) yv[k] = __ldcg(P.y + (size_t)P.K * P.H + d);
         float a = 0.f;
-        for (int k = 0; k < U; k++) a = __fadd_rn(a, __fmul_rn(m.w[k], ybuf[m.pos[k] * P.d1_rows + r]));
-        if (P.Is > 0) a = __fadd_rn(a, ybuf[U * P.d1_rows + r]);
+#pragma unroll
+        for (int k = 0; k < kMaxK; k++)
+            if (k < U) a = __fadd_rn(a, __fmul_rn(m.w[k], yv[k]));
+        if (P.Is > 0) {
+#pragma unroll
+            for (int k = 0; k <= kMaxK; k++)
+                if (k == U) a = __fadd_rn(a, yv[k]);
+        }
         P.out[d] = a;
     }
 }
@@ -479,7 +562,7 @@ KernelFn kernel_for(int rf, int sf) {
     return table[pick(rf)][pick(sf)];
 }
 
-size_t decode1_smem_bytes(const DecParams &P) { return (size_t)P.d1_y_off + (size_t)(P.K + 1) * P.d1_rows * 4; }
+size_t decode1_smem_bytes(const DecParams &P) { return (size_t)P.d1_y_off; }
 
 }  // namespace
 
@@ -504,12 +587,11 @@ bool decode1_plan(const coli_moe_desc &d, DecParams &P, int grid) {
     P.G_sh = d.I_shared > 0 ? (d.I_shared + 1) / 2 : 0;
     const bool two = d.I_shared > 0 && d.shared_fmt != d.routed_fmt;
     const size_t x_bytes = (size_t)3 * d.H * (two ? 2 : 1);
-    const size_t h_bytes = (size_t)3 * ((size_t)d.K * d.I + d.I_shared);
+    const size_t h_bytes = (size_t)3 * (d.K + 1) * std::max(d.I, d.I_shared);
     P.d1_act_off = (int)align_up(sizeof(D1S), 128);
     P.d1_rsc_off = P.d1_act_off + (int)align_up(std::max(x_bytes, h_bytes), 128);
-    P.d1_y_off = P.d1_rsc_off + (int)align_up((size_t)2 * ((d.E + 3) & ~3) * 4, 128);
-    const int ngr = d.H / 4;
-    P.d1_rows = 4 * ((ngr + grid - 1) / grid);
+    P.d1_y_off = P.d1_rsc_off + (int)align_up((size_t)2 * ((d.E + 3) & ~3) * 4, 128);  // end of smem
+    P.d1_rows = 0;
     return decode1_smem_bytes(P) <= 113u * 1024;
 }
 

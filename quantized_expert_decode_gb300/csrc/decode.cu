@@ -583,12 +583,12 @@ __device__ void gateup_units_int(const DecParams &P, const Seg &g, const void *x
             rr[3] = g.w1 + (size_t)j1 * rb;
         },
         [&](int) { return static_cast<const uint4 *>(xs); }, [](int) { return 0; },
-        [&](int i, const long long (&s)[4], int) {
-            const int lj = 2 * (warp + kNW * i) + lane;  // row within the piece's scales
+        [&](int i, long long tot, int) {  // lanes 0 / 16 hold gate j / j+1, lanes 8 / 24 up
+            const long long su = __shfl_down_sync(kFull, tot, 8);
+            const int lj = 2 * (warp + kNW * i) + (lane >> 4);  // row within the piece's scales
             const int jq = 2 * ubase + lj;
-            if (lane < 2 && jq < g.inter) {
-                const long long sg = lane ? s[2] : s[0], su = lane ? s[3] : s[1];
-                const float gv = (__ll2float_rn(sg) * xinv) * m.sc[0][lj];
+            if ((lane & 15) == 0 && jq < g.inter) {
+                const float gv = (__ll2float_rn(tot) * xinv) * m.sc[0][lj];
                 const float uv = (__ll2float_rn(su) * xinv) * m.sc[1][lj];
                 hrow[jq] = gv / (1.f + expf(-gv)) * uv;
             }
@@ -650,13 +650,10 @@ __device__ void down_units_int(const DecParams &P, const Seg &g, const void *xs,
             for (int q = 0; q < 4; q++) rr[q] = g.w0 + (size_t)min(d + q, P.H - 1) * rb;
         },
         [&](int) { return static_cast<const uint4 *>(xs); }, [](int) { return 0; },
-        [&](int i, const long long (&s)[4], int) {
-            const int ld = 4 * (warp + kNW * i) + lane;
+        [&](int i, long long tot, int) {  // lane 8q holds row q
+            const int ld = 4 * (warp + kNW * i) + (lane >> 3);
             const int d = 4 * ubase + ld;
-            if (lane < 4 && d < P.H) {
-                const long long sv = lane == 0 ? s[0] : lane == 1 ? s[1] : lane == 2 ? s[2] : s[3];
-                yrow[d] = (__ll2float_rn(sv) * xinv) * m.sc[0][ld];
-            }
+            if ((lane & 7) == 0 && d < P.H) yrow[d] = (__ll2float_rn(tot) * xinv) * m.sc[0][ld];
         });
 }
 

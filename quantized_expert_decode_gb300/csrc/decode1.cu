@@ -348,21 +348,21 @@ __device__ __noinline__ void gateup_run(const DecParams &P, D1S &m, const uint8_
             rr[3] = r.uw + (size_t)j1 * rb;
         },
         [&](int) { return reinterpret_cast<const uint4 *>(xq); },
-        [&](int i) {
+        [&](int i) {  // lanes 0 and 16: the scales of rows j and j + 1
             int slot, j;
             unit(i, slot, j);
             const Rec &r = m.rec[slot];
-            const int jq = min(j + (lane & 1), inter - 1);
-            return lane < 2 ? make_float2(__ldg(r.gs + jq), __ldg(r.us + jq)) : make_float2(0.f, 0.f);
+            const int jq = min(j + (lane >> 4), inter - 1);
+            return (lane & 15) == 0 ? make_float2(__ldg(r.gs + jq), __ldg(r.us + jq)) : make_float2(0.f, 0.f);
         },
-        [&](int i, const long long (&s)[4], float2 sc) {
+        [&](int i, long long tot, float2 sc) {  // lanes 0 / 16 hold gate j / j+1, lanes 8 / 24 up
+            const long long up = __shfl_down_sync(kFull, tot, 8);
             int slot, j;
             unit(i, slot, j);
-            const int jq = j + lane;
-            if (lane < 2 && jq < inter) {
-                const long long sgt = lane ? s[2] : s[0], sut = lane ? s[3] : s[1];
-                const float gv = (__ll2float_rn(sgt) * xinv) * sc.x;
-                const float uv = (__ll2float_rn(sut) * xinv) * sc.y;
+            const int jq = j + (lane >> 4);
+            if ((lane & 15) == 0 && jq < inter) {
+                const float gv = (__ll2float_rn(tot) * xinv) * sc.x;
+                const float uv = (__ll2float_rn(up) * xinv) * sc.y;
                 const float hv = gv / (1.f + expf(-gv)) * uv;
                 P.h[(size_t)(shared ? P.K : slot) * P.ldh + jq] = hv;
                 atomicMax(&m.hmax[slot], __float_as_int(fabsf(hv)));
@@ -406,16 +406,14 @@ __device__ __noinline__ void down_run(const DecParams &P, D1S &m, const uint8_t 
             int slot, grp;
             unit(i, slot, grp);
             const Rec &r = m.rec[sh ? kShSlot : slot];
-            return lane < 4 ? __ldg(r.ds + min(4 * grp + lane, P.H - 1)) : 0.f;
+            return (lane & 7) == 0 ? __ldg(r.ds + min(4 * grp + (lane >> 3), P.H - 1)) : 0.f;
         },
-        [&](int i, const long long (&s)[4], float sc) {
+        [&](int i, long long tot, float sc) {  // lane 8q holds row q
             int slot, grp;
             unit(i, slot, grp);
-            const int d = 4 * grp + lane;
-            if (lane < 4 && d < P.H) {
-                const long long sv = lane == 0 ? s[0] : lane == 1 ? s[1] : lane == 2 ? s[2] : s[3];
-                P.y[(size_t)(sh ? P.K : slot) * P.H + d] = (__ll2float_rn(sv) * m.hinv[slot - s0]) * sc;
-            }
+            const int d = 4 * grp + (lane >> 3);
+            if ((lane & 7) == 0 && d < P.H)
+                P.y[(size_t)(sh ? P.K : slot) * P.H + d] = (__ll2float_rn(tot) * m.hinv[slot - s0]) * sc;
         });
 }
 

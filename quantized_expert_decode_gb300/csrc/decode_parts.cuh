@@ -139,10 +139,10 @@ __device__ __forceinline__ void warp_stream(int nunits, int CPR, const float *xs
     }
 }
 
-// The same walk for single-token groups on the integer core (idot.cuh): xq_of(i) gives the
-// staged activation limbs unit i is dotted with; epi(i, sums, d) gets the exact warp totals S_r
-// of unit i's NR rows and d = pre(i), the unit's epilogue operands (row scales), which are
-// loaded two units ahead.
+// The same walk for single-token groups on the integer core (idot.cuh), four rows per unit:
+// xq_of(i) gives the staged activation limbs unit i is dotted with; epi(i, tot, d) gets, in
+// lane l, the exact warp total S of row l / 8 of unit i, and d = pre(i), the unit's epilogue
+// operands (row scales), which are loaded two units ahead.
 template <int FMT, int NR, int INFL = kInflight, class RowsOf, class XqOf, class Pre, class Epi>
 __device__ __forceinline__ void warp_stream_int(int nunits, int CPR, int lane, RowsOf rows_of, XqOf xq_of, Pre pre,
                                                 Epi epi) {
@@ -183,9 +183,8 @@ __device__ __forceinline__ void warp_stream_int(int nunits, int CPR, int lane, R
                 if (c < CPR) idot_chunk<FMT, NR>(buf[j], xq4, CPR, c, acc);
                 issue(buf[j]);
                 if (++ck == S) {
-                    long long sums[NR];
-                    idot_reduce<FMT, NR>(acc, sums);
-                    epi(cu, sums, d0);
+                    static_assert(NR == 4, "the integer walk reduces four rows per unit");
+                    epi(cu, idot_reduce4<FMT>(acc, lane), d0);
                     d0 = d1;
                     if (cu + 2 < nunits) d1 = pre(cu + 2);
 #pragma unroll

@@ -109,6 +109,30 @@ __device__ __forceinline__ void idot_reduce(const int (&acc)[NR][3], long long (
     }
 }
 
+// Four rows at once, transposing as it reduces: rows {0,1} and {2,3} are split between the lane
+// halves, then between the quarters, so 12 shuffles (instead of 40) leave every lane with the
+// exact total of row lane / 8.
+template <int FMT>
+__device__ __forceinline__ long long idot_reduce4(const int (&acc)[4][3], int lane) {
+    constexpr int LS = IQ<FMT>::LOG_SC;
+    long long p[4];
+#pragma unroll
+    for (int r = 0; r < 4; r++)
+        p[r] = ((long long)(acc[r][2] >> LS) << 16) + ((long long)(acc[r][1] >> LS) << 8) +
+               (long long)(acc[r][0] >> LS);
+    const bool h16 = (lane & 16) != 0, h8 = (lane & 8) != 0;
+    long long k0 = h16 ? p[2] : p[0], k1 = h16 ? p[3] : p[1];
+    const long long s0 = h16 ? p[0] : p[2], s1 = h16 ? p[1] : p[3];
+    k0 += __shfl_xor_sync(kFull, s0, 16);
+    k1 += __shfl_xor_sync(kFull, s1, 16);
+    long long k = h8 ? k1 : k0;
+    k += __shfl_xor_sync(kFull, h8 ? k0 : k1, 8);
+    k += __shfl_xor_sync(kFull, k, 4);
+    k += __shfl_xor_sync(kFull, k, 2);
+    k += __shfl_xor_sync(kFull, k, 1);
+    return k;
+}
+
 // the shift s of a vector whose largest magnitude is mx (0 for an all-zero vector)
 __device__ __forceinline__ int fixed_shift(float mx) {
     if (!(mx > 0.f)) return 0;

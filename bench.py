@@ -295,7 +295,11 @@ def run_colimoe(args, rank, world, local):
 
     stage = np.array([[step_ev[i][j].elapsed_time(step_ev[i][j + 1]) for j in range(4)]
                       for i in range(args.steps)])  # ms
-    step_ms = stage.sum(axis=1)
+    # decode (T <= 64) does all its work between events 0 and 2 (the counter memset, the router
+    # launch for T > 8, the persistent kernel); events 3 and 4 follow with no work between them
+    # and only add the recording overhead of an event pair, so they are not part of the step
+    fused = T <= DECODE_MAX_T
+    step_ms = stage[:, :2].sum(axis=1) if fused else stage.sum(axis=1)
     total_s = float(step_ms.sum()) / 1e3
     # distinct routed experts each rotated batch reads (from the library's own routing)
     idx = torch.empty((T, K), dtype=torch.int32, device=dev_name)
@@ -313,7 +317,6 @@ def run_colimoe(args, rank, world, local):
 
     bytes_per = [step_bytes(cfg, int(u)) for u in n_active]
     hbm_peak, peak_kind = load_peaks()
-    fused = T <= DECODE_MAX_T
     if fused:
         # one persistent kernel does the whole block (T = 1: the single-token kernel); for
         # T > 8 the router logits come from a separate launch before it

@@ -11,16 +11,17 @@
 //
 // One persistent CTA per SM walks the tiles (slot, token block, row block) of a launch, its
 // warps specialised:
-//   warps 0-7  producers, over the CTA's K-steps (64 wide) of all its tiles in order, thread
-//              (r, half) owning half a row: three steps ahead, cp.async copies that half of A
-//              row r's packed weight bytes into a raw buffer and of token row r < N of B (bf16)
-//              straight into its 128-byte-swizzled K-major slots; then, for the current step,
-//              it dequantises its raw half row into the swizzled bf16 A tile and the stage's
-//              `full` mbarrier collects the 256 arrivals (two producer warps per SMSP)
-//   warp 8     one thread issues four tcgen05.mma (K = 16 each) per stage into one of two TMEM
+//   warps 0-15 producers, over the CTA's K-steps (64 wide) of all its tiles in order, thread
+//              (r, quarter) owning a quarter row: three steps ahead, cp.async copies that quarter
+//              of A row r's packed weight bytes into a raw buffer and of token row r < N of B
+//              (bf16) straight into its 128-byte-swizzled K-major slots; then, for the current
+//              step, it dequantises its raw quarter row into the swizzled bf16 A tile and the
+//              stage's `full` mbarrier collects the 512 arrivals (four producer warps per SMSP
+//              hide each other's latency)
+//   warp 16    one thread issues four tcgen05.mma (K = 16 each) per stage into one of two TMEM
 //              accumulators and commits the stage's `empty` mbarrier to their completion; after
 //              a tile's last step it commits that accumulator's `accf`
-//   warps 9-12 epilogue: tcgen05.ld of the 128 x N tile (warp w reads TMEM lanes 32 (w % 4)..),
+//   warps 17-20 epilogue: tcgen05.ld of the 128 x N tile (warp w reads TMEM lanes 32 (w % 4)..),
 //              the fused epilogue, then `tfree` hands the accumulator back to the MMA warp, so
 //              the next tile's MMAs run while the epilogue reads this one
 // K order: the dot product does not depend on the order of K, so within each block of 8 (int4)
@@ -45,9 +46,10 @@ constexpr int kTcN = 128;        // max tokens per tile (MMA N, multiple of 16)
 constexpr int kTcKB = 64;        // K per stage (one 128-byte swizzle row of bf16)
 constexpr int kTcStages = 5;
 constexpr int kTcAhead = 3;      // K-steps the producers' copies run ahead
-constexpr int kTcThreads = 416;  // producers 0-7, MMA warp 8, epilogue 9-12
-constexpr int kTcProd = 256, kTcEpi = 128;
-constexpr int kTcMmaWarp = 8;
+constexpr int kTcThreads = 672;  // producers 0-15, MMA warp 16, epilogue 17-20
+constexpr int kTcProd = 512, kTcEpi = 128;
+constexpr int kTcMmaWarp = 16;
+constexpr int kTileCap = 128;    // tiles per CTA whose parameters are kept in shared memory
 constexpr int kTcRawStride = 80; // bytes per raw weight row in a stage (>= 64, bank-spread)
 constexpr unsigned long long kTcWaitNs = 2000000000ull;
 
@@ -63,11 +65,18 @@ struct PfParams {
     int down;                        // 0: gate/up GEMM, 1: down GEMM
 };
 
+struct Tile {
+    const uint8_t *w0, *w1;  // gate/up rows (or down rows in w0)
+    const float *s0, *s1;
+    int fmt, inter, n0, ncur, N, pbase, row0;  // row0: first j (gate/up) or d (down)
+};
+
 struct TcSmem {  // after the 1024-aligned stage buffers
     uint64_t full[kTcStages], empty[kTcStages], accf[2], tfree[2], drain;
     uint32_t tmem_base;
     int abort;
     int pref[kMaxE + 2];  // tiles before slot g (slots 0..E-1 routed, E shared)
+    Tile tiles[kTileCap]; // this CTA's tiles blockIdx.x + i * gridDim.x, looked up once
 };
 
 constexpr size_t kStageA = (size_t)kTcM * 128, kStageB = (size_t)kTcN * 128, kStageRaw = (size_t)kTcM * kTcRawStride;
@@ -98,29 +107,27 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     return d;
 }
 
-// Dequantise 32 consecutive weights (int4: 4 words, int2: 2, int8: 8) to 16 bf16 pairs in the
-// permuted K order. The bf16 magic: a field f in bits 0..3 (resp. 0..1) of a halfword OR-ed
-// with 0x4300 is the bf16 128 + f, exactly; adding -(128 + 8) (resp. -(128 + 2)) leaves f - 8
+// Dequantise 16 consecutive weights to 8 bf16 pairs in the permuted K order. The bf16 magic: a
+// field f in bits 0..3 (resp. 0..1) of a halfword OR-ed with 0x4300 is the bf16 128 + f, exactly; adding -(128 + 8) (resp. -(128 + 2)) leaves f - 8
 // (resp. f - 2) exactly. int8 bytes go through float (every int8 value is exact in bf16).
 template <int FMT>
-__device__ __forceinline__ void deq32_bf16(const uint32_t *w, uint32_t (&out)[16]) {
+__device__ __forceinline__ void deq16_bf16(const uint32_t *w, uint32_t (&out)[8]) {
+    // 16 consecutive weights (int4: 2 words, int2: 1, int8: 4) -> 8 bf16 pairs, permuted K order
     if (FMT == COLI_FMT_INT4) {
-        const uint32_t one = 0x3F803F80u, off = 0xC308C308u;  // 1.0, -136.0
+        const uint32_t one = 0x3F803F80u, off = 0xC308C308u;
 #pragma unroll
-        for (int i = 0; i < 4; i++)
+        for (int i = 0; i < 2; i++)
 #pragma unroll
             for (int m = 0; m < 4; m++)
                 out[4 * i + m] = bf16x2_fma(lop3_and_or(w[i] >> (4 * m), 0x000F000Fu, 0x43004300u), one, off);
     } else if (FMT == COLI_FMT_INT2) {
-        const uint32_t one = 0x3F803F80u, off = 0xC302C302u;  // 1.0, -130.0
+        const uint32_t one = 0x3F803F80u, off = 0xC302C302u;
 #pragma unroll
-        for (int i = 0; i < 2; i++)
-#pragma unroll
-            for (int m = 0; m < 8; m++)
-                out[8 * i + m] = bf16x2_fma(lop3_and_or(w[i] >> (2 * m), 0x00030003u, 0x43004300u), one, off);
+        for (int m = 0; m < 8; m++)
+            out[m] = bf16x2_fma(lop3_and_or(w[0] >> (2 * m), 0x00030003u, 0x43004300u), one, off);
     } else {
 #pragma unroll
-        for (int i = 0; i < 8; i++) {
+        for (int i = 0; i < 4; i++) {
             const int v = (int)w[i];
             out[2 * i] = pack_bf16((float)((v << 24) >> 24), (float)((v << 16) >> 24));
             out[2 * i + 1] = pack_bf16((float)((v << 8) >> 24), (float)(v >> 24));
@@ -147,11 +154,6 @@ __device__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity, TcSmem &ts, in
     return true;
 }
 
-struct Tile {
-    const uint8_t *w0, *w1;  // gate/up rows (or down rows in w0)
-    const float *s0, *s1;
-    int fmt, inter, n0, ncur, N, pbase, row0;  // row0: first j (gate/up) or d (down)
-};
 
 __device__ int slot_rows(const PfParams &P, int g) { return g < P.E ? P.counts[g] : P.T; }
 
@@ -192,40 +194,23 @@ __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commi
 template <int N>
 __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
-// ask L2 for rows [r0, r1) of a matrix with rb bytes per row (16-byte multiples), 32 KB a piece
-__device__ void prefetch_rows_l2(const uint8_t *base, int r0, int r1, int64_t rb) {
-    if (r1 <= r0) return;
-    const uint8_t *p = base + (size_t)r0 * rb;
-    const int64_t n = (int64_t)(r1 - r0) * rb;
-    for (int64_t o = 0; o < n; o += 32768)
-        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p + o), "r"((uint32_t)(n - o < 32768 ? n - o : 32768))
-                     : "memory");
-}
-
-// the weight rows of tile T
-__device__ void prefetch_tile_a(const PfParams &P, const Tile &T) {
-    if (P.down) {
-        prefetch_rows_l2(T.w0, T.row0, min(T.row0 + kTcM, P.H), row_bytes(T.fmt, T.inter));
-    } else {
-        const int j1 = min(T.row0 + kTcM / 2, T.inter);
-        prefetch_rows_l2(T.w0, T.row0, j1, row_bytes(T.fmt, P.H));
-        prefetch_rows_l2(T.w1, T.row0, j1, row_bytes(T.fmt, P.H));
-    }
-}
-
 __device__ __forceinline__ int qbytes(int fmt) { return fmt == COLI_FMT_INT4 ? 32 : fmt == COLI_FMT_INT2 ? 16 : 64; }
 
 __device__ __forceinline__ void cp_async8(void *dst_smem, const void *src) {
     asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(smem_u32(dst_smem)), "l"(src) : "memory");
 }
 
-// The producer thread (r, h) of a tile: its half h of A row r (gate/up interleaved — even rows
+__device__ __forceinline__ void cp_async4(void *dst_smem, const void *src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst_smem)), "l"(src) : "memory");
+}
+
+// The producer thread (r, h) of a tile: quarter h of A row r (gate/up interleaved — even rows
 // gate j0 + r/2, odd rows up — or down row d0 + r) and of B row r (token n0 + r, clamped to the
 // buffer; rows >= N are not copied).
 struct ProdRow {
-    const uint8_t *a;   // packed weights of A row r at K-step 0, half h
-    const uint16_t *b;  // bf16 activations of B row r at K-step 0, half h
-    int qh;             // packed bytes per half K-step
+    const uint8_t *a;   // packed weights of A row r at K-step 0, quarter h
+    const uint16_t *b;  // bf16 activations of B row r at K-step 0, quarter h
+    int qq;             // packed bytes per quarter K-step
     bool has_b;
 };
 
@@ -239,57 +224,55 @@ __device__ __forceinline__ ProdRow prod_row(const PfParams &P, const Tile &T, in
         const int j = min(T.row0 + (r >> 1), T.inter - 1);
         base = ((r & 1) ? T.w1 : T.w0) + (size_t)j * row_bytes(T.fmt, P.H);
     }
-    pr.qh = qb / 2;
-    pr.a = base + h * pr.qh;
+    pr.qq = qb / 4;
+    pr.a = base + h * pr.qq;
     const int rows_total = P.T * P.K + P.T;
     const int row = min(T.pbase + T.n0 + r, rows_total - 1);
-    pr.b = (P.down ? P.hb + (size_t)row * P.ldh : P.xb + (size_t)row * P.H) + 32 * h;
+    pr.b = (P.down ? P.hb + (size_t)row * P.ldh : P.xb + (size_t)row * P.H) + 16 * h;
     pr.has_b = r < T.N;
     return pr;
 }
 
-// K-step kb: cp.async of the half rows into the stage's raw buffer and B tile
+// K-step kb: cp.async of the quarter rows into the stage's raw buffer and B tile
 __device__ __forceinline__ void issue_step(const ProdRow &pr, int kb, uint8_t *raw, uint8_t *sb, int r, int h) {
-    const uint8_t *src = pr.a + (size_t)kb * 2 * pr.qh;
-    uint8_t *dst = raw + r * kTcRawStride + h * pr.qh;
-    if (pr.qh == 8) cp_async8(dst, src);
-    else
-        for (int i = 0; i < pr.qh / 16; i++) cp_async16(dst + 16 * i, src + 16 * i);
+    const uint8_t *src = pr.a + (size_t)kb * 4 * pr.qq;
+    uint8_t *dst = raw + r * kTcRawStride + h * pr.qq;
+    if (pr.qq == 4) cp_async4(dst, src);
+    else if (pr.qq == 8) cp_async8(dst, src);
+    else cp_async16(dst, src);
     if (pr.has_b) {
         const uint16_t *bs = pr.b + (size_t)kb * kTcKB;
 #pragma unroll
-        for (int c = 0; c < 4; c++) {
-            const int cc = 4 * h + c;
+        for (int c = 0; c < 2; c++) {
+            const int cc = 2 * h + c;
             cp_async16(sb + (r >> 3) * 1024 + (r & 7) * 128 + ((cc ^ (r & 7)) << 4), bs + 8 * c);
         }
     }
 }
 
-// dequantise the thread's raw half row into chunks 4h..4h+3 of row r of the swizzled bf16 A tile
+// dequantise the thread's raw quarter row into chunks 2h, 2h+1 of row r of the swizzled A tile
 template <int FMT>
-__device__ __forceinline__ void dequant_half(const uint8_t *raw, uint8_t *sa, int r, int h) {
-    constexpr int QH = (FMT == COLI_FMT_INT4 ? 32 : FMT == COLI_FMT_INT2 ? 16 : 64) / 2;
-    constexpr int NW = QH / 4;
-    uint32_t w[NW];
-    const uint8_t *src = raw + r * kTcRawStride + h * QH;
-    if (QH == 8) {
+__device__ __forceinline__ void dequant_quarter(const uint8_t *raw, uint8_t *sa, int r, int h) {
+    constexpr int QQ = (FMT == COLI_FMT_INT4 ? 32 : FMT == COLI_FMT_INT2 ? 16 : 64) / 4;
+    uint32_t w[4];
+    const uint8_t *src = raw + r * kTcRawStride + h * QQ;
+    if (QQ == 4) {
+        w[0] = *reinterpret_cast<const uint32_t *>(src);
+    } else if (QQ == 8) {
         const uint2 v = *reinterpret_cast<const uint2 *>(src);
         w[0] = v.x;
         w[1] = v.y;
     } else {
-#pragma unroll
-        for (int i = 0; i < QH / 16; i++) {
-            const uint4 v = *reinterpret_cast<const uint4 *>(src + 16 * i);
-            w[4 * i] = v.x;
-            w[4 * i + 1] = v.y;
-            w[4 * i + 2] = v.z;
-            w[4 * i + 3] = v.w;
-        }
+        const uint4 v = *reinterpret_cast<const uint4 *>(src);
+        w[0] = v.x;
+        w[1] = v.y;
+        w[2] = v.z;
+        w[3] = v.w;
     }
-    uint32_t o[16];
-    deq32_bf16<FMT>(w, o);
-#pragma unroll
-    for (int c = 0; c < 4; c++) st_sw128(sa, r, 4 * h + c, make_uint4(o[4 * c], o[4 * c + 1], o[4 * c + 2], o[4 * c + 3]));
+    uint32_t o[8];
+    deq16_bf16<FMT>(w, o);
+    st_sw128(sa, r, 2 * h, make_uint4(o[0], o[1], o[2], o[3]));
+    st_sw128(sa, r, 2 * h + 1, make_uint4(o[4], o[5], o[6], o[7]));
 }
 
 __device__ __forceinline__ uint16_t bf16_bits(float f) {
@@ -359,6 +342,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) moe_prefill_tc_kernel(const PfP
         }
         if (tid == 0) ts.pref[nslots] = total_tiles;
     }
+    __syncthreads();
+    {  // this CTA's tile parameters, looked up in parallel once
+        const int total0 = ts.pref[nslots];
+        const int t = blockIdx.x + tid * gridDim.x;
+        if (tid < kTileCap && t < total0) ts.tiles[tid] = make_tile(P, ts, t);
+    }
     if (tid == 0) {
         ts.abort = 0;
         for (int s = 0; s < kTcStages; s++) {
@@ -383,17 +372,18 @@ __global__ void __launch_bounds__(kTcThreads, 1) moe_prefill_tc_kernel(const PfP
     const int total = ts.pref[nslots];
     const int G = gridDim.x;
     auto nkb_of = [&](const Tile &T) { return (P.down ? T.inter : P.H) / kTcKB; };
+    auto tile_at = [&](int t) {  // t = blockIdx.x + i * G
+        const int i = (t - (int)blockIdx.x) / G;
+        return i < kTileCap ? ts.tiles[i] : make_tile(P, ts, t);
+    };
 
-    if (warp < 8) {
+    if (warp < kTcMmaWarp) {
         // ---------------- producers
         const int r = tid & 127, h = tid >> 7;
         int ti = blockIdx.x, ki = 0;  // issue cursor: tile, K-step
-        Tile Ti = ti < total ? make_tile(P, ts, ti) : Tile{};
+        Tile Ti = ti < total ? tile_at(ti) : Tile{};
         ProdRow pi = prod_row(P, Ti, r, h);
         int nki = ti < total ? nkb_of(Ti) : 0;
-        // weight rows go to L2 one tile ahead of the copies that read them
-        if (tid == 0 && ti < total) prefetch_tile_a(P, Ti);
-        if (tid == 0 && ti + G < total) prefetch_tile_a(P, make_tile(P, ts, ti + G));
         uint32_t gi = 0;              // steps issued
         auto issue_next = [&]() {
             if (ti < total) {
@@ -406,10 +396,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) moe_prefill_tc_kernel(const PfP
                     ki = 0;
                     ti += G;
                     if (ti < total) {
-                        Ti = make_tile(P, ts, ti);
+                        Ti = tile_at(ti);
                         pi = prod_row(P, Ti, r, h);
                         nki = nkb_of(Ti);
-                        if (tid == 0 && ti + G < total) prefetch_tile_a(P, make_tile(P, ts, ti + G));
                     }
                 }
             }
@@ -418,15 +407,15 @@ __global__ void __launch_bounds__(kTcThreads, 1) moe_prefill_tc_kernel(const PfP
         for (int d = 0; d < kTcAhead; d++) issue_next();
         uint32_t gp = 0;  // steps processed
         for (int t = blockIdx.x; t < total && !ts.abort; t += G) {
-            const Tile T = make_tile(P, ts, t);
+            const Tile T = tile_at(t);
             const int fmt = T.fmt, nkb = nkb_of(T);
             for (int kb = 0; kb < nkb; kb++, gp++) {
                 issue_next();
                 cp_async_wait<kTcAhead>();  // this step's copies have landed
                 const int s = gp % kTcStages;
-                if (fmt == COLI_FMT_INT4) dequant_half<COLI_FMT_INT4>(sR + s * kStageRaw, sA + s * kStageA, r, h);
-                else if (fmt == COLI_FMT_INT8) dequant_half<COLI_FMT_INT8>(sR + s * kStageRaw, sA + s * kStageA, r, h);
-                else dequant_half<COLI_FMT_INT2>(sR + s * kStageRaw, sA + s * kStageA, r, h);
+                if (fmt == COLI_FMT_INT4) dequant_quarter<COLI_FMT_INT4>(sR + s * kStageRaw, sA + s * kStageA, r, h);
+                else if (fmt == COLI_FMT_INT8) dequant_quarter<COLI_FMT_INT8>(sR + s * kStageRaw, sA + s * kStageA, r, h);
+                else dequant_quarter<COLI_FMT_INT2>(sR + s * kStageRaw, sA + s * kStageA, r, h);
                 fence_async_smem();
                 mbar_arrive(&ts.full[s]);
                 if (ts.abort) break;
@@ -439,7 +428,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) moe_prefill_tc_kernel(const PfP
             uint32_t gk = 0;
             int it = 0;
             for (int t = blockIdx.x; t < total && !ts.abort; t += G, it++) {
-                const Tile T = make_tile(P, ts, t);
+                const Tile T = tile_at(t);
                 const int nkb = nkb_of(T), b = it & 1;
                 if (it >= 2 && !mbar_wait_bounded(&ts.tfree[b], ((it >> 1) - 1) & 1, ts, P.err)) break;
                 tc_fence_after_sync();
@@ -466,7 +455,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) moe_prefill_tc_kernel(const PfP
         const int R = 32 * (warp % 4) + lane;  // accumulator row = TMEM lane of this thread
         int it = 0;
         for (int t = blockIdx.x; t < total && !ts.abort; t += G, it++) {
-            const Tile T = make_tile(P, ts, t);
+            const Tile T = tile_at(t);
             const int b = it & 1;
             float sc0 = 0.f, sc1 = 0.f;
             if (P.down) {

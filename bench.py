@@ -42,7 +42,11 @@ DECODE_MAX_T = 64  # the library runs T <= 64 as one persistent decode kernel
 # (dram__bytes_read.sum + dram__bytes_write.sum), keyed by workload, with the hash of the kernel
 # sources they were taken on; a changed kernel reports null until it is measured again.
 NCU_TRAFFIC = {
-    1: {"bytes": 25946368, "src": "43303e63175ee2b3"},  # moe_decode1_kernel, small decode
+    # moe_decode1_kernel, small decode: a full-size capture
+    1: {"bytes": 25944320, "src": "e853b94b89ff0e7f"},
+    # moe_decode1_kernel, large decode: captured with 32 experts (the per-call expert traffic is
+    # the same), plus the 224 further router rows the full 256-expert router reads
+    2: {"bytes": 171172864 + 2958336 + 224 * (6144 * 4 + 4), "src": "e853b94b89ff0e7f"},
 }
 
 

@@ -7,6 +7,10 @@
 #include <cstring>
 #include <mutex>
 
+#include <atomic>
+#include <chrono>
+#include <random>
+
 #include "kernels.h"
 
 using namespace colimoe;
@@ -124,6 +128,18 @@ int num_sms() {
     return n;
 }
 
+// Call ids of the single-token kernel: a random 64-bit base per process (so that ids left in a
+// workspace by another process never match) plus a counter.
+uint64_t next_call_id() {
+    static std::atomic<uint64_t> next{[] {
+        std::random_device rd;
+        uint64_t b = ((uint64_t)rd() << 32) ^ (uint64_t)rd();
+        b ^= (uint64_t)std::chrono::steady_clock::now().time_since_epoch().count() * 0x9E3779B97F4A7C15ull;
+        return b | 1ull;
+    }()};
+    return next.fetch_add(2, std::memory_order_relaxed);
+}
+
 // T <= 64: router, selection, buckets, experts and combine in one persistent launch
 // (decode.cu); T > 8 computes the router logits in a preceding launch.
 int run_forward_decode(const coli_moe_desc *d, const float *x, const float *W_r, const float *bias,
@@ -170,8 +186,14 @@ int run_forward_decode(const coli_moe_desc *d, const float *x, const float *W_r,
     if ((size_t)P.nks * d->T * d->E * sizeof(float) > L.sig - L.part) return COLI_MOE_ENOTSUP;
     int rc;
     if ((rc = record(events, 0, st))) return rc;
-    cudaError_t e = cudaMemsetAsync(P.ctrl, 0, sizeof(DecCtrl), st);
-    if (e != cudaSuccess) return cuda_fail(e);
+    cudaError_t e = cudaSuccess;
+    if (P.single) {
+        // the single-token kernel resets its own counters: CTA 0 zeroes them and publishes this
+        // call's id, which no earlier call (of this or another process) has used
+        P.call_id = next_call_id();
+    } else if ((e = cudaMemsetAsync(P.ctrl, 0, sizeof(DecCtrl), st)) != cudaSuccess) {
+        return cuda_fail(e);
+    }
     if (P.route_only &&
         (e = launch_router_partial(x, W_r, P.part, d->T, d->H, d->E, splits, st)) != cudaSuccess)
         return cuda_fail(e);

@@ -431,6 +431,35 @@ __global__ void __launch_bounds__(kNT, 2) moe_decode1_kernel(const DecParams P) 
 
     if (tid <= kMaxK) m.hmax[tid] = 0;
     if (tid == 0 && P.Is > 0) m.rec[kShSlot] = rec_of(P.shared);
+    // CTA 0 resets this call's counters and publishes the call id; every CTA sees the id before
+    // its first counter operation (a workspace's earlier contents never hold this id)
+    if (c == 0) {
+        if (tid <= kMaxK) P.ctrl->hmax[tid] = 0;
+        if (tid == 0) {
+            P.ctrl->err = 0;
+            P.ctrl->router_done = 0;
+            P.ctrl->gu_all = 0;
+            P.ctrl->dn_done = 0;
+        }
+        __syncthreads();
+        if (tid == 0) {
+            __threadfence();
+            *reinterpret_cast<volatile unsigned long long *>(&P.ctrl->call) = P.call_id;
+        }
+    }
+    auto await_call = [&]() {  // thread 0
+        const volatile unsigned long long *cp = &P.ctrl->call;
+        if (*cp == P.call_id) return;
+        const uint64_t t0 = globaltimer_ns();
+        while (*cp != P.call_id) {
+            __nanosleep(32);
+            if (globaltimer_ns() - t0 > kWaitNs) {
+                flag_error(P.ctrl, kErrWaitExpired);
+                return;
+            }
+        }
+        __threadfence();
+    };
     __syncthreads();
     // the shared expert's gate/up goes to the CTAs without a router item, so that every CTA
     // reaches the routing wait at about the same time
@@ -451,6 +480,7 @@ __global__ void __launch_bounds__(kNT, 2) moe_decode1_kernel(const DecParams P) 
         router_item<1>(P, c);
         __syncthreads();
         if (tid == 0) {
+            await_call();
             __threadfence();
             atomicAdd(&P.ctrl->router_done, 1);
         }
@@ -461,6 +491,7 @@ __global__ void __launch_bounds__(kNT, 2) moe_decode1_kernel(const DecParams P) 
 
     // ---------------- R: routing
     if (tid == 0) {
+        await_call();
         wait_at_least(&P.ctrl->router_done, P.R, P.ctrl);
         __threadfence();
     }

@@ -33,6 +33,7 @@ struct DecCtrl {
     int gu_all;                        // single-token kernel: finished gate/up units, all slots
     int q_b, q_c, q_d;                 // token-group kernel: next chunk of phases B, C, D
     int pad[9];
+    unsigned long long call;           // single-token kernel: id of the call whose counters these are
     int hmax[kMaxK + 1];               // single-token kernel: max |h| per slot (float bits)
     int gu_done[kMaxE + 1];            // finished gate/up units per slot (shared: index kMaxE)
 };
@@ -56,6 +57,7 @@ struct DecParams {
     int groups_sh, G_sh;       // shared expert token groups and gate/up units
     // single-token kernel (decode1.cu): shared-memory offsets and output rows per CTA
     int single, d1_act_off, d1_rsc_off, d1_y_off, d1_rows;
+    unsigned long long call_id;  // single-token kernel: unique per call (counters reset in-kernel)
 };
 
 bool decode_plan(const coli_moe_desc &d, DecParams &P, int grid);

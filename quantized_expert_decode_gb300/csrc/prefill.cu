@@ -11,13 +11,14 @@
 //
 // One persistent CTA per SM walks the tiles (slot, token block, row block) of a launch, its
 // warps specialised:
-//   warps 0-15 producers, over the CTA's K-steps (64 wide) of all its tiles in order, thread
-//              (r, quarter) owning a quarter row: three steps ahead, cp.async copies that quarter
-//              of A row r's packed weight bytes into a raw buffer and of token row r < N of B
-//              (bf16) straight into its 128-byte-swizzled K-major slots; then, for the current
-//              step, it dequantises its raw quarter row into the swizzled bf16 A tile and the
-//              stage's `full` mbarrier collects the 512 arrivals (four producer warps per SMSP
-//              hide each other's latency)
+//   warps 0-7  copy warps, over the CTA's K-steps (64 wide) of all its tiles in order, thread
+//              (r, half): once the stage is free, cp.async of that half of A row r's packed
+//              weight bytes into the stage's raw buffer and of token row r < N of B (bf16)
+//              straight into its 128-byte-swizzled K-major slots; two steps later the thread
+//              waits for those copies, fences them for the tensor core and arrives on the
+//              stage's `landed` mbarrier — copies run up to the ring's depth ahead
+//   warps 8-15 dequant warps: once a stage has landed, thread (r, half) turns its half of raw
+//              row r into the swizzled bf16 A tile, fences, and arrives on the stage's `full`
 //   warp 16    one thread issues four tcgen05.mma (K = 16 each) per stage into one of two TMEM
 //              accumulators and commits the stage's `empty` mbarrier to their completion; after
 //              a tile's last step it commits that accumulator's `accf`
@@ -44,13 +45,12 @@ namespace {
 constexpr int kTcM = 128;        // MMA M: weight rows per tile
 constexpr int kTcN = 128;        // max tokens per tile (MMA N, multiple of 16)
 constexpr int kTcKB = 64;        // K per stage (one 128-byte swizzle row of bf16)
-constexpr int kTcStages = 5;
-constexpr int kTcAhead = 3;      // K-steps the producers' copies run ahead
-constexpr int kTcThreads = 672;  // producers 0-15, MMA warp 16, epilogue 17-20
-constexpr int kTcProd = 512, kTcEpi = 128;
+constexpr int kTcA = 3;          // bf16 A tiles (the MMA runs at most a step behind the dequant)
+constexpr int kTcCMax = 7;       // copy stages (raw weights + B), the deepest ring
+constexpr int kTcThreads = 672;  // copy warps 0-7, dequant warps 8-15, MMA warp 16, epilogue 17-20
+constexpr int kTcCopy = 256, kTcDeq = 256, kTcEpi = 128;
 constexpr int kTcMmaWarp = 16;
 constexpr int kTileCap = 128;    // tiles per CTA whose parameters are kept in shared memory
-constexpr int kTcRawStride = 80; // bytes per raw weight row in a stage (>= 64, bank-spread)
 constexpr unsigned long long kTcWaitNs = 2000000000ull;
 
 struct PfParams {
@@ -72,15 +72,30 @@ struct Tile {
 };
 
 struct TcSmem {  // after the 1024-aligned stage buffers
-    uint64_t full[kTcStages], empty[kTcStages], accf[2], tfree[2], drain;
+    uint64_t landed[kTcCMax], emptyc[kTcCMax], full[kTcA], emptya[kTcA], accf[2], tfree[2], drain;
     uint32_t tmem_base;
     int abort;
     int pref[kMaxE + 2];  // tiles before slot g (slots 0..E-1 routed, E shared)
     Tile tiles[kTileCap]; // this CTA's tiles blockIdx.x + i * gridDim.x, looked up once
 };
 
-constexpr size_t kStageA = (size_t)kTcM * 128, kStageB = (size_t)kTcN * 128, kStageRaw = (size_t)kTcM * kTcRawStride;
-constexpr size_t kTcSmemBytes = 1024 + kTcStages * (kStageA + kStageB + kStageRaw) + sizeof(TcSmem);
+// Ring geometry per weight format: NC copy stages of raw weight rows (RS bytes per row: the
+// packed bytes of one K-step plus 16, which spreads the rows over the banks) and B tiles; a
+// copy thread fences and announces its copies LAG steps after issuing them (LAG <= NC - 2).
+template <int NC, int RS, int LAG>
+struct Ring {
+    static constexpr int kC = NC, kRS = RS, kLag = LAG;
+};
+// (measured on the prefill workload: lags 2 and 4 run at 6.7 ms, lags 3 and 5 at 7.7 ms, for 5 or
+// 7 copy stages alike)
+using RingNarrow = Ring<7, 48, 4>;  // int4 / int2 weights
+using RingWide = Ring<5, 80, 2>;    // int8 weights
+
+constexpr size_t kStageA = (size_t)kTcM * 128, kStageB = (size_t)kTcN * 128;
+template <class RG>
+constexpr size_t tc_smem_bytes() {
+    return 1024 + kTcA * kStageA + RG::kC * (kStageB + (size_t)kTcM * RG::kRS) + sizeof(TcSmem);
+}
 
 // position of element j of a K block in the permuted order of format fmt
 __host__ __device__ __forceinline__ int kperm(int fmt, int j) {
@@ -200,17 +215,14 @@ __device__ __forceinline__ void cp_async8(void *dst_smem, const void *src) {
     asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(smem_u32(dst_smem)), "l"(src) : "memory");
 }
 
-__device__ __forceinline__ void cp_async4(void *dst_smem, const void *src) {
-    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst_smem)), "l"(src) : "memory");
-}
 
-// The producer thread (r, h) of a tile: quarter h of A row r (gate/up interleaved — even rows
+// The copy / dequant thread (r, h) of a tile: half h of A row r (gate/up interleaved — even rows
 // gate j0 + r/2, odd rows up — or down row d0 + r) and of B row r (token n0 + r, clamped to the
 // buffer; rows >= N are not copied).
 struct ProdRow {
-    const uint8_t *a;   // packed weights of A row r at K-step 0, quarter h
-    const uint16_t *b;  // bf16 activations of B row r at K-step 0, quarter h
-    int qq;             // packed bytes per quarter K-step
+    const uint8_t *a;   // packed weights of A row r at K-step 0, half h
+    const uint16_t *b;  // bf16 activations of B row r at K-step 0, half h
+    int qh;             // packed bytes per half K-step
     bool has_b;
 };
 
@@ -224,66 +236,75 @@ __device__ __forceinline__ ProdRow prod_row(const PfParams &P, const Tile &T, in
         const int j = min(T.row0 + (r >> 1), T.inter - 1);
         base = ((r & 1) ? T.w1 : T.w0) + (size_t)j * row_bytes(T.fmt, P.H);
     }
-    pr.qq = qb / 4;
-    pr.a = base + h * pr.qq;
+    pr.qh = qb / 2;
+    pr.a = base + h * pr.qh;
     const int rows_total = P.T * P.K + P.T;
     const int row = min(T.pbase + T.n0 + r, rows_total - 1);
-    pr.b = (P.down ? P.hb + (size_t)row * P.ldh : P.xb + (size_t)row * P.H) + 16 * h;
+    pr.b = (P.down ? P.hb + (size_t)row * P.ldh : P.xb + (size_t)row * P.H) + 32 * h;
     pr.has_b = r < T.N;
     return pr;
 }
 
-// K-step kb: cp.async of the quarter rows into the stage's raw buffer and B tile
-__device__ __forceinline__ void issue_step(const ProdRow &pr, int kb, uint8_t *raw, uint8_t *sb, int r, int h) {
-    const uint8_t *src = pr.a + (size_t)kb * 4 * pr.qq;
-    uint8_t *dst = raw + r * kTcRawStride + h * pr.qq;
-    if (pr.qq == 4) cp_async4(dst, src);
-    else if (pr.qq == 8) cp_async8(dst, src);
-    else cp_async16(dst, src);
+// K-step kb: cp.async of the half rows into the stage's raw buffer and B tile
+__device__ __forceinline__ void issue_step(const ProdRow &pr, int kb, uint8_t *raw, int rs, uint8_t *sb, int r,
+                                           int h) {
+    const uint8_t *src = pr.a + (size_t)kb * 2 * pr.qh;
+    uint8_t *dst = raw + r * rs + h * pr.qh;
+    if (pr.qh == 8) cp_async8(dst, src);
+    else
+        for (int i = 0; i < pr.qh / 16; i++) cp_async16(dst + 16 * i, src + 16 * i);
     if (pr.has_b) {
         const uint16_t *bs = pr.b + (size_t)kb * kTcKB;
 #pragma unroll
-        for (int c = 0; c < 2; c++) {
-            const int cc = 2 * h + c;
+        for (int c = 0; c < 4; c++) {
+            const int cc = 4 * h + c;
             cp_async16(sb + (r >> 3) * 1024 + (r & 7) * 128 + ((cc ^ (r & 7)) << 4), bs + 8 * c);
         }
     }
 }
 
-// dequantise the thread's raw quarter row into chunks 2h, 2h+1 of row r of the swizzled A tile
+// dequantise the thread's raw half row into chunks 4h..4h+3 of row r of the swizzled A tile
 template <int FMT>
-__device__ __forceinline__ void dequant_quarter(const uint8_t *raw, uint8_t *sa, int r, int h) {
-    constexpr int QQ = (FMT == COLI_FMT_INT4 ? 32 : FMT == COLI_FMT_INT2 ? 16 : 64) / 4;
-    uint32_t w[4];
-    const uint8_t *src = raw + r * kTcRawStride + h * QQ;
-    if (QQ == 4) {
-        w[0] = *reinterpret_cast<const uint32_t *>(src);
-    } else if (QQ == 8) {
+__device__ __forceinline__ void dequant_half(const uint8_t *raw, int rs, uint8_t *sa, int r, int h) {
+    constexpr int QH = (FMT == COLI_FMT_INT4 ? 32 : FMT == COLI_FMT_INT2 ? 16 : 64) / 2;
+    const uint8_t *src = raw + r * rs + h * QH;
+    uint32_t w[8];
+    if (QH == 8) {
         const uint2 v = *reinterpret_cast<const uint2 *>(src);
         w[0] = v.x;
         w[1] = v.y;
     } else {
-        const uint4 v = *reinterpret_cast<const uint4 *>(src);
-        w[0] = v.x;
-        w[1] = v.y;
-        w[2] = v.z;
-        w[3] = v.w;
+#pragma unroll
+        for (int i = 0; i < QH / 16; i++) {
+            const uint4 v = *reinterpret_cast<const uint4 *>(src + 16 * i);
+            w[4 * i] = v.x;
+            w[4 * i + 1] = v.y;
+            w[4 * i + 2] = v.z;
+            w[4 * i + 3] = v.w;
+        }
     }
-    uint32_t o[8];
-    deq16_bf16<FMT>(w, o);
-    st_sw128(sa, r, 2 * h, make_uint4(o[0], o[1], o[2], o[3]));
-    st_sw128(sa, r, 2 * h + 1, make_uint4(o[4], o[5], o[6], o[7]));
+    constexpr int WPQ = QH / 8;  // words per 16 weights
+#pragma unroll
+    for (int c2 = 0; c2 < 2; c2++) {
+        uint32_t o[8];
+        deq16_bf16<FMT>(w + c2 * WPQ, o);
+        st_sw128(sa, r, 4 * h + 2 * c2, make_uint4(o[0], o[1], o[2], o[3]));
+        st_sw128(sa, r, 4 * h + 2 * c2 + 1, make_uint4(o[4], o[5], o[6], o[7]));
+    }
 }
 
 __device__ __forceinline__ uint16_t bf16_bits(float f) {
     return (uint16_t)(pack_bf16(f, 0.f) & 0xFFFFu);
 }
 
+template <class RG>
 __global__ void __launch_bounds__(kTcThreads, 1) moe_prefill_tc_kernel(const PfParams P) {
+    constexpr int kC = RG::kC, kRS = RG::kRS, kLag = RG::kLag;
+    constexpr size_t kStageRaw = (size_t)kTcM * kRS;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
-    uint8_t *sA = smem, *sB = smem + kTcStages * kStageA, *sR = sB + kTcStages * kStageB;
-    TcSmem &ts = *reinterpret_cast<TcSmem *>(sR + kTcStages * kStageRaw);
+    uint8_t *sA = smem, *sB = smem + kTcA * kStageA, *sR = sB + kC * kStageB;
+    TcSmem &ts = *reinterpret_cast<TcSmem *>(sR + kC * kStageRaw);
     const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
     const int nslots = P.E + (P.Is > 0 ? 1 : 0);
 
@@ -350,9 +371,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) moe_prefill_tc_kernel(const PfP
     }
     if (tid == 0) {
         ts.abort = 0;
-        for (int s = 0; s < kTcStages; s++) {
-            mbar_init(&ts.full[s], kTcProd);
-            mbar_init(&ts.empty[s], 1);
+        for (int s = 0; s < kC; s++) {
+            mbar_init(&ts.landed[s], kTcCopy);
+            mbar_init(&ts.emptyc[s], 1);
+        }
+        for (int s = 0; s < kTcA; s++) {
+            mbar_init(&ts.full[s], kTcDeq);
+            mbar_init(&ts.emptya[s], 1);
         }
         for (int b = 0; b < 2; b++) {
             mbar_init(&ts.accf[b], 1);
@@ -377,51 +402,59 @@ __global__ void __launch_bounds__(kTcThreads, 1) moe_prefill_tc_kernel(const PfP
         return i < kTileCap ? ts.tiles[i] : make_tile(P, ts, t);
     };
 
-    if (warp < kTcMmaWarp) {
-        // ---------------- producers
+    if (warp < 8) {
+        // ---------------- copy warps
         const int r = tid & 127, h = tid >> 7;
-        int ti = blockIdx.x, ki = 0;  // issue cursor: tile, K-step
+        int ti = blockIdx.x, ki = 0;  // copy cursor: tile, K-step
         Tile Ti = ti < total ? tile_at(ti) : Tile{};
         ProdRow pi = prod_row(P, Ti, r, h);
         int nki = ti < total ? nkb_of(Ti) : 0;
-        uint32_t gi = 0;              // steps issued
-        auto issue_next = [&]() {
-            if (ti < total) {
-                const int s = gi % kTcStages;
-                const uint32_t use = gi / kTcStages;
-                if (use > 0 && !mbar_wait_bounded(&ts.empty[s], (use - 1) & 1, ts, P.err)) return;
-                issue_step(pi, ki, sR + s * kStageRaw, sB + s * kStageB, r, h);
-                gi++;
-                if (++ki == nki) {
-                    ki = 0;
-                    ti += G;
-                    if (ti < total) {
-                        Ti = tile_at(ti);
-                        pi = prod_row(P, Ti, r, h);
-                        nki = nkb_of(Ti);
-                    }
+        uint32_t g = 0;  // steps issued
+        while (ti < total && !ts.abort) {
+            const int s = g % kC;
+            const uint32_t use = g / kC;
+            if (use > 0 && !mbar_wait_bounded(&ts.emptyc[s], (use - 1) & 1, ts, P.err)) break;
+            issue_step(pi, ki, sR + s * kStageRaw, kRS, sB + s * kStageB, r, h);
+            cp_async_commit();
+            if (++ki == nki) {
+                ki = 0;
+                ti += G;
+                if (ti < total) {
+                    Ti = tile_at(ti);
+                    pi = prod_row(P, Ti, r, h);
+                    nki = nkb_of(Ti);
                 }
             }
-            cp_async_commit();
-        };
-        for (int d = 0; d < kTcAhead; d++) issue_next();
-        uint32_t gp = 0;  // steps processed
+            if (g >= (uint32_t)kLag) {  // step g - kLag: its copies are in; fence and announce
+                cp_async_wait<kLag>();
+                fence_async_smem();
+                mbar_arrive(&ts.landed[(g - kLag) % kC]);
+            }
+            g++;
+        }
+        // the last steps inside the lag
+        cp_async_wait<0>();
+        fence_async_smem();
+        for (uint32_t q = g >= (uint32_t)kLag ? g - kLag : 0; q < g; q++) mbar_arrive(&ts.landed[q % kC]);
+    } else if (warp < kTcMmaWarp) {
+        // ---------------- dequant warps
+        const int r = (tid - kTcCopy) & 127, h = (tid - kTcCopy) >> 7;
+        uint32_t g = 0;
         for (int t = blockIdx.x; t < total && !ts.abort; t += G) {
             const Tile T = tile_at(t);
             const int fmt = T.fmt, nkb = nkb_of(T);
-            for (int kb = 0; kb < nkb; kb++, gp++) {
-                issue_next();
-                cp_async_wait<kTcAhead>();  // this step's copies have landed
-                const int s = gp % kTcStages;
-                if (fmt == COLI_FMT_INT4) dequant_quarter<COLI_FMT_INT4>(sR + s * kStageRaw, sA + s * kStageA, r, h);
-                else if (fmt == COLI_FMT_INT8) dequant_quarter<COLI_FMT_INT8>(sR + s * kStageRaw, sA + s * kStageA, r, h);
-                else dequant_quarter<COLI_FMT_INT2>(sR + s * kStageRaw, sA + s * kStageA, r, h);
+            for (int kb = 0; kb < nkb; kb++, g++) {
+                const int s = g % kC, a = g % kTcA;
+                if (!mbar_wait_bounded(&ts.landed[s], (g / kC) & 1, ts, P.err)) break;
+                if (g >= (uint32_t)kTcA && !mbar_wait_bounded(&ts.emptya[a], ((g / kTcA) - 1) & 1, ts, P.err)) break;
+                uint8_t *sa = sA + a * kStageA;
+                if (fmt == COLI_FMT_INT4) dequant_half<COLI_FMT_INT4>(sR + s * kStageRaw, kRS, sa, r, h);
+                else if (fmt == COLI_FMT_INT8) dequant_half<COLI_FMT_INT8>(sR + s * kStageRaw, kRS, sa, r, h);
+                else dequant_half<COLI_FMT_INT2>(sR + s * kStageRaw, kRS, sa, r, h);
                 fence_async_smem();
-                mbar_arrive(&ts.full[s]);
-                if (ts.abort) break;
+                mbar_arrive(&ts.full[a]);
             }
         }
-        cp_async_wait<0>();
     } else if (warp == kTcMmaWarp) {
         // ---------------- MMA issuer
         if (lane == 0) {
@@ -434,14 +467,15 @@ __global__ void __launch_bounds__(kTcThreads, 1) moe_prefill_tc_kernel(const PfP
                 tc_fence_after_sync();
                 const uint32_t idesc = idesc_bf16_f32(kTcM, T.N), dcol = tbase + b * kTcN;
                 for (int kb = 0; kb < nkb; kb++, gk++) {
-                    const int s = gk % kTcStages;
-                    if (!mbar_wait_bounded(&ts.full[s], (gk / kTcStages) & 1, ts, P.err)) break;
+                    const int s = gk % kC, a = gk % kTcA;
+                    if (!mbar_wait_bounded(&ts.full[a], (gk / kTcA) & 1, ts, P.err)) break;
                     tc_fence_after_sync();
-                    const uint32_t a0 = smem_u32(sA + s * kStageA), b0 = smem_u32(sB + s * kStageB);
+                    const uint32_t a0 = smem_u32(sA + a * kStageA), b0 = smem_u32(sB + s * kStageB);
 #pragma unroll
                     for (int k = 0; k < kTcKB / 16; k++)
                         tc_mma_bf16(dcol, sdesc_k_sw128(a0 + 32 * k), sdesc_k_sw128(b0 + 32 * k), idesc, (kb | k) != 0);
-                    tc_commit(&ts.empty[s]);
+                    tc_commit(&ts.emptyc[s]);
+                    tc_commit(&ts.emptya[a]);
                 }
                 tc_commit(&ts.accf[b]);
             }
@@ -561,7 +595,6 @@ bool prefill_supported(const coli_moe_desc &d) {
     return d.H % 64 == 0 && d.I % 64 == 0 && d.I_shared % 64 == 0 && d.E <= kMaxE;
 }
 
-size_t prefill_smem_bytes() { return kTcSmemBytes; }
 
 cudaError_t launch_prefill(const PrefillWork &w, int part, cudaStream_t st) {
     cudaError_t e;
@@ -573,9 +606,6 @@ cudaError_t launch_prefill(const PrefillWork &w, int part, cudaStream_t st) {
                                                            w.routed_fmt, w.shared_fmt, w.I_shared > 0);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
-    if ((e = cudaFuncSetAttribute(moe_prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  (int)kTcSmemBytes)) != cudaSuccess)
-        return e;
     PfParams P{};
     P.experts = w.experts;
     P.shared = w.shared;
@@ -595,7 +625,13 @@ cudaError_t launch_prefill(const PrefillWork &w, int part, cudaStream_t st) {
     P.sfmt = w.shared_fmt;
     P.ldh = w.ldh;
     P.down = part;
-    moe_prefill_tc_kernel<<<w.grid, kTcThreads, kTcSmemBytes, st>>>(P);
+    // the deeper copy ring unless an int8 matrix needs the wider raw rows
+    const bool wide = w.routed_fmt == COLI_FMT_INT8 || (w.I_shared > 0 && w.shared_fmt == COLI_FMT_INT8);
+    const void *fn = wide ? (const void *)moe_prefill_tc_kernel<RingWide> : (const void *)moe_prefill_tc_kernel<RingNarrow>;
+    const size_t smem = wide ? tc_smem_bytes<RingWide>() : tc_smem_bytes<RingNarrow>();
+    if ((e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) != cudaSuccess) return e;
+    if (wide) moe_prefill_tc_kernel<RingWide><<<w.grid, kTcThreads, smem, st>>>(P);
+    else moe_prefill_tc_kernel<RingNarrow><<<w.grid, kTcThreads, smem, st>>>(P);
     return cudaGetLastError();
 }
 

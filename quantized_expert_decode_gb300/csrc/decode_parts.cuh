@@ -37,17 +37,6 @@ __device__ bool wait_at_least(const int *p, int target, DecCtrl *c) {
 
 __device__ __forceinline__ int range_lo(int n, int c, int G) { return (int)((long long)n * c / G); }
 
-// first index i in [0, n) with off[i+1] > x (off: nondecreasing prefix array, off[0] = 0)
-__device__ int upper_slot(const int *off, int n, int x) {
-    int lo = 0, hi = n - 1;
-    while (lo < hi) {
-        const int mid = (lo + hi) >> 1;
-        if (__ldcg(off + mid + 1) > x) hi = mid;
-        else lo = mid + 1;
-    }
-    return lo;
-}
-
 __device__ __forceinline__ bool bad16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) != 0; }
 
 // ------------------------------------------------------------------ the streaming core

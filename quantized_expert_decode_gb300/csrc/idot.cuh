@@ -95,20 +95,6 @@ __device__ __forceinline__ void idot_chunk(const uint4 (&w)[NR], const uint4 *xq
     }
 }
 
-// lane partials -> exact warp totals S_r (every lane gets them)
-template <int FMT, int NR>
-__device__ __forceinline__ void idot_reduce(const int (&acc)[NR][3], long long (&out)[NR]) {
-    constexpr int LS = IQ<FMT>::LOG_SC;
-#pragma unroll
-    for (int r = 0; r < NR; r++) {
-        long long p = ((long long)(acc[r][2] >> LS) << 16) + ((long long)(acc[r][1] >> LS) << 8) +
-                      (long long)(acc[r][0] >> LS);
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) p += __shfl_xor_sync(kFull, p, o);
-        out[r] = p;
-    }
-}
-
 // Four rows at once, transposing as it reduces: rows {0,1} and {2,3} are split between the lane
 // halves, then between the quarters, so 12 shuffles (instead of 40) leave every lane with the
 // exact total of row lane / 8.

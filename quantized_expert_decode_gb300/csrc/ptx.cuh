@@ -1,5 +1,5 @@
-// ptx.cuh — thin inline-PTX helpers for sm_100+ (mbarrier, bulk async copies, timers,
-// named barriers, release/acquire flags). Internal to libcolimoe.
+// ptx.cuh — thin inline-PTX helpers for sm_100+ (mbarrier, timers, volatile flag loads).
+// Internal to libcolimoe.
 #pragma once
 
 #include <cstdint>
@@ -20,11 +20,6 @@ __device__ __forceinline__ void fence_mbar_init() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
-                 : "memory");
-}
-
 __device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
@@ -41,25 +36,10 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     return ok != 0;
 }
 
-// global -> shared bulk copy (16-byte aligned addresses, size a multiple of 16) completing
-// `bytes` of transaction count on `bar`
-__device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-            smem_u32(dst)),
-        "l"(src), "r"(bytes), "r"(smem_u32(bar))
-        : "memory");
-}
-
 __device__ __forceinline__ uint64_t globaltimer_ns() {
     uint64_t t;
     asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
     return t;
-}
-
-// barrier among `nthreads` threads (multiple of 32) on hardware barrier `id` (1..15)
-__device__ __forceinline__ void named_bar(int id, int nthreads) {
-    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
 __device__ __forceinline__ int ld_volatile(const int *p) {

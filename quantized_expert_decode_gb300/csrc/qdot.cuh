@@ -179,52 +179,6 @@ __device__ __forceinline__ void qdot_rows(const uint8_t *const (&rows)[NR], cons
         }
 }
 
-// Accumulating variant for weights already staged in shared memory: rows[r] points at the
-// first byte of this stage's slice of row r (nchunks 16-byte chunks), whose chunk c is chunk
-// cg0 + c of the full row (the staged activations are indexed by the full-row chunk). No
-// reduction: acc keeps the lane's f32x2 partial sums across stages.
-template <int FMT, int NR, int NV>
-__device__ __forceinline__ void qdot_smem_acc(const uint8_t *const (&rows)[NR], int cg0, int nchunks,
-                                              const float *xs, int xstride, int CPR, int lane,
-                                              float2 (&acc)[NR][NV]) {
-    using G = QGeom<FMT>;
-    const float4 *xs4 = reinterpret_cast<const float4 *>(xs);
-    const int xstride4 = xstride / 4;
-    for (int c = lane; c < nchunks; c += kWarp) {
-        const int cg = cg0 + c;
-        uint4 wv[NR];
-#pragma unroll
-        for (int r = 0; r < NR; r++) wv[r] = *reinterpret_cast<const uint4 *>(rows[r] + 16 * c);
-#pragma unroll
-        for (int wi = 0; wi < 4; wi++) {
-            float4 xv[NV][G::F4W];
-#pragma unroll
-            for (int v = 0; v < NV; v++)
-#pragma unroll
-                for (int j = 0; j < G::F4W; j++)
-                    xv[v][j] = xs4[v * xstride4 + (wi * G::F4W + j) * CPR + cg];
-#pragma unroll
-            for (int r = 0; r < NR; r++) {
-                const uint32_t q = word_of(wv[r], wi);
-                const uint32_t qh = q >> 16;
-#pragma unroll
-                for (int m = 0; m < G::HALF; m++) {
-                    const uint32_t lo = lop3_and_xor(q, G::mask(m), G::xorv(m));
-                    const uint32_t hi = lop3_and_xor(qh, G::mask(m), G::xorv(m));
-                    const float2 d = __fadd2_rn(make_float2(__uint_as_float(lo), __uint_as_float(hi)),
-                                                make_float2(-G::magic(m), -G::magic(m)));
-#pragma unroll
-                    for (int v = 0; v < NV; v++) {
-                        const float4 &x4 = xv[v][m >> 1];
-                        const float2 x2 = (m & 1) ? make_float2(x4.z, x4.w) : make_float2(x4.x, x4.y);
-                        acc[r][v] = __ffma2_rn(d, x2, acc[r][v]);
-                    }
-                }
-            }
-        }
-    }
-}
-
 // Warp-wide sums of f32x2 partials: every lane gets out[r][v].
 template <int NR, int NV>
 __device__ __forceinline__ void warp_reduce_acc(const float2 (&acc)[NR][NV], float (&out)[NR][NV]) {

@@ -322,3 +322,25 @@ def test_prefill_is_deterministic(qed):
     a, _, _ = run_forward(qed, dev, blk["x"])
     b, _, _ = run_forward(qed, dev, blk["x"])
     assert np.array_equal(a, b)
+
+
+def test_one_token_dirty_workspace(qed, blocks):
+    """The single-token kernel resets its own counters from a per-call id: a workspace full of
+    garbage (here: random bytes, then the bytes of the previous call's counter block) between
+    calls must not change the result."""
+    blk, dev = blocks(1)
+    cfg = blk["cfg"]
+    xs = synth.make_x_batches(cfg, 717, 3)
+    ref = []
+    for i in range(3):
+        out, _, _ = run_forward(qed, dev, xs[i])
+        ref.append(out)
+    ctrl = dev.ws[:4096].clone()
+    g = torch.Generator(device="cpu").manual_seed(5)
+    for i in range(3):
+        noise = torch.randint(0, 256, (dev.ws.numel(),), dtype=torch.uint8, generator=g)
+        dev.ws.copy_(noise.to(dev.ws.device))  # the workspace is a byte buffer
+        if i == 1:
+            dev.ws[:4096].copy_(ctrl)  # the counter block exactly as a finished call left it
+        out, _, _ = run_forward(qed, dev, xs[i])
+        assert np.array_equal(out, ref[i]), i

@@ -12,7 +12,8 @@
 //      bias, greedy top-K with ties to the lower index (found as ranks: an expert's place in
 //      the greedy order is the number of experts that beat it), TOPK/TOPP, renorm, routed
 //      scale. The kept experts become slots 0..U-1 in ascending id order; the shared expert
-//      is slot U. Their weight pointers go to shared memory in one round trip.
+//      is slot U. Their weight pointers are loaded by the selecting lanes while the weights
+//      are renormalised.
 //   C  routed gate/up rows: h = silu(gate.x * s_g) * (up.x * s_u); every CTA also records the
 //      largest |h| of each slot it wrote, the block fixed-point exponent of the down step
 //   D  once every gate/up row is in (one counter): (slot, 4-row group) units split slot-major
@@ -264,6 +265,10 @@ __device__ __noinline__ void route1(const DecParams &P, D1S &m, float *sg, float
         if (nsel < Ksel && out && lane == 0) flag_error(P.ctrl, kErrNoCandidate);
         int Ke = nsel;
         if (P.top_p > 0.f && P.top_p < 1.f) Ke = top_p_cut(P.top_p, nsel, id, wv);
+        // each kept lane asks for its expert's weight pointers now; they arrive while the
+        // weights are renormalised
+        coli_moe_expert ex{};
+        if (lane < Ke) ex = P.experts[id];
         float sm = 1.f;
         if (P.norm_topk) {
             sm = 0.f;
@@ -279,7 +284,11 @@ __device__ __noinline__ void route1(const DecParams &P, D1S &m, float *sg, float
         if (lane < K) {
             m.w[lane] = wk;
             m.pos[lane] = kept ? slot : -1;
-            if (kept) m.slot_e[slot] = id;
+            if (kept) {
+                m.slot_e[slot] = id;
+                if (bad16(ex.gate_w) || bad16(ex.up_w) || bad16(ex.down_w)) flag_error(P.ctrl, kErrBadExpert);
+                m.rec[slot] = rec_of(ex);
+            }
             if (out) {
                 P.idx[lane] = id;
                 P.w[lane] = wk;
@@ -296,9 +305,9 @@ __device__ __noinline__ void route1(const DecParams &P, D1S &m, float *sg, float
         }
     }
     __syncthreads();
-    // 4. bucket counts (CTA 0) and the kept experts' weight pointers (every CTA)
-    const int U = m.U;
+    // 4. bucket counts (CTA 0 only; nothing in this CTA reads them)
     if (out) {
+        const int U = m.U;
         for (int e = tid; e < E; e += kNT) {
             int cnt = 0, o = 0;
             for (int u = 0; u < U; u++) {
@@ -311,12 +320,6 @@ __device__ __noinline__ void route1(const DecParams &P, D1S &m, float *sg, float
         }
         if (tid == 0) P.offsets[E] = U;
     }
-    if (tid < U) {
-        const coli_moe_expert ex = P.experts[m.slot_e[tid]];
-        if (bad16(ex.gate_w) || bad16(ex.up_w) || bad16(ex.down_w)) flag_error(P.ctrl, kErrBadExpert);
-        m.rec[tid] = rec_of(ex);
-    }
-    __syncthreads();
 }
 
 // B / C: gate/up units [b, e) (shared: the shared expert's, else slot-major over the routed

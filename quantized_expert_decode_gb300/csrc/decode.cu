@@ -486,6 +486,9 @@ struct Misc {
     int xshift;               // integer core: X = round(x * 2^xshift)
     float xinv;               // 2^-xshift
     float redf[kNW];
+    float redv[4][kNW];       // tensor-core staging: per-token max |x| of each warp
+    float vf[4][2];           // ... the two exact factors of 2^e of each token
+    float vinv[4];            // ... and 2^-e
     float sc[2][4 * kScCap];  // row scales of the piece's units (gate/up: gate, up; down: [0])
 };
 
@@ -524,6 +527,46 @@ __device__ void stage_limbs(const float *__restrict__ src, int len, bool coheren
     }
 }
 
+// Multi-token groups: the group's vectors as f16 hi/lo parts in the tensor-core layout
+// (mma.cuh), token v scaled by its own 2^e so that max|x_v| * 2^e lies in [2^14, 2^15).
+template <int FMT, class SrcOf>
+__device__ void stage_mma(SrcOf src_of, int nv, int len, bool coherent, uint8_t *xs, size_t stride, Misc &m) {
+    const int tid = threadIdx.x, lane = tid % kWarp, warp = tid / kWarp;
+    const int n4 = len / 4;
+    for (int v = 0; v < nv; v++) {
+        const float *src = src_of(v);
+        float mx = 0.f;
+        for (int q = tid; q < n4; q += kNT) {
+            const float4 a = ld_act4(src, q, coherent);
+            mx = fmaxf(mx, fmaxf(fmaxf(fabsf(a.x), fabsf(a.y)), fmaxf(fabsf(a.z), fabsf(a.w))));
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, o));
+        if (lane == 0) m.redv[v][warp] = mx;
+    }
+    __syncthreads();
+    if (tid < nv) {
+        float mx = m.redv[tid][0];
+#pragma unroll
+        for (int w = 1; w < kNW; w++) mx = fmaxf(mx, m.redv[tid][w]);
+        int e = 0;
+        if (mx > 0.f) {
+            const int ex = (int)((__float_as_uint(mx) >> 23) & 255u);
+            e = 14 - (ex == 0 ? -126 : ex - 127);
+        }
+        const int e1 = max(-126, min(126, e)), e2 = e - e1;
+        m.vf[tid][0] = __int_as_float((e1 + 127) << 23);
+        m.vf[tid][1] = __int_as_float((e2 + 127) << 23);
+        m.vinv[tid] = ldexpf(1.f, -e);
+    }
+    __syncthreads();
+    const int items = mma_items<FMT>(len);
+    for (int idx = tid; idx < nv * items; idx += kNT) {
+        const int v = idx / items, it = idx - v * items;
+        stage_mma_item<FMT>(src_of(v), len, coherent, xs + (size_t)v * stride, m.vf[v][0], m.vf[v][1], it);
+    }
+}
+
 __device__ __noinline__ void stage_acts(const DecParams &P, const RTab &rt, const Seg &g, bool down, void *xs,
                                         Misc &m) {
     const int len = down ? g.inter : P.H;
@@ -536,24 +579,17 @@ __device__ __noinline__ void stage_acts(const DecParams &P, const RTab &rt, cons
         const int t = g.shared ? pv : rt.perm[g.pbase + pv] / P.K;
         return P.x + (size_t)t * P.H;
     };
+    uint8_t *xq = static_cast<uint8_t *>(xs);
     if (g.nv == 1) {
-        uint8_t *xq = static_cast<uint8_t *>(xs);
         if (g.fmt == COLI_FMT_INT4) stage_limbs<COLI_FMT_INT4>(src_of(0), len, down, xq, m);
         else if (g.fmt == COLI_FMT_INT8) stage_limbs<COLI_FMT_INT8>(src_of(0), len, down, xq, m);
         else stage_limbs<COLI_FMT_INT2>(src_of(0), len, down, xq, m);
         return;
     }
-    float *xf = static_cast<float *>(xs);
-    for (int v = 0; v < P.NV; v++) {
-        float *dst = xf + (size_t)v * P.xs_stride;
-        if (v < g.nv) {
-            if (g.fmt == COLI_FMT_INT4) stage_row<COLI_FMT_INT4>(src_of(v), dst, len, down);
-            else if (g.fmt == COLI_FMT_INT8) stage_row<COLI_FMT_INT8>(src_of(v), dst, len, down);
-            else stage_row<COLI_FMT_INT2>(src_of(v), dst, len, down);
-        } else {
-            for (int i = threadIdx.x; i < len; i += kNT) dst[i] = 0.f;
-        }
-    }
+    const size_t stride = (size_t)P.xs_stride * 4;
+    if (g.fmt == COLI_FMT_INT4) stage_mma<COLI_FMT_INT4>(src_of, g.nv, len, down, xq, stride, m);
+    else if (g.fmt == COLI_FMT_INT8) stage_mma<COLI_FMT_INT8>(src_of, g.nv, len, down, xq, stride, m);
+    else stage_mma<COLI_FMT_INT2>(src_of, g.nv, len, down, xq, stride, m);
 }
 
 // h or y row of token v of the piece's group
@@ -595,37 +631,38 @@ __device__ void gateup_units_int(const DecParams &P, const Seg &g, const void *x
         });
 }
 
-template <int FMT, int NV>
-__device__ void gateup_units_flt(const DecParams &P, const Seg &g, const float *xs, const Misc &m) {
+// Multi-token groups (tensor cores): blocks of 8 row pairs, gate row j in MMA row g and up
+// row j in row g + 8, so lane (g, c < 2) ends with gate and up of row pair g for tokens 2c, 2c + 1.
+template <int FMT>
+__device__ void gateup_units_mma(const DecParams &P, const Seg &g, const uint8_t *xs, const Misc &m) {
     const int warp = threadIdx.x / kWarp, lane = threadIdx.x % kWarp;
-    const int nu = g.uhi - g.ulo;
-    const int mine = nu > warp ? (nu - warp + kNW - 1) / kNW : 0;
+    const int gq = lane >> 2, c = lane & 3;
+    const int jlo = 2 * (g.ulo - g.ubase);                    // first row pair of the piece
+    const int np = min(2 * (g.uhi - g.ulo), g.inter - jlo);  // row pairs of the piece
+    const int nb = (np + 7) / 8;
+    const int mine = nb > warp ? (nb - warp + kNW - 1) / kNW : 0;
     const int64_t rb = row_bytes(FMT, P.H);
-    const int ubase = g.ulo - g.ubase;
-    warp_stream<FMT, 4, NV>(
-        mine, (int)(rb / 16), xs, P.xs_stride, lane,
-        [&](int i, const uint8_t *(&rr)[4]) {
-            const int j = 2 * (ubase + warp + kNW * i);
-            const int j1 = min(j + 1, g.inter - 1);
+    const int tok = (gq & 3) < g.nv ? (gq & 3) : 0;
+    const uint8_t *xb = xs + (size_t)tok * P.xs_stride * 4 + (gq >> 2) * 64 + c * 16;
+    warp_stream_mma<FMT>(
+        mine, (int)(rb / 16), xb, lane,
+        [&](int i, const uint8_t *(&rr)[2]) {
+            const int j = min(jlo + 8 * (warp + kNW * i) + gq, g.inter - 1);
             rr[0] = g.w0 + (size_t)j * rb;
             rr[1] = g.w1 + (size_t)j * rb;
-            rr[2] = g.w0 + (size_t)j1 * rb;
-            rr[3] = g.w1 + (size_t)j1 * rb;
         },
-        [&](int i, const float (&s)[4][NV]) {
-            const int lj = 2 * (warp + kNW * i);
-            const int j = 2 * ubase + lj;
+        [&](int i, float (&d)[4]) {
 #pragma unroll
-            for (int v = 0; v < NV; v++) {
-                if (lane == v && v < g.nv) {
-                    float *hrow = P.h + (size_t)act_row(P, g, v) * P.ldh;
+            for (int q = 0; q < 4; q++) d[q] += __shfl_xor_sync(kFull, d[q], 2);  // hi + lo columns
+            const int lj = 8 * (warp + kNW * i) + gq;
+            if (c < 2 && lj < np) {
 #pragma unroll
-                    for (int q = 0; q < 2; q++) {
-                        if (j + q < g.inter) {
-                            const float gv = s[2 * q][v] * m.sc[0][lj + q];
-                            const float uv = s[2 * q + 1][v] * m.sc[1][lj + q];
-                            hrow[j + q] = gv / (1.f + expf(-gv)) * uv;
-                        }
+                for (int t = 0; t < 2; t++) {
+                    const int v = 2 * c + t;
+                    if (v < g.nv) {
+                        const float gv = (d[t] * m.vinv[v]) * m.sc[0][lj];
+                        const float uv = (d[2 + t] * m.vinv[v]) * m.sc[1][lj];
+                        P.h[(size_t)act_row(P, g, v) * P.ldh + jlo + lj] = gv / (1.f + expf(-gv)) * uv;
                     }
                 }
             }
@@ -657,47 +694,47 @@ __device__ void down_units_int(const DecParams &P, const Seg &g, const void *xs,
         });
 }
 
-template <int FMT, int NV>
-__device__ void down_units_flt(const DecParams &P, const Seg &g, const float *xs, const Misc &m) {
+// Multi-token groups (tensor cores): blocks of 16 consecutive down rows.
+template <int FMT>
+__device__ void down_units_mma(const DecParams &P, const Seg &g, const uint8_t *xs, const Misc &m) {
     const int warp = threadIdx.x / kWarp, lane = threadIdx.x % kWarp;
-    const int nu = g.uhi - g.ulo;
-    const int mine = nu > warp ? (nu - warp + kNW - 1) / kNW : 0;
+    const int gq = lane >> 2, c = lane & 3;
+    const int dlo = 4 * (g.ulo - g.ubase);
+    const int nr = min(4 * (g.uhi - g.ulo), P.H - dlo);
+    const int nb = (nr + 15) / 16;
+    const int mine = nb > warp ? (nb - warp + kNW - 1) / kNW : 0;
     const int64_t rb = row_bytes(FMT, g.inter);
-    const int ubase = g.ulo - g.ubase;
-    warp_stream<FMT, 4, NV>(
-        mine, (int)(rb / 16), xs, P.xs_stride, lane,
-        [&](int i, const uint8_t *(&rr)[4]) {
-            const int d = 4 * (ubase + warp + kNW * i);
-#pragma unroll
-            for (int q = 0; q < 4; q++) rr[q] = g.w0 + (size_t)min(d + q, P.H - 1) * rb;
+    const int tok = (gq & 3) < g.nv ? (gq & 3) : 0;
+    const uint8_t *xb = xs + (size_t)tok * P.xs_stride * 4 + (gq >> 2) * 64 + c * 16;
+    warp_stream_mma<FMT>(
+        mine, (int)(rb / 16), xb, lane,
+        [&](int i, const uint8_t *(&rr)[2]) {
+            const int r = dlo + 16 * (warp + kNW * i) + gq;
+            rr[0] = g.w0 + (size_t)min(r, P.H - 1) * rb;
+            rr[1] = g.w0 + (size_t)min(r + 8, P.H - 1) * rb;
         },
-        [&](int i, const float (&s)[4][NV]) {
-            const int ld = 4 * (warp + kNW * i);
-            const int d = 4 * ubase + ld;
+        [&](int i, float (&d)[4]) {
 #pragma unroll
-            for (int v = 0; v < NV; v++) {
-                if (lane == v && v < g.nv) {
-                    float *yrow = P.y + (size_t)act_row(P, g, v) * P.H;
+            for (int q = 0; q < 4; q++) d[q] += __shfl_xor_sync(kFull, d[q], 2);
+            const int ld = 16 * (warp + kNW * i) + gq;
+            if (c < 2) {
 #pragma unroll
-                    for (int q = 0; q < 4; q++)
-                        if (d + q < P.H) yrow[d + q] = s[q][v] * m.sc[0][ld + q];
+                for (int t = 0; t < 2; t++) {
+                    const int v = 2 * c + t;
+                    if (v < g.nv) {
+                        float *yrow = P.y + (size_t)act_row(P, g, v) * P.H + dlo;
+                        if (ld < nr) yrow[ld] = (d[t] * m.vinv[v]) * m.sc[0][ld];
+                        if (ld + 8 < nr) yrow[ld + 8] = (d[2 + t] * m.vinv[v]) * m.sc[0][ld + 8];
+                    }
                 }
             }
         });
 }
 
-template <int NVF>
-__device__ void run_units_flt(const DecParams &P, const Seg &g, bool down, const void *xs, const Misc &m) {
-    const float *xf = static_cast<const float *>(xs);
-    if (down) {
-        if (g.fmt == COLI_FMT_INT4) down_units_flt<COLI_FMT_INT4, NVF>(P, g, xf, m);
-        else if (g.fmt == COLI_FMT_INT8) down_units_flt<COLI_FMT_INT8, NVF>(P, g, xf, m);
-        else down_units_flt<COLI_FMT_INT2, NVF>(P, g, xf, m);
-    } else {
-        if (g.fmt == COLI_FMT_INT4) gateup_units_flt<COLI_FMT_INT4, NVF>(P, g, xf, m);
-        else if (g.fmt == COLI_FMT_INT8) gateup_units_flt<COLI_FMT_INT8, NVF>(P, g, xf, m);
-        else gateup_units_flt<COLI_FMT_INT2, NVF>(P, g, xf, m);
-    }
+template <int FMT>
+__device__ void run_units_mma_fmt(const DecParams &P, const Seg &g, bool down, const uint8_t *xs, const Misc &m) {
+    if (down) down_units_mma<FMT>(P, g, xs, m);
+    else gateup_units_mma<FMT>(P, g, xs, m);
 }
 
 template <int NV>
@@ -715,19 +752,10 @@ __device__ void run_units(const DecParams &P, const Seg &g, bool down, const voi
         return;
     }
     if constexpr (NV > 1) {
-        // the float core sized to the group's own token count (a partial last group of an
-        // expert computes no lanes for tokens it does not have)
-        if constexpr (NV > 2) {
-            if (g.nv == 2) {
-                run_units_flt<2>(P, g, down, xs, m);
-                return;
-            }
-            if (g.nv == 3) {
-                run_units_flt<3>(P, g, down, xs, m);
-                return;
-            }
-        }
-        run_units_flt<NV>(P, g, down, xs, m);
+        const uint8_t *xq = static_cast<const uint8_t *>(xs);
+        if (g.fmt == COLI_FMT_INT4) run_units_mma_fmt<COLI_FMT_INT4>(P, g, down, xq, m);
+        else if (g.fmt == COLI_FMT_INT8) run_units_mma_fmt<COLI_FMT_INT8>(P, g, down, xq, m);
+        else run_units_mma_fmt<COLI_FMT_INT2>(P, g, down, xq, m);
     }
 }
 
@@ -977,8 +1005,11 @@ bool decode_plan(const coli_moe_desc &d, DecParams &P, int grid) {
     const int T = d.T;
     P.NV = T == 1 ? 1 : (T <= 2 ? 2 : 4);
     const int maxdim = std::max(d.H, std::max(d.I, d.I_shared));
-    P.xs_stride = maxdim;
-    const size_t xs_vec = (size_t)P.NV * maxdim * sizeof(float);
+    // per-token stride of the tensor-core staging, in 4-byte words: 4 bytes (f16 hi + lo) per
+    // element over whole 64-byte weight segments, plus 64 bytes so that consecutive tokens
+    // start 64 bytes apart modulo 128 (distinct shared-memory banks for a quarter-warp)
+    P.xs_stride = (int)align_up((size_t)maxdim, 256) + 16;
+    const size_t xs_vec = (size_t)P.NV * P.xs_stride * sizeof(float);
     const size_t scratch = rscratch_bytes(T, d.E, d.K);
     P.xs_bytes = (int)align_up(std::max(xs_vec, scratch), 128);
     P.rt_bytes = (int)align_up(rtab_bytes(T, d.E, d.K), 128);

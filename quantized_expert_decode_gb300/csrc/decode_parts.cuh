@@ -6,6 +6,7 @@
 
 #include "idot.cuh"
 #include "kernels.h"
+#include "mma.cuh"
 #include "ptx.cuh"
 #include "qdot.cuh"
 
@@ -39,96 +40,11 @@ __device__ __forceinline__ int range_lo(int n, int c, int G) { return (int)((lon
 
 __device__ __forceinline__ bool bad16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) != 0; }
 
-// ------------------------------------------------------------------ the streaming core
-// One warp streams `nunits` units of NR packed rows each (CPR 16-byte chunks per row), lane l
-// taking chunks l, l+32, ... of every row, with kDepth chunk-steps of loads in flight across unit
-// boundaries (kInflight / NR steps). rows_of(i, rows) gives unit i's row pointers; epi(i, sums) gets the finished
-// warp-reduced dot products with the NV staged vectors.
-template <int FMT, int NR, int NV, class RowsOf, class Epi>
-__device__ __forceinline__ void warp_stream(int nunits, int CPR, const float *xs, int xstride, int lane,
-                                            RowsOf rows_of, Epi epi) {
-    using G = QGeom<FMT>;
-    constexpr int kDepth = kInflight / NR;  // chunk-steps in flight
-    if (nunits <= 0) return;
-    const int S = (CPR + kWarp - 1) / kWarp;  // steps per unit
-    const int total = nunits * S;
-    uint4 buf[kDepth][NR];
-    int iu = 0, ik = 0;  // issue cursor: unit, step within unit
-    auto issue = [&](uint4 (&b)[NR]) {
-        if (iu < nunits) {
-            const int c = lane + kWarp * ik;
-            const uint8_t *rr[NR];
-            rows_of(iu, rr);
-#pragma unroll
-            for (int r = 0; r < NR; r++) b[r] = c < CPR ? ld_stream_16(rr[r] + 16 * c) : make_uint4(0, 0, 0, 0);
-            if (++ik == S) {
-                ik = 0;
-                iu++;
-            }
-        }
-    };
-#pragma unroll
-    for (int j = 0; j < kDepth; j++) issue(buf[j]);
-    float2 acc[NR][NV];
-#pragma unroll
-    for (int r = 0; r < NR; r++)
-#pragma unroll
-        for (int v = 0; v < NV; v++) acc[r][v] = make_float2(0.f, 0.f);
-    const float4 *xs4 = reinterpret_cast<const float4 *>(xs);
-    const int xstride4 = xstride / 4;
-    int cu = 0, ck = 0;  // compute cursor
-    for (int s0 = 0; s0 < total; s0 += kDepth) {
-#pragma unroll
-        for (int j = 0; j < kDepth; j++) {
-            if (s0 + j < total) {
-                const int c = lane + kWarp * ck;
-                if (c < CPR) {
-#pragma unroll
-                    for (int wi = 0; wi < 4; wi++) {
-                        float4 xv[NV][G::F4W];
-#pragma unroll
-                        for (int v = 0; v < NV; v++)
-#pragma unroll
-                            for (int q = 0; q < G::F4W; q++)
-                                xv[v][q] = xs4[v * xstride4 + (wi * G::F4W + q) * CPR + c];
-#pragma unroll
-                        for (int r = 0; r < NR; r++) {
-                            const uint32_t w = word_of(buf[j][r], wi);
-                            const uint32_t wh = w >> 16;
-#pragma unroll
-                            for (int m = 0; m < G::HALF; m++) {
-                                const uint32_t lo = lop3_and_xor(w, G::mask(m), G::xorv(m));
-                                const uint32_t hi = lop3_and_xor(wh, G::mask(m), G::xorv(m));
-                                const float2 d = __fadd2_rn(make_float2(__uint_as_float(lo), __uint_as_float(hi)),
-                                                            make_float2(-G::magic(m), -G::magic(m)));
-#pragma unroll
-                                for (int v = 0; v < NV; v++) {
-                                    const float4 &x4 = xv[v][m >> 1];
-                                    const float2 x2 = (m & 1) ? make_float2(x4.z, x4.w) : make_float2(x4.x, x4.y);
-                                    acc[r][v] = __ffma2_rn(d, x2, acc[r][v]);
-                                }
-                            }
-                        }
-                    }
-                }
-                issue(buf[j]);
-                if (++ck == S) {
-                    float sums[NR][NV];
-                    warp_reduce_acc<NR, NV>(acc, sums);
-                    epi(cu, sums);
-#pragma unroll
-                    for (int r = 0; r < NR; r++)
-#pragma unroll
-                        for (int v = 0; v < NV; v++) acc[r][v] = make_float2(0.f, 0.f);
-                    ck = 0;
-                    cu++;
-                }
-            }
-        }
-    }
-}
-
-// The same walk for single-token groups on the integer core (idot.cuh), four rows per unit:
+// ------------------------------------------------------------------ the streaming cores
+// Single-token groups on the integer core (idot.cuh), four rows per unit. One warp streams
+// `nunits` units of NR packed rows (CPR 16-byte chunks per row), lane l taking chunks l, l+32,
+// ... of every row, with INFL / NR chunk-steps of loads in flight across unit boundaries;
+// rows_of(i, rows) gives unit i's row pointers;
 // xq_of(i) gives the staged activation limbs unit i is dotted with; epi(i, tot, d) gets, in
 // lane l, the exact warp total S of row l / 8 of unit i, and d = pre(i), the unit's epilogue
 // operands (row scales), which are loaded two units ahead.
@@ -181,6 +97,56 @@ __device__ __forceinline__ void warp_stream_int(int nunits, int CPR, int lane, R
                     ck = 0;
                     cu++;
                     if (cu < nunits) xq4 = xq_of(cu);
+                }
+            }
+        }
+    }
+}
+
+// The walk for multi-token groups on the tensor-core core (mma.cuh): blocks of 16 rows, lane
+// (g, c) streaming chunk 4*sigma + c of rows g and g + 8 (rows_of(i, rr) gives block i's two row
+// pointers for this lane), kInflight / 2 segments of loads in flight across block boundaries.
+// xb: this lane's staged B column (token and part) at its chunk column; epi(i, d) gets block i's
+// accumulators (columns 2c, 2c + 1 of rows g and g + 8).
+template <int FMT, class RowsOf, class Epi>
+__device__ __forceinline__ void warp_stream_mma(int nblk, int CPR, const uint8_t *xb, int lane, RowsOf rows_of,
+                                                Epi epi) {
+    using M = MQ<FMT>;
+    constexpr int kDepth = kInflight / 2;
+    if (nblk <= 0) return;
+    const int NSEG = (CPR + 3) / 4;
+    const int total = nblk * NSEG;
+    const int c = lane & 3;
+    uint4 buf[kDepth][2];
+    int iu = 0, is = 0;
+    const uint8_t *rr[2];
+    rows_of(0, rr);
+    auto issue = [&](uint4 (&b)[2]) {
+        if (iu < nblk) {
+            const int ch = 4 * is + c;
+            b[0] = ch < CPR ? ld_stream_16(rr[0] + 16 * ch) : make_uint4(0, 0, 0, 0);
+            b[1] = ch < CPR ? ld_stream_16(rr[1] + 16 * ch) : make_uint4(0, 0, 0, 0);
+            if (++is == NSEG) {
+                is = 0;
+                if (++iu < nblk) rows_of(iu, rr);
+            }
+        }
+    };
+#pragma unroll
+    for (int j = 0; j < kDepth; j++) issue(buf[j]);
+    float d[4] = {0.f, 0.f, 0.f, 0.f};
+    int cu = 0, cs = 0;
+    for (int s0 = 0; s0 < total; s0 += kDepth) {
+#pragma unroll
+        for (int j = 0; j < kDepth; j++) {
+            if (s0 + j < total) {
+                seg_mma<FMT>(buf[j], xb + (size_t)cs * M::SEGB, d);
+                issue(buf[j]);
+                if (++cs == NSEG) {
+                    epi(cu, d);
+                    d[0] = d[1] = d[2] = d[3] = 0.f;
+                    cs = 0;
+                    cu++;
                 }
             }
         }
@@ -272,36 +238,6 @@ __device__ __noinline__ void reduce_logits(const DecParams &P, int lo, int hi) {
 __device__ __forceinline__ float4 ld_act4(const float *src, int q, bool coherent) {
     return coherent ? __ldcg(reinterpret_cast<const float4 *>(src) + q)
                     : __ldg(reinterpret_cast<const float4 *>(src) + q);
-}
-
-// stage the activations of token group tg (x rows for gate/up, h rows for down) into xs. Each
-// thread issues all its float4 loads of a row before it stores any.
-template <int FMT>
-__device__ __forceinline__ void stage_row(const float *__restrict__ src, float *dst, int len, bool coherent) {
-    const int CPR = len / QGeom<FMT>::EPC;
-    const int n4 = len / 4;
-    constexpr int B = 4;
-    for (int q0 = threadIdx.x; q0 < n4; q0 += kNT * B) {
-        float4 v[B];
-#pragma unroll
-        for (int j = 0; j < B; j++) {
-            const int q = q0 + j * kNT;
-            if (q < n4) v[j] = ld_act4(src, q, coherent);
-        }
-#pragma unroll
-        for (int j = 0; j < B; j++) {
-            const int q = q0 + j * kNT;
-            if (q < n4) {
-                const float e4[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
-#pragma unroll
-                for (int u = 0; u < 4; u++) {
-                    float sc;
-                    const int at = staged_index<FMT>(4 * q + u, CPR, sc);
-                    dst[at] = e4[u] * sc;
-                }
-            }
-        }
-    }
 }
 
 // one 128-byte line to L2 (no alignment rule beyond the natural one)

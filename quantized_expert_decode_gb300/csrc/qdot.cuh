@@ -179,18 +179,4 @@ __device__ __forceinline__ void qdot_rows(const uint8_t *const (&rows)[NR], cons
         }
 }
 
-// Warp-wide sums of f32x2 partials: every lane gets out[r][v].
-template <int NR, int NV>
-__device__ __forceinline__ void warp_reduce_acc(const float2 (&acc)[NR][NV], float (&out)[NR][NV]) {
-#pragma unroll
-    for (int r = 0; r < NR; r++)
-#pragma unroll
-        for (int v = 0; v < NV; v++) {
-            float s = acc[r][v].x + acc[r][v].y;
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(kFull, s, o);
-            out[r][v] = s;
-        }
-}
-
 }  // namespace colimoe

@@ -899,7 +899,7 @@ __device__ void run_share(const DecParams &P, const RTab &rt, int b, int e, bool
     __syncthreads();
 }
 
-constexpr int kChunk = 64;  // units per chunk of a phase queue
+constexpr int kChunk = 128;  // units per chunk of a phase queue (two pieces of one group share a staging)
 
 // Dynamic shares: chunks of kChunk units, handed out in order by the phase's counter, so that a
 // CTA whose units are cheaper (single-token groups on the integer core) takes more of them.

@@ -105,14 +105,15 @@ __device__ __forceinline__ void warp_stream_int(int nunits, int CPR, int lane, R
 
 // The walk for multi-token groups on the tensor-core core (mma.cuh): blocks of 16 rows, lane
 // (g, c) streaming chunk 4*sigma + c of rows g and g + 8 (rows_of(i, rr) gives block i's two row
-// pointers for this lane), kInflight / 2 segments of loads in flight across block boundaries.
+// pointers for this lane), two segments of loads in flight across block boundaries (deeper
+// register buffers spill at the kernel's 128-register budget and measured slower).
 // xb: this lane's staged B column (token and part) at its chunk column; epi(i, d) gets block i's
 // accumulators (columns 2c, 2c + 1 of rows g and g + 8).
 template <int FMT, class RowsOf, class Epi>
 __device__ __forceinline__ void warp_stream_mma(int nblk, int CPR, const uint8_t *xb, int lane, RowsOf rows_of,
                                                 Epi epi) {
     using M = MQ<FMT>;
-    constexpr int kDepth = kInflight / 2;
+    constexpr int kDepth = 2;
     if (nblk <= 0) return;
     const int NSEG = (CPR + 3) / 4;
     const int total = nblk * NSEG;

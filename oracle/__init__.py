@@ -26,7 +26,7 @@ _SO = os.path.join(_OUT_DIR, "libcolimoe_oracle.so")
 _lock = threading.Lock()
 _lib = None
 
-FMT_F32, FMT_INT8, FMT_INT4, FMT_INT2 = 0, 1, 2, 3
+FMT_F32, FMT_INT8, FMT_INT4, FMT_INT2, FMT_INT4G = 0, 1, 2, 3, 4
 
 
 def build(force: bool = False) -> str:
@@ -57,16 +57,18 @@ def _load():
         lib.oracle_deq.restype = F
         lib.oracle_qgemv.argtypes = [I, P, P, P, I, I, P]
         lib.oracle_qgemv.restype = None
+        lib.oracle_qgemv_grouped.argtypes = [P, P, I, P, I, I, P]
+        lib.oracle_qgemv_grouped.restype = None
         lib.oracle_router.argtypes = [P, I, I, P, P, I, P, P]
         lib.oracle_router.restype = I
         lib.oracle_select.argtypes = [P, P, I, I, I, I, F, I, F, P, P, P]
         lib.oracle_select.restype = I
         lib.oracle_buckets.argtypes = [P, P, I, I, I, P, P, P]
         lib.oracle_buckets.restype = I
-        lib.oracle_expert.argtypes = [I, P, P, P, P, P, P, I, I, P, P]
+        lib.oracle_expert.argtypes = [I, I, P, P, P, P, P, P, I, I, P, P]
         lib.oracle_expert.restype = None
         lib.oracle_moe_forward.argtypes = ([I, I, I, I, I, I, F, I, F, I, P, P, P] + [P] * 6 +
-                                           [I, I] + [P] * 6 + [P, P, P, P])
+                                           [I, I, I] + [P] * 6 + [P, P, P, P])
         lib.oracle_moe_forward.restype = I
         _lib = lib
         return lib
@@ -97,6 +99,15 @@ def qgemv(fmt: int, W: np.ndarray, s, v: np.ndarray, O: int, In: int) -> np.ndar
     s = None if s is None else _f32(s)
     y = np.empty(O, np.float32)
     _load().oracle_qgemv(fmt, _p(W), _p(s), _p(v), O, In, _p(y))
+    return y
+
+
+def qgemv_grouped(W: np.ndarray, s, gs: int, v: np.ndarray, O: int, In: int) -> np.ndarray:
+    """int4-grouped GEMV: s is [O, ceil(In/gs)] fp32."""
+    W = np.ascontiguousarray(W)
+    v, s = _f32(v), _f32(s)
+    y = np.empty(O, np.float32)
+    _load().oracle_qgemv_grouped(_p(W), _p(s), int(gs), _p(v), O, In, _p(y))
     return y
 
 
@@ -138,11 +149,11 @@ def buckets(idx, E, keff=None):
     return counts, offsets, perm[:n].copy()
 
 
-def expert(fmt, ex, x, H, Iin):
+def expert(fmt, ex, x, H, Iin, group_size=0):
     """One SwiGLU expert on one vector; ex is a dict with gate_w/gate_s/up_w/up_s/down_w/down_s."""
     y = np.empty(H, np.float32)
     arrs = [np.ascontiguousarray(ex[k]) for k in ("gate_w", "gate_s", "up_w", "up_s", "down_w", "down_s")]
-    _load().oracle_expert(fmt, *[_p(a) for a in arrs], H, Iin, _p(_f32(x)), _p(y))
+    _load().oracle_expert(fmt, int(group_size), *[_p(a) for a in arrs], H, Iin, _p(_f32(x)), _p(y))
     return y
 
 
@@ -179,7 +190,7 @@ def moe_forward(blk, x=None, ksel=0, top_p=0.0):
     rc = lib.oracle_moe_forward(T, H, I, E, K, ksel, float(top_p), int(cfg["norm_topk"]),
                                 float(cfg["routed_scale"]), cfg["routed_fmt"], _p(x), _p(Wr), _p(bias),
                                 *[ctypes.cast(t, ctypes.c_void_p) for t in tabs],
-                                Is, cfg["shared_fmt"], *[_p(a) for a in sh_arrs],
+                                Is, cfg["shared_fmt"], int(cfg.get("group_size", 0)), *[_p(a) for a in sh_arrs],
                                 _p(out), _p(idx), _p(w), _p(keff))
     if rc != 0:
         raise ValueError("oracle_moe_forward failed (bad arguments or non-finite router score)")

@@ -15,7 +15,8 @@ int64_t oracle_row_bytes(int fmt, int64_t In) {
     switch (fmt) {
     case ORACLE_FMT_F32:  return In * 4;
     case ORACLE_FMT_INT8: return In;
-    case ORACLE_FMT_INT4: return (In + 1) / 2;
+    case ORACLE_FMT_INT4:
+    case ORACLE_FMT_INT4G: return (In + 1) / 2;
     case ORACLE_FMT_INT2: return (In + 3) / 4;
     default: return -1;
     }
@@ -34,7 +35,8 @@ float oracle_deq(int fmt, const uint8_t *row, int64_t i) {
     }
     case ORACLE_FMT_INT8:
         return (float)(int8_t)row[i];
-    case ORACLE_FMT_INT4: {
+    case ORACLE_FMT_INT4:
+    case ORACLE_FMT_INT4G: {
         uint8_t b = row[i / 2];
         int nib = (i % 2 == 0) ? (b & 0x0F) : (b >> 4);
         return (float)(nib - 8);
@@ -61,6 +63,34 @@ void oracle_qgemv(int fmt, const void *W, const float *s, const float *v, int O,
         float a = (float)acc;
         y[o] = s ? a * s[o] : a;
     }
+}
+
+/* The int4-grouped tensor ([glm.c, quick-start diff] qt_resolve_fmt, qt_from_disk,
+ * expert_load_impl: format 4 keeps the int4 weight bytes and O * ceil(In/gs) fp32 scales, one per
+ * group of gs consecutive inputs of a row). The scale changes inside the sum, so it multiplies
+ * each group's partial sum: y[o] = sum_g s[o*ng + g] * (sum_{i in group g} deq(W[o,i]) * v[i]),
+ * ng = ceil(In/gs), the last group holding the remainder; accumulated in double, rounded once. */
+void oracle_qgemv_grouped(const void *W, const float *s, int gs, const float *v, int O, int In, float *y) {
+    int64_t rb = oracle_row_bytes(ORACLE_FMT_INT4G, In);
+    int ng = (In + gs - 1) / gs;
+    for (int o = 0; o < O; o++) {
+        const uint8_t *row = (const uint8_t *)W + (int64_t)o * rb;
+        double acc = 0.0;
+        for (int g = 0; g < ng; g++) {
+            double part = 0.0;
+            int64_t i1 = (int64_t)(g + 1) * gs < In ? (int64_t)(g + 1) * gs : In;
+            for (int64_t i = (int64_t)g * gs; i < i1; i++)
+                part += (double)oracle_deq(ORACLE_FMT_INT4G, row, i) * (double)v[i];
+            acc += (double)s[(int64_t)o * ng + g] * part;
+        }
+        y[o] = (float)acc;
+    }
+}
+
+/* one quantized matrix-vector product in either scale layout */
+static void matvec(int fmt, int gs, const void *W, const float *s, const float *v, int O, int In, float *y) {
+    if (fmt == ORACLE_FMT_INT4G) oracle_qgemv_grouped(W, s, gs, v, O, In, y);
+    else oracle_qgemv(fmt, W, s, v, O, In, y);
 }
 
 /* [glm.c] sigmoidf and siluf */
@@ -182,15 +212,15 @@ int oracle_buckets(const int32_t *idx, const int32_t *keff, int T, int K, int E,
 
 /* Phases C/D of [glm.c] moe() for one row (also [metal] moe_gemv + moe_silu):
  * g = gate.x, u = up.x, h = silu(g) * u, y = down.h. */
-void oracle_expert(int fmt, const void *gate_w, const float *gate_s, const void *up_w,
+void oracle_expert(int fmt, int gs, const void *gate_w, const float *gate_s, const void *up_w,
                    const float *up_s, const void *down_w, const float *down_s,
                    int H, int Iin, const float *x, float *y) {
     float *g = (float *)malloc(sizeof(float) * (size_t)Iin);
     float *u = (float *)malloc(sizeof(float) * (size_t)Iin);
-    oracle_qgemv(fmt, gate_w, gate_s, x, Iin, H, g);
-    oracle_qgemv(fmt, up_w, up_s, x, Iin, H, u);
+    matvec(fmt, gs, gate_w, gate_s, x, Iin, H, g);
+    matvec(fmt, gs, up_w, up_s, x, Iin, H, u);
     for (int j = 0; j < Iin; j++) g[j] = silu_f(g[j]) * u[j];
-    oracle_qgemv(fmt, down_w, down_s, g, H, Iin, y);
+    matvec(fmt, gs, down_w, down_s, g, H, Iin, y);
     free(g);
     free(u);
 }
@@ -206,7 +236,7 @@ int oracle_moe_forward(int T, int H, int I, int E, int K, int ksel, float top_p,
                        const void *const *gate_w, const float *const *gate_s,
                        const void *const *up_w, const float *const *up_s,
                        const void *const *down_w, const float *const *down_s,
-                       int I_shared, int shared_fmt,
+                       int I_shared, int shared_fmt, int group_size,
                        const void *sh_gate_w, const float *sh_gate_s,
                        const void *sh_up_w, const float *sh_up_s,
                        const void *sh_down_w, const float *sh_down_s,
@@ -214,6 +244,8 @@ int oracle_moe_forward(int T, int H, int I, int E, int K, int ksel, float top_p,
     if (T < 0 || H < 1 || I < 1 || E < 1 || K < 1 || K > E || I_shared < 0) return -1;
     if (oracle_row_bytes(routed_fmt, 1) < 0) return -1;
     if (I_shared > 0 && oracle_row_bytes(shared_fmt, 1) < 0) return -1;
+    if ((routed_fmt == ORACLE_FMT_INT4G || (I_shared > 0 && shared_fmt == ORACLE_FMT_INT4G)) && group_size < 1)
+        return -1;
     float *sig = (float *)malloc(sizeof(float) * (size_t)E);
     float *ch = (float *)malloc(sizeof(float) * (size_t)E);
     int32_t *id = (int32_t *)malloc(sizeof(int32_t) * (size_t)K);
@@ -232,13 +264,13 @@ int oracle_moe_forward(int T, int H, int I, int E, int K, int ksel, float top_p,
         for (int d = 0; d < H; d++) ot[d] = 0.f;
         for (int k = 0; k < ke; k++) {
             int e = id[k];
-            oracle_expert(routed_fmt, gate_w[e], gate_s[e], up_w[e], up_s[e], down_w[e], down_s[e],
-                          H, I, xt, y);
+            oracle_expert(routed_fmt, group_size, gate_w[e], gate_s[e], up_w[e], up_s[e], down_w[e],
+                          down_s[e], H, I, xt, y);
             for (int d = 0; d < H; d++) ot[d] += ww[k] * y[d];
         }
         if (I_shared > 0) {
-            oracle_expert(shared_fmt, sh_gate_w, sh_gate_s, sh_up_w, sh_up_s, sh_down_w, sh_down_s,
-                          H, I_shared, xt, y);
+            oracle_expert(shared_fmt, group_size, sh_gate_w, sh_gate_s, sh_up_w, sh_up_s, sh_down_w,
+                          sh_down_s, H, I_shared, xt, y);
             for (int d = 0; d < H; d++) ot[d] += y[d];
         }
         if (idx_out) memcpy(idx_out + (int64_t)t * K, id, sizeof(int32_t) * (size_t)K);

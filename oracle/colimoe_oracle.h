@@ -11,9 +11,13 @@
  *   [glm.c']  colibri-strix, c/glm.c @97c756a — same file, later revision (matmul_i4_pair).
  *   [metal]   colibri, c/backend_metal.mm @93cde63 — shaders mm_gemv, moe_gemv, moe_silu,
  *             r_router, r_top8, r_top8_par; host moe_submit/moe_finish.
+ *   [glm.c, quick-start diff]  colibri, compare main...docs-quickstart — c/glm.c qt_resolve_fmt,
+ *             qt_from_disk, expert_load_impl: tensor format 4 (int4 with per-group scales).
  *
  * Precision: dot products accumulate in double and are rounded once to float, then multiplied
- * by the float row scale (the pages apply the scale after the sum). Every elementwise step
+ * by the float row scale (the pages apply the scale after the sum). For format 4 the scale
+ * changes inside the sum: each group's double partial sum is multiplied by its scale, the
+ * products are summed in double and the total is rounded once. Every elementwise step
  * (sigmoid, bias add, renormalisation, SiLU·mul, weighted combine) runs in float, in the order
  * the pages give, because the pages hold those values in float and the router's comparisons
  * decide integers (the selected expert ids) in that precision.
@@ -29,11 +33,14 @@
 extern "C" {
 #endif
 
-/* weight formats of the QT tensor ([glm.c] QT struct): 0 f32, 1 int8, 2 int4, 3 int2 */
+/* weight formats of the QT tensor ([glm.c] QT struct): 0 f32, 1 int8, 2 int4, 3 int2, and
+ * 4 int4-grouped ([glm.c, quick-start diff] qt_resolve_fmt: int4 bytes, one fp32 scale per group
+ * of gs inputs of a row) */
 #define ORACLE_FMT_F32  0
 #define ORACLE_FMT_INT8 1
 #define ORACLE_FMT_INT4 2
 #define ORACLE_FMT_INT2 3
+#define ORACLE_FMT_INT4G 4
 
 /* bytes of one packed row of In elements */
 int64_t oracle_row_bytes(int fmt, int64_t In);
@@ -44,6 +51,10 @@ float oracle_deq(int fmt, const uint8_t *row, int64_t i);
 /* y[o] = (float)(sum_i deq(W[o,i]) * v[i]) * s[o]   for o in [0,O); W is [O][row_bytes(In)]
  * (f32 weights: s may be NULL, meaning scale 1). */
 void oracle_qgemv(int fmt, const void *W, const float *s, const float *v, int O, int In, float *y);
+
+/* int4-grouped: y[o] = (float)(sum_g s[o*ng + g] * sum_{i in group g} deq(W[o,i]) * v[i]) with
+ * ng = ceil(In/gs); s is [O][ng]. */
+void oracle_qgemv_grouped(const void *W, const float *s, int gs, const float *v, int O, int In, float *y);
 
 /* Router scores for T tokens: sig[t,e] = sigmoid(x_t . Wr_e), choice[t,e] = sig + bias[e].
  * Returns 0, or -1 if any score or choice is not finite. */
@@ -64,8 +75,9 @@ int oracle_buckets(const int32_t *idx, const int32_t *keff, int T, int K, int E,
                    int32_t *counts, int32_t *offsets, int32_t *perm);
 
 /* One SwiGLU expert on one vector: g = gate.x, u = up.x, h = silu(g)*u, y = down.h.
- * gate/up are [Iin][row_bytes(H)], down is [H][row_bytes(Iin)]. */
-void oracle_expert(int fmt, const void *gate_w, const float *gate_s, const void *up_w,
+ * gate/up are [Iin][row_bytes(H)], down is [H][row_bytes(Iin)]; gs is the group size of
+ * format 4 (its scales are [Iin][ceil(H/gs)] and [H][ceil(Iin/gs)]), ignored otherwise. */
+void oracle_expert(int fmt, int gs, const void *gate_w, const float *gate_s, const void *up_w,
                    const float *up_s, const void *down_w, const float *down_s,
                    int H, int Iin, const float *x, float *y);
 
@@ -78,7 +90,7 @@ int oracle_moe_forward(int T, int H, int I, int E, int K, int ksel, float top_p,
                        const void *const *gate_w, const float *const *gate_s,
                        const void *const *up_w, const float *const *up_s,
                        const void *const *down_w, const float *const *down_s,
-                       int I_shared, int shared_fmt,
+                       int I_shared, int shared_fmt, int group_size,
                        const void *sh_gate_w, const float *sh_gate_s,
                        const void *sh_up_w, const float *sh_up_s,
                        const void *sh_down_w, const float *sh_down_s,

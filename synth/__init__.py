@@ -18,14 +18,16 @@ Distributions (one numpy PCG64 stream per seed):
   int4   weight bytes uniform in [0, 255] (both nibbles uniform in 0..15),
          row scale ~ U(0.5, 1.5) / (8 * sqrt(in))
   int2   weight bytes uniform in [0, 255], row scale ~ U(0.5, 1.5) / (2 * sqrt(in))
+  int4-grouped (format 4): int4 bytes, one scale ~ U(0.5, 1.5) / (8 * sqrt(in)) per group of
+         `group_size` inputs of a row, stored [rows][ceil(in / group_size)]
 where "in" is the number of input features of that matrix (H for gate/up, I for down).
 """
 from __future__ import annotations
 
 import numpy as np
 
-FMT_INT8, FMT_INT4, FMT_INT2 = 1, 2, 3
-_QMAX = {FMT_INT8: 127.0, FMT_INT4: 8.0, FMT_INT2: 2.0}
+FMT_INT8, FMT_INT4, FMT_INT2, FMT_INT4G = 1, 2, 3, 4
+_QMAX = {FMT_INT8: 127.0, FMT_INT4: 8.0, FMT_INT2: 2.0, FMT_INT4G: 8.0}
 ALIGN = 256
 
 # Zipf amplitude added to the router bias of the skewed continuous-batch workload. Chosen so
@@ -60,7 +62,7 @@ def config(cfg_id: int, **over) -> dict:
 def row_bytes(fmt: int, n: int) -> int:
     if fmt == FMT_INT8:
         return n
-    if fmt == FMT_INT4:
+    if fmt in (FMT_INT4, FMT_INT4G):
         return (n + 1) // 2
     if fmt == FMT_INT2:
         return (n + 3) // 4
@@ -71,17 +73,24 @@ def _up(n: int) -> int:
     return (n + ALIGN - 1) // ALIGN * ALIGN
 
 
-def slab_layout(fmt: int, H: int, I: int) -> dict:
+def groups(fmt: int, n: int, gs: int) -> int:
+    """Scales per row of a matrix with n inputs: ceil(n / gs) for int4-grouped, else 1."""
+    return (n + gs - 1) // gs if fmt == FMT_INT4G else 1
+
+
+def slab_layout(fmt: int, H: int, I: int, gs: int = 0) -> dict:
     """Byte offsets of the six sections of one expert slab, and the slab size."""
     rb_h, rb_i = row_bytes(fmt, H), row_bytes(fmt, I)
+    ng_h, ng_i = groups(fmt, H, gs), groups(fmt, I, gs)
     off = {}
     p = 0
     for key, nbytes in (("gate_w", I * rb_h), ("up_w", I * rb_h), ("down_w", H * rb_i),
-                        ("gate_s", 4 * I), ("up_s", 4 * I), ("down_s", 4 * H)):
+                        ("gate_s", 4 * I * ng_h), ("up_s", 4 * I * ng_h), ("down_s", 4 * H * ng_i)):
         off[key] = p
         p += _up(nbytes)
     off["bytes"] = p
     off["rb_h"], off["rb_i"] = rb_h, rb_i
+    off["ng_h"], off["ng_i"] = ng_h, ng_i
     return off
 
 
@@ -96,31 +105,32 @@ def _scales(rng, fmt: int, n: int, fan_in: int) -> np.ndarray:
     return (rng.uniform(0.5, 1.5, size=n) / (_QMAX[fmt] * np.sqrt(fan_in))).astype(np.float32)
 
 
-def expert_views(slab_row: np.ndarray, fmt: int, H: int, I: int) -> dict:
-    """Numpy views of the six sections of one expert slab (no copy)."""
-    L = slab_layout(fmt, H, I)
-    rb_h, rb_i = L["rb_h"], L["rb_i"]
+def expert_views(slab_row: np.ndarray, fmt: int, H: int, I: int, gs: int = 0) -> dict:
+    """Numpy views of the six sections of one expert slab (no copy). Scales are flat:
+    [rows * groups] (row-major [rows][groups] for int4-grouped)."""
+    L = slab_layout(fmt, H, I, gs)
+    rb_h, rb_i, ng_h, ng_i = L["rb_h"], L["rb_i"], L["ng_h"], L["ng_i"]
     return {
         "gate_w": slab_row[L["gate_w"]:L["gate_w"] + I * rb_h].reshape(I, rb_h),
         "up_w": slab_row[L["up_w"]:L["up_w"] + I * rb_h].reshape(I, rb_h),
         "down_w": slab_row[L["down_w"]:L["down_w"] + H * rb_i].reshape(H, rb_i),
-        "gate_s": slab_row[L["gate_s"]:L["gate_s"] + 4 * I].view(np.float32),
-        "up_s": slab_row[L["up_s"]:L["up_s"] + 4 * I].view(np.float32),
-        "down_s": slab_row[L["down_s"]:L["down_s"] + 4 * H].view(np.float32),
+        "gate_s": slab_row[L["gate_s"]:L["gate_s"] + 4 * I * ng_h].view(np.float32),
+        "up_s": slab_row[L["up_s"]:L["up_s"] + 4 * I * ng_h].view(np.float32),
+        "down_s": slab_row[L["down_s"]:L["down_s"] + 4 * H * ng_i].view(np.float32),
     }
 
 
-def make_slabs(rng, n: int, fmt: int, H: int, I: int) -> np.ndarray:
+def make_slabs(rng, n: int, fmt: int, H: int, I: int, gs: int = 0) -> np.ndarray:
     """n expert slabs [n, slab_bytes] of random packed weights and scales."""
-    L = slab_layout(fmt, H, I)
+    L = slab_layout(fmt, H, I, gs)
     slabs = np.zeros((n, L["bytes"]), np.uint8)
     for e in range(n):
-        v = expert_views(slabs[e], fmt, H, I)
+        v = expert_views(slabs[e], fmt, H, I, gs)
         for key in ("gate_w", "up_w", "down_w"):
             _fill_weights(rng, fmt, v[key])
-        v["gate_s"][:] = _scales(rng, fmt, I, H)
-        v["up_s"][:] = _scales(rng, fmt, I, H)
-        v["down_s"][:] = _scales(rng, fmt, H, I)
+        v["gate_s"][:] = _scales(rng, fmt, I * L["ng_h"], H)
+        v["up_s"][:] = _scales(rng, fmt, I * L["ng_h"], H)
+        v["down_s"][:] = _scales(rng, fmt, H * L["ng_i"], I)
     return slabs
 
 
@@ -159,12 +169,13 @@ def make_block(cfg, seed=None, T=None, row_filter=None, max_redraws=1000) -> dic
     rng = np.random.Generator(np.random.PCG64(0 if seed is None else seed))
     H, I, E = cfg["H"], cfg["I"], cfg["E"]
     Wr, bias = make_router(rng, cfg)
-    slabs = make_slabs(rng, E, cfg["routed_fmt"], H, I)
-    routed = [expert_views(slabs[e], cfg["routed_fmt"], H, I) for e in range(E)]
+    gs = int(cfg.get("group_size", 0))
+    slabs = make_slabs(rng, E, cfg["routed_fmt"], H, I, gs)
+    routed = [expert_views(slabs[e], cfg["routed_fmt"], H, I, gs) for e in range(E)]
     shared_slab, shared = None, None
     if cfg["I_shared"] > 0:
-        shared_slab = make_slabs(rng, 1, cfg["shared_fmt"], H, cfg["I_shared"])
-        shared = expert_views(shared_slab[0], cfg["shared_fmt"], H, cfg["I_shared"])
+        shared_slab = make_slabs(rng, 1, cfg["shared_fmt"], H, cfg["I_shared"], gs)
+        shared = expert_views(shared_slab[0], cfg["shared_fmt"], H, cfg["I_shared"], gs)
     x = draw_x(rng, cfg["T"], H)
     if row_filter is not None:
         for _ in range(max_redraws):

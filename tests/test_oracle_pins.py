@@ -17,7 +17,7 @@ import oracle
 import synth
 from conftest import golden_lines, gap_filter
 
-F8, F4, F2, F32 = oracle.FMT_INT8, oracle.FMT_INT4, oracle.FMT_INT2, oracle.FMT_F32
+F8, F4, F2, F32, F4G = oracle.FMT_INT8, oracle.FMT_INT4, oracle.FMT_INT2, oracle.FMT_F32, oracle.FMT_INT4G
 
 
 # ---------------------------------------------------------------- independent decoder (numpy)
@@ -73,6 +73,7 @@ def test_row_bytes():
     assert [oracle.row_bytes(F4, n) for n in (1, 2, 3, 6144)] == [1, 1, 2, 3072]
     assert [oracle.row_bytes(F2, n) for n in (1, 4, 5, 2048)] == [1, 1, 2, 512]
     assert oracle.row_bytes(F32, 5) == 20
+    assert [oracle.row_bytes(F4G, n) for n in (1, 2, 3, 6144)] == [1, 1, 2, 3072]
 
 
 # ---------------------------------------------------------------- quantised GEMV
@@ -114,6 +115,56 @@ def test_scale_one_int_path_equals_float_path(fmt):
     y_int = oracle.qgemv(fmt, W, np.ones(O, np.float32), v, O, n)
     y_f32 = oracle.qgemv(F32, Wf.view(np.uint8), None, v, O, n)
     assert np.array_equal(y_int, y_f32)
+
+
+# ---------------------------------------------------------------- int4-grouped GEMV (format 4)
+def np_group_scales(s, O, n, gs):
+    """[O, n] float64 matrix of the scale that applies to each weight: s[o, i // gs]."""
+    ng = (n + gs - 1) // gs
+    return np.repeat(np.asarray(s, np.float64).reshape(O, ng), gs, axis=1)[:, :n]
+
+
+@pytest.mark.parametrize("O,n,gs", [(4, 96, 32), (3, 100, 32), (5, 64, 128)])
+def test_grouped_unit_vectors_pick_the_group_scale(O, n, gs):
+    # e_i selects column i: y[o] = deq(W[o,i]) * s[o, i // gs] — the scale of row o's group of i
+    # (a transposed [ng][O] scale layout or a wrong group index fails here)
+    rng = np.random.default_rng(500 + n + gs)
+    W = rand_packed(rng, F4G, O, n)
+    ng = (n + gs - 1) // gs
+    s = rng.uniform(0.5, 2.0, O * ng).astype(np.float32)
+    D = np_deq(F4, W, n)
+    S = np_group_scales(s, O, n, gs)
+    for i in range(n):
+        e = np.zeros(n, np.float32)
+        e[i] = 1.0
+        y = oracle.qgemv_grouped(W, s, gs, e, O, n)
+        assert np.array_equal(y, (D[:, i] * S[:, i]).astype(np.float32)), i
+
+
+@pytest.mark.parametrize("O,n,gs", [(7, 300, 32), (5, 256, 64), (3, 96, 128), (4, 37, 1)])
+def test_grouped_matches_dense_brute_force(O, n, gs):
+    # the exact sum of deq * group scale * v (math.fsum over the dense float64 matrix), rounded
+    # once to float: the oracle's double accumulation may differ by at most one float ulp
+    rng = np.random.default_rng(600 + n + gs)
+    W = rand_packed(rng, F4G, O, n)
+    ng = (n + gs - 1) // gs
+    s = rng.uniform(1e-3, 1e-2, O * ng).astype(np.float32)
+    v = rng.standard_normal(n).astype(np.float32)
+    y = oracle.qgemv_grouped(W, s, gs, v, O, n)
+    dense = np_deq(F4, W, n) * np_group_scales(s, O, n, gs)
+    expect = np.array([math.fsum(dense[o] * v.astype(np.float64)) for o in range(O)]).astype(np.float32)
+    assert ulp_close(y, expect, 1)
+
+
+def test_grouped_single_group_equals_per_row_int4():
+    # gs >= In: one scale per row, i.e. the per-row int4 format (rounded once here, twice there)
+    rng = np.random.default_rng(701)
+    O, n = 11, 192
+    W = rand_packed(rng, F4, O, n)
+    s = rng.uniform(0.5, 2.0, O).astype(np.float32)
+    v = rng.standard_normal(n).astype(np.float32)
+    for gs in (n, 4 * n):
+        assert ulp_close(oracle.qgemv_grouped(W, s, gs, v, O, n), oracle.qgemv(F4, W, s, v, O, n), 1)
 
 
 @pytest.mark.parametrize("fmt,bits", [(F8, 8), (F4, 4), (F2, 2)])
@@ -358,6 +409,64 @@ def test_block_single_expert_is_dense_swiglu(fmt):
         ref = (_torch_ffn(fmt, blk["routed"][0], blk["x"][t], 96, 64) +
                _torch_ffn(fmt, blk["shared"], blk["x"][t], 96, 32))
         assert np.allclose(out[t], ref, rtol=0, atol=2e-5 * np.sqrt(np.mean(ref ** 2)))
+
+
+def _torch_ffn_grouped(ex, x, H, Iin, gs):
+    """Dense SwiGLU on int4-grouped weights (numpy decode, per-group scales), float64 torch."""
+    Wg = torch.tensor(np_deq(F4, ex["gate_w"], H) * np_group_scales(ex["gate_s"], Iin, H, gs))
+    Wu = torch.tensor(np_deq(F4, ex["up_w"], H) * np_group_scales(ex["up_s"], Iin, H, gs))
+    Wd = torch.tensor(np_deq(F4, ex["down_w"], Iin) * np_group_scales(ex["down_s"], H, Iin, gs))
+    xt = torch.tensor(x.astype(np.float64))
+    return (Wd @ (torch.nn.functional.silu(Wg @ xt) * (Wu @ xt))).numpy()
+
+
+@pytest.mark.parametrize("gs", [32, 64])
+def test_block_grouped_single_expert_is_dense_swiglu(gs):
+    """Format 4 through the whole block: E=1, K=1 (weight exactly 1), so routed + shared are two
+    dense SwiGLU FFNs whose weights carry one scale per group of gs inputs (H=96 and I=80 leave
+    ragged last groups)."""
+    cfg = dict(T=3, H=96, I=80, E=1, K=1, I_shared=48, norm_topk=1, routed_scale=1.0,
+               routed_fmt=F4G, shared_fmt=F4G, group_size=gs, zipf=False)
+    blk = synth.make_block(cfg, seed=41 + gs)
+    out, idx, w, _ = oracle.moe_forward(blk)
+    assert np.all(idx == 0) and np.all(w == 1.0)
+    for t in range(cfg["T"]):
+        ref = (_torch_ffn_grouped(blk["routed"][0], blk["x"][t], 96, 80, gs) +
+               _torch_ffn_grouped(blk["shared"], blk["x"][t], 96, 48, gs))
+        assert np.allclose(out[t], ref, rtol=0, atol=2e-5 * np.sqrt(np.mean(ref ** 2)))
+
+
+def test_block_grouped_with_equal_group_scales_is_per_row_int4():
+    # every group of a row given the row's first scale: the block equals the per-row int4 block
+    # on the same weights (same routing; outputs within float rounding)
+    gs, H, I, Is = 32, 128, 64, 32
+    cfg = dict(T=5, H=H, I=I, E=6, K=3, I_shared=Is, norm_topk=1, routed_scale=2.5,
+               routed_fmt=F4G, shared_fmt=F4G, group_size=gs, zipf=False)
+    blk = synth.make_block(cfg, seed=77)
+
+    def inputs_of(key, Iin):
+        return Iin if key == "down_s" else H
+
+    def equalise(ex, Iin):  # in place: each row's groups all take the row's first scale
+        for k in ("gate_s", "up_s", "down_s"):
+            rows = ex[k].reshape(-1, (inputs_of(k, Iin) + gs - 1) // gs)
+            rows[:] = rows[:, :1]
+
+    def per_row(ex, Iin):  # the same expert with one scale per row
+        out = dict(ex)
+        for k in ("gate_s", "up_s", "down_s"):
+            out[k] = np.ascontiguousarray(ex[k].reshape(-1, (inputs_of(k, Iin) + gs - 1) // gs)[:, 0])
+        return out
+
+    for ex in blk["routed"]:
+        equalise(ex, I)
+    equalise(blk["shared"], Is)
+    blk4 = dict(blk, cfg=dict(cfg, routed_fmt=F4, shared_fmt=F4, group_size=0),
+                routed=[per_row(ex, I) for ex in blk["routed"]], shared=per_row(blk["shared"], Is))
+    o1, i1, w1, _ = oracle.moe_forward(blk)
+    o2, i2, w2, _ = oracle.moe_forward(blk4)
+    assert np.array_equal(i1, i2) and np.array_equal(w1, w2)
+    assert np.allclose(o1, o2, rtol=0, atol=1e-6 * np.sqrt(np.mean(o2 ** 2)))
 
 
 def test_block_combine_weights_and_shared_weight_one():

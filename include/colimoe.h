@@ -19,6 +19,11 @@
  *   deq: COLI_FMT_INT8 — signed byte; COLI_FMT_INT4 — element i in byte i/2, low nibble for
  *   even i, value = nibble - 8; COLI_FMT_INT2 — element i in byte i/4 at bit 2*(i%4),
  *   value = field - 2 (the QT tensor formats of glm.c).
+ *   COLI_FMT_INT4G (int4-grouped, tensor format 4 of glm.c's qt_resolve_fmt on the colibri
+ *   "compare main...docs-quickstart" page): the int4 bytes with one fp32 scale per group of
+ *   gs = desc->group_size consecutive inputs of a row, scales [O][ceil(In/gs)] row-major, and
+ *     (W v)[o] = sum_g s[o][g] * (sum_{i in group g} deq(W[o,i]) * v[i])
+ *   (the last group of a row holds In - (ceil(In/gs) - 1) * gs inputs).
  *
  * Conventions for every entry point:
  *  - All tensors are row-major and live in DEVICE memory unless the argument says HOST.
@@ -34,7 +39,7 @@
  *    route / forward calls clear that word when they start, so it reports the latest call.
  *  - There is no CPU fallback: every step runs in this library's kernels.
  *  - Packed weight rows must start on 16-byte boundaries: H and I must be multiples of 16
- *    (int8), 32 (int4) or 64 (int2), and every weight and scale pointer 16-byte aligned;
+ *    (int8), 32 (int4, int4-grouped) or 64 (int2), and every weight and scale pointer 16-byte aligned;
  *    x and out must be 16-byte aligned. Violations return COLI_MOE_EALIGN / COLI_MOE_ENOTSUP.
  *  - Limits: 1 <= K <= min(E, 32), E <= 1024, T <= 65536, H, I <= 65536.
  */
@@ -54,6 +59,7 @@ typedef struct CUstream_st *coli_stream_t; /* the same type as cudaStream_t */
 #define COLI_FMT_INT8 1
 #define COLI_FMT_INT4 2
 #define COLI_FMT_INT2 3
+#define COLI_FMT_INT4G 4 /* int4 with per-group scales; group size in coli_moe_desc.group_size */
 
 /* return codes */
 #define COLI_MOE_OK 0
@@ -81,10 +87,15 @@ typedef struct {
     int32_t shared_fmt;   /* COLI_FMT_* of the shared expert (may differ from routed_fmt) */
     int32_t ksel;         /* TOPK override: keep min(ksel, K) experts; 0 = K */
     float top_p;          /* adaptive top-p in (0,1); 0 = off */
+    int32_t group_size;   /* inputs per scale of COLI_FMT_INT4G tensors (routed and shared alike):
+                             a positive multiple of 32; ignored when neither format is 4.
+                             Blocks with an int4-grouped expert run the general kernels (router
+                             launch, gate/up, down and combine launches) for every T. */
 } coli_moe_desc;
 
 /* One expert's six device pointers: gate/up are [I][row_bytes(H)] with fp32 scales [I];
- * down is [H][row_bytes(I)] with fp32 scales [H] (I = I_shared for the shared expert). */
+ * down is [H][row_bytes(I)] with fp32 scales [H] (I = I_shared for the shared expert).
+ * For COLI_FMT_INT4G the scales are [I][ceil(H/gs)] (gate, up) and [H][ceil(I/gs)] (down). */
 typedef struct {
     const void *gate_w;
     const void *up_w;
@@ -147,6 +158,13 @@ int coli_moe_forward_host(const coli_moe_desc *desc, const float *x_host, const 
  * x [T][In] fp32, y [T][O] fp32. Uses no workspace. */
 int coli_moe_qgemv(int32_t fmt, const void *W, const float *s, const float *x, float *y,
                    int32_t O, int32_t In, int32_t T, coli_stream_t stream);
+
+/* The same for an int4-grouped matrix (COLI_FMT_INT4G; coli_moe_qgemv refuses that format with
+ * COLI_MOE_ENOTSUP because it needs the group size): W is [O][In/2] int4 bytes, s is
+ * [O][ceil(In/group_size)] fp32, y[t][o] = sum_g s[o][g] * sum_{i in group g} deq(W[o,i]) * x[t][i].
+ * group_size: a positive multiple of 32 (else COLI_MOE_EINVAL). Uses no workspace. */
+int coli_moe_qgemv_grouped(const void *W, const float *s, int32_t group_size, const float *x, float *y,
+                           int32_t O, int32_t In, int32_t T, coli_stream_t stream);
 
 /* Synchronises `stream`, reads and clears the workspace error word. Returns COLI_MOE_OK,
  * COLI_MOE_EKERNEL if a kernel flagged an error since the last check, or COLI_MOE_ECUDA. */

@@ -13,7 +13,7 @@ import os
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "lib", "libcolimoe.so")
 
-COLI_FMT_INT8, COLI_FMT_INT4, COLI_FMT_INT2 = 1, 2, 3
+COLI_FMT_INT8, COLI_FMT_INT4, COLI_FMT_INT2, COLI_FMT_INT4G = 1, 2, 3, 4
 COLI_MOE_OK = 0
 COLI_MOE_EINVAL = -1
 COLI_MOE_ENOTSUP = -2
@@ -25,7 +25,8 @@ COLI_MOE_EKERNEL = -7
 
 # every symbol include/colimoe.h declares
 EXPORTS = ("coli_moe_workspace_bytes", "coli_moe_route", "coli_moe_forward", "coli_moe_forward_profiled",
-           "coli_moe_forward_host", "coli_moe_qgemv", "coli_moe_check", "coli_moe_strerror",
+           "coli_moe_forward_host", "coli_moe_qgemv", "coli_moe_qgemv_grouped", "coli_moe_check",
+           "coli_moe_strerror",
            "coli_moe_last_cuda_error", "coli_moe_forward_noalloc")
 
 COLI_MOE_NOALLOC_SCRATCH_BYTES = 32 << 20
@@ -36,7 +37,7 @@ class coli_moe_desc(ctypes.Structure):
                 ("E", ctypes.c_int32), ("K", ctypes.c_int32), ("I_shared", ctypes.c_int32),
                 ("norm_topk", ctypes.c_int32), ("routed_scale", ctypes.c_float),
                 ("routed_fmt", ctypes.c_int32), ("shared_fmt", ctypes.c_int32),
-                ("ksel", ctypes.c_int32), ("top_p", ctypes.c_float)]
+                ("ksel", ctypes.c_int32), ("top_p", ctypes.c_float), ("group_size", ctypes.c_int32)]
 
 
 class coli_moe_expert(ctypes.Structure):
@@ -72,6 +73,8 @@ def _load():
     lib.coli_moe_forward_host.restype = ctypes.c_int
     lib.coli_moe_qgemv.argtypes = [I32, P, P, P, P, I32, I32, I32, P]
     lib.coli_moe_qgemv.restype = ctypes.c_int
+    lib.coli_moe_qgemv_grouped.argtypes = [P, P, I32, P, P, I32, I32, I32, P]
+    lib.coli_moe_qgemv_grouped.restype = ctypes.c_int
     lib.coli_moe_check.argtypes = [P, P]
     lib.coli_moe_check.restype = ctypes.c_int
     lib.coli_moe_strerror.argtypes = [ctypes.c_int]
@@ -118,9 +121,9 @@ def _check(rc, where, raise_on_error):
 
 
 def make_desc(T, H, I, E, K, I_shared=0, norm_topk=1, routed_scale=1.0, routed_fmt=COLI_FMT_INT4,
-              shared_fmt=COLI_FMT_INT4, ksel=0, top_p=0.0):
+              shared_fmt=COLI_FMT_INT4, ksel=0, top_p=0.0, group_size=0):
     return coli_moe_desc(T, H, I, E, K, I_shared, norm_topk, routed_scale, routed_fmt, shared_fmt,
-                         ksel, top_p)
+                         ksel, top_p, group_size)
 
 
 def coli_moe_workspace_bytes(desc) -> int:
@@ -169,6 +172,11 @@ def coli_moe_forward_host(desc, x_host, W_r, bias, experts, shared, out_host, ws
 def coli_moe_qgemv(fmt, W, s, x, y, O, In, T, stream=None, raise_on_error=True):
     rc = _lib.coli_moe_qgemv(fmt, _ptr(W), _ptr(s), _ptr(x), _ptr(y), O, In, T, _stream(stream))
     return _check(rc, "coli_moe_qgemv", raise_on_error)
+
+
+def coli_moe_qgemv_grouped(W, s, group_size, x, y, O, In, T, stream=None, raise_on_error=True):
+    rc = _lib.coli_moe_qgemv_grouped(_ptr(W), _ptr(s), group_size, _ptr(x), _ptr(y), O, In, T, _stream(stream))
+    return _check(rc, "coli_moe_qgemv_grouped", raise_on_error)
 
 
 def coli_moe_check(ws, stream=None, raise_on_error=True):

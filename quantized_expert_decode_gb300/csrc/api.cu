@@ -42,10 +42,19 @@ int check_device() {
 }
 
 int check_fmt(int fmt) {
-    if (fmt == COLI_FMT_INT8 || fmt == COLI_FMT_INT4 || fmt == COLI_FMT_INT2) return COLI_MOE_OK;
+    if (fmt == COLI_FMT_INT8 || fmt == COLI_FMT_INT4 || fmt == COLI_FMT_INT2 || fmt == COLI_FMT_INT4G)
+        return COLI_MOE_OK;
     if (fmt == 0) return COLI_MOE_ENOTSUP;  // f32 experts: a glm.c format this library does not take
     return COLI_MOE_EINVAL;
 }
+
+// an expert of the block is int4-grouped (those run the general kernels)
+bool grouped(const coli_moe_desc &d) {
+    return d.routed_fmt == COLI_FMT_INT4G || (d.I_shared > 0 && d.shared_fmt == COLI_FMT_INT4G);
+}
+
+// group sizes the grouped kernels take: whole 16-byte chunks (32 int4 inputs) per group
+bool group_size_ok(int gs) { return gs >= 32 && gs <= kMaxDim && gs % 32 == 0; }
 
 int validate_desc(const coli_moe_desc *d) {
     if (!d) return COLI_MOE_EINVAL;
@@ -63,6 +72,7 @@ int validate_desc(const coli_moe_desc *d) {
         const int gs = elems_per_chunk(d->shared_fmt);
         if (d->H % gs || d->I_shared % gs) return COLI_MOE_ENOTSUP;
     }
+    if (grouped(*d) && !group_size_ok(d->group_size)) return COLI_MOE_EINVAL;
     return COLI_MOE_OK;
 }
 
@@ -207,6 +217,7 @@ int run_forward_decode(const coli_moe_desc *d, const float *x, const float *W_r,
 // the persistent decode kernel's plan and grid for this description (false: not applicable):
 // the single-token kernel for T = 1 when its shared memory fits, else the token-group kernel
 bool decode_plan_for(const coli_moe_desc &d, DecParams &P, int &grid) {
+    if (grouped(d)) return false;
     const int sms0 = num_sms();
     for (int per_sm = 2; per_sm >= 1 && d.T == 1; per_sm--) {
         DecParams Q{};
@@ -248,7 +259,7 @@ int run_forward(const coli_moe_desc *d, const float *x, const float *W_r, const 
     int rc = run_route(d, x, W_r, bias, idx, w, keff, nullptr, nullptr, nullptr, true, ws, st);
     if (rc) return rc;
     if ((rc = record(events, 1, st))) return rc;
-    if (d->T > kDecMaxT && prefill_supported(*d)) {
+    if (d->T > kDecMaxT && !grouped(*d) && prefill_supported(*d)) {
         PrefillWork pw{};
         pw.experts = experts;
         if (shared) pw.shared = *shared;
@@ -301,6 +312,7 @@ int run_forward(const coli_moe_desc *d, const float *x, const float *W_r, const 
     W.routed_fmt = d->routed_fmt;
     W.shared_fmt = d->shared_fmt;
     W.ldh = d->I > d->I_shared ? d->I : d->I_shared;
+    W.group_size = d->group_size;
     const long max_active = std::min<long>((long)d->E, (long)d->T * ksel_of(d));
     W.slots = (int)max_active + (d->I_shared > 0 ? 1 : 0);
     cudaError_t e;
@@ -405,13 +417,28 @@ int coli_moe_qgemv(int32_t fmt, const void *W, const float *s, const float *x, f
                    int32_t In, int32_t T, coli_stream_t stream) {
     int rc = check_fmt(fmt);
     if (rc) return rc;
+    if (fmt == COLI_FMT_INT4G) return COLI_MOE_ENOTSUP;  // needs the group size: coli_moe_qgemv_grouped
     if (!W || !s || !x || !y || O < 1 || In < 1 || T < 1 || O > (1 << 24) || In > kMaxDim ||
         T > (1 << 24))
         return COLI_MOE_EINVAL;
     if (In % elems_per_chunk(fmt)) return COLI_MOE_ENOTSUP;
     if (!aligned(W, 16) || !aligned(s, 4) || !aligned(x, 4) || !aligned(y, 4)) return COLI_MOE_EALIGN;
     if ((rc = check_device())) return rc;
-    cudaError_t e = launch_qgemv(fmt, W, s, x, y, O, In, T, reinterpret_cast<cudaStream_t>(stream));
+    cudaError_t e = launch_qgemv(fmt, W, s, 0, x, y, O, In, T, reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? COLI_MOE_OK : cuda_fail(e);
+}
+
+int coli_moe_qgemv_grouped(const void *W, const float *s, int32_t group_size, const float *x, float *y,
+                           int32_t O, int32_t In, int32_t T, coli_stream_t stream) {
+    if (!W || !s || !x || !y || O < 1 || In < 1 || T < 1 || O > (1 << 24) || In > kMaxDim ||
+        T > (1 << 24) || !group_size_ok(group_size))
+        return COLI_MOE_EINVAL;
+    if (In % elems_per_chunk(COLI_FMT_INT4G)) return COLI_MOE_ENOTSUP;
+    if (!aligned(W, 16) || !aligned(s, 4) || !aligned(x, 4) || !aligned(y, 4)) return COLI_MOE_EALIGN;
+    int rc = check_device();
+    if (rc) return rc;
+    cudaError_t e = launch_qgemv(COLI_FMT_INT4G, W, s, group_size, x, y, O, In, T,
+                                 reinterpret_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? COLI_MOE_OK : cuda_fail(e);
 }
 

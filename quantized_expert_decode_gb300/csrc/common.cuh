@@ -28,12 +28,12 @@ __host__ __device__ inline size_t align_up(size_t n, size_t a) { return (n + a -
 
 // Bytes of one packed row of n elements.
 __host__ __device__ inline int64_t row_bytes(int fmt, int64_t n) {
-    return fmt == COLI_FMT_INT8 ? n : fmt == COLI_FMT_INT4 ? (n + 1) / 2 : (n + 3) / 4;
+    return fmt == COLI_FMT_INT8 ? n : (fmt == COLI_FMT_INT4 || fmt == COLI_FMT_INT4G) ? (n + 1) / 2 : (n + 3) / 4;
 }
 
 // Elements per 16-byte chunk and the element-count granule the kernels need per format.
 __host__ __device__ inline int elems_per_chunk(int fmt) {
-    return fmt == COLI_FMT_INT8 ? 16 : fmt == COLI_FMT_INT4 ? 32 : 64;
+    return fmt == COLI_FMT_INT8 ? 16 : (fmt == COLI_FMT_INT4 || fmt == COLI_FMT_INT4G) ? 32 : 64;
 }
 
 // Device workspace layout. Every region starts on a 256-byte boundary.

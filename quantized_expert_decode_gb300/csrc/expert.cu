@@ -68,7 +68,8 @@ __device__ __forceinline__ int slot_token(const ExpertWork &W, const Slot &s, in
     return s.shared ? v : W.perm[s.pbase + v] / W.K;
 }
 
-template <int FMT, int NV>
+// GRP: COLI_FMT_INT4G weights (FMT is then the int4 layout): per-group scales inside the sum
+template <int FMT, int NV, bool GRP>
 __device__ __forceinline__ void gateup_pass(const ExpertWork &W, const Slot &s, int j0, int v0, int nv,
                                             const float *xs, int CPR) {
     const int warp = threadIdx.x / kWarp, lane = threadIdx.x % kWarp;
@@ -83,7 +84,19 @@ __device__ __forceinline__ void gateup_pass(const ExpertWork &W, const Slot &s, 
         rows[2 * p + 1] = static_cast<const uint8_t *>(s.ex.up_w) + jc * rb;
     }
     float out[4][NV];
-    qdot_rows<FMT, 4, NV>(rows, xs, W.H, CPR, lane, out);
+    if constexpr (GRP) {
+        const int ng = (W.H + W.group_size - 1) / W.group_size;
+        const float *srows[4];
+#pragma unroll
+        for (int p = 0; p < 2; p++) {
+            const int jc = min(jp[p], s.inter - 1);
+            srows[2 * p] = s.ex.gate_s + (size_t)jc * ng;
+            srows[2 * p + 1] = s.ex.up_s + (size_t)jc * ng;
+        }
+        qdot_rows_grouped<4, NV>(rows, srows, W.group_size / 32, xs, W.H, CPR, lane, out);
+    } else {
+        qdot_rows<FMT, 4, NV>(rows, xs, W.H, CPR, lane, out);
+    }
 #pragma unroll
     for (int v = 0; v < NV; v++) {
         if (lane != v || v >= nv) continue;
@@ -91,14 +104,14 @@ __device__ __forceinline__ void gateup_pass(const ExpertWork &W, const Slot &s, 
 #pragma unroll
         for (int p = 0; p < 2; p++) {
             if (jp[p] >= s.inter) continue;
-            const float g = out[2 * p][v] * s.ex.gate_s[jp[p]];
-            const float u = out[2 * p + 1][v] * s.ex.up_s[jp[p]];
+            const float g = GRP ? out[2 * p][v] : out[2 * p][v] * s.ex.gate_s[jp[p]];
+            const float u = GRP ? out[2 * p + 1][v] : out[2 * p + 1][v] * s.ex.up_s[jp[p]];
             W.h[(size_t)hr * W.ldh + jp[p]] = silu_mul(g, u);
         }
     }
 }
 
-template <int FMT>
+template <int FMT, bool GRP = false>
 __device__ void gateup_slot(const ExpertWork &W, const Slot &s, float *xs) {
     using G = QGeom<FMT>;
     const int j0 = blockIdx.x * kGuRowsPerCta;
@@ -113,9 +126,9 @@ __device__ void gateup_slot(const ExpertWork &W, const Slot &s, float *xs) {
         if (nv == 3)
             for (int i = threadIdx.x; i < W.H; i += kThreads) xs[3 * W.H + i] = 0.f;
         __syncthreads();
-        if (nv == 1) gateup_pass<FMT, 1>(W, s, j0, v0, nv, xs, CPR);
-        else if (nv == 2) gateup_pass<FMT, 2>(W, s, j0, v0, nv, xs, CPR);
-        else gateup_pass<FMT, 4>(W, s, j0, v0, nv, xs, CPR);
+        if (nv == 1) gateup_pass<FMT, 1, GRP>(W, s, j0, v0, nv, xs, CPR);
+        else if (nv == 2) gateup_pass<FMT, 2, GRP>(W, s, j0, v0, nv, xs, CPR);
+        else gateup_pass<FMT, 4, GRP>(W, s, j0, v0, nv, xs, CPR);
     }
 }
 
@@ -125,11 +138,12 @@ __global__ void __launch_bounds__(kThreads) gateup_kernel(ExpertWork W) {
     Slot s;
     if (!resolve_slot(W, blockIdx.y, s)) return;
     if (s.fmt == COLI_FMT_INT4) gateup_slot<COLI_FMT_INT4>(W, s, xs);
+    else if (s.fmt == COLI_FMT_INT4G) gateup_slot<COLI_FMT_INT4, true>(W, s, xs);
     else if (s.fmt == COLI_FMT_INT8) gateup_slot<COLI_FMT_INT8>(W, s, xs);
     else gateup_slot<COLI_FMT_INT2>(W, s, xs);
 }
 
-template <int FMT, int NV>
+template <int FMT, int NV, bool GRP>
 __device__ __forceinline__ void down_pass(const ExpertWork &W, const Slot &s, int d0, int v0, int nv,
                                           const float *xs, int CPR) {
     const int warp = threadIdx.x / kWarp, lane = threadIdx.x % kWarp;
@@ -142,18 +156,26 @@ __device__ __forceinline__ void down_pass(const ExpertWork &W, const Slot &s, in
         rows[r] = static_cast<const uint8_t *>(s.ex.down_w) + min(d[r], W.H - 1) * rb;
     }
     float out[4][NV];
-    qdot_rows<FMT, 4, NV>(rows, xs, s.inter, CPR, lane, out);
+    if constexpr (GRP) {
+        const int ng = (s.inter + W.group_size - 1) / W.group_size;
+        const float *srows[4];
+#pragma unroll
+        for (int r = 0; r < 4; r++) srows[r] = s.ex.down_s + (size_t)min(d[r], W.H - 1) * ng;
+        qdot_rows_grouped<4, NV>(rows, srows, W.group_size / 32, xs, s.inter, CPR, lane, out);
+    } else {
+        qdot_rows<FMT, 4, NV>(rows, xs, s.inter, CPR, lane, out);
+    }
 #pragma unroll
     for (int v = 0; v < NV; v++) {
         if (lane != v || v >= nv) continue;
         const int yr = slot_row(W, s, v0 + v);
 #pragma unroll
         for (int r = 0; r < 4; r++)
-            if (d[r] < W.H) W.y[(size_t)yr * W.H + d[r]] = out[r][v] * s.ex.down_s[d[r]];
+            if (d[r] < W.H) W.y[(size_t)yr * W.H + d[r]] = GRP ? out[r][v] : out[r][v] * s.ex.down_s[d[r]];
     }
 }
 
-template <int FMT>
+template <int FMT, bool GRP = false>
 __device__ void down_slot(const ExpertWork &W, const Slot &s, float *xs) {
     using G = QGeom<FMT>;
     const int d0 = blockIdx.x * kDnRowsPerCta;
@@ -168,9 +190,9 @@ __device__ void down_slot(const ExpertWork &W, const Slot &s, float *xs) {
         if (nv == 3)
             for (int i = threadIdx.x; i < s.inter; i += kThreads) xs[3 * s.inter + i] = 0.f;
         __syncthreads();
-        if (nv == 1) down_pass<FMT, 1>(W, s, d0, v0, nv, xs, CPR);
-        else if (nv == 2) down_pass<FMT, 2>(W, s, d0, v0, nv, xs, CPR);
-        else down_pass<FMT, 4>(W, s, d0, v0, nv, xs, CPR);
+        if (nv == 1) down_pass<FMT, 1, GRP>(W, s, d0, v0, nv, xs, CPR);
+        else if (nv == 2) down_pass<FMT, 2, GRP>(W, s, d0, v0, nv, xs, CPR);
+        else down_pass<FMT, 4, GRP>(W, s, d0, v0, nv, xs, CPR);
     }
 }
 
@@ -180,6 +202,7 @@ __global__ void __launch_bounds__(kThreads) down_kernel(ExpertWork W) {
     Slot s;
     if (!resolve_slot(W, blockIdx.y, s)) return;
     if (s.fmt == COLI_FMT_INT4) down_slot<COLI_FMT_INT4>(W, s, xs);
+    else if (s.fmt == COLI_FMT_INT4G) down_slot<COLI_FMT_INT4, true>(W, s, xs);
     else if (s.fmt == COLI_FMT_INT8) down_slot<COLI_FMT_INT8>(W, s, xs);
     else down_slot<COLI_FMT_INT2>(W, s, xs);
 }
@@ -248,8 +271,9 @@ cudaError_t launch_combine(const float *y, const float *wts, const int32_t *keff
 }
 
 // ---------------------------------------------------------------- standalone quantized GEMV
-template <int FMT, int NV>
-__device__ __forceinline__ void qgemv_pass(const uint8_t *W, const float *sc, float *y, int O, int In,
+// gs > 0: COLI_FMT_INT4G (FMT is the int4 layout), sc is [O][ceil(In/gs)]
+template <int FMT, int NV, bool GRP>
+__device__ __forceinline__ void qgemv_pass(const uint8_t *W, const float *sc, int gs, float *y, int O, int In,
                                            int o0, int t0, int nv, const float *xs, int CPR) {
     const int warp = threadIdx.x / kWarp, lane = threadIdx.x % kWarp;
     const int64_t rb = row_bytes(FMT, In);
@@ -261,19 +285,27 @@ __device__ __forceinline__ void qgemv_pass(const uint8_t *W, const float *sc, fl
         rows[r] = W + min(o[r], O - 1) * rb;
     }
     float out[4][NV];
-    qdot_rows<FMT, 4, NV>(rows, xs, In, CPR, lane, out);
+    if constexpr (GRP) {
+        const int ng = (In + gs - 1) / gs;
+        const float *srows[4];
+#pragma unroll
+        for (int r = 0; r < 4; r++) srows[r] = sc + (size_t)min(o[r], O - 1) * ng;
+        qdot_rows_grouped<4, NV>(rows, srows, gs / 32, xs, In, CPR, lane, out);
+    } else {
+        qdot_rows<FMT, 4, NV>(rows, xs, In, CPR, lane, out);
+    }
 #pragma unroll
     for (int v = 0; v < NV; v++) {
         if (lane != v || v >= nv) continue;
 #pragma unroll
         for (int r = 0; r < 4; r++)
-            if (o[r] < O) y[(size_t)(t0 + v) * O + o[r]] = out[r][v] * sc[o[r]];
+            if (o[r] < O) y[(size_t)(t0 + v) * O + o[r]] = GRP ? out[r][v] : out[r][v] * sc[o[r]];
     }
 }
 
-template <int FMT>
+template <int FMT, bool GRP>
 __global__ void __launch_bounds__(kThreads)
-qgemv_kernel(const uint8_t *__restrict__ W, const float *__restrict__ sc, const float *__restrict__ x,
+qgemv_kernel(const uint8_t *__restrict__ W, const float *__restrict__ sc, int gs, const float *__restrict__ x,
              float *__restrict__ y, int O, int In, int T) {
     extern __shared__ __align__(16) float xs[];
     using G = QGeom<FMT>;
@@ -285,12 +317,12 @@ qgemv_kernel(const uint8_t *__restrict__ W, const float *__restrict__ sc, const 
     if (nv == 3)
         for (int i = threadIdx.x; i < In; i += kThreads) xs[3 * In + i] = 0.f;
     __syncthreads();
-    if (nv == 1) qgemv_pass<FMT, 1>(W, sc, y, O, In, o0, t0, nv, xs, CPR);
-    else if (nv == 2) qgemv_pass<FMT, 2>(W, sc, y, O, In, o0, t0, nv, xs, CPR);
-    else qgemv_pass<FMT, 4>(W, sc, y, O, In, o0, t0, nv, xs, CPR);
+    if (nv == 1) qgemv_pass<FMT, 1, GRP>(W, sc, gs, y, O, In, o0, t0, nv, xs, CPR);
+    else if (nv == 2) qgemv_pass<FMT, 2, GRP>(W, sc, gs, y, O, In, o0, t0, nv, xs, CPR);
+    else qgemv_pass<FMT, 4, GRP>(W, sc, gs, y, O, In, o0, t0, nv, xs, CPR);
 }
 
-cudaError_t launch_qgemv(int fmt, const void *W, const float *sc, const float *x, float *y, int O,
+cudaError_t launch_qgemv(int fmt, const void *W, const float *sc, int gs, const float *x, float *y, int O,
                          int In, int T, cudaStream_t st) {
     const int nv = T < kNV ? T : kNV;
     const size_t smem = (size_t)(nv == 3 ? 4 : nv) * In * sizeof(float);
@@ -298,12 +330,13 @@ cudaError_t launch_qgemv(int fmt, const void *W, const float *sc, const float *x
     auto go = [&](auto kern) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
-        kern<<<grid, kThreads, smem, st>>>(static_cast<const uint8_t *>(W), sc, x, y, O, In, T);
+        kern<<<grid, kThreads, smem, st>>>(static_cast<const uint8_t *>(W), sc, gs, x, y, O, In, T);
         return cudaGetLastError();
     };
-    if (fmt == COLI_FMT_INT8) return go(qgemv_kernel<COLI_FMT_INT8>);
-    if (fmt == COLI_FMT_INT4) return go(qgemv_kernel<COLI_FMT_INT4>);
-    return go(qgemv_kernel<COLI_FMT_INT2>);
+    if (fmt == COLI_FMT_INT8) return go(qgemv_kernel<COLI_FMT_INT8, false>);
+    if (fmt == COLI_FMT_INT4) return go(qgemv_kernel<COLI_FMT_INT4, false>);
+    if (fmt == COLI_FMT_INT4G) return go(qgemv_kernel<COLI_FMT_INT4, true>);
+    return go(qgemv_kernel<COLI_FMT_INT2, false>);
 }
 
 }  // namespace colimoe

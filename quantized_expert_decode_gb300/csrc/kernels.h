@@ -21,6 +21,7 @@ struct ExpertWork {
     int T, H, I, E, K, I_shared, routed_fmt, shared_fmt;
     int ldh;                         // row stride of h in floats (max(I, I_shared))
     int slots;                       // grid.y: max active routed experts + (shared ? 1 : 0)
+    int group_size;                  // inputs per scale of COLI_FMT_INT4G experts
 };
 
 // ---------------------------------------------------------------- decode.cu
@@ -103,7 +104,8 @@ cudaError_t launch_down(const ExpertWork &w, cudaStream_t s);
 cudaError_t launch_combine(const float *y, const float *wts, const int32_t *keff,
                            const int32_t *pos, int T, int H, int K, int has_shared, float *out,
                            cudaStream_t s);
-cudaError_t launch_qgemv(int fmt, const void *W, const float *sc, const float *x, float *y, int O,
-                         int In, int T, cudaStream_t s);
+// gs: inputs per scale when fmt is COLI_FMT_INT4G (sc is then [O][ceil(In/gs)]), else unused
+cudaError_t launch_qgemv(int fmt, const void *W, const float *sc, int gs, const float *x, float *y, int O,
+                         int In, int T, cudaStream_t st);
 
 }  // namespace colimoe

@@ -179,4 +179,75 @@ __device__ __forceinline__ void qdot_rows(const uint8_t *const (&rows)[NR], cons
         }
 }
 
+// The int4-grouped form (COLI_FMT_INT4G: int4 bytes, one scale per group of gs inputs): each
+// 16-byte chunk (32 inputs) lies in one group when gs is a multiple of 32, so a lane forms the
+// chunk's partial sums, multiplies them by the group scale srows[r][c / cpg] (cpg = gs / 32
+// chunks per group) and adds them to its accumulators. The staged layout is the int4 one.
+template <int NR, int NV>
+__device__ __forceinline__ void qdot_rows_grouped(const uint8_t *const (&rows)[NR], const float *const (&srows)[NR],
+                                                  int cpg, const float *xs, int xstride, int CPR, int lane,
+                                                  float (&out)[NR][NV]) {
+    using G = QGeom<COLI_FMT_INT4>;
+    float2 acc[NR][NV];
+#pragma unroll
+    for (int r = 0; r < NR; r++)
+#pragma unroll
+        for (int v = 0; v < NV; v++) acc[r][v] = make_float2(0.f, 0.f);
+    const float4 *xs4 = reinterpret_cast<const float4 *>(xs);
+    const int xstride4 = xstride / 4;
+    for (int c = lane; c < CPR; c += kWarp) {
+        uint4 cur[NR];
+        float sg[NR];
+#pragma unroll
+        for (int r = 0; r < NR; r++) {
+            cur[r] = ld_stream_16(rows[r] + 16 * c);
+            sg[r] = __ldg(srows[r] + c / cpg);
+        }
+        float2 part[NR][NV];
+#pragma unroll
+        for (int r = 0; r < NR; r++)
+#pragma unroll
+            for (int v = 0; v < NV; v++) part[r][v] = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int wi = 0; wi < 4; wi++) {
+            float4 xv[NV][G::F4W];
+#pragma unroll
+            for (int v = 0; v < NV; v++)
+#pragma unroll
+                for (int j = 0; j < G::F4W; j++) xv[v][j] = xs4[v * xstride4 + (wi * G::F4W + j) * CPR + c];
+#pragma unroll
+            for (int r = 0; r < NR; r++) {
+                const uint32_t q = word_of(cur[r], wi);
+                const uint32_t qh = q >> 16;
+#pragma unroll
+                for (int m = 0; m < G::HALF; m++) {
+                    const uint32_t lo = lop3_and_xor(q, G::mask(m), G::xorv(m));
+                    const uint32_t hi = lop3_and_xor(qh, G::mask(m), G::xorv(m));
+                    const float2 d = __fadd2_rn(make_float2(__uint_as_float(lo), __uint_as_float(hi)),
+                                                make_float2(-G::magic(m), -G::magic(m)));
+#pragma unroll
+                    for (int v = 0; v < NV; v++) {
+                        const float4 &x4 = xv[v][m >> 1];
+                        const float2 x2 = (m & 1) ? make_float2(x4.z, x4.w) : make_float2(x4.x, x4.y);
+                        part[r][v] = __ffma2_rn(d, x2, part[r][v]);
+                    }
+                }
+            }
+        }
+#pragma unroll
+        for (int r = 0; r < NR; r++)
+#pragma unroll
+            for (int v = 0; v < NV; v++) acc[r][v] = __ffma2_rn(part[r][v], make_float2(sg[r], sg[r]), acc[r][v]);
+    }
+#pragma unroll
+    for (int r = 0; r < NR; r++)
+#pragma unroll
+        for (int v = 0; v < NV; v++) {
+            float s = acc[r][v].x + acc[r][v].y;
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(kFull, s, o);
+            out[r][v] = s;
+        }
+}
+
 }  // namespace colimoe

@@ -112,3 +112,33 @@ def test_qgemv_rejects_bad_arguments(q):
     assert g(O=0) == q.COLI_MOE_EINVAL
     assert g(In=48) == q.COLI_MOE_ENOTSUP
     assert g(W=FAKE + 8) == q.COLI_MOE_EALIGN
+
+
+def test_grouped_format_validation(q):
+    # int4-grouped blocks need a group size that is a positive multiple of 32 (whole chunks)
+    G = q.COLI_FMT_INT4G
+    assert q.coli_moe_workspace_bytes(good_desc(q, routed_fmt=G, group_size=32)) > 0
+    assert q.coli_moe_workspace_bytes(good_desc(q, routed_fmt=G, shared_fmt=G, group_size=128)) > 0
+    for gs in (0, -32, 16, 48, 1 << 20):
+        assert q.coli_moe_workspace_bytes(good_desc(q, routed_fmt=G, group_size=gs)) == 0, gs
+        assert q.coli_moe_workspace_bytes(good_desc(q, shared_fmt=G, group_size=gs)) == 0, gs
+    # without a grouped expert the field is ignored; a grouped shared slot without a shared
+    # expert is not a grouped block
+    assert q.coli_moe_workspace_bytes(good_desc(q, group_size=7)) > 0
+    assert q.coli_moe_workspace_bytes(good_desc(q, I_shared=0, shared_fmt=G, group_size=0)) > 0
+    assert call_forward(q, good_desc(q, routed_fmt=G, group_size=48)) == q.COLI_MOE_EINVAL
+    assert call_forward(q, good_desc(q, routed_fmt=G, group_size=64, H=272)) == q.COLI_MOE_ENOTSUP
+
+
+def test_qgemv_grouped_rejects_bad_arguments(q):
+    g = lambda W=FAKE, gs=64, O=8, In=64, T=1: q.coli_moe_qgemv_grouped(W, FAKE, gs, FAKE, FAKE, O, In, T,
+                                                                         raise_on_error=False)
+    # the plain entry point needs the group size for format 4
+    assert q.coli_moe_qgemv(q.COLI_FMT_INT4G, FAKE, FAKE, FAKE, FAKE, 8, 64, 1,
+                            raise_on_error=False) == q.COLI_MOE_ENOTSUP
+    assert g(gs=0) == q.COLI_MOE_EINVAL
+    assert g(gs=48) == q.COLI_MOE_EINVAL
+    assert g(W=None) == q.COLI_MOE_EINVAL
+    assert g(O=0) == q.COLI_MOE_EINVAL
+    assert g(In=48) == q.COLI_MOE_ENOTSUP
+    assert g(W=FAKE + 8) == q.COLI_MOE_EALIGN

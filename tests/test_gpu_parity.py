@@ -344,3 +344,63 @@ def test_one_token_dirty_workspace(qed, blocks):
             dev.ws[:4096].copy_(ctrl)  # the counter block exactly as a finished call left it
         out, _, _ = run_forward(qed, dev, xs[i])
         assert np.array_equal(out, ref[i]), i
+
+
+# ------------------------------------------------------------------ int4-grouped tensors (format 4)
+def rand_grouped(rng, O, In, gs):
+    W = rng.integers(0, 256, size=(O, In // 2), dtype=np.uint8)
+    s = rng.uniform(0.5, 2, O * ((In + gs - 1) // gs)).astype(np.float32)
+    return W, s
+
+
+@pytest.mark.parametrize("gs", [32, 64, 128])
+def test_qgemv_grouped_unit_vectors_exact(qed, gs):
+    rng = np.random.default_rng(900 + gs)
+    O, In = 21, 160  # gs = 64, 128: a ragged last group
+    W, s = rand_grouped(rng, O, In, gs)
+    x = np.eye(In, dtype=np.float32)
+    d = torch.device("cuda")
+    y = torch.empty((In, O), dtype=torch.float32, device=d)
+    qed.coli_moe_qgemv_grouped(torch.from_numpy(W).to(d), torch.from_numpy(s).to(d), gs,
+                               torch.from_numpy(x).to(d), y, O, In, In)
+    got = y.cpu().numpy()
+    for i in range(In):
+        assert np.array_equal(got[i], oracle.qgemv_grouped(W, s, gs, x[i], O, In)), i
+
+
+@pytest.mark.parametrize("gs", [32, 96, 128])
+@pytest.mark.parametrize("T", [1, 4, 9])
+def test_qgemv_grouped_random(qed, gs, T):
+    rng = np.random.default_rng(950 + gs + T)
+    O, In = 70, 6 * 32
+    W, s = rand_grouped(rng, O, In, gs)
+    x = rng.standard_normal((T, In)).astype(np.float32)
+    d = torch.device("cuda")
+    y = torch.empty((T, O), dtype=torch.float32, device=d)
+    qed.coli_moe_qgemv_grouped(torch.from_numpy(W).to(d), torch.from_numpy(s).to(d), gs,
+                               torch.from_numpy(x).to(d), y, O, In, T)
+    got = y.cpu().numpy()
+    for t in range(T):
+        assert_out_close(got[t], oracle.qgemv_grouped(W, s, gs, x[t], O, In), what=f"t={t}")
+
+
+GROUPED = [
+    ("g32-one-token", dict(T=1, H=256, I=128, E=16, K=4, I_shared=64, group_size=32)),
+    ("g64-ragged", dict(T=5, H=352, I=160, E=12, K=3, I_shared=96, group_size=64)),
+    ("g128-routed-only", dict(T=4, H=256, I=192, E=10, K=2, I_shared=64, shared_fmt=1, group_size=128)),
+    ("g32-shared-only", dict(T=3, H=256, I=128, E=8, K=2, I_shared=128, routed_fmt=2, shared_fmt=4,
+                             group_size=32)),
+    ("g64-long", dict(T=70, H=128, I=64, E=9, K=2, I_shared=64, group_size=64)),
+]
+
+
+@pytest.mark.parametrize("name,over", GROUPED, ids=[e[0] for e in GROUPED])
+def test_grouped_blocks(qed, name, over):
+    from quantized_expert_decode_gb300.device import DeviceBlock
+    cfg = dict(norm_topk=1, routed_scale=2.5, routed_fmt=4, shared_fmt=4, zipf=False)
+    cfg.update(over)
+    blk = make(cfg, seed=zlib.crc32(name.encode()) % 1000)
+    dev = DeviceBlock(blk)
+    check_route(qed, blk, dev)
+    tokens = None if cfg["T"] <= 9 else [0, 33, 69]
+    check_forward(qed, blk, dev, tokens)

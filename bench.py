@@ -73,6 +73,9 @@ def parse():
                          "them) and exit; for ncu captures")
     ap.add_argument("--experts", type=int, default=0, help="profiling mode: override E")
     ap.add_argument("--tokens", type=int, default=0, help="profiling mode: override T")
+    ap.add_argument("--group-size", type=int, default=0,
+                    help="run the workload's int4 experts as int4-grouped tensors (format 4) with "
+                         "this many inputs per scale")
     return ap.parse_args()
 
 
@@ -87,7 +90,7 @@ def run_calls(args):
         over["E"] = args.experts
     if args.tokens:
         over["T"] = args.tokens
-    cfg = synth.config(args.workload, **over)
+    cfg = workload_cfg(args, **over)
     blk = synth.make_block(cfg, seed=synth.seed_for(args.workload))
     dev = DeviceBlock(blk)
     T, H = cfg["T"], cfg["H"]
@@ -105,21 +108,33 @@ def run_calls(args):
 
 
 # ------------------------------------------------------------------ algorithmic bytes
-def expert_bytes(fmt, H, I):
-    """(gate+up bytes, down bytes) of one expert: packed weights + fp32 row scales."""
-    gu = 2 * (I * synth.row_bytes(fmt, H) + 4 * I)
-    dn = H * synth.row_bytes(fmt, I) + 4 * H
+def workload_cfg(args, **over):
+    """The workload's config; with --group-size its int4 experts become int4-grouped."""
+    cfg = synth.config(args.workload, **over)
+    gs = getattr(args, "group_size", 0)
+    if gs:
+        g = {f: (synth.FMT_INT4G if cfg[f] == synth.FMT_INT4 else cfg[f]) for f in ("routed_fmt", "shared_fmt")}
+        cfg.update(g, group_size=gs, name=f"{cfg['name']}-grouped{gs}")
+    return cfg
+
+
+def expert_bytes(fmt, H, I, gs=0):
+    """(gate+up bytes, down bytes) of one expert: packed weights + fp32 scales (one per row, or
+    one per group of gs inputs for int4-grouped)."""
+    gu = 2 * (I * synth.row_bytes(fmt, H) + 4 * I * synth.groups(fmt, H, gs))
+    dn = H * synth.row_bytes(fmt, I) + 4 * H * synth.groups(fmt, I, gs)
     return gu, dn
 
 
 def step_bytes(cfg, n_active):
     """Algorithmic bytes one block call must read: each distinct selected expert once, the
     shared expert, the router weights and bias (activations excluded)."""
-    gu, dn = expert_bytes(cfg["routed_fmt"], cfg["H"], cfg["I"])
+    gs = cfg.get("group_size", 0)
+    gu, dn = expert_bytes(cfg["routed_fmt"], cfg["H"], cfg["I"], gs)
     b = n_active * (gu + dn)
     gu_s = dn_s = 0
     if cfg["I_shared"] > 0:
-        gu_s, dn_s = expert_bytes(cfg["shared_fmt"], cfg["H"], cfg["I_shared"])
+        gu_s, dn_s = expert_bytes(cfg["shared_fmt"], cfg["H"], cfg["I_shared"], gs)
     router = cfg["E"] * cfg["H"] * 4 + cfg["E"] * 4
     return dict(total=b + gu_s + dn_s + router, experts=b + gu_s + dn_s,
                 gateup=n_active * gu + gu_s, down=n_active * dn + dn_s)
@@ -257,8 +272,8 @@ def run_colimoe(args, rank, world, local):
     dev_name = f"cuda:{local}"
     torch.cuda.set_device(local)
     cid = args.workload
-    cfg = synth.config(cid)
-    blk = synth.make_block(cid)
+    cfg = workload_cfg(args)
+    blk = synth.make_block(cfg, seed=synth.seed_for(cid))
     dev = DeviceBlock(blk, device=dev_name)
     T, H, K = cfg["T"], cfg["H"], cfg["K"]
     xs_np = synth.make_x_batches(cfg, synth.seed_for(cid) + 97 * rank, ROTATE)
@@ -302,7 +317,9 @@ def run_colimoe(args, rank, world, local):
     # decode (T <= 64) does all its work between events 0 and 2 (the counter memset, the router
     # launch for T > 8, the persistent kernel); events 3 and 4 follow with no work between them
     # and only add the recording overhead of an event pair, so they are not part of the step
-    fused = T <= DECODE_MAX_T
+    # int4-grouped blocks run the general launches (router, gate/up, down, combine) for any T
+    general = bool(cfg.get("group_size", 0)) and synth.FMT_INT4G in (cfg["routed_fmt"], cfg["shared_fmt"])
+    fused = T <= DECODE_MAX_T and not general
     step_ms = stage[:, :2].sum(axis=1) if fused else stage.sum(axis=1)
     total_s = float(step_ms.sum()) / 1e3
     # distinct routed experts each rotated batch reads (from the library's own routing)
@@ -329,6 +346,11 @@ def run_colimoe(args, rank, world, local):
         k_bytes = np.array([b["experts"] + (b["total"] - b["experts"] if T <= 8 else 0)
                             for b in bytes_per], np.float64)
         launches = 1 if T <= 8 else 2
+    elif general:
+        kname = "gateup_kernel"
+        k_ms = stage[:, 1]
+        k_bytes = np.array([b["gateup"] for b in bytes_per], np.float64)
+        launches = 6  # router partial, select, bucket, gate/up, down, combine
     else:
         # T > 64: the expert products run as tcgen05 GEMMs; the gate/up launch (with its bf16
         # activation pre-pass) is the dominant kernel and its bound is the tensor pipe
@@ -337,14 +359,15 @@ def run_colimoe(args, rank, world, local):
         k_bytes = np.array([b["gateup"] for b in bytes_per], np.float64)
         launches = 7  # router partial, select, bucket, pre-pass, two GEMMs, combine
     achieved = float(k_bytes.sum() / (k_ms.sum() / 1e3) / 1e9)
-    if not fused:
+    hbm_bound = fused or general
+    if not hbm_bound:
         flops = gateup_flops(cfg, T * K)
         tc_peak, tc_kind = load_peaks("tensor")
         tc_achieved = flops / (float(k_ms.mean()) / 1e3) / 1e12
     block_gbs = float(sum(b["total"] for b in bytes_per) / total_s / 1e9)
     expert_gbs = float(sum(b["experts"] for b in bytes_per) / total_s / 1e9)
     src = kernel_source_hash()
-    tr = NCU_TRAFFIC.get(cid)
+    tr = None if general else NCU_TRAFFIC.get(cid)
     traffic = tr["bytes"] if tr and tr["src"] == src else None
 
     # end to end through the host-buffer entry point: H2D of x and D2H of out inside each step
@@ -388,6 +411,9 @@ def run_colimoe(args, rank, world, local):
         "active_experts_mean": float(np.mean(n_active)),
         "stages_ms": ({"prologue": float(stage[:, 0].mean()), kname: k_launch_ms}
                       if fused else
+                      {"route": float(stage[:, 0].mean()), kname: k_launch_ms,
+                       "down_kernel": float(stage[:, 2].mean()), "combine": float(stage[:, 3].mean())}
+                      if general else
                       {"route": float(stage[:, 0].mean()), "prepass_gateup_gemm": k_launch_ms,
                        "down_gemm": float(stage[:, 2].mean()), "combine": float(stage[:, 3].mean())}),
         "roofline": ({"kernel": kname, "bound": "hbm", "achieved": achieved,
@@ -395,7 +421,7 @@ def run_colimoe(args, rank, world, local):
                       "frac": achieved / hbm_peak, "traffic": traffic,
                       "algorithmic_bytes_per_launch": float(k_bytes.mean()),
                       "avg_launch_ms": k_launch_ms, "kernel_src": src}
-                     if fused else
+                     if hbm_bound else
                      {"kernel": kname, "bound": "tensor", "achieved": tc_achieved,
                       "peak": tc_peak, "peak_kind": tc_kind + " bf16 burst", "unit": "TFLOP/s",
                       "frac": tc_achieved / tc_peak, "traffic": traffic,
@@ -415,8 +441,8 @@ def run_reference(args, rank, world):
     if rank != 0:
         return None
     cid = args.workload
-    cfg = synth.config(cid)
-    blk = synth.make_block(cid)
+    cfg = workload_cfg(args)
+    blk = synth.make_block(cfg, seed=synth.seed_for(cid))
     xs = synth.make_x_batches(cfg, synth.seed_for(cid), ROTATE)
     import oracle
     oracle.build()

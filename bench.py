@@ -43,10 +43,10 @@ DECODE_MAX_T = 64  # the library runs T <= 64 as one persistent decode kernel
 # sources they were taken on; a changed kernel reports null until it is measured again.
 NCU_TRAFFIC = {
     # moe_decode1_kernel, small decode: a full-size capture
-    1: {"bytes": 25944320, "src": "e853b94b89ff0e7f"},
+    1: {"bytes": 25944576, "src": "656e0c972c31c826"},
     # moe_decode1_kernel, large decode: captured with 32 experts (the per-call expert traffic is
     # the same), plus the 224 further router rows the full 256-expert router reads
-    2: {"bytes": 171172864 + 2958336 + 224 * (6144 * 4 + 4), "src": "e853b94b89ff0e7f"},
+    2: {"bytes": 171162880 + 2850560 + 224 * (6144 * 4 + 4), "src": "656e0c972c31c826"},
 }
 
 
@@ -103,8 +103,21 @@ def run_calls(args):
                            ws=dev.ws, ws_bytes=dev.ws_bytes)
     q.coli_moe_check(dev.ws)
     torch.cuda.synchronize()
+    # distinct experts of each call and the algorithmic bytes of its decode kernel (for scaling
+    # the DRAM traffic of a capture to the benchmark's launches)
+    K = cfg["K"]
+    idx = torch.empty((T, K), dtype=torch.int32, device="cuda")
+    wts = torch.empty((T, K), dtype=torch.float32, device="cuda")
+    active, kbytes = [], []
+    for i in range(args.calls):
+        q.coli_moe_route(dev.desc, xs[i % 4], dev.Wr, dev.bias, idx, wts, None, None, None, None,
+                         dev.ws, dev.ws_bytes)
+        ids = idx.cpu().numpy()
+        active.append(int(len(np.unique(ids[ids >= 0]))))
+        kbytes.append(decode_kernel_bytes(cfg, T, active[-1]))
     print(json.dumps({"calls": args.calls, "workload": cfg["name"], "T": T, "E": cfg["E"],
-                      "out_abs_sum": float(out.abs().sum())}))
+                      "out_abs_sum": float(out.abs().sum()), "active": active,
+                      "decode_kernel_bytes": kbytes}))
 
 
 # ------------------------------------------------------------------ algorithmic bytes
@@ -138,6 +151,13 @@ def step_bytes(cfg, n_active):
     router = cfg["E"] * cfg["H"] * 4 + cfg["E"] * 4
     return dict(total=b + gu_s + dn_s + router, experts=b + gu_s + dn_s,
                 gateup=n_active * gu + gu_s, down=n_active * dn + dn_s)
+
+
+def decode_kernel_bytes(cfg, T, n_active):
+    """Algorithmic bytes of one persistent decode launch: the experts it streams, plus the
+    router weights when the launch computes the logits itself (T <= 8)."""
+    b = step_bytes(cfg, n_active)
+    return b["experts"] + (b["total"] - b["experts"] if T <= 8 else 0)
 
 
 def load_peaks(kind="hbm"):
@@ -343,8 +363,7 @@ def run_colimoe(args, rank, world, local):
         # T > 8 the router logits come from a separate launch before it
         kname = "moe_decode1_kernel" if T == 1 else "moe_decode_kernel"
         k_ms = stage[:, 1]
-        k_bytes = np.array([b["experts"] + (b["total"] - b["experts"] if T <= 8 else 0)
-                            for b in bytes_per], np.float64)
+        k_bytes = np.array([decode_kernel_bytes(cfg, T, int(u)) for u in n_active], np.float64)
         launches = 1 if T <= 8 else 2
     elif general:
         kname = "gateup_kernel"
@@ -368,7 +387,11 @@ def run_colimoe(args, rank, world, local):
     expert_gbs = float(sum(b["experts"] for b in bytes_per) / total_s / 1e9)
     src = kernel_source_hash()
     tr = None if general else NCU_TRAFFIC.get(cid)
-    traffic = tr["bytes"] if tr and tr["src"] == src else None
+    traffic = None
+    if tr and tr["src"] == src:
+        # a full-size capture gives bytes per launch; a capture of a smaller case gives the
+        # ratio of DRAM bytes to algorithmic bytes, applied to this run's mean launch
+        traffic = tr["bytes"] if "bytes" in tr else tr["ratio"] * float(k_bytes.mean())
 
     # end to end through the host-buffer entry point: H2D of x and D2H of out inside each step
     x_host = torch.from_numpy(xs_np).pin_memory()

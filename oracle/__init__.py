@@ -59,16 +59,20 @@ def _load():
         lib.oracle_qgemv.restype = None
         lib.oracle_qgemv_grouped.argtypes = [P, P, I, P, I, I, P]
         lib.oracle_qgemv_grouped.restype = None
+        lib.oracle_qrow_i8.argtypes = [P, P, I]
+        lib.oracle_qrow_i8.restype = F
+        lib.oracle_qgemv_idot.argtypes = [I, P, P, P, F, I, I, P]
+        lib.oracle_qgemv_idot.restype = None
         lib.oracle_router.argtypes = [P, I, I, P, P, I, P, P]
         lib.oracle_router.restype = I
         lib.oracle_select.argtypes = [P, P, I, I, I, I, F, I, F, P, P, P]
         lib.oracle_select.restype = I
         lib.oracle_buckets.argtypes = [P, P, I, I, I, P, P, P]
         lib.oracle_buckets.restype = I
-        lib.oracle_expert.argtypes = [I, I, P, P, P, P, P, P, I, I, P, P]
+        lib.oracle_expert.argtypes = [I, I, I, P, P, P, P, P, P, I, I, P, P]
         lib.oracle_expert.restype = None
         lib.oracle_moe_forward.argtypes = ([I, I, I, I, I, I, F, I, F, I, P, P, P] + [P] * 6 +
-                                           [I, I, I] + [P] * 6 + [P, P, P, P])
+                                           [I, I, I, I] + [P] * 6 + [P, P, P, P])
         lib.oracle_moe_forward.restype = I
         _lib = lib
         return lib
@@ -111,6 +115,24 @@ def qgemv_grouped(W: np.ndarray, s, gs: int, v: np.ndarray, O: int, In: int) -> 
     return y
 
 
+def qrow_i8(x):
+    """IDOT activation quantiser: (q int8 [n], s)."""
+    x = _f32(x)
+    q = np.empty(len(x), np.int8)
+    s = _load().oracle_qrow_i8(_p(x), _p(q), len(x))
+    return q, float(np.float32(s))
+
+
+def qgemv_idot(fmt, W, s, q, sx, O, In):
+    """IDOT GEMV on int8 activations q with their scale sx (int8 / int4 weights)."""
+    W = np.ascontiguousarray(W)
+    s = _f32(s)
+    q = np.ascontiguousarray(q, dtype=np.int8)
+    y = np.empty(O, np.float32)
+    _load().oracle_qgemv_idot(fmt, _p(W), _p(s), _p(q), float(sx), O, In, _p(y))
+    return y
+
+
 def router(x, Wr, bias):
     x, Wr, bias = _f32(x), _f32(Wr), _f32(bias)
     T, H = x.shape
@@ -149,11 +171,11 @@ def buckets(idx, E, keff=None):
     return counts, offsets, perm[:n].copy()
 
 
-def expert(fmt, ex, x, H, Iin, group_size=0):
+def expert(fmt, ex, x, H, Iin, group_size=0, idot=0):
     """One SwiGLU expert on one vector; ex is a dict with gate_w/gate_s/up_w/up_s/down_w/down_s."""
     y = np.empty(H, np.float32)
     arrs = [np.ascontiguousarray(ex[k]) for k in ("gate_w", "gate_s", "up_w", "up_s", "down_w", "down_s")]
-    _load().oracle_expert(fmt, int(group_size), *[_p(a) for a in arrs], H, Iin, _p(_f32(x)), _p(y))
+    _load().oracle_expert(fmt, int(group_size), int(idot), *[_p(a) for a in arrs], H, Iin, _p(_f32(x)), _p(y))
     return y
 
 
@@ -190,7 +212,8 @@ def moe_forward(blk, x=None, ksel=0, top_p=0.0):
     rc = lib.oracle_moe_forward(T, H, I, E, K, ksel, float(top_p), int(cfg["norm_topk"]),
                                 float(cfg["routed_scale"]), cfg["routed_fmt"], _p(x), _p(Wr), _p(bias),
                                 *[ctypes.cast(t, ctypes.c_void_p) for t in tabs],
-                                Is, cfg["shared_fmt"], int(cfg.get("group_size", 0)), *[_p(a) for a in sh_arrs],
+                                Is, cfg["shared_fmt"], int(cfg.get("group_size", 0)), int(cfg.get("idot", 0)),
+                                *[_p(a) for a in sh_arrs],
                                 _p(out), _p(idx), _p(w), _p(keff))
     if rc != 0:
         raise ValueError("oracle_moe_forward failed (bad arguments or non-finite router score)")

@@ -87,10 +87,50 @@ void oracle_qgemv_grouped(const void *W, const float *s, int gs, const float *v,
     }
 }
 
-/* one quantized matrix-vector product in either scale layout */
-static void matvec(int fmt, int gs, const void *W, const float *s, const float *v, int O, int In, float *y) {
-    if (fmt == ORACLE_FMT_INT4G) oracle_qgemv_grouped(W, s, gs, v, O, In, y);
-    else oracle_qgemv(fmt, W, s, v, O, In, y);
+/* [glm.c] qrow_i8 (the IDOT kernels' activation quantiser): amax = max |x_i| in float,
+ * s = amax / 127 (at least 1e-12), q_i = lrintf(x_i * (1 / s)) as a signed byte; returns s. */
+float oracle_qrow_i8(const float *x, int8_t *q, int n) {
+    float amax = 0.f;
+    for (int i = 0; i < n; i++) {
+        float a = fabsf(x[i]);
+        if (a > amax) amax = a;
+    }
+    float s = amax / 127.f;
+    if (s < 1e-12f) s = 1e-12f;
+    float inv = 1.f / s;
+    for (int i = 0; i < n; i++) q[i] = (int8_t)lrintf(x[i] * inv);
+    return s;
+}
+
+/* [glm.c] matmul_q_idot / matmul_i4_idot (dot_i8i8, dot_i4i8): the integer dot of the
+ * dequantised weights with the int8 activations, then y[o] = (float)dot * scale[o] * sx,
+ * multiplied left to right. int8 and int4 weights only. */
+void oracle_qgemv_idot(int fmt, const void *W, const float *s, const int8_t *q, float sx, int O, int In,
+                       float *y) {
+    int64_t rb = oracle_row_bytes(fmt, In);
+    for (int o = 0; o < O; o++) {
+        const uint8_t *row = (const uint8_t *)W + (int64_t)o * rb;
+        int64_t dot = 0;
+        for (int64_t i = 0; i < In; i++) dot += (int64_t)oracle_deq(fmt, row, i) * (int64_t)q[i];
+        y[o] = ((float)dot * s[o]) * sx;
+    }
+}
+
+/* one quantized matrix-vector product: the int4-grouped layout, the IDOT kernels (when idot is
+ * set, for int8 and int4 weights only, as glm.c's matmul_qt selects them; int2 and format 4 keep
+ * the exact path), or the exact per-row path */
+static void matvec(int fmt, int gs, int idot, const void *W, const float *s, const float *v, int O, int In,
+                   float *y) {
+    if (fmt == ORACLE_FMT_INT4G) {
+        oracle_qgemv_grouped(W, s, gs, v, O, In, y);
+    } else if (idot && (fmt == ORACLE_FMT_INT8 || fmt == ORACLE_FMT_INT4)) {
+        int8_t *q = (int8_t *)malloc((size_t)In);
+        float sx = oracle_qrow_i8(v, q, In);
+        oracle_qgemv_idot(fmt, W, s, q, sx, O, In, y);
+        free(q);
+    } else {
+        oracle_qgemv(fmt, W, s, v, O, In, y);
+    }
 }
 
 /* [glm.c] sigmoidf and siluf */
@@ -212,15 +252,15 @@ int oracle_buckets(const int32_t *idx, const int32_t *keff, int T, int K, int E,
 
 /* Phases C/D of [glm.c] moe() for one row (also [metal] moe_gemv + moe_silu):
  * g = gate.x, u = up.x, h = silu(g) * u, y = down.h. */
-void oracle_expert(int fmt, int gs, const void *gate_w, const float *gate_s, const void *up_w,
+void oracle_expert(int fmt, int gs, int idot, const void *gate_w, const float *gate_s, const void *up_w,
                    const float *up_s, const void *down_w, const float *down_s,
                    int H, int Iin, const float *x, float *y) {
     float *g = (float *)malloc(sizeof(float) * (size_t)Iin);
     float *u = (float *)malloc(sizeof(float) * (size_t)Iin);
-    matvec(fmt, gs, gate_w, gate_s, x, Iin, H, g);
-    matvec(fmt, gs, up_w, up_s, x, Iin, H, u);
+    matvec(fmt, gs, idot, gate_w, gate_s, x, Iin, H, g);
+    matvec(fmt, gs, idot, up_w, up_s, x, Iin, H, u);
     for (int j = 0; j < Iin; j++) g[j] = silu_f(g[j]) * u[j];
-    matvec(fmt, gs, down_w, down_s, g, H, Iin, y);
+    matvec(fmt, gs, idot, down_w, down_s, g, H, Iin, y);
     free(g);
     free(u);
 }
@@ -236,7 +276,7 @@ int oracle_moe_forward(int T, int H, int I, int E, int K, int ksel, float top_p,
                        const void *const *gate_w, const float *const *gate_s,
                        const void *const *up_w, const float *const *up_s,
                        const void *const *down_w, const float *const *down_s,
-                       int I_shared, int shared_fmt, int group_size,
+                       int I_shared, int shared_fmt, int group_size, int idot,
                        const void *sh_gate_w, const float *sh_gate_s,
                        const void *sh_up_w, const float *sh_up_s,
                        const void *sh_down_w, const float *sh_down_s,
@@ -264,12 +304,12 @@ int oracle_moe_forward(int T, int H, int I, int E, int K, int ksel, float top_p,
         for (int d = 0; d < H; d++) ot[d] = 0.f;
         for (int k = 0; k < ke; k++) {
             int e = id[k];
-            oracle_expert(routed_fmt, group_size, gate_w[e], gate_s[e], up_w[e], up_s[e], down_w[e],
+            oracle_expert(routed_fmt, group_size, idot, gate_w[e], gate_s[e], up_w[e], up_s[e], down_w[e],
                           down_s[e], H, I, xt, y);
             for (int d = 0; d < H; d++) ot[d] += ww[k] * y[d];
         }
         if (I_shared > 0) {
-            oracle_expert(shared_fmt, group_size, sh_gate_w, sh_gate_s, sh_up_w, sh_up_s, sh_down_w,
+            oracle_expert(shared_fmt, group_size, idot, sh_gate_w, sh_gate_s, sh_up_w, sh_up_s, sh_down_w,
                           sh_down_s, H, I_shared, xt, y);
             for (int d = 0; d < H; d++) ot[d] += y[d];
         }

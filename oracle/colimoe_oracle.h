@@ -13,6 +13,8 @@
  *             r_router, r_top8, r_top8_par; host moe_submit/moe_finish.
  *   [glm.c, quick-start diff]  colibri, compare main...docs-quickstart — c/glm.c qt_resolve_fmt,
  *             qt_from_disk, expert_load_impl: tensor format 4 (int4 with per-group scales).
+ *   [glm.c] also: qrow_i8, dot_i8i8 / dot_i4i8, matmul_q_idot / matmul_i4_idot, matmul_qt —
+ *             the IDOT kernels (int8 activations, integer dot), the lossy default of the engine.
  *
  * Precision: dot products accumulate in double and are rounded once to float, then multiplied
  * by the float row scale (the pages apply the scale after the sum). For format 4 the scale
@@ -56,6 +58,13 @@ void oracle_qgemv(int fmt, const void *W, const float *s, const float *v, int O,
  * ng = ceil(In/gs); s is [O][ng]. */
 void oracle_qgemv_grouped(const void *W, const float *s, int gs, const float *v, int O, int In, float *y);
 
+/* IDOT activation quantiser: q[i] = lrintf(x[i] / s) with s = max(max|x| / 127, 1e-12); returns s. */
+float oracle_qrow_i8(const float *x, int8_t *q, int n);
+
+/* IDOT GEMV (int8 or int4 weights): y[o] = ((float)sum_i deq(W[o,i]) * q[i]) * s[o] * sx. */
+void oracle_qgemv_idot(int fmt, const void *W, const float *s, const int8_t *q, float sx, int O, int In,
+                       float *y);
+
 /* Router scores for T tokens: sig[t,e] = sigmoid(x_t . Wr_e), choice[t,e] = sig + bias[e].
  * Returns 0, or -1 if any score or choice is not finite. */
 int oracle_router(const float *x, int T, int H, const float *Wr, const float *bias, int E,
@@ -76,8 +85,9 @@ int oracle_buckets(const int32_t *idx, const int32_t *keff, int T, int K, int E,
 
 /* One SwiGLU expert on one vector: g = gate.x, u = up.x, h = silu(g)*u, y = down.h.
  * gate/up are [Iin][row_bytes(H)], down is [H][row_bytes(Iin)]; gs is the group size of
- * format 4 (its scales are [Iin][ceil(H/gs)] and [H][ceil(Iin/gs)]), ignored otherwise. */
-void oracle_expert(int fmt, int gs, const void *gate_w, const float *gate_s, const void *up_w,
+ * format 4 (its scales are [Iin][ceil(H/gs)] and [H][ceil(Iin/gs)]), ignored otherwise; idot:
+ * int8 and int4 products through the IDOT kernels (int8 activations). */
+void oracle_expert(int fmt, int gs, int idot, const void *gate_w, const float *gate_s, const void *up_w,
                    const float *up_s, const void *down_w, const float *down_s,
                    int H, int Iin, const float *x, float *y);
 
@@ -90,7 +100,7 @@ int oracle_moe_forward(int T, int H, int I, int E, int K, int ksel, float top_p,
                        const void *const *gate_w, const float *const *gate_s,
                        const void *const *up_w, const float *const *up_s,
                        const void *const *down_w, const float *const *down_s,
-                       int I_shared, int shared_fmt, int group_size,
+                       int I_shared, int shared_fmt, int group_size, int idot,
                        const void *sh_gate_w, const float *sh_gate_s,
                        const void *sh_up_w, const float *sh_up_s,
                        const void *sh_down_w, const float *sh_down_s,

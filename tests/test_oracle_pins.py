@@ -167,6 +167,77 @@ def test_grouped_single_group_equals_per_row_int4():
         assert ulp_close(oracle.qgemv_grouped(W, s, gs, v, O, n), oracle.qgemv(F4, W, s, v, O, n), 1)
 
 
+# ---------------------------------------------------------------- IDOT (int8 activations)
+def test_qrow_i8_hand_worked_half_even():
+    # amax = 127 gives s = 1 and 1/s = 1 exactly, so q is lrintf(x): ties go to the even integer
+    x = np.array([127.0, 2.5, 3.5, -2.5, -0.5, 0.5, 1.5, -126.6, 0.49], np.float32)
+    q, s = oracle.qrow_i8(x)
+    assert s == 1.0
+    assert q.tolist() == [127, 2, 4, -2, 0, 0, 2, -127, 0]
+
+
+def test_qrow_i8_extremes_and_floor():
+    rng = np.random.default_rng(801)
+    x = rng.standard_normal(301).astype(np.float32)
+    q, s = oracle.qrow_i8(x)
+    i = int(np.argmax(np.abs(x)))
+    assert abs(int(q[i])) == 127 and np.sign(q[i]) == np.sign(x[i])
+    assert np.all(np.abs(q.astype(np.int64)) <= 127)
+    # every element within half a step (plus float rounding of x / s)
+    assert np.all(np.abs(x.astype(np.float64) - q * np.float64(s)) <= 0.5 * s * (1 + 1e-6))
+    # all-zero row: the scale floor 1e-12, q = 0
+    q0, s0 = oracle.qrow_i8(np.zeros(7, np.float32))
+    assert s0 == np.float32(1e-12) and not q0.any()
+    # power-of-two scaling of x scales s exactly and leaves q unchanged
+    q2, s2 = oracle.qrow_i8(x * np.float32(8.0))
+    assert np.array_equal(q2, q) and s2 == np.float32(8.0) * np.float32(s)
+
+
+@pytest.mark.parametrize("fmt", [F8, F4])
+def test_idot_gemv_is_exact_integer_dot_then_two_products(fmt):
+    # brute force with numpy's integer matmul on the independently decoded weights
+    rng = np.random.default_rng(810 + fmt)
+    O, n = 13, 352
+    W = rand_packed(rng, fmt, O, n)
+    s = rng.uniform(1e-3, 1e-2, O).astype(np.float32)
+    q = rng.integers(-127, 128, n).astype(np.int8)
+    sx = np.float32(0.0137)
+    y = oracle.qgemv_idot(fmt, W, s, q, sx, O, n)
+    dot = np_deq(fmt, W, n).astype(np.int64) @ q.astype(np.int64)
+    expect = (dot.astype(np.float32) * s) * sx
+    assert np.array_equal(y, expect)
+
+
+@pytest.mark.parametrize("fmt", [F8, F4])
+def test_idot_on_integer_activations_equals_exact_path(fmt):
+    # x already on the int8 grid with max |x| = 127: s = 1, q = x, and the IDOT product equals
+    # the exact path bit for bit (both round the exact integer sum once, then scale)
+    rng = np.random.default_rng(820 + fmt)
+    O, n = 9, 256
+    W = rand_packed(rng, fmt, O, n)
+    s = rng.uniform(0.5, 2.0, O).astype(np.float32)
+    x = rng.integers(-126, 127, n).astype(np.float32)
+    x[17] = -127.0
+    q, sx = oracle.qrow_i8(x)
+    assert sx == 1.0 and np.array_equal(q.astype(np.float32), x)
+    assert np.array_equal(oracle.qgemv_idot(fmt, W, s, q, sx, O, n), oracle.qgemv(fmt, W, s, x, O, n))
+
+
+@pytest.mark.parametrize("fmt", [F8, F4])
+def test_idot_error_is_a_fraction_of_a_percent(fmt):
+    # the pages state ~0.3 % RMS added error per matmul for int8 activations
+    rng = np.random.default_rng(830 + fmt)
+    O, n = 256, 2048
+    W = rand_packed(rng, fmt, O, n)
+    s = rng.uniform(0.5, 1.5, O).astype(np.float32)
+    x = rng.standard_normal(n).astype(np.float32)
+    q, sx = oracle.qrow_i8(x)
+    y_i = oracle.qgemv_idot(fmt, W, s, q, sx, O, n).astype(np.float64)
+    y_e = oracle.qgemv(fmt, W, s, x, O, n).astype(np.float64)
+    rel = np.sqrt(np.mean((y_i - y_e) ** 2) / np.mean(y_e ** 2))
+    assert 1e-4 < rel < 1e-2, rel
+
+
 @pytest.mark.parametrize("fmt,bits", [(F8, 8), (F4, 4), (F2, 2)])
 def test_pages_quantizer_roundtrip(fmt, bits):
     """Quantise float rows the way the pages' quantize_rows / pack_int4 / pack_int2 do
@@ -467,6 +538,41 @@ def test_block_grouped_with_equal_group_scales_is_per_row_int4():
     o2, i2, w2, _ = oracle.moe_forward(blk4)
     assert np.array_equal(i1, i2) and np.array_equal(w1, w2)
     assert np.allclose(o1, o2, rtol=0, atol=1e-6 * np.sqrt(np.mean(o2 ** 2)))
+
+
+def test_block_idot_leaves_int2_and_grouped_experts_exact():
+    # the engine's matmul_qt takes the IDOT kernels for int8 and int4 weights only
+    for fmt, extra in ((F2, {}), (F4G, {"group_size": 32})):
+        cfg = dict(T=3, H=128, I=64, E=5, K=2, I_shared=32, norm_topk=1, routed_scale=2.5,
+                   routed_fmt=fmt, shared_fmt=fmt, zipf=False, **extra)
+        blk = synth.make_block(cfg, seed=91)
+        o1 = oracle.moe_forward(blk)[0]
+        o2 = oracle.moe_forward(dict(blk, cfg=dict(cfg, idot=1)))[0]
+        assert np.array_equal(o1, o2), fmt
+
+
+def test_block_idot_matches_composed_idot_gemvs():
+    # one token through the IDOT block equals the IDOT GEMVs composed by hand (gate and up on
+    # qrow_i8(x), SwiGLU in float, down on qrow_i8(h)), weighted and combined in selection order
+    cfg = dict(T=1, H=128, I=64, E=4, K=2, I_shared=32, norm_topk=1, routed_scale=2.5,
+               routed_fmt=F4, shared_fmt=F8, idot=1, zipf=False)
+    blk = synth.make_block(cfg, seed=93)
+    out, idx, w, _ = oracle.moe_forward(blk)
+
+    def ffn(fmt, ex, x, Iin):
+        qx, sx = oracle.qrow_i8(x)
+        g = oracle.qgemv_idot(fmt, ex["gate_w"], ex["gate_s"], qx, sx, Iin, 128)
+        u = oracle.qgemv_idot(fmt, ex["up_w"], ex["up_s"], qx, sx, Iin, 128)
+        h = (g / (np.float32(1) + np.exp(-g))) * u
+        qh, sh = oracle.qrow_i8(h.astype(np.float32))
+        return oracle.qgemv_idot(fmt, ex["down_w"], ex["down_s"], qh, sh, 128, Iin)
+
+    x = blk["x"][0]
+    ref = np.zeros(128, np.float32)
+    for k in range(2):
+        ref = ref + w[0, k] * ffn(F4, blk["routed"][idx[0, k]], x, 64)
+    ref = ref + ffn(F8, blk["shared"], x, 32)
+    assert np.allclose(out[0], ref, rtol=0, atol=1e-5 * np.sqrt(np.mean(ref ** 2)))
 
 
 def test_block_combine_weights_and_shared_weight_one():

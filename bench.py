@@ -73,6 +73,8 @@ def parse():
                          "them) and exit; for ncu captures")
     ap.add_argument("--experts", type=int, default=0, help="profiling mode: override E")
     ap.add_argument("--tokens", type=int, default=0, help="profiling mode: override T")
+    ap.add_argument("--idot", action="store_true",
+                    help="int8 and int4 experts through the IDOT kernels (int8 activations, lossy)")
     ap.add_argument("--group-size", type=int, default=0,
                     help="run the workload's int4 experts as int4-grouped tensors (format 4) with "
                          "this many inputs per scale")
@@ -128,6 +130,8 @@ def workload_cfg(args, **over):
     if gs:
         g = {f: (synth.FMT_INT4G if cfg[f] == synth.FMT_INT4 else cfg[f]) for f in ("routed_fmt", "shared_fmt")}
         cfg.update(g, group_size=gs, name=f"{cfg['name']}-grouped{gs}")
+    if getattr(args, "idot", False):
+        cfg.update(idot=1, name=f"{cfg['name']}-idot")
     return cfg
 
 
@@ -338,7 +342,8 @@ def run_colimoe(args, rank, world, local):
     # launch for T > 8, the persistent kernel); events 3 and 4 follow with no work between them
     # and only add the recording overhead of an event pair, so they are not part of the step
     # int4-grouped blocks run the general launches (router, gate/up, down, combine) for any T
-    general = bool(cfg.get("group_size", 0)) and synth.FMT_INT4G in (cfg["routed_fmt"], cfg["shared_fmt"])
+    general = ((bool(cfg.get("group_size", 0)) and synth.FMT_INT4G in (cfg["routed_fmt"], cfg["shared_fmt"]))
+               or bool(cfg.get("idot", 0)))
     fused = T <= DECODE_MAX_T and not general
     step_ms = stage[:, :2].sum(axis=1) if fused else stage.sum(axis=1)
     total_s = float(step_ms.sum()) / 1e3
@@ -422,7 +427,8 @@ def run_colimoe(args, rank, world, local):
     return {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": float(step_ms.mean()), "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "f32 (int4/int8 weights dequantised exactly)",
+        "scaling": "weak", "vs_baseline": None, "dtype": ("i8 activations x int4/int8 weights, exact int32 sums (IDOT)" if cfg.get("idot", 0)
+                  else "f32 (int4/int8 weights dequantised exactly)"),
         "data": "synthetic (seeded; random-init int weights with the workload's shapes)",
         "config": {"workload": f"{cfg['name']} (T={T}, H={H}, I={cfg['I']}, E={cfg['E']}, K={K}, "
                                f"I_shared={cfg['I_shared']})",

@@ -91,6 +91,14 @@ typedef struct {
                              a positive multiple of 32; ignored when neither format is 4.
                              Blocks with an int4-grouped expert run the general kernels (router
                              launch, gate/up, down and combine launches) for every T. */
+    int32_t idot;         /* 0: exact products (the default, IDOT=0 in glm.c). 1: glm.c's IDOT
+                             kernels for int8 and int4 experts (qrow_i8 / matmul_q_idot /
+                             matmul_i4_idot): each activation row x (x for gate and up, h for
+                             down) is quantised to q = round-half-even(x / s) with
+                             s = max(max|x| / 127, 1e-12), the integer sum of deq(W) * q is exact,
+                             and y[o] = ((float)sum * scale[o]) * s — lossy (about 0.3 % RMS per
+                             product, as the pages state). int2 and int4-grouped experts keep the
+                             exact path. Runs the general kernels for every T. */
 } coli_moe_desc;
 
 /* One expert's six device pointers: gate/up are [I][row_bytes(H)] with fp32 scales [I];

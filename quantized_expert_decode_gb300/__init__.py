@@ -37,7 +37,8 @@ class coli_moe_desc(ctypes.Structure):
                 ("E", ctypes.c_int32), ("K", ctypes.c_int32), ("I_shared", ctypes.c_int32),
                 ("norm_topk", ctypes.c_int32), ("routed_scale", ctypes.c_float),
                 ("routed_fmt", ctypes.c_int32), ("shared_fmt", ctypes.c_int32),
-                ("ksel", ctypes.c_int32), ("top_p", ctypes.c_float), ("group_size", ctypes.c_int32)]
+                ("ksel", ctypes.c_int32), ("top_p", ctypes.c_float), ("group_size", ctypes.c_int32),
+                ("idot", ctypes.c_int32)]
 
 
 class coli_moe_expert(ctypes.Structure):
@@ -121,9 +122,9 @@ def _check(rc, where, raise_on_error):
 
 
 def make_desc(T, H, I, E, K, I_shared=0, norm_topk=1, routed_scale=1.0, routed_fmt=COLI_FMT_INT4,
-              shared_fmt=COLI_FMT_INT4, ksel=0, top_p=0.0, group_size=0):
+              shared_fmt=COLI_FMT_INT4, ksel=0, top_p=0.0, group_size=0, idot=0):
     return coli_moe_desc(T, H, I, E, K, I_shared, norm_topk, routed_scale, routed_fmt, shared_fmt,
-                         ksel, top_p, group_size)
+                         ksel, top_p, group_size, idot)
 
 
 def coli_moe_workspace_bytes(desc) -> int:

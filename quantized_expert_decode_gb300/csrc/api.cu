@@ -53,6 +53,9 @@ bool grouped(const coli_moe_desc &d) {
     return d.routed_fmt == COLI_FMT_INT4G || (d.I_shared > 0 && d.shared_fmt == COLI_FMT_INT4G);
 }
 
+// blocks that run the general launches: a grouped expert, or the IDOT kernels requested
+bool general_only(const coli_moe_desc &d) { return grouped(d) || d.idot != 0; }
+
 // group sizes the grouped kernels take: whole 16-byte chunks (32 int4 inputs) per group
 bool group_size_ok(int gs) { return gs >= 32 && gs <= kMaxDim && gs % 32 == 0; }
 
@@ -61,7 +64,8 @@ int validate_desc(const coli_moe_desc *d) {
     if (d->T < 1 || d->T > kMaxT || d->H < 1 || d->H > kMaxDim || d->I < 1 || d->I > kMaxDim ||
         d->E < 1 || d->E > kMaxE || d->K < 1 || d->K > d->E || d->K > kMaxK || d->I_shared < 0 ||
         d->I_shared > kMaxDim || (d->norm_topk != 0 && d->norm_topk != 1) || d->ksel < 0 ||
-        d->ksel > d->K || !(d->top_p >= 0.f && d->top_p < 1.f) || !std::isfinite(d->routed_scale))
+        d->ksel > d->K || !(d->top_p >= 0.f && d->top_p < 1.f) || !std::isfinite(d->routed_scale) ||
+        (d->idot != 0 && d->idot != 1))
         return COLI_MOE_EINVAL;
     int rc = check_fmt(d->routed_fmt);
     if (rc) return rc;
@@ -217,7 +221,7 @@ int run_forward_decode(const coli_moe_desc *d, const float *x, const float *W_r,
 // the persistent decode kernel's plan and grid for this description (false: not applicable):
 // the single-token kernel for T = 1 when its shared memory fits, else the token-group kernel
 bool decode_plan_for(const coli_moe_desc &d, DecParams &P, int &grid) {
-    if (grouped(d)) return false;
+    if (general_only(d)) return false;
     const int sms0 = num_sms();
     for (int per_sm = 2; per_sm >= 1 && d.T == 1; per_sm--) {
         DecParams Q{};
@@ -259,7 +263,7 @@ int run_forward(const coli_moe_desc *d, const float *x, const float *W_r, const 
     int rc = run_route(d, x, W_r, bias, idx, w, keff, nullptr, nullptr, nullptr, true, ws, st);
     if (rc) return rc;
     if ((rc = record(events, 1, st))) return rc;
-    if (d->T > kDecMaxT && !grouped(*d) && prefill_supported(*d)) {
+    if (d->T > kDecMaxT && !general_only(*d) && prefill_supported(*d)) {
         PrefillWork pw{};
         pw.experts = experts;
         if (shared) pw.shared = *shared;
@@ -313,6 +317,7 @@ int run_forward(const coli_moe_desc *d, const float *x, const float *W_r, const 
     W.shared_fmt = d->shared_fmt;
     W.ldh = d->I > d->I_shared ? d->I : d->I_shared;
     W.group_size = d->group_size;
+    W.idot = d->idot;
     const long max_active = std::min<long>((long)d->E, (long)d->T * ksel_of(d));
     W.slots = (int)max_active + (d->I_shared > 0 ? 1 : 0);
     cudaError_t e;

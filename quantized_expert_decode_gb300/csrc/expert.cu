@@ -5,6 +5,7 @@
 // g = gate.x, u = up.x, h = silu(g)*u, y = down.h, out[row] += w*y; then the shared expert with
 // weight 1) and the moe_gemv / moe_silu shaders of colibri c/backend_metal.mm @93cde63.
 // Gate and up are fused in one pass over x (the idea of matmul_i4_pair in the later glm.c).
+#include "idot.cuh"
 #include "kernels.h"
 #include "qdot.cuh"
 
@@ -58,6 +59,96 @@ __device__ __forceinline__ bool resolve_slot(const ExpertWork &W, int slot, Slot
         return false;
     }
     return true;
+}
+
+// ---------------------------------------------------------------- IDOT (int8 activations)
+// glm.c's IDOT kernels (qrow_i8, dot_i8i8 / dot_i4i8, matmul_q_idot / matmul_i4_idot): each
+// activation row is quantised to int8 with one scale, s = max(max|x| / 127, 1e-12) and
+// q = round-half-even(x * (1/s)), every division and product rounded as IEEE fp32; the dot with
+// the dequantised weights is an exact integer sum, and y[o] = ((float)dot * scale[o]) * s.
+// Staged layout (one u32 = four activation bytes per token): u32 (wi * NGW + g) * CPR + c holds
+// the elements that meet field group g of word wi of chunk c (idot.cuh signed_fields), so the
+// 32 lanes of a warp, on consecutive chunks, read consecutive u32s.
+template <int FMT>
+__device__ void stage_idot(const float *__restrict__ src, int len, uint32_t *xq, float *sx_out) {
+    using G = QGeom<FMT>;
+    using I = IQ<FMT>;
+    __shared__ float red[kWarps];
+    const int tid = threadIdx.x, lane = tid % kWarp, warp = tid / kWarp;
+    float mx = 0.f;
+    for (int i = tid; i < len / 4; i += kThreads) {
+        const float4 v = __ldg(reinterpret_cast<const float4 *>(src) + i);
+        mx = fmaxf(mx, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, o));
+    if (lane == 0) red[warp] = mx;
+    __syncthreads();
+    float amax = red[0];
+#pragma unroll
+    for (int w = 1; w < kWarps; w++) amax = fmaxf(amax, red[w]);
+    __syncthreads();  // red is reused by the next vector
+    float sq = __fdiv_rn(amax, 127.f);
+    if (sq < 1e-12f) sq = 1e-12f;
+    const float inv = __fdiv_rn(1.f, sq);
+    const int CPR = len / G::EPC, n = 4 * I::NGW * CPR;
+    for (int it = tid; it < n; it += kThreads) {
+        const int c = it % CPR, rest = it / CPR, g = rest % I::NGW, wi = rest / I::NGW;
+        uint32_t word = 0;
+#pragma unroll
+        for (int b = 0; b < 4; b++) {
+            const int el = c * G::EPC + wi * G::EPW + (FMT == COLI_FMT_INT4 ? 2 * b + g : b);
+            const int q = __float2int_rn(__fmul_rn(__ldg(src + el), inv));
+            word |= (uint32_t)(q & 0xFF) << (8 * b);
+        }
+        xq[it] = word;
+    }
+    if (tid == 0) *sx_out = sq;
+}
+
+// exact integer dots of NR packed rows (int8 or int4) with NV staged int8 vectors (xq, xstride
+// u32 per vector), lane share of the chunks reduced across the warp: every lane gets the totals
+template <int FMT, int NR, int NV>
+__device__ __forceinline__ void idot_rows(const uint8_t *const (&rows)[NR], const uint32_t *xq, int xstride, int CPR,
+                                          int lane, int (&out)[NR][NV]) {
+    using I = IQ<FMT>;
+    int acc[NR][NV];
+#pragma unroll
+    for (int r = 0; r < NR; r++)
+#pragma unroll
+        for (int v = 0; v < NV; v++) acc[r][v] = 0;
+    for (int c = lane; c < CPR; c += kWarp) {
+        uint4 w[NR];
+#pragma unroll
+        for (int r = 0; r < NR; r++) w[r] = ld_stream_16(rows[r] + 16 * c);
+#pragma unroll
+        for (int wi = 0; wi < 4; wi++)
+#pragma unroll
+            for (int g = 0; g < I::NGW; g++) {
+                uint32_t a[NR];
+#pragma unroll
+                for (int r = 0; r < NR; r++) a[r] = signed_fields<FMT>(word_of(w[r], wi), g);
+#pragma unroll
+                for (int v = 0; v < NV; v++) {
+                    const uint32_t xv = xq[v * xstride + (wi * I::NGW + g) * CPR + c];
+#pragma unroll
+                    for (int r = 0; r < NR; r++) acc[r][v] = dp4a_s<true>(a[r], xv, acc[r][v]);
+                }
+            }
+    }
+#pragma unroll
+    for (int r = 0; r < NR; r++)
+#pragma unroll
+        for (int v = 0; v < NV; v++) {
+            int t = acc[r][v];
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(kFull, t, o);
+            out[r][v] = t >> I::LOG_SC;  // every product carries the exact factor 2^LOG_SC
+        }
+}
+
+__device__ __forceinline__ float idot_scale(int dot, float sc, float sx) {
+    return __fmul_rn(__fmul_rn(__int2float_rn(dot), sc), sx);
 }
 
 // Row of h / y that holds token v of the slot (routed: its bucket position; shared: T*K + t).
@@ -132,12 +223,64 @@ __device__ void gateup_slot(const ExpertWork &W, const Slot &s, float *xs) {
     }
 }
 
+template <int FMT, int NV>
+__device__ __forceinline__ void gateup_pass_idot(const ExpertWork &W, const Slot &s, int j0, int v0, int nv,
+                                                 const uint32_t *xq, const float *sxv, int CPR) {
+    const int warp = threadIdx.x / kWarp, lane = threadIdx.x % kWarp;
+    const int64_t rb = row_bytes(FMT, W.H);
+    int jp[2];
+    const uint8_t *rows[4];
+#pragma unroll
+    for (int p = 0; p < 2; p++) {
+        jp[p] = j0 + 2 * warp + p;
+        const int jc = min(jp[p], s.inter - 1);
+        rows[2 * p] = static_cast<const uint8_t *>(s.ex.gate_w) + jc * rb;
+        rows[2 * p + 1] = static_cast<const uint8_t *>(s.ex.up_w) + jc * rb;
+    }
+    int out[4][NV];
+    idot_rows<FMT, 4, NV>(rows, xq, W.H / 4, CPR, lane, out);
+#pragma unroll
+    for (int v = 0; v < NV; v++) {
+        if (lane != v || v >= nv) continue;
+        const int hr = slot_row(W, s, v0 + v);
+#pragma unroll
+        for (int p = 0; p < 2; p++) {
+            if (jp[p] >= s.inter) continue;
+            const float g = idot_scale(out[2 * p][v], s.ex.gate_s[jp[p]], sxv[v]);
+            const float u = idot_scale(out[2 * p + 1][v], s.ex.up_s[jp[p]], sxv[v]);
+            W.h[(size_t)hr * W.ldh + jp[p]] = silu_mul(g, u);
+        }
+    }
+}
+
+template <int FMT>
+__device__ void gateup_slot_idot(const ExpertWork &W, const Slot &s, float *xs) {
+    __shared__ float sxv[kNV];
+    const int j0 = blockIdx.x * kGuRowsPerCta;
+    if (j0 >= s.inter) return;
+    const int CPR = W.H / QGeom<FMT>::EPC;
+    uint32_t *xq = reinterpret_cast<uint32_t *>(xs);
+    for (int v0 = 0; v0 < s.n; v0 += kNV) {
+        const int nv = min(kNV, s.n - v0);
+        __syncthreads();
+        for (int v = 0; v < nv; v++)
+            stage_idot<FMT>(W.x + (size_t)slot_token(W, s, v0 + v) * W.H, W.H, xq + v * (W.H / 4), &sxv[v]);
+        __syncthreads();
+        // (a missing fourth vector leaves stale integers in its slot; its sums are not stored)
+        if (nv == 1) gateup_pass_idot<FMT, 1>(W, s, j0, v0, nv, xq, sxv, CPR);
+        else if (nv == 2) gateup_pass_idot<FMT, 2>(W, s, j0, v0, nv, xq, sxv, CPR);
+        else gateup_pass_idot<FMT, 4>(W, s, j0, v0, nv, xq, sxv, CPR);
+    }
+}
+
 // grid = (ceil(max inter / 16), slots); slot 0 is the shared expert when there is one.
 __global__ void __launch_bounds__(kThreads) gateup_kernel(ExpertWork W) {
     extern __shared__ __align__(16) float xs[];
     Slot s;
     if (!resolve_slot(W, blockIdx.y, s)) return;
-    if (s.fmt == COLI_FMT_INT4) gateup_slot<COLI_FMT_INT4>(W, s, xs);
+    if (W.idot && s.fmt == COLI_FMT_INT4) gateup_slot_idot<COLI_FMT_INT4>(W, s, xs);
+    else if (W.idot && s.fmt == COLI_FMT_INT8) gateup_slot_idot<COLI_FMT_INT8>(W, s, xs);
+    else if (s.fmt == COLI_FMT_INT4) gateup_slot<COLI_FMT_INT4>(W, s, xs);
     else if (s.fmt == COLI_FMT_INT4G) gateup_slot<COLI_FMT_INT4, true>(W, s, xs);
     else if (s.fmt == COLI_FMT_INT8) gateup_slot<COLI_FMT_INT8>(W, s, xs);
     else gateup_slot<COLI_FMT_INT2>(W, s, xs);
@@ -196,12 +339,57 @@ __device__ void down_slot(const ExpertWork &W, const Slot &s, float *xs) {
     }
 }
 
+template <int FMT, int NV>
+__device__ __forceinline__ void down_pass_idot(const ExpertWork &W, const Slot &s, int d0, int v0, int nv,
+                                               const uint32_t *xq, const float *sxv, int CPR) {
+    const int warp = threadIdx.x / kWarp, lane = threadIdx.x % kWarp;
+    const int64_t rb = row_bytes(FMT, s.inter);
+    int d[4];
+    const uint8_t *rows[4];
+#pragma unroll
+    for (int r = 0; r < 4; r++) {
+        d[r] = d0 + 4 * warp + r;
+        rows[r] = static_cast<const uint8_t *>(s.ex.down_w) + min(d[r], W.H - 1) * rb;
+    }
+    int out[4][NV];
+    idot_rows<FMT, 4, NV>(rows, xq, s.inter / 4, CPR, lane, out);
+#pragma unroll
+    for (int v = 0; v < NV; v++) {
+        if (lane != v || v >= nv) continue;
+        const int yr = slot_row(W, s, v0 + v);
+#pragma unroll
+        for (int r = 0; r < 4; r++)
+            if (d[r] < W.H) W.y[(size_t)yr * W.H + d[r]] = idot_scale(out[r][v], s.ex.down_s[d[r]], sxv[v]);
+    }
+}
+
+template <int FMT>
+__device__ void down_slot_idot(const ExpertWork &W, const Slot &s, float *xs) {
+    __shared__ float sxv[kNV];
+    const int d0 = blockIdx.x * kDnRowsPerCta;
+    if (d0 >= W.H) return;
+    const int CPR = s.inter / QGeom<FMT>::EPC;
+    uint32_t *xq = reinterpret_cast<uint32_t *>(xs);
+    for (int v0 = 0; v0 < s.n; v0 += kNV) {
+        const int nv = min(kNV, s.n - v0);
+        __syncthreads();
+        for (int v = 0; v < nv; v++)
+            stage_idot<FMT>(W.h + (size_t)slot_row(W, s, v0 + v) * W.ldh, s.inter, xq + v * (s.inter / 4), &sxv[v]);
+        __syncthreads();
+        if (nv == 1) down_pass_idot<FMT, 1>(W, s, d0, v0, nv, xq, sxv, CPR);
+        else if (nv == 2) down_pass_idot<FMT, 2>(W, s, d0, v0, nv, xq, sxv, CPR);
+        else down_pass_idot<FMT, 4>(W, s, d0, v0, nv, xq, sxv, CPR);
+    }
+}
+
 // grid = (ceil(H / 32), slots)
 __global__ void __launch_bounds__(kThreads) down_kernel(ExpertWork W) {
     extern __shared__ __align__(16) float xs[];
     Slot s;
     if (!resolve_slot(W, blockIdx.y, s)) return;
-    if (s.fmt == COLI_FMT_INT4) down_slot<COLI_FMT_INT4>(W, s, xs);
+    if (W.idot && s.fmt == COLI_FMT_INT4) down_slot_idot<COLI_FMT_INT4>(W, s, xs);
+    else if (W.idot && s.fmt == COLI_FMT_INT8) down_slot_idot<COLI_FMT_INT8>(W, s, xs);
+    else if (s.fmt == COLI_FMT_INT4) down_slot<COLI_FMT_INT4>(W, s, xs);
     else if (s.fmt == COLI_FMT_INT4G) down_slot<COLI_FMT_INT4, true>(W, s, xs);
     else if (s.fmt == COLI_FMT_INT8) down_slot<COLI_FMT_INT8>(W, s, xs);
     else down_slot<COLI_FMT_INT2>(W, s, xs);

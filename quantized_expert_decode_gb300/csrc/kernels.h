@@ -22,6 +22,7 @@ struct ExpertWork {
     int ldh;                         // row stride of h in floats (max(I, I_shared))
     int slots;                       // grid.y: max active routed experts + (shared ? 1 : 0)
     int group_size;                  // inputs per scale of COLI_FMT_INT4G experts
+    int idot;                        // int8 and int4 experts through the IDOT kernels
 };
 
 // ---------------------------------------------------------------- decode.cu

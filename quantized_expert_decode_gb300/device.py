@@ -27,7 +27,8 @@ class DeviceBlock:
         E = cfg["E"]
         self.desc = make_desc(cfg["T"] if T is None else T, cfg["H"], cfg["I"], E, cfg["K"],
                               cfg["I_shared"], cfg["norm_topk"], cfg["routed_scale"],
-                              cfg["routed_fmt"], cfg["shared_fmt"], ksel, top_p, cfg.get("group_size", 0))
+                              cfg["routed_fmt"], cfg["shared_fmt"], ksel, top_p, cfg.get("group_size", 0),
+                              cfg.get("idot", 0))
         self.Wr = torch.from_numpy(np.ascontiguousarray(blk["Wr"])).to(self.device)
         self.bias = torch.from_numpy(np.ascontiguousarray(blk["bias"])).to(self.device)
         slabs = blk["routed_slabs"]

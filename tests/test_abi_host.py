@@ -142,3 +142,9 @@ def test_qgemv_grouped_rejects_bad_arguments(q):
     assert g(O=0) == q.COLI_MOE_EINVAL
     assert g(In=48) == q.COLI_MOE_ENOTSUP
     assert g(W=FAKE + 8) == q.COLI_MOE_EALIGN
+
+
+def test_idot_flag_validation(q):
+    assert q.coli_moe_workspace_bytes(good_desc(q, idot=1)) > 0
+    for bad in (2, -1):
+        assert q.coli_moe_workspace_bytes(good_desc(q, idot=bad)) == 0, bad

@@ -404,3 +404,35 @@ def test_grouped_blocks(qed, name, over):
     check_route(qed, blk, dev)
     tokens = None if cfg["T"] <= 9 else [0, 33, 69]
     check_forward(qed, blk, dev, tokens)
+
+
+# ------------------------------------------------------------------ IDOT kernels (int8 activations)
+# Up to x's quantisation the gate/up products are bit-identical to the oracle's (same IEEE
+# quantiser, exact integer sums, the same two products); SiLU's expf may differ by an ulp
+# between CUDA and the C library, which can move an element of h across a rounding boundary
+# of its int8 grid (one step of 1/127 of max|h|) before the down product. The bar allows a few
+# such steps: max|err| <= 2e-3 * rms(ref); the IDOT error itself (vs the exact block) is ~0.3 %.
+IDOT_TOL = 2e-3
+IDOT = [
+    ("idot-one-token", dict(T=1, H=256, I=128, E=16, K=4, I_shared=64, routed_fmt=2, shared_fmt=1)),
+    ("idot-int8", dict(T=5, H=256, I=128, E=12, K=3, I_shared=128, routed_fmt=1, shared_fmt=1)),
+    ("idot-int2-shared", dict(T=4, H=256, I=128, E=8, K=2, I_shared=64, routed_fmt=2, shared_fmt=3)),
+    ("idot-long", dict(T=70, H=128, I=64, E=9, K=2, I_shared=64, routed_fmt=2, shared_fmt=2)),
+]
+
+
+@pytest.mark.parametrize("name,over", IDOT, ids=[e[0] for e in IDOT])
+def test_idot_blocks(qed, name, over):
+    from quantized_expert_decode_gb300.device import DeviceBlock
+    cfg = dict(norm_topk=1, routed_scale=2.5, zipf=False, idot=1)
+    cfg.update(over)
+    blk = make(cfg, seed=zlib.crc32(name.encode()) % 1000)
+    dev = DeviceBlock(blk)
+    check_route(qed, blk, dev)
+    tokens = None if cfg["T"] <= 9 else [0, 33, 69]
+    out = check_forward(qed, blk, dev, tokens, tol=IDOT_TOL)
+    # the IDOT kernels ran: the result is not the exact block's
+    exact = oracle.moe_forward(dict(blk, cfg=dict(cfg, idot=0)))[0]
+    rows = list(range(cfg["T"])) if tokens is None else tokens
+    rel = rms(out[rows] - exact[rows]) / rms(exact[rows])
+    assert 1e-4 < rel < 2e-2, rel

@@ -208,6 +208,10 @@ EDGE = [
     ("no-renorm", dict(T=3, H=128, I=64, E=12, K=3, I_shared=32, norm_topk=0, routed_scale=1.5)),
     ("hot-bucket", dict(T=23, H=128, I=64, E=3, K=2, I_shared=64)),
     ("max-e-k", dict(T=2, H=64, I=32, E=1024, K=32, I_shared=0)),
+    # T > 8: the token images of the tensor-core core, per routed format, ragged segments
+    ("int8-t12", dict(T=12, H=256, I=128, E=6, K=3, I_shared=64, routed_fmt=1, shared_fmt=2)),
+    ("int2-t16", dict(T=16, H=256, I=128, E=5, K=2, I_shared=64, routed_fmt=3, shared_fmt=1)),
+    ("ragged-t20", dict(T=20, H=352, I=160, E=7, K=3, I_shared=96, routed_fmt=2, shared_fmt=2)),
 ]
 
 

@@ -43,18 +43,26 @@ DECODE_MAX_T = 64  # the library runs T <= 64 as one persistent decode kernel
 # sources they were taken on; a changed kernel reports null until it is measured again.
 NCU_TRAFFIC = {
     # moe_decode1_kernel, small decode: a full-size capture
-    1: {"bytes": 25944576, "src": "656e0c972c31c826"},
+    1: {"bytes": 25950720, "src": "6880ce5670d4b383"},
     # moe_decode1_kernel, large decode: captured with 32 experts (the per-call expert traffic is
     # the same), plus the 224 further router rows the full 256-expert router reads
-    2: {"bytes": 171162880 + 2850560 + 224 * (6144 * 4 + 4), "src": "656e0c972c31c826"},
+    2: {"bytes": 171171328 + 2830080 + 224 * (6144 * 4 + 4), "src": "6880ce5670d4b383"},
+    # moe_decode_kernel, batch-32 decode: a full-size capture (single-pass DRAM counters) of a
+    # call whose algorithmic bytes were 2402205696; its ratio applies to each bench launch
+    3: {"ratio": (2456768000 + 12263936) / 2402205696, "src": "6880ce5670d4b383"},
 }
 
 
 def kernel_source_hash() -> str:
+    """Hash of the sources the persistent decode kernels are compiled from (their translation
+    units and everything they include)."""
     h = hashlib.sha256()
-    for name in ("decode.cu", "decode1.cu", "decode_parts.cuh", "idot.cuh", "expert.cu", "qdot.cuh",
-                 "common.cuh", "ptx.cuh"):
-        with open(os.path.join(ROOT, "quantized_expert_decode_gb300", "csrc", name), "rb") as f:
+    csrc = os.path.join(ROOT, "quantized_expert_decode_gb300", "csrc")
+    paths = [os.path.join(csrc, n) for n in ("decode.cu", "decode1.cu", "decode_parts.cuh", "idot.cuh",
+                                             "mma.cuh", "qdot.cuh", "kernels.h", "common.cuh", "ptx.cuh")]
+    paths.append(os.path.join(ROOT, "include", "colimoe.h"))
+    for path in paths:
+        with open(path, "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
 

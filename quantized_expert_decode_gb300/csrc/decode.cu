@@ -770,7 +770,7 @@ __device__ __forceinline__ int upper_slot_smem(const int *off, int n, int x) {
     return lo;
 }
 
-// fill the piece of unit l (thread 0 only) and ask L2 for its rows. Unit spaces run slot by
+// fill the piece of unit l (thread 0 only). Unit spaces run slot by
 // slot, then token group, then unit; shared_phase: the shared expert's gate/up before routing.
 __device__ __noinline__ void make_seg(const DecParams &P, const RTab &rt, int slot, int U, int slot_base, int l,
                                       int e_share, bool down, bool shared_phase, Seg &g) {
@@ -808,15 +808,6 @@ __device__ __noinline__ void make_seg(const DecParams &P, const RTab &rt, int sl
     g.ubase = slot_base + g.tg * per;
     g.ulo = l;
     g.uhi = min(min(e_share, g.ubase + per), l + kScCap);
-    if (down) {
-        const int64_t rb = row_bytes(g.fmt, g.inter);
-        prefetch_rows(g.w0, 4 * (g.ulo - g.ubase), min(4 * (g.uhi - g.ubase), P.H), rb);
-    } else {
-        const int64_t rb = row_bytes(g.fmt, P.H);
-        const int j0 = 2 * (g.ulo - g.ubase), j1 = min(2 * (g.uhi - g.ubase), g.inter);
-        prefetch_rows(g.w0, j0, j1, rb);
-        prefetch_rows(g.w1, j0, j1, rb);
-    }
 }
 
 // walk this CTA's share [b, e) of a unit space piece by piece; off/nslots: the unit prefix

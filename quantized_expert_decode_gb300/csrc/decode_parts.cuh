@@ -246,18 +246,5 @@ __device__ __forceinline__ void prefetch_line_l2(const void *p) {
     asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
 }
 
-__device__ __forceinline__ void prefetch_l2(const void *p, uint32_t bytes) {
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
-}
-
-// ask L2 for rows [r0, r1) of a matrix with rb bytes per row (16-byte multiples), 32 KB a piece
-__device__ void prefetch_rows(const uint8_t *base, int r0, int r1, int64_t rb) {
-    if (r1 <= r0) return;
-    const uint8_t *p = base + (size_t)r0 * rb;
-    const int64_t n = (int64_t)(r1 - r0) * rb;
-    constexpr int64_t kPiece = 32768;
-    for (int64_t o = 0; o < n; o += kPiece) prefetch_l2(p + o, (uint32_t)(n - o < kPiece ? n - o : kPiece));
-}
-
 }  // namespace
 }  // namespace colimoe

@@ -274,7 +274,9 @@ __device__ void gateup_slot_idot(const ExpertWork &W, const Slot &s, float *xs) 
 }
 
 // grid = (ceil(max inter / 16), slots); slot 0 is the shared expert when there is one.
-__global__ void __launch_bounds__(kThreads) gateup_kernel(ExpertWork W) {
+// Two CTAs per SM (128 registers): measured faster than the unbounded 218-register build
+// (large decode with int4-grouped weights 175 -> 135 us, batch-32 2.50 -> 1.66 ms).
+__global__ void __launch_bounds__(kThreads, 2) gateup_kernel(ExpertWork W) {
     extern __shared__ __align__(16) float xs[];
     Slot s;
     if (!resolve_slot(W, blockIdx.y, s)) return;
@@ -383,7 +385,7 @@ __device__ void down_slot_idot(const ExpertWork &W, const Slot &s, float *xs) {
 }
 
 // grid = (ceil(H / 32), slots)
-__global__ void __launch_bounds__(kThreads) down_kernel(ExpertWork W) {
+__global__ void __launch_bounds__(kThreads, 2) down_kernel(ExpertWork W) {
     extern __shared__ __align__(16) float xs[];
     Slot s;
     if (!resolve_slot(W, blockIdx.y, s)) return;

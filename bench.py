@@ -50,16 +50,21 @@ NCU_TRAFFIC = {
     # moe_decode_kernel, batch-32 decode: a full-size capture (single-pass DRAM counters) of a
     # call whose algorithmic bytes were 2402205696; its ratio applies to each bench launch
     3: {"ratio": (2456768000 + 12263936) / 2402205696, "src": "6880ce5670d4b383"},
+    # moe_prefill_tc_kernel, prefill: the gate/up GEMM launch, a full-size capture (single-pass
+    # DRAM counters; 248 routed experts + the shared one, the bf16 activations and h)
+    4: {"bytes": 3711238912 + 70183936, "src": "4a14435d51861454"},
 }
 
 
-def kernel_source_hash() -> str:
-    """Hash of the sources the persistent decode kernels are compiled from (their translation
-    units and everything they include)."""
+def kernel_source_hash(kind: str = "decode") -> str:
+    """Hash of the sources a roofline kernel is compiled from (its translation units and
+    everything they include): the persistent decode kernels, or the prefill GEMM."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "quantized_expert_decode_gb300", "csrc")
-    paths = [os.path.join(csrc, n) for n in ("decode.cu", "decode1.cu", "decode_parts.cuh", "idot.cuh",
-                                             "mma.cuh", "qdot.cuh", "kernels.h", "common.cuh", "ptx.cuh")]
+    names = (("prefill.cu", "tc.cuh", "kernels.h", "common.cuh", "ptx.cuh") if kind == "prefill" else
+             ("decode.cu", "decode1.cu", "decode_parts.cuh", "idot.cuh", "mma.cuh", "qdot.cuh", "kernels.h",
+              "common.cuh", "ptx.cuh"))
+    paths = [os.path.join(csrc, n) for n in names]
     paths.append(os.path.join(ROOT, "include", "colimoe.h"))
     for path in paths:
         with open(path, "rb") as f:
@@ -398,7 +403,7 @@ def run_colimoe(args, rank, world, local):
         tc_achieved = flops / (float(k_ms.mean()) / 1e3) / 1e12
     block_gbs = float(sum(b["total"] for b in bytes_per) / total_s / 1e9)
     expert_gbs = float(sum(b["experts"] for b in bytes_per) / total_s / 1e9)
-    src = kernel_source_hash()
+    src = kernel_source_hash("decode" if fused else "prefill")
     tr = None if general else NCU_TRAFFIC.get(cid)
     traffic = None
     if tr and tr["src"] == src:

@@ -19,6 +19,7 @@ import argparse
 import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -43,16 +44,16 @@ DECODE_MAX_T = 64  # the library runs T <= 64 as one persistent decode kernel
 # sources they were taken on; a changed kernel reports null until it is measured again.
 NCU_TRAFFIC = {
     # moe_decode1_kernel, small decode: a full-size capture
-    1: {"bytes": 25950720, "src": "6880ce5670d4b383"},
+    1: {"bytes": 25950720, "src": "f947919a3e718fc5"},
     # moe_decode1_kernel, large decode: captured with 32 experts (the per-call expert traffic is
     # the same), plus the 224 further router rows the full 256-expert router reads
-    2: {"bytes": 171171328 + 2830080 + 224 * (6144 * 4 + 4), "src": "6880ce5670d4b383"},
+    2: {"bytes": 171171328 + 2830080 + 224 * (6144 * 4 + 4), "src": "f947919a3e718fc5"},
     # moe_decode_kernel, batch-32 decode: a full-size capture (single-pass DRAM counters) of a
     # call whose algorithmic bytes were 2402205696; its ratio applies to each bench launch
-    3: {"ratio": (2456768000 + 12263936) / 2402205696, "src": "6880ce5670d4b383"},
+    3: {"ratio": (2456768000 + 12263936) / 2402205696, "src": "f947919a3e718fc5"},
     # moe_prefill_tc_kernel, prefill: the gate/up GEMM launch, a full-size capture (single-pass
     # DRAM counters; 248 routed experts + the shared one, the bf16 activations and h)
-    4: {"bytes": 3711238912 + 70183936, "src": "4a14435d51861454"},
+    4: {"bytes": 3711238912 + 70183936, "src": "2f8cbde9f18cf240"},
 }
 
 
@@ -68,8 +69,15 @@ def kernel_source_hash(kind: str = "decode") -> str:
     paths.append(os.path.join(ROOT, "include", "colimoe.h"))
     for path in paths:
         with open(path, "rb") as f:
-            h.update(f.read())
+            h.update(_code_only(f.read().decode()).encode())
     return h.hexdigest()[:16]
+
+
+def _code_only(src: str) -> str:
+    """C/C++ source without comments and blank lines (a comment edit does not change a kernel)."""
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    lines = (re.sub(r"//.*$", "", l).rstrip() for l in src.splitlines())
+    return "\n".join(l for l in lines if l)
 
 
 def parse():

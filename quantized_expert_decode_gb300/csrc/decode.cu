@@ -16,13 +16,16 @@
 //   E  combine: out = sum_k w_k y_k in selection order + y_shared   (moe() phases C/D/E)
 // Units of B/C are two row pairs (gate and up rows j, j+1) of one expert for one group of up to
 // NV tokens; units of D are four down rows. Each phase's units are handed out in chunks by an
-// atomic counter (CTAs whose units are cheaper take more). A CTA walks its share in segments that have the same
-// expert and tokens: the segment's activations are staged once in shared memory (pre-scaled and
-// permuted, see qdot.cuh), then each warp streams its units' rows with 16-byte loads kept
-// several chunks ahead in registers, across unit boundaries.
+// atomic counter (CTAs whose units are cheaper take more). A CTA walks its share in pieces that
+// have the same expert and tokens: the piece's activations are staged once in shared memory,
+// then each warp streams its units' rows with 16-byte loads kept ahead in registers across unit
+// boundaries. A single-token group runs the integer core (x as fixed-point limbs, idot.cuh);
+// a group of 2-4 tokens runs the tensor-core core (x as f16 hi + lo parts, mma.cuh) on blocks
+// of 16 rows.
 // Dependencies are counters in the workspace: router items -> routing, gate/up -> down (raised
-// once per CTA per expert), down -> combine (once per CTA). Every wait is bounded (2 s of %globaltimer); on expiry the kernel
-// records kErrWaitExpired and carries on, so a fault in the schedule can not hang the GPU.
+// once per CTA per expert), down -> combine (once per CTA). Every wait is bounded (2 s of
+// %globaltimer); on expiry the kernel records kErrWaitExpired and carries on, so a fault in the
+// schedule can not hang the GPU.
 #include <algorithm>
 
 #include "decode_parts.cuh"

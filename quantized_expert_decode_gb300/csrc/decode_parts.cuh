@@ -1,7 +1,7 @@
 // decode_parts.cuh — device pieces shared by the persistent decode kernels (decode.cu for
-// token groups, decode1.cu for one token): bounded waits, the router item, the float and
-// integer streaming cores, activation staging and L2 prefetch. Internal to libcolimoe; every
-// translation unit gets its own copy (anonymous namespace).
+// token groups, decode1.cu for one token): bounded waits, the router item, the integer and
+// tensor-core streaming walks, activation loads and an L2 line warm-up. Internal to
+// libcolimoe; every translation unit gets its own copy (anonymous namespace).
 #pragma once
 
 #include "idot.cuh"

@@ -2,10 +2,11 @@
 """Benchmark of the quantized MoE feed-forward block on GB300.
 
 A step is one whole block (router, selection, buckets, gate/up + SiLU*mul, down, combine) over
-one batch of synthetic tokens, through the C ABI. Default workload: small decode (T=1, H=2048,
-I=1024, 64 int4 experts top-8, no shared expert). Inputs are resident in HBM; activations
-rotate through 16 pre-drawn batches and a 512 MiB buffer is written between timed steps so that
-no step finds its expert weights in the 129 MB L2.
+one batch of synthetic tokens, through the C ABI. Default workload: large decode at GLM-5.2
+block shapes (T=1, H=6144, I=2048, 256 int4 experts top-8 + an int4 shared expert of 2048,
+~176.5 MB of packed weights, scales and router weights per token). Inputs are resident in HBM;
+activations rotate through 16 pre-drawn batches and a 512 MiB buffer is written between timed
+steps so that no step finds its expert weights in the 129 MB L2.
 
 Prints one JSON line (rank 0). `--impl reference` times the CPU oracle instead, on the host
 cores, on the same workload.
@@ -63,8 +64,8 @@ def kernel_source_hash(kind: str = "decode") -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "quantized_expert_decode_gb300", "csrc")
     names = (("prefill.cu", "tc.cuh", "kernels.h", "common.cuh", "ptx.cuh") if kind == "prefill" else
-             ("decode.cu", "decode1.cu", "decode_parts.cuh", "idot.cuh", "mma.cuh", "qdot.cuh", "kernels.h",
-              "common.cuh", "ptx.cuh"))
+             ("decode.cu", "decode1.cu", "decode_parts.cuh", "idot.cuh", "mma.cuh", "qdot.cuh", "select.cuh",
+              "kernels.h", "common.cuh", "ptx.cuh"))
     paths = [os.path.join(csrc, n) for n in names]
     paths.append(os.path.join(ROOT, "include", "colimoe.h"))
     for path in paths:
@@ -86,7 +87,7 @@ def parse():
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="colimoe", choices=["colimoe", "reference"])
-    ap.add_argument("--workload", type=int, default=1, choices=sorted(synth.CONFIGS))
+    ap.add_argument("--workload", type=int, default=2, choices=sorted(synth.CONFIGS))
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="CPU work budget of the oracle baseline sample")
     ap.add_argument("--calls", type=int, default=0,
@@ -448,6 +449,8 @@ def run_colimoe(args, rank, world, local):
     return {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": float(step_ms.mean()), "higher_is_better": True,
+        "step_ms": {"mean": float(step_ms.mean()), "median": float(np.median(step_ms)),
+                    "p10": float(np.percentile(step_ms, 10)), "p90": float(np.percentile(step_ms, 90))},
         "scaling": "weak", "vs_baseline": None, "dtype": ("i8 activations x int4/int8 weights, exact int32 sums (IDOT)" if cfg.get("idot", 0)
                   else "f32 (int4/int8 weights dequantised exactly)"),
         "data": "synthetic (seeded; random-init int weights with the workload's shapes)",

@@ -137,7 +137,30 @@ int coli_moe_route(const coli_moe_desc *desc, const float *x, const float *W_r,
  *   shared:  HOST pointer to one coli_moe_expert holding device pointers; NULL iff
  *            desc->I_shared == 0.
  *   idx_out / w_out: optional DEVICE [T,K] copies of the routing (may be NULL).
- * Every step runs in fp32 on the CUDA cores (exact dequantisation, fp32 accumulation). */
+ * Arithmetic. The router (logits, sigmoid, bias, selection, renorm) is fp32 on every path;
+ * expert ids are decided exactly as the serial scan decides them on the fp32 choices. The
+ * dequantised weights are always exact (small integers times the fp32 row scale, applied after
+ * the sum). The expert products depend on the path the description selects:
+ *  - T = 1, formats 1-3: one persistent launch. Each activation vector (x for gate/up, h for
+ *    down) is put in 24-bit block fixed point, X = round(v * 2^s) with s set by max|v|, so
+ *    every element is exact to 2^-23 of max|v|; the integer products and their sums are exact
+ *    (int32 lanes, int64 totals), then one conversion to float and the row scale. Output error
+ *    within 1e-4 * rms(out) of the exact block.
+ *  - 2 <= T <= 64, formats 1-3: one persistent launch (plus a router launch for T > 8).
+ *    Single-token expert groups run as above; groups of 2-4 tokens run on the tensor cores
+ *    (mma.sync f16) with each token's vector split into two f16 parts (hi + lo, 22 significant
+ *    bits relative to that token's max|v|), exact f16 weights, exact products and fp32
+ *    accumulation. Output error within 1e-4 * rms(out).
+ *  - T > 64 with H, I, I_shared multiples of 64, formats 1-3: x and h are rounded to bf16
+ *    (round to nearest even) and the expert products run as tcgen05 bf16 GEMMs with fp32
+ *    accumulation in tensor memory; scales and SiLU are fp32. Output error within
+ *    2e-2 * rms(out).
+ *  - A block with a COLI_FMT_INT4G expert, or with desc->idot set, and T > 64 shapes the GEMMs
+ *    do not take: separate router, selection, bucket, gate/up, down and combine launches with
+ *    fp32 products and fp32 accumulation (1e-4 * rms(out)); with idot, the IDOT quantisation
+ *    described at coli_moe_desc.idot (2e-3 * rms(out) of the IDOT definition).
+ * Results are deterministic: the same inputs give the same bits (fixed summation orders, no
+ * float atomics). */
 int coli_moe_forward(const coli_moe_desc *desc, const float *x, const float *W_r,
                      const float *bias, const coli_moe_expert *experts,
                      const coli_moe_expert *shared, float *out, int32_t *idx_out,
@@ -192,25 +215,37 @@ int coli_moe_last_cuda_error(void);
  * therefore cannot provide the workspace coli_moe_forward asks for.
  *
  * It computes exactly what coli_moe_forward computes, with the same arguments minus the
- * workspace and the optional routing outputs. Its scratch is one fixed array of
- * COLI_MOE_NOALLOC_SCRATCH_BYTES inside the library's device image: every GPU on which the
- * library is loaded holds that much memory until the process exits. The caller still owns
- * and passes x, the weights and out.
+ * workspace and the optional routing outputs, and its result is bit-identical to that call's.
+ * Its scratch is one fixed array of COLI_MOE_NOALLOC_SCRATCH_BYTES inside the library's device
+ * image: every GPU on which the library is loaded holds that much memory until the process
+ * exits. The caller still owns and passes x, the weights and out.
  *   - Sizes: a description whose coli_moe_workspace_bytes() exceeds
  *     COLI_MOE_NOALLOC_SCRATCH_BYTES is rejected with COLI_MOE_EWORKSPACE before anything is
- *     launched (at H = 6144, I = I_shared = 2048, E = 256, K = 8 this admits T <= 64).
+ *     launched. At H = 6144, I = I_shared = 2048, E = 256, K = 8 that admits T <= 89 (T up to
+ *     64 on the persistent decode kernels, 65..89 on the tensor-core GEMMs).
  *   - Set-up: the first call on each device looks up the array's device address
- *     (cudaGetSymbolAddress, with that device current) and keeps it; make that first call
- *     before any stream capture.
+ *     (cudaGetSymbolAddress, with that device current) and keeps it for the life of the
+ *     process; make that first call before any stream capture. The kept address belongs to
+ *     the device's primary context: after cudaDeviceReset (or any teardown of that context) do
+ *     not call this entry point again in the same process.
  *   - Sharing: all calls, on every stream and thread, use the same array, which keeps the last
  *     call's contents (each call clears what must start at zero). Calls whose work overlaps on
  *     the GPU — on different streams, or from different threads without ordering — race on
  *     it and give wrong results; order them on one stream.
+ *   - Errors: kernel-detected conditions (no selectable expert, a misaligned expert pointer,
+ *     an expired bounded wait) land in the array's error word; coli_moe_noalloc_check reads
+ *     and clears it.
  *   - It calls no cudaMalloc, cudaFree or other allocating routine. */
 #define COLI_MOE_NOALLOC_SCRATCH_BYTES ((size_t)32 << 20)
 int coli_moe_forward_noalloc(const coli_moe_desc *desc, const float *x, const float *W_r,
                              const float *bias, const coli_moe_expert *experts,
                              const coli_moe_expert *shared, float *out, coli_stream_t stream);
+
+/* coli_moe_check for the fixed array of coli_moe_forward_noalloc, on the current device:
+ * synchronises `stream`, reads and clears the array's error word. Returns COLI_MOE_OK,
+ * COLI_MOE_EKERNEL if a kernel flagged an error since the last check, or COLI_MOE_ECUDA.
+ * Allocates nothing. */
+int coli_moe_noalloc_check(coli_stream_t stream);
 
 #ifdef __cplusplus
 }

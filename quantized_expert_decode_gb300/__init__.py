@@ -27,7 +27,7 @@ COLI_MOE_EKERNEL = -7
 EXPORTS = ("coli_moe_workspace_bytes", "coli_moe_route", "coli_moe_forward", "coli_moe_forward_profiled",
            "coli_moe_forward_host", "coli_moe_qgemv", "coli_moe_qgemv_grouped", "coli_moe_check",
            "coli_moe_strerror",
-           "coli_moe_last_cuda_error", "coli_moe_forward_noalloc")
+           "coli_moe_last_cuda_error", "coli_moe_forward_noalloc", "coli_moe_noalloc_check")
 
 COLI_MOE_NOALLOC_SCRATCH_BYTES = 32 << 20
 
@@ -82,6 +82,8 @@ def _load():
     lib.coli_moe_strerror.restype = ctypes.c_char_p
     lib.coli_moe_forward_noalloc.argtypes = [D, P, P, P, P, X, P, P]
     lib.coli_moe_forward_noalloc.restype = ctypes.c_int
+    lib.coli_moe_noalloc_check.argtypes = [P]
+    lib.coli_moe_noalloc_check.restype = ctypes.c_int
     lib.coli_moe_last_cuda_error.argtypes = []
     lib.coli_moe_last_cuda_error.restype = ctypes.c_int
     return lib
@@ -199,3 +201,10 @@ def coli_moe_forward_noalloc(desc, x, W_r, bias, experts, shared, out, stream=No
     rc = _lib.coli_moe_forward_noalloc(ctypes.byref(desc), _ptr(x), _ptr(W_r), _ptr(bias),
                                        _ptr(experts), sh, _ptr(out), _stream(stream))
     return _check(rc, "coli_moe_forward_noalloc", raise_on_error)
+
+
+def coli_moe_noalloc_check(stream=None, raise_on_error=True):
+    """Reads and clears the error word of coli_moe_forward_noalloc's fixed array (synchronises
+    the stream)."""
+    rc = _lib.coli_moe_noalloc_check(_stream(stream))
+    return _check(rc, "coli_moe_noalloc_check", raise_on_error)

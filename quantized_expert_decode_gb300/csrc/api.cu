@@ -524,3 +524,12 @@ extern "C" int coli_moe_forward_noalloc(const coli_moe_desc *desc, const float *
     return coli_moe_forward(desc, x, W_r, bias, experts, shared, out, nullptr, nullptr, ws,
                             COLI_MOE_NOALLOC_SCRATCH_BYTES, stream);
 }
+
+// the error word is the first int32 of the array, as of every workspace
+extern "C" int coli_moe_noalloc_check(coli_stream_t stream) {
+    int rc = check_device();
+    if (rc) return rc;
+    void *ws = nullptr;
+    if ((rc = noalloc_scratch(&ws))) return rc;
+    return coli_moe_check(ws, stream);
+}

@@ -8,7 +8,7 @@
 //   B  shared expert gate/up rows (independent of routing: runs while A completes)
 //   R  routing, by EVERY CTA for itself once all partials are in (one counter wait): logits
 //      summed in a fixed order, sigmoid, bias, greedy top-K with ties to the lower index
-//      (r_top8 / r_top8_par), TOPK/TOPP, renorm, routed scale, stable token->expert buckets and
+//      (select.cuh, one warp per token), TOPK/TOPP, renorm, routed scale, stable token->expert buckets and
 //      the unit tables — all in shared memory; CTA 0 also writes the routing outputs. Running
 //      it everywhere keeps a cold, single-CTA step off the critical path.
 //   C  routed gate/up rows: h = silu(gate.x * s_g) * (up.x * s_u)   (moe() phases C/D)
@@ -29,6 +29,7 @@
 #include <algorithm>
 
 #include "decode_parts.cuh"
+#include "select.cuh"
 
 namespace colimoe {
 
@@ -68,22 +69,20 @@ __device__ __forceinline__ RTab rtab_of(void *base, int T, int E, int K) {
 
 // Scratch of the routing step (inside the activation staging buffer).
 struct RScratch {
-    float *sg, *ch;          // [T][E] sigmoid scores, choices
-    int *sel_i;              // [T][K] selected expert ids in selection order
-    float *sel_w;            // [T][K] their scores
-    int *nvalid;             // [T]
+    float *sg, *ch;          // [T][sel_padded(E)] sigmoid scores, choices (-inf past E)
+    int *sel_i;              // [T][K] picks in selection order, then the kept ids (-1 past keff)
+    float2 *cand;            // [kNW][sel_cand_cap(E, Ksel)] selection candidates of each warp
     int *cnt, *off, *fill, *chk, *actv, *wc, *tmp;
 };
 
 __device__ __forceinline__ RScratch rscratch_of(void *base, const DecParams &P) {
     RScratch s;
-    const int TE = P.T * P.E, TK = P.T * P.K, E = P.E;
+    const int TE = P.T * sel_padded(P.E), TK = P.T * P.K, E = P.E;
     s.sg = static_cast<float *>(base);
     s.ch = s.sg + TE;
-    s.sel_w = s.ch + TE;
-    s.sel_i = reinterpret_cast<int *>(s.sel_w + TK);
-    s.nvalid = s.sel_i + TK;
-    s.cnt = s.nvalid + P.T;
+    s.cand = reinterpret_cast<float2 *>(s.ch + TE);
+    s.sel_i = reinterpret_cast<int *>(s.cand + kNW * sel_cand_cap(E, P.Ksel));
+    s.cnt = s.sel_i + TK;
     s.off = s.cnt + E;
     s.fill = s.off + E;
     s.chk = s.fill + E;
@@ -93,8 +92,8 @@ __device__ __forceinline__ RScratch rscratch_of(void *base, const DecParams &P) 
     return s;
 }
 
-size_t rscratch_bytes(int T, int E, int K) {
-    return (size_t)(2 * T * E + 2 * T * K + T + 5 * E + kNW * E + 16 + 16) * 4;
+size_t rscratch_bytes(int T, int E, int K, int Ksel) {
+    return (size_t)(2 * T * sel_padded(E) + 2 * kNW * sel_cand_cap(E, Ksel) + T * K + 5 * E + kNW * E + 16 + 16) * 4;
 }
 
 // exclusive scan in place of n <= 2048 ints in shared memory by the CTA; returns the total
@@ -137,55 +136,6 @@ __device__ int scan_smem(int *a, int n, int *tmp) {
     return total;
 }
 
-// one warp: greedy top-Ksel of token t over the choices in shared memory. Lane l owns experts
-// [l*PER, l*PER + PER), so a lane-local strict '>' ascending scan plus a cross-lane argmax
-// preferring the lower index reproduce the serial first-max-wins order.
-template <int PER>
-__device__ void argmax_rounds(const DecParams &P, const RScratch &s, int t, int lane) {
-    const int base = lane * PER;
-    float ch[PER], sg[PER];
-#pragma unroll
-    for (int j = 0; j < PER; j++) {
-        const int e = base + j;
-        ch[j] = e < P.E ? s.ch[t * P.E + e] : -INFINITY;
-        sg[j] = e < P.E ? s.sg[t * P.E + e] : 0.f;
-    }
-    uint32_t taken = 0;
-    int nsel = 0;
-    for (int k = 0; k < P.Ksel; k++) {
-        float bv = -1e30f, bs = 0.f;
-        int bi = 0x7fffffff;
-#pragma unroll
-        for (int j = 0; j < PER; j++)
-            if (!((taken >> j) & 1u) && ch[j] > bv) {
-                bv = ch[j];
-                bi = base + j;
-                bs = sg[j];
-            }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            const float ov = __shfl_down_sync(kFull, bv, o);
-            const int oi = __shfl_down_sync(kFull, bi, o);
-            const float os = __shfl_down_sync(kFull, bs, o);
-            if (ov > bv || (ov == bv && oi < bi)) {
-                bv = ov;
-                bi = oi;
-                bs = os;
-            }
-        }
-        bi = __shfl_sync(kFull, bi, 0);
-        bs = __shfl_sync(kFull, bs, 0);
-        if (bi == 0x7fffffff) break;
-        if (bi >= base && bi < base + PER) taken |= 1u << (bi - base);
-        if (lane == 0) {
-            s.sel_i[t * P.K + k] = bi;
-            s.sel_w[t * P.K + k] = bs;
-        }
-        nsel = k + 1;
-    }
-    if (lane == 0) s.nvalid[t] = nsel;
-}
-
 // The routing of all T tokens by this CTA, from the logits (the fixed-order sum of the nks
 // partial slices when from_partials, else slice 0 already holds them). Results go to rt; CTA 0
 // also writes the routing outputs of the workspace / caller.
@@ -193,145 +143,86 @@ __device__ __noinline__ void route_local(const DecParams &P, float *scratch, con
     const int tid = threadIdx.x, lane = tid % kWarp, warp = tid / kWarp;
     const bool out = blockIdx.x == 0;
     const RScratch s = rscratch_of(scratch, P);
-    const int T = P.T, E = P.E, K = P.K, TE = T * E;
-    // 1. logits -> sigmoid scores and choices (all loads of a thread issued together)
+    const int T = P.T, E = P.E, K = P.K, Ep = sel_padded(E), TE = T * Ep;
+    // 1. logits -> sigmoid scores and choices, rows padded to whole selection blocks
     if (!from_partials) {  // slice 0 holds the summed logits: batch a thread's loads
         constexpr int B = 8;
         for (int i0 = tid; i0 < TE; i0 += kNT * B) {
             float lg[B], bs[B];
 #pragma unroll
             for (int j = 0; j < B; j++) {
-                const int i = i0 + j * kNT;
-                if (i < TE) {
-                    lg[j] = __ldcg(P.part + i);
-                    bs[j] = __ldg(P.bias + i % E);
+                const int i = i0 + j * kNT, t = i / Ep, e = i - t * Ep;
+                if (i < TE && e < E) {
+                    lg[j] = __ldcg(P.part + (size_t)t * E + e);
+                    bs[j] = __ldg(P.bias + e);
                 }
             }
 #pragma unroll
             for (int j = 0; j < B; j++) {
-                const int i = i0 + j * kNT;
-                if (i < TE) {
-                    const float sv = 1.f / (1.f + expf(-lg[j]));
-                    const float cv = sv + bs[j];
-                    s.sg[i] = sv;
-                    s.ch[i] = cv;
+                const int i = i0 + j * kNT, t = i / Ep, e = i - t * Ep;
+                if (i >= TE) continue;
+                float sv = 0.f, cv = -INFINITY;
+                if (e < E) {
+                    sv = 1.f / (1.f + expf(-lg[j]));
+                    cv = sv + bs[j];
                     if (out) {
-                        P.sig[i] = sv;
-                        P.choice[i] = cv;
+                        P.sig[(size_t)t * E + e] = sv;
+                        P.choice[(size_t)t * E + e] = cv;
                     }
                 }
+                s.sg[i] = sv;
+                s.ch[i] = cv;
             }
         }
-    }
-    for (int i = tid; i < TE && from_partials; i += kNT) {
-        float lg = 0.f;
-        if (from_partials) {
-            float a[16];
-#pragma unroll
-            for (int k = 0; k < 16; k++)
-                if (k < P.nks) a[k] = __ldcg(P.part + (size_t)k * TE + i);
-#pragma unroll
-            for (int k = 0; k < 16; k++)
-                if (k < P.nks) lg += a[k];
-        } else {
-            lg = __ldcg(P.part + i);
-        }
-        const float sv = 1.f / (1.f + expf(-lg));
-        const float cv = sv + P.bias[i % E];
-        s.sg[i] = sv;
-        s.ch[i] = cv;
-        if (out) {
-            P.sig[i] = sv;
-            P.choice[i] = cv;
-        }
-    }
-    if (tid < T) s.nvalid[tid] = 0;
-    __syncthreads();
-    // 2. greedy top-Ksel. T <= 8: by rank — every (token, expert) counts the experts that beat
-    //    it (a higher choice, or an equal choice and a lower index); that count is its position
-    //    in the serial greedy order. Larger T: warp rounds of lane-blocked argmax.
-    if (T <= 8) {
-        for (int i = tid; i < TE; i += kNT) {
-            const int t = i / E, e = i % E;
-            const float c = s.ch[i];
-            if (!(c > -1e30f)) continue;  // never selectable: the serial scan starts at -1e30
-            const float *row = s.ch + t * E;
-            int r = 0;
-            for (int e2 = 0; e2 < E; e2++) {
-                const float c2 = row[e2];
-                r += (c2 > c) || (c2 == c && e2 < e);
-            }
-            atomicAdd(&s.nvalid[t], 1);
-            if (r < P.Ksel) {
-                s.sel_i[t * K + r] = e;
-                s.sel_w[t * K + r] = s.sg[i];
-            }
-        }
-        __syncthreads();
-        if (tid < T) s.nvalid[tid] = min(s.nvalid[tid], P.Ksel);
     } else {
-        const int per = (E + kWarp - 1) / kWarp;
-        for (int t = warp; t < T; t += kNW) {
-            if (per <= 1) argmax_rounds<1>(P, s, t, lane);
-            else if (per <= 2) argmax_rounds<2>(P, s, t, lane);
-            else if (per <= 4) argmax_rounds<4>(P, s, t, lane);
-            else if (per <= 8) argmax_rounds<8>(P, s, t, lane);
-            else if (per <= 16) argmax_rounds<16>(P, s, t, lane);
-            else argmax_rounds<32>(P, s, t, lane);
+        for (int i = tid; i < TE; i += kNT) {
+            const int t = i / Ep, e = i - t * Ep;
+            float sv = 0.f, cv = -INFINITY;
+            if (e < E) {
+                float a[16];
+                const size_t j = (size_t)t * E + e;
+#pragma unroll
+                for (int k = 0; k < 16; k++)
+                    if (k < P.nks) a[k] = __ldcg(P.part + (size_t)k * T * E + j);
+                float lg = 0.f;
+#pragma unroll
+                for (int k = 0; k < 16; k++)
+                    if (k < P.nks) lg += a[k];
+                sv = 1.f / (1.f + expf(-lg));
+                cv = sv + P.bias[e];
+                if (out) {
+                    P.sig[j] = sv;
+                    P.choice[j] = cv;
+                }
+            }
+            s.sg[i] = sv;
+            s.ch[i] = cv;
         }
     }
     __syncthreads();
-    // 3. per token: TOPP truncation, renormalisation, routed scale (the pages' float order)
-    for (int t = tid; t < T; t += kNT) {
-        const int nsel = s.nvalid[t];
+    // 2. per token, one warp: the picks (select.cuh), then TOPP, renormalisation and routed
+    //    scale in the serial code's float order
+    float2 *cand = s.cand + warp * sel_cand_cap(E, P.Ksel);
+    for (int t = warp; t < T; t += kNW) {
         int *id = s.sel_i + t * K;
-        float *ww = s.sel_w + t * K;
-        if (nsel < P.Ksel && out) flag_error(P.ctrl, kErrNoCandidate);
-        int Ke = nsel;
-        if (P.top_p > 0.f && P.top_p < 1.f) {
-            for (int a = 1; a < nsel; a++) {
-                const int ia = id[a];
-                const float wa = ww[a];
-                int b = a - 1;
-                while (b >= 0 && ww[b] < wa) {
-                    ww[b + 1] = ww[b];
-                    id[b + 1] = id[b];
-                    b--;
-                }
-                ww[b + 1] = wa;
-                id[b + 1] = ia;
-            }
-            float tot = 1e-20f;
-            for (int k = 0; k < nsel; k++) tot = __fadd_rn(tot, ww[k]);
-            float cum = 0.f;
-            for (int k = 0; k < nsel; k++) {
-                cum = __fadd_rn(cum, ww[k]);
-                if (cum >= __fmul_rn(P.top_p, tot)) {
-                    Ke = k + 1;
-                    break;
-                }
-            }
-        }
-        float sm = 1.f;
-        if (P.norm_topk) {
-            sm = 0.f;
-            for (int k = 0; k < Ke; k++) sm = __fadd_rn(sm, ww[k]);
-            sm = __fadd_rn(sm, 1e-20f);
-        }
-        for (int k = 0; k < K; k++) {
-            const bool kept = k < Ke;
-            const float wn = kept ? (P.norm_topk ? __fdiv_rn(ww[k], sm) : ww[k]) : 0.f;
-            const float wk = kept ? __fmul_rn(wn, P.rscale) : 0.f;
-            const int ik = kept ? id[k] : -1;
-            id[k] = ik;
-            rt.w[t * K + k] = wk;
+        const int nsel = sel_topk_warp(s.ch + t * Ep, E, P.Ksel, cand, id);
+        if (nsel < P.Ksel && out && lane == 0) flag_error(P.ctrl, kErrNoCandidate);
+        const int pick = lane < nsel ? id[lane] : -1;
+        const SelKept kp = sel_finish_warp(nsel, pick, lane < nsel ? s.sg[t * Ep + pick] : 0.f, P.top_p,
+                                           P.norm_topk, P.rscale);
+        __syncwarp();
+        if (lane < K) {
+            id[lane] = kp.id;
+            rt.w[t * K + lane] = kp.w;
             if (out) {
-                P.idx[(size_t)t * K + k] = ik;
-                P.w[(size_t)t * K + k] = wk;
+                P.idx[(size_t)t * K + lane] = kp.id;
+                P.w[(size_t)t * K + lane] = kp.w;
             }
         }
-        rt.keff[t] = Ke;
-        if (out) P.keff[t] = Ke;
+        if (lane == 0) {
+            rt.keff[t] = kp.ke;
+            if (out) P.keff[t] = kp.ke;
+        }
     }
     __syncthreads();
     // 4. buckets and the unit tables (slot u < U: u-th active expert, ascending id; U: shared)
@@ -1004,7 +895,8 @@ bool decode_plan(const coli_moe_desc &d, DecParams &P, int grid) {
     // start 64 bytes apart modulo 128 (distinct shared-memory banks for a quarter-warp)
     P.xs_stride = (int)align_up((size_t)maxdim, 256) + 16;
     const size_t xs_vec = (size_t)P.NV * P.xs_stride * sizeof(float);
-    const size_t scratch = rscratch_bytes(T, d.E, d.K);
+    const int ksel = (d.ksel > 0 && d.ksel < d.K) ? d.ksel : d.K;
+    const size_t scratch = rscratch_bytes(T, d.E, d.K, ksel);
     P.xs_bytes = (int)align_up(std::max(xs_vec, scratch), 128);
     P.rt_bytes = (int)align_up(rtab_bytes(T, d.E, d.K), 128);
     P.route_only = T <= 8 ? 0 : 1;

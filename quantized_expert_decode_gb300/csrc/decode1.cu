@@ -9,11 +9,11 @@
 //   A  router items: partial logits of 32 experts over one slice of H (r_router shader)
 //   B  shared expert gate/up rows (independent of routing)
 //   R  routing by EVERY CTA from the partial logits: logits summed in a fixed order, sigmoid,
-//      bias, greedy top-K with ties to the lower index (found as ranks: an expert's place in
-//      the greedy order is the number of experts that beat it), TOPK/TOPP, renorm, routed
-//      scale. The kept experts become slots 0..U-1 in ascending id order; the shared expert
-//      is slot U. Their weight pointers are loaded by the selecting lanes while the weights
-//      are renormalised.
+//      bias, greedy top-K with ties to the lower index (select.cuh: an expert's place in the
+//      greedy order is the number of experts that beat it, counted over candidates),
+//      TOPK/TOPP, renorm, routed scale. The kept experts become slots 0..U-1 in ascending id
+//      order; the shared expert is slot U. Their weight pointers are loaded by the lanes that
+//      hold them.
 //   C  routed gate/up rows: h = silu(gate.x * s_g) * (up.x * s_u); every CTA also records the
 //      largest |h| of each slot it wrote, the block fixed-point exponent of the down step
 //   D  once every gate/up row is in (one counter): (slot, 4-row group) units split slot-major
@@ -28,6 +28,7 @@
 #include <algorithm>
 
 #include "decode_parts.cuh"
+#include "select.cuh"
 
 namespace colimoe {
 
@@ -47,7 +48,7 @@ struct D1S {  // the fixed part of the CTA's shared memory
     int pos[kMaxK];     // slot of selection k, -1 beyond keff
     float w[kMaxK];     // kept routing weights, 0 beyond keff
     int sel_i[kMaxK];
-    float sel_w[kMaxK];
+    int ncand, nok;  // selection: candidates, selectable experts
     int U;
     int xshift;
     float xinv;
@@ -166,51 +167,14 @@ __device__ void stage_x(const DecParams &P, uint8_t *xq_r, uint8_t *xq_s, bool t
     __syncthreads();
 }
 
-// TOPP on the nsel selected (one per lane, selection order): sort by weight, descending and
-// stable (the insertion sort of the pages' top-p step), then keep the shortest prefix whose
-// running sum reaches top_p * (1e-20 + total). Returns the kept count; id/wv come back sorted.
-__device__ __noinline__ int top_p_cut(float top_p, int nsel, int &id, float &wv) {
-    const int lane = threadIdx.x % kWarp;
-    int p = 0;
-    for (int k = 0; k < nsel; k++) {
-        const float o = __shfl_sync(kFull, wv, k);
-        p += (o > wv) || (o == wv && k < lane);
-    }
-    int nid = id;
-    float nwv = wv;
-    for (int k = 0; k < nsel; k++) {
-        const int pk = __shfl_sync(kFull, p, k);
-        const int ik = __shfl_sync(kFull, id, k);
-        const float wk = __shfl_sync(kFull, wv, k);
-        if (pk == lane && lane < nsel) {
-            nid = ik;
-            nwv = wk;
-        }
-    }
-    id = nid;
-    wv = nwv;
-    float tot = 1e-20f;
-    for (int k = 0; k < nsel; k++) tot = __fadd_rn(tot, __shfl_sync(kFull, wv, k));
-    const float lim = __fmul_rn(top_p, tot);
-    float cum = 0.f;
-    int ke = nsel;
-    for (int k = 0; k < nsel; k++) {
-        cum = __fadd_rn(cum, __shfl_sync(kFull, wv, k));
-        if (cum >= lim) {
-            ke = k + 1;
-            break;
-        }
-    }
-    return ke;
-}
-
-// R: the routing of the token by this CTA (sg/ch: shared scratch of E rounded up to 4 floats)
-__device__ __noinline__ void route1(const DecParams &P, D1S &m, float *sg, float *ch) {
+// R: the routing of the token by this CTA (sg/ch: shared scratch of sel_padded(E) floats each,
+// cand: sel_cand_cap(E, Ksel) float2)
+__device__ __noinline__ void route1(const DecParams &P, D1S &m, float *sg, float *ch, float2 *cand) {
     const int tid = threadIdx.x, lane = tid % kWarp, warp = tid / kWarp;
     const bool out = blockIdx.x == 0;
-    const int E = P.E, E4 = (E + 3) & ~3;
+    const int E = P.E, Ep = sel_padded(E);
     // 1. logits (fixed-order sum of the partial slices) -> sigmoid scores and choices
-    for (int e = tid; e < E4; e += kNT) {
+    for (int e = tid; e < Ep; e += kNT) {
         if (e < E) {
             float a[16];
 #pragma unroll
@@ -233,56 +197,26 @@ __device__ __noinline__ void route1(const DecParams &P, D1S &m, float *sg, float
             ch[e] = -INFINITY;
         }
     }
-    if (tid < kMaxK) m.sel_i[tid] = -1;
+    if (tid == 0) m.ncand = m.nok = 0;
     __syncthreads();
-    // 2. greedy top-Ksel as ranks: an expert beaten by r others (a higher choice, or an equal
-    //    choice and a lower id) is the (r+1)-th pick of the serial scan, which starts at -1e30
-    const float4 *c4 = reinterpret_cast<const float4 *>(ch);
-    for (int e = tid; e < E; e += kNT) {
-        const float cv = ch[e];
-        if (!(cv > -1e30f)) continue;
-        int r = 0;
-        for (int q = 0; q < E4 / 4; q++) {
-            const float4 v = c4[q];
-            const int e0 = 4 * q;
-            r += (v.x > cv) || (v.x == cv && e0 < e);
-            r += (v.y > cv) || (v.y == cv && e0 + 1 < e);
-            r += (v.z > cv) || (v.z == cv && e0 + 2 < e);
-            r += (v.w > cv) || (v.w == cv && e0 + 3 < e);
-        }
-        if (r < P.Ksel) {
-            m.sel_i[r] = e;
-            m.sel_w[r] = sg[e];
-        }
-    }
-    __syncthreads();
-    // 3. the kept experts, their weights and slots (warp 0, one selection per lane)
+    // 2. the picks, by the whole CTA (select.cuh)
+    sel_topk_cta(ch, E, P.Ksel, cand, &m.ncand, &m.nok, m.sel_i);
+    // 3. the kept experts, their weights and slots (warp 0, one pick per lane)
     if (warp == 0) {
         const int K = P.K, Ksel = P.Ksel;
-        int id = lane < Ksel ? m.sel_i[lane] : -1;
-        float wv = lane < Ksel ? m.sel_w[lane] : 0.f;
-        const int nsel = __popc(__ballot_sync(kFull, id >= 0));
+        const int nsel = min(m.nok, Ksel);
         if (nsel < Ksel && out && lane == 0) flag_error(P.ctrl, kErrNoCandidate);
-        int Ke = nsel;
-        if (P.top_p > 0.f && P.top_p < 1.f) Ke = top_p_cut(P.top_p, nsel, id, wv);
-        // each kept lane asks for its expert's weight pointers now; they arrive while the
-        // weights are renormalised
+        const int pick = lane < nsel ? m.sel_i[lane] : -1;
+        const SelKept kp = sel_finish_warp(nsel, pick, lane < nsel ? sg[pick] : 0.f, P.top_p, P.norm_topk, P.rscale);
+        const int Ke = kp.ke, id = kp.id;
+        // each kept lane asks for its expert's weight pointers
         coli_moe_expert ex{};
         if (lane < Ke) ex = P.experts[id];
-        float sm = 1.f;
-        if (P.norm_topk) {
-            sm = 0.f;
-            for (int k = 0; k < Ke; k++) sm = __fadd_rn(sm, __shfl_sync(kFull, wv, k));
-            sm = __fadd_rn(sm, 1e-20f);
-        }
         const bool kept = lane < Ke;
-        const float wn = kept ? (P.norm_topk ? __fdiv_rn(wv, sm) : wv) : 0.f;
-        const float wk = kept ? __fmul_rn(wn, P.rscale) : 0.f;
-        id = kept ? id : -1;
         int slot = 0;
         for (int k = 0; k < Ke; k++) slot += __shfl_sync(kFull, id, k) < id;
         if (lane < K) {
-            m.w[lane] = wk;
+            m.w[lane] = kp.w;
             m.pos[lane] = kept ? slot : -1;
             if (kept) {
                 m.slot_e[slot] = id;
@@ -291,7 +225,7 @@ __device__ __noinline__ void route1(const DecParams &P, D1S &m, float *sg, float
             }
             if (out) {
                 P.idx[lane] = id;
-                P.w[lane] = wk;
+                P.w[lane] = kp.w;
                 P.pos[lane] = kept ? slot : -1;
                 if (kept) {
                     P.perm[slot] = lane;
@@ -426,7 +360,8 @@ __global__ void __launch_bounds__(kNT, 2) moe_decode1_kernel(const DecParams P) 
     D1S &m = *reinterpret_cast<D1S *>(smem);
     uint8_t *act = smem + P.d1_act_off;
     float *rsg = reinterpret_cast<float *>(smem + P.d1_rsc_off);
-    float *rch = rsg + ((P.E + 3) & ~3);
+    float *rch = rsg + sel_padded(P.E);
+    float2 *rcand = reinterpret_cast<float2 *>(rch + sel_padded(P.E));
     const int tid = threadIdx.x, G = gridDim.x, c = blockIdx.x;
     const bool two = P.Is > 0 && SF != RF;
     uint8_t *xq_r = act, *xq_s = two ? act + 3 * P.H : act;
@@ -499,7 +434,7 @@ __global__ void __launch_bounds__(kNT, 2) moe_decode1_kernel(const DecParams P) 
         __threadfence();
     }
     __syncthreads();
-    route1(P, m, rsg, rch);
+    route1(P, m, rsg, rch, rcand);
     const int U = m.U;
 
     // ---------------- C: routed gate/up
@@ -622,7 +557,9 @@ bool decode1_plan(const coli_moe_desc &d, DecParams &P, int grid) {
     const size_t h_bytes = (size_t)3 * (d.K + 1) * std::max(d.I, d.I_shared);
     P.d1_act_off = (int)align_up(sizeof(D1S), 128);
     P.d1_rsc_off = P.d1_act_off + (int)align_up(std::max(x_bytes, h_bytes), 128);
-    P.d1_y_off = P.d1_rsc_off + (int)align_up((size_t)2 * ((d.E + 3) & ~3) * 4, 128);  // end of smem
+    const int ksel = (d.ksel > 0 && d.ksel < d.K) ? d.ksel : d.K;
+    const size_t sel_bytes = (size_t)2 * sel_padded(d.E) * 4 + (size_t)sel_cand_cap(d.E, ksel) * 8;
+    P.d1_y_off = P.d1_rsc_off + (int)align_up(sel_bytes, 128);  // end of smem
     P.d1_rows = 0;
     return decode1_smem_bytes(P) <= 113u * 1024;
 }

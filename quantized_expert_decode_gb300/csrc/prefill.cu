@@ -29,8 +29,8 @@
 // or 16 (int2) elements K is permuted the same way in A and B — the order in which the
 // magic-number unpack produces bf16 pairs — and no byte shuffles are needed. The activations
 // (x, and h written by the gate/up epilogue) are stored in that order.
-// Every mbarrier wait is bounded; on expiry the CTA flags the error, drains the MMAs it issued,
-// frees its tensor memory and returns.
+// Every mbarrier wait is bounded; on expiry the CTA flags the error, drains the MMAs it issued
+// (a wait no other warp's abort cuts short), frees its tensor memory and returns.
 #include <algorithm>
 
 #include "common.cuh"
@@ -169,6 +169,19 @@ __device__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity, TcSmem &ts, in
     return true;
 }
 
+
+// the final drain of a CTA's MMAs: bounded, but not cut short by another warp's abort
+__device__ bool mbar_wait_drain(uint64_t *bar, uint32_t parity, int32_t *err) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    while (!mbar_try_wait(bar, parity)) {
+        if (globaltimer_ns() - t0 > kTcWaitNs) {
+            atomicCAS(err, 0, (int)kErrWaitExpired);
+            return false;
+        }
+    }
+    return true;
+}
 
 __device__ int slot_rows(const PfParams &P, int g) { return g < P.E ? P.counts[g] : P.T; }
 
@@ -479,9 +492,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) moe_prefill_tc_kernel(const PfP
                 }
                 tc_commit(&ts.accf[b]);
             }
-            // every MMA issued has completed before the tensor memory is freed
+            // every MMA issued has completed before the tensor memory is freed: this wait ignores
+            // the abort flag (an aborted CTA still drains what it issued). The MMAs in flight
+            // are a few microseconds of work; should even this bounded wait expire, the error
+            // word already says so and the context's results are undefined from then on.
             tc_commit(&ts.drain);
-            mbar_wait_bounded(&ts.drain, 0, ts, P.err);
+            mbar_wait_drain(&ts.drain, 0, P.err);
         }
         __syncwarp();
     } else {

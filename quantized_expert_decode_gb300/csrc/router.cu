@@ -1,15 +1,15 @@
 // router.cu — router logits, top-K selection and token->expert bucketing.
 //
-// Phase A of moe() in colibri-strix c/glm.c @98759bf (and the r_router / r_top8 / r_top8_par
-// shaders of colibri c/backend_metal.mm @93cde63): logit = x . W_r[e] in fp32,
+// Phase A of moe() in colibri-strix c/glm.c @98759bf (and the r_router
+// shader of colibri c/backend_metal.mm @93cde63): logit = x . W_r[e] in fp32,
 // sig = 1/(1+exp(-logit)), choice = sig + bias[e], greedy top-K over choice with ties to the
 // lower expert index, w = sig of the chosen experts, optional TOPK / TOPP, renormalisation
 // and routed_scale. Phase B (batch union) becomes a stable counting sort of the assignment
 // ids a = t*K + k by expert.
-#include <cfloat>
-#include <climits>
+#include <cmath>
 
 #include "kernels.h"
+#include "select.cuh"
 
 namespace colimoe {
 
@@ -90,27 +90,32 @@ cudaError_t launch_router_partial(const float *x, const float *W_r, float *part,
 }
 
 // ---------------------------------------------------------------- top-K selection
-// One warp per token. Lane l owns experts [l*PER, l*PER + PER) (a contiguous block, as in
-// r_top8_par), so a lane-local ascending scan with strict '>' keeps the lowest index among
-// equal choices, and the cross-lane argmax breaks ties toward the lower index: together the
-// serial first-max-wins order of moe()'s greedy loop. The TOPP / renorm / scale tail runs on
-// lane 0 with the same float operations in the same order as the serial code.
-template <int PER>
-__global__ void __launch_bounds__(256)
+// One warp per token (eight per CTA): the logits are the partial slices summed in a fixed
+// order, then sigmoid and bias; the selection and the kept weights are select.cuh's (candidate
+// ranks over blocks of 32 experts, then the TOPP / renorm / scale tail in the serial code's
+// float order). Per warp, shared memory holds the token's choices and scores (padded to whole
+// blocks), the candidates and the picks.
+constexpr int kSelWarps = 8;
+
+__host__ __device__ __forceinline__ int select_warp_floats(int E, int Ksel) {
+    return (2 * sel_padded(E) + 2 * sel_cand_cap(E, Ksel) + kMaxK + 3) / 4 * 4;
+}
+
+__global__ void __launch_bounds__(kSelWarps * kWarp)
 select_kernel(const float *__restrict__ part, int S, const float *__restrict__ bias, int T, int E,
               int K, int Ksel, float top_p, int norm_topk, float routed_scale,
               float *__restrict__ sig_out, float *__restrict__ ch_out, int32_t *__restrict__ idx,
               float *__restrict__ w, int32_t *__restrict__ keff, int32_t *__restrict__ err) {
-    __shared__ float s_w[8][kMaxK];
-    __shared__ int s_i[8][kMaxK];
+    extern __shared__ __align__(16) float sel_smem[];
     const int warp = threadIdx.x / kWarp, lane = threadIdx.x % kWarp;
-    const int t = blockIdx.x * 8 + warp;
-    if (t >= T) return;
-    const int base = lane * PER;
-    float ch[PER], sg[PER];
-#pragma unroll
-    for (int j = 0; j < PER; j++) {
-        const int e = base + j;
+    const int t = blockIdx.x * kSelWarps + warp;
+    if (t >= T) return;  // the whole warp: nothing below synchronises the CTA
+    const int Ep = sel_padded(E), cap = sel_cand_cap(E, Ksel);
+    float *ch = sel_smem + (size_t)warp * select_warp_floats(E, Ksel);
+    float *sg = ch + Ep;
+    float2 *cand = reinterpret_cast<float2 *>(sg + Ep);
+    int *sel_i = reinterpret_cast<int *>(cand + cap);
+    for (int e = lane; e < Ep; e += kWarp) {
         if (e < E) {
             float lg = 0.f;
             for (int s = 0; s < S; s++) lg += part[((size_t)s * T + t) * E + e];
@@ -118,91 +123,23 @@ select_kernel(const float *__restrict__ part, int S, const float *__restrict__ b
             const float cv = sv + bias[e];
             sig_out[(size_t)t * E + e] = sv;
             ch_out[(size_t)t * E + e] = cv;
-            sg[j] = sv;
-            ch[j] = cv;
+            sg[e] = sv;
+            ch[e] = cv;
         } else {
-            sg[j] = 0.f;
-            ch[j] = -INFINITY;
+            sg[e] = 0.f;
+            ch[e] = -INFINITY;
         }
-    }
-    uint32_t taken = 0;
-    int nsel = 0;
-    for (int k = 0; k < Ksel; k++) {
-        float bv = -1e30f, bs = 0.f;
-        int bi = INT_MAX;
-#pragma unroll
-        for (int j = 0; j < PER; j++) {
-            if (!((taken >> j) & 1u) && ch[j] > bv) {
-                bv = ch[j];
-                bi = base + j;
-                bs = sg[j];
-            }
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            const float ov = __shfl_down_sync(kFull, bv, o);
-            const int oi = __shfl_down_sync(kFull, bi, o);
-            const float os = __shfl_down_sync(kFull, bs, o);
-            if (ov > bv || (ov == bv && oi < bi)) {
-                bv = ov;
-                bi = oi;
-                bs = os;
-            }
-        }
-        bi = __shfl_sync(kFull, bi, 0);
-        bs = __shfl_sync(kFull, bs, 0);
-        if (bi == INT_MAX) {
-            if (lane == 0) atomicCAS(err, 0, (int)kErrNoCandidate);
-            break;
-        }
-        if (bi >= base && bi < base + PER) taken |= 1u << (bi - base);
-        if (lane == 0) {
-            s_i[warp][k] = bi;
-            s_w[warp][k] = bs;
-        }
-        nsel = k + 1;
     }
     __syncwarp();
-    if (lane != 0) return;
-    float *ww = s_w[warp];
-    int *id = s_i[warp];
-    int Ke = nsel;
-    if (top_p > 0.f && top_p < 1.f) {
-        for (int a = 1; a < nsel; a++) {
-            const int ia = id[a];
-            const float wa = ww[a];
-            int b = a - 1;
-            while (b >= 0 && ww[b] < wa) {
-                ww[b + 1] = ww[b];
-                id[b + 1] = id[b];
-                b--;
-            }
-            ww[b + 1] = wa;
-            id[b + 1] = ia;
-        }
-        float tot = 1e-20f;
-        for (int k = 0; k < nsel; k++) tot = __fadd_rn(tot, ww[k]);
-        float cum = 0.f;
-        for (int k = 0; k < nsel; k++) {
-            cum = __fadd_rn(cum, ww[k]);
-            if (cum >= __fmul_rn(top_p, tot)) {
-                Ke = k + 1;
-                break;
-            }
-        }
+    const int nsel = sel_topk_warp(ch, E, Ksel, cand, sel_i);
+    if (nsel < Ksel && lane == 0) atomicCAS(err, 0, (int)kErrNoCandidate);
+    const int id = lane < nsel ? sel_i[lane] : -1;
+    const SelKept kp = sel_finish_warp(nsel, id, lane < nsel ? sg[id] : 0.f, top_p, norm_topk, routed_scale);
+    if (lane < K) {
+        idx[(size_t)t * K + lane] = kp.id;
+        w[(size_t)t * K + lane] = kp.w;
     }
-    if (norm_topk) {
-        float sm = 0.f;
-        for (int k = 0; k < Ke; k++) sm = __fadd_rn(sm, ww[k]);
-        sm = __fadd_rn(sm, 1e-20f);
-        for (int k = 0; k < Ke; k++) ww[k] = __fdiv_rn(ww[k], sm);
-    }
-    for (int k = 0; k < K; k++) {
-        const bool kept = k < Ke;
-        idx[(size_t)t * K + k] = kept ? id[k] : -1;
-        w[(size_t)t * K + k] = kept ? __fmul_rn(ww[k], routed_scale) : 0.f;
-    }
-    if (keff) keff[t] = Ke;
+    if (lane == 0 && keff) keff[t] = kp.ke;
 }
 
 cudaError_t launch_select(const float *part, int splits, const float *bias, int T, int E, int K,
@@ -210,18 +147,11 @@ cudaError_t launch_select(const float *part, int splits, const float *bias, int 
                           float *choice, int32_t *idx, float *w, int32_t *keff, int32_t *err,
                           cudaStream_t st) {
     const int Ksel = (ksel > 0 && ksel < K) ? ksel : K;
-    const int per = (E + kWarp - 1) / kWarp;
-    dim3 grid((T + 7) / 8);
-#define COLI_SELECT(P)                                                                            \
-    select_kernel<P><<<grid, 256, 0, st>>>(part, splits, bias, T, E, K, Ksel, top_p, norm_topk,   \
-                                           routed_scale, sig, choice, idx, w, keff, err)
-    if (per <= 1) COLI_SELECT(1);
-    else if (per <= 2) COLI_SELECT(2);
-    else if (per <= 4) COLI_SELECT(4);
-    else if (per <= 8) COLI_SELECT(8);
-    else if (per <= 16) COLI_SELECT(16);
-    else COLI_SELECT(32);
-#undef COLI_SELECT
+    const size_t smem = (size_t)kSelWarps * select_warp_floats(E, Ksel) * sizeof(float);
+    cudaError_t e = cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    select_kernel<<<(T + kSelWarps - 1) / kSelWarps, kSelWarps * kWarp, smem, st>>>(
+        part, splits, bias, T, E, K, Ksel, top_p, norm_topk, routed_scale, sig, choice, idx, w, keff, err);
     return cudaGetLastError();
 }
 

@@ -97,6 +97,9 @@ def parse():
     ap.add_argument("--tokens", type=int, default=0, help="profiling mode: override T")
     ap.add_argument("--idot", action="store_true",
                     help="int8 and int4 experts through the IDOT kernels (int8 activations, lossy)")
+    ap.add_argument("--tail", action="store_true",
+                    help="also time the block as a decoder-layer tail (RMSNorm folded in, residual "
+                         "added) against the same work as a separate RMSNorm launch plus the block")
     ap.add_argument("--group-size", type=int, default=0,
                     help="run the workload's int4 experts as int4-grouped tensors (format 4) with "
                          "this many inputs per scale")
@@ -436,6 +439,8 @@ def run_colimoe(args, rank, world, local):
         e2e_s += time.perf_counter() - t0
     e2e_max = dist_max(e2e_s, world, dev_name if world > 1 else "cpu")
 
+    tail = measure_tail(q, dev, cfg, xs, flush, stream, args) if args.tail else None
+
     cpu = None
     if rank == 0:
         v, n, el = oracle_sample(cfg, blk, xs_np, args.cpu_seconds)
@@ -485,8 +490,51 @@ def run_colimoe(args, rank, world, local):
         "e2e": {"value": tokens / e2e_max, "unit": UNIT, "h2d_bytes_per_step": T * H * 4,
                 "d2h_bytes_per_step": T * H * 4},
         "gpu_launches": launches * args.steps,
+        **({"layer_tail": tail} if tail else {}),
         "clocks": clk,
     }
+
+
+def measure_tail(q, dev, cfg, xs, flush, stream, args):
+    """The block as a decoder-layer tail: coli_moe_forward_tail (RMSNorm folded into the
+    single-token kernel at T = 1) against coli_moe_rmsnorm + coli_moe_forward (one launch more),
+    CUDA events around each step, L2 flushed between steps. The residual rows are the workload's
+    rotating activation batches times 3; the norm weight is U(0.5, 1.5)."""
+    import torch
+    T, H = cfg["T"], cfg["H"]
+    rng = np.random.default_rng(5)
+    nw = torch.from_numpy(rng.uniform(0.5, 1.5, H).astype(np.float32)).to(xs.device)
+    resid = xs * 3.0
+    out = torch.empty((T, H), dtype=torch.float32, device=xs.device)
+    xn = torch.empty((T, H), dtype=torch.float32, device=xs.device)
+    eps = 1e-5
+
+    def fused(i):
+        q.coli_moe_forward_tail(dev.desc, resid[i % ROTATE], nw, eps, dev.Wr, dev.bias, dev.table, dev.shared,
+                                out, ws=dev.ws, ws_bytes=dev.ws_bytes, stream=stream)
+
+    def separate(i):
+        q.coli_moe_rmsnorm(resid[i % ROTATE], nw, eps, xn, T, H, stream=stream)
+        q.coli_moe_forward(dev.desc, xn, dev.Wr, dev.bias, dev.table, dev.shared, out, ws=dev.ws,
+                           ws_bytes=dev.ws_bytes, stream=stream)
+
+    res = {}
+    for name, fn in (("fused", fused), ("separate", separate)):
+        for i in range(args.warmup):
+            fn(i)
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+        for i in range(args.steps):
+            flush.fill_(float(i))
+            ev[i][0].record(stream)
+            fn(i)
+            ev[i][1].record(stream)
+        torch.cuda.synchronize()
+        ms = np.array([a.elapsed_time(b) for a, b in ev])
+        res[name + "_ms_median"] = float(np.median(ms))
+    q.coli_moe_check(dev.ws, stream)
+    res["launches_fused"] = 1 if T == 1 else None
+    res["saved_ms"] = res["separate_ms_median"] - res["fused_ms_median"]
+    return res
 
 
 # ------------------------------------------------------------------ the reference arm

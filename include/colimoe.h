@@ -176,6 +176,27 @@ int coli_moe_forward_profiled(const coli_moe_desc *desc, const float *x, const f
                               const coli_moe_expert *shared, float *out, void *const *events,
                               int n_events, void *ws, size_t ws_bytes, coli_stream_t stream);
 
+/* The block as the tail of a decoder layer (colibri-strix c/glm.c @98759bf, the layer forward
+ * after the attention residual: rmsnorm with post_ln, moe(), x += tmp; the Metal path runs the
+ * norm, the router and the shared expert in one command buffer, coli_metal_layer_decode):
+ *   xn[t]  = resid[t] * r_t * norm_w,   r_t = 1 / sqrtf(mean_i resid[t][i]^2 + eps)
+ *            (the mean square accumulated in double, the rest in float, in that order)
+ *   out[t] = resid[t] + block(xn)[t]   (the block exactly as coli_moe_forward computes it)
+ *   resid [T,H] fp32, norm_w [H] fp32 (16-byte aligned), eps >= 0 (rms_norm_eps); out may be
+ *   resid itself (an in-place residual update). Other arguments as coli_moe_forward.
+ * T = 1 runs as one launch: the single-token kernel normalises resid itself in every CTA.
+ * Other T add one small launch that writes the normalised rows into the workspace. */
+int coli_moe_forward_tail(const coli_moe_desc *desc, const float *resid, const float *norm_w, float eps,
+                          const float *W_r, const float *bias, const coli_moe_expert *experts,
+                          const coli_moe_expert *shared, float *out, int32_t *idx_out, float *w_out, void *ws,
+                          size_t ws_bytes, coli_stream_t stream);
+
+/* The normalisation of coli_moe_forward_tail on its own: xn[t] = resid[t] * r_t * norm_w for
+ * T rows of H (H a multiple of 4; resid, norm_w, xn 16-byte aligned; xn may be resid). Uses no
+ * workspace. */
+int coli_moe_rmsnorm(const float *resid, const float *norm_w, float eps, float *xn, int32_t T, int32_t H,
+                     coli_stream_t stream);
+
 /* Same as coli_moe_forward, but x_host and out_host are HOST buffers (page-locked memory
  * gives asynchronous copies). The copies go through the workspace; the call synchronises
  * `stream` before it returns, so out_host is ready on return. */

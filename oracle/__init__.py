@@ -71,6 +71,8 @@ def _load():
         lib.oracle_buckets.restype = I
         lib.oracle_expert.argtypes = [I, I, I, P, P, P, P, P, P, I, I, P, P]
         lib.oracle_expert.restype = None
+        lib.oracle_rmsnorm.argtypes = [P, P, I, F, P]
+        lib.oracle_rmsnorm.restype = None
         lib.oracle_moe_forward.argtypes = ([I, I, I, I, I, I, F, I, F, I, P, P, P] + [P] * 6 +
                                            [I, I, I, I] + [P] * 6 + [P, P, P, P])
         lib.oracle_moe_forward.restype = I
@@ -218,3 +220,28 @@ def moe_forward(blk, x=None, ksel=0, top_p=0.0):
     if rc != 0:
         raise ValueError("oracle_moe_forward failed (bad arguments or non-finite router score)")
     return out, idx, w, keff
+
+
+def rmsnorm(x, w, eps):
+    """RMS normalisation of each row of x (glm.c rmsnorm): rows * r * w, r from the row's mean
+    square accumulated in double."""
+    x = np.atleast_2d(_f32(x))
+    w = _f32(w)
+    out = np.empty_like(x)
+    lib = _load()
+    for t in range(x.shape[0]):
+        row = np.ascontiguousarray(x[t])
+        o = np.empty_like(row)
+        lib.oracle_rmsnorm(_p(row), _p(w), x.shape[1], float(eps), _p(o))
+        out[t] = o
+    return out
+
+
+def moe_tail(blk, resid, norm_w, eps, ksel=0, top_p=0.0):
+    """The block as the tail of a decoder layer (glm.c layer forward after the attention
+    residual): xn = rmsnorm(resid, post_ln); out = resid + moe(xn), the residual added in float
+    as `x[j] += tmp[j]` does. Returns (out, idx, w, keff) like moe_forward."""
+    resid = np.atleast_2d(_f32(resid))
+    xn = rmsnorm(resid, norm_w, eps)
+    y, idx, w, keff = moe_forward(blk, x=xn, ksel=ksel, top_p=top_p)
+    return (resid + y).astype(np.float32), idx, w, keff

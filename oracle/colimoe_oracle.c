@@ -265,6 +265,16 @@ void oracle_expert(int fmt, int gs, int idot, const void *gate_w, const float *g
     free(u);
 }
 
+/* [glm.c] rmsnorm(), the normalisation that feeds moe() in the layer forward (post_ln after
+ * the attention residual): the mean square in double, its reciprocal root in float, then each
+ * element times r times its weight, in that order. */
+void oracle_rmsnorm(const float *x, const float *w, int D, float eps, float *out) {
+    double ms = 0.0;
+    for (int i = 0; i < D; i++) ms += (double)x[i] * x[i];
+    const float r = 1.f / sqrtf((float)(ms / D) + eps);
+    for (int i = 0; i < D; i++) out[i] = x[i] * r * w[i];
+}
+
 /* The block, [glm.c] moe(): per token, route (phase A), run each kept routed expert in
  * selection order and accumulate out += w * y (phases C/D), then add the shared expert with
  * weight 1 (phase E).  Tokens are independent rows, so the per-token loop gives the same

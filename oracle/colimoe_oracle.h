@@ -91,6 +91,10 @@ void oracle_expert(int fmt, int gs, int idot, const void *gate_w, const float *g
                    const float *up_s, const void *down_w, const float *down_s,
                    int H, int Iin, const float *x, float *y);
 
+/* RMS normalisation of one row, [glm.c] rmsnorm(): ms = sum_i x[i]^2 accumulated in double;
+ * r = 1 / sqrtf((float)(ms / D) + eps); out[i] = (x[i] * r) * w[i] in float. out may be x. */
+void oracle_rmsnorm(const float *x, const float *w, int D, float eps, float *out);
+
 /* The whole block for T tokens.  Experts are given as host pointer tables of length E.
  * shared_* may be NULL when I_shared == 0.  idx_out/w_out/keff_out optional ([T,K], [T]).
  * Returns 0, or -1 on bad arguments or non-finite router scores. */

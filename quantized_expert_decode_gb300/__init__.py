@@ -27,7 +27,8 @@ COLI_MOE_EKERNEL = -7
 EXPORTS = ("coli_moe_workspace_bytes", "coli_moe_route", "coli_moe_forward", "coli_moe_forward_profiled",
            "coli_moe_forward_host", "coli_moe_qgemv", "coli_moe_qgemv_grouped", "coli_moe_check",
            "coli_moe_strerror",
-           "coli_moe_last_cuda_error", "coli_moe_forward_noalloc", "coli_moe_noalloc_check")
+           "coli_moe_last_cuda_error", "coli_moe_forward_noalloc", "coli_moe_noalloc_check",
+           "coli_moe_forward_tail", "coli_moe_rmsnorm")
 
 COLI_MOE_NOALLOC_SCRATCH_BYTES = 32 << 20
 
@@ -82,6 +83,10 @@ def _load():
     lib.coli_moe_strerror.restype = ctypes.c_char_p
     lib.coli_moe_forward_noalloc.argtypes = [D, P, P, P, P, X, P, P]
     lib.coli_moe_forward_noalloc.restype = ctypes.c_int
+    lib.coli_moe_forward_tail.argtypes = [D, P, P, ctypes.c_float, P, P, P, X, P, P, P, P, SZ, P]
+    lib.coli_moe_forward_tail.restype = ctypes.c_int
+    lib.coli_moe_rmsnorm.argtypes = [P, P, ctypes.c_float, P, I32, I32, P]
+    lib.coli_moe_rmsnorm.restype = ctypes.c_int
     lib.coli_moe_noalloc_check.argtypes = [P]
     lib.coli_moe_noalloc_check.restype = ctypes.c_int
     lib.coli_moe_last_cuda_error.argtypes = []
@@ -161,6 +166,20 @@ def coli_moe_forward_profiled(desc, x, W_r, bias, experts, shared, out, events, 
                                         _ptr(experts), sh, _ptr(out), arr, len(handles), _ptr(ws),
                                         ws_bytes, _stream(stream))
     return _check(rc, "coli_moe_forward_profiled", raise_on_error)
+
+
+def coli_moe_forward_tail(desc, resid, norm_w, eps, W_r, bias, experts, shared, out, idx_out=None,
+                          w_out=None, ws=None, ws_bytes=0, stream=None, raise_on_error=True):
+    sh = ctypes.byref(shared) if shared is not None else None
+    rc = _lib.coli_moe_forward_tail(ctypes.byref(desc), _ptr(resid), _ptr(norm_w), float(eps), _ptr(W_r),
+                                    _ptr(bias), _ptr(experts), sh, _ptr(out), _ptr(idx_out), _ptr(w_out),
+                                    _ptr(ws), ws_bytes, _stream(stream))
+    return _check(rc, "coli_moe_forward_tail", raise_on_error)
+
+
+def coli_moe_rmsnorm(resid, norm_w, eps, xn, T, H, stream=None, raise_on_error=True):
+    rc = _lib.coli_moe_rmsnorm(_ptr(resid), _ptr(norm_w), float(eps), _ptr(xn), T, H, _stream(stream))
+    return _check(rc, "coli_moe_rmsnorm", raise_on_error)
 
 
 def coli_moe_forward_host(desc, x_host, W_r, bias, experts, shared, out_host, ws=None, ws_bytes=0,

@@ -154,15 +154,27 @@ uint64_t next_call_id() {
     return next.fetch_add(2, std::memory_order_relaxed);
 }
 
+// The layer tail (coli_moe_forward_tail): the block runs on rmsnorm(resid) * norm_w and adds
+// resid to its output. NULL when the call is the block alone.
+struct Tail {
+    const float *resid, *norm_w;
+    float eps;
+};
+
 // T <= 64: router, selection, buckets, experts and combine in one persistent launch
 // (decode.cu); T > 8 computes the router logits in a preceding launch.
 int run_forward_decode(const coli_moe_desc *d, const float *x, const float *W_r, const float *bias,
                        const coli_moe_expert *experts, const coli_moe_expert *shared, float *out,
                        int32_t *idx_out, float *w_out, void *ws, cudaStream_t st,
-                       void *const *events, const DecParams &plan, int grid) {
+                       void *const *events, const DecParams &plan, int grid, const Tail *tail) {
     const WsLayout L = ws_layout(*d);
     DecParams P = plan;
     P.x = x;
+    if (tail) {  // the single-token kernel normalises resid itself; the others get x normalised
+        P.resid = tail->resid;
+        P.norm_w = tail->norm_w;
+        P.eps = tail->eps;
+    }
     P.Wr = W_r;
     P.bias = bias;
     P.experts = experts;
@@ -247,15 +259,32 @@ bool decode_plan_for(const coli_moe_desc &d, DecParams &P, int &grid) {
 int run_forward(const coli_moe_desc *d, const float *x, const float *W_r, const float *bias,
                 const coli_moe_expert *experts, const coli_moe_expert *shared, float *out,
                 int32_t *idx_out, float *w_out, void *ws, cudaStream_t st,
-                void *const *events = nullptr) {
+                void *const *events = nullptr, const Tail *tail = nullptr) {
+    const WsLayout L = ws_layout(*d);
+    const float *resid = tail ? tail->resid : nullptr;
+    // the layer tail outside the single-token kernel: a prologue launch writes the normalised
+    // rows into the workspace's staging rows, which the rest of the block reads as x
+    auto normalise = [&]() -> int {
+        float *xn = ws_ptr<float>(ws, L.xstage);
+        cudaError_t e = launch_rmsnorm(tail->resid, tail->norm_w, tail->eps, d->T, d->H, xn, st);
+        if (e != cudaSuccess) return cuda_fail(e);
+        x = xn;
+        return COLI_MOE_OK;
+    };
     {
         DecParams plan{};
         int grid = 0;
-        if (decode_plan_for(*d, plan, grid))
+        if (decode_plan_for(*d, plan, grid)) {
+            if (tail && !plan.single) {
+                if (int rc = normalise()) return rc;
+            }
             return run_forward_decode(d, x, W_r, bias, experts, shared, out, idx_out, w_out, ws, st, events,
-                                      plan, grid);
+                                      plan, grid, tail);
+        }
     }
-    const WsLayout L = ws_layout(*d);
+    if (tail) {
+        if (int rc = normalise()) return rc;
+    }
     if (int rc0 = record(events, 0, st)) return rc0;
     int32_t *idx = idx_out ? idx_out : ws_ptr<int32_t>(ws, L.idx);
     float *w = w_out ? w_out : ws_ptr<float>(ws, L.w);
@@ -271,7 +300,11 @@ int run_forward(const coli_moe_desc *d, const float *x, const float *W_r, const 
         pw.counts = ws_ptr<int32_t>(ws, L.counts);
         pw.offsets = ws_ptr<int32_t>(ws, L.offsets);
         pw.perm = ws_ptr<int32_t>(ws, L.perm);
-        pw.xb = ws_ptr<uint16_t>(ws, L.y);  // read by the gate/up GEMM only, before y is written
+        // the f16 activations and their row exponents live in the y region: only the gate/up
+        // GEMM reads them, before the down GEMM writes y
+        pw.xb = ws_ptr<uint16_t>(ws, L.y);
+        const size_t rows = (size_t)d->T * d->K + (d->I_shared > 0 ? d->T : 0);  // the rows of y
+        pw.xe = ws_ptr<int32_t>(ws, L.y + align_up(rows * d->H * sizeof(uint16_t), 256));
         pw.hb = ws_ptr<uint16_t>(ws, L.h);
         pw.y = ws_ptr<float>(ws, L.y);
         pw.err = ws_ptr<int32_t>(ws, L.err);
@@ -291,7 +324,7 @@ int run_forward(const coli_moe_desc *d, const float *x, const float *W_r, const 
         if ((e = launch_prefill(pw, 1, st)) != cudaSuccess) return cuda_fail(e);
         if ((rc = record(events, 3, st))) return rc;
         if ((e = launch_combine(pw.y, w, keff, ws_ptr<int32_t>(ws, L.pos), d->T, d->H, d->K,
-                                d->I_shared > 0, out, st)) != cudaSuccess)
+                                d->I_shared > 0, resid, out, st)) != cudaSuccess)
             return cuda_fail(e);
         return record(events, 4, st);
     }
@@ -326,7 +359,7 @@ int run_forward(const coli_moe_desc *d, const float *x, const float *W_r, const 
     if ((e = launch_down(W, st)) != cudaSuccess) return cuda_fail(e);
     if ((rc = record(events, 3, st))) return rc;
     if ((e = launch_combine(W.y, w, keff, ws_ptr<int32_t>(ws, L.pos), d->T, d->H, d->K,
-                            d->I_shared > 0, out, st)) != cudaSuccess)
+                            d->I_shared > 0, resid, out, st)) != cudaSuccess)
         return cuda_fail(e);
     return record(events, 4, st);
 }
@@ -395,6 +428,34 @@ int coli_moe_forward_profiled(const coli_moe_desc *desc, const float *x, const f
     if ((rc = check_device())) return rc;
     return run_forward(desc, x, W_r, bias, experts, shared, out, nullptr, nullptr, ws,
                        reinterpret_cast<cudaStream_t>(stream), events);
+}
+
+int coli_moe_forward_tail(const coli_moe_desc *desc, const float *resid, const float *norm_w, float eps,
+                          const float *W_r, const float *bias, const coli_moe_expert *experts,
+                          const coli_moe_expert *shared, float *out, int32_t *idx_out, float *w_out, void *ws,
+                          size_t ws_bytes, coli_stream_t stream) {
+    int rc = validate_forward(desc, resid, W_r, bias, experts, shared, out, ws, ws_bytes);
+    if (rc) return rc;
+    if (!norm_w || !std::isfinite(eps) || eps < 0.f) return COLI_MOE_EINVAL;
+    if (!aligned(resid, 16) || !aligned(out, 16) || !aligned(norm_w, 16) || (idx_out && !aligned(idx_out, 4)) ||
+        (w_out && !aligned(w_out, 4)))
+        return COLI_MOE_EALIGN;
+    if ((rc = check_device())) return rc;
+    const Tail tail{resid, norm_w, eps};
+    return run_forward(desc, resid, W_r, bias, experts, shared, out, idx_out, w_out, ws,
+                       reinterpret_cast<cudaStream_t>(stream), nullptr, &tail);
+}
+
+int coli_moe_rmsnorm(const float *resid, const float *norm_w, float eps, float *xn, int32_t T, int32_t H,
+                     coli_stream_t stream) {
+    if (!resid || !norm_w || !xn || T < 1 || H < 4 || H > kMaxDim || T > kMaxT || !std::isfinite(eps) || eps < 0.f)
+        return COLI_MOE_EINVAL;
+    if (H % 4) return COLI_MOE_ENOTSUP;
+    if (!aligned(resid, 16) || !aligned(norm_w, 16) || !aligned(xn, 16)) return COLI_MOE_EALIGN;
+    int rc = check_device();
+    if (rc) return rc;
+    cudaError_t e = launch_rmsnorm(resid, norm_w, eps, T, H, xn, reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? COLI_MOE_OK : cuda_fail(e);
 }
 
 int coli_moe_forward_host(const coli_moe_desc *desc, const float *x_host, const float *W_r,

@@ -875,6 +875,7 @@ __global__ void __launch_bounds__(kNT, 2) moe_decode_kernel(const DecParams P) {
         for (int k = 0; k < ke; k++)
             a = __fadd_rn(a, __fmul_rn(rt.w[t * P.K + k], __ldcg(P.y + (size_t)rt.pos[t * P.K + k] * P.H + d)));
         if (P.Is > 0) a = __fadd_rn(a, __ldcg(P.y + ((size_t)P.T * P.K + t) * P.H + d));
+        if (P.resid) a = __fadd_rn(P.resid[(size_t)t * P.H + d], a);  // the layer tail: x += tmp
         P.out[(size_t)t * P.H + d] = a;
     }
 }

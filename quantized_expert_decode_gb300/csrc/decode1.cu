@@ -1,30 +1,30 @@
 // decode1.cu — the whole MoE block for ONE token (T = 1) in one persistent launch.
 //
 // The single-token call is the decode step of the engine (colibri-strix c/glm.c @98759bf
-// moe() with S = 1; the Metal path's moe_gemv). Its work is tiny per CTA — a few row chunks per
-// warp — so the kernel is built around the number of dependent memory round trips rather than
-// around tiling. Phases, split statically over the CTAs (two per SM, cooperative launch):
-//   X  the token's x in 24-bit block fixed point (idot.cuh), staged once per CTA, in the
-//      layout of each weight format the block uses
-//   A  router items: partial logits of 32 experts over one slice of H (r_router shader)
-//   B  shared expert gate/up rows (independent of routing)
+// moe() with S = 1; the Metal path's moe_gemv). Its work is small per CTA, so the kernel is
+// built around the dependent memory round trips between its phases rather than around tiling:
+// every phase issues its independent loads together, and the rows the down phase will read
+// first are asked of L2 before the wait that precedes it. Phases, split statically over the
+// CTAs (two per SM, cooperative launch):
+//   A  router items: partial logits of 32 experts over one slice of H (r_router shader), the
+//      slice's router rows and x in flight together
+//   X  the expert table and the bias copied into shared memory; the token's x in 24-bit block
+//      fixed point (idot.cuh), in the layout of each weight format the block uses
+//   B  shared expert gate/up rows (independent of routing), spread over every CTA
 //   R  routing by EVERY CTA from the partial logits: logits summed in a fixed order, sigmoid,
-//      bias, greedy top-K with ties to the lower index (select.cuh: an expert's place in the
-//      greedy order is the number of experts that beat it, counted over candidates),
-//      TOPK/TOPP, renorm, routed scale. The kept experts become slots 0..U-1 in ascending id
-//      order; the shared expert is slot U. Their weight pointers are loaded by the lanes that
-//      hold them.
-//   C  routed gate/up rows: h = silu(gate.x * s_g) * (up.x * s_u); every CTA also records the
-//      largest |h| of each slot it wrote, the block fixed-point exponent of the down step
-//   D  once every gate/up row is in (one counter): (slot, 4-row group) units split slot-major
-//      over the CTAs, so each stages only the one or two h vectors its units read; y rows
-//      go to the workspace
+//      bias, greedy top-K with ties to the lower index (select.cuh), TOPK/TOPP, renorm, routed
+//      scale. The kept experts become slots 0..U-1 in ascending id order; the shared expert is
+//      slot U. Their weight pointers come from the shared-memory copy of the table.
+//   C  routed gate/up units (rows j of gate and up of one slot): h = silu(gate.x * s_g) *
+//      (up.x * s_u); each CTA keeps the largest |h| of every slot it wrote, the exponent of the
+//      down step's fixed point. A warp that is done asks L2 for the first down rows it will
+//      read; the CTA then raises one counter.
+//   D  once every gate/up unit is in (that counter): (slot, 4-row group) units split
+//      slot-major over the CTAs, so each stages only the one or two h vectors its units read
+//      (h and the slots' maxima in one round trip); y rows go to the workspace
 //   E  once every down row is in (one counter): each CTA's rows of
 //      out[d] = sum_k w_k y[pos_k][d] in selection order, + y[U][d]  (moe() phases C/D/E)
-//      (staging every h vector in every CTA to combine without y was measured slower)
-// Warps walk their gate/up and down units without CTA barriers. (Asking L2 for each phase's
-// rows ahead with cp.async.bulk.prefetch was measured: it slowed large decode by 11 %, so the
-// loads go straight to HBM.) Every wait is bounded.
+// Warps walk their gate/up and down units without CTA barriers. Every wait is bounded.
 #include <algorithm>
 
 #include "decode_parts.cuh"
@@ -41,6 +41,12 @@ struct Rec {  // one expert's weight pointers
 
 constexpr int kShSlot = kMaxK;  // index of the shared expert in rec[] and hmax[]
 constexpr int kInfl1 = 8;       // 16-byte loads in flight per lane in the streaming phases
+constexpr int kRtQ = 4;         // float4 steps per lane and router row held at once
+constexpr int kDnPf = 0;        // down units per warp asked of L2 before the gate/up wait
+constexpr int kHB = 2;          // staged h items (16 elements each) per thread per round trip
+constexpr int kMaxSlices = 16;  // router slices of H per expert block
+constexpr int kGuRows = 4;      // rows per gate/up unit: gate j, up j, gate j + 1, up j + 1 (or 2)
+constexpr bool kOnce = false;   // true: expert rows stream with an evict-first L2 policy
 
 struct D1S {  // the fixed part of the CTA's shared memory
     Rec rec[kMaxK + 1];
@@ -48,14 +54,15 @@ struct D1S {  // the fixed part of the CTA's shared memory
     int pos[kMaxK];     // slot of selection k, -1 beyond keff
     float w[kMaxK];     // kept routing weights, 0 beyond keff
     int sel_i[kMaxK];
-    int ncand, nok;  // selection: candidates, selectable experts
+    int ncand, nok;     // selection: candidates, selectable experts
     int U;
     int xshift;
     float xinv;
-    int hshift[kMaxK + 1];
+    int hshift[kMaxK + 1];  // per slot (shared: at U) in the down phase
     float hinv[kMaxK + 1];
-    int hmax[kMaxK + 1];  // this CTA's max |h| per slot (float bits); shared at kShSlot
+    int hmax[kMaxK + 1];    // this CTA's max |h| per slot (float bits); shared at kShSlot
     float redf[kNW];
+    double redd[kNW];
 };
 
 __device__ __forceinline__ Rec rec_of(const coli_moe_expert &e) {
@@ -67,6 +74,54 @@ __device__ __forceinline__ Rec rec_of(const coli_moe_expert &e) {
     r.us = e.up_s;
     r.ds = e.down_s;
     return r;
+}
+
+
+// A: partial logits of 32 experts (4 per warp) over one slice of H. Each lane holds up to kRtQ
+// float4 steps of the four router rows and of x, so a slice of up to 512 floats is one round
+// trip; the sums run in the same order for every expert (equal rows give equal partials).
+// xsrc: x in global memory, or the normalised row in shared memory (the layer tail)
+__device__ __noinline__ void router_item1(const DecParams &P, int item, const float *xsrc) {
+    const int warp = threadIdx.x / kWarp, lane = threadIdx.x % kWarp;
+    const int eb = item % P.neb, ks = item / P.neb;
+    const int kb = ks * P.rks_floats, ke = min(P.H, kb + P.rks_floats), nq = (ke - kb) / 4;
+    const float *xs = xsrc + kb;
+    const float *wr[4];
+#pragma unroll
+    for (int r = 0; r < 4; r++) wr[r] = P.Wr + (size_t)min(eb * kRtE + warp * 4 + r, P.E - 1) * P.H + kb;
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    const uint64_t pol = policy_evict_first();
+    for (int q0 = 0; q0 < nq; q0 += kWarp * kRtQ) {
+        uint4 wv[4][kRtQ];
+        float4 xv[kRtQ];
+#pragma unroll
+        for (int j = 0; j < kRtQ; j++) {
+            const int q = q0 + lane + kWarp * j;
+            const bool in = q < nq;
+#pragma unroll
+            for (int r = 0; r < 4; r++) wv[r][j] = in ? ld_once_16(wr[r] + 4 * q, pol) : make_uint4(0, 0, 0, 0);
+            xv[j] = in ? reinterpret_cast<const float4 *>(xs)[q] : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int j = 0; j < kRtQ; j++)
+#pragma unroll
+            for (int r = 0; r < 4; r++) {
+                float a = acc[r];
+                a = fmaf(__uint_as_float(wv[r][j].x), xv[j].x, a);
+                a = fmaf(__uint_as_float(wv[r][j].y), xv[j].y, a);
+                a = fmaf(__uint_as_float(wv[r][j].z), xv[j].z, a);
+                a = fmaf(__uint_as_float(wv[r][j].w), xv[j].w, a);
+                acc[r] = a;
+            }
+    }
+#pragma unroll
+    for (int r = 0; r < 4; r++) {
+        float s = acc[r];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(kFull, s, o);
+        const int er = eb * kRtE + warp * 4 + r;
+        if (lane == 0 && er < P.E) P.part[(size_t)ks * P.E + er] = s;
+    }
 }
 
 // X: x -> limbs in the routed layout (and the shared one when it differs). A thread's items
@@ -101,10 +156,10 @@ __device__ __forceinline__ void limbs_from_regs(const float4 (&v)[4], uint8_t *x
 }
 
 template <int RF, int SF>
-__device__ void stage_x(const DecParams &P, uint8_t *xq_r, uint8_t *xq_s, bool two, D1S &m) {
+__device__ void stage_x(const DecParams &P, const float *xsrc, uint8_t *xq_r, uint8_t *xq_s, bool two, D1S &m) {
     const int tid = threadIdx.x, lane = tid % kWarp, warp = tid / kWarp;
     const int n16 = P.H / 16;  // 16-element groups; group q is item q of every layout ordering
-    const float4 *x4 = reinterpret_cast<const float4 *>(P.x);
+    const float4 *x4 = reinterpret_cast<const float4 *>(xsrc);
     const bool in_regs = n16 <= 2 * kNT;
     float4 v[2][4];
     float mx = 0.f;
@@ -114,7 +169,7 @@ __device__ void stage_x(const DecParams &P, uint8_t *xq_r, uint8_t *xq_s, bool t
             const int q = q0 + j * kNT;
             if (q < n16)
 #pragma unroll
-                for (int k = 0; k < 4; k++) v[j][k] = __ldg(x4 + 4 * q + k);
+                for (int k = 0; k < 4; k++) v[j][k] = x4[4 * q + k];
         }
 #pragma unroll
         for (int j = 0; j < 2; j++)
@@ -147,7 +202,7 @@ __device__ void stage_x(const DecParams &P, uint8_t *xq_r, uint8_t *xq_s, bool t
                 const int q = q0 + j * kNT;
                 if (q < n16)
 #pragma unroll
-                    for (int k = 0; k < 4; k++) v[j][k] = __ldg(x4 + 4 * q + k);
+                    for (int k = 0; k < 4; k++) v[j][k] = x4[4 * q + k];
             }
         }
 #pragma unroll
@@ -167,25 +222,59 @@ __device__ void stage_x(const DecParams &P, uint8_t *xq_r, uint8_t *xq_s, bool t
     __syncthreads();
 }
 
+// The layer tail's normalised row, by this CTA into shared memory (xf, H floats):
+// xf = (resid * r) * norm_w with r = 1 / sqrtf(mean square of resid + eps), the squares summed
+// in double (per thread in a fixed stride order, then over the warps in a fixed order), as
+// glm.c's rmsnorm computes the post-attention norm that feeds moe().
+__device__ __noinline__ void stage_xn(const DecParams &P, float *xf, D1S &m) {
+    const int tid = threadIdx.x, lane = tid % kWarp, warp = tid / kWarp;
+    const float4 *r4 = reinterpret_cast<const float4 *>(P.resid);
+    const float4 *w4 = reinterpret_cast<const float4 *>(P.norm_w);
+    double ms = 0.0;
+    for (int q = tid; q < P.H / 4; q += kNT) {
+        const float4 v = __ldg(r4 + q);
+        ms += (double)v.x * v.x;
+        ms += (double)v.y * v.y;
+        ms += (double)v.z * v.z;
+        ms += (double)v.w * v.w;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ms += __shfl_xor_sync(kFull, ms, o);
+    if (lane == 0) m.redd[warp] = ms;
+    __syncthreads();
+    double tot = 0.0;
+#pragma unroll
+    for (int k = 0; k < kNW; k++) tot += m.redd[k];
+    const float r = 1.f / sqrtf((float)(tot / P.H) + P.eps);
+    float4 *o4 = reinterpret_cast<float4 *>(xf);
+    for (int q = tid; q < P.H / 4; q += kNT) {
+        const float4 v = __ldg(r4 + q), g = __ldg(w4 + q);
+        o4[q] = make_float4(v.x * r * g.x, v.y * r * g.y, v.z * r * g.z, v.w * r * g.w);
+    }
+    __syncthreads();
+}
+
 // R: the routing of the token by this CTA (sg/ch: shared scratch of sel_padded(E) floats each,
-// cand: sel_cand_cap(E, Ksel) float2)
-__device__ __noinline__ void route1(const DecParams &P, D1S &m, float *sg, float *ch, float2 *cand) {
+// cand: sel_cand_cap(E, Ksel) float2; bias and tab: the bias and the expert table, in shared
+// memory when they fit). Inlined into the kernel: its code then follows the wait before it.
+__device__ __forceinline__ void route1(const DecParams &P, D1S &m, float *sg, float *ch, float2 *cand,
+                                       const float *bias, const coli_moe_expert *tab) {
     const int tid = threadIdx.x, lane = tid % kWarp, warp = tid / kWarp;
     const bool out = blockIdx.x == 0;
     const int E = P.E, Ep = sel_padded(E);
     // 1. logits (fixed-order sum of the partial slices) -> sigmoid scores and choices
     for (int e = tid; e < Ep; e += kNT) {
         if (e < E) {
-            float a[16];
+            float a[kMaxSlices];
 #pragma unroll
-            for (int k = 0; k < 16; k++)
+            for (int k = 0; k < kMaxSlices; k++)
                 if (k < P.nks) a[k] = __ldcg(P.part + (size_t)k * E + e);
             float lg = 0.f;
 #pragma unroll
-            for (int k = 0; k < 16; k++)
+            for (int k = 0; k < kMaxSlices; k++)
                 if (k < P.nks) lg += a[k];
             const float sv = 1.f / (1.f + expf(-lg));
-            const float cv = sv + __ldg(P.bias + e);
+            const float cv = sv + bias[e];
             sg[e] = sv;
             ch[e] = cv;
             if (out) {
@@ -209,10 +298,9 @@ __device__ __noinline__ void route1(const DecParams &P, D1S &m, float *sg, float
         const int pick = lane < nsel ? m.sel_i[lane] : -1;
         const SelKept kp = sel_finish_warp(nsel, pick, lane < nsel ? sg[pick] : 0.f, P.top_p, P.norm_topk, P.rscale);
         const int Ke = kp.ke, id = kp.id;
-        // each kept lane asks for its expert's weight pointers
-        coli_moe_expert ex{};
-        if (lane < Ke) ex = P.experts[id];
         const bool kept = lane < Ke;
+        coli_moe_expert ex{};
+        if (kept) ex = tab[id];
         int slot = 0;
         for (int k = 0; k < Ke; k++) slot += __shfl_sync(kFull, id, k) < id;
         if (lane < K) {
@@ -257,54 +345,84 @@ __device__ __noinline__ void route1(const DecParams &P, D1S &m, float *sg, float
 }
 
 // B / C: gate/up units [b, e) (shared: the shared expert's, else slot-major over the routed
-// slots), each two rows j, j+1 of gate and of up; warps take units round-robin, no barriers
+// slots; kGuRows / 2 row pairs j, j + 1 .. of gate and of up per unit); warps take units
+// round-robin, no barriers
+// (warps wfirst .. wfirst + wcount - 1 of the CTA take part)
 template <int FMT>
-__device__ __noinline__ void gateup_run(const DecParams &P, D1S &m, const uint8_t *xq, int b, int e, bool shared) {
-    const int warp = threadIdx.x / kWarp, lane = threadIdx.x % kWarp;
+__device__ __noinline__ void gateup_run(const DecParams &P, D1S &m, const uint8_t *xq, int b, int e, bool shared,
+                                        int wfirst = 0, int wcount = kNW) {
+    constexpr int NP = kGuRows / 2;  // row pairs per unit
+    const int warp = threadIdx.x / kWarp - wfirst, lane = threadIdx.x % kWarp;
     const int nu = e - b;
-    const int mine = nu > warp ? (nu - warp + kNW - 1) / kNW : 0;
+    const int mine = nu > warp ? (nu - warp + wcount - 1) / wcount : 0;
     const int inter = shared ? P.Is : P.I;
-    const int per = (inter + 1) / 2;
+    const int per = (inter + NP - 1) / NP;  // units per slot
     const int64_t rb = row_bytes(FMT, P.H);
     const float xinv = m.xinv;
     auto unit = [&](int i, int &slot, int &j) {
-        const int l = b + warp + kNW * i;
+        const int l = b + warp + wcount * i;
         slot = shared ? kShSlot : l / per;
-        j = 2 * (shared ? l : l - slot * per);
+        j = NP * (shared ? l : l - slot * per);
     };
-    warp_stream_int<FMT, 4, kInfl1>(
+    warp_stream_int<FMT, kGuRows, kInfl1, kOnce>(
         mine, (int)(rb / 16), lane,
-        [&](int i, const uint8_t *(&rr)[4]) {
+        [&](int i, const uint8_t *(&rr)[kGuRows]) {
             int slot, j;
             unit(i, slot, j);
             const Rec &r = m.rec[slot];
-            const int j1 = min(j + 1, inter - 1);
-            rr[0] = r.gw + (size_t)j * rb;
-            rr[1] = r.uw + (size_t)j * rb;
-            rr[2] = r.gw + (size_t)j1 * rb;
-            rr[3] = r.uw + (size_t)j1 * rb;
+#pragma unroll
+            for (int q = 0; q < NP; q++) {
+                const int jq = min(j + q, inter - 1);
+                rr[2 * q] = r.gw + (size_t)jq * rb;
+                rr[2 * q + 1] = r.uw + (size_t)jq * rb;
+            }
         },
         [&](int) { return reinterpret_cast<const uint4 *>(xq); },
-        [&](int i) {  // lanes 0 and 16: the scales of rows j and j + 1
+        [&](int i) {  // lane 16 q: the scales of gate row and up row j + q
             int slot, j;
             unit(i, slot, j);
             const Rec &r = m.rec[slot];
-            const int jq = min(j + (lane >> 4), inter - 1);
-            return (lane & 15) == 0 ? make_float2(__ldg(r.gs + jq), __ldg(r.us + jq)) : make_float2(0.f, 0.f);
+            const int jq = min(j + (NP > 1 ? lane >> 4 : 0), inter - 1);
+            const bool ld = NP > 1 ? (lane & 15) == 0 : lane == 0;
+            return ld ? make_float2(__ldg(r.gs + jq), __ldg(r.us + jq)) : make_float2(0.f, 0.f);
         },
-        [&](int i, long long tot, float2 sc) {  // lanes 0 / 16 hold gate j / j+1, lanes 8 / 24 up
-            const long long up = __shfl_down_sync(kFull, tot, 8);
+        [&](int i, long long tot, float2 sc) {
+            // 2 rows: lanes 0-15 hold gate j, 16-31 up j; 4 rows: lanes 8 r hold row r of
+            // (gate j, up j, gate j + 1, up j + 1)
+            constexpr int UPD = kGuRows == 2 ? 16 : 8;
+            const long long up = __shfl_down_sync(kFull, tot, UPD);
             int slot, j;
             unit(i, slot, j);
-            const int jq = j + (lane >> 4);
-            if ((lane & 15) == 0 && jq < inter) {
+            const int q = kGuRows == 2 ? 0 : (lane >> 4);
+            const bool mine_row = kGuRows == 2 ? lane == 0 : (lane & 15) == 0;
+            if (mine_row && j + q < inter) {
                 const float gv = (__ll2float_rn(tot) * xinv) * sc.x;
                 const float uv = (__ll2float_rn(up) * xinv) * sc.y;
                 const float hv = gv / (1.f + expf(-gv)) * uv;
-                P.h[(size_t)(shared ? P.K : slot) * P.ldh + jq] = hv;
+                P.h[(size_t)(shared ? P.K : slot) * P.ldh + j + q] = hv;
                 atomicMax(&m.hmax[slot], __float_as_int(fabsf(hv)));
             }
         });
+}
+
+// the rows of a warp's first down units (slot-major units [db, de) of the grid, unit l: slot
+// l / ngr, rows 4 (l % ngr) .. + 3), asked of L2; the gate/up rows stream with an evict-first
+// policy, so these lines stay until they are read
+__device__ void prefetch_down(const DecParams &P, const D1S &m, int db, int de, int ngr) {
+    const int warp = threadIdx.x / kWarp, lane = threadIdx.x % kWarp;
+    for (int i = 0; i < kDnPf; i++) {
+        const int l = db + warp + kNW * i;
+        if (l >= de) break;
+        const int slot = l / ngr, grp = l - slot * ngr;
+        const bool sh = slot == m.U;
+        const int64_t rb = row_bytes(sh ? P.sfmt : P.rfmt, sh ? P.Is : P.I);
+        const uint8_t *base = m.rec[sh ? kShSlot : slot].dw;
+        const int nl = (int)((rb + 127) / 128);  // lines per row
+        for (int q = lane; q < 4 * nl; q += kWarp) {
+            const int d = min(4 * grp + q / nl, P.H - 1);
+            prefetch_line_l2(base + (size_t)d * rb + 128 * (q % nl));
+        }
+    }
 }
 
 // D: down units [lo, hi) of the slot-major space (unit l: slot l / ngr, rows 4 (l % ngr) .. +3);
@@ -325,7 +443,7 @@ __device__ __noinline__ void down_run(const DecParams &P, D1S &m, const uint8_t 
         slot = l / ngr;
         grp = l - slot * ngr;
     };
-    warp_stream_int<FMT, 4, kInfl1>(
+    warp_stream_int<FMT, 4, kInfl1, kOnce>(
         mine, (int)(rb / 16), lane,
         [&](int i, const uint8_t *(&rr)[4]) {
             int slot, grp;
@@ -350,8 +468,66 @@ __device__ __noinline__ void down_run(const DecParams &P, D1S &m, const uint8_t 
             unit(i, slot, grp);
             const int d = 4 * grp + (lane >> 3);
             if ((lane & 7) == 0 && d < P.H)
-                P.y[(size_t)(sh ? P.K : slot) * P.H + d] = (__ll2float_rn(tot) * m.hinv[slot - s0]) * sc;
+                P.y[(size_t)(slot == m.U ? P.K : slot) * P.H + d] = (__ll2float_rn(tot) * m.hinv[slot - s0]) * sc;
         });
+}
+
+// D: the h vectors of slots s0 .. s0 + ns - 1 as limbs (slot s0 + j at act + j * hs, in the
+// routed layout, or the shared one for slot U), each in block fixed point from the largest |h|
+// of the slot over all CTAs. A thread loads up to kHB 16-element items while threads below ns
+// read the slots' maxima: one round trip for the usual one or two vectors.
+template <int RF, int SF>
+__device__ void stage_h(const DecParams &P, D1S &m, uint8_t *act, int hs, int s0, int ns) {
+    const int tid = threadIdx.x;
+    const int U = m.U;
+    const int items_r = limb_items<RF>(P.I), items_s = P.Is > 0 ? limb_items<SF>(P.Is) : 0;
+    const int cpr_r = P.I / QGeom<RF>::EPC, cpr_s = P.Is > 0 ? P.Is / QGeom<SF>::EPC : 1;
+    // items of staged vector j start at ib[j]
+    int total = 0;
+    for (int j = 0; j < ns; j++) total += s0 + j < U ? items_r : items_s;
+    for (int b0 = 0; b0 < total; b0 += kNT * kHB) {
+        float4 v[kHB][4];
+        int jv[kHB], pv[kHB];
+#pragma unroll
+        for (int k = 0; k < kHB; k++) {
+            int i = b0 + tid + kNT * k;
+            jv[k] = -1;
+            if (i < total) {
+                int j = 0;
+                while (true) {  // at most kMaxK + 1 vectors, usually one or two
+                    const int n = s0 + j < U ? items_r : items_s;
+                    if (i < n) break;
+                    i -= n;
+                    j++;
+                }
+                const int u = s0 + j;
+                const bool rt = u < U;
+                const int cpr = rt ? cpr_r : cpr_s, epc = rt ? QGeom<RF>::EPC : QGeom<SF>::EPC;
+                const int c = i % cpr, ss = i / cpr;
+                const float4 *src = reinterpret_cast<const float4 *>(P.h + (size_t)(rt ? u : P.K) * P.ldh + c * epc + ss * 16);
+#pragma unroll
+                for (int q = 0; q < 4; q++) v[k][q] = __ldcg(src + q);
+                jv[k] = j;
+                pv[k] = i;
+            }
+        }
+        if (b0 == 0 && tid < ns) {  // the exponent of each staged slot, read while the items are in flight
+            const int u = s0 + tid;
+            const int sh = fixed_shift(__int_as_float(__ldcg(&P.ctrl->hmax[u < U ? u : kShSlot])));
+            m.hshift[tid] = sh;
+            m.hinv[tid] = ldexpf(1.f, -sh);
+        }
+        __syncthreads();
+#pragma unroll
+        for (int k = 0; k < kHB; k++) {
+            if (jv[k] >= 0) {
+                const FixedScale fx(m.hshift[jv[k]]);
+                if (s0 + jv[k] < U) limbs_from_regs<RF>(v[k], act + (size_t)jv[k] * hs, cpr_r, pv[k], fx);
+                else limbs_from_regs<SF>(v[k], act + (size_t)jv[k] * hs, cpr_s, pv[k], fx);
+            }
+        }
+    }
+    __syncthreads();
 }
 
 template <int RF, int SF>
@@ -365,7 +541,6 @@ __global__ void __launch_bounds__(kNT, 2) moe_decode1_kernel(const DecParams P) 
     const int tid = threadIdx.x, G = gridDim.x, c = blockIdx.x;
     const bool two = P.Is > 0 && SF != RF;
     uint8_t *xq_r = act, *xq_s = two ? act + 3 * P.H : act;
-    const int GUPER = (P.I + 1) / 2;
 
     if (tid <= kMaxK) m.hmax[tid] = 0;
     if (tid == 0 && P.Is > 0) m.rec[kShSlot] = rec_of(P.shared);
@@ -398,24 +573,21 @@ __global__ void __launch_bounds__(kNT, 2) moe_decode1_kernel(const DecParams P) 
         }
         __threadfence();
     };
+    // the shared expert's gate/up units, spread over every CTA
+    const int bb = range_lo(P.G_sh, c, G), be = range_lo(P.G_sh, c + 1, G);
     __syncthreads();
-    // the shared expert's gate/up goes to the CTAs without a router item, so that every CTA
-    // reaches the routing wait at about the same time
-    const int nb = G - P.R > 0 ? G - P.R : G, cb0 = G - P.R > 0 ? c - P.R : c;
-    const int bb = cb0 < 0 ? 0 : range_lo(P.G_sh, cb0, nb), be = cb0 < 0 ? 0 : range_lo(P.G_sh, cb0 + 1, nb);
-    // routing reads the bias and the expert table right after its wait: warm them in L2
-    {
-        const int lb = (P.E * 4 + 127) / 128, lt = (P.E * (int)sizeof(coli_moe_expert) + 127) / 128;
-        const int per = (lb + lt + G - 1) / G;
-        for (int i = c * per + tid; i < min(lb + lt, (c + 1) * per) && tid < per; i += kNT) {
-            if (i < lb) prefetch_line_l2(reinterpret_cast<const uint8_t *>(P.bias) + 128 * i);
-            else prefetch_line_l2(reinterpret_cast<const uint8_t *>(P.experts) + 128 * (i - lb));
-        }
+
+    // the layer tail normalises resid into shared memory first; else x is read where it is
+    const float *xsrc = P.x;
+    if (P.resid) {
+        float *xf = reinterpret_cast<float *>(smem + P.d1_xf_off);
+        stage_xn(P, xf, m);
+        xsrc = xf;
     }
 
     // ---------------- A: router partial logits
     if (c < P.R) {
-        router_item<1>(P, c);
+        router_item1(P, c, xsrc);
         __syncthreads();
         if (tid == 0) {
             await_call();
@@ -423,8 +595,41 @@ __global__ void __launch_bounds__(kNT, 2) moe_decode1_kernel(const DecParams P) 
             atomicAdd(&P.ctrl->router_done, 1);
         }
     }
-    // ---------------- X, then B: the shared expert's gate/up
-    stage_x<RF, SF>(P, xq_r, xq_s, two, m);
+    // ---------------- X: the expert table and the bias into shared memory, then x as limbs
+    // (read by routing only, after the barriers below). A thread's share of the copy is held in
+    // registers while x loads, so the two share one round trip; a table too large for that is
+    // copied first.
+    const float *bias_s = P.bias;
+    const coli_moe_expert *tab_s = P.experts;
+    constexpr int kTabRegs = 8;  // 8-byte table words per thread held across the x staging
+    const int n8 = P.E * (int)(sizeof(coli_moe_expert) / 8);
+    uint2 *ts = reinterpret_cast<uint2 *>(smem + P.d1_tab_off);
+    float *bs = reinterpret_cast<float *>(smem + P.d1_bias_off);
+    const uint2 *tg = reinterpret_cast<const uint2 *>(P.experts);
+    const bool tab_regs = P.d1_tab_off > 0 && n8 <= kTabRegs * kNT && P.E <= kNT;
+    uint2 tv[kTabRegs];
+    float bv = 0.f;
+    if (tab_regs) {
+#pragma unroll
+        for (int k = 0; k < kTabRegs; k++)
+            if (tid + k * kNT < n8) tv[k] = __ldg(tg + tid + k * kNT);
+        if (tid < P.E) bv = __ldg(P.bias + tid);
+    } else if (P.d1_tab_off > 0) {
+        for (int i = tid; i < n8; i += kNT) ts[i] = __ldg(tg + i);
+        for (int i = tid; i < P.E; i += kNT) bs[i] = __ldg(P.bias + i);
+    }
+    if (P.d1_tab_off > 0) {
+        bias_s = bs;
+        tab_s = reinterpret_cast<const coli_moe_expert *>(ts);
+    }
+    stage_x<RF, SF>(P, xsrc, xq_r, xq_s, two, m);
+    if (tab_regs) {
+#pragma unroll
+        for (int k = 0; k < kTabRegs; k++)
+            if (tid + k * kNT < n8) ts[tid + k * kNT] = tv[k];
+        if (tid < P.E) bs[tid] = bv;
+    }
+    // ---------------- B: the shared expert's gate/up
     if (be > bb) gateup_run<SF>(P, m, xq_s, bb, be, true);
 
     // ---------------- R: routing
@@ -434,13 +639,18 @@ __global__ void __launch_bounds__(kNT, 2) moe_decode1_kernel(const DecParams P) 
         __threadfence();
     }
     __syncthreads();
-    route1(P, m, rsg, rch, rcand);
+    route1(P, m, rsg, rch, rcand, bias_s, tab_s);
     const int U = m.U;
+    const int nsl = U + (P.Is > 0 ? 1 : 0);
+    const int ngr = (P.H + 3) / 4, ND = nsl * ngr;
+    const int db = range_lo(ND, c, G), de = range_lo(ND, c + 1, G);
 
-    // ---------------- C: routed gate/up
-    const int gu_tot = U * GUPER;
+    // ---------------- C: routed gate/up, then the first down rows asked of L2
+    const int gu_per = (P.I + kGuRows / 2 - 1) / (kGuRows / 2);  // units per routed slot
+    const int gu_tot = U * gu_per;
     const int cb = range_lo(gu_tot, c, G), ce = range_lo(gu_tot, c + 1, G);
     gateup_run<RF>(P, m, xq_r, cb, ce, false);
+    prefetch_down(P, m, db, de, ngr);
     __syncthreads();
     if (tid < U || (tid == kShSlot && P.Is > 0))
         if (m.hmax[tid] != 0) atomicMax(&P.ctrl->hmax[tid], m.hmax[tid]);
@@ -450,32 +660,15 @@ __global__ void __launch_bounds__(kNT, 2) moe_decode1_kernel(const DecParams P) 
         atomicAdd(&P.ctrl->gu_all, (be - bb) + (ce - cb));
     }
 
-    // ---------------- D: down rows, (slot, 4-row group) units split slot-major over the CTAs, so
-    // a CTA stages only the one or two h vectors its units read
+    // ---------------- D: down rows, (slot, 4-row group) units split slot-major over the CTAs
     if (tid == 0) {
         wait_at_least(&P.ctrl->gu_all, P.G_sh + gu_tot, P.ctrl);
         __threadfence();
     }
     __syncthreads();
-    const int nsl = U + (P.Is > 0 ? 1 : 0);
-    const int ngr = P.H / 4, ND = nsl * ngr;
-    const int db = range_lo(ND, c, G), de = range_lo(ND, c + 1, G);
     const int s0 = db / ngr, ns = de > db ? (de - 1) / ngr - s0 + 1 : 0;
-    const int hs = 3 * (P.I > P.Is ? P.I : P.Is);  // staged bytes per h vector
-    if (tid < ns) {
-        const int u = s0 + tid;
-        const int s = fixed_shift(__int_as_float(__ldcg(&P.ctrl->hmax[u < U ? u : kShSlot])));
-        m.hshift[tid] = s;
-        m.hinv[tid] = ldexpf(1.f, -s);
-    }
-    __syncthreads();
-    for (int j = 0; j < ns; j++) {
-        const int u = s0 + j;
-        const FixedScale fx(m.hshift[j]);
-        if (u < U) stage_limbs_vec<RF>(P.h + (size_t)u * P.ldh, P.I, true, act + (size_t)j * hs, fx, tid, kNT);
-        else stage_limbs_vec<SF>(P.h + (size_t)P.K * P.ldh, P.Is, true, act + (size_t)j * hs, fx, tid, kNT);
-    }
-    __syncthreads();
+    const int hs = P.d1_hs;
+    stage_h<RF, SF>(P, m, act, hs, s0, ns);
     {
         const int split = U * ngr;  // routed units below, shared units from here
         const int rlo = db, rhi = min(de, split), slo = max(db, split), shi = de;
@@ -510,6 +703,7 @@ __global__ void __launch_bounds__(kNT, 2) moe_decode1_kernel(const DecParams P) 
             for (int k = 0; k <= kMaxK; k++)
                 if (k == U) a = __fadd_rn(a, yv[k]);
         }
+        if (P.resid) a = __fadd_rn(P.resid[d], a);  // the layer tail: x += tmp
         P.out[d] = a;
     }
 }
@@ -529,7 +723,7 @@ KernelFn kernel_for(int rf, int sf) {
     return table[pick(rf)][pick(sf)];
 }
 
-size_t decode1_smem_bytes(const DecParams &P) { return (size_t)P.d1_y_off; }
+size_t decode1_smem_bytes(const DecParams &P) { return (size_t)P.d1_end; }
 
 }  // namespace
 
@@ -544,23 +738,46 @@ bool decode1_plan(const coli_moe_desc &d, DecParams &P, int grid) {
     P.route_only = 0;
     P.neb = (d.E + kRtE - 1) / kRtE;
     const int max_slices = std::max(1, d.H / 128);
-    int nks = std::max(1, std::min({grid / P.neb, max_slices, 16}));
+    int nks = std::max(1, std::min({grid / P.neb, max_slices, kMaxSlices}));
     P.rks_floats = (d.H / nks + 3) / 4 * 4;
     nks = (d.H + P.rks_floats - 1) / P.rks_floats;
     P.nks = nks;
     P.R = P.neb * nks;
     if (P.R > grid) return false;
     P.groups_sh = d.I_shared > 0 ? 1 : 0;
-    P.G_sh = d.I_shared > 0 ? (d.I_shared + 1) / 2 : 0;
+    P.G_sh = d.I_shared > 0 ? (d.I_shared + kGuRows / 2 - 1) / (kGuRows / 2) : 0;  // shared gate/up units
     const bool two = d.I_shared > 0 && d.shared_fmt != d.routed_fmt;
     const size_t x_bytes = (size_t)3 * d.H * (two ? 2 : 1);
-    const size_t h_bytes = (size_t)3 * (d.K + 1) * std::max(d.I, d.I_shared);
-    P.d1_act_off = (int)align_up(sizeof(D1S), 128);
-    P.d1_rsc_off = P.d1_act_off + (int)align_up(std::max(x_bytes, h_bytes), 128);
+    P.d1_hs = 3 * std::max(d.I, d.I_shared);  // limbs of one staged h vector (a multiple of 16)
+    // the slots one CTA's down units can touch: its share of (K + 1) * ngr units over `grid`
+    const int ngr = (d.H + 3) / 4;
+    const int share = ((d.K + 1) * ngr + grid - 1) / grid;
+    const int ns_max = std::min(d.K + 1, (share + ngr - 1) / ngr + 1);
+    const size_t h_bytes = (size_t)P.d1_hs * ns_max;
     const int ksel = (d.ksel > 0 && d.ksel < d.K) ? d.ksel : d.K;
     const size_t sel_bytes = (size_t)2 * sel_padded(d.E) * 4 + (size_t)sel_cand_cap(d.E, ksel) * 8;
-    P.d1_y_off = P.d1_rsc_off + (int)align_up(sel_bytes, 128);  // end of smem
-    P.d1_rows = 0;
+    size_t o = align_up(sizeof(D1S), 128);
+    P.d1_act_off = (int)o;
+    o += align_up(std::max(x_bytes, h_bytes), 128);
+    P.d1_rsc_off = (int)o;
+    o += align_up(sel_bytes, 128);
+    P.d1_ylo_off = 0;
+    P.d1_pairs = 0;
+    // the expert table and the bias in shared memory when they are small
+    const size_t tab_bytes = (size_t)d.E * sizeof(coli_moe_expert);
+    if (tab_bytes + (size_t)d.E * 4 <= 32 * 1024) {
+        P.d1_tab_off = (int)o;
+        o += align_up(tab_bytes, 128);
+        P.d1_bias_off = (int)o;
+        o += align_up((size_t)d.E * 4, 128);
+    } else {
+        P.d1_tab_off = P.d1_bias_off = 0;
+    }
+    // the layer tail's normalised row (H floats), reserved by every plan: the kernel reads it
+    // only when it is given a residual
+    P.d1_xf_off = (int)o;
+    o += align_up((size_t)d.H * 4, 128);
+    P.d1_end = (int)o;
     return decode1_smem_bytes(P) <= 113u * 1024;
 }
 

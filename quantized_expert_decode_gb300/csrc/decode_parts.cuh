@@ -40,19 +40,35 @@ __device__ __forceinline__ int range_lo(int n, int c, int G) { return (int)((lon
 
 __device__ __forceinline__ bool bad16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) != 0; }
 
+// weight rows read once per call can be streamed with an evict-first L2 policy, so that they do
+// not push out lines that were asked of L2 ahead of their use
+__device__ __forceinline__ uint64_t policy_evict_first() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+__device__ __forceinline__ uint4 ld_once_16(const void *p, uint64_t pol) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.L2::256B.v4.u32 {%0,%1,%2,%3}, [%4], %5;"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p), "l"(pol));
+    return v;
+}
+
 // ------------------------------------------------------------------ the streaming cores
-// Single-token groups on the integer core (idot.cuh), four rows per unit. One warp streams
-// `nunits` units of NR packed rows (CPR 16-byte chunks per row), lane l taking chunks l, l+32,
-// ... of every row, with INFL / NR chunk-steps of loads in flight across unit boundaries;
-// rows_of(i, rows) gives unit i's row pointers;
+// Single-token groups on the integer core (idot.cuh), four or two rows per unit. One warp
+// streams `nunits` units of NR packed rows (CPR 16-byte chunks per row), lane l taking chunks
+// l, l+32, ... of every row, with INFL / NR chunk-steps of loads in flight across unit
+// boundaries; rows_of(i, rows) gives unit i's row pointers;
 // xq_of(i) gives the staged activation limbs unit i is dotted with; epi(i, tot, d) gets, in
-// lane l, the exact warp total S of row l / 8 of unit i, and d = pre(i), the unit's epilogue
-// operands (row scales), which are loaded two units ahead.
-template <int FMT, int NR, int INFL = kInflight, class RowsOf, class XqOf, class Pre, class Epi>
+// lane l, the exact warp total S of row l / (32 / NR) of unit i, and d = pre(i), the unit's
+// epilogue operands (row scales), which are loaded two units ahead.
+template <int FMT, int NR, int INFL = kInflight, bool ONCE = false, class RowsOf, class XqOf, class Pre, class Epi>
 __device__ __forceinline__ void warp_stream_int(int nunits, int CPR, int lane, RowsOf rows_of, XqOf xq_of, Pre pre,
                                                 Epi epi) {
     constexpr int kDepth = INFL / NR;
     if (nunits <= 0) return;
+    const uint64_t pol = ONCE ? policy_evict_first() : 0;  // ONCE: the rows are read once (evict first)
     const int S = (CPR + kWarp - 1) / kWarp;
     const int total = nunits * S;
     uint4 buf[kDepth][NR];
@@ -63,7 +79,9 @@ __device__ __forceinline__ void warp_stream_int(int nunits, int CPR, int lane, R
         if (iu < nunits) {
             const int c = lane + kWarp * ik;
 #pragma unroll
-            for (int r = 0; r < NR; r++) b[r] = c < CPR ? ld_stream_16(rr[r] + 16 * c) : make_uint4(0, 0, 0, 0);
+            for (int r = 0; r < NR; r++)
+                b[r] = c < CPR ? (ONCE ? ld_once_16(rr[r] + 16 * c, pol) : ld_stream_16(rr[r] + 16 * c))
+                               : make_uint4(0, 0, 0, 0);
             if (++ik == S) {
                 ik = 0;
                 if (++iu < nunits) rows_of(iu, rr);
@@ -88,8 +106,9 @@ __device__ __forceinline__ void warp_stream_int(int nunits, int CPR, int lane, R
                 if (c < CPR) idot_chunk<FMT, NR>(buf[j], xq4, CPR, c, acc);
                 issue(buf[j]);
                 if (++ck == S) {
-                    static_assert(NR == 4, "the integer walk reduces four rows per unit");
-                    epi(cu, idot_reduce4<FMT>(acc, lane), d0);
+                    static_assert(NR == 4 || NR == 2, "the integer walk reduces four or two rows per unit");
+                    if constexpr (NR == 4) epi(cu, idot_reduce4<FMT>(acc, lane), d0);
+                    else epi(cu, idot_reduce2<FMT>(acc, lane), d0);
                     d0 = d1;
                     if (cu + 2 < nunits) d1 = pre(cu + 2);
 #pragma unroll

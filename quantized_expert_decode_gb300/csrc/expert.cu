@@ -428,7 +428,7 @@ cudaError_t launch_down(const ExpertWork &w, cudaStream_t st) {
 __global__ void __launch_bounds__(256)
 combine_kernel(const float *__restrict__ y, const float *__restrict__ wts,
                const int32_t *__restrict__ keff, const int32_t *__restrict__ pos, int T, int H,
-               int K, int has_shared, float *__restrict__ out) {
+               int K, int has_shared, const float *resid, float *out) {
     const int t = blockIdx.y;
     const int d = 4 * (blockIdx.x * blockDim.x + threadIdx.x);
     if (d >= H) return;
@@ -449,14 +449,57 @@ combine_kernel(const float *__restrict__ y, const float *__restrict__ wts,
         acc.z = __fadd_rn(acc.z, v.z);
         acc.w = __fadd_rn(acc.w, v.w);
     }
+    if (resid) {  // the layer tail: the residual plus the block (x += tmp)
+        const float4 r = *reinterpret_cast<const float4 *>(resid + (size_t)t * H + d);
+        acc = make_float4(__fadd_rn(r.x, acc.x), __fadd_rn(r.y, acc.y), __fadd_rn(r.z, acc.z), __fadd_rn(r.w, acc.w));
+    }
     *reinterpret_cast<float4 *>(out + (size_t)t * H + d) = acc;
 }
 
 cudaError_t launch_combine(const float *y, const float *wts, const int32_t *keff,
-                           const int32_t *pos, int T, int H, int K, int has_shared, float *out,
-                           cudaStream_t st) {
+                           const int32_t *pos, int T, int H, int K, int has_shared, const float *resid,
+                           float *out, cudaStream_t st) {
     dim3 grid((H / 4 + 255) / 256, T);
-    combine_kernel<<<grid, 256, 0, st>>>(y, wts, keff, pos, T, H, K, has_shared, out);
+    combine_kernel<<<grid, 256, 0, st>>>(y, wts, keff, pos, T, H, K, has_shared, resid, out);
+    return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------- RMS normalisation of the rows
+// xn[t] = (resid[t] * r_t) * w with r_t = 1 / sqrtf(mean square of resid[t] + eps), the mean
+// square summed in double (colibri-strix c/glm.c @98759bf rmsnorm, applied with the post-attention
+// norm before moe() in the layer forward). One CTA per row; the squares are summed per thread in
+// a fixed stride order, then over the warps in a fixed order.
+__global__ void __launch_bounds__(256) rmsnorm_rows_kernel(const float *__restrict__ resid, const float *__restrict__ w,
+                                                           float eps, int H, float *__restrict__ xn) {
+    __shared__ double red[8];
+    const int t = blockIdx.x, tid = threadIdx.x, lane = tid % kWarp, warp = tid / kWarp;
+    const float4 *r4 = reinterpret_cast<const float4 *>(resid + (size_t)t * H);
+    double ms = 0.0;
+    for (int q = tid; q < H / 4; q += 256) {
+        const float4 v = r4[q];
+        ms += (double)v.x * v.x;
+        ms += (double)v.y * v.y;
+        ms += (double)v.z * v.z;
+        ms += (double)v.w * v.w;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ms += __shfl_xor_sync(kFull, ms, o);
+    if (lane == 0) red[warp] = ms;
+    __syncthreads();
+    double tot = 0.0;
+#pragma unroll
+    for (int k = 0; k < 8; k++) tot += red[k];
+    const float r = 1.f / sqrtf((float)(tot / H) + eps);
+    const float4 *w4 = reinterpret_cast<const float4 *>(w);
+    float4 *o4 = reinterpret_cast<float4 *>(xn + (size_t)t * H);
+    for (int q = tid; q < H / 4; q += 256) {
+        const float4 v = r4[q], g = w4[q];
+        o4[q] = make_float4(v.x * r * g.x, v.y * r * g.y, v.z * r * g.z, v.w * r * g.w);
+    }
+}
+
+cudaError_t launch_rmsnorm(const float *resid, const float *w, float eps, int T, int H, float *xn, cudaStream_t st) {
+    rmsnorm_rows_kernel<<<T, 256, 0, st>>>(resid, w, eps, H, xn);
     return cudaGetLastError();
 }
 

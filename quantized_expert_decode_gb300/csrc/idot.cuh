@@ -119,6 +119,26 @@ __device__ __forceinline__ long long idot_reduce4(const int (&acc)[4][3], int la
     return k;
 }
 
+// Two rows: the lane halves split the rows, then a butterfly over the half; every lane ends
+// with the exact total of row lane / 16.
+template <int FMT>
+__device__ __forceinline__ long long idot_reduce2(const int (&acc)[2][3], int lane) {
+    constexpr int LS = IQ<FMT>::LOG_SC;
+    long long p[2];
+#pragma unroll
+    for (int r = 0; r < 2; r++)
+        p[r] = ((long long)(acc[r][2] >> LS) << 16) + ((long long)(acc[r][1] >> LS) << 8) +
+               (long long)(acc[r][0] >> LS);
+    const bool h16 = (lane & 16) != 0;
+    long long k = h16 ? p[1] : p[0];
+    k += __shfl_xor_sync(kFull, h16 ? p[0] : p[1], 16);
+    k += __shfl_xor_sync(kFull, k, 8);
+    k += __shfl_xor_sync(kFull, k, 4);
+    k += __shfl_xor_sync(kFull, k, 2);
+    k += __shfl_xor_sync(kFull, k, 1);
+    return k;
+}
+
 // the shift s of a vector whose largest magnitude is mx (0 for an all-zero vector)
 __device__ __forceinline__ int fixed_shift(float mx) {
     if (!(mx > 0.f)) return 0;

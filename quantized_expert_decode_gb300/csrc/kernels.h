@@ -42,6 +42,10 @@ struct DecCtrl {
 
 struct DecParams {
     const float *x, *Wr, *bias;
+    // the layer tail: out = resid + block; the single-token kernel also normalises resid itself
+    // (x = rmsnorm(resid) * norm_w); the other kernels take x already normalised
+    const float *resid, *norm_w;
+    float eps;
     const coli_moe_expert *experts;
     coli_moe_expert shared;
     float *out;
@@ -57,8 +61,10 @@ struct DecParams {
     int R, route_only;         // router items; route_only: logits come from a separate launch
     int neb, nks, rks_floats;  // router expert blocks, k-slices, floats per k-slice
     int groups_sh, G_sh;       // shared expert token groups and gate/up units
-    // single-token kernel (decode1.cu): shared-memory offsets and output rows per CTA
-    int single, d1_act_off, d1_rsc_off, d1_y_off, d1_rows;
+    // single-token kernel (decode1.cu): shared-memory offsets (activation limbs, routing
+    // scratch, per-CTA down results, expert table, bias, end), the bytes of one slot's staged h,
+    // and the row pairs of the down phase per CTA at most
+    int single, d1_act_off, d1_rsc_off, d1_ylo_off, d1_tab_off, d1_bias_off, d1_xf_off, d1_end, d1_hs, d1_pairs;
     unsigned long long call_id;  // single-token kernel: unique per call (counters reset in-kernel)
 };
 
@@ -79,7 +85,8 @@ struct PrefillWork {
     coli_moe_expert shared;
     const float *x;
     const int32_t *counts, *offsets, *perm;
-    uint16_t *xb, *hb;               // bf16 activations / h (block-permuted K order)
+    uint16_t *xb, *hb;               // f16 activations (row p scaled by 2^xe[p]) / bf16 h (block-permuted K order)
+    int32_t *xe;                     // [T*K + T] exponents of the activation rows' scales
     float *y;
     int32_t *err;
     int T, H, I, E, K, I_shared, routed_fmt, shared_fmt, ldh, grid;
@@ -102,9 +109,12 @@ cudaError_t launch_bucket(const int32_t *idx, const int32_t *keff, int T, int K,
 // expert.cu
 cudaError_t launch_gateup(const ExpertWork &w, cudaStream_t s);
 cudaError_t launch_down(const ExpertWork &w, cudaStream_t s);
+// resid: the layer tail's residual added to the block (NULL: the block alone)
 cudaError_t launch_combine(const float *y, const float *wts, const int32_t *keff,
-                           const int32_t *pos, int T, int H, int K, int has_shared, float *out,
-                           cudaStream_t s);
+                           const int32_t *pos, int T, int H, int K, int has_shared, const float *resid,
+                           float *out, cudaStream_t s);
+// xn[t] = rmsnorm(resid[t]) * w for T rows of H (H a multiple of 4)
+cudaError_t launch_rmsnorm(const float *resid, const float *w, float eps, int T, int H, float *xn, cudaStream_t s);
 // gs: inputs per scale when fmt is COLI_FMT_INT4G (sc is then [O][ceil(In/gs)]), else unused
 cudaError_t launch_qgemv(int fmt, const void *W, const float *sc, int gs, const float *x, float *y, int O,
                          int In, int T, cudaStream_t st);

@@ -57,7 +57,8 @@ struct PfParams {
     const coli_moe_expert *experts;  // device [E]
     coli_moe_expert shared;
     const int32_t *counts, *offsets; // routed buckets
-    const uint16_t *xb;              // bf16 activations [T*K + T][H] (block-permuted per format)
+    const uint16_t *xb;              // f16 activations [T*K + T][H], row p scaled by 2^xe[p] (block-permuted per format)
+    const int32_t *xe;               // [T*K + T] the exponent of each activation row's scale
     uint16_t *hb;                    // bf16 h [T*K + T][ldh] (block-permuted per format)
     float *y;                        // [T*K + T][H]
     int32_t *err;
@@ -122,30 +123,47 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     return d;
 }
 
-// Dequantise 16 consecutive weights to 8 bf16 pairs in the permuted K order. The bf16 magic: a
-// field f in bits 0..3 (resp. 0..1) of a halfword OR-ed with 0x4300 is the bf16 128 + f, exactly; adding -(128 + 8) (resp. -(128 + 2)) leaves f - 8
-// (resp. f - 2) exactly. int8 bytes go through float (every int8 value is exact in bf16).
-template <int FMT>
-__device__ __forceinline__ void deq16_bf16(const uint32_t *w, uint32_t (&out)[8]) {
-    // 16 consecutive weights (int4: 2 words, int2: 1, int8: 4) -> 8 bf16 pairs, permuted K order
+__device__ __forceinline__ uint32_t f16x2_fma(uint32_t a, uint32_t b, uint32_t c) {
+    uint32_t d;
+    asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+
+// f16 pair (lo, hi) of two floats, round to nearest even
+__device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
+    uint32_t d;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+    return d;
+}
+
+// Dequantise 16 consecutive weights to 8 pairs of 16-bit floats (F16: IEEE half, else bf16) in
+// the permuted K order. The magic: a field f in the low bits of a halfword OR-ed with the bits of
+// 2^m (f16: 1024, 0x6400; bf16: 128, 0x4300) is the float 2^m + f exactly (f < 2^m fits the
+// mantissa); one fused multiply-add by 1 and -(2^m + 8) (int2: -(2^m + 2)) leaves f - 8
+// (f - 2) exactly. int8 bytes go through float (every int8 value is exact in both types).
+template <int FMT, bool F16>
+__device__ __forceinline__ void deq16(const uint32_t *w, uint32_t (&out)[8]) {
+    // 16 consecutive weights (int4: 2 words, int2: 1, int8: 4) -> 8 pairs, permuted K order
+    const uint32_t base = F16 ? 0x64006400u : 0x43004300u, one = F16 ? 0x3C003C00u : 0x3F803F80u;
+    auto fma2 = [&](uint32_t a, uint32_t c) { return F16 ? f16x2_fma(a, one, c) : bf16x2_fma(a, one, c); };
     if (FMT == COLI_FMT_INT4) {
-        const uint32_t one = 0x3F803F80u, off = 0xC308C308u;
+        const uint32_t off = F16 ? 0xE408E408u : 0xC308C308u;  // -(1024 + 8) / -(128 + 8)
 #pragma unroll
         for (int i = 0; i < 2; i++)
 #pragma unroll
-            for (int m = 0; m < 4; m++)
-                out[4 * i + m] = bf16x2_fma(lop3_and_or(w[i] >> (4 * m), 0x000F000Fu, 0x43004300u), one, off);
+            for (int m = 0; m < 4; m++) out[4 * i + m] = fma2(lop3_and_or(w[i] >> (4 * m), 0x000F000Fu, base), off);
     } else if (FMT == COLI_FMT_INT2) {
-        const uint32_t one = 0x3F803F80u, off = 0xC302C302u;
+        const uint32_t off = F16 ? 0xE402E402u : 0xC302C302u;  // -(1024 + 2) / -(128 + 2)
 #pragma unroll
-        for (int m = 0; m < 8; m++)
-            out[m] = bf16x2_fma(lop3_and_or(w[0] >> (2 * m), 0x00030003u, 0x43004300u), one, off);
+        for (int m = 0; m < 8; m++) out[m] = fma2(lop3_and_or(w[0] >> (2 * m), 0x00030003u, base), off);
     } else {
 #pragma unroll
         for (int i = 0; i < 4; i++) {
             const int v = (int)w[i];
-            out[2 * i] = pack_bf16((float)((v << 24) >> 24), (float)((v << 16) >> 24));
-            out[2 * i + 1] = pack_bf16((float)((v << 8) >> 24), (float)(v >> 24));
+            const float a = (float)((v << 24) >> 24), b = (float)((v << 16) >> 24);
+            const float c = (float)((v << 8) >> 24), d = (float)(v >> 24);
+            out[2 * i] = F16 ? pack_f16(a, b) : pack_bf16(a, b);
+            out[2 * i + 1] = F16 ? pack_f16(c, d) : pack_bf16(c, d);
         }
     }
 }
@@ -277,7 +295,7 @@ __device__ __forceinline__ void issue_step(const ProdRow &pr, int kb, uint8_t *r
 }
 
 // dequantise the thread's raw half row into chunks 4h..4h+3 of row r of the swizzled A tile
-template <int FMT>
+template <int FMT, bool F16>
 __device__ __forceinline__ void dequant_half(const uint8_t *raw, int rs, uint8_t *sa, int r, int h) {
     constexpr int QH = (FMT == COLI_FMT_INT4 ? 32 : FMT == COLI_FMT_INT2 ? 16 : 64) / 2;
     const uint8_t *src = raw + r * rs + h * QH;
@@ -300,10 +318,16 @@ __device__ __forceinline__ void dequant_half(const uint8_t *raw, int rs, uint8_t
 #pragma unroll
     for (int c2 = 0; c2 < 2; c2++) {
         uint32_t o[8];
-        deq16_bf16<FMT>(w + c2 * WPQ, o);
+        deq16<FMT, F16>(w + c2 * WPQ, o);
         st_sw128(sa, r, 4 * h + 2 * c2, make_uint4(o[0], o[1], o[2], o[3]));
         st_sw128(sa, r, 4 * h + 2 * c2 + 1, make_uint4(o[4], o[5], o[6], o[7]));
     }
+}
+
+// 2^-e for the exponents the prepass writes (e in [-113, 275]): two exact factors
+__device__ __forceinline__ float exp2_neg(int e) {
+    const int e1 = max(-126, min(126, -e)), e2 = -e - e1;
+    return __int_as_float((e1 + 127) << 23) * __int_as_float((max(-126, e2) + 127) << 23);
 }
 
 __device__ __forceinline__ uint16_t bf16_bits(float f) {
@@ -461,9 +485,17 @@ __global__ void __launch_bounds__(kTcThreads, 1) moe_prefill_tc_kernel(const PfP
                 if (!mbar_wait_bounded(&ts.landed[s], (g / kC) & 1, ts, P.err)) break;
                 if (g >= (uint32_t)kTcA && !mbar_wait_bounded(&ts.emptya[a], ((g / kTcA) - 1) & 1, ts, P.err)) break;
                 uint8_t *sa = sA + a * kStageA;
-                if (fmt == COLI_FMT_INT4) dequant_half<COLI_FMT_INT4>(sR + s * kStageRaw, kRS, sa, r, h);
-                else if (fmt == COLI_FMT_INT8) dequant_half<COLI_FMT_INT8>(sR + s * kStageRaw, kRS, sa, r, h);
-                else dequant_half<COLI_FMT_INT2>(sR + s * kStageRaw, kRS, sa, r, h);
+                // gate/up: f16 (the activations are per-token scaled f16); down: bf16 (h)
+                const uint8_t *raw = sR + s * kStageRaw;
+                if (!P.down) {
+                    if (fmt == COLI_FMT_INT4) dequant_half<COLI_FMT_INT4, true>(raw, kRS, sa, r, h);
+                    else if (fmt == COLI_FMT_INT8) dequant_half<COLI_FMT_INT8, true>(raw, kRS, sa, r, h);
+                    else dequant_half<COLI_FMT_INT2, true>(raw, kRS, sa, r, h);
+                } else {
+                    if (fmt == COLI_FMT_INT4) dequant_half<COLI_FMT_INT4, false>(raw, kRS, sa, r, h);
+                    else if (fmt == COLI_FMT_INT8) dequant_half<COLI_FMT_INT8, false>(raw, kRS, sa, r, h);
+                    else dequant_half<COLI_FMT_INT2, false>(raw, kRS, sa, r, h);
+                }
                 fence_async_smem();
                 mbar_arrive(&ts.full[a]);
             }
@@ -478,7 +510,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) moe_prefill_tc_kernel(const PfP
                 const int nkb = nkb_of(T), b = it & 1;
                 if (it >= 2 && !mbar_wait_bounded(&ts.tfree[b], ((it >> 1) - 1) & 1, ts, P.err)) break;
                 tc_fence_after_sync();
-                const uint32_t idesc = idesc_bf16_f32(kTcM, T.N), dcol = tbase + b * kTcN;
+                const uint32_t idesc = idesc_f32acc(kTcM, T.N, P.down != 0), dcol = tbase + b * kTcN;
                 for (int kb = 0; kb < nkb; kb++, gk++) {
                     const int s = gk % kC, a = gk % kTcA;
                     if (!mbar_wait_bounded(&ts.full[a], (gk / kTcA) & 1, ts, P.err)) break;
@@ -486,7 +518,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) moe_prefill_tc_kernel(const PfP
                     const uint32_t a0 = smem_u32(sA + a * kStageA), b0 = smem_u32(sB + s * kStageB);
 #pragma unroll
                     for (int k = 0; k < kTcKB / 16; k++)
-                        tc_mma_bf16(dcol, sdesc_k_sw128(a0 + 32 * k), sdesc_k_sw128(b0 + 32 * k), idesc, (kb | k) != 0);
+                        tc_mma_f16kind(dcol, sdesc_k_sw128(a0 + 32 * k), sdesc_k_sw128(b0 + 32 * k), idesc, (kb | k) != 0);
                     tc_commit(&ts.emptyc[s]);
                     tc_commit(&ts.emptya[a]);
                 }
@@ -542,8 +574,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) moe_prefill_tc_kernel(const PfP
                         for (int i = 0; i < 16; i++) {
                             const int n = c0 + i;
                             if (n < T.ncur) {
-                                const float gv = __uint_as_float(v[i]) * sc0;
-                                const float uv = __uint_as_float(pv[i]) * sc1;
+                                // undo the token's 2^e of the f16 staging (exact), then the row scale
+                                const float inv = exp2_neg(__ldg(P.xe + T.pbase + T.n0 + n));
+                                const float gv = (__uint_as_float(v[i]) * inv) * sc0;
+                                const float uv = (__uint_as_float(pv[i]) * inv) * sc1;
                                 const float hv = gv / (1.f + expf(-gv)) * uv;
                                 P.hb[(size_t)(T.pbase + T.n0 + n) * P.ldh + col] = bf16_bits(hv);
                             }
@@ -563,17 +597,20 @@ __global__ void __launch_bounds__(kTcThreads, 1) moe_prefill_tc_kernel(const PfP
     }
 }
 
-// x (fp32) -> bf16 rows in bucket order (rows p < T*K: token perm[p] / K, up to offsets[E]) and
-// plain order for the shared expert (rows T*K + t), K-permuted per the rows' weight format.
-__global__ void prefill_prepass_kernel(const float *__restrict__ x, const int32_t *__restrict__ perm,
-                                       const int32_t *__restrict__ offsets, uint16_t *xb, int T, int H, int K, int E,
-                                       int rfmt, int sfmt, int has_shared) {
-    const int nblk = H / 16;
-    const long long total = (long long)(T * K + (has_shared ? T : 0)) * nblk;
+// x (fp32) -> f16 rows in bucket order (rows p < T*K: token perm[p] / K, up to offsets[E]) and
+// plain order for the shared expert (rows T*K + t), K-permuted per the rows' weight format. One
+// warp per row: row p is scaled by 2^xe[p], chosen from the row's max |x| so that the largest
+// element lands in [2^14, 2^15), then rounded to f16 (nearest even): every element keeps an
+// 11-bit significand unless it is below 2^-24 of the row's largest.
+__global__ void __launch_bounds__(256) prefill_prepass_kernel(const float *__restrict__ x, const int32_t *__restrict__ perm,
+                                                              const int32_t *__restrict__ offsets, uint16_t *xb,
+                                                              int32_t *xe, int T, int H, int K, int E, int rfmt,
+                                                              int sfmt, int has_shared) {
+    const int lane = threadIdx.x % 32;
+    const int warp0 = (blockIdx.x * blockDim.x + threadIdx.x) / 32, nwarps = gridDim.x * blockDim.x / 32;
+    const int rows = T * K + (has_shared ? T : 0);
     const int kept = offsets[E];
-    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
-         i += (long long)gridDim.x * blockDim.x) {
-        const int p = (int)(i / nblk), b = (int)(i % nblk);
+    for (int p = warp0; p < rows; p += nwarps) {
         int t, fmt;
         if (p < T * K) {
             if (p >= kept) continue;
@@ -583,25 +620,42 @@ __global__ void prefill_prepass_kernel(const float *__restrict__ x, const int32_
             t = p - T * K;
             fmt = sfmt;
         }
-        const float4 *src = reinterpret_cast<const float4 *>(x + (size_t)t * H + b * 16);
-        float v[16];
-#pragma unroll
-        for (int q = 0; q < 4; q++) {
-            const float4 f = __ldg(src + q);
-            v[4 * q] = f.x;
-            v[4 * q + 1] = f.y;
-            v[4 * q + 2] = f.z;
-            v[4 * q + 3] = f.w;
+        const float4 *src = reinterpret_cast<const float4 *>(x + (size_t)t * H);
+        float mx = 0.f;
+        for (int q = lane; q < H / 4; q += 32) {
+            const float4 v = __ldg(src + q);
+            mx = fmaxf(mx, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
         }
-        float o[16];
 #pragma unroll
-        for (int j = 0; j < 16; j++) o[kperm(fmt, j)] = v[j];
-        uint32_t w[8];
+        for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        int e = 0;
+        if (mx > 0.f) {
+            const int ex = (int)((__float_as_uint(mx) >> 23) & 255u);
+            e = 14 - (ex == 0 ? -126 : ex - 127);
+        }
+        const int e1 = max(-126, min(126, e)), e2 = e - e1;  // 2^e as two exact factors
+        const float f1 = __int_as_float((e1 + 127) << 23), f2 = __int_as_float((e2 + 127) << 23);
+        for (int b = lane; b < H / 16; b += 32) {
+            float v[16];
 #pragma unroll
-        for (int j = 0; j < 8; j++) w[j] = pack_bf16(o[2 * j], o[2 * j + 1]);
-        uint4 *dst = reinterpret_cast<uint4 *>(xb + (size_t)p * H + b * 16);
-        dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
-        dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+            for (int q = 0; q < 4; q++) {
+                const float4 f = __ldg(src + 4 * b + q);
+                v[4 * q] = f.x;
+                v[4 * q + 1] = f.y;
+                v[4 * q + 2] = f.z;
+                v[4 * q + 3] = f.w;
+            }
+            float o[16];
+#pragma unroll
+            for (int j = 0; j < 16; j++) o[kperm(fmt, j)] = (v[j] * f1) * f2;
+            uint32_t w[8];
+#pragma unroll
+            for (int j = 0; j < 8; j++) w[j] = pack_f16(o[2 * j], o[2 * j + 1]);
+            uint4 *dst = reinterpret_cast<uint4 *>(xb + (size_t)p * H + b * 16);
+            dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+            dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+        }
+        if (lane == 0) xe[p] = e;
     }
 }
 
@@ -615,11 +669,10 @@ bool prefill_supported(const coli_moe_desc &d) {
 cudaError_t launch_prefill(const PrefillWork &w, int part, cudaStream_t st) {
     cudaError_t e;
     if (part == 0) {
-        const long long total = (long long)(w.T * w.K + (w.I_shared > 0 ? w.T : 0)) * (w.H / 16);
-        const int threads = 256;
-        const int blocks = (int)std::min<long long>((total + threads - 1) / threads, 152LL * 16);
-        prefill_prepass_kernel<<<blocks, threads, 0, st>>>(w.x, w.perm, w.offsets, w.xb, w.T, w.H, w.K, w.E,
-                                                           w.routed_fmt, w.shared_fmt, w.I_shared > 0);
+        const long long rows = (long long)w.T * w.K + (w.I_shared > 0 ? w.T : 0);
+        const int blocks = (int)std::min<long long>((rows + 7) / 8, (long long)w.grid * 16);
+        prefill_prepass_kernel<<<blocks, 256, 0, st>>>(w.x, w.perm, w.offsets, w.xb, w.xe, w.T, w.H, w.K, w.E,
+                                                       w.routed_fmt, w.shared_fmt, w.I_shared > 0);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
     PfParams P{};
@@ -628,6 +681,7 @@ cudaError_t launch_prefill(const PrefillWork &w, int part, cudaStream_t st) {
     P.counts = w.counts;
     P.offsets = w.offsets;
     P.xb = w.xb;
+    P.xe = w.xe;
     P.hb = w.hb;
     P.y = w.y;
     P.err = w.err;

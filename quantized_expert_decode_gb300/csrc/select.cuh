@@ -57,9 +57,11 @@ __device__ __forceinline__ int sel_block_rank(const float *chb, float c, int lan
     return r;
 }
 
-// number of the n candidates (choice, id bits) that beat (c, e)
+// number of the n candidates (choice, id bits) that beat (c, e); unrolled so that several
+// shared-memory loads are in flight
 __device__ __forceinline__ int sel_cand_rank(const float2 *cand, int n, float c, int e) {
     int r = 0;
+#pragma unroll 8
     for (int j = 0; j < n; j++) {
         const float2 o = cand[j];
         r += sel_beats(o.x, __float_as_int(o.y), c, e);

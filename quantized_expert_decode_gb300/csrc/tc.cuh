@@ -1,5 +1,5 @@
 // tc.cuh — thin inline-PTX wrappers for the 5th-generation tensor cores (tcgen05) used by the
-// prefill GEMMs: tensor-memory allocation, the bf16 MMA with fp32 accumulators in TMEM, its
+// prefill GEMMs: tensor-memory allocation, the f16 / bf16 MMA with fp32 accumulators in TMEM, its
 // completion commit to an mbarrier, TMEM loads and the ordering fences. cta_group::1 only.
 // Internal to libcolimoe.
 #pragma once
@@ -44,17 +44,18 @@ __device__ __forceinline__ uint64_t sdesc_k_sw128(uint32_t saddr) {
     return d;
 }
 
-// Instruction descriptor of kind::f16 with bf16 A and B (both K-major), fp32 D, shape M x N.
-__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
+// Instruction descriptor of kind::f16 with A and B both f16 or both bf16 (K-major), fp32 D,
+// shape M x N.
+__host__ __device__ constexpr uint32_t idesc_f32acc(int M, int N, bool bf16) {
     return (1u << 4)                          // D format: f32
-           | (1u << 7)                        // A format: bf16
-           | (1u << 10)                       // B format: bf16
+           | ((bf16 ? 1u : 0u) << 7)          // A format: f16 (0) or bf16 (1)
+           | ((bf16 ? 1u : 0u) << 10)         // B format: the same as A
            | ((uint32_t)(N >> 3) << 17)       // N / 8
            | ((uint32_t)(M >> 4) << 24);      // M / 16
 }
 
 // ---- MMA: D[tmem] (+)= A[smem] * B[smem]^T, issued by ONE thread
-__device__ __forceinline__ void tc_mma_bf16(uint32_t d_taddr, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+__device__ __forceinline__ void tc_mma_f16kind(uint32_t d_taddr, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
                                             uint32_t accumulate) {
     asm volatile(
         "{\n\t.reg .pred p;\n\t"

@@ -159,3 +159,23 @@ def plant_tie(blk, K, places, seed, b_off=None, gap=GAP, tries=200):
         else:
             raise RuntimeError(f"plant_tie: token {t} found no place {want}")
     return dict(blk, x=x, Wr=Wr, bias=bias), a, b
+
+
+def tail_inputs(blk, seed, K, scale=3.0, max_redraws=1000):
+    """Inputs of the layer tail for blk's shapes: a residual row per token (N(0, scale^2)) and a
+    norm weight ~ U(0.5, 1.5); rows are redrawn until the normalised rows pass gap_filter(K).
+    Returns (resid, norm_w, eps)."""
+    import oracle
+    rng = np.random.default_rng(seed)
+    T, H = blk["x"].shape
+    eps = 1e-5
+    w = rng.uniform(0.5, 1.5, H).astype(np.float32)
+    resid = (rng.standard_normal((T, H)) * scale).astype(np.float32)
+    ok = gap_filter(K)
+    for _ in range(max_redraws):
+        good = ok(oracle.rmsnorm(resid, w, eps), blk["Wr"], blk["bias"])
+        if good.all():
+            return resid, w, eps
+        bad = np.nonzero(~good)[0]
+        resid[bad] = (rng.standard_normal((len(bad), H)) * scale).astype(np.float32)
+    raise RuntimeError("tail_inputs: no rows pass the gap filter")

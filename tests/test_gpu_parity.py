@@ -15,7 +15,7 @@ import torch
 
 import oracle
 import synth
-from conftest import gap_filter, oracle_rows, plant_tie, top_p_filter, with_heavy_tails
+from conftest import gap_filter, oracle_rows, plant_tie, tail_inputs, top_p_filter, with_heavy_tails
 
 pytestmark = pytest.mark.gpu
 
@@ -494,3 +494,66 @@ def test_idot_blocks(qed, name, over):
     rows = list(range(cfg["T"])) if tokens is None else tokens
     rel = rms(out[rows] - exact[rows]) / rms(exact[rows])
     assert 1e-4 < rel < 2e-2, rel
+
+
+# ------------------------------------------------------------------ the layer tail (RMSNorm folded in)
+# coli_moe_forward_tail: out = resid + block(rmsnorm(resid) * norm_w), the post-attention norm
+# and residual of the layer forward (colibri-strix c/glm.c @98759bf). T = 1 normalises inside the
+# single-token kernel; other T through a prologue launch. Compared with oracle.moe_tail token by
+# token at the path's bar (the residual is added after, so rms(out) includes it: the bar is taken
+# on the block part, out - resid, against the oracle's block part).
+TAILS = [
+    ("one-token", dict(T=1, H=512, I=256, E=32, K=4, I_shared=128, routed_fmt=2, shared_fmt=1), False),
+    ("one-token-in-place", dict(T=1, H=512, I=256, E=32, K=4, I_shared=128, routed_fmt=2, shared_fmt=2), True),
+    ("token-group", dict(T=6, H=512, I=256, E=32, K=4, I_shared=128, routed_fmt=2, shared_fmt=1), True),
+    ("tensor-core", dict(T=96, H=256, I=128, E=16, K=2, I_shared=128, routed_fmt=2, shared_fmt=2), False),
+    ("grouped", dict(T=3, H=256, I=128, E=8, K=2, I_shared=64, routed_fmt=4, shared_fmt=4, group_size=64), False),
+]
+
+
+@pytest.mark.parametrize("name,over,in_place", TAILS, ids=[t[0] for t in TAILS])
+def test_layer_tail(qed, name, over, in_place):
+    from quantized_expert_decode_gb300.device import DeviceBlock
+    cfg = dict(norm_topk=1, routed_scale=2.5, zipf=False)
+    cfg.update(over)
+    blk = make(cfg, seed=zlib.crc32(("tail-" + name).encode()) % 1000)
+    resid, nw, eps = tail_inputs(blk, seed=31, K=cfg["K"])
+    dev = DeviceBlock(blk)
+    T, H, K = cfg["T"], cfg["H"], cfg["K"]
+    d = dev.device
+    r = torch.from_numpy(resid).to(d)
+    w = torch.from_numpy(nw).to(d)
+    out = r if in_place else torch.empty((T, H), dtype=torch.float32, device=d)
+    idx = torch.empty((T, K), dtype=torch.int32, device=d)
+    wt = torch.empty((T, K), dtype=torch.float32, device=d)
+    qed.coli_moe_forward_tail(dev.desc, r, w, eps, dev.Wr, dev.bias, dev.table, dev.shared, out, idx, wt,
+                              dev.ws, dev.ws_bytes)
+    qed.coli_moe_check(dev.ws)
+    torch.cuda.synchronize()
+    got, gi = out.cpu().numpy(), idx.cpu().numpy()
+    ro, ri, rw, _ = oracle.moe_tail(blk, resid, nw, eps)
+    assert np.array_equal(gi, ri)
+    assert np.allclose(wt.cpu().numpy(), rw, rtol=W_RTOL, atol=0)
+    tol = PREFILL_TOL if T >= PREFILL_MIN_T else OUT_TOL
+    for t in range(T):
+        block_ref = ro[t].astype(np.float64) - resid[t]
+        block_got = got[t].astype(np.float64) - resid[t]
+        # the residual's own rounding in the final add is one ulp of |out|
+        slack = 2 * np.max(np.spacing(np.abs(ro[t])))
+        err = np.max(np.abs(block_got - block_ref))
+        assert err <= tol * rms(block_ref) + slack, (name, t, err, rms(block_ref))
+
+
+def test_rmsnorm_entry_point(qed):
+    rng = np.random.default_rng(8)
+    T, H = 5, 768
+    x = (rng.standard_normal((T, H)) * rng.uniform(0.1, 40, (T, 1))).astype(np.float32)
+    w = rng.uniform(0.5, 1.5, H).astype(np.float32)
+    d = torch.device("cuda")
+    xn = torch.empty((T, H), dtype=torch.float32, device=d)
+    qed.coli_moe_rmsnorm(torch.from_numpy(x).to(d), torch.from_numpy(w).to(d), 1e-5, xn, T, H)
+    torch.cuda.synchronize()
+    ref = oracle.rmsnorm(x, w, 1e-5)
+    # the same float operations; only the order of the double sum differs, which can move r by
+    # at most an ulp
+    assert np.max(np.abs(xn.cpu().numpy() - ref) / np.abs(ref).max()) < 4e-7

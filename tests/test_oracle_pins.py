@@ -660,3 +660,87 @@ def test_skewed_bias_concentrates_assignments():
     counts = np.bincount(idx.reshape(-1), minlength=cfg["E"])
     top = np.sort(counts)[::-1][: cfg["E"] // 5].sum() / counts.sum()
     assert 0.45 <= top <= 0.55, top
+
+
+# ------------------------------------------------------------------ RMS normalisation (layer tail)
+# glm.c rmsnorm(): r = 1 / sqrtf(mean square + eps) with the mean square accumulated in double,
+# out = x * r * w. The block as the tail of a decoder layer: out = resid + moe(rmsnorm(resid)).
+def test_rmsnorm_constant_rows_closed_form():
+    w = np.ones(16, np.float32)
+    # a constant row c has mean square c^2: r = 1 / |c| exactly for these c, eps = 0
+    for c in (2.0, 0.25, -4.0):
+        out = oracle.rmsnorm(np.full((1, 16), c, np.float32), w, 0.0)
+        assert np.array_equal(out[0], np.full(16, np.sign(c), np.float32)), c
+    # eps enters under the root: c = 1, eps = 3 gives r = 1 / 2
+    out = oracle.rmsnorm(np.ones((1, 16), np.float32), w, 3.0)
+    assert np.array_equal(out[0], np.full(16, 0.5, np.float32))
+
+
+def test_rmsnorm_weights_multiply_elementwise():
+    rng = np.random.default_rng(3)
+    w = rng.uniform(0.5, 2.0, 64).astype(np.float32)
+    out = oracle.rmsnorm(np.full((1, 64), 2.0, np.float32), w, 0.0)  # r * 2 = 1 exactly
+    assert np.array_equal(out[0], w)
+
+
+def test_rmsnorm_matches_float64_definition():
+    rng = np.random.default_rng(4)
+    x = (rng.standard_normal((5, 300)) * rng.uniform(0.1, 30, (5, 1))).astype(np.float32)
+    w = rng.uniform(0.5, 1.5, 300).astype(np.float32)
+    eps = 1e-5
+    got = oracle.rmsnorm(x, w, eps).astype(np.float64)
+    xt = torch.from_numpy(x.astype(np.float64))
+    ref = (xt / torch.sqrt((xt * xt).mean(dim=1, keepdim=True) + eps) * torch.from_numpy(w.astype(np.float64))).numpy()
+    assert np.max(np.abs(got - ref) / np.abs(ref).max()) < 1e-6
+
+
+def test_tail_normalises_the_residual_before_the_block():
+    # rmsnorm is invariant to scaling its input by 2 (eps = 0), so doubling the residual doubles
+    # only the residual term of the tail: tail(2 r) - 2 r == tail(r) - r up to the rounding of
+    # the two residual additions. A tail that fed the raw residual to the block, or skipped the
+    # norm, would differ by far more.
+    cfg = dict(T=3, H=128, I=64, E=8, K=2, I_shared=64, norm_topk=1, routed_scale=2.5,
+               routed_fmt=2, shared_fmt=1, zipf=False)
+    blk = synth.make_block(cfg, seed=12, row_filter=gap_filter(2))
+    rng = np.random.default_rng(12)
+    w = rng.uniform(0.5, 1.5, 128).astype(np.float32)
+    r = blk["x"] * 3.0
+    a, ia, _, _ = oracle.moe_tail(blk, r, w, 0.0)
+    b, ib, _, _ = oracle.moe_tail(blk, 2 * r, w, 0.0)
+    assert np.array_equal(ia, ib)
+    assert np.array_equal(oracle.rmsnorm(2 * r, w, 0.0), oracle.rmsnorm(r, w, 0.0))
+    ulp = np.spacing(np.maximum(np.abs(b), 2 * np.abs(r)).astype(np.float32)).astype(np.float64)
+    diff = np.abs((b.astype(np.float64) - 2 * r) - (a.astype(np.float64) - r))
+    assert np.all(diff <= 2 * ulp)
+    assert np.max(np.abs(a - r)) > 1e-3  # the block's part is not negligible
+
+
+def test_tail_single_expert_is_dense_swiglu_of_the_normalised_residual():
+    # E = K = 1 (weight exactly 1), int8 weights with scale 1 and |w| <= 1: the block is two dense
+    # SwiGLU FFNs; the tail adds the residual to them, all in float64 here
+    H, I = 64, 32
+    cfg = dict(T=2, H=H, I=I, E=1, K=1, I_shared=32, norm_topk=1, routed_scale=1.0,
+               routed_fmt=1, shared_fmt=1, zipf=False)
+    blk = synth.make_block(cfg, seed=21)
+    rng = np.random.default_rng(21)
+    for ex in [blk["routed"][0], blk["shared"]]:
+        for k in ("gate_w", "up_w", "down_w"):
+            ex[k][...] = rng.integers(-1, 2, ex[k].shape, dtype=np.int8).view(np.uint8)
+        for k in ("gate_s", "up_s", "down_s"):
+            ex[k][...] = 1.0
+    resid = (rng.standard_normal((2, H)) * 4).astype(np.float32)
+    nw = rng.uniform(0.5, 1.5, H).astype(np.float32)
+    eps = 1e-6
+    out, _, _, _ = oracle.moe_tail(blk, resid, nw, eps)
+    r64 = resid.astype(np.float64)
+    xn = r64 / np.sqrt((r64 ** 2).mean(axis=1, keepdims=True) + eps) * nw.astype(np.float64)
+
+    def ffn(ex, Iin):
+        G = ex["gate_w"].view(np.int8)[:, :H].astype(np.float64)
+        U = ex["up_w"].view(np.int8)[:, :H].astype(np.float64)
+        D = ex["down_w"].view(np.int8)[:, :Iin].astype(np.float64)
+        g, u = xn @ G.T, xn @ U.T
+        return (g / (1 + np.exp(-g)) * u) @ D.T
+
+    ref = r64 + ffn(blk["routed"][0], I) + ffn(blk["shared"], 32)
+    assert np.max(np.abs(out - ref)) < 1e-4 * np.sqrt(np.mean(ref ** 2))

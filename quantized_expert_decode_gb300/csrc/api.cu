@@ -318,6 +318,7 @@ int run_forward(const coli_moe_desc *d, const float *x, const float *W_r, const 
         pw.shared_fmt = d->shared_fmt;
         pw.ldh = d->I > d->I_shared ? d->I : d->I_shared;
         pw.grid = num_sms();
+        pw.tmaps = ws_ptr<void>(ws, L.tmaps);
         cudaError_t e;
         if ((e = launch_prefill(pw, 0, st)) != cudaSuccess) return cuda_fail(e);
         if ((rc = record(events, 2, st))) return rc;

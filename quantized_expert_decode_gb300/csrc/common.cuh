@@ -55,6 +55,8 @@ struct WsLayout {
     size_t y;         // f32 [T*K + T][H]                 down-projection rows
     size_t xstage;    // f32 [T][H]  device copy of a host x
     size_t ostage;    // f32 [T][H]  device staging of a host out
+    size_t tmaps;     // 128-byte tensor maps [E + 1][3] (gate, up, down of every expert; the
+                      // shared expert last), written on the device for the tensor-core GEMMs
     size_t total;
     int router_splits;
 };
@@ -107,6 +109,7 @@ inline WsLayout ws_layout(const coli_moe_desc &d) {
     L.y = take(rows * H * 4);
     L.xstage = take(T * H * 4);
     L.ostage = take(T * H * 4);
+    L.tmaps = take((E + 1) * 3 * 128);
     L.total = p;
     return L;
 }

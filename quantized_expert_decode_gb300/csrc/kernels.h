@@ -87,6 +87,7 @@ struct PrefillWork {
     const int32_t *counts, *offsets, *perm;
     uint16_t *xb, *hb;               // f16 activations (row p scaled by 2^xe[p]) / bf16 h (block-permuted K order)
     int32_t *xe;                     // [T*K + T] exponents of the activation rows' scales
+    void *tmaps;                     // [E + 1][3] tensor maps of the expert matrices (workspace)
     float *y;
     int32_t *err;
     int T, H, I, E, K, I_shared, routed_fmt, shared_fmt, ldh, grid;

@@ -11,27 +11,36 @@
 //
 // One persistent CTA per SM walks the tiles (slot, token block, row block) of a launch, its
 // warps specialised:
-//   warps 0-7  copy warps, over the CTA's K-steps (64 wide) of all its tiles in order, thread
-//              (r, half): once the stage is free, cp.async of that half of A row r's packed
-//              weight bytes into the stage's raw buffer and of token row r < N of B (bf16)
-//              straight into its 128-byte-swizzled K-major slots; two steps later the thread
-//              waits for those copies, fences them for the tensor core and arrives on the
-//              stage's `landed` mbarrier — copies run up to the ring's depth ahead
-//   warps 8-15 dequant warps: once a stage has landed, thread (r, half) turns its half of raw
-//              row r into the swizzled bf16 A tile, fences, and arrives on the stage's `full`
-//   warp 16    one thread issues four tcgen05.mma (K = 16 each) per stage into one of two TMEM
-//              accumulators and commits the stage's `empty` mbarrier to their completion; after
-//              a tile's last step it commits that accumulator's `accf`
-//   warps 17-20 epilogue: tcgen05.ld of the 128 x N tile (warp w reads TMEM lanes 32 (w % 4)..),
+//   warp 0     weight copies: for each 128-byte K-chunk of the tile's 128 weight rows (four
+//              K-steps of int4, two of int8, eight of int2), 2-D tensor copies (64 gate rows and
+//              64 up rows, or 128 down rows; 128-byte swizzle) into a raw stage, completed on
+//              that stage's `rfull` mbarrier. Every expert matrix has its own tensor map, written
+//              on the device by a prologue launch from a host-encoded template (only the base
+//              address differs: the expert table holds device pointers the host cannot read)
+//   warp 1     activation copies: for each K-step, 2-D tensor copies (cp.async.bulk.tensor, a
+//              tensor map over the workspace's activation rows, 128-byte swizzle) of the tile's
+//              token rows straight into the B stage, in the K-major layout the MMA reads
+//   warps 2-9  dequant warps: thread (r, half) turns its half of raw row r's K-step into the
+//              swizzled 16-bit A tile, fences, and arrives on the A tile's `full`
+//   warp 10    one thread issues four tcgen05.mma (K = 16 each) per K-step into one of two TMEM
+//              accumulators and commits the A tile's and the B stage's `empty` mbarriers to
+//              their completion; after a tile's last step it commits that accumulator's `accf`
+//   warps 11-14 epilogue: tcgen05.ld of the 128 x N tile (warp w reads TMEM lanes 32 (w % 4)..),
 //              the fused epilogue, then `tfree` hands the accumulator back to the MMA warp, so
 //              the next tile's MMAs run while the epilogue reads this one
+// The copies are issued by single threads and land without any instruction of the dequant
+// warps; the dequant warps only dequantise.
 // K order: the dot product does not depend on the order of K, so within each block of 8 (int4)
 // or 16 (int2) elements K is permuted the same way in A and B — the order in which the
 // magic-number unpack produces bf16 pairs — and no byte shuffles are needed. The activations
 // (x, and h written by the gate/up epilogue) are stored in that order.
-// Every mbarrier wait is bounded; on expiry the CTA flags the error, drains the MMAs it issued
-// (a wait no other warp's abort cuts short), frees its tensor memory and returns.
+// Every mbarrier wait is bounded; on expiry the CTA flags the error, drains the copies and the
+// MMAs it issued (waits no other warp's abort cuts short), frees its tensor memory and returns.
 #include <algorithm>
+#include <mutex>
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
 
 #include "common.cuh"
 #include "kernels.h"
@@ -44,12 +53,15 @@ namespace {
 
 constexpr int kTcM = 128;        // MMA M: weight rows per tile
 constexpr int kTcN = 128;        // max tokens per tile (MMA N, multiple of 16)
-constexpr int kTcKB = 64;        // K per stage (one 128-byte swizzle row of bf16)
-constexpr int kTcA = 3;          // bf16 A tiles (the MMA runs at most a step behind the dequant)
-constexpr int kTcCMax = 7;       // copy stages (raw weights + B), the deepest ring
-constexpr int kTcThreads = 672;  // copy warps 0-7, dequant warps 8-15, MMA warp 16, epilogue 17-20
-constexpr int kTcCopy = 256, kTcDeq = 256, kTcEpi = 128;
-constexpr int kTcMmaWarp = 16;
+constexpr int kTcKB = 64;        // K per step (one 128-byte swizzle row of 16-bit values)
+constexpr int kTcA = 3;          // A tiles (the MMA runs at most a step behind the dequant)
+constexpr int kTcBS = 4;         // B stages, one K-step of up to 128 token rows each
+constexpr int kTcRS = 4;         // raw weight stages, one 128-byte K-chunk of the 128 rows each
+constexpr int kChunkB = 128;     // packed bytes of a row per raw stage (128-byte swizzled rows)
+constexpr int kBoxRows = 32;     // token rows per tensor copy of a B stage
+constexpr int kTcThreads = 480;  // warps: 0 weights, 1 activations, 2-9 dequant, 10 MMA, 11-14 epilogue
+constexpr int kTcDeq = 256, kTcEpi = 128;
+constexpr int kWarpB = 1, kDeq0 = 2, kTcMmaWarp = 10;
 constexpr int kTileCap = 128;    // tiles per CTA whose parameters are kept in shared memory
 constexpr unsigned long long kTcWaitNs = 2000000000ull;
 
@@ -60,6 +72,7 @@ struct PfParams {
     const uint16_t *xb;              // f16 activations [T*K + T][H], row p scaled by 2^xe[p] (block-permuted per format)
     const int32_t *xe;               // [T*K + T] the exponent of each activation row's scale
     uint16_t *hb;                    // bf16 h [T*K + T][ldh] (block-permuted per format)
+    const CUtensorMap *tmaps;        // [E + 1][3]: gate, up, down of every expert, the shared one last
     float *y;                        // [T*K + T][H]
     int32_t *err;
     int T, H, I, E, K, Is, rfmt, sfmt, ldh;
@@ -70,32 +83,21 @@ struct Tile {
     const uint8_t *w0, *w1;  // gate/up rows (or down rows in w0)
     const float *s0, *s1;
     int fmt, inter, n0, ncur, N, pbase, row0;  // row0: first j (gate/up) or d (down)
+    int slot, sh;                              // expert slot (E: the shared expert)
 };
 
 struct TcSmem {  // after the 1024-aligned stage buffers
-    uint64_t landed[kTcCMax], emptyc[kTcCMax], full[kTcA], emptya[kTcA], accf[2], tfree[2], drain;
+    uint64_t rfull[kTcRS], rempty[kTcRS], bfull[kTcBS], bempty[kTcBS], full[kTcA], emptya[kTcA], accf[2], tfree[2],
+        drain;
     uint32_t tmem_base;
     int abort;
     int pref[kMaxE + 2];  // tiles before slot g (slots 0..E-1 routed, E shared)
     Tile tiles[kTileCap]; // this CTA's tiles blockIdx.x + i * gridDim.x, looked up once
 };
 
-// Ring geometry per weight format: NC copy stages of raw weight rows (RS bytes per row: the
-// packed bytes of one K-step plus 16, which spreads the rows over the banks) and B tiles; a
-// copy thread fences and announces its copies LAG steps after issuing them (LAG <= NC - 2).
-template <int NC, int RS, int LAG>
-struct Ring {
-    static constexpr int kC = NC, kRS = RS, kLag = LAG;
-};
-// (measured on the prefill workload: lags 2 and 4 run at 6.7 ms, lags 3 and 5 at 7.7 ms, for 5 or
-// 7 copy stages alike)
-using RingNarrow = Ring<7, 48, 4>;  // int4 / int2 weights
-using RingWide = Ring<5, 80, 2>;    // int8 weights
-
-constexpr size_t kStageA = (size_t)kTcM * 128, kStageB = (size_t)kTcN * 128;
-template <class RG>
+constexpr size_t kStageA = (size_t)kTcM * 128, kStageB = (size_t)kTcN * 128, kStageRaw = (size_t)kTcM * kChunkB;
 constexpr size_t tc_smem_bytes() {
-    return 1024 + kTcA * kStageA + RG::kC * (kStageB + (size_t)kTcM * RG::kRS) + sizeof(TcSmem);
+    return 1024 + kTcA * kStageA + kTcBS * kStageB + kTcRS * kStageRaw + sizeof(TcSmem);
 }
 
 // position of element j of a K block in the permuted order of format fmt
@@ -230,84 +232,50 @@ __device__ Tile make_tile(const PfParams &P, const TcSmem &ts, int t) {
     T.w1 = static_cast<const uint8_t *>(ex.up_w);
     T.s0 = P.down ? ex.down_s : ex.gate_s;
     T.s1 = ex.up_s;
+    T.slot = g;
+    T.sh = sh ? 1 : 0;
     return T;
 }
 
-__device__ __forceinline__ void cp_async16(void *dst_smem, const void *src) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst_smem)), "l"(src) : "memory");
+// a tensor map written by the generic proxy is made visible to this thread's later tensor copies
+__device__ __forceinline__ void tmap_acquire(const CUtensorMap *map) {
+    asm volatile("fence.proxy.tensormap::generic.acquire.gpu [%0], 128;" ::"l"(map) : "memory");
 }
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
 __device__ __forceinline__ int qbytes(int fmt) { return fmt == COLI_FMT_INT4 ? 32 : fmt == COLI_FMT_INT2 ? 16 : 64; }
 
-__device__ __forceinline__ void cp_async8(void *dst_smem, const void *src) {
-    asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(smem_u32(dst_smem)), "l"(src) : "memory");
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
 }
 
-
-// The copy / dequant thread (r, h) of a tile: half h of A row r (gate/up interleaved — even rows
-// gate j0 + r/2, odd rows up — or down row d0 + r) and of B row r (token n0 + r, clamped to the
-// buffer; rows >= N are not copied).
-struct ProdRow {
-    const uint8_t *a;   // packed weights of A row r at K-step 0, half h
-    const uint16_t *b;  // bf16 activations of B row r at K-step 0, half h
-    int qh;             // packed bytes per half K-step
-    bool has_b;
-};
-
-__device__ __forceinline__ ProdRow prod_row(const PfParams &P, const Tile &T, int r, int h) {
-    ProdRow pr;
-    const int qb = qbytes(T.fmt);
-    const uint8_t *base;
-    if (P.down) {
-        base = T.w0 + (size_t)min(T.row0 + r, P.H - 1) * row_bytes(T.fmt, T.inter);
-    } else {
-        const int j = min(T.row0 + (r >> 1), T.inter - 1);
-        base = ((r & 1) ? T.w1 : T.w0) + (size_t)j * row_bytes(T.fmt, P.H);
-    }
-    pr.qh = qb / 2;
-    pr.a = base + h * pr.qh;
-    const int rows_total = P.T * P.K + P.T;
-    const int row = min(T.pbase + T.n0 + r, rows_total - 1);
-    pr.b = (P.down ? P.hb + (size_t)row * P.ldh : P.xb + (size_t)row * P.H) + 32 * h;
-    pr.has_b = r < T.N;
-    return pr;
+// 2-D tensor copy of the box at (x = innermost element, y = row) into shared memory, counted on bar
+__device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, int x, int y, uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+            smem_u32(dst)),
+        "l"(map), "r"(x), "r"(y), "r"(smem_u32(bar))
+        : "memory");
 }
 
-// K-step kb: cp.async of the half rows into the stage's raw buffer and B tile
-__device__ __forceinline__ void issue_step(const ProdRow &pr, int kb, uint8_t *raw, int rs, uint8_t *sb, int r,
-                                           int h) {
-    const uint8_t *src = pr.a + (size_t)kb * 2 * pr.qh;
-    uint8_t *dst = raw + r * rs + h * pr.qh;
-    if (pr.qh == 8) cp_async8(dst, src);
-    else
-        for (int i = 0; i < pr.qh / 16; i++) cp_async16(dst + 16 * i, src + 16 * i);
-    if (pr.has_b) {
-        const uint16_t *bs = pr.b + (size_t)kb * kTcKB;
-#pragma unroll
-        for (int c = 0; c < 4; c++) {
-            const int cc = 4 * h + c;
-            cp_async16(sb + (r >> 3) * 1024 + (r & 7) * 128 + ((cc ^ (r & 7)) << 4), bs + 8 * c);
-        }
-    }
-}
-
-// dequantise the thread's raw half row into chunks 4h..4h+3 of row r of the swizzled A tile
+// dequantise half h of K-step kin of the tile's A row r into chunks 4h..4h+3 of row r of the
+// swizzled A tile. The raw stage holds the tensor copy of 128 rows of 128 bytes with the 128-byte
+// swizzle (16-byte chunk c of raw row rr at chunk c ^ (rr % 8)); gate/up tiles keep gate row j0 + i
+// in raw row i and up row j0 + i in raw row 64 + i, down tiles row d0 + r in raw row r.
 template <int FMT, bool F16>
-__device__ __forceinline__ void dequant_half(const uint8_t *raw, int rs, uint8_t *sa, int r, int h) {
-    constexpr int QH = (FMT == COLI_FMT_INT4 ? 32 : FMT == COLI_FMT_INT2 ? 16 : 64) / 2;
-    const uint8_t *src = raw + r * rs + h * QH;
+__device__ __forceinline__ void dequant_half(const uint8_t *raw, int rr, int kin, uint8_t *sa, int r, int h) {
+    constexpr int QH = (FMT == COLI_FMT_INT4 ? 32 : FMT == COLI_FMT_INT2 ? 16 : 64) / 2;  // bytes of the half step
+    const uint8_t *row = raw + rr * kChunkB;
+    const int o = kin * 2 * QH + h * QH;  // byte offset of the half step in the logical row
+    auto at = [&](int off) { return row + ((((off >> 4) ^ (rr & 7)) << 4) | (off & 15)); };
     uint32_t w[8];
     if (QH == 8) {
-        const uint2 v = *reinterpret_cast<const uint2 *>(src);
+        const uint2 v = *reinterpret_cast<const uint2 *>(at(o));
         w[0] = v.x;
         w[1] = v.y;
     } else {
 #pragma unroll
         for (int i = 0; i < QH / 16; i++) {
-            const uint4 v = *reinterpret_cast<const uint4 *>(src + 16 * i);
+            const uint4 v = *reinterpret_cast<const uint4 *>(at(o + 16 * i));
             w[4 * i] = v.x;
             w[4 * i + 1] = v.y;
             w[4 * i + 2] = v.z;
@@ -317,10 +285,10 @@ __device__ __forceinline__ void dequant_half(const uint8_t *raw, int rs, uint8_t
     constexpr int WPQ = QH / 8;  // words per 16 weights
 #pragma unroll
     for (int c2 = 0; c2 < 2; c2++) {
-        uint32_t o[8];
-        deq16<FMT, F16>(w + c2 * WPQ, o);
-        st_sw128(sa, r, 4 * h + 2 * c2, make_uint4(o[0], o[1], o[2], o[3]));
-        st_sw128(sa, r, 4 * h + 2 * c2 + 1, make_uint4(o[4], o[5], o[6], o[7]));
+        uint32_t out[8];
+        deq16<FMT, F16>(w + c2 * WPQ, out);
+        st_sw128(sa, r, 4 * h + 2 * c2, make_uint4(out[0], out[1], out[2], out[3]));
+        st_sw128(sa, r, 4 * h + 2 * c2 + 1, make_uint4(out[4], out[5], out[6], out[7]));
     }
 }
 
@@ -334,14 +302,12 @@ __device__ __forceinline__ uint16_t bf16_bits(float f) {
     return (uint16_t)(pack_bf16(f, 0.f) & 0xFFFFu);
 }
 
-template <class RG>
-__global__ void __launch_bounds__(kTcThreads, 1) moe_prefill_tc_kernel(const PfParams P) {
-    constexpr int kC = RG::kC, kRS = RG::kRS, kLag = RG::kLag;
-    constexpr size_t kStageRaw = (size_t)kTcM * kRS;
+__global__ void __launch_bounds__(kTcThreads, 1)
+moe_prefill_tc_kernel(const PfParams P, const __grid_constant__ CUtensorMap tmB) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
-    uint8_t *sA = smem, *sB = smem + kTcA * kStageA, *sR = sB + kC * kStageB;
-    TcSmem &ts = *reinterpret_cast<TcSmem *>(sR + kC * kStageRaw);
+    uint8_t *sA = smem, *sB = smem + kTcA * kStageA, *sR = sB + kTcBS * kStageB;
+    TcSmem &ts = *reinterpret_cast<TcSmem *>(sR + kTcRS * kStageRaw);
     const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
     const int nslots = P.E + (P.Is > 0 ? 1 : 0);
 
@@ -408,9 +374,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) moe_prefill_tc_kernel(const PfP
     }
     if (tid == 0) {
         ts.abort = 0;
-        for (int s = 0; s < kC; s++) {
-            mbar_init(&ts.landed[s], kTcCopy);
-            mbar_init(&ts.emptyc[s], 1);
+        for (int s = 0; s < kTcRS; s++) {
+            mbar_init(&ts.rfull[s], 1);
+            mbar_init(&ts.rempty[s], kTcDeq);
+        }
+        for (int s = 0; s < kTcBS; s++) {
+            mbar_init(&ts.bfull[s], 1);
+            mbar_init(&ts.bempty[s], 1);
         }
         for (int s = 0; s < kTcA; s++) {
             mbar_init(&ts.full[s], kTcDeq);
@@ -434,70 +404,108 @@ __global__ void __launch_bounds__(kTcThreads, 1) moe_prefill_tc_kernel(const PfP
     const int total = ts.pref[nslots];
     const int G = gridDim.x;
     auto nkb_of = [&](const Tile &T) { return (P.down ? T.inter : P.H) / kTcKB; };
+    auto spc_of = [&](const Tile &T) { return kChunkB / qbytes(T.fmt); };  // K-steps per raw chunk
     auto tile_at = [&](int t) {  // t = blockIdx.x + i * G
         const int i = (t - (int)blockIdx.x) / G;
         return i < kTileCap ? ts.tiles[i] : make_tile(P, ts, t);
     };
 
-    if (warp < 8) {
-        // ---------------- copy warps
-        const int r = tid & 127, h = tid >> 7;
-        int ti = blockIdx.x, ki = 0;  // copy cursor: tile, K-step
-        Tile Ti = ti < total ? tile_at(ti) : Tile{};
-        ProdRow pi = prod_row(P, Ti, r, h);
-        int nki = ti < total ? nkb_of(Ti) : 0;
-        uint32_t g = 0;  // steps issued
-        while (ti < total && !ts.abort) {
-            const int s = g % kC;
-            const uint32_t use = g / kC;
-            if (use > 0 && !mbar_wait_bounded(&ts.emptyc[s], (use - 1) & 1, ts, P.err)) break;
-            issue_step(pi, ki, sR + s * kStageRaw, kRS, sB + s * kStageB, r, h);
-            cp_async_commit();
-            if (++ki == nki) {
-                ki = 0;
-                ti += G;
-                if (ti < total) {
-                    Ti = tile_at(ti);
-                    pi = prod_row(P, Ti, r, h);
-                    nki = nkb_of(Ti);
+    if (warp == 0) {
+        // ---------------- weight copies: 2-D tensor copies of 128-byte K-chunks of the rows
+        uint32_t gc = 0;  // chunks issued
+        if (lane == 0) {
+            bool ok = true;
+            for (int t = blockIdx.x; t < total && ok; t += G) {
+                const Tile T = tile_at(t);
+                const int nkb = nkb_of(T), spc = spc_of(T), qb = qbytes(T.fmt);
+                const CUtensorMap *maps = P.tmaps + 3 * (T.sh ? P.E : T.slot);
+                const CUtensorMap *m0 = P.down ? maps + 2 : maps, *m1 = maps + 1;
+                tmap_acquire(m0);
+                if (!P.down) tmap_acquire(m1);
+                for (int kb0 = 0; kb0 < nkb; kb0 += spc, gc++) {
+                    const int s = gc % kTcRS;
+                    const uint32_t use = gc / kTcRS;
+                    if (use > 0 && !mbar_wait_bounded(&ts.rempty[s], (use - 1) & 1, ts, P.err)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(&ts.rfull[s], (uint32_t)kStageRaw);
+                    uint8_t *dst = sR + s * kStageRaw;
+                    if (P.down) {
+                        tma_load_2d(dst, m0, kb0 * qb, T.row0, &ts.rfull[s]);
+                    } else {
+                        tma_load_2d(dst, m0, kb0 * qb, T.row0, &ts.rfull[s]);
+                        tma_load_2d(dst + 64 * kChunkB, m1, kb0 * qb, T.row0, &ts.rfull[s]);
+                    }
                 }
             }
-            if (g >= (uint32_t)kLag) {  // step g - kLag: its copies are in; fence and announce
-                cp_async_wait<kLag>();
-                fence_async_smem();
-                mbar_arrive(&ts.landed[(g - kLag) % kC]);
-            }
-            g++;
+            // every copy issued has landed before the CTA can end
+            for (uint32_t q = gc > (uint32_t)kTcRS ? gc - kTcRS : 0; q < gc; q++)
+                mbar_wait_drain(&ts.rfull[q % kTcRS], (q / kTcRS) & 1, P.err);
         }
-        // the last steps inside the lag
-        cp_async_wait<0>();
-        fence_async_smem();
-        for (uint32_t q = g >= (uint32_t)kLag ? g - kLag : 0; q < g; q++) mbar_arrive(&ts.landed[q % kC]);
+        __syncwarp();
+    } else if (warp == kWarpB) {
+        // ---------------- activation copies: 2-D tensor copies of 32 token rows each
+        uint32_t gb = 0;  // K-steps issued
+        if (lane == 0) {
+            bool ok = true;
+            for (int t = blockIdx.x; t < total && ok; t += G) {
+                const Tile T = tile_at(t);
+                const int nkb = nkb_of(T), nbox = (T.N + kBoxRows - 1) / kBoxRows, row = T.pbase + T.n0;
+                for (int kb = 0; kb < nkb; kb++, gb++) {
+                    const int s = gb % kTcBS;
+                    const uint32_t use = gb / kTcBS;
+                    if (use > 0 && !mbar_wait_bounded(&ts.bempty[s], (use - 1) & 1, ts, P.err)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(&ts.bfull[s], (uint32_t)(nbox * kBoxRows * 128));
+                    for (int i = 0; i < nbox; i++)
+                        tma_load_2d(sB + s * kStageB + i * kBoxRows * 128, &tmB, kb * kTcKB, row + i * kBoxRows,
+                                    &ts.bfull[s]);
+                }
+            }
+            for (uint32_t q = gb > (uint32_t)kTcBS ? gb - kTcBS : 0; q < gb; q++)
+                mbar_wait_drain(&ts.bfull[q % kTcBS], (q / kTcBS) & 1, P.err);
+        }
+        __syncwarp();
     } else if (warp < kTcMmaWarp) {
         // ---------------- dequant warps
-        const int r = (tid - kTcCopy) & 127, h = (tid - kTcCopy) >> 7;
-        uint32_t g = 0;
-        for (int t = blockIdx.x; t < total && !ts.abort; t += G) {
+        const int r = (tid - kDeq0 * 32) & 127, h = (tid - kDeq0 * 32) >> 7;
+        uint32_t g = 0, gc = 0;  // K-steps and raw chunks consumed
+        bool ok = true;
+        for (int t = blockIdx.x; t < total && ok; t += G) {
             const Tile T = tile_at(t);
-            const int fmt = T.fmt, nkb = nkb_of(T);
+            const int fmt = T.fmt, nkb = nkb_of(T), spc = spc_of(T);
             for (int kb = 0; kb < nkb; kb++, g++) {
-                const int s = g % kC, a = g % kTcA;
-                if (!mbar_wait_bounded(&ts.landed[s], (g / kC) & 1, ts, P.err)) break;
-                if (g >= (uint32_t)kTcA && !mbar_wait_bounded(&ts.emptya[a], ((g / kTcA) - 1) & 1, ts, P.err)) break;
+                const int kin = kb % spc, s = gc % kTcRS, a = g % kTcA;
+                if (kin == 0 && !mbar_wait_bounded(&ts.rfull[s], (gc / kTcRS) & 1, ts, P.err)) {
+                    ok = false;
+                    break;
+                }
+                if (g >= (uint32_t)kTcA && !mbar_wait_bounded(&ts.emptya[a], ((g / kTcA) - 1) & 1, ts, P.err)) {
+                    ok = false;
+                    break;
+                }
                 uint8_t *sa = sA + a * kStageA;
-                // gate/up: f16 (the activations are per-token scaled f16); down: bf16 (h)
                 const uint8_t *raw = sR + s * kStageRaw;
+                const int rr = P.down ? r : (r & 1) * 64 + (r >> 1);  // raw row of A row r
+                // gate/up: f16 (the activations are per-token scaled f16); down: bf16 (h)
                 if (!P.down) {
-                    if (fmt == COLI_FMT_INT4) dequant_half<COLI_FMT_INT4, true>(raw, kRS, sa, r, h);
-                    else if (fmt == COLI_FMT_INT8) dequant_half<COLI_FMT_INT8, true>(raw, kRS, sa, r, h);
-                    else dequant_half<COLI_FMT_INT2, true>(raw, kRS, sa, r, h);
+                    if (fmt == COLI_FMT_INT4) dequant_half<COLI_FMT_INT4, true>(raw, rr, kin, sa, r, h);
+                    else if (fmt == COLI_FMT_INT8) dequant_half<COLI_FMT_INT8, true>(raw, rr, kin, sa, r, h);
+                    else dequant_half<COLI_FMT_INT2, true>(raw, rr, kin, sa, r, h);
                 } else {
-                    if (fmt == COLI_FMT_INT4) dequant_half<COLI_FMT_INT4, false>(raw, kRS, sa, r, h);
-                    else if (fmt == COLI_FMT_INT8) dequant_half<COLI_FMT_INT8, false>(raw, kRS, sa, r, h);
-                    else dequant_half<COLI_FMT_INT2, false>(raw, kRS, sa, r, h);
+                    if (fmt == COLI_FMT_INT4) dequant_half<COLI_FMT_INT4, false>(raw, rr, kin, sa, r, h);
+                    else if (fmt == COLI_FMT_INT8) dequant_half<COLI_FMT_INT8, false>(raw, rr, kin, sa, r, h);
+                    else dequant_half<COLI_FMT_INT2, false>(raw, rr, kin, sa, r, h);
                 }
                 fence_async_smem();
                 mbar_arrive(&ts.full[a]);
+                if (kin == spc - 1 || kb == nkb - 1) {  // the chunk's last step: the raw stage is free
+                    mbar_arrive(&ts.rempty[s]);
+                    gc++;
+                }
             }
         }
     } else if (warp == kTcMmaWarp) {
@@ -512,14 +520,15 @@ __global__ void __launch_bounds__(kTcThreads, 1) moe_prefill_tc_kernel(const PfP
                 tc_fence_after_sync();
                 const uint32_t idesc = idesc_f32acc(kTcM, T.N, P.down != 0), dcol = tbase + b * kTcN;
                 for (int kb = 0; kb < nkb; kb++, gk++) {
-                    const int s = gk % kC, a = gk % kTcA;
+                    const int s = gk % kTcBS, a = gk % kTcA;
                     if (!mbar_wait_bounded(&ts.full[a], (gk / kTcA) & 1, ts, P.err)) break;
+                    if (!mbar_wait_bounded(&ts.bfull[s], (gk / kTcBS) & 1, ts, P.err)) break;
                     tc_fence_after_sync();
                     const uint32_t a0 = smem_u32(sA + a * kStageA), b0 = smem_u32(sB + s * kStageB);
 #pragma unroll
                     for (int k = 0; k < kTcKB / 16; k++)
                         tc_mma_f16kind(dcol, sdesc_k_sw128(a0 + 32 * k), sdesc_k_sw128(b0 + 32 * k), idesc, (kb | k) != 0);
-                    tc_commit(&ts.emptyc[s]);
+                    tc_commit(&ts.bempty[s]);
                     tc_commit(&ts.emptya[a]);
                 }
                 tc_commit(&ts.accf[b]);
@@ -597,6 +606,38 @@ __global__ void __launch_bounds__(kTcThreads, 1) moe_prefill_tc_kernel(const PfP
     }
 }
 
+// The tensor maps of every expert matrix: templates encoded on the host (the matrix shapes: routed
+// gate/up, routed down, shared gate/up, shared down) with each expert's base address put in on the
+// device, one warp per map, written to the workspace table with the fence that orders them before
+// any tensor copy that reads them.
+struct TmapTemplates {
+    CUtensorMap t[4];
+};
+
+__global__ void __launch_bounds__(96) tmap_build_kernel(const __grid_constant__ TmapTemplates tp,
+                                                        const coli_moe_expert *experts, coli_moe_expert shared,
+                                                        int E, CUtensorMap *out) {
+    __shared__ __align__(128) CUtensorMap sm[3];
+    const int slot = blockIdx.x, warp = threadIdx.x / 32, lane = threadIdx.x % 32;  // warp: gate, up, down
+    const bool sh = slot == E;
+    const coli_moe_expert ex = sh ? shared : experts[slot];
+    const CUtensorMap &src = tp.t[(sh ? 2 : 0) + (warp == 2 ? 1 : 0)];
+    reinterpret_cast<uint32_t *>(&sm[warp])[lane] = reinterpret_cast<const uint32_t *>(&src)[lane];
+    __syncwarp();
+    if (lane == 0) {
+        const void *addr = warp == 0 ? ex.gate_w : warp == 1 ? ex.up_w : ex.down_w;
+        asm volatile("tensormap.replace.tile.global_address.shared::cta.b1024.b64 [%0], %1;" ::"r"(smem_u32(&sm[warp])),
+                     "l"(addr)
+                     : "memory");
+    }
+    __syncwarp();
+    asm volatile(
+        "tensormap.cp_fenceproxy.global.shared::cta.tensormap::generic.release.gpu.sync.aligned [%0], [%1], 128;" ::"l"(
+            out + 3 * slot + warp),
+        "r"(smem_u32(&sm[warp]))
+        : "memory");
+}
+
 // x (fp32) -> f16 rows in bucket order (rows p < T*K: token perm[p] / K, up to offsets[E]) and
 // plain order for the shared expert (rows T*K + t), K-permuted per the rows' weight format. One
 // warp per row: row p is scaled by 2^xe[p], chosen from the row's max |x| so that the largest
@@ -661,6 +702,21 @@ __global__ void __launch_bounds__(256) prefill_prepass_kernel(const float *__res
 
 }  // namespace
 
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no link against libcuda)
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
 bool prefill_supported(const coli_moe_desc &d) {
     return d.H % 64 == 0 && d.I % 64 == 0 && d.I_shared % 64 == 0 && d.E <= kMaxE;
 }
@@ -675,7 +731,35 @@ cudaError_t launch_prefill(const PrefillWork &w, int part, cudaStream_t st) {
                                                        w.routed_fmt, w.shared_fmt, w.I_shared > 0);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
+    PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
+    if (!encode) return cudaErrorNotSupported;
+    // a 2-D map of 16-bit or 8-bit rows, boxes of 128 bytes x box_rows, 128-byte swizzle; the base
+    // address is a placeholder for the weight templates (replaced per expert on the device)
+    auto map2d = [&](CUtensorMap *m, CUtensorMapDataType dt, size_t esize, const void *base, size_t cols, size_t rows,
+                     uint32_t box_rows) {
+        const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+        const cuuint64_t strides[1] = {(cuuint64_t)(cols * esize)};
+        const cuuint32_t box[2] = {(cuuint32_t)(128 / esize), box_rows};
+        const cuuint32_t estr[2] = {1, 1};
+        return encode(m, dt, 2, const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                      CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    };
+    if (part == 0) {
+        TmapTemplates tp;
+        const int sfmt = w.I_shared > 0 ? w.shared_fmt : w.routed_fmt, Is = w.I_shared > 0 ? w.I_shared : w.I;
+        if (!map2d(&tp.t[0], CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, w.xb, row_bytes(w.routed_fmt, w.H), w.I, 64) ||
+            !map2d(&tp.t[1], CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, w.xb, row_bytes(w.routed_fmt, w.I), w.H, 128) ||
+            !map2d(&tp.t[2], CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, w.xb, row_bytes(sfmt, w.H), Is, 64) ||
+            !map2d(&tp.t[3], CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, w.xb, row_bytes(sfmt, Is), w.H, 128))
+            return cudaErrorInvalidValue;
+        coli_moe_expert sh = w.shared;
+        if (w.I_shared == 0) sh = coli_moe_expert{w.xb, w.xb, w.xb, nullptr, nullptr, nullptr};  // unused slot
+        tmap_build_kernel<<<w.E + 1, 96, 0, st>>>(tp, w.experts, sh, w.E, static_cast<CUtensorMap *>(w.tmaps));
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
     PfParams P{};
+    P.tmaps = static_cast<const CUtensorMap *>(w.tmaps);
     P.experts = w.experts;
     P.shared = w.shared;
     P.counts = w.counts;
@@ -695,13 +779,20 @@ cudaError_t launch_prefill(const PrefillWork &w, int part, cudaStream_t st) {
     P.sfmt = w.shared_fmt;
     P.ldh = w.ldh;
     P.down = part;
-    // the deeper copy ring unless an int8 matrix needs the wider raw rows
-    const bool wide = w.routed_fmt == COLI_FMT_INT8 || (w.I_shared > 0 && w.shared_fmt == COLI_FMT_INT8);
-    const void *fn = wide ? (const void *)moe_prefill_tc_kernel<RingWide> : (const void *)moe_prefill_tc_kernel<RingNarrow>;
-    const size_t smem = wide ? tc_smem_bytes<RingWide>() : tc_smem_bytes<RingNarrow>();
-    if ((e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) != cudaSuccess) return e;
-    if (wide) moe_prefill_tc_kernel<RingWide><<<w.grid, kTcThreads, smem, st>>>(P);
-    else moe_prefill_tc_kernel<RingNarrow><<<w.grid, kTcThreads, smem, st>>>(P);
+    // the tensor map of the B operand: the activation rows (f16, gate/up) or h (bf16, down),
+    // [rows][cols] 16-bit values, copied 64 columns (128 bytes) x 32 rows at a time with the
+    // 128-byte swizzle of the MMA's K-major layout; rows past the end read as zeros
+    const size_t rows = (size_t)w.T * w.K + (w.I_shared > 0 ? w.T : 0);
+    const size_t cols = part == 0 ? (size_t)w.H : (size_t)w.ldh;
+    CUtensorMap tmB;
+    if (!map2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, part == 0 ? (const void *)w.xb : (const void *)w.hb, cols, rows,
+               kBoxRows))
+        return cudaErrorInvalidValue;
+    const size_t smem = tc_smem_bytes();
+    if ((e = cudaFuncSetAttribute(moe_prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) !=
+        cudaSuccess)
+        return e;
+    moe_prefill_tc_kernel<<<w.grid, kTcThreads, smem, st>>>(P, tmB);
     return cudaGetLastError();
 }
 

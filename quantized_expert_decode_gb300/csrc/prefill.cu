@@ -20,16 +20,20 @@
 //   warp 1     activation copies: for each K-step, 2-D tensor copies (cp.async.bulk.tensor, a
 //              tensor map over the workspace's activation rows, 128-byte swizzle) of the tile's
 //              token rows straight into the B stage, in the K-major layout the MMA reads
-//   warps 2-9  dequant warps: thread (r, half) turns its half of raw row r's K-step into the
-//              swizzled 16-bit A tile, fences, and arrives on the A tile's `full`
-//   warp 10    one thread issues four tcgen05.mma (K = 16 each) per K-step into one of two TMEM
-//              accumulators and commits the A tile's and the B stage's `empty` mbarriers to
-//              their completion; after a tile's last step it commits that accumulator's `accf`
+//   warps 2-9  dequant warps: thread (r, half) turns its half of raw row r's K-step into 16
+//              columns of 16-bit pairs and stores them to the A tile in tensor memory (row r =
+//              TMEM lane r, tcgen05.st), then arrives on the A tile's `full`
+//   warp 10    one thread issues four tcgen05.mma (K = 16 each, A from tensor memory, B from
+//              shared memory) per K-step into one of two TMEM accumulators and commits the A
+//              tile's and the B stage's `empty` mbarriers to their completion; after a tile's
+//              last step it commits that accumulator's `accf`
 //   warps 11-14 epilogue: tcgen05.ld of the 128 x N tile (warp w reads TMEM lanes 32 (w % 4)..),
 //              the fused epilogue, then `tfree` hands the accumulator back to the MMA warp, so
 //              the next tile's MMAs run while the epilogue reads this one
 // The copies are issued by single threads and land without any instruction of the dequant
-// warps; the dequant warps only dequantise.
+// warps; the dequant warps only dequantise. A lives in tensor memory, so the 16-bit A tile never
+// passes through shared memory (at N ~ 64 tokens per expert the operand traffic of shared memory
+// is what limits the MMA rate).
 // K order: the dot product does not depend on the order of K, so within each block of 8 (int4)
 // or 16 (int2) elements K is permuted the same way in A and B — the order in which the
 // magic-number unpack produces bf16 pairs — and no byte shuffles are needed. The activations
@@ -54,8 +58,8 @@ namespace {
 constexpr int kTcM = 128;        // MMA M: weight rows per tile
 constexpr int kTcN = 128;        // max tokens per tile (MMA N, multiple of 16)
 constexpr int kTcKB = 64;        // K per step (one 128-byte swizzle row of 16-bit values)
-constexpr int kTcA = 3;          // A tiles (the MMA runs at most a step behind the dequant)
-constexpr int kTcBS = 4;         // B stages, one K-step of up to 128 token rows each
+constexpr int kTcA = 4;          // A tiles in tensor memory (32 columns each, after the accumulators)
+constexpr int kTcBS = 6;         // B stages, one K-step of up to 128 token rows each
 constexpr int kTcRS = 4;         // raw weight stages, one 128-byte K-chunk of the 128 rows each
 constexpr int kChunkB = 128;     // packed bytes of a row per raw stage (128-byte swizzled rows)
 constexpr int kBoxRows = 32;     // token rows per tensor copy of a B stage
@@ -95,10 +99,11 @@ struct TcSmem {  // after the 1024-aligned stage buffers
     Tile tiles[kTileCap]; // this CTA's tiles blockIdx.x + i * gridDim.x, looked up once
 };
 
-constexpr size_t kStageA = (size_t)kTcM * 128, kStageB = (size_t)kTcN * 128, kStageRaw = (size_t)kTcM * kChunkB;
-constexpr size_t tc_smem_bytes() {
-    return 1024 + kTcA * kStageA + kTcBS * kStageB + kTcRS * kStageRaw + sizeof(TcSmem);
-}
+constexpr size_t kStageB = (size_t)kTcN * 128, kStageRaw = (size_t)kTcM * kChunkB;
+constexpr size_t tc_smem_bytes() { return 1024 + kTcBS * kStageB + kTcRS * kStageRaw + sizeof(TcSmem); }
+constexpr uint32_t kTmemCols = 512;  // two accumulators of kTcN columns, then the A tiles
+constexpr uint32_t kTmemA = 2 * kTcN;
+static_assert(kTmemA + 32 * kTcA <= kTmemCols, "tensor memory holds the accumulators and the A tiles");
 
 // position of element j of a K block in the permuted order of format fmt
 __host__ __device__ __forceinline__ int kperm(int fmt, int j) {
@@ -168,11 +173,6 @@ __device__ __forceinline__ void deq16(const uint32_t *w, uint32_t (&out)[8]) {
             out[2 * i + 1] = F16 ? pack_f16(c, d) : pack_bf16(c, d);
         }
     }
-}
-
-// store 16-byte chunk c (0..7) of row r of a K-major 128-byte-swizzled tile
-__device__ __forceinline__ void st_sw128(uint8_t *tile, int r, int c, uint4 v) {
-    *reinterpret_cast<uint4 *>(tile + (r >> 3) * 1024 + (r & 7) * 128 + ((c ^ (r & 7)) << 4)) = v;
 }
 
 __device__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity, TcSmem &ts, int32_t *err) {
@@ -257,12 +257,13 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, i
         : "memory");
 }
 
-// dequantise half h of K-step kin of the tile's A row r into chunks 4h..4h+3 of row r of the
-// swizzled A tile. The raw stage holds the tensor copy of 128 rows of 128 bytes with the 128-byte
-// swizzle (16-byte chunk c of raw row rr at chunk c ^ (rr % 8)); gate/up tiles keep gate row j0 + i
-// in raw row i and up row j0 + i in raw row 64 + i, down tiles row d0 + r in raw row r.
+// dequantise half h of K-step kin of a raw row into the 16 columns (16-bit K pairs, permuted K
+// order) it fills in the A tile. The raw stage holds the tensor copy of 128 rows of 128 bytes with
+// the 128-byte swizzle (16-byte chunk c of raw row rr at chunk c ^ (rr % 8)); gate/up tiles keep
+// gate row j0 + i in raw row i and up row j0 + i in raw row 64 + i, down tiles row d0 + r in
+// raw row r.
 template <int FMT, bool F16>
-__device__ __forceinline__ void dequant_half(const uint8_t *raw, int rr, int kin, uint8_t *sa, int r, int h) {
+__device__ __forceinline__ void dequant_half(const uint8_t *raw, int rr, int kin, int h, uint32_t (&col)[16]) {
     constexpr int QH = (FMT == COLI_FMT_INT4 ? 32 : FMT == COLI_FMT_INT2 ? 16 : 64) / 2;  // bytes of the half step
     const uint8_t *row = raw + rr * kChunkB;
     const int o = kin * 2 * QH + h * QH;  // byte offset of the half step in the logical row
@@ -287,8 +288,8 @@ __device__ __forceinline__ void dequant_half(const uint8_t *raw, int rr, int kin
     for (int c2 = 0; c2 < 2; c2++) {
         uint32_t out[8];
         deq16<FMT, F16>(w + c2 * WPQ, out);
-        st_sw128(sa, r, 4 * h + 2 * c2, make_uint4(out[0], out[1], out[2], out[3]));
-        st_sw128(sa, r, 4 * h + 2 * c2 + 1, make_uint4(out[4], out[5], out[6], out[7]));
+#pragma unroll
+        for (int k = 0; k < 8; k++) col[8 * c2 + k] = out[k];
     }
 }
 
@@ -306,7 +307,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 moe_prefill_tc_kernel(const PfParams P, const __grid_constant__ CUtensorMap tmB) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
-    uint8_t *sA = smem, *sB = smem + kTcA * kStageA, *sR = sB + kTcBS * kStageB;
+    uint8_t *sB = smem, *sR = sB + kTcBS * kStageB;
     TcSmem &ts = *reinterpret_cast<TcSmem *>(sR + kTcRS * kStageRaw);
     const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
     const int nslots = P.E + (P.Is > 0 ? 1 : 0);
@@ -394,7 +395,7 @@ moe_prefill_tc_kernel(const PfParams P, const __grid_constant__ CUtensorMap tmB)
         fence_mbar_init();
     }
     if (warp == kTcMmaWarp) {
-        tmem_alloc(&ts.tmem_base, 2 * kTcN);
+        tmem_alloc(&ts.tmem_base, kTmemCols);
         tmem_relinquish();
     }
     tc_fence_before_sync();
@@ -471,7 +472,10 @@ moe_prefill_tc_kernel(const PfParams P, const __grid_constant__ CUtensorMap tmB)
         __syncwarp();
     } else if (warp < kTcMmaWarp) {
         // ---------------- dequant warps
-        const int r = (tid - kDeq0 * 32) & 127, h = (tid - kDeq0 * 32) >> 7;
+        // TMEM lanes 32 (w % 4) .. + 31 belong to warp w: row r = lane of that quarter, and
+        // warps 2-5 / 6-9 take the two halves of the K-step
+        const int r = 32 * (warp % 4) + lane, h = (warp - kDeq0) / 4;
+        const uint32_t tlane = (uint32_t)(32 * (warp % 4)) << 16;
         uint32_t g = 0, gc = 0;  // K-steps and raw chunks consumed
         bool ok = true;
         for (int t = blockIdx.x; t < total && ok; t += G) {
@@ -487,20 +491,23 @@ moe_prefill_tc_kernel(const PfParams P, const __grid_constant__ CUtensorMap tmB)
                     ok = false;
                     break;
                 }
-                uint8_t *sa = sA + a * kStageA;
+                tc_fence_after_sync();  // the MMAs that read this A tile have completed
                 const uint8_t *raw = sR + s * kStageRaw;
                 const int rr = P.down ? r : (r & 1) * 64 + (r >> 1);  // raw row of A row r
+                uint32_t col[16];
                 // gate/up: f16 (the activations are per-token scaled f16); down: bf16 (h)
                 if (!P.down) {
-                    if (fmt == COLI_FMT_INT4) dequant_half<COLI_FMT_INT4, true>(raw, rr, kin, sa, r, h);
-                    else if (fmt == COLI_FMT_INT8) dequant_half<COLI_FMT_INT8, true>(raw, rr, kin, sa, r, h);
-                    else dequant_half<COLI_FMT_INT2, true>(raw, rr, kin, sa, r, h);
+                    if (fmt == COLI_FMT_INT4) dequant_half<COLI_FMT_INT4, true>(raw, rr, kin, h, col);
+                    else if (fmt == COLI_FMT_INT8) dequant_half<COLI_FMT_INT8, true>(raw, rr, kin, h, col);
+                    else dequant_half<COLI_FMT_INT2, true>(raw, rr, kin, h, col);
                 } else {
-                    if (fmt == COLI_FMT_INT4) dequant_half<COLI_FMT_INT4, false>(raw, rr, kin, sa, r, h);
-                    else if (fmt == COLI_FMT_INT8) dequant_half<COLI_FMT_INT8, false>(raw, rr, kin, sa, r, h);
-                    else dequant_half<COLI_FMT_INT2, false>(raw, rr, kin, sa, r, h);
+                    if (fmt == COLI_FMT_INT4) dequant_half<COLI_FMT_INT4, false>(raw, rr, kin, h, col);
+                    else if (fmt == COLI_FMT_INT8) dequant_half<COLI_FMT_INT8, false>(raw, rr, kin, h, col);
+                    else dequant_half<COLI_FMT_INT2, false>(raw, rr, kin, h, col);
                 }
-                fence_async_smem();
+                tmem_st_x16(tbase + tlane + kTmemA + 32 * a + 16 * h, col);
+                tmem_st_wait();
+                tc_fence_before_sync();
                 mbar_arrive(&ts.full[a]);
                 if (kin == spc - 1 || kb == nkb - 1) {  // the chunk's last step: the raw stage is free
                     mbar_arrive(&ts.rempty[s]);
@@ -524,10 +531,10 @@ moe_prefill_tc_kernel(const PfParams P, const __grid_constant__ CUtensorMap tmB)
                     if (!mbar_wait_bounded(&ts.full[a], (gk / kTcA) & 1, ts, P.err)) break;
                     if (!mbar_wait_bounded(&ts.bfull[s], (gk / kTcBS) & 1, ts, P.err)) break;
                     tc_fence_after_sync();
-                    const uint32_t a0 = smem_u32(sA + a * kStageA), b0 = smem_u32(sB + s * kStageB);
+                    const uint32_t ta = tbase + kTmemA + 32 * a, b0 = smem_u32(sB + s * kStageB);
 #pragma unroll
-                    for (int k = 0; k < kTcKB / 16; k++)
-                        tc_mma_f16kind(dcol, sdesc_k_sw128(a0 + 32 * k), sdesc_k_sw128(b0 + 32 * k), idesc, (kb | k) != 0);
+                    for (int k = 0; k < kTcKB / 16; k++)  // K = 16: 8 columns of A, 32 bytes of each B row
+                        tc_mma_f16kind_ta(dcol, ta + 8 * k, sdesc_k_sw128(b0 + 32 * k), idesc, (kb | k) != 0);
                     tc_commit(&ts.bempty[s]);
                     tc_commit(&ts.emptya[a]);
                 }
@@ -602,7 +609,7 @@ moe_prefill_tc_kernel(const PfParams P, const __grid_constant__ CUtensorMap tmB)
     __syncthreads();
     if (warp == kTcMmaWarp) {
         tc_fence_after_sync();
-        tmem_dealloc(tbase, 2 * kTcN);
+        tmem_dealloc(tbase, kTmemCols);
     }
 }
 

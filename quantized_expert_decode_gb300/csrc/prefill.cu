@@ -476,8 +476,18 @@ moe_prefill_tc_kernel(const PfParams P, const __grid_constant__ CUtensorMap tmB)
         // warps 2-5 / 6-9 take the two halves of the K-step
         const int r = 32 * (warp % 4) + lane, h = (warp - kDeq0) / 4;
         const uint32_t tlane = (uint32_t)(32 * (warp % 4)) << 16;
+        // Software-pipelined: the store of step g to tensor memory completes while step g + 1 is
+        // dequantised; only then is step g announced to the MMA warp.
         uint32_t g = 0, gc = 0;  // K-steps and raw chunks consumed
+        int pend = -1;            // the A tile whose store is in flight, not yet announced
         bool ok = true;
+        auto announce = [&]() {
+            if (pend < 0) return;
+            tmem_st_wait();
+            tc_fence_before_sync();
+            mbar_arrive(&ts.full[pend]);
+            pend = -1;
+        };
         for (int t = blockIdx.x; t < total && ok; t += G) {
             const Tile T = tile_at(t);
             const int fmt = T.fmt, nkb = nkb_of(T), spc = spc_of(T);
@@ -505,16 +515,16 @@ moe_prefill_tc_kernel(const PfParams P, const __grid_constant__ CUtensorMap tmB)
                     else if (fmt == COLI_FMT_INT8) dequant_half<COLI_FMT_INT8, false>(raw, rr, kin, h, col);
                     else dequant_half<COLI_FMT_INT2, false>(raw, rr, kin, h, col);
                 }
-                tmem_st_x16(tbase + tlane + kTmemA + 32 * a + 16 * h, col);
-                tmem_st_wait();
-                tc_fence_before_sync();
-                mbar_arrive(&ts.full[a]);
-                if (kin == spc - 1 || kb == nkb - 1) {  // the chunk's last step: the raw stage is free
+                if (kin == spc - 1 || kb == nkb - 1) {  // the chunk's last step is read: the raw stage is free
                     mbar_arrive(&ts.rempty[s]);
                     gc++;
                 }
+                announce();  // the previous step's store has had this step's dequantisation to land
+                tmem_st_x16(tbase + tlane + kTmemA + 32 * a + 16 * h, col);
+                pend = a;
             }
         }
+        if (ok) announce();
     } else if (warp == kTcMmaWarp) {
         // ---------------- MMA issuer
         if (lane == 0) {

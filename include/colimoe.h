@@ -89,8 +89,9 @@ typedef struct {
     float top_p;          /* adaptive top-p in (0,1); 0 = off */
     int32_t group_size;   /* inputs per scale of COLI_FMT_INT4G tensors (routed and shared alike):
                              a positive multiple of 32; ignored when neither format is 4.
-                             Blocks with an int4-grouped expert run the general kernels (router
-                             launch, gate/up, down and combine launches) for every T. */
+                             Blocks with an int4-grouped expert run the single-token kernel at
+                             T = 1 and the general kernels (router launch, gate/up, down and
+                             combine launches) for every other T. */
     int32_t idot;         /* 0: exact products (the default, IDOT=0 in glm.c). 1: glm.c's IDOT
                              kernels for int8 and int4 experts (qrow_i8 / matmul_q_idot /
                              matmul_i4_idot): each activation row x (x for gate and up, h for
@@ -146,6 +147,10 @@ int coli_moe_route(const coli_moe_desc *desc, const float *x, const float *W_r,
  *    every element is exact to 2^-23 of max|v|; the integer products and their sums are exact
  *    (int32 lanes, int64 totals), then one conversion to float and the row scale. Output error
  *    within 1e-4 * rms(out) of the exact block.
+ *  - T = 1 with a COLI_FMT_INT4G expert (the rest formats 1-4): the same launch and activation
+ *    fixed point; each 16-byte chunk of a row (32 inputs, inside one group) gets its exact
+ *    integer sum, converted to float and multiplied by its group's scale, and the row's chunk
+ *    products are summed in fp32. Output error within 1e-4 * rms(out).
  *  - 2 <= T <= 64, formats 1-3: one persistent launch (plus a router launch for T > 8).
  *    Single-token expert groups run as above; groups of 2-4 tokens run on the tensor cores
  *    (mma.sync f16) with each token's vector split into two f16 parts (hi + lo, 22 significant
@@ -155,8 +160,8 @@ int coli_moe_route(const coli_moe_desc *desc, const float *x, const float *W_r,
  *    (round to nearest even) and the expert products run as tcgen05 bf16 GEMMs with fp32
  *    accumulation in tensor memory; scales and SiLU are fp32. Output error within
  *    2e-2 * rms(out).
- *  - A block with a COLI_FMT_INT4G expert, or with desc->idot set, and T > 64 shapes the GEMMs
- *    do not take: separate router, selection, bucket, gate/up, down and combine launches with
+ *  - A block with a COLI_FMT_INT4G expert at T > 1, or with desc->idot set, and T > 64 shapes
+ *    the GEMMs do not take: separate router, selection, bucket, gate/up, down and combine launches with
  *    fp32 products and fp32 accumulation (1e-4 * rms(out)); with idot, the IDOT quantisation
  *    described at coli_moe_desc.idot (2e-3 * rms(out) of the IDOT definition).
  * Results are deterministic: the same inputs give the same bits (fixed summation orders, no

@@ -200,8 +200,9 @@ int run_forward_decode(const coli_moe_desc *d, const float *x, const float *W_r,
     P.E = d->E;
     P.K = d->K;
     P.Is = d->I_shared;
-    P.rfmt = d->routed_fmt;
-    P.sfmt = d->shared_fmt;
+    // int4-grouped weights run in the int4 instances, their scales applied by group (rgs, sgs)
+    P.rfmt = d->routed_fmt == COLI_FMT_INT4G ? COLI_FMT_INT4 : d->routed_fmt;
+    P.sfmt = d->shared_fmt == COLI_FMT_INT4G ? COLI_FMT_INT4 : d->shared_fmt;
     P.Ksel = ksel_of(d);
     P.norm_topk = d->norm_topk;
     P.top_p = d->top_p;
@@ -231,9 +232,11 @@ int run_forward_decode(const coli_moe_desc *d, const float *x, const float *W_r,
 }
 
 // the persistent decode kernel's plan and grid for this description (false: not applicable):
-// the single-token kernel for T = 1 when its shared memory fits, else the token-group kernel
+// the single-token kernel for T = 1 when its shared memory fits, else the token-group kernel.
+// IDOT blocks run the general launches; int4-grouped ones the single-token kernel at T = 1 and
+// the general launches otherwise.
 bool decode_plan_for(const coli_moe_desc &d, DecParams &P, int &grid) {
-    if (general_only(d)) return false;
+    if (d.idot != 0 || (grouped(d) && d.T != 1)) return false;
     const int sms0 = num_sms();
     for (int per_sm = 2; per_sm >= 1 && d.T == 1; per_sm--) {
         DecParams Q{};
@@ -243,7 +246,7 @@ bool decode_plan_for(const coli_moe_desc &d, DecParams &P, int &grid) {
             return true;
         }
     }
-    if (!decode_supported(d)) return false;
+    if (!decode_supported(d) || grouped(d)) return false;
     const int sms = num_sms();
     grid = 2 * sms;
     if (!decode_plan(d, P, grid)) return false;

@@ -405,6 +405,62 @@ __device__ __noinline__ void gateup_run(const DecParams &P, D1S &m, const uint8_
         });
 }
 
+// B / C for int4-grouped weights (one fp32 scale per gs inputs of a row): the units of
+// gateup_run (two row pairs each), every 16-byte chunk's integer sum scaled by its group
+__device__ __noinline__ void gateup_run_grouped(const DecParams &P, D1S &m, const uint8_t *xq, int b, int e,
+                                                bool shared) {
+    static_assert(kGuRows == 4, "the grouped walk takes four rows per unit");
+    const int warp = threadIdx.x / kWarp, lane = threadIdx.x % kWarp;
+    const int nu = e - b;
+    const int mine = nu > warp ? (nu - warp + kNW - 1) / kNW : 0;
+    const int inter = shared ? P.Is : P.I;
+    const int per = (inter + 1) / 2;  // units per slot
+    const int64_t rb = row_bytes(COLI_FMT_INT4, P.H);
+    const float xinv = m.xinv;
+    const int gs = shared ? P.sgs : P.rgs;
+    auto unit = [&](int i, int &slot, int &j) {
+        const int l = b + warp + kNW * i;
+        slot = shared ? kShSlot : l / per;
+        j = 2 * (shared ? l : l - slot * per);
+    };
+    const int ng = (P.H + gs - 1) / gs;
+    warp_stream_int_grouped<COLI_FMT_INT4, kInfl1>(
+        mine, (int)(rb / 16), gs, lane,
+        [&](int i, const uint8_t *(&rr)[4]) {
+            int slot, j;
+            unit(i, slot, j);
+            const Rec &r = m.rec[slot];
+            const int j1 = min(j + 1, inter - 1);
+            rr[0] = r.gw + (size_t)j * rb;
+            rr[1] = r.uw + (size_t)j * rb;
+            rr[2] = r.gw + (size_t)j1 * rb;
+            rr[3] = r.uw + (size_t)j1 * rb;
+        },
+        [&](int i, const float *(&sr)[4]) {
+            int slot, j;
+            unit(i, slot, j);
+            const Rec &r = m.rec[slot];
+            const int j1 = min(j + 1, inter - 1);
+            sr[0] = r.gs + (size_t)j * ng;
+            sr[1] = r.us + (size_t)j * ng;
+            sr[2] = r.gs + (size_t)j1 * ng;
+            sr[3] = r.us + (size_t)j1 * ng;
+        },
+        [&](int) { return reinterpret_cast<const uint4 *>(xq); },
+        [&](int i, float tot) {  // lanes 0 / 16 hold gate j / j + 1, lanes 8 / 24 up, scaled
+            const float up = __shfl_down_sync(kFull, tot, 8);
+            int slot, j;
+            unit(i, slot, j);
+            const int q = lane >> 4;
+            if ((lane & 15) == 0 && j + q < inter) {
+                const float gv = tot * xinv, uv = up * xinv;
+                const float hv = gv / (1.f + expf(-gv)) * uv;
+                P.h[(size_t)(shared ? P.K : slot) * P.ldh + j + q] = hv;
+                atomicMax(&m.hmax[slot], __float_as_int(fabsf(hv)));
+            }
+        });
+}
+
 // the rows of a warp's first down units (slot-major units [db, de) of the grid, unit l: slot
 // l / ngr, rows 4 (l % ngr) .. + 3), asked of L2; the gate/up rows stream with an evict-first
 // policy, so these lines stay until they are read
@@ -472,6 +528,53 @@ __device__ __noinline__ void down_run(const DecParams &P, D1S &m, const uint8_t 
         });
 }
 
+// D for int4-grouped weights: the units of down_run, every chunk scaled by its group
+__device__ __noinline__ void down_run_grouped(const DecParams &P, D1S &m, const uint8_t *hq, int hs, int s0, int lo,
+                                              int hi, int ngr, int rot) {
+    const int lane = threadIdx.x % kWarp;
+    const int warp = (threadIdx.x / kWarp + kNW - rot) % kNW;
+    const int nu = hi - lo;
+    const int mine = nu > warp ? (nu - warp + kNW - 1) / kNW : 0;
+    const bool sh = P.Is > 0 && lo / ngr == m.U;
+    const int inter = sh ? P.Is : P.I;
+    const int64_t rb = row_bytes(COLI_FMT_INT4, inter);
+    const int gs = sh ? P.sgs : P.rgs;
+    auto unit = [&](int i, int &slot, int &grp) {
+        const int l = lo + warp + kNW * i;
+        slot = l / ngr;
+        grp = l - slot * ngr;
+    };
+    const int ng = (inter + gs - 1) / gs;
+    warp_stream_int_grouped<COLI_FMT_INT4, kInfl1>(
+        mine, (int)(rb / 16), gs, lane,
+        [&](int i, const uint8_t *(&rr)[4]) {
+            int slot, grp;
+            unit(i, slot, grp);
+            const Rec &r = m.rec[sh ? kShSlot : slot];
+#pragma unroll
+            for (int q = 0; q < 4; q++) rr[q] = r.dw + (size_t)min(4 * grp + q, P.H - 1) * rb;
+        },
+        [&](int i, const float *(&sr)[4]) {
+            int slot, grp;
+            unit(i, slot, grp);
+            const Rec &r = m.rec[sh ? kShSlot : slot];
+#pragma unroll
+            for (int q = 0; q < 4; q++) sr[q] = r.ds + (size_t)min(4 * grp + q, P.H - 1) * ng;
+        },
+        [&](int i) {
+            int slot, grp;
+            unit(i, slot, grp);
+            return reinterpret_cast<const uint4 *>(hq + (size_t)(slot - s0) * hs);
+        },
+        [&](int i, float tot) {  // lane 8q holds row q, scaled
+            int slot, grp;
+            unit(i, slot, grp);
+            const int d = 4 * grp + (lane >> 3);
+            if ((lane & 7) == 0 && d < P.H)
+                P.y[(size_t)(slot == m.U ? P.K : slot) * P.H + d] = tot * m.hinv[slot - s0];
+        });
+}
+
 // D: the h vectors of slots s0 .. s0 + ns - 1 as limbs (slot s0 + j at act + j * hs, in the
 // routed layout, or the shared one for slot U), each in block fixed point from the largest |h|
 // of the slot over all CTAs. A thread loads up to kHB 16-element items while threads below ns
@@ -530,7 +633,8 @@ __device__ void stage_h(const DecParams &P, D1S &m, uint8_t *act, int hs, int s0
     __syncthreads();
 }
 
-template <int RF, int SF>
+// GRP: bit 0 the routed experts, bit 1 the shared expert are int4-grouped (RF / SF then int4)
+template <int RF, int SF, int GRP>
 __global__ void __launch_bounds__(kNT, 2) moe_decode1_kernel(const DecParams P) {
     extern __shared__ __align__(128) uint8_t smem[];
     D1S &m = *reinterpret_cast<D1S *>(smem);
@@ -630,7 +734,10 @@ __global__ void __launch_bounds__(kNT, 2) moe_decode1_kernel(const DecParams P) 
         if (tid < P.E) bs[tid] = bv;
     }
     // ---------------- B: the shared expert's gate/up
-    if (be > bb) gateup_run<SF>(P, m, xq_s, bb, be, true);
+    if (be > bb) {
+        if constexpr ((GRP & 2) != 0) gateup_run_grouped(P, m, xq_s, bb, be, true);
+        else gateup_run<SF>(P, m, xq_s, bb, be, true);
+    }
 
     // ---------------- R: routing
     if (tid == 0) {
@@ -649,7 +756,8 @@ __global__ void __launch_bounds__(kNT, 2) moe_decode1_kernel(const DecParams P) 
     const int gu_per = (P.I + kGuRows / 2 - 1) / (kGuRows / 2);  // units per routed slot
     const int gu_tot = U * gu_per;
     const int cb = range_lo(gu_tot, c, G), ce = range_lo(gu_tot, c + 1, G);
-    gateup_run<RF>(P, m, xq_r, cb, ce, false);
+    if constexpr ((GRP & 1) != 0) gateup_run_grouped(P, m, xq_r, cb, ce, false);
+    else gateup_run<RF>(P, m, xq_r, cb, ce, false);
     prefetch_down(P, m, db, de, ngr);
     __syncthreads();
     if (tid < U || (tid == kShSlot && P.Is > 0))
@@ -672,8 +780,15 @@ __global__ void __launch_bounds__(kNT, 2) moe_decode1_kernel(const DecParams P) 
     {
         const int split = U * ngr;  // routed units below, shared units from here
         const int rlo = db, rhi = min(de, split), slo = max(db, split), shi = de;
-        if (rhi > rlo) down_run<RF>(P, m, act, hs, s0, rlo, rhi, ngr, 0);
-        if (shi > slo) down_run<SF>(P, m, act, hs, s0, slo, shi, ngr, rhi > rlo ? (rhi - rlo) % kNW : 0);
+        const int rot = rhi > rlo ? (rhi - rlo) % kNW : 0;
+        if (rhi > rlo) {
+            if constexpr ((GRP & 1) != 0) down_run_grouped(P, m, act, hs, s0, rlo, rhi, ngr, 0);
+            else down_run<RF>(P, m, act, hs, s0, rlo, rhi, ngr, 0);
+        }
+        if (shi > slo) {
+            if constexpr ((GRP & 2) != 0) down_run_grouped(P, m, act, hs, s0, slo, shi, ngr, rot);
+            else down_run<SF>(P, m, act, hs, s0, slo, shi, ngr, rot);
+        }
     }
     __syncthreads();
     if (tid == 0) {
@@ -710,18 +825,28 @@ __global__ void __launch_bounds__(kNT, 2) moe_decode1_kernel(const DecParams P) 
 
 using KernelFn = void (*)(DecParams);
 
-KernelFn kernel_for(int rf, int sf) {
+// rf, sf: the formats of the instance (int4-grouped weights run as int4); grp as in the kernel
+KernelFn kernel_for(int rf, int sf, int grp) {
+    constexpr int I8 = COLI_FMT_INT8, I4 = COLI_FMT_INT4, I2 = COLI_FMT_INT2;
     auto pick = [](int f) { return f == COLI_FMT_INT8 ? 0 : f == COLI_FMT_INT4 ? 1 : 2; };
-    static const KernelFn table[3][3] = {
-        {moe_decode1_kernel<COLI_FMT_INT8, COLI_FMT_INT8>, moe_decode1_kernel<COLI_FMT_INT8, COLI_FMT_INT4>,
-         moe_decode1_kernel<COLI_FMT_INT8, COLI_FMT_INT2>},
-        {moe_decode1_kernel<COLI_FMT_INT4, COLI_FMT_INT8>, moe_decode1_kernel<COLI_FMT_INT4, COLI_FMT_INT4>,
-         moe_decode1_kernel<COLI_FMT_INT4, COLI_FMT_INT2>},
-        {moe_decode1_kernel<COLI_FMT_INT2, COLI_FMT_INT8>, moe_decode1_kernel<COLI_FMT_INT2, COLI_FMT_INT4>,
-         moe_decode1_kernel<COLI_FMT_INT2, COLI_FMT_INT2>},
+    static const KernelFn plain[3][3] = {
+        {moe_decode1_kernel<I8, I8, 0>, moe_decode1_kernel<I8, I4, 0>, moe_decode1_kernel<I8, I2, 0>},
+        {moe_decode1_kernel<I4, I8, 0>, moe_decode1_kernel<I4, I4, 0>, moe_decode1_kernel<I4, I2, 0>},
+        {moe_decode1_kernel<I2, I8, 0>, moe_decode1_kernel<I2, I4, 0>, moe_decode1_kernel<I2, I2, 0>},
     };
-    return table[pick(rf)][pick(sf)];
+    // routed grouped (by the shared format), shared grouped (by the routed format), both
+    static const KernelFn rgrp[3] = {moe_decode1_kernel<I4, I8, 1>, moe_decode1_kernel<I4, I4, 1>,
+                                     moe_decode1_kernel<I4, I2, 1>};
+    static const KernelFn sgrp[3] = {moe_decode1_kernel<I8, I4, 2>, moe_decode1_kernel<I4, I4, 2>,
+                                     moe_decode1_kernel<I2, I4, 2>};
+    if (grp == 3) return moe_decode1_kernel<I4, I4, 3>;
+    if (grp == 1) return rgrp[pick(sf)];
+    if (grp == 2) return sgrp[pick(rf)];
+    return plain[pick(rf)][pick(sf)];
 }
+
+// the grouped bits of a plan
+int grp_of(const DecParams &P) { return (P.rgs > 0 ? 1 : 0) | (P.sgs > 0 ? 2 : 0); }
 
 size_t decode1_smem_bytes(const DecParams &P) { return (size_t)P.d1_end; }
 
@@ -732,8 +857,11 @@ bool decode1_plan(const coli_moe_desc &d, DecParams &P, int grid) {
     if (d.T != 1 || d.K > kMaxK || d.E > kMaxE) return false;
     P.single = 1;
     P.K = d.K;
-    P.rfmt = d.routed_fmt;
-    P.sfmt = d.shared_fmt;
+    // int4-grouped weights run in the int4 instances, their scales applied per 16-byte chunk
+    P.rfmt = d.routed_fmt == COLI_FMT_INT4G ? COLI_FMT_INT4 : d.routed_fmt;
+    P.sfmt = d.shared_fmt == COLI_FMT_INT4G ? COLI_FMT_INT4 : d.shared_fmt;
+    P.rgs = d.routed_fmt == COLI_FMT_INT4G ? d.group_size : 0;
+    P.sgs = d.I_shared > 0 && d.shared_fmt == COLI_FMT_INT4G ? d.group_size : 0;
     P.NV = 1;
     P.route_only = 0;
     P.neb = (d.E + kRtE - 1) / kRtE;
@@ -746,7 +874,7 @@ bool decode1_plan(const coli_moe_desc &d, DecParams &P, int grid) {
     if (P.R > grid) return false;
     P.groups_sh = d.I_shared > 0 ? 1 : 0;
     P.G_sh = d.I_shared > 0 ? (d.I_shared + kGuRows / 2 - 1) / (kGuRows / 2) : 0;  // shared gate/up units
-    const bool two = d.I_shared > 0 && d.shared_fmt != d.routed_fmt;
+    const bool two = d.I_shared > 0 && P.sfmt != P.rfmt;
     const size_t x_bytes = (size_t)3 * d.H * (two ? 2 : 1);
     P.d1_hs = 3 * std::max(d.I, d.I_shared);  // limbs of one staged h vector (a multiple of 16)
     // the slots one CTA's down units can touch: its share of (K + 1) * ngr units over `grid`
@@ -783,7 +911,7 @@ bool decode1_plan(const coli_moe_desc &d, DecParams &P, int grid) {
 
 int decode1_ctas_per_sm(const DecParams &P) {
     int n = 0;
-    const void *fn = (const void *)kernel_for(P.rfmt, P.sfmt);
+    const void *fn = (const void *)kernel_for(P.rfmt, P.sfmt, grp_of(P));
     const size_t smem = decode1_smem_bytes(P);
     // the query counts against the kernel's dynamic shared-memory limit: raise it first
     if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) return 0;
@@ -793,7 +921,7 @@ int decode1_ctas_per_sm(const DecParams &P) {
 
 cudaError_t launch_decode1(const DecParams &P, int grid, cudaStream_t st) {
     const size_t smem = decode1_smem_bytes(P);
-    const void *fn = (const void *)kernel_for(P.rfmt, P.sfmt);
+    const void *fn = (const void *)kernel_for(P.rfmt, P.sfmt, grp_of(P));
     cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     void *args[] = {const_cast<DecParams *>(&P)};

@@ -122,6 +122,111 @@ __device__ __forceinline__ void warp_stream_int(int nunits, int CPR, int lane, R
     }
 }
 
+// Four rows of float lane partials at once, transposing as it reduces (the shuffle pattern of
+// idot_reduce4): every lane ends with the total of row lane / 8.
+__device__ __forceinline__ float freduce4(const float (&p)[4], int lane) {
+    const bool h16 = (lane & 16) != 0, h8 = (lane & 8) != 0;
+    float k0 = h16 ? p[2] : p[0], k1 = h16 ? p[3] : p[1];
+    const float s0 = h16 ? p[0] : p[2], s1 = h16 ? p[1] : p[3];
+    k0 += __shfl_xor_sync(kFull, s0, 16);
+    k1 += __shfl_xor_sync(kFull, s1, 16);
+    float k = h8 ? k1 : k0;
+    k += __shfl_xor_sync(kFull, h8 ? k0 : k1, 8);
+    k += __shfl_xor_sync(kFull, k, 4);
+    k += __shfl_xor_sync(kFull, k, 2);
+    k += __shfl_xor_sync(kFull, k, 1);
+    return k;
+}
+
+// The integer walk for int4-grouped rows (one fp32 scale per gs inputs of a row, gs a multiple of
+// 32, so a 16-byte chunk lies in one group): each chunk's limb sums (exact integers, multiples of
+// 2^LOG_SC) are converted to float, joined and multiplied by the chunk's group scale as the chunk
+// is consumed; the rows' float partials are reduced across the warp at the unit's end. Lane l
+// takes chunks l + 32 k, whose group it tracks incrementally (no division per chunk), and loads
+// each chunk's scale with its weights. scl_of(i, sr) gives unit i's rows' scale rows
+// ([ceil(In / gs)] floats each); epi(i, tot) gets, in lane l, the scaled total of row l / 8 (in
+// units of the activations' fixed point).
+template <int FMT, int INFL, class RowsOf, class SclOf, class XqOf, class Epi>
+__device__ __forceinline__ void warp_stream_int_grouped(int nunits, int CPR, int gs, int lane, RowsOf rows_of,
+                                                        SclOf scl_of, XqOf xq_of, Epi epi) {
+    constexpr int NR = 4, kDepth = INFL / NR;
+    constexpr int LS = IQ<FMT>::LOG_SC;
+    constexpr float k0 = 1.f / (1 << LS), k1 = 256.f / (1 << LS), k2 = 65536.f / (1 << LS);
+    if (nunits <= 0) return;
+    const int S = (CPR + kWarp - 1) / kWarp;
+    const int total = nunits * S;
+    const int cpg = gs / 32;  // 16-byte int4 chunks per group
+    // group of chunk lane + 32 k: starts at lane / cpg and advances by 32 chunks a step
+    const int g0 = lane / cpg, r0 = lane - g0 * cpg, gq = kWarp / cpg, gr = kWarp - gq * cpg;
+    int ig = g0, irem = r0;
+    uint4 buf[kDepth][NR];
+    float sbuf[kDepth][NR];
+    int iu = 0, ik = 0;
+    const uint8_t *rr[NR];
+    const float *sr[NR];
+    rows_of(0, rr);
+    scl_of(0, sr);
+    auto issue = [&](uint4 (&b)[NR], float (&sb)[NR]) {
+        if (iu < nunits) {
+            const int c = lane + kWarp * ik;
+#pragma unroll
+            for (int r = 0; r < NR; r++) {
+                b[r] = c < CPR ? ld_stream_16(rr[r] + 16 * c) : make_uint4(0, 0, 0, 0);
+                sb[r] = c < CPR ? __ldg(sr[r] + ig) : 0.f;
+            }
+            if (++ik == S) {
+                ik = 0;
+                ig = g0;
+                irem = r0;
+                if (++iu < nunits) {
+                    rows_of(iu, rr);
+                    scl_of(iu, sr);
+                }
+            } else {
+                ig += gq;
+                irem += gr;
+                if (irem >= cpg) {
+                    irem -= cpg;
+                    ig++;
+                }
+            }
+        }
+    };
+#pragma unroll
+    for (int j = 0; j < kDepth; j++) issue(buf[j], sbuf[j]);
+    float facc[NR] = {0.f, 0.f, 0.f, 0.f};
+    int cu = 0, ck = 0;
+    const uint4 *xq4 = xq_of(0);
+    for (int s0 = 0; s0 < total; s0 += kDepth) {
+#pragma unroll
+        for (int j = 0; j < kDepth; j++) {
+            if (s0 + j < total) {
+                const int c = lane + kWarp * ck;
+                if (c < CPR) {
+                    int acc[NR][3];
+#pragma unroll
+                    for (int r = 0; r < NR; r++) acc[r][0] = acc[r][1] = acc[r][2] = 0;
+                    idot_chunk<FMT, NR>(buf[j], xq4, CPR, c, acc);
+#pragma unroll
+                    for (int r = 0; r < NR; r++) {
+                        const float v = fmaf((float)acc[r][2], k2, fmaf((float)acc[r][1], k1, (float)acc[r][0] * k0));
+                        facc[r] = fmaf(v, sbuf[j][r], facc[r]);
+                    }
+                }
+                issue(buf[j], sbuf[j]);
+                if (++ck == S) {
+                    epi(cu, freduce4(facc, lane));
+#pragma unroll
+                    for (int r = 0; r < NR; r++) facc[r] = 0.f;
+                    ck = 0;
+                    cu++;
+                    if (cu < nunits) xq4 = xq_of(cu);
+                }
+            }
+        }
+    }
+}
+
 // The walk for multi-token groups on the tensor-core core (mma.cuh): blocks of 16 rows, lane
 // (g, c) streaming chunk 4*sigma + c of rows g and g + 8 (rows_of(i, rr) gives block i's two row
 // pointers for this lane), two segments of loads in flight across block boundaries (deeper

@@ -55,6 +55,7 @@ struct DecParams {
     float *h, *y;
     DecCtrl *ctrl;
     int T, H, I, E, K, Is, rfmt, sfmt, Ksel, norm_topk;
+    int rgs, sgs;              // inputs per scale of int4-grouped routed / shared weights (0: per-row scales)
     float top_p, rscale;
     int ldh;
     int NV, xs_stride, xs_bytes, rt_bytes;

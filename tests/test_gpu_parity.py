@@ -449,6 +449,13 @@ GROUPED = [
     ("g32-shared-only", dict(T=3, H=256, I=128, E=8, K=2, I_shared=128, routed_fmt=2, shared_fmt=4,
                              group_size=32)),
     ("g64-long", dict(T=70, H=128, I=64, E=9, K=2, I_shared=64, group_size=64)),
+    # T = 1 runs the single-token kernel, each chunk's integer sum scaled by its group
+    ("g128-one-token-large", dict(T=1, H=6144, I=2048, E=256, K=8, I_shared=2048, group_size=128)),
+    ("g96-one-token-ragged", dict(T=1, H=352, I=160, E=12, K=3, I_shared=96, group_size=96)),
+    ("g64-one-token-int8-shared", dict(T=1, H=256, I=128, E=16, K=4, I_shared=128, shared_fmt=1,
+                                       group_size=64)),
+    ("g32-one-token-int2-routed", dict(T=1, H=256, I=128, E=16, K=4, I_shared=128, routed_fmt=3,
+                                       shared_fmt=4, group_size=32)),
 ]
 
 
@@ -508,6 +515,8 @@ TAILS = [
     ("token-group", dict(T=6, H=512, I=256, E=32, K=4, I_shared=128, routed_fmt=2, shared_fmt=1), True),
     ("tensor-core", dict(T=96, H=256, I=128, E=16, K=2, I_shared=128, routed_fmt=2, shared_fmt=2), False),
     ("grouped", dict(T=3, H=256, I=128, E=8, K=2, I_shared=64, routed_fmt=4, shared_fmt=4, group_size=64), False),
+    ("grouped-one-token", dict(T=1, H=256, I=128, E=8, K=2, I_shared=64, routed_fmt=4, shared_fmt=4,
+                               group_size=64), True),
 ]
 
 

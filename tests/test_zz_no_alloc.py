@@ -6,8 +6,8 @@ entry point runs the same block on a fixed scratch array inside the library's de
 The tests compare it with coli_moe_forward on the same inputs, two calls in a row (the second
 on fresh activations, so stale scratch from the first call would show), on every path the
 fixed array can serve: the single-token kernel, the token-group kernel, the tensor-core GEMMs
-(T > 64, which reuse the scratch for bf16 activations) and the general kernels of an
-int4-grouped block. Both entry points run the same deterministic kernels, so the outputs must
+(T > 64, which reuse the scratch for bf16 activations), the general kernels of an
+int4-grouped block and the single-token kernel on int4-grouped weights. Both entry points run the same deterministic kernels, so the outputs must
 be identical bit for bit; the fixed array's error word must read clear afterwards. A
 description needing more than the fixed scratch is refused. The tests build their own inputs,
 so they pass alone in a fresh process as well as after the rest of the suite; the file name
@@ -29,6 +29,8 @@ CASES = [
                                routed_fmt=2, shared_fmt=2, zipf=False)),
     ("int4-grouped", dict(T=5, H=512, I=256, E=12, K=3, I_shared=128, norm_topk=1, routed_scale=2.5,
                           routed_fmt=4, shared_fmt=4, group_size=64, zipf=False)),
+    ("int4-grouped-one-token", dict(T=1, H=512, I=256, E=12, K=3, I_shared=128, norm_topk=1, routed_scale=2.5,
+                                    routed_fmt=4, shared_fmt=4, group_size=64, zipf=False)),
 ]
 
 

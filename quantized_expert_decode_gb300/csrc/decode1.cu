@@ -10,7 +10,9 @@
 //      slice's router rows and x in flight together
 //   X  the expert table and the bias copied into shared memory; the token's x in 24-bit block
 //      fixed point (idot.cuh), in the layout of each weight format the block uses
-//   B  shared expert gate/up rows (independent of routing), spread over every CTA
+//   B  shared expert gate/up rows (independent of routing), spread over every CTA: here only
+//      when the shared expert's walk differs from the routed experts' (another format); else
+//      its units follow each CTA's routed units in phase C, one stream of loads through both
 //   R  routing by EVERY CTA from the partial logits: logits summed in a fixed order, sigmoid,
 //      bias, greedy top-K with ties to the lower index (select.cuh), TOPK/TOPP, renorm, routed
 //      scale. The kept experts become slots 0..U-1 in ascending id order; the shared expert is
@@ -344,32 +346,43 @@ __device__ __forceinline__ void route1(const DecParams &P, D1S &m, float *sg, fl
     }
 }
 
-// B / C: gate/up units [b, e) (shared: the shared expert's, else slot-major over the routed
-// slots; kGuRows / 2 row pairs j, j + 1 .. of gate and of up per unit); warps take units
-// round-robin, no barriers
-// (warps wfirst .. wfirst + wcount - 1 of the CTA take part)
+// The CTA's gate/up units: routed units [rb0, re0) of the slot-major routed space (kGuRows / 2
+// row pairs j, j + 1 .. of gate and of up of one slot per unit), then the shared expert's units
+// [sb0, se0). Warps take the combined list round-robin, with no barriers, so one stream of loads
+// runs through both when the formats agree.
+// list entry w -> slot (kShSlot for the shared expert) and first row j; per: units per routed
+// slot, nr: routed units in the list
+__device__ __forceinline__ void gu_unit(int per, int rb, int nr, int sb, int w, int &slot, int &j) {
+    constexpr int NP = kGuRows / 2;
+    if (w < nr) {
+        const int l = rb + w;
+        slot = l / per;
+        j = NP * (l - slot * per);
+    } else {
+        slot = kShSlot;
+        j = NP * (sb + w - nr);
+    }
+}
+
+// B / C: the units of g; warps wfirst .. wfirst + wcount - 1 of the CTA take part
 template <int FMT>
-__device__ __noinline__ void gateup_run(const DecParams &P, D1S &m, const uint8_t *xq, int b, int e, bool shared,
-                                        int wfirst = 0, int wcount = kNW) {
+__device__ __noinline__ void gateup_run(const DecParams &P, D1S &m, const uint8_t *xq, int rb0, int re0, int sb0,
+                                        int se0, int wfirst = 0, int wcount = kNW) {
     constexpr int NP = kGuRows / 2;  // row pairs per unit
     const int warp = threadIdx.x / kWarp - wfirst, lane = threadIdx.x % kWarp;
-    const int nu = e - b;
+    const int nr = re0 - rb0, nu = nr + (se0 - sb0);
     const int mine = nu > warp ? (nu - warp + wcount - 1) / wcount : 0;
-    const int inter = shared ? P.Is : P.I;
-    const int per = (inter + NP - 1) / NP;  // units per slot
     const int64_t rb = row_bytes(FMT, P.H);
     const float xinv = m.xinv;
-    auto unit = [&](int i, int &slot, int &j) {
-        const int l = b + warp + wcount * i;
-        slot = shared ? kShSlot : l / per;
-        j = NP * (shared ? l : l - slot * per);
-    };
+    const int per = (P.I + NP - 1) / NP;
+    auto unit = [&](int i, int &slot, int &j) { gu_unit(per, rb0, nr, sb0, warp + wcount * i, slot, j); };
     warp_stream_int<FMT, kGuRows, kInfl1, kOnce>(
         mine, (int)(rb / 16), lane,
         [&](int i, const uint8_t *(&rr)[kGuRows]) {
             int slot, j;
             unit(i, slot, j);
             const Rec &r = m.rec[slot];
+            const int inter = slot == kShSlot ? P.Is : P.I;
 #pragma unroll
             for (int q = 0; q < NP; q++) {
                 const int jq = min(j + q, inter - 1);
@@ -382,6 +395,7 @@ __device__ __noinline__ void gateup_run(const DecParams &P, D1S &m, const uint8_
             int slot, j;
             unit(i, slot, j);
             const Rec &r = m.rec[slot];
+            const int inter = slot == kShSlot ? P.Is : P.I;
             const int jq = min(j + (NP > 1 ? lane >> 4 : 0), inter - 1);
             const bool ld = NP > 1 ? (lane & 15) == 0 : lane == 0;
             return ld ? make_float2(__ldg(r.gs + jq), __ldg(r.us + jq)) : make_float2(0.f, 0.f);
@@ -393,13 +407,14 @@ __device__ __noinline__ void gateup_run(const DecParams &P, D1S &m, const uint8_
             const long long up = __shfl_down_sync(kFull, tot, UPD);
             int slot, j;
             unit(i, slot, j);
+            const int inter = slot == kShSlot ? P.Is : P.I;
             const int q = kGuRows == 2 ? 0 : (lane >> 4);
             const bool mine_row = kGuRows == 2 ? lane == 0 : (lane & 15) == 0;
             if (mine_row && j + q < inter) {
                 const float gv = (__ll2float_rn(tot) * xinv) * sc.x;
                 const float uv = (__ll2float_rn(up) * xinv) * sc.y;
                 const float hv = gv / (1.f + expf(-gv)) * uv;
-                P.h[(size_t)(shared ? P.K : slot) * P.ldh + j + q] = hv;
+                P.h[(size_t)(slot == kShSlot ? P.K : slot) * P.ldh + j + q] = hv;
                 atomicMax(&m.hmax[slot], __float_as_int(fabsf(hv)));
             }
         });
@@ -407,22 +422,18 @@ __device__ __noinline__ void gateup_run(const DecParams &P, D1S &m, const uint8_
 
 // B / C for int4-grouped weights (one fp32 scale per gs inputs of a row): the units of
 // gateup_run (two row pairs each), every 16-byte chunk's integer sum scaled by its group
-__device__ __noinline__ void gateup_run_grouped(const DecParams &P, D1S &m, const uint8_t *xq, int b, int e,
-                                                bool shared) {
+__device__ __noinline__ void gateup_run_grouped(const DecParams &P, D1S &m, const uint8_t *xq, int rb0, int re0,
+                                                int sb0, int se0) {
     static_assert(kGuRows == 4, "the grouped walk takes four rows per unit");
     const int warp = threadIdx.x / kWarp, lane = threadIdx.x % kWarp;
-    const int nu = e - b;
+    const int nr = re0 - rb0, nu = nr + (se0 - sb0);
     const int mine = nu > warp ? (nu - warp + kNW - 1) / kNW : 0;
-    const int inter = shared ? P.Is : P.I;
-    const int per = (inter + 1) / 2;  // units per slot
     const int64_t rb = row_bytes(COLI_FMT_INT4, P.H);
     const float xinv = m.xinv;
-    const int gs = shared ? P.sgs : P.rgs;
-    auto unit = [&](int i, int &slot, int &j) {
-        const int l = b + warp + kNW * i;
-        slot = shared ? kShSlot : l / per;
-        j = 2 * (shared ? l : l - slot * per);
-    };
+    const int per = (P.I + 1) / 2;
+    auto unit = [&](int i, int &slot, int &j) { gu_unit(per, rb0, nr, sb0, warp + kNW * i, slot, j); };
+    // both lists of one call are int4-grouped with the same group size
+    const int gs = nr > 0 ? P.rgs : P.sgs;
     const int ng = (P.H + gs - 1) / gs;
     warp_stream_int_grouped<COLI_FMT_INT4, kInfl1>(
         mine, (int)(rb / 16), gs, lane,
@@ -430,7 +441,7 @@ __device__ __noinline__ void gateup_run_grouped(const DecParams &P, D1S &m, cons
             int slot, j;
             unit(i, slot, j);
             const Rec &r = m.rec[slot];
-            const int j1 = min(j + 1, inter - 1);
+            const int j1 = min(j + 1, (slot == kShSlot ? P.Is : P.I) - 1);
             rr[0] = r.gw + (size_t)j * rb;
             rr[1] = r.uw + (size_t)j * rb;
             rr[2] = r.gw + (size_t)j1 * rb;
@@ -440,7 +451,7 @@ __device__ __noinline__ void gateup_run_grouped(const DecParams &P, D1S &m, cons
             int slot, j;
             unit(i, slot, j);
             const Rec &r = m.rec[slot];
-            const int j1 = min(j + 1, inter - 1);
+            const int j1 = min(j + 1, (slot == kShSlot ? P.Is : P.I) - 1);
             sr[0] = r.gs + (size_t)j * ng;
             sr[1] = r.us + (size_t)j * ng;
             sr[2] = r.gs + (size_t)j1 * ng;
@@ -452,10 +463,10 @@ __device__ __noinline__ void gateup_run_grouped(const DecParams &P, D1S &m, cons
             int slot, j;
             unit(i, slot, j);
             const int q = lane >> 4;
-            if ((lane & 15) == 0 && j + q < inter) {
+            if ((lane & 15) == 0 && j + q < (slot == kShSlot ? P.Is : P.I)) {
                 const float gv = tot * xinv, uv = up * xinv;
                 const float hv = gv / (1.f + expf(-gv)) * uv;
-                P.h[(size_t)(shared ? P.K : slot) * P.ldh + j + q] = hv;
+                P.h[(size_t)(slot == kShSlot ? P.K : slot) * P.ldh + j + q] = hv;
                 atomicMax(&m.hmax[slot], __float_as_int(fabsf(hv)));
             }
         });
@@ -733,10 +744,12 @@ __global__ void __launch_bounds__(kNT, 2) moe_decode1_kernel(const DecParams P) 
             if (tid + k * kNT < n8) ts[tid + k * kNT] = tv[k];
         if (tid < P.E) bs[tid] = bv;
     }
-    // ---------------- B: the shared expert's gate/up
-    if (be > bb) {
-        if constexpr ((GRP & 2) != 0) gateup_run_grouped(P, m, xq_s, bb, be, true);
-        else gateup_run<SF>(P, m, xq_s, bb, be, true);
+    // ---------------- B: the shared expert's gate/up, here only when its walk differs from the
+    // routed experts' (else its units follow the routed ones in one stream, phase C)
+    constexpr bool kMerged = RF == SF && ((GRP & 1) != 0) == ((GRP & 2) != 0);
+    if (!kMerged && be > bb) {
+        if constexpr ((GRP & 2) != 0) gateup_run_grouped(P, m, xq_s, 0, 0, bb, be);
+        else gateup_run<SF>(P, m, xq_s, 0, 0, bb, be);
     }
 
     // ---------------- R: routing
@@ -756,8 +769,8 @@ __global__ void __launch_bounds__(kNT, 2) moe_decode1_kernel(const DecParams P) 
     const int gu_per = (P.I + kGuRows / 2 - 1) / (kGuRows / 2);  // units per routed slot
     const int gu_tot = U * gu_per;
     const int cb = range_lo(gu_tot, c, G), ce = range_lo(gu_tot, c + 1, G);
-    if constexpr ((GRP & 1) != 0) gateup_run_grouped(P, m, xq_r, cb, ce, false);
-    else gateup_run<RF>(P, m, xq_r, cb, ce, false);
+    if constexpr ((GRP & 1) != 0) gateup_run_grouped(P, m, xq_r, cb, ce, kMerged ? bb : 0, kMerged ? be : 0);
+    else gateup_run<RF>(P, m, xq_r, cb, ce, kMerged ? bb : 0, kMerged ? be : 0);
     prefetch_down(P, m, db, de, ngr);
     __syncthreads();
     if (tid < U || (tid == kShSlot && P.Is > 0))

@@ -366,10 +366,11 @@ def run_colimoe(args, rank, world, local):
     # decode (T <= 64) does all its work between events 0 and 2 (the counter memset, the router
     # launch for T > 8, the persistent kernel); events 3 and 4 follow with no work between them
     # and only add the recording overhead of an event pair, so they are not part of the step
-    # int4-grouped blocks run the single-token kernel at T = 1 and the general launches (router,
-    # gate/up, down, combine) for other T; IDOT blocks run the general launches for any T
+    # int4-grouped and IDOT blocks run the single-token kernel at T = 1 (not both at once) and
+    # the general launches (router, gate/up, down, combine) for other T
     grouped = bool(cfg.get("group_size", 0)) and synth.FMT_INT4G in (cfg["routed_fmt"], cfg["shared_fmt"])
-    general = (grouped and T != 1) or bool(cfg.get("idot", 0))
+    idot = bool(cfg.get("idot", 0))
+    general = (T != 1 and (grouped or idot)) or (grouped and idot)
     fused = T <= DECODE_MAX_T and not general
     step_ms = stage[:, :2].sum(axis=1) if fused else stage.sum(axis=1)
     total_s = float(step_ms.sum()) / 1e3

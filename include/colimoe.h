@@ -90,8 +90,8 @@ typedef struct {
     int32_t group_size;   /* inputs per scale of COLI_FMT_INT4G tensors (routed and shared alike):
                              a positive multiple of 32; ignored when neither format is 4.
                              Blocks with an int4-grouped expert run the single-token kernel at
-                             T = 1 and the general kernels (router launch, gate/up, down and
-                             combine launches) for every other T. */
+                             T = 1 (unless idot is also set) and the general kernels (router
+                             launch, gate/up, down and combine launches) for every other T. */
     int32_t idot;         /* 0: exact products (the default, IDOT=0 in glm.c). 1: glm.c's IDOT
                              kernels for int8 and int4 experts (qrow_i8 / matmul_q_idot /
                              matmul_i4_idot): each activation row x (x for gate and up, h for
@@ -99,7 +99,9 @@ typedef struct {
                              s = max(max|x| / 127, 1e-12), the integer sum of deq(W) * q is exact,
                              and y[o] = ((float)sum * scale[o]) * s — lossy (about 0.3 % RMS per
                              product, as the pages state). int2 and int4-grouped experts keep the
-                             exact path. Runs the general kernels for every T. */
+                             exact path. T = 1 runs the single-token kernel (int8 bytes on the
+                             DP4A core; with an int4-grouped expert in the block, the general
+                             kernels); other T the general kernels. */
 } coli_moe_desc;
 
 /* One expert's six device pointers: gate/up are [I][row_bytes(H)] with fp32 scales [I];
@@ -160,8 +162,11 @@ int coli_moe_route(const coli_moe_desc *desc, const float *x, const float *W_r,
  *    (round to nearest even) and the expert products run as tcgen05 bf16 GEMMs with fp32
  *    accumulation in tensor memory; scales and SiLU are fp32. Output error within
  *    2e-2 * rms(out).
- *  - A block with a COLI_FMT_INT4G expert at T > 1, or with desc->idot set, and T > 64 shapes
- *    the GEMMs do not take: separate router, selection, bucket, gate/up, down and combine launches with
+ *  - T = 1 with desc->idot set: the same launch on the IDOT quantisation (int8 activations, one
+ *    scale per vector, exact int32 sums, y = ((float)dot * scale) * s), as described at
+ *    coli_moe_desc.idot; within 2e-3 * rms(out) of the IDOT definition.
+ *  - A block with a COLI_FMT_INT4G expert at T > 1, or with desc->idot set at T > 1, and T > 64
+ *    shapes the GEMMs do not take: separate router, selection, bucket, gate/up, down and combine launches with
  *    fp32 products and fp32 accumulation (1e-4 * rms(out)); with idot, the IDOT quantisation
  *    described at coli_moe_desc.idot (2e-3 * rms(out) of the IDOT definition).
  * Results are deterministic: the same inputs give the same bits (fixed summation orders, no

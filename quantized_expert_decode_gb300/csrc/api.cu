@@ -53,7 +53,7 @@ bool grouped(const coli_moe_desc &d) {
     return d.routed_fmt == COLI_FMT_INT4G || (d.I_shared > 0 && d.shared_fmt == COLI_FMT_INT4G);
 }
 
-// blocks that run the general launches: a grouped expert, or the IDOT kernels requested
+// blocks that run the general launches for T > 1: a grouped expert, or the IDOT kernels requested
 bool general_only(const coli_moe_desc &d) { return grouped(d) || d.idot != 0; }
 
 // group sizes the grouped kernels take: whole 16-byte chunks (32 int4 inputs) per group
@@ -233,10 +233,10 @@ int run_forward_decode(const coli_moe_desc *d, const float *x, const float *W_r,
 
 // the persistent decode kernel's plan and grid for this description (false: not applicable):
 // the single-token kernel for T = 1 when its shared memory fits, else the token-group kernel.
-// IDOT blocks run the general launches; int4-grouped ones the single-token kernel at T = 1 and
-// the general launches otherwise.
+// IDOT and int4-grouped blocks run the single-token kernel at T = 1 (not both at once) and the
+// general launches otherwise.
 bool decode_plan_for(const coli_moe_desc &d, DecParams &P, int &grid) {
-    if (d.idot != 0 || (grouped(d) && d.T != 1)) return false;
+    if (general_only(d) && d.T != 1) return false;
     const int sms0 = num_sms();
     for (int per_sm = 2; per_sm >= 1 && d.T == 1; per_sm--) {
         DecParams Q{};
@@ -246,7 +246,7 @@ bool decode_plan_for(const coli_moe_desc &d, DecParams &P, int &grid) {
             return true;
         }
     }
-    if (!decode_supported(d) || grouped(d)) return false;
+    if (!decode_supported(d) || general_only(d)) return false;
     const int sms = num_sms();
     grid = 2 * sms;
     if (!decode_plan(d, P, grid)) return false;

@@ -807,7 +807,7 @@ __device__ int run_queue(const DecParams &P, const RTab &rt, int tot, int *q, bo
 }
 
 template <int NV>
-__global__ void __launch_bounds__(kNT, 2) moe_decode_kernel(const DecParams P) {
+__global__ void __launch_bounds__(kNT, 2) moe_decode_kernel(const __grid_constant__ DecParams P) {
     extern __shared__ __align__(128) uint8_t smem[];
     void *xs = smem;
     const RTab rt = rtab_of(smem + P.xs_bytes, P.T, P.E, P.K);

@@ -62,6 +62,9 @@ struct D1S {  // the fixed part of the CTA's shared memory
     float xinv;
     int hshift[kMaxK + 1];  // per slot (shared: at U) in the down phase
     float hinv[kMaxK + 1];
+    float hamax[kMaxK + 1]; // max |h| of each staged slot (the int8 quantisation's amax)
+    float hsq[kMaxK + 1];   // ... and its int8 scale
+    float xsq;              // the int8 scale of x
     int hmax[kMaxK + 1];    // this CTA's max |h| per slot (float bits); shared at kShSlot
     float redf[kNW];
     double redd[kNW];
@@ -157,7 +160,8 @@ __device__ __forceinline__ void limbs_from_regs(const float4 (&v)[4], uint8_t *x
         xq4[(ss * 3 + j) * CPR + c] = make_uint4(o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
 }
 
-template <int RF, int SF>
+// RQ / SQ: the routed / shared side takes int8 bytes (the IDOT quantisation) instead of limbs
+template <int RF, int SF, bool RQ, bool SQ>
 __device__ void stage_x(const DecParams &P, const float *xsrc, uint8_t *xq_r, uint8_t *xq_s, bool two, D1S &m) {
     const int tid = threadIdx.x, lane = tid % kWarp, warp = tid / kWarp;
     const int n16 = P.H / 16;  // 16-element groups; group q is item q of every layout ordering
@@ -190,6 +194,7 @@ __device__ void stage_x(const DecParams &P, const float *xsrc, uint8_t *xq_r, ui
     for (int w = 1; w < kNW; w++) mx = fmaxf(mx, m.redf[w]);
     const int s = fixed_shift(mx);
     const FixedScale fx(s);
+    const Q8Scale qs(mx);
     // the 16 elements of group q are item q of a layout whose items are (ss, c) with
     // p = ss * CPR + c covering elements c * EPC + ss * 16: map q to that p
     auto item_of = [&](int fmt_epc, int fmt_nss, int q) {
@@ -211,15 +216,21 @@ __device__ void stage_x(const DecParams &P, const float *xsrc, uint8_t *xq_r, ui
         for (int j = 0; j < 2; j++) {
             const int q = q0 + j * kNT;
             if (q < n16) {
-                limbs_from_regs<RF>(v[j], xq_r, P.H / QGeom<RF>::EPC, item_of(QGeom<RF>::EPC, IQ<RF>::NSS, q), fx);
-                if (two)
-                    limbs_from_regs<SF>(v[j], xq_s, P.H / QGeom<SF>::EPC, item_of(QGeom<SF>::EPC, IQ<SF>::NSS, q), fx);
+                const int pr = item_of(QGeom<RF>::EPC, IQ<RF>::NSS, q);
+                if constexpr (RQ) q8_from_regs<RF>(v[j], xq_r, P.H / QGeom<RF>::EPC, pr, qs);
+                else limbs_from_regs<RF>(v[j], xq_r, P.H / QGeom<RF>::EPC, pr, fx);
+                if (two) {
+                    const int ps = item_of(QGeom<SF>::EPC, IQ<SF>::NSS, q);
+                    if constexpr (SQ) q8_from_regs<SF>(v[j], xq_s, P.H / QGeom<SF>::EPC, ps, qs);
+                    else limbs_from_regs<SF>(v[j], xq_s, P.H / QGeom<SF>::EPC, ps, fx);
+                }
             }
         }
     }
     if (tid == 0) {
         m.xshift = s;
         m.xinv = ldexpf(1.f, -s);
+        m.xsq = qs.s;
     }
     __syncthreads();
 }
@@ -365,7 +376,8 @@ __device__ __forceinline__ void gu_unit(int per, int rb, int nr, int sb, int w, 
 }
 
 // B / C: the units of g; warps wfirst .. wfirst + wcount - 1 of the CTA take part
-template <int FMT>
+// Q8: int8 activations (the IDOT quantisation; x at m.xsq), else limbs
+template <int FMT, bool Q8>
 __device__ __noinline__ void gateup_run(const DecParams &P, D1S &m, const uint8_t *xq, int rb0, int re0, int sb0,
                                         int se0, int wfirst = 0, int wcount = kNW) {
     constexpr int NP = kGuRows / 2;  // row pairs per unit
@@ -376,48 +388,58 @@ __device__ __noinline__ void gateup_run(const DecParams &P, D1S &m, const uint8_
     const float xinv = m.xinv;
     const int per = (P.I + NP - 1) / NP;
     auto unit = [&](int i, int &slot, int &j) { gu_unit(per, rb0, nr, sb0, warp + wcount * i, slot, j); };
-    warp_stream_int<FMT, kGuRows, kInfl1, kOnce>(
-        mine, (int)(rb / 16), lane,
-        [&](int i, const uint8_t *(&rr)[kGuRows]) {
-            int slot, j;
-            unit(i, slot, j);
-            const Rec &r = m.rec[slot];
-            const int inter = slot == kShSlot ? P.Is : P.I;
+    auto rows_of = [&](int i, const uint8_t *(&rr)[kGuRows]) {
+        int slot, j;
+        unit(i, slot, j);
+        const Rec &r = m.rec[slot];
+        const int inter = slot == kShSlot ? P.Is : P.I;
 #pragma unroll
-            for (int q = 0; q < NP; q++) {
-                const int jq = min(j + q, inter - 1);
-                rr[2 * q] = r.gw + (size_t)jq * rb;
-                rr[2 * q + 1] = r.uw + (size_t)jq * rb;
-            }
-        },
-        [&](int) { return reinterpret_cast<const uint4 *>(xq); },
-        [&](int i) {  // lane 16 q: the scales of gate row and up row j + q
-            int slot, j;
-            unit(i, slot, j);
-            const Rec &r = m.rec[slot];
-            const int inter = slot == kShSlot ? P.Is : P.I;
-            const int jq = min(j + (NP > 1 ? lane >> 4 : 0), inter - 1);
-            const bool ld = NP > 1 ? (lane & 15) == 0 : lane == 0;
-            return ld ? make_float2(__ldg(r.gs + jq), __ldg(r.us + jq)) : make_float2(0.f, 0.f);
-        },
-        [&](int i, long long tot, float2 sc) {
-            // 2 rows: lanes 0-15 hold gate j, 16-31 up j; 4 rows: lanes 8 r hold row r of
-            // (gate j, up j, gate j + 1, up j + 1)
-            constexpr int UPD = kGuRows == 2 ? 16 : 8;
-            const long long up = __shfl_down_sync(kFull, tot, UPD);
-            int slot, j;
-            unit(i, slot, j);
-            const int inter = slot == kShSlot ? P.Is : P.I;
-            const int q = kGuRows == 2 ? 0 : (lane >> 4);
-            const bool mine_row = kGuRows == 2 ? lane == 0 : (lane & 15) == 0;
-            if (mine_row && j + q < inter) {
-                const float gv = (__ll2float_rn(tot) * xinv) * sc.x;
-                const float uv = (__ll2float_rn(up) * xinv) * sc.y;
-                const float hv = gv / (1.f + expf(-gv)) * uv;
-                P.h[(size_t)(slot == kShSlot ? P.K : slot) * P.ldh + j + q] = hv;
-                atomicMax(&m.hmax[slot], __float_as_int(fabsf(hv)));
-            }
+        for (int q = 0; q < NP; q++) {
+            const int jq = min(j + q, inter - 1);
+            rr[2 * q] = r.gw + (size_t)jq * rb;
+            rr[2 * q + 1] = r.uw + (size_t)jq * rb;
+        }
+    };
+    auto xq_of = [&](int) { return reinterpret_cast<const uint4 *>(xq); };
+    auto pre = [&](int i) {  // lane 16 q: the scales of gate row and up row j + q
+        int slot, j;
+        unit(i, slot, j);
+        const Rec &r = m.rec[slot];
+        const int inter = slot == kShSlot ? P.Is : P.I;
+        const int jq = min(j + (NP > 1 ? lane >> 4 : 0), inter - 1);
+        const bool ld = NP > 1 ? (lane & 15) == 0 : lane == 0;
+        return ld ? make_float2(__ldg(r.gs + jq), __ldg(r.us + jq)) : make_float2(0.f, 0.f);
+    };
+    // 2 rows: lanes 0-15 hold gate j, 16-31 up j; 4 rows: lanes 8 r hold row r of (gate j, up j,
+    // gate j + 1, up j + 1); gv / uv are the gate and up values of the lane's row pair
+    auto finish = [&](int i, float gv, float uv) {
+        int slot, j;
+        unit(i, slot, j);
+        const int inter = slot == kShSlot ? P.Is : P.I;
+        const int q = kGuRows == 2 ? 0 : (lane >> 4);
+        const bool mine_row = kGuRows == 2 ? lane == 0 : (lane & 15) == 0;
+        if (mine_row && j + q < inter) {
+            const float hv = gv / (1.f + expf(-gv)) * uv;
+            P.h[(size_t)(slot == kShSlot ? P.K : slot) * P.ldh + j + q] = hv;
+            atomicMax(&m.hmax[slot], __float_as_int(fabsf(hv)));
+        }
+    };
+    constexpr int UPD = kGuRows == 2 ? 16 : 8;
+    if constexpr (Q8) {
+        static_assert(kGuRows == 4, "the int8 walk takes four rows per unit");
+        const float sx = m.xsq;
+        warp_stream_q8<FMT, kInfl1>(mine, (int)(rb / 16), lane, rows_of, xq_of, pre, [&](int i, int dot, float2 sc) {
+            const int up = __shfl_down_sync(kFull, dot, UPD);
+            finish(i, __fmul_rn(__fmul_rn(__int2float_rn(dot), sc.x), sx),
+                   __fmul_rn(__fmul_rn(__int2float_rn(up), sc.y), sx));
         });
+    } else {
+        warp_stream_int<FMT, kGuRows, kInfl1, kOnce>(
+            mine, (int)(rb / 16), lane, rows_of, xq_of, pre, [&](int i, long long tot, float2 sc) {
+                const long long up = __shfl_down_sync(kFull, tot, UPD);
+                finish(i, (__ll2float_rn(tot) * xinv) * sc.x, (__ll2float_rn(up) * xinv) * sc.y);
+            });
+    }
 }
 
 // B / C for int4-grouped weights (one fp32 scale per gs inputs of a row): the units of
@@ -495,7 +517,8 @@ __device__ void prefetch_down(const DecParams &P, const D1S &m, int db, int de, 
 // D: down units [lo, hi) of the slot-major space (unit l: slot l / ngr, rows 4 (l % ngr) .. +3);
 // slot u's staged h sits at hq + (u - s0) * hs. y goes to the workspace row of the slot.
 // rot rotates the warp order so that two calls share the warps evenly.
-template <int FMT>
+// Q8: int8 activations (the IDOT quantisation; slot u's h at m.hsq[u - s0]), else limbs
+template <int FMT, bool Q8>
 __device__ __noinline__ void down_run(const DecParams &P, D1S &m, const uint8_t *hq, int hs, int s0, int lo, int hi,
                                       int ngr, int rot) {
     const int lane = threadIdx.x % kWarp;
@@ -510,33 +533,42 @@ __device__ __noinline__ void down_run(const DecParams &P, D1S &m, const uint8_t 
         slot = l / ngr;
         grp = l - slot * ngr;
     };
-    warp_stream_int<FMT, 4, kInfl1, kOnce>(
-        mine, (int)(rb / 16), lane,
-        [&](int i, const uint8_t *(&rr)[4]) {
-            int slot, grp;
-            unit(i, slot, grp);
-            const Rec &r = m.rec[sh ? kShSlot : slot];
+    auto rows_of = [&](int i, const uint8_t *(&rr)[4]) {
+        int slot, grp;
+        unit(i, slot, grp);
+        const Rec &r = m.rec[sh ? kShSlot : slot];
 #pragma unroll
-            for (int q = 0; q < 4; q++) rr[q] = r.dw + (size_t)min(4 * grp + q, P.H - 1) * rb;
-        },
-        [&](int i) {
-            int slot, grp;
-            unit(i, slot, grp);
-            return reinterpret_cast<const uint4 *>(hq + (size_t)(slot - s0) * hs);
-        },
-        [&](int i) {
-            int slot, grp;
-            unit(i, slot, grp);
-            const Rec &r = m.rec[sh ? kShSlot : slot];
-            return (lane & 7) == 0 ? __ldg(r.ds + min(4 * grp + (lane >> 3), P.H - 1)) : 0.f;
-        },
-        [&](int i, long long tot, float sc) {  // lane 8q holds row q
-            int slot, grp;
-            unit(i, slot, grp);
-            const int d = 4 * grp + (lane >> 3);
-            if ((lane & 7) == 0 && d < P.H)
-                P.y[(size_t)(slot == m.U ? P.K : slot) * P.H + d] = (__ll2float_rn(tot) * m.hinv[slot - s0]) * sc;
+        for (int q = 0; q < 4; q++) rr[q] = r.dw + (size_t)min(4 * grp + q, P.H - 1) * rb;
+    };
+    auto xq_of = [&](int i) {
+        int slot, grp;
+        unit(i, slot, grp);
+        return reinterpret_cast<const uint4 *>(hq + (size_t)(slot - s0) * hs);
+    };
+    auto pre = [&](int i) {
+        int slot, grp;
+        unit(i, slot, grp);
+        const Rec &r = m.rec[sh ? kShSlot : slot];
+        return (lane & 7) == 0 ? __ldg(r.ds + min(4 * grp + (lane >> 3), P.H - 1)) : 0.f;
+    };
+    auto store = [&](int i, auto value_of) {  // lane 8q holds row q
+        int slot, grp;
+        unit(i, slot, grp);
+        const int d = 4 * grp + (lane >> 3);
+        if ((lane & 7) == 0 && d < P.H) P.y[(size_t)(slot == m.U ? P.K : slot) * P.H + d] = value_of(slot);
+    };
+    if constexpr (Q8) {
+        warp_stream_q8<FMT, kInfl1>(mine, (int)(rb / 16), lane, rows_of, xq_of, pre, [&](int i, int dot, float sc) {
+            store(i, [&](int slot) { return __fmul_rn(__fmul_rn(__int2float_rn(dot), sc), m.hsq[slot - s0]); });
         });
+    } else {
+        warp_stream_int<FMT, 4, kInfl1, kOnce>(mine, (int)(rb / 16), lane, rows_of, xq_of, pre,
+                                               [&](int i, long long tot, float sc) {
+                                                   store(i, [&](int slot) {
+                                                       return (__ll2float_rn(tot) * m.hinv[slot - s0]) * sc;
+                                                   });
+                                               });
+    }
 }
 
 // D for int4-grouped weights: the units of down_run, every chunk scaled by its group
@@ -590,7 +622,7 @@ __device__ __noinline__ void down_run_grouped(const DecParams &P, D1S &m, const 
 // routed layout, or the shared one for slot U), each in block fixed point from the largest |h|
 // of the slot over all CTAs. A thread loads up to kHB 16-element items while threads below ns
 // read the slots' maxima: one round trip for the usual one or two vectors.
-template <int RF, int SF>
+template <int RF, int SF, bool RQ, bool SQ>
 __device__ void stage_h(const DecParams &P, D1S &m, uint8_t *act, int hs, int s0, int ns) {
     const int tid = threadIdx.x;
     const int U = m.U;
@@ -627,26 +659,35 @@ __device__ void stage_h(const DecParams &P, D1S &m, uint8_t *act, int hs, int s0
         }
         if (b0 == 0 && tid < ns) {  // the exponent of each staged slot, read while the items are in flight
             const int u = s0 + tid;
-            const int sh = fixed_shift(__int_as_float(__ldcg(&P.ctrl->hmax[u < U ? u : kShSlot])));
+            const float amax = __int_as_float(__ldcg(&P.ctrl->hmax[u < U ? u : kShSlot]));
+            const int sh = fixed_shift(amax);
             m.hshift[tid] = sh;
             m.hinv[tid] = ldexpf(1.f, -sh);
+            m.hamax[tid] = amax;
+            m.hsq[tid] = Q8Scale(amax).s;
         }
         __syncthreads();
 #pragma unroll
         for (int k = 0; k < kHB; k++) {
             if (jv[k] >= 0) {
-                const FixedScale fx(m.hshift[jv[k]]);
-                if (s0 + jv[k] < U) limbs_from_regs<RF>(v[k], act + (size_t)jv[k] * hs, cpr_r, pv[k], fx);
-                else limbs_from_regs<SF>(v[k], act + (size_t)jv[k] * hs, cpr_s, pv[k], fx);
+                uint8_t *dst = act + (size_t)jv[k] * hs;
+                if (s0 + jv[k] < U) {
+                    if constexpr (RQ) q8_from_regs<RF>(v[k], dst, cpr_r, pv[k], Q8Scale(m.hamax[jv[k]]));
+                    else limbs_from_regs<RF>(v[k], dst, cpr_r, pv[k], FixedScale(m.hshift[jv[k]]));
+                } else {
+                    if constexpr (SQ) q8_from_regs<SF>(v[k], dst, cpr_s, pv[k], Q8Scale(m.hamax[jv[k]]));
+                    else limbs_from_regs<SF>(v[k], dst, cpr_s, pv[k], FixedScale(m.hshift[jv[k]]));
+                }
             }
         }
     }
     __syncthreads();
 }
 
-// GRP: bit 0 the routed experts, bit 1 the shared expert are int4-grouped (RF / SF then int4)
+// GRP: bit 0 the routed experts, bit 1 the shared expert are int4-grouped (RF / SF then int4);
+// bit 2 the routed experts, bit 3 the shared expert take int8 activations (IDOT)
 template <int RF, int SF, int GRP>
-__global__ void __launch_bounds__(kNT, 2) moe_decode1_kernel(const DecParams P) {
+__global__ void __launch_bounds__(kNT, 2) moe_decode1_kernel(const __grid_constant__ DecParams P) {
     extern __shared__ __align__(128) uint8_t smem[];
     D1S &m = *reinterpret_cast<D1S *>(smem);
     uint8_t *act = smem + P.d1_act_off;
@@ -737,7 +778,8 @@ __global__ void __launch_bounds__(kNT, 2) moe_decode1_kernel(const DecParams P) 
         bias_s = bs;
         tab_s = reinterpret_cast<const coli_moe_expert *>(ts);
     }
-    stage_x<RF, SF>(P, xsrc, xq_r, xq_s, two, m);
+    constexpr bool RQ = (GRP & 4) != 0, SQ = (GRP & 8) != 0;
+    stage_x<RF, SF, RQ, SQ>(P, xsrc, xq_r, xq_s, two, m);
     if (tab_regs) {
 #pragma unroll
         for (int k = 0; k < kTabRegs; k++)
@@ -746,10 +788,10 @@ __global__ void __launch_bounds__(kNT, 2) moe_decode1_kernel(const DecParams P) 
     }
     // ---------------- B: the shared expert's gate/up, here only when its walk differs from the
     // routed experts' (else its units follow the routed ones in one stream, phase C)
-    constexpr bool kMerged = RF == SF && ((GRP & 1) != 0) == ((GRP & 2) != 0);
+    constexpr bool kMerged = RF == SF && ((GRP & 1) != 0) == ((GRP & 2) != 0) && RQ == SQ;
     if (!kMerged && be > bb) {
         if constexpr ((GRP & 2) != 0) gateup_run_grouped(P, m, xq_s, 0, 0, bb, be);
-        else gateup_run<SF>(P, m, xq_s, 0, 0, bb, be);
+        else gateup_run<SF, SQ>(P, m, xq_s, 0, 0, bb, be);
     }
 
     // ---------------- R: routing
@@ -770,7 +812,7 @@ __global__ void __launch_bounds__(kNT, 2) moe_decode1_kernel(const DecParams P) 
     const int gu_tot = U * gu_per;
     const int cb = range_lo(gu_tot, c, G), ce = range_lo(gu_tot, c + 1, G);
     if constexpr ((GRP & 1) != 0) gateup_run_grouped(P, m, xq_r, cb, ce, kMerged ? bb : 0, kMerged ? be : 0);
-    else gateup_run<RF>(P, m, xq_r, cb, ce, kMerged ? bb : 0, kMerged ? be : 0);
+    else gateup_run<RF, RQ>(P, m, xq_r, cb, ce, kMerged ? bb : 0, kMerged ? be : 0);
     prefetch_down(P, m, db, de, ngr);
     __syncthreads();
     if (tid < U || (tid == kShSlot && P.Is > 0))
@@ -789,18 +831,18 @@ __global__ void __launch_bounds__(kNT, 2) moe_decode1_kernel(const DecParams P) 
     __syncthreads();
     const int s0 = db / ngr, ns = de > db ? (de - 1) / ngr - s0 + 1 : 0;
     const int hs = P.d1_hs;
-    stage_h<RF, SF>(P, m, act, hs, s0, ns);
+    stage_h<RF, SF, RQ, SQ>(P, m, act, hs, s0, ns);
     {
         const int split = U * ngr;  // routed units below, shared units from here
         const int rlo = db, rhi = min(de, split), slo = max(db, split), shi = de;
         const int rot = rhi > rlo ? (rhi - rlo) % kNW : 0;
         if (rhi > rlo) {
             if constexpr ((GRP & 1) != 0) down_run_grouped(P, m, act, hs, s0, rlo, rhi, ngr, 0);
-            else down_run<RF>(P, m, act, hs, s0, rlo, rhi, ngr, 0);
+            else down_run<RF, RQ>(P, m, act, hs, s0, rlo, rhi, ngr, 0);
         }
         if (shi > slo) {
             if constexpr ((GRP & 2) != 0) down_run_grouped(P, m, act, hs, s0, slo, shi, ngr, rot);
-            else down_run<SF>(P, m, act, hs, s0, slo, shi, ngr, rot);
+            else down_run<SF, SQ>(P, m, act, hs, s0, slo, shi, ngr, rot);
         }
     }
     __syncthreads();
@@ -852,6 +894,14 @@ KernelFn kernel_for(int rf, int sf, int grp) {
                                      moe_decode1_kernel<I4, I2, 1>};
     static const KernelFn sgrp[3] = {moe_decode1_kernel<I8, I4, 2>, moe_decode1_kernel<I4, I4, 2>,
                                      moe_decode1_kernel<I2, I4, 2>};
+    // int8 activations (IDOT): routed and shared (int8 / int4 each), routed only, shared only
+    static const KernelFn q8both[2][2] = {{moe_decode1_kernel<I8, I8, 12>, moe_decode1_kernel<I8, I4, 12>},
+                                          {moe_decode1_kernel<I4, I8, 12>, moe_decode1_kernel<I4, I4, 12>}};
+    static const KernelFn q8r[2] = {moe_decode1_kernel<I8, I2, 4>, moe_decode1_kernel<I4, I2, 4>};
+    static const KernelFn q8s[2] = {moe_decode1_kernel<I2, I8, 8>, moe_decode1_kernel<I2, I4, 8>};
+    if (grp == 12) return q8both[pick(rf)][pick(sf)];
+    if (grp == 4) return q8r[pick(rf)];
+    if (grp == 8) return q8s[pick(sf)];
     if (grp == 3) return moe_decode1_kernel<I4, I4, 3>;
     if (grp == 1) return rgrp[pick(sf)];
     if (grp == 2) return sgrp[pick(rf)];
@@ -859,7 +909,9 @@ KernelFn kernel_for(int rf, int sf, int grp) {
 }
 
 // the grouped bits of a plan
-int grp_of(const DecParams &P) { return (P.rgs > 0 ? 1 : 0) | (P.sgs > 0 ? 2 : 0); }
+int grp_of(const DecParams &P) {
+    return (P.rgs > 0 ? 1 : 0) | (P.sgs > 0 ? 2 : 0) | (P.rq8 ? 4 : 0) | (P.sq8 ? 8 : 0);
+}
 
 size_t decode1_smem_bytes(const DecParams &P) { return (size_t)P.d1_end; }
 
@@ -875,6 +927,11 @@ bool decode1_plan(const coli_moe_desc &d, DecParams &P, int grid) {
     P.sfmt = d.shared_fmt == COLI_FMT_INT4G ? COLI_FMT_INT4 : d.shared_fmt;
     P.rgs = d.routed_fmt == COLI_FMT_INT4G ? d.group_size : 0;
     P.sgs = d.I_shared > 0 && d.shared_fmt == COLI_FMT_INT4G ? d.group_size : 0;
+    // IDOT: int8 activations for the int8 and int4 experts (int2 and int4-grouped keep limbs)
+    auto q8 = [&](int f) { return d.idot != 0 && (f == COLI_FMT_INT8 || f == COLI_FMT_INT4); };
+    P.rq8 = q8(d.routed_fmt) ? 1 : 0;
+    P.sq8 = d.I_shared > 0 && q8(d.shared_fmt) ? 1 : 0;
+    if ((P.rgs > 0 || P.sgs > 0) && (P.rq8 || P.sq8)) return false;  // the general kernels take those
     P.NV = 1;
     P.route_only = 0;
     P.neb = (d.E + kRtE - 1) / kRtE;

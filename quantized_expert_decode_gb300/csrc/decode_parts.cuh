@@ -122,6 +122,60 @@ __device__ __forceinline__ void warp_stream_int(int nunits, int CPR, int lane, R
     }
 }
 
+// The same walk for int8 activations (the IDOT quantisation, idot.cuh q8_chunk): four rows per
+// unit, one int accumulator per row; epi(i, dot, pre) gets, in lane l, the exact dot of row l / 8.
+template <int FMT, int INFL, class RowsOf, class XqOf, class Pre, class Epi>
+__device__ __forceinline__ void warp_stream_q8(int nunits, int CPR, int lane, RowsOf rows_of, XqOf xq_of, Pre pre,
+                                               Epi epi) {
+    constexpr int NR = 4, kDepth = INFL / NR;
+    if (nunits <= 0) return;
+    const int S = (CPR + kWarp - 1) / kWarp;
+    const int total = nunits * S;
+    uint4 buf[kDepth][NR];
+    int iu = 0, ik = 0;
+    const uint8_t *rr[NR];
+    rows_of(0, rr);
+    auto issue = [&](uint4 (&b)[NR]) {
+        if (iu < nunits) {
+            const int c = lane + kWarp * ik;
+#pragma unroll
+            for (int r = 0; r < NR; r++) b[r] = c < CPR ? ld_stream_16(rr[r] + 16 * c) : make_uint4(0, 0, 0, 0);
+            if (++ik == S) {
+                ik = 0;
+                if (++iu < nunits) rows_of(iu, rr);
+            }
+        }
+    };
+#pragma unroll
+    for (int j = 0; j < kDepth; j++) issue(buf[j]);
+    auto d0 = pre(0);
+    decltype(d0) d1 = d0;
+    if (nunits > 1) d1 = pre(1);
+    int acc[NR] = {0, 0, 0, 0};
+    int cu = 0, ck = 0;
+    const uint4 *xq4 = xq_of(0);
+    for (int s0 = 0; s0 < total; s0 += kDepth) {
+#pragma unroll
+        for (int j = 0; j < kDepth; j++) {
+            if (s0 + j < total) {
+                const int c = lane + kWarp * ck;
+                if (c < CPR) q8_chunk<FMT, NR>(buf[j], xq4, CPR, c, acc);
+                issue(buf[j]);
+                if (++ck == S) {
+                    epi(cu, q8_reduce4<FMT>(acc, lane), d0);
+                    d0 = d1;
+                    if (cu + 2 < nunits) d1 = pre(cu + 2);
+#pragma unroll
+                    for (int r = 0; r < NR; r++) acc[r] = 0;
+                    ck = 0;
+                    cu++;
+                    if (cu < nunits) xq4 = xq_of(cu);
+                }
+            }
+        }
+    }
+}
+
 // Four rows of float lane partials at once, transposing as it reduces (the shuffle pattern of
 // idot_reduce4): every lane ends with the total of row lane / 8.
 __device__ __forceinline__ float freduce4(const float (&p)[4], int lane) {

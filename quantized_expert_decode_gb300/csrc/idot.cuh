@@ -205,6 +205,87 @@ __device__ __forceinline__ void stage_limb_item(const float *__restrict__ src, i
         xq4[(ss * 3 + j) * CPR + c] = make_uint4(o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
 }
 
+// ---------------------------------------------------------------- IDOT activations (int8)
+// glm.c's IDOT kernels quantise an activation row to int8 with one scale (qrow_i8):
+// s = max(max|x| / 127, 1e-12), q = round-half-even(x * (1 / s)), every division and product
+// rounded as IEEE fp32; the dot with the dequantised weights is an exact integer sum, and
+// y[o] = ((float)dot * scale[o]) * s. For the single-token walk the bytes sit in the layout of
+// the limbs with one limb: item p = ss * CPR + c (the 16 elements of sub-step ss of chunk c) is
+// one uint4 at p, u32 number u = wl * NGW + g holding the four elements that meet field group g
+// of word wl (byte b: element wl * EPW + g + b * NGW of the item).
+struct Q8Scale {
+    float s, inv;
+    __device__ __forceinline__ explicit Q8Scale(float amax) {
+        s = __fdiv_rn(amax, 127.f);
+        if (s < 1e-12f) s = 1e-12f;
+        inv = __fdiv_rn(1.f, s);
+    }
+    __device__ __forceinline__ int operator()(float x) const { return __float2int_rn(__fmul_rn(x, inv)); }
+};
+
+// item p of a vector as int8 bytes (v: its 16 elements)
+template <int FMT>
+__device__ __forceinline__ void q8_from_regs(const float4 (&v)[4], uint8_t *xq, int CPR, int p, const Q8Scale &qs) {
+    using G = QGeom<FMT>;
+    using I = IQ<FMT>;
+    int X[16];
+#pragma unroll
+    for (int k = 0; k < 4; k++) {
+        X[4 * k + 0] = qs(v[k].x);
+        X[4 * k + 1] = qs(v[k].y);
+        X[4 * k + 2] = qs(v[k].z);
+        X[4 * k + 3] = qs(v[k].w);
+    }
+    static_assert(I::WPSS * I::NGW == 4, "one uint4 of int8 bytes per item");
+    uint32_t o[4];
+#pragma unroll
+    for (int wl = 0; wl < I::WPSS; wl++)
+#pragma unroll
+        for (int g = 0; g < I::NGW; g++) {
+            const int e0 = wl * G::EPW + g;
+            const uint32_t ab = prmt(X[e0], X[e0 + I::NGW], 0x0040u), cd = prmt(X[e0 + 2 * I::NGW], X[e0 + 3 * I::NGW], 0x0040u);
+            o[wl * I::NGW + g] = prmt(ab, cd, 0x5410u);
+        }
+    reinterpret_cast<uint4 *>(xq)[p] = make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+// one 16-byte chunk of NR rows against the int8 bytes: acc[r] += sum of SC * deq * q
+template <int FMT, int NR>
+__device__ __forceinline__ void q8_chunk(const uint4 (&w)[NR], const uint4 *xq4, int CPR, int c, int (&acc)[NR]) {
+    using I = IQ<FMT>;
+#pragma unroll
+    for (int ss = 0; ss < I::NSS; ss++) {
+        const uint4 xa = xq4[ss * CPR + c];
+        const uint32_t xv[4] = {xa.x, xa.y, xa.z, xa.w};
+#pragma unroll
+        for (int r = 0; r < NR; r++)
+#pragma unroll
+            for (int wl = 0; wl < I::WPSS; wl++) {
+                const uint32_t wd = word_of(w[r], ss * I::WPSS + wl);
+#pragma unroll
+                for (int g = 0; g < I::NGW; g++)
+                    acc[r] = dp4a_s<true>(signed_fields<FMT>(wd, g), xv[wl * I::NGW + g], acc[r]);
+            }
+    }
+}
+
+// four rows of lane partials at once (the transposing pattern of idot_reduce4): every lane ends
+// with the exact dot of row lane / 8, the factor SC dropped
+template <int FMT>
+__device__ __forceinline__ int q8_reduce4(const int (&p)[4], int lane) {
+    const bool h16 = (lane & 16) != 0, h8 = (lane & 8) != 0;
+    int k0 = h16 ? p[2] : p[0], k1 = h16 ? p[3] : p[1];
+    const int s0 = h16 ? p[0] : p[2], s1 = h16 ? p[1] : p[3];
+    k0 += __shfl_xor_sync(kFull, s0, 16);
+    k1 += __shfl_xor_sync(kFull, s1, 16);
+    int k = h8 ? k1 : k0;
+    k += __shfl_xor_sync(kFull, h8 ? k0 : k1, 8);
+    k += __shfl_xor_sync(kFull, k, 4);
+    k += __shfl_xor_sync(kFull, k, 2);
+    k += __shfl_xor_sync(kFull, k, 1);
+    return k >> IQ<FMT>::LOG_SC;
+}
+
 // items per vector of n elements
 template <int FMT>
 __host__ __device__ __forceinline__ int limb_items(int n) {

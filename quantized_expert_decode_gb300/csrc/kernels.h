@@ -56,6 +56,7 @@ struct DecParams {
     DecCtrl *ctrl;
     int T, H, I, E, K, Is, rfmt, sfmt, Ksel, norm_topk;
     int rgs, sgs;              // inputs per scale of int4-grouped routed / shared weights (0: per-row scales)
+    int rq8, sq8;              // single-token kernel: routed / shared products on int8 activations (IDOT)
     float top_p, rscale;
     int ldh;
     int NV, xs_stride, xs_bytes, rt_bytes;

@@ -479,7 +479,15 @@ def test_grouped_blocks(qed, name, over):
 # such steps: max|err| <= 2e-3 * rms(ref); the IDOT error itself (vs the exact block) is ~0.3 %.
 IDOT_TOL = 2e-3
 IDOT = [
+    # T = 1 runs the single-token kernel on int8 activations (both sides, one side, none when a
+    # grouped expert is present: the general kernels then)
     ("idot-one-token", dict(T=1, H=256, I=128, E=16, K=4, I_shared=64, routed_fmt=2, shared_fmt=1)),
+    ("idot-one-token-large", dict(T=1, H=6144, I=2048, E=256, K=8, I_shared=2048, routed_fmt=2, shared_fmt=2)),
+    ("idot-one-token-int2-routed", dict(T=1, H=512, I=256, E=16, K=4, I_shared=128, routed_fmt=3, shared_fmt=1)),
+    ("idot-one-token-int2-shared", dict(T=1, H=512, I=256, E=16, K=4, I_shared=128, routed_fmt=1, shared_fmt=3)),
+    ("idot-one-token-int8", dict(T=1, H=512, I=256, E=16, K=4, I_shared=0, routed_fmt=1, shared_fmt=1)),
+    ("idot-one-token-grouped-shared", dict(T=1, H=512, I=256, E=16, K=4, I_shared=128, routed_fmt=2,
+                                           shared_fmt=4, group_size=64)),
     ("idot-int8", dict(T=5, H=256, I=128, E=12, K=3, I_shared=128, routed_fmt=1, shared_fmt=1)),
     ("idot-int2-shared", dict(T=4, H=256, I=128, E=8, K=2, I_shared=64, routed_fmt=2, shared_fmt=3)),
     ("idot-long", dict(T=70, H=128, I=64, E=9, K=2, I_shared=64, routed_fmt=2, shared_fmt=2)),
@@ -496,11 +504,15 @@ def test_idot_blocks(qed, name, over):
     check_route(qed, blk, dev)
     tokens = None if cfg["T"] <= 9 else [0, 33, 69]
     out = check_forward(qed, blk, dev, tokens, tol=IDOT_TOL)
-    # the IDOT kernels ran: the result is not the exact block's
+    # the IDOT kernels ran: the result departs from the exact block's by what the IDOT definition
+    # itself departs (the oracle's IDOT block against its exact block; a few percent at the
+    # large shapes, where max|h| / rms(h) is large and the int8 grid coarse)
     exact = oracle.moe_forward(dict(blk, cfg=dict(cfg, idot=0)))[0]
+    ref = oracle.moe_forward(blk)[0]
     rows = list(range(cfg["T"])) if tokens is None else tokens
     rel = rms(out[rows] - exact[rows]) / rms(exact[rows])
-    assert 1e-4 < rel < 2e-2, rel
+    ref_rel = rms(ref[rows] - exact[rows]) / rms(exact[rows])
+    assert rel > 1e-4 and abs(rel - ref_rel) <= 0.1 * ref_rel, (rel, ref_rel)
 
 
 # ------------------------------------------------------------------ the layer tail (RMSNorm folded in)
@@ -517,6 +529,7 @@ TAILS = [
     ("grouped", dict(T=3, H=256, I=128, E=8, K=2, I_shared=64, routed_fmt=4, shared_fmt=4, group_size=64), False),
     ("grouped-one-token", dict(T=1, H=256, I=128, E=8, K=2, I_shared=64, routed_fmt=4, shared_fmt=4,
                                group_size=64), True),
+    ("idot-one-token", dict(T=1, H=512, I=256, E=16, K=4, I_shared=128, routed_fmt=2, shared_fmt=1, idot=1), False),
 ]
 
 
@@ -543,7 +556,7 @@ def test_layer_tail(qed, name, over, in_place):
     ro, ri, rw, _ = oracle.moe_tail(blk, resid, nw, eps)
     assert np.array_equal(gi, ri)
     assert np.allclose(wt.cpu().numpy(), rw, rtol=W_RTOL, atol=0)
-    tol = PREFILL_TOL if T >= PREFILL_MIN_T else OUT_TOL
+    tol = IDOT_TOL if cfg.get("idot", 0) else (PREFILL_TOL if T >= PREFILL_MIN_T else OUT_TOL)
     for t in range(T):
         block_ref = ro[t].astype(np.float64) - resid[t]
         block_got = got[t].astype(np.float64) - resid[t]

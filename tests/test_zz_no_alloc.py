@@ -7,7 +7,8 @@ The tests compare it with coli_moe_forward on the same inputs, two calls in a ro
 on fresh activations, so stale scratch from the first call would show), on every path the
 fixed array can serve: the single-token kernel, the token-group kernel, the tensor-core GEMMs
 (T > 64, which reuse the scratch for bf16 activations), the general kernels of an
-int4-grouped block and the single-token kernel on int4-grouped weights. Both entry points run the same deterministic kernels, so the outputs must
+int4-grouped block and the single-token kernel on int4-grouped weights and on int8 activations
+(IDOT). Both entry points run the same deterministic kernels, so the outputs must
 be identical bit for bit; the fixed array's error word must read clear afterwards. A
 description needing more than the fixed scratch is refused. The tests build their own inputs,
 so they pass alone in a fresh process as well as after the rest of the suite; the file name
@@ -31,6 +32,8 @@ CASES = [
                           routed_fmt=4, shared_fmt=4, group_size=64, zipf=False)),
     ("int4-grouped-one-token", dict(T=1, H=512, I=256, E=12, K=3, I_shared=128, norm_topk=1, routed_scale=2.5,
                                     routed_fmt=4, shared_fmt=4, group_size=64, zipf=False)),
+    ("idot-one-token", dict(T=1, H=512, I=256, E=12, K=3, I_shared=128, norm_topk=1, routed_scale=2.5,
+                            routed_fmt=2, shared_fmt=1, idot=1, zipf=False)),
 ]
 
 

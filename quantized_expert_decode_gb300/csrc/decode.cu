@@ -4,9 +4,11 @@
 // launch, so every CTA is resident and a wait is only ever on an earlier phase):
 //   A  router logits (colibri-strix c/glm.c @98759bf moe() phase A; r_router shader):
 //      T <= 8: router items — partial logits of 32 experts over one slice of H; T > 8: the
-//      partials come from a router launch before this kernel and every CTA sums a share.
+//      partials come from a router launch before this kernel, and CTA t routes token t alone
+//      (logits, picks, kept weights: route_token), writing its row of the routing outputs.
 //   B  shared expert gate/up rows (independent of routing: runs while A completes)
-//   R  routing, by EVERY CTA for itself once all partials are in (one counter wait): logits
+//   R  routing, by EVERY CTA for itself once all partials are in (one counter wait; T > 8: once
+//      every token CTA has written its picks, which every CTA then loads): logits
 //      summed in a fixed order, sigmoid, bias, greedy top-K with ties to the lower index
 //      (select.cuh, one warp per token), TOPK/TOPP, renorm, routed scale, stable token->expert buckets and
 //      the unit tables — all in shared memory; CTA 0 also writes the routing outputs. Running
@@ -136,45 +138,75 @@ __device__ int scan_smem(int *a, int n, int *tmp) {
     return total;
 }
 
-// The routing of all T tokens by this CTA, from the logits (the fixed-order sum of the nks
-// partial slices when from_partials, else slice 0 already holds them). Results go to rt; CTA 0
-// also writes the routing outputs of the workspace / caller.
-__device__ __noinline__ void route_local(const DecParams &P, float *scratch, const RTab &rt, bool from_partials) {
+// T > 8: CTA t routes token t alone, with all its threads: the logits are the fixed-order sum
+// of the nks partial slices, then sigmoid and bias; the picks by the whole CTA (select.cuh), the
+// kept weights by warp 0. The token's rows of the routing outputs go to the workspace / caller,
+// then the CTA raises routed_done. scratch: shared memory of at least rscratch_bytes.
+__device__ __noinline__ void route_token(const DecParams &P, int t, float *scratch) {
+    const int tid = threadIdx.x, lane = tid % kWarp, warp = tid / kWarp;
+    const int T = P.T, E = P.E, K = P.K, Ep = sel_padded(E);
+    float *sg = scratch, *ch = sg + Ep;
+    float2 *cand = reinterpret_cast<float2 *>(ch + Ep);
+    int *nc = reinterpret_cast<int *>(cand + sel_cand_cap(E, P.Ksel));  // candidates, selectable
+    int *sel_i = nc + 2;
+    for (int e = tid; e < Ep; e += kNT) {
+        float sv = 0.f, cv = -INFINITY;
+        if (e < E) {
+            float a[16];
+            const size_t j = (size_t)t * E + e;
+#pragma unroll
+            for (int k = 0; k < 16; k++)
+                if (k < P.nks) a[k] = __ldcg(P.part + (size_t)k * T * E + j);
+            float lg = 0.f;
+#pragma unroll
+            for (int k = 0; k < 16; k++)
+                if (k < P.nks) lg += a[k];
+            sv = 1.f / (1.f + expf(-lg));
+            cv = sv + __ldg(P.bias + e);
+            P.sig[j] = sv;
+            P.choice[j] = cv;
+        }
+        sg[e] = sv;
+        ch[e] = cv;
+    }
+    if (tid == 0) nc[0] = nc[1] = 0;
+    __syncthreads();
+    sel_topk_cta(ch, E, P.Ksel, cand, &nc[0], &nc[1], sel_i);
+    if (warp == 0) {
+        const int nsel = min(nc[1], P.Ksel);
+        if (nsel < P.Ksel && lane == 0) flag_error(P.ctrl, kErrNoCandidate);
+        const int pick = lane < nsel ? sel_i[lane] : -1;
+        const SelKept kp = sel_finish_warp(nsel, pick, lane < nsel ? sg[pick] : 0.f, P.top_p, P.norm_topk, P.rscale);
+        if (lane < K) {
+            P.idx[(size_t)t * K + lane] = kp.id;
+            P.w[(size_t)t * K + lane] = kp.w;
+        }
+        if (lane == 0) P.keff[t] = kp.ke;
+    }
+    __syncthreads();
+    if (tid == 0) {
+        __threadfence();
+        atomicAdd(&P.ctrl->routed_done, 1);
+    }
+}
+
+// The routing of all T tokens into this CTA's tables: from the logits (the fixed-order sum of
+// the nks partial slices, T <= 8) or, from_tokens, from the kept picks and weights the token
+// CTAs wrote (T > 8). Results go to rt; CTA 0 also writes the routing outputs of the workspace /
+// caller that the token CTAs do not.
+__device__ __noinline__ void route_local(const DecParams &P, float *scratch, const RTab &rt, bool from_tokens) {
     const int tid = threadIdx.x, lane = tid % kWarp, warp = tid / kWarp;
     const bool out = blockIdx.x == 0;
     const RScratch s = rscratch_of(scratch, P);
     const int T = P.T, E = P.E, K = P.K, Ep = sel_padded(E), TE = T * Ep;
-    // 1. logits -> sigmoid scores and choices, rows padded to whole selection blocks
-    if (!from_partials) {  // slice 0 holds the summed logits: batch a thread's loads
-        constexpr int B = 8;
-        for (int i0 = tid; i0 < TE; i0 += kNT * B) {
-            float lg[B], bs[B];
-#pragma unroll
-            for (int j = 0; j < B; j++) {
-                const int i = i0 + j * kNT, t = i / Ep, e = i - t * Ep;
-                if (i < TE && e < E) {
-                    lg[j] = __ldcg(P.part + (size_t)t * E + e);
-                    bs[j] = __ldg(P.bias + e);
-                }
-            }
-#pragma unroll
-            for (int j = 0; j < B; j++) {
-                const int i = i0 + j * kNT, t = i / Ep, e = i - t * Ep;
-                if (i >= TE) continue;
-                float sv = 0.f, cv = -INFINITY;
-                if (e < E) {
-                    sv = 1.f / (1.f + expf(-lg[j]));
-                    cv = sv + bs[j];
-                    if (out) {
-                        P.sig[(size_t)t * E + e] = sv;
-                        P.choice[(size_t)t * E + e] = cv;
-                    }
-                }
-                s.sg[i] = sv;
-                s.ch[i] = cv;
-            }
+    if (from_tokens) {
+        for (int i = tid; i < T * K; i += kNT) {
+            s.sel_i[i] = __ldcg(P.idx + i);
+            rt.w[i] = __ldcg(P.w + i);
         }
+        for (int t = tid; t < T; t += kNT) rt.keff[t] = __ldcg(P.keff + t);
     } else {
+        // 1. logits -> sigmoid scores and choices, rows padded to whole selection blocks
         for (int i = tid; i < TE; i += kNT) {
             const int t = i / Ep, e = i - t * Ep;
             float sv = 0.f, cv = -INFINITY;
@@ -198,30 +230,30 @@ __device__ __noinline__ void route_local(const DecParams &P, float *scratch, con
             s.sg[i] = sv;
             s.ch[i] = cv;
         }
-    }
-    __syncthreads();
-    // 2. per token, one warp: the picks (select.cuh), then TOPP, renormalisation and routed
-    //    scale in the serial code's float order
-    float2 *cand = s.cand + warp * sel_cand_cap(E, P.Ksel);
-    for (int t = warp; t < T; t += kNW) {
-        int *id = s.sel_i + t * K;
-        const int nsel = sel_topk_warp(s.ch + t * Ep, E, P.Ksel, cand, id);
-        if (nsel < P.Ksel && out && lane == 0) flag_error(P.ctrl, kErrNoCandidate);
-        const int pick = lane < nsel ? id[lane] : -1;
-        const SelKept kp = sel_finish_warp(nsel, pick, lane < nsel ? s.sg[t * Ep + pick] : 0.f, P.top_p,
-                                           P.norm_topk, P.rscale);
-        __syncwarp();
-        if (lane < K) {
-            id[lane] = kp.id;
-            rt.w[t * K + lane] = kp.w;
-            if (out) {
-                P.idx[(size_t)t * K + lane] = kp.id;
-                P.w[(size_t)t * K + lane] = kp.w;
+        __syncthreads();
+        // 2. per token, one warp: the picks (select.cuh), then TOPP, renormalisation and routed
+        //    scale in the serial code's float order
+        float2 *cand = s.cand + warp * sel_cand_cap(E, P.Ksel);
+        for (int t = warp; t < T; t += kNW) {
+            int *id = s.sel_i + t * K;
+            const int nsel = sel_topk_warp(s.ch + t * Ep, E, P.Ksel, cand, id);
+            if (nsel < P.Ksel && out && lane == 0) flag_error(P.ctrl, kErrNoCandidate);
+            const int pick = lane < nsel ? id[lane] : -1;
+            const SelKept kp = sel_finish_warp(nsel, pick, lane < nsel ? s.sg[t * Ep + pick] : 0.f, P.top_p,
+                                               P.norm_topk, P.rscale);
+            __syncwarp();
+            if (lane < K) {
+                id[lane] = kp.id;
+                rt.w[t * K + lane] = kp.w;
+                if (out) {
+                    P.idx[(size_t)t * K + lane] = kp.id;
+                    P.w[(size_t)t * K + lane] = kp.w;
+                }
             }
-        }
-        if (lane == 0) {
-            rt.keff[t] = kp.ke;
-            if (out) P.keff[t] = kp.ke;
+            if (lane == 0) {
+                rt.keff[t] = kp.ke;
+                if (out) P.keff[t] = kp.ke;
+            }
         }
     }
     __syncthreads();
@@ -825,13 +857,8 @@ __global__ void __launch_bounds__(kNT, 2) moe_decode_kernel(const __grid_constan
                 atomicAdd(&P.ctrl->router_done, 1);
             }
         }
-    } else {
-        reduce_logits(P, range_lo(P.T * P.E, c, G), range_lo(P.T * P.E, c + 1, G));
-        __syncthreads();
-        if (tid == 0) {
-            __threadfence();
-            atomicAdd(&P.ctrl->router_done, 1);
-        }
+    } else if (c < P.T) {  // the partials come from the router launch before this kernel
+        route_token(P, c, static_cast<float *>(xs));
     }
 
     // ---------------- B: the shared expert's gate/up (independent of routing)
@@ -840,12 +867,13 @@ __global__ void __launch_bounds__(kNT, 2) moe_decode_kernel(const __grid_constan
 
     // ---------------- R: routing, by this CTA for itself
     if (tid == 0) {
-        wait_at_least(&P.ctrl->router_done, P.route_only ? G : P.R, P.ctrl);
+        if (P.route_only) wait_at_least(&P.ctrl->routed_done, P.T, P.ctrl);
+        else wait_at_least(&P.ctrl->router_done, P.R, P.ctrl);
         __threadfence();
         m.skey[0] = -1;  // xs becomes routing scratch
     }
     __syncthreads();
-    route_local(P, static_cast<float *>(xs), rt, !P.route_only);
+    route_local(P, static_cast<float *>(xs), rt, P.route_only != 0);
     const int U = *rt.U;
 
     // ---------------- C: routed gate/up

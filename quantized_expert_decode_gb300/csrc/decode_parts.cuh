@@ -398,21 +398,6 @@ __device__ __noinline__ void router_item(const DecParams &P, int item) {
         }
 }
 
-// T > 8: logits = fixed-order sums of the partials for flat indices [lo, hi), into slice 0
-__device__ __noinline__ void reduce_logits(const DecParams &P, int lo, int hi) {
-    for (int i = lo + (int)threadIdx.x; i < hi; i += kNT) {
-        float a[16];
-#pragma unroll
-        for (int k = 0; k < 16; k++)
-            if (k < P.nks) a[k] = __ldcg(P.part + (size_t)k * P.T * P.E + i);
-        float s = 0.f;
-#pragma unroll
-        for (int k = 0; k < 16; k++)
-            if (k < P.nks) s += a[k];
-        P.part[i] = s;  // slice 0, index i: only this thread reads or writes it here
-    }
-}
-
 // ------------------------------------------------------------------ staging and prefetch
 __device__ __forceinline__ float4 ld_act4(const float *src, int q, bool coherent) {
     return coherent ? __ldcg(reinterpret_cast<const float4 *>(src) + q)

@@ -34,7 +34,8 @@ struct DecCtrl {
     int err, router_done, dn_done;
     int gu_all;                        // single-token kernel: finished gate/up units, all slots
     int q_b, q_c, q_d;                 // token-group kernel: next chunk of phases B, C, D
-    int pad[9];
+    int routed_done;                   // token-group kernel, T > 8: tokens routed by their CTA
+    int pad[8];
     unsigned long long call;           // single-token kernel: id of the call whose counters these are
     int hmax[kMaxK + 1];               // single-token kernel: max |h| per slot (float bits)
     int gu_done[kMaxE + 1];            // finished gate/up units per slot (shared: index kMaxE)
@@ -49,7 +50,7 @@ struct DecParams {
     const coli_moe_expert *experts;
     coli_moe_expert shared;
     float *out;
-    float *part;               // router partial logits [nks][T][E] (T > 8: slice 0 = logits)
+    float *part;               // router partial logits [nks][T][E]
     float *sig, *choice, *w;
     int32_t *idx, *keff, *counts, *offsets, *perm, *pos, *act;
     float *h, *y;

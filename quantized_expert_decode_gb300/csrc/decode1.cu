@@ -536,7 +536,7 @@ __device__ __noinline__ void down_run(const DecParams &P, D1S &m, const uint8_t 
     auto rows_of = [&](int i, const uint8_t *(&rr)[4]) {
         int slot, grp;
         unit(i, slot, grp);
-        const Rec &r = m.rec[sh ? kShSlot : slot];
+        const Rec &r = m.rec[slot == m.U ? kShSlot : slot];
 #pragma unroll
         for (int q = 0; q < 4; q++) rr[q] = r.dw + (size_t)min(4 * grp + q, P.H - 1) * rb;
     };
@@ -548,7 +548,7 @@ __device__ __noinline__ void down_run(const DecParams &P, D1S &m, const uint8_t 
     auto pre = [&](int i) {
         int slot, grp;
         unit(i, slot, grp);
-        const Rec &r = m.rec[sh ? kShSlot : slot];
+        const Rec &r = m.rec[slot == m.U ? kShSlot : slot];
         return (lane & 7) == 0 ? __ldg(r.ds + min(4 * grp + (lane >> 3), P.H - 1)) : 0.f;
     };
     auto store = [&](int i, auto value_of) {  // lane 8q holds row q
@@ -593,14 +593,14 @@ __device__ __noinline__ void down_run_grouped(const DecParams &P, D1S &m, const 
         [&](int i, const uint8_t *(&rr)[4]) {
             int slot, grp;
             unit(i, slot, grp);
-            const Rec &r = m.rec[sh ? kShSlot : slot];
+            const Rec &r = m.rec[slot == m.U ? kShSlot : slot];
 #pragma unroll
             for (int q = 0; q < 4; q++) rr[q] = r.dw + (size_t)min(4 * grp + q, P.H - 1) * rb;
         },
         [&](int i, const float *(&sr)[4]) {
             int slot, grp;
             unit(i, slot, grp);
-            const Rec &r = m.rec[sh ? kShSlot : slot];
+            const Rec &r = m.rec[slot == m.U ? kShSlot : slot];
 #pragma unroll
             for (int q = 0; q < 4; q++) sr[q] = r.ds + (size_t)min(4 * grp + q, P.H - 1) * ng;
         },
@@ -833,7 +833,8 @@ __global__ void __launch_bounds__(kNT, 2) moe_decode1_kernel(const __grid_consta
     const int hs = P.d1_hs;
     stage_h<RF, SF, RQ, SQ>(P, m, act, hs, s0, ns);
     {
-        const int split = U * ngr;  // routed units below, shared units from here
+        // one stream through routed and shared units when their rows have the same walk and length
+        const int split = (kMerged && P.I == P.Is) ? de : U * ngr;  // routed units below, shared from here
         const int rlo = db, rhi = min(de, split), slo = max(db, split), shi = de;
         const int rot = rhi > rlo ? (rhi - rlo) % kNW : 0;
         if (rhi > rlo) {

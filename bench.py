@@ -44,17 +44,17 @@ DECODE_MAX_T = 64  # the library runs T <= 64 as one persistent decode kernel
 # (dram__bytes_read.sum + dram__bytes_write.sum), keyed by workload, with the hash of the kernel
 # sources they were taken on; a changed kernel reports null until it is measured again.
 NCU_TRAFFIC = {
-    # moe_decode1_kernel, small decode: a full-size capture
-    1: {"bytes": 25950720, "src": "f947919a3e718fc5"},
-    # moe_decode1_kernel, large decode: captured with 32 experts (the per-call expert traffic is
-    # the same), plus the 224 further router rows the full 256-expert router reads
-    2: {"bytes": 171171328 + 2830080 + 224 * (6144 * 4 + 4), "src": "f947919a3e718fc5"},
+    # moe_decode1_kernel, small decode: a full-size capture (single-pass DRAM counters)
+    1: {"bytes": 25958912 + 0, "src": "d0b0d5967fad6f6d"},
+    # moe_decode1_kernel, large decode: a full-size capture (256 experts; single-pass DRAM
+    # counters) of a call whose algorithmic bytes are 176530432
+    2: {"bytes": 176696832 + 2725632, "src": "d0b0d5967fad6f6d"},
     # moe_decode_kernel, batch-32 decode: a full-size capture (single-pass DRAM counters) of a
     # call whose algorithmic bytes were 2402205696; its ratio applies to each bench launch
-    3: {"ratio": (2456768000 + 12263936) / 2402205696, "src": "f947919a3e718fc5"},
+    3: {"ratio": (2456893696 + 12781312) / 2402205696, "src": "d0b0d5967fad6f6d"},
     # moe_prefill_tc_kernel, prefill: the gate/up GEMM launch, a full-size capture (single-pass
-    # DRAM counters; 248 routed experts + the shared one, the bf16 activations and h)
-    4: {"bytes": 3711238912 + 70183936, "src": "2f8cbde9f18cf240"},
+    # DRAM counters; 248 routed experts + the shared one, the f16 activations and h)
+    4: {"bytes": 3372507904 + 68764672, "src": "f5eb5a8ae6a17ac6"},
 }
 
 

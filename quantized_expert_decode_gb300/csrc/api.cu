@@ -208,7 +208,7 @@ int run_forward_decode(const coli_moe_desc *d, const float *x, const float *W_r,
     P.top_p = d->top_p;
     P.rscale = d->routed_scale;
     P.ldh = d->I > d->I_shared ? d->I : d->I_shared;
-    const int splits = std::min(L.router_splits, 16);
+    const int splits = std::min(L.router_splits, kTokSlices);
     if (P.route_only) P.nks = splits;
     if ((size_t)P.nks * d->T * d->E * sizeof(float) > L.sig - L.part) return COLI_MOE_ENOTSUP;
     int rc;

@@ -68,10 +68,18 @@ constexpr int kRouterTK = 32;   // k per smem stage
 
 constexpr int kRouterTargetCtas = 304;  // two per SM of a 152-SM GB300
 
+// From kRouterBigT tokens the logits run as 128-token x 128-expert tiles with 8 x 8 outputs per
+// thread (router_gemm_kernel), k in steps of kRgK.
+constexpr int kRouterBigT = 128;
+constexpr int kRgT = 128, kRgE = 128, kRgK = 16;
+
 inline int router_splits(const coli_moe_desc &d) {
-    long tiles = (long)((d.T + kRouterTM - 1) / kRouterTM) * ((d.E + kRouterTE - 1) / kRouterTE);
+    const bool big = d.T >= kRouterBigT;
+    const int tm = big ? kRgT : kRouterTM, te = big ? kRgE : kRouterTE;
+    long tiles = (long)((d.T + tm - 1) / tm) * ((d.E + te - 1) / te);
     long want = (kRouterTargetCtas + tiles - 1) / tiles;
-    long max_s = (d.H + kRouterTK - 1) / kRouterTK;  // at least one k-stage per split
+    // at least one k-stage per split (four of the big tiles' shorter stages)
+    long max_s = big ? (d.H + 4 * kRgK - 1) / (4 * kRgK) : (d.H + kRouterTK - 1) / kRouterTK;
     if (want > max_s) want = max_s;
     if (want < 1) want = 1;
     if (want > 128) want = 128;

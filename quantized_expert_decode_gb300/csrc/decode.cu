@@ -138,7 +138,7 @@ __device__ int scan_smem(int *a, int n, int *tmp) {
     return total;
 }
 
-// T > 8: CTA t routes token t alone, with all its threads: the logits are the fixed-order sum
+// T > 8: CTA t routes token t alone, with all its threads (at most kTokSlices partial slices): the logits are the fixed-order sum
 // of the nks partial slices, then sigmoid and bias; the picks by the whole CTA (select.cuh), the
 // kept weights by warp 0. The token's rows of the routing outputs go to the workspace / caller,
 // then the CTA raises routed_done. scratch: shared memory of at least rscratch_bytes.
@@ -152,14 +152,14 @@ __device__ __noinline__ void route_token(const DecParams &P, int t, float *scrat
     for (int e = tid; e < Ep; e += kNT) {
         float sv = 0.f, cv = -INFINITY;
         if (e < E) {
-            float a[16];
+            float a[kTokSlices];
             const size_t j = (size_t)t * E + e;
 #pragma unroll
-            for (int k = 0; k < 16; k++)
+            for (int k = 0; k < kTokSlices; k++)
                 if (k < P.nks) a[k] = __ldcg(P.part + (size_t)k * T * E + j);
             float lg = 0.f;
 #pragma unroll
-            for (int k = 0; k < 16; k++)
+            for (int k = 0; k < kTokSlices; k++)
                 if (k < P.nks) lg += a[k];
             sv = 1.f / (1.f + expf(-lg));
             cv = sv + __ldg(P.bias + e);

@@ -27,6 +27,7 @@ struct ExpertWork {
 
 // ---------------------------------------------------------------- decode.cu
 constexpr int kDecMaxT = 64;              // the persistent decode kernel serves T <= 64
+constexpr int kTokSlices = 32;            // T > 8: router partial slices the token CTAs sum
 
 // Counters of one decode call (zeroed before each launch; err stays the first word, which is
 // also the workspace error word read by coli_moe_check).

@@ -80,8 +80,97 @@ router_partial_kernel(const float *__restrict__ x, const float *__restrict__ Wr,
     }
 }
 
+// The same partials for many tokens: a 128-token x 128-expert tile per CTA over one k slice,
+// each thread 8 tokens x 8 experts (tokens 4 ty + i and 64 + 4 ty + i, experts 4 tx + j and
+// 64 + 4 tx + j), k staged through shared memory kRgK at a time in two buffers (the next stage's
+// loads in registers while this one is used). Each partial is a plain fp32 sum in k order.
+__global__ void __launch_bounds__(256)
+router_gemm_kernel(const float *__restrict__ x, const float *__restrict__ Wr, float *__restrict__ part, int T,
+                   int H, int E, int kslice) {
+    __shared__ __align__(16) float xs[2][kRgK][kRgT + 4];
+    __shared__ __align__(16) float ws[2][kRgK][kRgE + 4];
+    const int tid = threadIdx.x, tx = tid % 16, ty = tid / 16;
+    const int t0 = blockIdx.x * kRgT, e0 = blockIdx.y * kRgE, s = blockIdx.z;
+    const int kb = s * kslice, ke = min(H, kb + kslice);
+    float acc[8][8];
+#pragma unroll
+    for (int i = 0; i < 8; i++)
+#pragma unroll
+        for (int j = 0; j < 8; j++) acc[i][j] = 0.f;
+    // global loads: row r = tid / 4 + 64 i of each operand tile, float4 q = tid % 4 of the stage
+    const int lr = tid / 4, lq = tid % 4;
+    float4 xv[2], wv[2];
+    auto gload = [&](int k0) {
+        const int k = k0 + 4 * lq;  // H and the slices are multiples of 16: k < ke covers k + 3
+#pragma unroll
+        for (int i = 0; i < 2; i++) {
+            const int r = lr + 64 * i;
+            const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+            xv[i] = (t0 + r < T && k < ke) ? __ldg(reinterpret_cast<const float4 *>(x + (size_t)(t0 + r) * H + k)) : z;
+            wv[i] = (e0 + r < E && k < ke) ? __ldg(reinterpret_cast<const float4 *>(Wr + (size_t)(e0 + r) * H + k)) : z;
+        }
+    };
+    auto sstore = [&](int b) {
+#pragma unroll
+        for (int i = 0; i < 2; i++) {
+            const int r = lr + 64 * i;
+            xs[b][4 * lq + 0][r] = xv[i].x;
+            xs[b][4 * lq + 1][r] = xv[i].y;
+            xs[b][4 * lq + 2][r] = xv[i].z;
+            xs[b][4 * lq + 3][r] = xv[i].w;
+            ws[b][4 * lq + 0][r] = wv[i].x;
+            ws[b][4 * lq + 1][r] = wv[i].y;
+            ws[b][4 * lq + 2][r] = wv[i].z;
+            ws[b][4 * lq + 3][r] = wv[i].w;
+        }
+    };
+    int buf = 0;
+    if (kb < ke) {
+        gload(kb);
+        sstore(0);
+    }
+    __syncthreads();
+    for (int k0 = kb; k0 < ke; k0 += kRgK) {
+        const bool more = k0 + kRgK < ke;
+        if (more) gload(k0 + kRgK);
+#pragma unroll
+        for (int k = 0; k < kRgK; k++) {
+            const float4 a0 = *reinterpret_cast<const float4 *>(&xs[buf][k][4 * ty]);
+            const float4 a1 = *reinterpret_cast<const float4 *>(&xs[buf][k][64 + 4 * ty]);
+            const float4 b0 = *reinterpret_cast<const float4 *>(&ws[buf][k][4 * tx]);
+            const float4 b1 = *reinterpret_cast<const float4 *>(&ws[buf][k][64 + 4 * tx]);
+            const float a[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+            const float b[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+#pragma unroll
+            for (int i = 0; i < 8; i++)
+#pragma unroll
+                for (int j = 0; j < 8; j++) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+        }
+        if (more) sstore(buf ^ 1);  // the other buffer: every thread is past its last use
+        __syncthreads();
+        buf ^= 1;
+    }
+#pragma unroll
+    for (int i = 0; i < 8; i++) {
+        const int t = t0 + (i < 4 ? 4 * ty + i : 64 + 4 * ty + i - 4);
+        if (t >= T) continue;
+#pragma unroll
+        for (int j = 0; j < 8; j++) {
+            const int e = e0 + (j < 4 ? 4 * tx + j : 64 + 4 * tx + j - 4);
+            if (e < E) part[((size_t)s * T + t) * E + e] = acc[i][j];
+        }
+    }
+}
+
 cudaError_t launch_router_partial(const float *x, const float *W_r, float *part, int T, int H,
                                   int E, int splits, cudaStream_t st) {
+    if (T >= kRouterBigT) {
+        int kslice = (H + splits - 1) / splits;
+        kslice = (kslice + kRgK - 1) / kRgK * kRgK;
+        dim3 grid((T + kRgT - 1) / kRgT, (E + kRgE - 1) / kRgE, splits);
+        router_gemm_kernel<<<grid, 256, 0, st>>>(x, W_r, part, T, H, E, kslice);
+        return cudaGetLastError();
+    }
     int kslice = (H + splits - 1) / splits;
     kslice = (kslice + kRouterTK - 1) / kRouterTK * kRouterTK;
     dim3 grid((T + kRouterTM - 1) / kRouterTM, (E + kRouterTE - 1) / kRouterTE, splits);
@@ -115,19 +204,43 @@ select_kernel(const float *__restrict__ part, int S, const float *__restrict__ b
     float *sg = ch + Ep;
     float2 *cand = reinterpret_cast<float2 *>(sg + Ep);
     int *sel_i = reinterpret_cast<int *>(cand + cap);
-    for (int e = lane; e < Ep; e += kWarp) {
-        if (e < E) {
-            float lg = 0.f;
-            for (int s = 0; s < S; s++) lg += part[((size_t)s * T + t) * E + e];
-            const float sv = 1.f / (1.f + expf(-lg));
-            const float cv = sv + bias[e];
-            sig_out[(size_t)t * E + e] = sv;
-            ch_out[(size_t)t * E + e] = cv;
-            sg[e] = sv;
-            ch[e] = cv;
-        } else {
-            sg[e] = 0.f;
-            ch[e] = -INFINITY;
+    // the lane's experts e = lane + 32 j, kEL at a time, their partial slices summed in slice
+    // order; the loads of kSB slices of all kEL experts are in flight together
+    constexpr int kEL = 8, kSB = 8;
+    for (int e0 = lane; e0 < Ep; e0 += kWarp * kEL) {
+        float lg[kEL];
+#pragma unroll
+        for (int j = 0; j < kEL; j++) lg[j] = 0.f;
+        for (int s0 = 0; s0 < S; s0 += kSB) {
+            float v[kEL][kSB];
+#pragma unroll
+            for (int j = 0; j < kEL; j++)
+#pragma unroll
+                for (int b = 0; b < kSB; b++) {
+                    const int e = e0 + kWarp * j, s = s0 + b;
+                    v[j][b] = (e < E && s < S) ? part[((size_t)s * T + t) * E + e] : 0.f;
+                }
+#pragma unroll
+            for (int j = 0; j < kEL; j++)
+#pragma unroll
+                for (int b = 0; b < kSB; b++)
+                    if (s0 + b < S) lg[j] += v[j][b];
+        }
+#pragma unroll
+        for (int j = 0; j < kEL; j++) {
+            const int e = e0 + kWarp * j;
+            if (e >= Ep) break;
+            if (e < E) {
+                const float sv = 1.f / (1.f + expf(-lg[j]));
+                const float cv = sv + bias[e];
+                sig_out[(size_t)t * E + e] = sv;
+                ch_out[(size_t)t * E + e] = cv;
+                sg[e] = sv;
+                ch[e] = cv;
+            } else {
+                sg[e] = 0.f;
+                ch[e] = -INFINITY;
+            }
         }
     }
     __syncwarp();

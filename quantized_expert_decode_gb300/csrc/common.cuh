@@ -77,7 +77,8 @@ inline int router_splits(const coli_moe_desc &d) {
     const bool big = d.T >= kRouterBigT;
     const int tm = big ? kRgT : kRouterTM, te = big ? kRgE : kRouterTE;
     long tiles = (long)((d.T + tm - 1) / tm) * ((d.E + te - 1) / te);
-    long want = (kRouterTargetCtas + tiles - 1) / tiles;
+    // the big tiles fill one wave of two CTAs per SM without a partial second one
+    long want = big ? kRouterTargetCtas / tiles : (kRouterTargetCtas + tiles - 1) / tiles;
     // at least one k-stage per split (four of the big tiles' shorter stages)
     long max_s = big ? (d.H + 4 * kRgK - 1) / (4 * kRgK) : (d.H + kRouterTK - 1) / kRouterTK;
     if (want > max_s) want = max_s;

@@ -418,7 +418,10 @@ def run_colimoe(args, rank, world, local):
     block_gbs = float(sum(b["total"] for b in bytes_per) / total_s / 1e9)
     expert_gbs = float(sum(b["experts"] for b in bytes_per) / total_s / 1e9)
     src = kernel_source_hash("decode" if fused else "prefill")
-    tr = None if general else NCU_TRAFFIC.get(cid)
+    # the captures are of the plain workloads (per-row scales, exact products): a variant's
+    # kernel instance reads other bytes and reports null until captured
+    variant = bool(cfg.get("group_size", 0)) or bool(cfg.get("idot", 0))
+    tr = None if (general or variant) else NCU_TRAFFIC.get(cid)
     traffic = None
     if tr and tr["src"] == src:
         # a full-size capture gives bytes per launch; a capture of a smaller case gives the

@@ -356,6 +356,9 @@ PREFILL = [
     ("i4-i8", dict(T=130, H=320, I=64, E=4, K=3, I_shared=192, routed_fmt=2, shared_fmt=1)),
     ("hot-expert", dict(T=300, H=128, I=128, E=3, K=1, I_shared=0)),
     ("no-shared", dict(T=100, H=256, I=256, E=16, K=4, I_shared=0)),
+    # T >= 128: the router partials run as 128 x 128 tiles; 200 experts leave a ragged second
+    # expert tile and 160 tokens a ragged second token tile
+    ("wide-router", dict(T=160, H=256, I=128, E=200, K=4, I_shared=64)),
 ]
 
 

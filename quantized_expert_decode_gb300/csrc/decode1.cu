@@ -3,13 +3,13 @@
 // The single-token call is the decode step of the engine (colibri-strix c/glm.c @98759bf
 // moe() with S = 1; the Metal path's moe_gemv). Its work is small per CTA, so the kernel is
 // built around the dependent memory round trips between its phases rather than around tiling:
-// every phase issues its independent loads together, and the rows the down phase will read
-// first are asked of L2 before the wait that precedes it. Phases, split statically over the
-// CTAs (two per SM, cooperative launch):
+// every phase issues its independent loads together. Phases, split statically over the CTAs
+// (two per SM, cooperative launch):
 //   A  router items: partial logits of 32 experts over one slice of H (r_router shader), the
 //      slice's router rows and x in flight together
 //   X  the expert table and the bias copied into shared memory; the token's x in 24-bit block
-//      fixed point (idot.cuh), in the layout of each weight format the block uses
+//      fixed point (idot.cuh), in the layout of each weight format the block uses (int8 bytes
+//      instead for the sides that run on int8 activations, IDOT)
 //   B  shared expert gate/up rows (independent of routing), spread over every CTA: here only
 //      when the shared expert's walk differs from the routed experts' (another format); else
 //      its units follow each CTA's routed units in phase C, one stream of loads through both
@@ -19,14 +19,17 @@
 //      slot U. Their weight pointers come from the shared-memory copy of the table.
 //   C  routed gate/up units (rows j of gate and up of one slot): h = silu(gate.x * s_g) *
 //      (up.x * s_u); each CTA keeps the largest |h| of every slot it wrote, the exponent of the
-//      down step's fixed point. A warp that is done asks L2 for the first down rows it will
-//      read; the CTA then raises one counter.
+//      down step's fixed point (or the scale of its int8 quantisation); the CTA then raises
+//      one counter.
 //   D  once every gate/up unit is in (that counter): (slot, 4-row group) units split
 //      slot-major over the CTAs, so each stages only the one or two h vectors its units read
-//      (h and the slots' maxima in one round trip); y rows go to the workspace
+//      (h and the slots' maxima in one round trip); y rows go to the workspace. Routed and
+//      shared units are one stream when their rows have the same walk and length.
 //   E  once every down row is in (one counter): each CTA's rows of
 //      out[d] = sum_k w_k y[pos_k][d] in selection order, + y[U][d]  (moe() phases C/D/E)
 // Warps walk their gate/up and down units without CTA barriers. Every wait is bounded.
+// Instances: <routed format, shared format, GRP>, GRP marking int4-grouped sides (a scale per
+// group of inputs, applied per 16-byte chunk) and sides on int8 activations (IDOT).
 #include <algorithm>
 
 #include "decode_parts.cuh"

@@ -148,3 +148,14 @@ def test_idot_flag_validation(q):
     assert q.coli_moe_workspace_bytes(good_desc(q, idot=1)) > 0
     for bad in (2, -1):
         assert q.coli_moe_workspace_bytes(good_desc(q, idot=bad)) == 0, bad
+
+
+def test_noalloc_scratch_bound_at_block_shapes(q):
+    # the fixed scratch of coli_moe_forward_noalloc admits T <= 89 at the GLM-5.2 block shapes
+    # (the bound the header states); the workspace grows with T on both sides of it, also where
+    # the router partials switch to the 128 x 128 tiles (T = 128)
+    shapes = dict(H=6144, I=2048, E=256, K=8, I_shared=2048, routed_scale=2.5)
+    ws = {T: q.coli_moe_workspace_bytes(q.make_desc(T=T, **shapes)) for T in (1, 64, 89, 90, 127, 128, 2048)}
+    assert ws[89] <= q.COLI_MOE_NOALLOC_SCRATCH_BYTES < ws[90]
+    order = sorted(ws)
+    assert all(ws[a] < ws[b] for a, b in zip(order, order[1:])), ws

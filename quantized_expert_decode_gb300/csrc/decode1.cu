@@ -47,7 +47,6 @@ struct Rec {  // one expert's weight pointers
 constexpr int kShSlot = kMaxK;  // index of the shared expert in rec[] and hmax[]
 constexpr int kInfl1 = 8;       // 16-byte loads in flight per lane in the streaming phases
 constexpr int kRtQ = 4;         // float4 steps per lane and router row held at once
-constexpr int kDnPf = 0;        // down units per warp asked of L2 before the gate/up wait
 constexpr int kHB = 2;          // staged h items (16 elements each) per thread per round trip
 constexpr int kMaxSlices = 16;  // router slices of H per expert block
 constexpr int kGuRows = 4;      // rows per gate/up unit: gate j, up j, gate j + 1, up j + 1 (or 2)
@@ -497,26 +496,6 @@ __device__ __noinline__ void gateup_run_grouped(const DecParams &P, D1S &m, cons
         });
 }
 
-// the rows of a warp's first down units (slot-major units [db, de) of the grid, unit l: slot
-// l / ngr, rows 4 (l % ngr) .. + 3), asked of L2; the gate/up rows stream with an evict-first
-// policy, so these lines stay until they are read
-__device__ void prefetch_down(const DecParams &P, const D1S &m, int db, int de, int ngr) {
-    const int warp = threadIdx.x / kWarp, lane = threadIdx.x % kWarp;
-    for (int i = 0; i < kDnPf; i++) {
-        const int l = db + warp + kNW * i;
-        if (l >= de) break;
-        const int slot = l / ngr, grp = l - slot * ngr;
-        const bool sh = slot == m.U;
-        const int64_t rb = row_bytes(sh ? P.sfmt : P.rfmt, sh ? P.Is : P.I);
-        const uint8_t *base = m.rec[sh ? kShSlot : slot].dw;
-        const int nl = (int)((rb + 127) / 128);  // lines per row
-        for (int q = lane; q < 4 * nl; q += kWarp) {
-            const int d = min(4 * grp + q / nl, P.H - 1);
-            prefetch_line_l2(base + (size_t)d * rb + 128 * (q % nl));
-        }
-    }
-}
-
 // D: down units [lo, hi) of the slot-major space (unit l: slot l / ngr, rows 4 (l % ngr) .. +3);
 // slot u's staged h sits at hq + (u - s0) * hs. y goes to the workspace row of the slot.
 // rot rotates the warp order so that two calls share the warps evenly.
@@ -810,13 +789,12 @@ __global__ void __launch_bounds__(kNT, 2) moe_decode1_kernel(const __grid_consta
     const int ngr = (P.H + 3) / 4, ND = nsl * ngr;
     const int db = range_lo(ND, c, G), de = range_lo(ND, c + 1, G);
 
-    // ---------------- C: routed gate/up, then the first down rows asked of L2
+    // ---------------- C: routed gate/up (then the shared expert's, one stream, when merged)
     const int gu_per = (P.I + kGuRows / 2 - 1) / (kGuRows / 2);  // units per routed slot
     const int gu_tot = U * gu_per;
     const int cb = range_lo(gu_tot, c, G), ce = range_lo(gu_tot, c + 1, G);
     if constexpr ((GRP & 1) != 0) gateup_run_grouped(P, m, xq_r, cb, ce, kMerged ? bb : 0, kMerged ? be : 0);
     else gateup_run<RF, RQ>(P, m, xq_r, cb, ce, kMerged ? bb : 0, kMerged ? be : 0);
-    prefetch_down(P, m, db, de, ngr);
     __syncthreads();
     if (tid < U || (tid == kShSlot && P.Is > 0))
         if (m.hmax[tid] != 0) atomicMax(&P.ctrl->hmax[tid], m.hmax[tid]);

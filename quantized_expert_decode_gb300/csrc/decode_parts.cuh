@@ -398,15 +398,10 @@ __device__ __noinline__ void router_item(const DecParams &P, int item) {
         }
 }
 
-// ------------------------------------------------------------------ staging and prefetch
+// ------------------------------------------------------------------ staging
 __device__ __forceinline__ float4 ld_act4(const float *src, int q, bool coherent) {
     return coherent ? __ldcg(reinterpret_cast<const float4 *>(src) + q)
                     : __ldg(reinterpret_cast<const float4 *>(src) + q);
-}
-
-// one 128-byte line to L2 (no alignment rule beyond the natural one)
-__device__ __forceinline__ void prefetch_line_l2(const void *p) {
-    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
 }
 
 }  // namespace

@@ -45,13 +45,13 @@ DECODE_MAX_T = 64  # the library runs T <= 64 as one persistent decode kernel
 # sources they were taken on; a changed kernel reports null until it is measured again.
 NCU_TRAFFIC = {
     # moe_decode1_kernel, small decode: a full-size capture (single-pass DRAM counters)
-    1: {"bytes": 25965568 + 0, "src": "f617e23037f851a1"},
+    1: {"bytes": 25958656 + 0, "src": "0e3695ff713bdd7e"},
     # moe_decode1_kernel, large decode: a full-size capture (256 experts; single-pass DRAM
     # counters) of a call whose algorithmic bytes are 176530432
-    2: {"bytes": 176696576 + 2463488, "src": "f617e23037f851a1"},
+    2: {"bytes": 176697600 + 2807040, "src": "0e3695ff713bdd7e"},
     # moe_decode_kernel, batch-32 decode: a full-size capture (single-pass DRAM counters) of a
     # call whose algorithmic bytes were 2402205696; its ratio applies to each bench launch
-    3: {"ratio": (2454131200 + 12269568) / 2402205696, "src": "f617e23037f851a1"},
+    3: {"ratio": (2456358656 + 12191232) / 2402205696, "src": "0e3695ff713bdd7e"},
     # moe_prefill_tc_kernel, prefill: the gate/up GEMM launch, a full-size capture (single-pass
     # DRAM counters; 248 routed experts + the shared one, the f16 activations and h)
     4: {"bytes": 3376586240 + 68475904, "src": "8f8ba21abc55adc7"},

@@ -58,6 +58,20 @@ NCU_TRAFFIC = {
 }
 
 
+def recorded_traffic(cfg, cid, general, src, mean_kernel_bytes):
+    """DRAM bytes per launch of the dominant kernel from the recorded ncu captures, or None.
+    The captures are of the plain workloads (per-row scales, exact products) on the general-free
+    paths: a variant's kernel instance (int4-grouped, IDOT) or the general kernels read other
+    bytes, and a capture taken on other kernel sources (src) no longer describes this kernel.
+    A full-size capture gives bytes per launch; one of a smaller case gives the ratio of DRAM
+    bytes to algorithmic bytes, applied to this run's mean launch."""
+    variant = bool(cfg.get("group_size", 0)) or bool(cfg.get("idot", 0))
+    tr = None if (general or variant) else NCU_TRAFFIC.get(cid)
+    if not tr or tr["src"] != src:
+        return None
+    return tr["bytes"] if "bytes" in tr else tr["ratio"] * mean_kernel_bytes
+
+
 def kernel_source_hash(kind: str = "decode") -> str:
     """Hash of the sources a roofline kernel is compiled from (its translation units and
     everything they include): the persistent decode kernels, or the prefill GEMM."""
@@ -418,15 +432,7 @@ def run_colimoe(args, rank, world, local):
     block_gbs = float(sum(b["total"] for b in bytes_per) / total_s / 1e9)
     expert_gbs = float(sum(b["experts"] for b in bytes_per) / total_s / 1e9)
     src = kernel_source_hash("decode" if fused else "prefill")
-    # the captures are of the plain workloads (per-row scales, exact products): a variant's
-    # kernel instance reads other bytes and reports null until captured
-    variant = bool(cfg.get("group_size", 0)) or bool(cfg.get("idot", 0))
-    tr = None if (general or variant) else NCU_TRAFFIC.get(cid)
-    traffic = None
-    if tr and tr["src"] == src:
-        # a full-size capture gives bytes per launch; a capture of a smaller case gives the
-        # ratio of DRAM bytes to algorithmic bytes, applied to this run's mean launch
-        traffic = tr["bytes"] if "bytes" in tr else tr["ratio"] * float(k_bytes.mean())
+    traffic = recorded_traffic(cfg, cid, general, src, float(k_bytes.mean()))
 
     # end to end through the host-buffer entry point: H2D of x and D2H of out inside each step
     x_host = torch.from_numpy(xs_np).pin_memory()

@@ -45,3 +45,18 @@ def test_source_hash_ignores_comments_only():
     code = "int f(int a) {\n    return a + 1;  // one more\n}\n/* block\n comment */\n"
     assert bench._code_only(code) == bench._code_only(code.replace("one more", "plus one"))
     assert bench._code_only(code) != bench._code_only(code.replace("a + 1", "a + 2"))
+
+
+def test_recorded_traffic_only_for_the_captured_plain_kernels():
+    src = bench.NCU_TRAFFIC[2]["src"]
+    plain = synth.config(2)
+    assert bench.recorded_traffic(plain, 2, False, src, 1.0) == bench.NCU_TRAFFIC[2]["bytes"]
+    # another kernel source, a variant instance or the general kernels: no recorded traffic
+    assert bench.recorded_traffic(plain, 2, False, "0" * 16, 1.0) is None
+    assert bench.recorded_traffic(dict(plain, group_size=128, routed_fmt=synth.FMT_INT4G), 2, False, src, 1.0) is None
+    assert bench.recorded_traffic(dict(plain, idot=1), 2, False, src, 1.0) is None
+    assert bench.recorded_traffic(plain, 2, True, src, 1.0) is None
+    # a ratio capture scales with this run's algorithmic bytes
+    r3 = bench.NCU_TRAFFIC[3]
+    got = bench.recorded_traffic(synth.config(3), 3, False, r3["src"], 2.0e9)
+    assert abs(got - r3["ratio"] * 2.0e9) < 1.0 and 1.0 < r3["ratio"] < 1.1
